@@ -1,0 +1,175 @@
+/*
+ * fp64 CPU oracle for RMSNorm followed by MatMul.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the package smoke check and
+ * the benchmark's CPU-baseline leg may load or run this file.  The CUDA
+ * library never links, includes or calls it, and this file includes nothing
+ * from the CUDA library.
+ *
+ * What it computes (plain definition, no blocking, no fusion, no reordering):
+ *
+ *   ms[m]   = (1/K) * sum_k X[m,k]^2                      (row mean square)
+ *   r[m]    = 1 / sqrt(ms[m] + eps)                       (reciprocal RMS)
+ *   Xn[m,k] = X[m,k] * g[k] * r[m]                        (RMSNorm with gain g)
+ *   Y[m,n]  = sum_k Xn[m,k] * W[k,n]                      (MatMul)
+ *
+ * This is the unfused pair that the Mirage review page ("Mirage: A
+ * Multi-Level Superoptimizer for Tensor Programs" review, section 3,
+ * "muGraph example") describes existing systems running as two kernels:
+ * RMSNorm, then MatMul.  The MatMul is the broadcast-multiply-then-sum
+ * definition (Luminal talk page, "12 primitive ops": matmul is a multiply
+ * followed by a sum reduction).  The pages do not write the RMSNorm formula;
+ * the placement of eps inside the square root, the mean over K (not K-1) and
+ * the per-k multiplicative gain applied to X while the statistic uses the
+ * unscaled X are the plain reading of RMSNorm.
+ *
+ * oracle_rmsnorm_matmul_rewritten() evaluates the form that the fusion rests
+ * on (review page, section 3, "core formula": E(O) = sum(k, div(mul(E(I1),
+ * E(I2)), E(I3))) with a divisor I3 that does not depend on k, so the division
+ * may move outside the sum):
+ *
+ *   Y[m,n] = ( sum_k (X[m,k]*g[k]) * W[k,n] ) * r[m]
+ *
+ * Everything is double precision; nothing is rounded to bf16.  Row-major
+ * layouts: X [M,K], g [K], W [K,N], Y [M,N].
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_ERR_ALLOC 1
+
+/* Mean square of one row: (1/K) * sum_k x_k^2, summed in k order. */
+static double row_mean_square(const double *x, long K)
+{
+    double ss = 0.0;
+    for (long k = 0; k < K; ++k)
+        ss += x[k] * x[k];
+    return ss / (double)K;
+}
+
+/* Reciprocal RMS: 1 / sqrt(ms + eps).  libm sqrt is correctly rounded. */
+static double reciprocal_rms(double ms, double eps)
+{
+    return 1.0 / sqrt(ms + eps);
+}
+
+static int resolve_threads(int nthreads)
+{
+#ifdef _OPENMP
+    return nthreads > 0 ? nthreads : omp_get_max_threads();
+#else
+    (void)nthreads;
+    return 1;
+#endif
+}
+
+/* RMSNorm: Xn[m,k] = X[m,k] * g[k] * r[m]. */
+int oracle_rmsnorm(const double *X, const double *g, double *Xn,
+                   long M, long K, double eps, int nthreads)
+{
+    int nt = resolve_threads(nthreads);
+    (void)nt;
+#pragma omp parallel for num_threads(nt) schedule(static)
+    for (long m = 0; m < M; ++m) {
+        const double *x = X + m * K;
+        double r = reciprocal_rms(row_mean_square(x, K), eps);
+        for (long k = 0; k < K; ++k)
+            Xn[m * K + k] = x[k] * g[k] * r;
+    }
+    return ORACLE_OK;
+}
+
+/* MatMul: C[m,n] = sum_k A[m,k] * B[k,n], loop order m, k, n. */
+int oracle_matmul(const double *A, const double *B, double *C,
+                  long M, long K, long N, int nthreads)
+{
+    int nt = resolve_threads(nthreads);
+    (void)nt;
+#pragma omp parallel for num_threads(nt) schedule(static)
+    for (long m = 0; m < M; ++m) {
+        double *c = C + m * N;
+        for (long n = 0; n < N; ++n)
+            c[n] = 0.0;
+        for (long k = 0; k < K; ++k) {
+            const double a = A[m * K + k];
+            const double *b = B + k * N;
+            for (long n = 0; n < N; ++n)
+                c[n] += a * b[n];
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* Unfused RMSNorm then MatMul, one row at a time (the rows are independent). */
+int oracle_rmsnorm_matmul(const double *X, const double *g, const double *W,
+                          double *Y, long M, long K, long N, double eps,
+                          int nthreads)
+{
+    int nt = resolve_threads(nthreads);
+    int failed = 0;
+    (void)nt;
+#pragma omp parallel num_threads(nt) reduction(| : failed)
+    {
+        double *xn = (double *)malloc((size_t)(K > 0 ? K : 1) * sizeof(double));
+        if (!xn) {
+            failed = 1;
+        } else {
+#pragma omp for schedule(static)
+            for (long m = 0; m < M; ++m) {
+                const double *x = X + m * K;
+                /* step 1-3: the normalised row, kept in fp64 */
+                double r = reciprocal_rms(row_mean_square(x, K), eps);
+                for (long k = 0; k < K; ++k)
+                    xn[k] = x[k] * g[k] * r;
+                /* step 4: y = xn . W */
+                double *y = Y + m * N;
+                for (long n = 0; n < N; ++n)
+                    y[n] = 0.0;
+                for (long k = 0; k < K; ++k) {
+                    const double a = xn[k];
+                    const double *w = W + k * N;
+                    for (long n = 0; n < N; ++n)
+                        y[n] += a * w[n];
+                }
+            }
+            free(xn);
+        }
+    }
+    return failed ? ORACLE_ERR_ALLOC : ORACLE_OK;
+}
+
+/* The rewritten form: contract (X*g) with W first, divide by the RMS after. */
+int oracle_rmsnorm_matmul_rewritten(const double *X, const double *g,
+                                    const double *W, double *Y, long M, long K,
+                                    long N, double eps, int nthreads)
+{
+    int nt = resolve_threads(nthreads);
+    (void)nt;
+#pragma omp parallel for num_threads(nt) schedule(static)
+    for (long m = 0; m < M; ++m) {
+        const double *x = X + m * K;
+        double *y = Y + m * N;
+        for (long n = 0; n < N; ++n)
+            y[n] = 0.0;
+        for (long k = 0; k < K; ++k) {
+            const double a = x[k] * g[k];
+            const double *w = W + k * N;
+            for (long n = 0; n < N; ++n)
+                y[n] += a * w[n];
+        }
+        double r = reciprocal_rms(row_mean_square(x, K), eps);
+        for (long n = 0; n < N; ++n)
+            y[n] *= r;
+    }
+    return ORACLE_OK;
+}
+
+int oracle_max_threads(void)
+{
+    return resolve_threads(0);
+}

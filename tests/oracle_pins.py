@@ -1,0 +1,235 @@
+"""Pins that tie the fp64 oracle to facts other than its own code.
+
+Each ``pin_*`` function takes a loaded oracle library (so the mutation tests
+can run the same pins against a deliberately broken copy) and returns
+``(ok, detail)``.  None of them re-types the oracle's formula: each checks a
+property that the operation must have, a closed form, a library routine, or
+values worked out by hand.
+
+Operation (Mirage review page, section 3, "muGraph example" and "core
+formula"): Y = RMSNorm(X; g, eps) @ W with
+r[m] = 1/sqrt(mean_k X[m,k]^2 + eps) and Y[m,n] = sum_k X[m,k] g[k] r[m] W[k,n].
+"""
+from __future__ import annotations
+
+import math
+import os
+import random
+from fractions import Fraction
+
+import numpy as np
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _rel_normwise(a, b):
+    scale = max(float(np.abs(b).max()), 1e-300)
+    return float(np.abs(a - b).max()) / scale
+
+
+# ---------------------------------------------------------------------------
+# P1: the identity behind the fusion, checked exactly in a finite field (the
+# review page's equivalence verifier tests programs on random inputs in Z_p;
+# section 3 "equivalence verification").  sum_k (a_k * c) == (sum_k a_k) * c
+# when c does not depend on k; a k-dependent divisor breaks it.
+# ---------------------------------------------------------------------------
+P_PRIME = 2_147_483_647  # 2^31 - 1
+
+
+def zp_rewrite_holds(K: int, seed: int, k_dependent_divisor: bool = False) -> bool:
+    rnd = random.Random(seed)
+    p = P_PRIME
+    x = [rnd.randrange(p) for _ in range(K)]
+    g = [rnd.randrange(p) for _ in range(K)]
+    w = [rnd.randrange(p) for _ in range(K)]
+    r = rnd.randrange(1, p)
+    rk = [rnd.randrange(1, p) for _ in range(K)]
+    divisor = [rk[k] if k_dependent_divisor else r for k in range(K)]
+    inv = [pow(d, p - 2, p) for d in divisor]  # division = multiplication by inverse
+    lhs = sum(x[k] * g[k] % p * w[k] % p * inv[k] for k in range(K)) % p
+    rhs = sum(x[k] * g[k] % p * w[k] for k in range(K)) % p * pow(r, p - 2, p) % p
+    return lhs == rhs
+
+
+def pin_rewrite_agrees(lib, seed=11):
+    """The oracle's unfused and rewritten forms agree to fp64 rounding."""
+    rng = _rng(seed)
+    X = rng.standard_normal((7, 96))
+    g = rng.uniform(0.5, 1.5, 96)
+    W = rng.standard_normal((96, 40)) / math.sqrt(96)
+    a = oracle.rmsnorm_matmul(X, g, W, 1e-6, lib=lib)
+    b = oracle.rmsnorm_matmul_rewritten(X, g, W, 1e-6, lib=lib)
+    err = _rel_normwise(a, b)
+    return err <= 1e-12, f"normwise rel diff {err:.3e}"
+
+
+# ---------------------------------------------------------------------------
+# P2: scale invariance.  RMSNorm(c X) = RMSNorm(X) when eps = 0; for a power
+# of two c every fp64 rounding scales exactly, so the outputs are bitwise equal.
+# ---------------------------------------------------------------------------
+def pin_scale_invariance(lib, seed=12):
+    rng = _rng(seed)
+    X = rng.standard_normal((5, 64))
+    g = rng.uniform(0.5, 1.5, 64)
+    W = rng.standard_normal((64, 24)) / 8.0
+    y = oracle.rmsnorm_matmul(X, g, W, 0.0, lib=lib)
+    for c in (2.0 ** -4, 2.0, 2.0 ** 8):
+        yc = oracle.rmsnorm_matmul(c * X, g, W, 0.0, lib=lib)
+        if not np.array_equal(y, yc):
+            return False, f"Y(cX) != Y(X) bitwise for c={c}"
+    y3 = oracle.rmsnorm_matmul(3.0 * X, g, W, 1e-12, lib=lib)
+    err = _rel_normwise(y3, y)
+    if err > 1e-11:
+        return False, f"c=3, eps=1e-12: normwise rel diff {err:.3e}"
+    return True, "ok"
+
+
+# ---------------------------------------------------------------------------
+# P3: W = identity reduces the operation to RMSNorm alone; torch's
+# functional rms_norm (a library routine) computes x * rsqrt(mean(x^2)+eps) * g.
+# ---------------------------------------------------------------------------
+def pin_identity_is_rmsnorm(lib, seed=13):
+    import torch
+    rng = _rng(seed)
+    K = 48
+    X = rng.standard_normal((6, K)) * rng.uniform(0.1, 10.0, (6, 1))
+    g = rng.uniform(0.5, 1.5, K)
+    for eps in (1e-6, 0.5):
+        y = oracle.rmsnorm_matmul(X, g, np.eye(K), eps, lib=lib)
+        ref = torch.nn.functional.rms_norm(torch.from_numpy(X), (K,),
+                                           weight=torch.from_numpy(g), eps=eps).numpy()
+        err = _rel_normwise(y, ref)
+        if err > 1e-13:
+            return False, f"eps={eps}: normwise rel diff {err:.3e}"
+        xn = oracle.rmsnorm(X, g, eps, lib=lib)
+        err = _rel_normwise(xn, ref)
+        if err > 1e-13:
+            return False, f"rmsnorm alone, eps={eps}: normwise rel diff {err:.3e}"
+    return True, "ok"
+
+
+# ---------------------------------------------------------------------------
+# P4: constant rows.  X[m,:] = c gives mean square c^2, so
+# Y[m,n] = c / sqrt(c^2 + eps) * sum_k g[k] W[k,n]  (numpy's g @ W).
+# ---------------------------------------------------------------------------
+def pin_constant_rows(lib, seed=14):
+    rng = _rng(seed)
+    K, N = 40, 12
+    g = rng.uniform(0.5, 1.5, K)
+    W = rng.standard_normal((K, N))
+    cs = np.array([1.0, -2.5, 0.125, 7.0])
+    X = np.repeat(cs[:, None], K, axis=1)
+    gw = g @ W
+    for eps in (0.0, 1e-6, 3.0):
+        y = oracle.rmsnorm_matmul(X, g, W, eps, lib=lib)
+        ref = (cs / np.sqrt(cs * cs + eps))[:, None] * gw[None, :]
+        err = _rel_normwise(y, ref)
+        if err > 1e-13:
+            return False, f"eps={eps}: normwise rel diff {err:.3e}"
+    return True, "ok"
+
+
+# ---------------------------------------------------------------------------
+# P5: hand-worked 2x3x2 examples (tests/golden/p5_bruteforce.txt).
+# ---------------------------------------------------------------------------
+def _parse_rows(s, conv):
+    return [[conv(v) for v in row.split()] for row in s.split(";")]
+
+
+def _parse_value(tok):
+    if "@" in tok:
+        num, d = tok.split("@")
+        return float(Fraction(num)) / math.sqrt(int(d))
+    return float(Fraction(tok))
+
+
+def load_p5_cases():
+    cases, cur = [], None
+    with open(os.path.join(GOLDEN, "p5_bruteforce.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, _, rest = line.partition(" ")
+            if key == "case":
+                cur = {"name": rest}
+                cases.append(cur)
+            elif key == "eps":
+                cur["eps"] = float(Fraction(rest))
+            elif key in ("X", "W"):
+                cur[key] = np.array(_parse_rows(rest, lambda v: float(Fraction(v))))
+            elif key == "g":
+                cur["g"] = np.array([float(Fraction(v)) for v in rest.split()])
+            elif key == "Y":
+                cur["Y"] = np.array(_parse_rows(rest, _parse_value))
+    return cases
+
+
+def pin_hand_worked(lib):
+    for c in load_p5_cases():
+        y = oracle.rmsnorm_matmul(c["X"], c["g"], c["W"], c["eps"], lib=lib)
+        if not np.allclose(y, c["Y"], rtol=1e-15, atol=1e-15):
+            return False, f"case {c['name']}: got {y.tolist()} want {c['Y'].tolist()}"
+    return True, "ok"
+
+
+# ---------------------------------------------------------------------------
+# P6: the matmul part.  g = 1 and rows of +-1 with eps = 0 give r = 1, so
+# Y = X @ W, which numpy computes independently.
+# ---------------------------------------------------------------------------
+def pin_matmul_part(lib, seed=16):
+    rng = _rng(seed)
+    M, K, N = 9, 33, 17
+    X = rng.choice([-1.0, 1.0], size=(M, K))
+    W = rng.standard_normal((K, N))
+    y = oracle.rmsnorm_matmul(X, np.ones(K), W, 0.0, lib=lib)
+    err = _rel_normwise(y, X @ W)
+    if err > 1e-13:
+        return False, f"fused vs numpy: normwise rel diff {err:.3e}"
+    c = oracle.matmul(X, W, lib=lib)
+    err = _rel_normwise(c, X @ W)
+    if err > 1e-13:
+        return False, f"matmul vs numpy: normwise rel diff {err:.3e}"
+    return True, "ok"
+
+
+# ---------------------------------------------------------------------------
+# P7: structure.  Rows are independent (a row permutation of X permutes Y's
+# rows bitwise), columns are independent (a column permutation of W permutes
+# Y's columns bitwise), and g travels with the k index (permuting k in X, g
+# and W together changes only the summation order).
+# ---------------------------------------------------------------------------
+def pin_permutations(lib, seed=17):
+    rng = _rng(seed)
+    M, K, N = 6, 20, 10
+    X = rng.standard_normal((M, K))
+    g = rng.uniform(0.5, 1.5, K)
+    W = rng.standard_normal((K, N))
+    y = oracle.rmsnorm_matmul(X, g, W, 1e-6, lib=lib)
+    pm, pn, pk = rng.permutation(M), rng.permutation(N), rng.permutation(K)
+    if not np.array_equal(oracle.rmsnorm_matmul(X[pm], g, W, 1e-6, lib=lib), y[pm]):
+        return False, "row permutation"
+    if not np.array_equal(oracle.rmsnorm_matmul(X, g, W[:, pn], 1e-6, lib=lib), y[:, pn]):
+        return False, "column permutation"
+    yk = oracle.rmsnorm_matmul(X[:, pk], g[pk], W[pk], 1e-6, lib=lib)
+    err = _rel_normwise(yk, y)
+    if err > 1e-13:
+        return False, f"k permutation: normwise rel diff {err:.3e}"
+    return True, "ok"
+
+
+ALL_PINS = {
+    "rewrite_agrees": pin_rewrite_agrees,
+    "scale_invariance": pin_scale_invariance,
+    "identity_is_rmsnorm": pin_identity_is_rmsnorm,
+    "constant_rows": pin_constant_rows,
+    "hand_worked": pin_hand_worked,
+    "matmul_part": pin_matmul_part,
+    "permutations": pin_permutations,
+}

@@ -1,0 +1,119 @@
+"""The fp64 oracle against its pins, and planted mistakes against the pins.
+
+CPU only.  The mutation tests copy the oracle's C source to a temporary
+directory, plant one plausible mistake in the copy, compile it, and check
+that at least one pin fails; the committed oracle is never modified.
+"""
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle_pins import ALL_PINS, load_p5_cases, zp_rewrite_holds
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return oracle.load()
+
+
+@pytest.mark.parametrize("name", sorted(ALL_PINS))
+def test_pin(lib, name):
+    ok, detail = ALL_PINS[name](lib)
+    assert ok, detail
+
+
+@pytest.mark.parametrize("K", [1, 3, 64, 1000])
+def test_zp_identity_holds(K):
+    for seed in range(5):
+        assert zp_rewrite_holds(K, seed)
+
+
+def test_zp_identity_catches_k_dependent_divisor():
+    # A divisor that varies with k cannot move past the sum; the finite-field
+    # test must see the difference (with overwhelming probability).
+    assert not any(zp_rewrite_holds(16, s, k_dependent_divisor=True) for s in range(5))
+
+
+def test_golden_fixture_parses():
+    cases = load_p5_cases()
+    assert [c["name"] for c in cases] == ["A", "B", "C"]
+    for c in cases:
+        assert c["X"].shape == (2, 3) and c["W"].shape == (3, 2) and c["Y"].shape == (2, 2)
+
+
+def test_bf16_decode_exact():
+    bits = np.array([0x0000, 0x3F80, 0xBF80, 0x4049, 0x7F7F, 0x0001, 0x8000], dtype=np.uint16)
+    vals = oracle.bf16_bits_to_f64(bits)
+    assert vals[0] == 0.0 and vals[1] == 1.0 and vals[2] == -1.0
+    assert vals[3] == 3.140625
+    assert vals[4] == float(np.float32(3.3895313892515355e38))
+    assert vals[5] == 2.0 ** -133  # smallest bf16 subnormal
+    assert vals[6] == 0.0 and np.signbit(vals[6])
+
+
+def test_bf16_decode_matches_torch():
+    torch = pytest.importorskip("torch")
+    t = torch.randn(1000, dtype=torch.float32).to(torch.bfloat16)
+    assert np.array_equal(oracle.to_f64(t), t.double().numpy())
+
+
+def test_zero_row_gives_zero():
+    y = oracle.rmsnorm_matmul(np.zeros((1, 8)), np.ones(8), np.ones((8, 3)), 1e-6)
+    assert np.array_equal(y, np.zeros((1, 3)))
+
+
+def test_empty_rows():
+    y = oracle.rmsnorm_matmul(np.zeros((0, 8)), np.ones(8), np.ones((8, 3)), 1e-6)
+    assert y.shape == (0, 3)
+
+
+def test_threads_do_not_change_result(lib):
+    rng = np.random.default_rng(5)
+    X, g, W = rng.standard_normal((33, 50)), rng.uniform(0.5, 1.5, 50), rng.standard_normal((50, 21))
+    a = oracle.rmsnorm_matmul(X, g, W, 1e-5, nthreads=1, lib=lib)
+    b = oracle.rmsnorm_matmul(X, g, W, 1e-5, nthreads=4, lib=lib)
+    assert np.array_equal(a, b)
+
+
+# Each mutant: (description, original snippet, replacement).  Every occurrence
+# of the snippet is replaced.
+MUTANTS = [
+    ("eps outside the square root", "1.0 / sqrt(ms + eps)", "1.0 / (sqrt(ms) + eps)"),
+    ("mean over K-1", "ss / (double)K", "ss / (double)(K - 1)"),
+    ("no square root", "1.0 / sqrt(ms + eps)", "1.0 / (ms + eps)"),
+    ("gain dropped", "x[k] * g[k] * r", "x[k] * r"),
+    ("gain read as 1+g", "x[k] * g[k] * r", "x[k] * (1.0 + g[k]) * r"),
+    ("W read transposed", "const double *w = W + k * N;",
+     "const double *w = W + k; /* mutant */"),
+    ("sign flipped", "y[n] += a * w[n];", "y[n] -= a * w[n];"),
+    ("last k dropped from the statistic", "for (long k = 0; k < K; ++k)\n        ss +=",
+     "for (long k = 0; k < K - 1; ++k)\n        ss +="),
+    ("statistic scaled by a constant", "ss += x[k] * x[k];", "ss += x[k] * x[k] * 1.25;"),
+]
+
+
+@pytest.mark.parametrize("desc,orig,repl", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(tmp_path, desc, orig, repl):
+    with open(oracle.SOURCE) as f:
+        src = f.read()
+    assert orig in src, f"mutation site for {desc!r} not found"
+    mutated = src.replace(orig, repl)
+    if desc == "W read transposed":
+        # read W as if stored [N,K]: element (k,n) at n*K + k (stays in bounds)
+        mutated = mutated.replace("y[n] += a * w[n];", "y[n] += a * w[n * K];")
+    path = tmp_path / "mutant.c"
+    path.write_text(mutated)
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", *oracle.CFLAGS, "-o", str(so), str(path), "-lm"], check=True)
+    mlib = oracle.load(str(so))
+    failed = []
+    for name, pin in ALL_PINS.items():
+        try:
+            ok, _ = pin(mlib)
+        except Exception:  # noqa: BLE001 - a crash also counts as caught
+            ok = False
+        if not ok:
+            failed.append(name)
+    assert failed, f"no pin caught the mutant: {desc}"
