@@ -1,0 +1,126 @@
+/*
+ * rmsnorm_matmul.h -- C ABI of libsm_rmsnorm_matmul.so, a GB300 (sm_103a)
+ * library for RMSNorm followed by MatMul, fused into one pass.
+ *
+ * Operation (Mirage review page, "Mirage: A Multi-Level Superoptimizer for
+ * Tensor Programs", section 3 "muGraph example": existing systems run RMSNorm
+ * and MatMul as two kernels, Mirage fuses them and never materialises the
+ * normalised tensor; section 3 "core formula": E(O) = sum(k, div(mul(E(I1),
+ * E(I2)), E(I3))), i.e. a divisor that does not depend on k moves past the
+ * k-sum):
+ *
+ *     r[m]   = 1 / sqrt( (1/K) * sum_k X[m,k]^2 + eps )
+ *     Y[m,n] = r[m] * sum_k (X[m,k] * g[k]) * W[k,n]
+ *
+ * Conventions shared by every entry point:
+ *  - Tensors are dense, row-major (last index contiguous) bf16 arrays in
+ *    device memory of the CURRENT device: X [M,K], g [K], W [K,N], Y [M,N].
+ *    W is stored K-by-N (N contiguous), as the product X.W is written.
+ *  - Pointers are owned by the caller.  The library never frees them and
+ *    keeps none of them after the call returns.
+ *  - Every call is stream-ordered and asynchronous on `stream` (a
+ *    cudaStream_t; NULL means the legacy default stream).  RMM_OK means the
+ *    work was enqueued.  Faults inside a kernel surface at the caller's next
+ *    synchronisation with that stream; a bounded wait that ran out inside a
+ *    kernel is reported by rmm_device_status().
+ *  - Arguments are validated before any CUDA call.  Rules:
+ *      M >= 0, N >= 0, K >= 1 (an empty row has no mean square);
+ *      M == 0 or N == 0 is a no-op that returns RMM_OK (pointers unused);
+ *      K and N multiples of 8 (16-byte row strides) -> else RMM_ERR_ALIGNMENT;
+ *      every pointer non-NULL and 16-byte aligned -> else RMM_ERR_INVALID_ARG
+ *        (NULL) or RMM_ERR_ALIGNMENT (misaligned);
+ *      eps finite and >= 0 -> else RMM_ERR_INVALID_ARG;
+ *      the output may not overlap any input -> else RMM_ERR_INVALID_ARG;
+ *      the current device must have compute capability 10.3
+ *        -> else RMM_ERR_UNSUPPORTED_DEVICE.
+ *  - Rounding: products X*g are rounded to bf16 before the tensor-core
+ *    contraction; accumulation is fp32; Y is rounded once to bf16 (nearest
+ *    even).  eps = 0 on an all-zero row gives NaN, as the formula does.
+ *  - Thread safety: calls from several host threads are safe.  The
+ *    library's lazily created per-(device, stream) state is guarded by a
+ *    mutex; rmm_force_path() is a process-wide test and benchmark switch.
+ */
+#ifndef SM_RMSNORM_MATMUL_H
+#define SM_RMSNORM_MATMUL_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    RMM_OK = 0,
+    RMM_ERR_INVALID_ARG = 1,        /* NULL pointer, bad size, bad eps, aliasing */
+    RMM_ERR_ALIGNMENT = 2,          /* pointer not 16-byte aligned, K or N % 8 != 0 */
+    RMM_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not compute capability 10.3 */
+    RMM_ERR_LAUNCH = 4,             /* a CUDA launch or API call failed */
+    RMM_ERR_DEVICE_TIMEOUT = 5,     /* a bounded in-kernel wait ran out (rmm_device_status) */
+    RMM_ERR_INTERNAL = 6            /* workspace allocation or tensor-map encoding failed */
+} rmm_status;
+
+/*
+ * Fused RMSNorm + MatMul (the operation above), one launch.
+ *   X  [M,K] bf16 input rows           g [K] bf16 gain
+ *   W  [K,N] bf16 weights (N contiguous) Y [M,N] bf16 output (written)
+ *   eps added to the mean square inside the square root.
+ * A shape-based dispatcher picks the tensor-core row-tile path (large M:
+ * X tiles are the MMA A operand) or the small-M weight-streaming path (W
+ * tiles are the MMA A operand, split over K when N alone gives too few
+ * tiles).  Both compute X*g and the row sum of squares in the same pass as
+ * the contraction and apply r[m] in the epilogue.  The small-M path may use
+ * a library-owned fp32 workspace per (device, stream), allocated on first
+ * use (so make the first call outside any CUDA-graph capture).
+ * Returns an rmm_status.
+ */
+int rmsnorm_matmul(const void* X, const void* g, const void* W, void* Y,
+                   int64_t M, int64_t K, int64_t N, float eps, cudaStream_t stream);
+
+/*
+ * Unfused RMSNorm alone (the first of the two kernels that the review page's
+ * muGraph example says existing systems launch):
+ *   Xn[m,k] = bf16( X[m,k] * g[k] * r[m] ),  X, Xn [M,K] bf16, g [K] bf16.
+ * Kept for comparison with the fused path.  Xn may not overlap X or g.
+ */
+int rmsnorm(const void* X, const void* g, void* Xn,
+            int64_t M, int64_t K, float eps, cudaStream_t stream);
+
+/*
+ * Unfused MatMul alone (the second kernel of that pair):
+ *   C[m,n] = bf16( sum_k A[m,k] * B[k,n] ),  A [M,K], B [K,N], C [M,N] bf16,
+ * fp32 accumulation on the tensor cores.  Same validation rules.
+ */
+int matmul(const void* A, const void* B, void* C,
+           int64_t M, int64_t K, int64_t N, cudaStream_t stream);
+
+/*
+ * Test and benchmark switch for the dispatcher of rmsnorm_matmul() and
+ * matmul(): 0 = shape-based choice (default), 1 = always the row-tile path,
+ * 2 = always the small-M path (requires M <= 128; larger M returns
+ * RMM_ERR_INVALID_ARG while forced).  Returns the previous setting, or -1 for
+ * an unknown value (the setting is then unchanged).
+ */
+int rmm_force_path(int path);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's
+ * in-kernel status word: RMM_OK, or RMM_ERR_DEVICE_TIMEOUT if a bounded wait
+ * inside a kernel gave up (that kernel then skipped its remaining work and
+ * released its tensor memory).  RMM_ERR_LAUNCH if the synchronisation itself
+ * failed.
+ */
+int rmm_device_status(cudaStream_t stream);
+
+/* Static, NUL-terminated name of a status code ("RMM_OK", ...). */
+const char* rmm_status_string(int code);
+
+/* Which path the dispatcher would take for this shape right now:
+ * 1 = row-tile path, 2 = small-M path.  Host-only; no CUDA call. */
+int rmm_dispatch_path(int64_t M, int64_t K, int64_t N);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SM_RMSNORM_MATMUL_H */

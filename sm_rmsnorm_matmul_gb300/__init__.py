@@ -1,0 +1,185 @@
+"""Python binding of libsm_rmsnorm_matmul.so (GB300 / sm_103a).
+
+Argument marshalling only: tensors are checked (bf16, contiguous, on the
+current CUDA device), their data pointers and the current CUDA stream are
+passed to the C ABI declared in ``include/rmsnorm_matmul.h``, and a non-zero
+status is raised as :class:`RmmError`.  Every step of the computation runs in
+the library's kernels; there is no CPU or PyTorch fallback.  If the library
+has not been built, the first call raises.
+
+    Y = rmsnorm_matmul(X, g, W, eps)   # RMSNorm(X; g, eps) @ W, fused
+    Xn = rmsnorm(X, g, eps)            # unfused pair, for comparison
+    C = matmul(A, B)
+
+PyTorch provides device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB_PATH
+
+__all__ = [
+    "RmmError", "lib", "rmsnorm_matmul", "rmsnorm", "matmul", "force_path",
+    "dispatch_path", "device_status", "status_string", "STATUS", "PATH_AUTO",
+    "PATH_ROWS", "PATH_COLS", "ABI_FUNCTIONS",
+]
+
+STATUS = {
+    0: "RMM_OK", 1: "RMM_ERR_INVALID_ARG", 2: "RMM_ERR_ALIGNMENT",
+    3: "RMM_ERR_UNSUPPORTED_DEVICE", 4: "RMM_ERR_LAUNCH",
+    5: "RMM_ERR_DEVICE_TIMEOUT", 6: "RMM_ERR_INTERNAL",
+}
+PATH_AUTO, PATH_ROWS, PATH_COLS = 0, 1, 2
+
+# Every function declared in include/rmsnorm_matmul.h.
+ABI_FUNCTIONS = ("rmsnorm_matmul", "rmsnorm", "matmul", "rmm_force_path",
+                 "rmm_device_status", "rmm_status_string", "rmm_dispatch_path")
+
+
+class RmmError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {STATUS.get(code, code)}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def _bind(l: ctypes.CDLL) -> ctypes.CDLL:
+    vp, i64, f32, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
+    l.rmsnorm_matmul.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, vp]
+    l.rmsnorm.argtypes = [vp, vp, vp, i64, i64, f32, vp]
+    l.matmul.argtypes = [vp, vp, vp, i64, i64, i64, vp]
+    l.rmm_force_path.argtypes = [i32]
+    l.rmm_device_status.argtypes = [vp]
+    l.rmm_status_string.argtypes = [i32]
+    l.rmm_status_string.restype = ctypes.c_char_p
+    l.rmm_dispatch_path.argtypes = [i64, i64, i64]
+    for name in ("rmsnorm_matmul", "rmsnorm", "matmul", "rmm_force_path",
+                 "rmm_device_status", "rmm_dispatch_path"):
+        getattr(l, name).restype = i32
+    return l
+
+
+def lib(path: str | None = None) -> ctypes.CDLL:
+    """The loaded C library.  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(
+                    f"CUDA library not built ({p} missing): run "
+                    "`python -m sm_rmsnorm_matmul_gb300.build` or __graft_entry__.build()")
+            _lib = _bind(ctypes.CDLL(p))
+        return _lib
+
+
+def _stream_ptr(stream) -> int:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _check_bf16(name, t, ndim):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got shape {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _raise(code: int, what: str):
+    if code != 0:
+        raise RmmError(code, what)
+
+
+def rmsnorm_matmul(X, g, W, eps: float = 1e-6, out=None, stream=None):
+    """Y[M,N] = RMSNorm(X[M,K]; g[K], eps) @ W[K,N] in one fused launch (bf16)."""
+    import torch
+    _check_bf16("X", X, 2)
+    _check_bf16("g", g, 1)
+    _check_bf16("W", W, 2)
+    M, K = X.shape
+    if g.shape[0] != K or W.shape[0] != K:
+        raise ValueError(f"shape mismatch: X {tuple(X.shape)}, g {tuple(g.shape)}, W {tuple(W.shape)}")
+    N = W.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    else:
+        _check_bf16("out", out, 2)
+        if tuple(out.shape) != (M, N):
+            raise ValueError(f"out must have shape {(M, N)}")
+    _raise(lib().rmsnorm_matmul(X.data_ptr(), g.data_ptr(), W.data_ptr(), out.data_ptr(),
+                                M, K, N, float(eps), _stream_ptr(stream)), "rmsnorm_matmul")
+    return out
+
+
+def rmsnorm(X, g, eps: float = 1e-6, out=None, stream=None):
+    """Xn[M,K] = bf16(X * g * r) (unfused RMSNorm)."""
+    import torch
+    _check_bf16("X", X, 2)
+    _check_bf16("g", g, 1)
+    M, K = X.shape
+    if g.shape[0] != K:
+        raise ValueError("g must have K elements")
+    if out is None:
+        out = torch.empty_like(X)
+    else:
+        _check_bf16("out", out, 2)
+        if out.shape != X.shape:
+            raise ValueError("out must have the shape of X")
+    _raise(lib().rmsnorm(X.data_ptr(), g.data_ptr(), out.data_ptr(), M, K, float(eps),
+                         _stream_ptr(stream)), "rmsnorm")
+    return out
+
+
+def matmul(A, B, out=None, stream=None):
+    """C[M,N] = bf16(A[M,K] @ B[K,N]) with fp32 accumulation (unfused MatMul)."""
+    import torch
+    _check_bf16("A", A, 2)
+    _check_bf16("B", B, 2)
+    M, K = A.shape
+    if B.shape[0] != K:
+        raise ValueError("inner dimensions differ")
+    N = B.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    else:
+        _check_bf16("out", out, 2)
+        if tuple(out.shape) != (M, N):
+            raise ValueError(f"out must have shape {(M, N)}")
+    _raise(lib().matmul(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, K, N,
+                        _stream_ptr(stream)), "matmul")
+    return out
+
+
+def force_path(path: int) -> int:
+    """0 auto, 1 row-tile path, 2 small-M path.  Returns the previous value."""
+    prev = lib().rmm_force_path(int(path))
+    if prev < 0:
+        raise ValueError(f"unknown path {path}")
+    return prev
+
+
+def dispatch_path(M: int, K: int, N: int) -> int:
+    return int(lib().rmm_dispatch_path(M, K, N))
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the in-kernel status."""
+    return int(lib().rmm_device_status(_stream_ptr(stream)))
+
+
+def status_string(code: int) -> str:
+    return lib().rmm_status_string(int(code)).decode()

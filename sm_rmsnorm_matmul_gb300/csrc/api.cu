@@ -1,0 +1,379 @@
+// api.cu -- the C ABI declared in include/rmsnorm_matmul.h: argument
+// validation, the shape dispatcher, TMA tensor-map encoding, the per-(device,
+// stream) split-K workspace, and launches.  Every step of the computation
+// runs in the kernels of kernels.cu; nothing here touches tensor data.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "launch.h"
+#include "rmsnorm_matmul.h"
+
+namespace {
+
+using rmm::kBK;
+
+std::atomic<int> g_force_path{0};
+
+constexpr int kPathRows = 1;
+constexpr int kPathCols = 2;
+// The dispatcher sends M <= kColsMaxRowsAuto to the small-M path.
+constexpr int64_t kColsMaxRowsAuto = 64;
+
+// ------------------------------------------------------------------ device
+struct DeviceInfo {
+    bool known = false;
+    bool supported = false;
+    int sm_count = 0;
+    int smem_optin = 0;
+};
+
+std::mutex g_dev_mu;
+std::map<int, DeviceInfo> g_dev;
+
+int current_device(int* dev, DeviceInfo* info) {
+    if (cudaGetDevice(dev) != cudaSuccess) return RMM_ERR_LAUNCH;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = g_dev[*dev];
+    if (!d.known) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, *dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, *dev) !=
+                cudaSuccess)
+            return RMM_ERR_LAUNCH;
+        d.supported = (major == 10 && minor == 3);
+        d.known = true;
+    }
+    *info = d;
+    return d.supported ? RMM_OK : RMM_ERR_UNSUPPORTED_DEVICE;
+}
+
+// ------------------------------------------------------------- tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Row-major bf16 matrix [rows, cols] read in boxes of [box_rows, 64 columns]
+// with the 128-byte swizzle; out-of-range elements read as zero.
+bool map_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// bf16 vector [n] read in boxes of 64 elements.
+bool map_1d(CUtensorMap* m, const void* ptr, uint64_t n) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    const cuuint64_t dims[1] = {n};
+    const cuuint64_t strides[1] = {n * 2};  // not read for rank 1
+    const cuuint32_t box[1] = {64};
+    const cuuint32_t estr[1] = {1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 1, const_cast<void*>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// -------------------------------------------------------------- validation
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const auto pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa < pb + nb && pb < pa + na;
+}
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int kNoop = -1;
+
+// Shared checks for (M, K, N) and eps.  Returns kNoop for an empty output.
+int check_sizes(int64_t M, int64_t K, int64_t N, float eps, bool has_eps) {
+    if (M < 0 || N < 0 || K < 1) return RMM_ERR_INVALID_ARG;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return RMM_ERR_INVALID_ARG;
+    if (has_eps && (!std::isfinite(eps) || eps < 0.f)) return RMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return kNoop;
+    if (K % 8 != 0 || N % 8 != 0) return RMM_ERR_ALIGNMENT;
+    return RMM_OK;
+}
+
+int check_ptrs(const void* out, size_t out_bytes, std::initializer_list<std::pair<const void*, size_t>> ins) {
+    if (!out) return RMM_ERR_INVALID_ARG;
+    for (auto& in : ins)
+        if (!in.first) return RMM_ERR_INVALID_ARG;
+    if (!aligned16(out)) return RMM_ERR_ALIGNMENT;
+    for (auto& in : ins)
+        if (!aligned16(in.first)) return RMM_ERR_ALIGNMENT;
+    for (auto& in : ins)
+        if (overlaps(out, out_bytes, in.first, in.second)) return RMM_ERR_INVALID_ARG;
+    return RMM_OK;
+}
+
+// --------------------------------------------------------------- workspace
+struct Workspace {
+    float* acc = nullptr;
+    size_t acc_bytes = 0;
+    float* ss = nullptr;
+    size_t ss_bytes = 0;
+    int* counters = nullptr;
+    size_t n_counters = 0;
+};
+
+std::mutex g_ws_mu;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+size_t round_up_pow2(size_t v) {
+    size_t p = 1 << 20;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+// Returns the split-K workspace of (dev, stream), grown to at least the given
+// sizes.  Growing synchronises the stream and is refused during capture.
+int get_workspace(int dev, cudaStream_t s, size_t acc_bytes, size_t ss_bytes, size_t ncount,
+                  Workspace* out) {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    Workspace& w = g_ws[{dev, s}];
+    if (w.acc_bytes >= acc_bytes && w.ss_bytes >= ss_bytes && w.n_counters >= ncount) {
+        *out = w;
+        return RMM_OK;
+    }
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+        return RMM_ERR_INTERNAL;  // first use of a shape must happen outside capture
+    if (cudaStreamSynchronize(s) != cudaSuccess) return RMM_ERR_LAUNCH;
+    Workspace n;
+    n.acc_bytes = round_up_pow2(std::max(acc_bytes, w.acc_bytes));
+    n.ss_bytes = round_up_pow2(std::max(ss_bytes, w.ss_bytes));
+    n.n_counters = std::max<size_t>(std::max(ncount, w.n_counters), 4096);
+    if (cudaMalloc(&n.acc, n.acc_bytes) != cudaSuccess) return RMM_ERR_INTERNAL;
+    if (cudaMalloc(&n.ss, n.ss_bytes) != cudaSuccess) {
+        cudaFree(n.acc);
+        return RMM_ERR_INTERNAL;
+    }
+    if (cudaMalloc(&n.counters, n.n_counters * sizeof(int)) != cudaSuccess) {
+        cudaFree(n.acc);
+        cudaFree(n.ss);
+        return RMM_ERR_INTERNAL;
+    }
+    if (cudaMemsetAsync(n.counters, 0, n.n_counters * sizeof(int), s) != cudaSuccess)
+        return RMM_ERR_LAUNCH;
+    if (w.acc) cudaFree(w.acc);
+    if (w.ss) cudaFree(w.ss);
+    if (w.counters) cudaFree(w.counters);
+    w = n;
+    *out = w;
+    return RMM_OK;
+}
+
+// ---------------------------------------------------------------- planning
+struct ColsPlan {
+    int MP, n_tiles, k_blocks, splits, kb_per_split, stages, grid;
+    uint32_t tmem_cols;
+};
+
+// Split K so that (column tiles x splits) fills the SMs: minimise the number
+// of k-blocks the busiest CTA streams, plus a fixed cost per unit of work.
+ColsPlan plan_cols(int64_t M, int64_t K, int64_t N, const DeviceInfo& d) {
+    ColsPlan p{};
+    p.MP = static_cast<int>(((M + 15) / 16) * 16);
+    p.n_tiles = static_cast<int>((N + rmm::kColsBN - 1) / rmm::kColsBN);
+    p.k_blocks = static_cast<int>((K + kBK - 1) / kBK);
+    const int G = d.sm_count > 0 ? d.sm_count : 1;
+    double best = 1e300;
+    for (int s = 1; s <= rmm::kColsMaxSplits && s <= p.k_blocks; ++s) {
+        const int kbps = (p.k_blocks + s - 1) / s;
+        const int real = (p.k_blocks + kbps - 1) / kbps;
+        if (real != s) continue;
+        const long units = static_cast<long>(p.n_tiles) * s;
+        const long waves = (units + G - 1) / G;
+        const double cost = static_cast<double>(waves) * (kbps + 2.0) + (s > 1 ? 1.0 : 0.0);
+        if (cost < best - 1e-9) {
+            best = cost;
+            p.splits = s;
+            p.kb_per_split = kbps;
+        }
+    }
+    const long units = static_cast<long>(p.n_tiles) * p.splits;
+    p.grid = static_cast<int>(std::min<long>(units, G));
+    const size_t fixed = rmm::cols_fixed_smem_bytes();
+    const size_t per = rmm::cols_stage_bytes(p.MP);
+    const size_t avail = d.smem_optin > 0 ? static_cast<size_t>(d.smem_optin) : 227 * 1024;
+    int st = static_cast<int>((avail - fixed) / per);
+    p.stages = std::max(2, std::min(rmm::kColsMaxStages, st));
+    uint32_t cols = 32;
+    while (cols < static_cast<uint32_t>(2 * p.MP)) cols <<= 1;
+    p.tmem_cols = cols;
+    return p;
+}
+
+int choose_path(int64_t M) {
+    const int f = g_force_path.load();
+    if (f == kPathRows || f == kPathCols) return f;
+    return M <= kColsMaxRowsAuto ? kPathCols : kPathRows;
+}
+
+// One launch of the tensor-core contraction, fused (RMSNorm folded in) or not.
+int run_contraction(bool fused, const void* X, const void* g, const void* W, void* Y, int64_t M,
+                    int64_t K, int64_t N, float eps, cudaStream_t stream) {
+    int dev = 0;
+    DeviceInfo d;
+    int rc = current_device(&dev, &d);
+    if (rc != RMM_OK) return rc;
+    const int path = choose_path(M);
+    CUtensorMap tmX, tmW, tmG;
+    if (!map_2d(&tmW, W, K, N, kBK)) return RMM_ERR_INTERNAL;
+    if (fused) {
+        if (!map_1d(&tmG, g, K)) return RMM_ERR_INTERNAL;
+    }
+    if (path == kPathCols) {
+        if (M > rmm::kColsMaxMP) return RMM_ERR_INVALID_ARG;
+        const ColsPlan p = plan_cols(M, K, N, d);
+        if (!map_2d(&tmX, X, M, K, p.MP)) return RMM_ERR_INTERNAL;
+        if (!fused) tmG = tmX;  // unused by the kernel
+        rmm::ColsLaunch a{};
+        a.M = static_cast<int>(M);
+        a.N = static_cast<int>(N);
+        a.K = static_cast<int>(K);
+        a.eps = eps;
+        a.MP = p.MP;
+        a.n_tiles = p.n_tiles;
+        a.k_blocks = p.k_blocks;
+        a.splits = p.splits;
+        a.kb_per_split = p.kb_per_split;
+        a.stages = p.stages;
+        a.grid = p.grid;
+        a.tmem_cols = p.tmem_cols;
+        if (p.splits > 1) {
+            Workspace w;
+            rc = get_workspace(dev, stream, static_cast<size_t>(p.splits) * M * N * sizeof(float),
+                               static_cast<size_t>(p.n_tiles) * p.splits * rmm::kColsMaxMP * sizeof(float),
+                               static_cast<size_t>(p.n_tiles), &w);
+            if (rc != RMM_OK) return rc;
+            a.ws_acc = w.acc;
+            a.ws_ss = w.ss;
+            a.counters = w.counters;
+        }
+        return rmm::launch_cols(fused, tmX, tmW, tmG, Y, a, stream) == cudaSuccess ? RMM_OK
+                                                                                  : RMM_ERR_LAUNCH;
+    }
+    if (!map_2d(&tmX, X, M, K, rmm::kRowsBM)) return RMM_ERR_INTERNAL;
+    if (!fused) tmG = tmX;
+    rmm::RowsLaunch a{};
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.eps = eps;
+    a.m_tiles = static_cast<int>((M + rmm::kRowsBM - 1) / rmm::kRowsBM);
+    a.n_tiles = static_cast<int>((N + rmm::kRowsBN - 1) / rmm::kRowsBN);
+    a.k_blocks = static_cast<int>((K + kBK - 1) / kBK);
+    const long tiles = static_cast<long>(a.m_tiles) * a.n_tiles;
+    a.grid = static_cast<int>(std::min<long>(tiles, d.sm_count));
+    return rmm::launch_rows(fused, tmX, tmW, tmG, Y, a, stream) == cudaSuccess ? RMM_OK
+                                                                              : RMM_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+int rmsnorm_matmul(const void* X, const void* g, const void* W, void* Y, int64_t M, int64_t K,
+                   int64_t N, float eps, cudaStream_t stream) {
+    int rc = check_sizes(M, K, N, eps, true);
+    if (rc == kNoop) return RMM_OK;
+    if (rc != RMM_OK) return rc;
+    rc = check_ptrs(Y, static_cast<size_t>(M) * N * 2,
+                    {{X, static_cast<size_t>(M) * K * 2}, {g, static_cast<size_t>(K) * 2},
+                     {W, static_cast<size_t>(K) * N * 2}});
+    if (rc != RMM_OK) return rc;
+    return run_contraction(true, X, g, W, Y, M, K, N, eps, stream);
+}
+
+int matmul(const void* A, const void* B, void* C, int64_t M, int64_t K, int64_t N,
+           cudaStream_t stream) {
+    int rc = check_sizes(M, K, N, 0.f, false);
+    if (rc == kNoop) return RMM_OK;
+    if (rc != RMM_OK) return rc;
+    rc = check_ptrs(C, static_cast<size_t>(M) * N * 2,
+                    {{A, static_cast<size_t>(M) * K * 2}, {B, static_cast<size_t>(K) * N * 2}});
+    if (rc != RMM_OK) return rc;
+    return run_contraction(false, A, nullptr, B, C, M, K, N, 0.f, stream);
+}
+
+int rmsnorm(const void* X, const void* g, void* Xn, int64_t M, int64_t K, float eps,
+            cudaStream_t stream) {
+    // N plays no part; pass K so that the N checks pass trivially.
+    int rc = check_sizes(M, K, K, eps, true);
+    if (rc == kNoop) return RMM_OK;
+    if (rc != RMM_OK) return rc;
+    rc = check_ptrs(Xn, static_cast<size_t>(M) * K * 2,
+                    {{X, static_cast<size_t>(M) * K * 2}, {g, static_cast<size_t>(K) * 2}});
+    if (rc != RMM_OK) return rc;
+    int dev = 0;
+    DeviceInfo d;
+    rc = current_device(&dev, &d);
+    if (rc != RMM_OK) return rc;
+    return rmm::launch_rmsnorm(X, g, Xn, static_cast<int>(M), static_cast<int>(K), eps, stream) ==
+                   cudaSuccess
+               ? RMM_OK
+               : RMM_ERR_LAUNCH;
+}
+
+int rmm_force_path(int path) {
+    if (path < 0 || path > 2) return -1;
+    return g_force_path.exchange(path);
+}
+
+int rmm_dispatch_path(int64_t M, int64_t K, int64_t N) {
+    (void)K;
+    (void)N;
+    return choose_path(M);
+}
+
+int rmm_device_status(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return RMM_ERR_LAUNCH;
+    int v = 0;
+    if (rmm::read_and_clear_status(&v) != cudaSuccess) return RMM_ERR_LAUNCH;
+    return v;
+}
+
+const char* rmm_status_string(int code) {
+    switch (code) {
+        case RMM_OK: return "RMM_OK";
+        case RMM_ERR_INVALID_ARG: return "RMM_ERR_INVALID_ARG";
+        case RMM_ERR_ALIGNMENT: return "RMM_ERR_ALIGNMENT";
+        case RMM_ERR_UNSUPPORTED_DEVICE: return "RMM_ERR_UNSUPPORTED_DEVICE";
+        case RMM_ERR_LAUNCH: return "RMM_ERR_LAUNCH";
+        case RMM_ERR_DEVICE_TIMEOUT: return "RMM_ERR_DEVICE_TIMEOUT";
+        case RMM_ERR_INTERNAL: return "RMM_ERR_INTERNAL";
+        default: return "RMM_UNKNOWN_STATUS";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,123 @@
+"""The C ABI on the CPU: the library loads, exports every declared symbol, and
+rejects bad arguments before making any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sm_rmsnorm_matmul_gb300 as rmm
+from sm_rmsnorm_matmul_gb300 import build as rbuild
+
+HEADER = os.path.join(rbuild.INCLUDE, "rmsnorm_matmul.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    rbuild.build()
+    return rmm.lib()
+
+
+def declared_functions():
+    with open(HEADER) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return set(re.findall(r"^\s*(?:int|const char\*)\s+(\w+)\s*\(", src, flags=re.M))
+
+
+def test_header_declares_binding_functions():
+    assert declared_functions() == set(rmm.ABI_FUNCTIONS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for code, name in rmm.STATUS.items():
+        assert rmm.status_string(code) == name
+    assert rmm.status_string(99) == "RMM_UNKNOWN_STATUS"
+
+
+def test_force_path_roundtrip(lib):
+    assert rmm.force_path(rmm.PATH_ROWS) == rmm.PATH_AUTO
+    assert rmm.dispatch_path(8, 1024, 1024) == rmm.PATH_ROWS
+    assert rmm.force_path(rmm.PATH_COLS) == rmm.PATH_ROWS
+    assert rmm.dispatch_path(4096, 4096, 4096) == rmm.PATH_COLS
+    assert rmm.force_path(rmm.PATH_AUTO) == rmm.PATH_COLS
+    assert lib.rmm_force_path(7) == -1
+    assert rmm.force_path(rmm.PATH_AUTO) == rmm.PATH_AUTO
+
+
+def test_dispatch_by_rows(lib):
+    assert rmm.dispatch_path(1, 4096, 6144) == rmm.PATH_COLS
+    assert rmm.dispatch_path(64, 4096, 28672) == rmm.PATH_COLS
+    assert rmm.dispatch_path(65, 4096, 6144) == rmm.PATH_ROWS
+    assert rmm.dispatch_path(4096, 4096, 6144) == rmm.PATH_ROWS
+
+
+A16 = 0x10000          # a 16-byte aligned fake address; never dereferenced
+B16 = 0x20000000
+C16 = 0x40000000
+D16 = 0x60000000
+
+
+@pytest.mark.parametrize("args,expect", [
+    # (X, g, W, Y, M, K, N, eps)
+    ((0, B16, C16, D16, 8, 64, 64, 1e-6), 1),                  # NULL X
+    ((A16, B16, C16, 0, 8, 64, 64, 1e-6), 1),                  # NULL Y
+    ((A16, B16, C16, D16, -1, 64, 64, 1e-6), 1),               # M < 0
+    ((A16, B16, C16, D16, 8, 0, 64, 1e-6), 1),                 # K = 0
+    ((A16, B16, C16, D16, 8, 64, -8, 1e-6), 1),                # N < 0
+    ((A16, B16, C16, D16, 8, 64, 64, -1.0), 1),                # eps < 0
+    ((A16, B16, C16, D16, 8, 64, 64, float("nan")), 1),        # eps NaN
+    ((A16, B16, C16, D16, 8, 64, 64, float("inf")), 1),        # eps inf
+    ((A16, B16, C16, D16, 8, 60, 64, 1e-6), 2),                # K % 8
+    ((A16, B16, C16, D16, 8, 64, 68, 1e-6), 2),                # N % 8
+    ((A16 + 2, B16, C16, D16, 8, 64, 64, 1e-6), 2),            # X misaligned
+    ((A16, B16, C16, D16 + 8, 8, 64, 64, 1e-6), 2),            # Y misaligned
+    ((A16, B16, C16, A16 + 512, 8, 64, 64, 1e-6), 1),          # Y overlaps X
+    ((A16, B16, C16, C16, 8, 64, 64, 1e-6), 1),                # Y aliases W
+    ((A16, B16, C16, D16, 2**31, 64, 64, 1e-6), 1),            # M too large
+    ((0, 0, 0, 0, 0, 64, 64, 1e-6), 0),                        # M = 0: no-op
+    ((0, 0, 0, 0, 8, 64, 0, 1e-6), 0),                         # N = 0: no-op
+])
+def test_fused_validation(lib, args, expect):
+    X, g, W, Y, M, K, N, eps = args
+    assert lib.rmsnorm_matmul(X, g, W, Y, M, K, N, eps, None) == expect
+
+
+def test_unfused_validation(lib):
+    assert lib.rmsnorm(0, B16, D16, 8, 64, 1e-6, None) == 1
+    assert lib.rmsnorm(A16, B16, D16, 8, 63, 1e-6, None) == 2
+    assert lib.rmsnorm(A16, B16, A16, 8, 64, 1e-6, None) == 1
+    assert lib.rmsnorm(0, 0, 0, 0, 64, 1e-6, None) == 0
+    assert lib.matmul(A16, C16, 0, 8, 64, 64, None) == 1
+    assert lib.matmul(A16, C16, D16 + 4, 8, 64, 64, None) == 2
+    assert lib.matmul(A16, C16, D16, 8, 0, 64, None) == 1
+    assert lib.matmul(0, 0, 0, 8, 64, 0, None) == 0
+
+
+def test_binding_rejects_cpu_tensors(lib):
+    torch = pytest.importorskip("torch")
+    X = torch.zeros(8, 64, dtype=torch.bfloat16)
+    g = torch.ones(64, dtype=torch.bfloat16)
+    W = torch.zeros(64, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        rmm.rmsnorm_matmul(X, g, W)
+    with pytest.raises(TypeError, match="bfloat16"):
+        rmm.rmsnorm_matmul(X.float(), g, W)
+
+
+def test_no_oracle_in_product_path():
+    # The library package must not import the test oracle.
+    pkg = os.path.dirname(rmm.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                with open(os.path.join(root, f)) as fh:
+                    src = fh.read()
+                assert not re.search(r"^\s*(import|from)\s+oracle", src, flags=re.M), f
+                assert "rmm_oracle" not in src, f

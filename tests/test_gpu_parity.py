@@ -1,0 +1,216 @@
+"""GPU parity: the CUDA library, called through its C ABI, against the fp64
+oracle on the same seeded inputs.
+
+Acceptance for every checked element (bf16 in/out, fp32 accumulation):
+    |y - y_ref| <= 1e-2 + 1e-2 * |y_ref|,   NaN/Inf fail.
+"""
+import numpy as np
+import pytest
+
+import oracle
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+ATOL = 1e-2
+RTOL = 1e-2
+
+
+@pytest.fixture(scope="module")
+def rmm():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sm_rmsnorm_matmul_gb300 as m
+    from sm_rmsnorm_matmul_gb300 import build
+    build.build()
+    m.lib()
+    return m
+
+
+@pytest.fixture
+def forced(rmm):
+    prev = []
+
+    def set_path(p):
+        prev.append(rmm.force_path(p))
+
+    yield set_path
+    if prev:
+        rmm.force_path(prev[0])
+
+
+def run_fused(rmm, X, g, W, eps):
+    Y = rmm.rmsnorm_matmul(X.cuda(), g.cuda(), W.cuda(), eps)
+    torch.cuda.synchronize()
+    assert rmm.device_status() == 0
+    return Y.cpu()
+
+
+def assert_close(Y, ref, what):
+    bad, max_abs, max_rel = oracle.tolerance_violations(Y, ref, ATOL, RTOL)
+    assert bad == 0, f"{what}: {bad} of {ref.size} elements out of tolerance (max abs err {max_abs:.3e})"
+
+
+# --------------------------------------------------------------- workloads
+SMALL_WORKLOADS = ["tiny_8x1024x1024", "decode_qkv_16x4096x6144",
+                   "decode_gatedmlp_64x4096x28672"]
+LARGE_WORKLOADS = ["prefill_qkv_4096x4096x6144", "large_prefill_16384x8192x8192"]
+
+
+@pytest.mark.parametrize("name", SMALL_WORKLOADS)
+@pytest.mark.parametrize("path", [0, 1, 2])
+def test_workload_all_rows(rmm, forced, name, path):
+    from sm_rmsnorm_matmul_gb300 import inputs
+    w = inputs.WORKLOADS[name]
+    X, g, W = inputs.generate_workload(w)
+    forced(path)
+    Y = run_fused(rmm, X, g, W, w.eps)
+    ref = oracle.rmsnorm_matmul(X, g, W, w.eps)
+    assert_close(Y, ref, f"{name} path {path}")
+
+
+@pytest.mark.parametrize("name", LARGE_WORKLOADS)
+def test_workload_sampled_rows(rmm, name):
+    """Full-size launch (the configuration the benchmark times); the oracle
+    checks a 256-row sample of every output column."""
+    from sm_rmsnorm_matmul_gb300 import inputs
+    w = inputs.WORKLOADS[name]
+    X, g, W = inputs.generate_workload(w)
+    Y = run_fused(rmm, X, g, W, w.eps)
+    rows = inputs.sample_rows(w.M, 256)
+    ref = oracle.rmsnorm_matmul(X[rows], g, W, w.eps)
+    assert_close(Y[rows], ref, name)
+    assert torch.isfinite(Y.float()).all()
+
+
+# -------------------------------------------------------- ragged and edges
+RAGGED = [
+    (1, 64, 8), (7, 72, 136), (16, 1024, 1000), (33, 520, 264), (64, 4096, 1032),
+    (65, 256, 256), (129, 1032, 520), (255, 328, 392), (300, 2048, 2056),
+]
+
+
+@pytest.mark.parametrize("M,K,N", RAGGED)
+@pytest.mark.parametrize("path", [1, 2])
+def test_ragged(rmm, forced, M, K, N, path):
+    from sm_rmsnorm_matmul_gb300 import inputs
+    if path == 2 and M > 128:
+        pytest.skip("small-M path holds at most 128 rows")
+    X, g, W = inputs.random_problem(M, K, N, seed=M * 7 + K + N, x_kind="row_scaled")
+    forced(path)
+    Y = run_fused(rmm, X, g, W, 1e-5)
+    ref = oracle.rmsnorm_matmul(X, g, W, 1e-5)
+    assert_close(Y, ref, f"{M}x{K}x{N} path {path}")
+
+
+def test_small_m_rejects_large_m_when_forced(rmm, forced):
+    forced(2)
+    X = torch.zeros(129, 64, dtype=torch.bfloat16, device="cuda")
+    g = torch.ones(64, dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(rmm.RmmError):
+        rmm.rmsnorm_matmul(X, g, W)
+
+
+def test_empty_output_is_noop(rmm):
+    X = torch.zeros(0, 64, dtype=torch.bfloat16, device="cuda")
+    g = torch.ones(64, dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
+    Y = rmm.rmsnorm_matmul(X, g, W)
+    assert Y.shape == (0, 64)
+
+
+def test_zero_row_gives_zero(rmm):
+    from sm_rmsnorm_matmul_gb300 import inputs
+    X, g, W = inputs.random_problem(16, 256, 128, seed=3)
+    X[5] = 0
+    for path in (1, 2):
+        prev = rmm.force_path(path)
+        try:
+            Y = run_fused(rmm, X, g, W, 1e-6)
+        finally:
+            rmm.force_path(prev)
+        assert torch.all(Y[5] == 0)
+        assert_close(Y, oracle.rmsnorm_matmul(X, g, W, 1e-6), f"zero row, path {path}")
+
+
+def test_deterministic(rmm):
+    from sm_rmsnorm_matmul_gb300 import inputs
+    X, g, W = inputs.random_problem(16, 4096, 6144, seed=21)
+    a = run_fused(rmm, X, g, W, 1e-6)
+    b = run_fused(rmm, X, g, W, 1e-6)
+    assert torch.equal(a, b)
+
+
+def test_scale_invariance_on_gpu(rmm):
+    # Scaling X by a power of two leaves the rounded products and the
+    # statistic's ratio unchanged; with eps = 0 the outputs stay in tolerance
+    # of each other and of the oracle.
+    from sm_rmsnorm_matmul_gb300 import inputs
+    X, g, W = inputs.random_problem(64, 2048, 1024, seed=8)
+    for path in (1, 2):
+        prev = rmm.force_path(path)
+        try:
+            a = run_fused(rmm, X, g, W, 0.0)
+            b = run_fused(rmm, (X.float() * 4).to(torch.bfloat16), g, W, 0.0)
+        finally:
+            rmm.force_path(prev)
+        assert_close(b, a.double().numpy(), f"scale invariance path {path}")
+
+
+def test_identity_weight_is_rmsnorm(rmm):
+    from sm_rmsnorm_matmul_gb300 import inputs
+    X, g, _ = inputs.random_problem(48, 256, 8, seed=4, x_kind="row_scaled")
+    W = torch.eye(256, dtype=torch.bfloat16)
+    Y = run_fused(rmm, X, g, W, 1e-6)
+    ref = oracle.rmsnorm(X, g, 1e-6)
+    assert_close(Y, ref, "W = I")
+
+
+# ------------------------------------------------------------ unfused pair
+@pytest.mark.parametrize("M,K", [(1, 8), (16, 4096), (300, 1032), (4096, 4096)])
+def test_unfused_rmsnorm(rmm, M, K):
+    from sm_rmsnorm_matmul_gb300 import inputs
+    X, g, _ = inputs.random_problem(M, K, 8, seed=M + K, x_kind="outlier_entries")
+    Xn = rmm.rmsnorm(X.cuda(), g.cuda(), 1e-6)
+    torch.cuda.synchronize()
+    assert_close(Xn.cpu(), oracle.rmsnorm(X, g, 1e-6), f"rmsnorm {M}x{K}")
+
+
+@pytest.mark.parametrize("M,K,N", [(16, 4096, 6144), (100, 520, 264), (512, 1024, 2048)])
+@pytest.mark.parametrize("path", [0, 1, 2])
+def test_unfused_matmul(rmm, forced, M, K, N, path):
+    from sm_rmsnorm_matmul_gb300 import inputs
+    if path == 2 and M > 128:
+        pytest.skip("small-M path holds at most 128 rows")
+    A, _, B = inputs.random_problem(M, K, N, seed=M * 3 + N)
+    forced(path)
+    C = rmm.matmul(A.cuda(), B.cuda())
+    torch.cuda.synchronize()
+    assert rmm.device_status() == 0
+    assert_close(C.cpu(), oracle.matmul(A, B), f"matmul {M}x{K}x{N} path {path}")
+
+
+def test_unfused_pair_matches_fused(rmm):
+    from sm_rmsnorm_matmul_gb300 import inputs
+    w = inputs.WORKLOADS["decode_qkv_16x4096x6144"]
+    X, g, W = inputs.generate_workload(w)
+    Xd, gd, Wd = X.cuda(), g.cuda(), W.cuda()
+    Y2 = rmm.matmul(rmm.rmsnorm(Xd, gd, w.eps), Wd)
+    torch.cuda.synchronize()
+    assert_close(Y2.cpu(), oracle.rmsnorm_matmul(X, g, W, w.eps), "unfused pair")
+
+
+def test_streams_are_honoured(rmm):
+    from sm_rmsnorm_matmul_gb300 import inputs
+    X, g, W = inputs.random_problem(16, 1024, 2048, seed=6)
+    Xd, gd, Wd = X.cuda(), g.cuda(), W.cuda()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        Y = rmm.rmsnorm_matmul(Xd, gd, Wd, 1e-6)
+    s.synchronize()
+    assert_close(Y.cpu(), oracle.rmsnorm_matmul(X, g, W, 1e-6), "side stream")
+
+
+def test_device_status_clean(rmm):
+    assert rmm.device_status() == 0
