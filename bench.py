@@ -1,0 +1,550 @@
+"""Benchmark of fused RMSNorm+MatMul on GB300 through the library's C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--shapes all|none] [--no-cpu-baseline]
+
+One step = one rmsnorm_matmul() call over one batch of the workload (the whole
+hot path: gain, row statistic, contraction, scaled epilogue, all in one
+kernel).  Default workload: decode-time QKV projection, X [16,4096], W
+[4096,6144] (HBM-bound on W).  The headline value is HBM GB/s of algorithmic
+traffic (X + W + Y bytes, each moved once) over the device time of exactly K
+steps.
+
+Timing: the K steps are captured as back-to-back calls in CUDA graphs on one
+stream and replayed once, bracketed by CUDA events on that stream, after W
+untimed warm-up calls.  Cold L2: every step reads its own copy of X, g, W and
+writes its own Y; the copies rotate and together exceed 3x the L2 size, so no
+step finds its inputs in L2.  SM clocks and throttle reasons are sampled with
+nvidia-smi during the timed region.
+
+Also reported on the same JSON line: a roofline object for the fused kernel,
+an end-to-end number through the C ABI from pinned host buffers (host->device
+copies of X, g and W and the device->host copy of Y inside the timed region),
+the fp64 CPU oracle timed on the host cores (cpu_baseline), and per-shape
+results for all five workloads.
+
+--impl reference times the fp64 CPU oracle (the only reference available:
+the pages ship no code) on the same workload and prints the same JSON line
+with "impl": "reference".
+
+Multi-GPU: the operation has no exchange step at this size, so N GPUs run N
+independent replicas (weak scaling); a gloo barrier brackets the timed region
+and rank 0 reports the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from datetime import datetime
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "RMSNorm+MatMul TFLOP/s & HBM GB/s, % of GB300 roofline, per shape"
+DEFAULT_WORKLOAD = "decode_qkv_16x4096x6144"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------ helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+    def find(obj, key):
+        if isinstance(obj, dict):
+            if key in obj and isinstance(obj[key], (int, float)):
+                return float(obj[key])
+            for v in obj.values():
+                r = find(v, key)
+                if r is not None:
+                    return r
+        return None
+
+    out = {}
+    for k in FALLBACK_PEAKS:
+        v = find(d, k)
+        out[k] = v if v is not None else FALLBACK_PEAKS[k]
+    return out, "measured"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+        self.windows = []
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def mark(self, t0, t1):
+        self.windows.append((t0, t1))
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) < 9:
+                        continue
+                    try:
+                        ts = datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                        rows.append((ts, float(parts[1]), float(parts[2]), parts[3], parts[4:]))
+                    except ValueError:
+                        continue
+            os.unlink(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        inside = [r for r in rows if any(a - 0.15 <= r[0] <= b + 0.15 for a, b in self.windows)]
+        use = inside or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[4][1:5])
+                          if v.lower().startswith("active")})
+        powers = []
+        for r in use:
+            try:
+                powers.append(float(r[3]))
+            except ValueError:
+                pass
+        return {"sm_mhz": statistics.median(r[1] for r in use),
+                "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons,
+                "power_w": statistics.median(powers) if powers else None,
+                "samples": len(use), "in_window": bool(inside)}
+
+
+def traffic_from_profile(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    source is unchanged since the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        with open(os.path.join(ROOT, "sm_rmsnorm_matmul_gb300", "csrc", "kernels.cu"), "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()[:16]
+    except (OSError, ValueError):
+        return None
+    e = d.get(workload)
+    if not e or e.get("kernels_cu_sha256_16") != h:
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------- GPU timing
+def make_copies(w, n_copies, device, torch, inputs):
+    X, g, W = inputs.generate_workload(w)
+    Xd, gd, Wd = X.to(device), g.to(device), W.to(device)
+    copies = []
+    for i in range(n_copies):
+        if i == 0:
+            xs, gs, ws = Xd, gd, Wd
+        else:
+            xs, gs, ws = Xd.clone(), gd.clone(), Wd.clone()
+        ys = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device)
+        copies.append((xs, gs, ws, ys))
+    return (X, g, W), copies
+
+
+def n_rotating_copies(w, l2_bytes):
+    per = w.bytes_algorithmic
+    return max(1, math.ceil(3 * l2_bytes / per) + 1) if per < 3 * l2_bytes else 1
+
+
+def time_graph(torch, stream, step_fn, n_copies, K, chunk=500):
+    """Capture K back-to-back steps (step i uses copy i % n_copies) in CUDA
+    graphs of at most `chunk` steps, replay them once, return seconds."""
+    graphs = []
+    done = 0
+    while done < K:
+        c = min(chunk, K - done)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for i in range(done, done + c):
+                step_fn(i % n_copies)
+        graphs.append(gr)
+        done += c
+    for gr in graphs:          # upload / first replay, untimed
+        gr.replay()
+    stream.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for gr in graphs:
+            gr.replay()
+        end.record(stream)
+    end.synchronize()
+    t1 = time.time()
+    return start.elapsed_time(end) / 1e3, (t0, t1), graphs
+
+
+def bench_workload(torch, rmm, inputs, w, K, W_warm, device, stream, l2, with_unfused=True,
+                   sampler=None, barrier=None):
+    n_copies = n_rotating_copies(w, l2)
+    host, copies = make_copies(w, n_copies, device, torch, inputs)
+
+    def step(i):
+        x, g, wt, y = copies[i]
+        rmm.rmsnorm_matmul(x, g, wt, w.eps, out=y, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(W_warm, 1)):
+            step(i % n_copies)
+    stream.synchronize()
+    if rmm.device_status(stream) != 0:
+        raise RuntimeError("device status not clean after warm-up")
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    secs, window, graphs = time_graph(torch, stream, step, n_copies, K)
+    torch.cuda.synchronize()
+    if barrier:
+        secs = barrier(secs)
+    if sampler:
+        sampler.mark(*window)
+    status = rmm.device_status(stream)
+    del graphs
+    res = {"secs": secs, "n_copies": n_copies, "status": status, "host": host,
+           "copies": copies, "path": rmm.dispatch_path(w.M, w.K, w.N)}
+    if with_unfused:
+        xn = [torch.empty((w.M, w.K), dtype=torch.bfloat16, device=device) for _ in range(n_copies)]
+
+        def step_unfused(i):
+            x, g, wt, y = copies[i]
+            rmm.rmsnorm(x, g, w.eps, out=xn[i], stream=stream)
+            rmm.matmul(xn[i], wt, out=y, stream=stream)
+
+        with torch.cuda.stream(stream):
+            for i in range(2):
+                step_unfused(i % n_copies)
+        stream.synchronize()
+        ku = max(1, min(K, 200))
+        s_unf, _, g2 = time_graph(torch, stream, step_unfused, n_copies, ku)
+        res["unfused_secs_per_step"] = s_unf / ku
+        del g2, xn
+    return res
+
+
+def e2e_bench(torch, rmm, w, host, device, stream, K):
+    """Pinned host X, g, W -> device, fused call, Y -> pinned host, per step."""
+    X, g, W = host
+    hX, hg, hW = X.pin_memory(), g.pin_memory(), W.pin_memory()
+    hY = torch.empty((w.M, w.N), dtype=torch.bfloat16).pin_memory()
+    dX = torch.empty_like(hX, device=device)
+    dg = torch.empty_like(hg, device=device)
+    dW = torch.empty_like(hW, device=device)
+    dY = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device)
+
+    def step():
+        with torch.cuda.stream(stream):
+            dX.copy_(hX, non_blocking=True)
+            dg.copy_(hg, non_blocking=True)
+            dW.copy_(hW, non_blocking=True)
+            rmm.rmsnorm_matmul(dX, dg, dW, w.eps, out=dY, stream=stream)
+            hY.copy_(dY, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    stream.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+    for _ in range(K):
+        step()
+    with torch.cuda.stream(stream):
+        end.record(stream)
+    end.synchronize()
+    secs = start.elapsed_time(end) / 1e3
+    h2d = (hX.numel() + hg.numel() + hW.numel()) * 2
+    d2h = hY.numel() * 2
+    return secs, h2d, d2h
+
+
+# ----------------------------------------------------------- CPU reference
+def cpu_oracle_run(w, budget_s, steps=None, warmup=0):
+    """Time the fp64 oracle on host cores.  Returns (secs_per_step, bytes per
+    step, sample description, threads).  With `steps`, runs exactly that many
+    steps, each on a row sample sized so the whole run fits the budget."""
+    import numpy as np
+    import oracle
+    from sm_rmsnorm_matmul_gb300 import inputs
+    X, g, W = inputs.generate_workload(w)
+    Xf, gf, Wf = oracle.to_f64(X), oracle.to_f64(g), oracle.to_f64(W)
+    lib = oracle.load()
+    threads = oracle.max_threads(lib)
+    # probe: one row block to estimate the cost per row
+    probe_rows = min(w.M, max(1, threads))
+    t = time.perf_counter()
+    oracle.rmsnorm_matmul(Xf[:probe_rows], gf, Wf, w.eps, lib=lib)
+    per_row = (time.perf_counter() - t) / probe_rows
+    total_steps = steps if steps is not None else None
+    if total_steps is None:
+        rows = w.M if per_row * w.M <= budget_s else max(1, int(budget_s / per_row))
+        rows = min(rows, w.M)
+        reps = max(1, int(budget_s / max(per_row * rows, 1e-6)))
+    else:
+        rows_fit = int(budget_s / max(per_row * total_steps, 1e-9))
+        rows = max(1, min(w.M, rows_fit))
+        reps = total_steps
+    rows = max(1, min(rows, w.M))
+    idx = inputs.sample_rows(w.M, rows) if rows < w.M else list(range(w.M))
+    Xs = np.ascontiguousarray(Xf[idx])
+    for _ in range(warmup):
+        oracle.rmsnorm_matmul(Xs, gf, Wf, w.eps, lib=lib)
+    t = time.perf_counter()
+    for _ in range(reps):
+        oracle.rmsnorm_matmul(Xs, gf, Wf, w.eps, lib=lib)
+    secs = (time.perf_counter() - t) / reps
+    nbytes = 2 * (len(idx) * w.K + w.K * w.N + len(idx) * w.N)
+    sample = (f"{len(idx)} of {w.M} rows x all {w.N} columns, {reps} repetitions, "
+              f"fp64 oracle, {threads} OpenMP threads")
+    return secs, nbytes, sample, threads, len(idx), reps
+
+
+# ---------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--shapes", choices=["all", "none"], default="all")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    from sm_rmsnorm_matmul_gb300 import inputs
+    w = inputs.WORKLOADS[args.workload]
+    ws, rank, local = dist_env()
+
+    if args.impl == "reference":
+        return run_reference(args, w, ws, rank)
+
+    import torch
+    import sm_rmsnorm_matmul_gb300 as rmm
+    rmm.lib()  # fail loudly if the CUDA library is missing
+
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        pg = dist
+
+    def barrier(val=None):
+        if pg is None:
+            return val
+        if val is None:
+            pg.barrier()
+            return None
+        t = torch.tensor([val], dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        return float(t.item())
+
+    device = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(device)
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 1024 * 1024))
+    gpu_id = None
+    try:
+        gpu_id = f"GPU-{props.uuid}"
+    except Exception:  # noqa: BLE001
+        pass
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.Stream(device=device)
+
+    with ClockSampler(gpu_id) as sampler:
+        main_res = bench_workload(torch, rmm, inputs, w, args.steps, args.warmup, device,
+                                  stream, l2, with_unfused=True, sampler=sampler,
+                                  barrier=barrier if ws > 1 else None)
+        host = main_res["host"]
+        e2e_steps = max(3, min(args.steps, 200))
+        e2e_secs, h2d, d2h = e2e_bench(torch, rmm, w, host, device, stream, e2e_steps)
+        if ws > 1:
+            e2e_secs = barrier(e2e_secs)
+        del main_res["copies"]
+        shapes = []
+        if args.shapes == "all" and rank == 0:
+            for name in inputs.WORKLOAD_ORDER:
+                ww = inputs.WORKLOADS[name]
+                est = max(ww.flops / (peaks["bf16_tflops"] * 1e12),
+                          ww.bytes_xwy / (peaks["hbm_gbs"] * 1e9))
+                k = int(min(5000, max(20, 0.2 / max(est, 1e-7))))
+                r = bench_workload(torch, rmm, inputs, ww, k, 3, device, stream, l2,
+                                   with_unfused=True, sampler=sampler)
+                t = r["secs"] / k
+                shapes.append(shape_entry(ww, t, r, peaks, k))
+                del r
+                torch.cuda.empty_cache()
+    clocks = sampler.summary()
+
+    K = args.steps
+    t_step = main_res["secs"] / K
+    bytes_step = w.bytes_xwy
+    value = ws * bytes_step / t_step / 1e9
+    achieved = w.bytes_algorithmic / t_step / 1e9
+    bound = "hbm" if w.flops / w.bytes_xwy < 290 else "tensor"
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
+    else:
+        tf = w.flops / t_step / 1e12
+        roof = {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4)}
+    roof["traffic"] = traffic_from_profile(w.name)
+    roof["peak_source"] = peak_src
+    roof["kernel"] = "cols_kernel<fused>" if main_res["path"] == 2 else "rows_kernel<fused>"
+    roof["algorithmic_bytes_per_launch"] = w.bytes_algorithmic
+
+    out = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_step * 1e3, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; see sm_rmsnorm_matmul_gb300/inputs.py)",
+        "config": {
+            "workload": w.name, "M": w.M, "K": w.K, "N": w.N, "eps": w.eps, "seed": w.seed,
+            "accumulate": "fp32", "path": "small-M (cols)" if main_res["path"] == 2 else "row-tile",
+            "l2": f"rotating input/output copies: {main_res['n_copies']} x "
+                  f"{w.bytes_algorithmic / 1e6:.1f} MB > 3 x L2 ({l2 / 1e6:.0f} MB)"
+                  if main_res["n_copies"] > 1 else
+                  f"inputs ({w.bytes_algorithmic / 1e6:.0f} MB) larger than L2 ({l2 / 1e6:.0f} MB)",
+            "timing": "CUDA graphs of back-to-back C-ABI calls, CUDA events on the launch stream",
+            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+        },
+        "tflops": round(w.flops / t_step / 1e12, 2),
+        "roofline": roof,
+        "roofline_time_frac": round(max(w.flops / (peaks["bf16_tflops"] * 1e12),
+                                        w.bytes_xwy / (peaks["hbm_gbs"] * 1e9)) / t_step, 4),
+        "unfused_pair_ms_per_step": round(main_res["unfused_secs_per_step"] * 1e3, 6),
+        "e2e": {"value": round(ws * bytes_step / (e2e_secs / e2e_steps) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_secs / e2e_steps * 1e3, 4), "steps": e2e_steps},
+        "gpu_launches": K,
+        "clocks": clocks,
+        "device_status": main_res["status"],
+    }
+    if shapes:
+        out["shapes"] = shapes
+    if rank == 0 and not args.no_cpu_baseline:
+        secs, nbytes, sample, threads, _, _ = cpu_oracle_run(w, args.cpu_budget)
+        out["cpu_baseline"] = {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s",
+                               "cores": threads, "kind": "oracle", "sample": sample,
+                               "secs_per_call": round(secs, 4)}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if pg is not None:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+def shape_entry(w, t, r, peaks, k):
+    tflops = w.flops / t / 1e12
+    gbs = w.bytes_xwy / t / 1e9
+    roof_t = max(w.flops / (peaks["bf16_tflops"] * 1e12), w.bytes_xwy / (peaks["hbm_gbs"] * 1e9))
+    bound = "tensor" if w.flops / (peaks["bf16_tflops"] * 1e12) > w.bytes_xwy / (peaks["hbm_gbs"] * 1e9) else "hbm"
+    e = {"workload": w.name, "path": "small-M (cols)" if r["path"] == 2 else "row-tile",
+         "steps": k, "us_per_call": round(t * 1e6, 3), "tflops": round(tflops, 2),
+         "hbm_gbs": round(gbs, 1), "bound": bound, "roofline_frac": round(roof_t / t, 4),
+         "copies": r["n_copies"], "device_status": r["status"]}
+    if bound == "tensor":
+        e["frac_of_tensor_peak_sustained"] = round(tflops / peaks["bf16_tflops_sustained"], 4)
+    if "unfused_secs_per_step" in r:
+        e["unfused_pair_us"] = round(r["unfused_secs_per_step"] * 1e6, 3)
+    return e
+
+
+def run_reference(args, w, ws, rank):
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    budget = 90.0
+    K, Wm = args.steps, args.warmup
+    # W untimed warm-up steps, then exactly K timed steps, each on a row sample
+    # sized so that the whole run stays within the budget
+    secs, nbytes, sample, threads, rows, reps = cpu_oracle_run(w, budget / (1 + Wm / max(K, 1)),
+                                                               steps=K, warmup=Wm)
+    value = nbytes / secs / 1e9
+    out = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
+        "steps": K, "warmup": Wm, "ms_per_step": round(secs * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; see sm_rmsnorm_matmul_gb300/inputs.py)",
+        "config": {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "eps": w.eps,
+                   "seed": w.seed, "reference": "fp64 CPU oracle (oracle/rmm_oracle.c); "
+                   "the pages ship no implementation"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main() or 0)
