@@ -199,7 +199,8 @@ struct ColsPlan {
 };
 
 // Split K so that (column tiles x splits) fills the SMs: minimise the number
-// of k-blocks the busiest CTA streams, plus a fixed cost per unit of work.
+// of k-blocks the busiest CTA streams, plus a fixed cost per unit of work and
+// per split.
 ColsPlan plan_cols(int64_t M, int64_t K, int64_t N, const DeviceInfo& d) {
     ColsPlan p{};
     p.MP = static_cast<int>(((M + 15) / 16) * 16);
@@ -213,7 +214,9 @@ ColsPlan plan_cols(int64_t M, int64_t K, int64_t N, const DeviceInfo& d) {
         if (real != s) continue;
         const long units = static_cast<long>(p.n_tiles) * s;
         const long waves = (units + G - 1) / G;
-        const double cost = static_cast<double>(waves) * (kbps + 2.0) + (s > 1 ? 1.0 : 0.0);
+        // 2 k-blocks of fixed cost per unit (pipeline fill, epilogue), half a
+        // k-block per extra split for the reduction tail
+        const double cost = static_cast<double>(waves) * (kbps + 2.0) + 0.5 * (s - 1);
         if (cost < best - 1e-9) {
             best = cost;
             p.splits = s;

@@ -199,31 +199,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= 4 && warp < 8) {
         // ------------------------------------------------ transform: X*g, sum of squares
         if (kFused) {
-            const int row = threadIdx.x - 128;   // one row of the X tile per thread
-            const uint32_t swz = row & 7;        // 128-byte swizzle: chunk c sits at c ^ (row & 7)
+            // 8 consecutive threads cover the 8 16-byte chunks of one 128-byte
+            // row, so each warp access touches 4 whole rows (no bank conflicts).
+            const int t = threadIdx.x - 128;
+            const int kc = t & 7;           // chunk of the row
+            const int rb = t >> 3;          // rows rb + 16 i, i = 0..7
+            const uint32_t swz_off = static_cast<uint32_t>((kc ^ (rb & 7)) << 4);
             uint32_t it = 0, tl = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++tl) {
+            for (int t_ = blockIdx.x; ok && t_ < num_tiles; t_ += gridDim.x, ++tl) {
                 const uint32_t buf = tl & 1, use = tl >> 1;
                 // sr[buf] is free once the epilogue released this accumulator
                 if (!warp_wait(accempty(buf), (use & 1) ^ 1, abort)) break;
-                float ss = 0.f;
+                float ss[kRowsBM / 16];
+#pragma unroll
+                for (int i = 0; i < kRowsBM / 16; ++i) ss[i] = 0.f;
                 for (int kb = 0; kb < k_blocks; ++kb) {
                     const uint32_t s = it % kRowsStages, ph = (it / kRowsStages) & 1;
                     if (!warp_wait(full(s), ph, abort)) { ok = false; break; }
-                    const uint32_t xrow = sx + s * kRowsXBytes + row * 128;
-                    const uint32_t ga = sg + s * kGBytes;
+                    const uint4 gv = lds128(sg + s * kGBytes + kc * 16);
+                    const uint32_t xt = sx + s * kRowsXBytes + swz_off;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint32_t a = xrow + ((c ^ swz) << 4);
-                        sts128(a, gain8(lds128(a), lds128(ga + c * 16), ss));
+                    for (int i = 0; i < kRowsBM / 16; ++i) {
+                        // row rb + 16 i has the same (row & 7) as rb
+                        const uint32_t a = xt + (rb + 16 * i) * 128;
+                        sts128(a, gain8(lds128(a), gv, ss[i]));
                     }
                     fence_proxy_async_smem();
                     mbar_arrive(xform(s));
                     ++it;
                 }
                 if (!ok) break;
-                sr[buf * kRowsBM + row] = rsqrtf(ss / static_cast<float>(K) + eps);
+#pragma unroll
+                for (int i = 0; i < kRowsBM / 16; ++i) {
+                    float v = ss[i];
+                    v += __shfl_xor_sync(0xffffffffu, v, 1);
+                    v += __shfl_xor_sync(0xffffffffu, v, 2);
+                    v += __shfl_xor_sync(0xffffffffu, v, 4);
+                    if (kc == 0) sr[buf * kRowsBM + rb + 16 * i] = rsqrtf(v / static_cast<float>(K) + eps);
+                }
                 mbar_arrive(srfull(buf));
             }
         }
@@ -513,6 +527,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 mbar_arrive(accempty(buf));
             } else {
+                // publish this split's partial sums, then the last CTA to finish
+                // the column tile adds all splits in split order (its own from
+                // tensor memory, which it still holds) and writes Y.
                 float* part = a.ws_acc + static_cast<size_t>(sp) * a.M * a.N;
                 for (int j = 0; j < jmax; ++j) {
                     uint32_t v[16];
@@ -527,35 +544,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (kFused && e < a.M)
                     a.ws_ss[(static_cast<size_t>(nt) * a.splits + sp) * kColsMaxMP + e] =
                         ss_s[buf * kColsMaxMP + e];
-                tc_fence_before();
-                mbar_arrive(accempty(buf));
-                // the last CTA to finish this column tile sums the partials in split order
                 __threadfence();
-                if (!epi_sync()) break;
-                if (e == 0) *last_flag = (atomicAdd(&a.counters[nt], 1) == a.splits - 1);
-                if (!epi_sync()) break;
-                if (*last_flag) {
+                bool go = epi_sync();
+                if (go && e == 0) *last_flag = (atomicAdd(&a.counters[nt], 1) == a.splits - 1);
+                go = go && epi_sync();
+                if (go && *last_flag) {
                     __threadfence();
                     if (kFused && e < a.M) {
                         float tot = 0.f;
+#pragma unroll 4
                         for (int s2 = 0; s2 < a.splits; ++s2)
                             tot += __ldcg(&a.ws_ss[(static_cast<size_t>(nt) * a.splits + s2) *
                                                        kColsMaxMP + e]);
                         r_red[e] = rsqrtf(tot / static_cast<float>(a.K) + a.eps);
                     }
-                    if (!epi_sync()) break;
-                    if (n_ok) {
-                        for (int m = 0; m < a.M; ++m) {
-                            float acc = 0.f;
-                            for (int s2 = 0; s2 < a.splits; ++s2)
-                                acc += __ldcg(&a.ws_acc[(static_cast<size_t>(s2) * a.M + m) * a.N + n]);
-                            const float r = kFused ? r_red[m] : 1.f;
-                            Y[static_cast<size_t>(m) * a.N + n] = __float2bfloat16_rn(acc * r);
+                    go = epi_sync();
+                    for (int j = 0; go && j < jmax; ++j) {
+                        uint32_t v[16];
+                        tmem_ld_32x16(taddr + j * 16, v);
+                        float acc[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+                        if (n_ok) {
+#pragma unroll 2
+                            for (int s2 = 0; s2 < a.splits; ++s2) {
+                                const float* p2 = a.ws_acc + static_cast<size_t>(s2) * a.M * a.N + n;
+                                float pv[16];
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) {
+                                    const int m = j * 16 + i;
+                                    pv[i] = (s2 == sp) ? __uint_as_float(v[i])
+                                            : (m < a.M ? __ldcg(p2 + static_cast<size_t>(m) * a.N) : 0.f);
+                                }
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) acc[i] += pv[i];
+                            }
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const int m = j * 16 + i;
+                                if (m < a.M) {
+                                    const float r = kFused ? r_red[m] : 1.f;
+                                    Y[static_cast<size_t>(m) * a.N + n] = __float2bfloat16_rn(acc[i] * r);
+                                }
+                            }
                         }
                     }
                     if (e == 0) a.counters[nt] = 0;
                 }
-                if (!epi_sync()) break;
+                tc_fence_before();
+                mbar_arrive(accempty(buf));
+                if (!go || !epi_sync()) break;
             }
         }
     }
