@@ -57,7 +57,8 @@ typedef enum {
     RMM_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not compute capability 10.3 */
     RMM_ERR_LAUNCH = 4,             /* a CUDA launch or API call failed */
     RMM_ERR_DEVICE_TIMEOUT = 5,     /* a bounded in-kernel wait ran out (rmm_device_status) */
-    RMM_ERR_INTERNAL = 6            /* workspace allocation or tensor-map encoding failed */
+    RMM_ERR_INTERNAL = 6,           /* workspace allocation or tensor-map encoding failed */
+    RMM_ERR_SCRATCH_LIMIT = 7       /* rmsnorm_matmul_noalloc: problem needs more than its fixed scratch */
 } rmm_status;
 
 /*
@@ -114,6 +115,33 @@ int rmm_device_status(cudaStream_t stream);
 
 /* Static, NUL-terminated name of a status code ("RMM_OK", ...). */
 const char* rmm_status_string(int code);
+
+/*
+ * rmsnorm_matmul_noalloc -- the same computation, arguments and results as
+ * rmsnorm_matmul(), for callers that cannot let a library allocate device
+ * memory: code being captured into a CUDA graph (where cudaMalloc is
+ * refused), runtimes and plugin hosts that own all device memory and forbid
+ * allocation inside their enqueue call, and processes with a fixed memory
+ * budget.  It calls no cudaMalloc, cudaFree or allocating library routine.
+ * The paper has no counterpart to this entry point.
+ *
+ * Scratch: where the small-M path splits K, its fp32 partial sums live in one
+ * fixed 16 MiB device array inside this library (a file-scope __device__
+ * array), held on every device where the library's device code is loaded
+ * until the process exits.  Limit: splits x M x N x 4 bytes must fit in
+ * 15 MiB (for example M = 64, N = 28672 with two K splits uses 14 MiB);
+ * larger problems return RMM_ERR_SCRATCH_LIMIT.  The row-tile path (M > 64)
+ * and unsplit small-M launches use no scratch.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call shares the one array, which keeps the previous call's
+ * contents; each call clears its arrival counters on `stream` before its
+ * kernel.  Calls whose kernels overlap on the GPU (for example on two streams
+ * at once) race on the array: order them on one stream or with events.
+ */
+int rmsnorm_matmul_noalloc(const void* X, const void* g, const void* W, void* Y,
+                           int64_t M, int64_t K, int64_t N, float eps, cudaStream_t stream);
 
 /* Which path the dispatcher would take for this shape right now:
  * 1 = row-tile path, 2 = small-M path.  Host-only; no CUDA call. */

@@ -22,7 +22,7 @@ import threading
 from .build import LIB_PATH
 
 __all__ = [
-    "RmmError", "lib", "rmsnorm_matmul", "rmsnorm", "matmul", "force_path",
+    "RmmError", "lib", "rmsnorm_matmul", "rmsnorm_matmul_noalloc", "rmsnorm", "matmul", "force_path",
     "dispatch_path", "device_status", "status_string", "STATUS", "PATH_AUTO",
     "PATH_ROWS", "PATH_COLS", "ABI_FUNCTIONS",
 ]
@@ -30,13 +30,14 @@ __all__ = [
 STATUS = {
     0: "RMM_OK", 1: "RMM_ERR_INVALID_ARG", 2: "RMM_ERR_ALIGNMENT",
     3: "RMM_ERR_UNSUPPORTED_DEVICE", 4: "RMM_ERR_LAUNCH",
-    5: "RMM_ERR_DEVICE_TIMEOUT", 6: "RMM_ERR_INTERNAL",
+    5: "RMM_ERR_DEVICE_TIMEOUT", 6: "RMM_ERR_INTERNAL", 7: "RMM_ERR_SCRATCH_LIMIT",
 }
 PATH_AUTO, PATH_ROWS, PATH_COLS = 0, 1, 2
 
 # Every function declared in include/rmsnorm_matmul.h.
 ABI_FUNCTIONS = ("rmsnorm_matmul", "rmsnorm", "matmul", "rmm_force_path",
-                 "rmm_device_status", "rmm_status_string", "rmm_dispatch_path")
+                 "rmm_device_status", "rmm_status_string", "rmm_dispatch_path",
+                 "rmsnorm_matmul_noalloc")
 
 
 class RmmError(RuntimeError):
@@ -52,6 +53,7 @@ _lib = None
 def _bind(l: ctypes.CDLL) -> ctypes.CDLL:
     vp, i64, f32, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
     l.rmsnorm_matmul.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, vp]
+    l.rmsnorm_matmul_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, vp]
     l.rmsnorm.argtypes = [vp, vp, vp, i64, i64, f32, vp]
     l.matmul.argtypes = [vp, vp, vp, i64, i64, i64, vp]
     l.rmm_force_path.argtypes = [i32]
@@ -59,7 +61,7 @@ def _bind(l: ctypes.CDLL) -> ctypes.CDLL:
     l.rmm_status_string.argtypes = [i32]
     l.rmm_status_string.restype = ctypes.c_char_p
     l.rmm_dispatch_path.argtypes = [i64, i64, i64]
-    for name in ("rmsnorm_matmul", "rmsnorm", "matmul", "rmm_force_path",
+    for name in ("rmsnorm_matmul", "rmsnorm_matmul_noalloc", "rmsnorm", "matmul", "rmm_force_path",
                  "rmm_device_status", "rmm_dispatch_path"):
         getattr(l, name).restype = i32
     return l
@@ -122,6 +124,30 @@ def rmsnorm_matmul(X, g, W, eps: float = 1e-6, out=None, stream=None):
             raise ValueError(f"out must have shape {(M, N)}")
     _raise(lib().rmsnorm_matmul(X.data_ptr(), g.data_ptr(), W.data_ptr(), out.data_ptr(),
                                 M, K, N, float(eps), _stream_ptr(stream)), "rmsnorm_matmul")
+    return out
+
+
+def rmsnorm_matmul_noalloc(X, g, W, eps: float = 1e-6, out=None, stream=None):
+    """rmsnorm_matmul() for callers that cannot let the library allocate device
+    memory (graph capture, runtimes that own all device memory, fixed budgets).
+
+    The library allocates nothing: split-K partial sums use a fixed 16 MiB
+    array inside the library.  `out` must be given, since allocating it here
+    would defeat the purpose.  Calls that overlap on the GPU share that array
+    and race; problems needing more than 15 MiB of partials raise
+    RmmError(RMM_ERR_SCRATCH_LIMIT).
+    """
+    _check_bf16("X", X, 2)
+    _check_bf16("g", g, 1)
+    _check_bf16("W", W, 2)
+    _check_bf16("out", out, 2)
+    M, K = X.shape
+    N = W.shape[1]
+    if g.shape[0] != K or W.shape[0] != K or tuple(out.shape) != (M, N):
+        raise ValueError("shape mismatch")
+    _raise(lib().rmsnorm_matmul_noalloc(X.data_ptr(), g.data_ptr(), W.data_ptr(), out.data_ptr(),
+                                        M, K, N, float(eps), _stream_ptr(stream)),
+           "rmsnorm_matmul_noalloc")
     return out
 
 

@@ -375,8 +375,111 @@ const char* rmm_status_string(int code) {
         case RMM_ERR_LAUNCH: return "RMM_ERR_LAUNCH";
         case RMM_ERR_DEVICE_TIMEOUT: return "RMM_ERR_DEVICE_TIMEOUT";
         case RMM_ERR_INTERNAL: return "RMM_ERR_INTERNAL";
+        case RMM_ERR_SCRATCH_LIMIT: return "RMM_ERR_SCRATCH_LIMIT";
         default: return "RMM_UNKNOWN_STATUS";
     }
 }
 
 }  // extern "C"
+
+// ============================================================================
+// Allocation-free variant of rmsnorm_matmul().
+//
+// Some callers cannot let a library allocate device memory: code that is being
+// captured into a CUDA graph (cudaMalloc is not a stream operation and is
+// refused there), inference runtimes and plugin hosts that own every byte of
+// device memory and forbid allocation inside their enqueue call, and
+// processes with a fixed memory budget set at start-up.  For them,
+// rmsnorm_matmul_noalloc() runs the same kernels; where the small-M path
+// splits K, its fp32 partial sums, partial row sums of squares and arrival
+// counters live in the fixed array below instead of a workspace allocated on
+// first use.
+// ============================================================================
+namespace {
+
+constexpr size_t kScratchBytes = size_t(16) << 20;           // 16 MiB in total
+constexpr size_t kScratchCounterBytes = size_t(64) << 10;    // up to 16384 column tiles
+constexpr size_t kScratchSsBytes = size_t(960) << 10;        // partial sums of squares
+constexpr size_t kScratchAccBytes = kScratchBytes - kScratchCounterBytes - kScratchSsBytes;
+
+// Held on every device where this module is loaded, until the process exits.
+static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
+
+std::mutex g_scratch_mu;
+std::map<int, unsigned char*> g_scratch_addr;
+
+// Device address of g_scratch on `dev`, which must be the current device.
+// Looked up once per device (the first call may load this library's device
+// code on that device).
+int scratch_address(int dev, unsigned char** out) {
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    auto it = g_scratch_addr.find(dev);
+    if (it != g_scratch_addr.end()) {
+        *out = it->second;
+        return RMM_OK;
+    }
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || p == nullptr) return RMM_ERR_LAUNCH;
+    g_scratch_addr[dev] = static_cast<unsigned char*>(p);
+    *out = static_cast<unsigned char*>(p);
+    return RMM_OK;
+}
+
+}  // namespace
+
+extern "C" int rmsnorm_matmul_noalloc(const void* X, const void* g, const void* W, void* Y,
+                                      int64_t M, int64_t K, int64_t N, float eps,
+                                      cudaStream_t stream) {
+    int rc = check_sizes(M, K, N, eps, true);
+    if (rc == kNoop) return RMM_OK;
+    if (rc != RMM_OK) return rc;
+    rc = check_ptrs(Y, static_cast<size_t>(M) * N * 2,
+                    {{X, static_cast<size_t>(M) * K * 2}, {g, static_cast<size_t>(K) * 2},
+                     {W, static_cast<size_t>(K) * N * 2}});
+    if (rc != RMM_OK) return rc;
+    int dev = 0;
+    DeviceInfo d;
+    rc = current_device(&dev, &d);
+    if (rc != RMM_OK) return rc;
+    // The row-tile path and an unsplit small-M launch use no scratch at all.
+    if (choose_path(M) == kPathRows) return run_contraction(true, X, g, W, Y, M, K, N, eps, stream);
+    if (M > rmm::kColsMaxMP) return RMM_ERR_INVALID_ARG;
+    const ColsPlan p = plan_cols(M, K, N, d);
+    if (p.splits == 1) return run_contraction(true, X, g, W, Y, M, K, N, eps, stream);
+
+    const size_t acc_bytes = static_cast<size_t>(p.splits) * M * N * sizeof(float);
+    const size_t ss_bytes = static_cast<size_t>(p.n_tiles) * p.splits * rmm::kColsMaxMP * sizeof(float);
+    const size_t cnt_bytes = static_cast<size_t>(p.n_tiles) * sizeof(int);
+    if (acc_bytes > kScratchAccBytes || ss_bytes > kScratchSsBytes || cnt_bytes > kScratchCounterBytes)
+        return RMM_ERR_SCRATCH_LIMIT;
+    unsigned char* base = nullptr;
+    rc = scratch_address(dev, &base);
+    if (rc != RMM_OK) return rc;
+    int* counters = reinterpret_cast<int*>(base);
+    float* ss = reinterpret_cast<float*>(base + kScratchCounterBytes);
+    float* acc = reinterpret_cast<float*>(base + kScratchCounterBytes + kScratchSsBytes);
+    // The array keeps the previous call's contents; the counters must start at 0.
+    if (cudaMemsetAsync(counters, 0, cnt_bytes, stream) != cudaSuccess) return RMM_ERR_LAUNCH;
+
+    CUtensorMap tmX, tmW, tmG;
+    if (!map_2d(&tmW, W, K, N, kBK) || !map_1d(&tmG, g, K) || !map_2d(&tmX, X, M, K, p.MP))
+        return RMM_ERR_INTERNAL;
+    rmm::ColsLaunch a{};
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.eps = eps;
+    a.MP = p.MP;
+    a.n_tiles = p.n_tiles;
+    a.k_blocks = p.k_blocks;
+    a.splits = p.splits;
+    a.kb_per_split = p.kb_per_split;
+    a.stages = p.stages;
+    a.grid = p.grid;
+    a.tmem_cols = p.tmem_cols;
+    a.ws_acc = acc;
+    a.ws_ss = ss;
+    a.counters = counters;
+    return rmm::launch_cols(true, tmX, tmW, tmG, Y, a, stream) == cudaSuccess ? RMM_OK
+                                                                            : RMM_ERR_LAUNCH;
+}
