@@ -143,6 +143,16 @@ const char* rmm_status_string(int code);
 int rmsnorm_matmul_noalloc(const void* X, const void* g, const void* W, void* Y,
                            int64_t M, int64_t K, int64_t N, float eps, cudaStream_t stream);
 
+/*
+ * Launch plan the library would use for this shape on the current device
+ * (introspection for tests and benchmarks; `fused` = 1 for rmsnorm_matmul,
+ * 0 for matmul).  Fills info[0..7] with: path (1 row-tile, 2 small-M),
+ * K splits, 1 if the splits reduce through a cluster's shared memory, grid
+ * size, pipeline stages, padded rows MP, column tiles, k-blocks per split.
+ * Queries device attributes; launches nothing.
+ */
+int rmm_describe_plan(int64_t M, int64_t K, int64_t N, int fused, int* info);
+
 /* Which path the dispatcher would take for this shape right now:
  * 1 = row-tile path, 2 = small-M path.  Host-only; no CUDA call. */
 int rmm_dispatch_path(int64_t M, int64_t K, int64_t N);

@@ -23,7 +23,7 @@ from .build import LIB_PATH
 
 __all__ = [
     "RmmError", "lib", "rmsnorm_matmul", "rmsnorm_matmul_noalloc", "rmsnorm", "matmul", "force_path",
-    "dispatch_path", "device_status", "status_string", "STATUS", "PATH_AUTO",
+    "dispatch_path", "describe_plan", "device_status", "status_string", "STATUS", "PATH_AUTO",
     "PATH_ROWS", "PATH_COLS", "ABI_FUNCTIONS",
 ]
 
@@ -37,7 +37,7 @@ PATH_AUTO, PATH_ROWS, PATH_COLS = 0, 1, 2
 # Every function declared in include/rmsnorm_matmul.h.
 ABI_FUNCTIONS = ("rmsnorm_matmul", "rmsnorm", "matmul", "rmm_force_path",
                  "rmm_device_status", "rmm_status_string", "rmm_dispatch_path",
-                 "rmsnorm_matmul_noalloc")
+                 "rmsnorm_matmul_noalloc", "rmm_describe_plan")
 
 
 class RmmError(RuntimeError):
@@ -61,8 +61,9 @@ def _bind(l: ctypes.CDLL) -> ctypes.CDLL:
     l.rmm_status_string.argtypes = [i32]
     l.rmm_status_string.restype = ctypes.c_char_p
     l.rmm_dispatch_path.argtypes = [i64, i64, i64]
+    l.rmm_describe_plan.argtypes = [i64, i64, i64, i32, ctypes.POINTER(ctypes.c_int)]
     for name in ("rmsnorm_matmul", "rmsnorm_matmul_noalloc", "rmsnorm", "matmul", "rmm_force_path",
-                 "rmm_device_status", "rmm_dispatch_path"):
+                 "rmm_device_status", "rmm_dispatch_path", "rmm_describe_plan"):
         getattr(l, name).restype = i32
     return l
 
@@ -196,6 +197,16 @@ def force_path(path: int) -> int:
     if prev < 0:
         raise ValueError(f"unknown path {path}")
     return prev
+
+
+PLAN_FIELDS = ("path", "splits", "cluster", "grid", "stages", "MP", "tiles", "kb_per_split")
+
+
+def describe_plan(M: int, K: int, N: int, fused: bool = True) -> dict:
+    """The launch plan for this shape on the current device (no launch)."""
+    info = (ctypes.c_int * 8)()
+    _raise(lib().rmm_describe_plan(M, K, N, int(fused), info), "rmm_describe_plan")
+    return dict(zip(PLAN_FIELDS, list(info)))
 
 
 def dispatch_path(M: int, K: int, N: int) -> int:

@@ -10,6 +10,7 @@
 #include <cstdint>
 #include <cstring>
 #include <map>
+#include <tuple>
 #include <mutex>
 #include <utility>
 
@@ -24,8 +25,6 @@ std::atomic<int> g_force_path{0};
 
 constexpr int kPathRows = 1;
 constexpr int kPathCols = 2;
-// The dispatcher sends M <= kColsMaxRowsAuto to the small-M path.
-constexpr int64_t kColsMaxRowsAuto = 64;
 
 // ------------------------------------------------------------------ device
 struct DeviceInfo {
@@ -194,52 +193,183 @@ int get_workspace(int dev, cudaStream_t s, size_t acc_bytes, size_t ss_bytes, si
 
 // ---------------------------------------------------------------- planning
 struct ColsPlan {
-    int MP, n_tiles, k_blocks, splits, kb_per_split, stages, grid;
+    int MP, n_tiles, k_blocks, splits, kb_per_split, stages, grid, cluster;
     uint32_t tmem_cols;
 };
 
-// Split K so that (column tiles x splits) fills the SMs: minimise the number
-// of k-blocks the busiest CTA streams, plus a fixed cost per unit of work and
-// per split.
-ColsPlan plan_cols(int64_t M, int64_t K, int64_t N, const DeviceInfo& d) {
+std::mutex g_occ_mu;
+std::map<std::tuple<int, bool, int, size_t>, int> g_occ;
+
+// Clusters of `splits` CTAs that can be resident at once, cached per device.
+int max_clusters(int dev, bool fused, int splits, size_t smem) {
+    std::lock_guard<std::mutex> lk(g_occ_mu);
+    auto key = std::make_tuple(dev, fused, splits, smem);
+    auto it = g_occ.find(key);
+    if (it != g_occ.end()) return it->second;
+    const int n = rmm::cols_max_active_clusters(fused, splits, smem);
+    g_occ[key] = n;
+    return n;
+}
+
+int cols_stages(int MP, int red_slots, const DeviceInfo& d) {
+    const size_t fixed = rmm::cols_fixed_smem_bytes(MP, red_slots);
+    const size_t per = rmm::cols_stage_bytes(MP);
+    const size_t avail = d.smem_optin > 0 ? static_cast<size_t>(d.smem_optin) : 227 * 1024;
+    const int st = avail > fixed ? static_cast<int>((avail - fixed) / per) : 0;
+    return std::min(rmm::kColsMaxStages, st);
+}
+
+// Model of one launch of the small-M path, in microseconds (fitted to
+// measurements on GB300): each CTA keeps `stages` W tiles in flight with about
+// 3.2 us from issue to release, the whole GPU streams W at about 5.8 TB/s, a
+// unit of work costs about 1 us of pipeline fill and epilogue, and the last
+// unit's K-split reduction adds about 0.5 us (no split), 1.5 us (cluster) or
+// 3.5 us (global workspace, a few L2 round trips).
+double cols_cost_us(int64_t N, int64_t K, int n_tiles, int splits, int kbps, int resident, int stages,
+                    int mode) {
+    const long units = static_cast<long>(n_tiles) * splits;
+    const long waves = (units + resident - 1) / resident;
+    const double cta_rate = stages * 16384.0 / 3.2e-6;                   // bytes/s per CTA
+    const double per_cta = static_cast<double>(waves) * kbps * 16384.0 / cta_rate;
+    const double total = static_cast<double>(K) * N * 2 / 5.8e12;
+    const double tail = mode == 0 ? 0.5 : (mode == 1 ? 1.5 : 3.5);
+    return std::max(per_cta, total) * 1e6 + waves * 1.0 + tail;
+}
+
+// Choose the K split of the small-M path and how the splits are combined:
+// mode 0 = no split, 1 = cluster (splits 1.. push partials into split 0's
+// shared memory), 2 = global workspace (last arriving warp reduces).
+ColsPlan plan_cols(int dev, bool fused, int64_t M, int64_t K, int64_t N, const DeviceInfo& d,
+                   bool allow_cluster) {
     ColsPlan p{};
     p.MP = static_cast<int>(((M + 15) / 16) * 16);
     p.n_tiles = static_cast<int>((N + rmm::kColsBN - 1) / rmm::kColsBN);
     p.k_blocks = static_cast<int>((K + kBK - 1) / kBK);
-    const int G = d.sm_count > 0 ? d.sm_count : 1;
+    const int sms = d.sm_count > 0 ? d.sm_count : 1;
     double best = 1e300;
     for (int s = 1; s <= rmm::kColsMaxSplits && s <= p.k_blocks; ++s) {
         const int kbps = (p.k_blocks + s - 1) / s;
         const int real = (p.k_blocks + kbps - 1) / kbps;
         if (real != s) continue;
-        const long units = static_cast<long>(p.n_tiles) * s;
-        const long waves = (units + G - 1) / G;
-        // 2 k-blocks of fixed cost per unit (pipeline fill, epilogue), half a
-        // k-block per extra split for the reduction tail
-        const double cost = static_cast<double>(waves) * (kbps + 2.0) + 0.5 * (s - 1);
-        if (cost < best - 1e-9) {
-            best = cost;
-            p.splits = s;
-            p.kb_per_split = kbps;
+        for (int mode = (s == 1 ? 0 : 1); mode <= (s == 1 ? 0 : 2); ++mode) {
+            const bool cl = mode == 1;
+            if (cl && (!allow_cluster || s > rmm::kClusterMaxSplits ||
+                       static_cast<size_t>(s - 1) * p.MP * rmm::kColsBN * 4 > 64 * 1024))
+                continue;
+            const int red_slots = cl ? s - 1 : 0;
+            const int st = cols_stages(p.MP, red_slots, d);
+            if (st < 2) continue;
+            int resident = sms;
+            if (cl) {
+                resident = max_clusters(dev, fused, s, rmm::cols_smem_bytes(p.MP, st, red_slots)) * s;
+                if (resident <= 0) continue;
+            }
+            const double cost = cols_cost_us(N, K, p.n_tiles, s, kbps, resident, st, mode);
+            if (cost < best - 1e-9) {
+                best = cost;
+                p.splits = s;
+                p.kb_per_split = kbps;
+                p.cluster = cl ? 1 : 0;
+                p.stages = st;
+                const long units = static_cast<long>(p.n_tiles) * s;
+                p.grid = static_cast<int>(std::min<long>(units, resident));
+            }
         }
     }
-    const long units = static_cast<long>(p.n_tiles) * p.splits;
-    p.grid = static_cast<int>(std::min<long>(units, G));
-    const size_t fixed = rmm::cols_fixed_smem_bytes();
-    const size_t per = rmm::cols_stage_bytes(p.MP);
-    const size_t avail = d.smem_optin > 0 ? static_cast<size_t>(d.smem_optin) : 227 * 1024;
-    int st = static_cast<int>((avail - fixed) / per);
-    p.stages = std::max(2, std::min(rmm::kColsMaxStages, st));
+    if (p.cluster) p.grid = (p.grid / p.splits) * p.splits;
     uint32_t cols = 32;
     while (cols < static_cast<uint32_t>(2 * p.MP)) cols <<= 1;
     p.tmem_cols = cols;
     return p;
 }
 
+struct RowsPlan {
+    int m_tiles, n_tiles, k_blocks, splits, kb_per_split, cluster, xrows, MP, stages, grid;
+};
+
+int rows_stages(int xrows, int red_slots, int MP, const DeviceInfo& d) {
+    const size_t fixed = rmm::rows_smem_bytes(xrows, 0, red_slots, MP);
+    const size_t per = rmm::rows_stage_bytes(xrows);
+    const size_t avail = d.smem_optin > 0 ? static_cast<size_t>(d.smem_optin) : 227 * 1024;
+    const int st = avail > fixed ? static_cast<int>((avail - fixed) / per) : 0;
+    return std::min(rmm::kRowsMaxStages, st);
+}
+
+std::mutex g_rows_occ_mu;
+std::map<std::tuple<int, bool, int, size_t>, int> g_rows_occ;
+
+int rows_max_clusters(int dev, bool fused, int splits, size_t smem) {
+    std::lock_guard<std::mutex> lk(g_rows_occ_mu);
+    auto key = std::make_tuple(dev, fused, splits, smem);
+    auto it = g_rows_occ.find(key);
+    if (it != g_rows_occ.end()) return it->second;
+    const int n = rmm::rows_max_active_clusters(fused, splits, smem);
+    g_rows_occ[key] = n;
+    return n;
+}
+
+// Row-tile path plan.  More than one row tile: no K split, 128-row X boxes.
+// One row tile (M <= 128, the W-streaming regime): X boxes of M rounded up to
+// 16 rows, and K split over 1..8 CTAs of a cluster chosen with a model of one
+// launch in microseconds (fitted to GB300 measurements): each CTA streams W at
+// about 55 GB/s, the GPU at about 6 TB/s, a unit costs about 1 us of fill and
+// drain, and the cluster reduction about 1.5 us.
+RowsPlan plan_rows(int dev, bool fused, int64_t M, int64_t K, int64_t N, const DeviceInfo& d) {
+    RowsPlan p{};
+    p.m_tiles = static_cast<int>((M + rmm::kRowsBM - 1) / rmm::kRowsBM);
+    p.n_tiles = static_cast<int>((N + rmm::kRowsBN - 1) / rmm::kRowsBN);
+    p.k_blocks = static_cast<int>((K + kBK - 1) / kBK);
+    p.MP = static_cast<int>(std::min<int64_t>(rmm::kRowsBM, ((M + 15) / 16) * 16));
+    const int sms = d.sm_count > 0 ? d.sm_count : 1;
+    p.splits = 1;
+    p.kb_per_split = p.k_blocks;
+    p.cluster = 0;
+    if (p.m_tiles > 1) {
+        p.xrows = rmm::kRowsBM;
+        p.stages = rows_stages(p.xrows, 0, p.MP, d);
+        p.grid = static_cast<int>(std::min<long>(static_cast<long>(p.m_tiles) * p.n_tiles, sms));
+        return p;
+    }
+    p.xrows = p.MP;
+    double best = 1e300;
+    const double w_total = static_cast<double>(K) * N * 2;
+    for (int s = 1; s <= rmm::kClusterMaxSplits && s <= p.k_blocks; ++s) {
+        const int kbps = (p.k_blocks + s - 1) / s;
+        if ((p.k_blocks + kbps - 1) / kbps != s) continue;
+        const int red_slots = s > 1 ? s : 0;
+        const int st = rows_stages(p.xrows, red_slots, p.MP, d);
+        if (st < 2) continue;
+        int resident = sms;
+        if (s > 1) {
+            resident = rows_max_clusters(dev, fused, s, rmm::rows_smem_bytes(p.xrows, st, red_slots, p.MP)) * s;
+            if (resident <= 0) continue;
+        }
+        const long units = static_cast<long>(p.n_tiles) * s;
+        const long waves = (units + resident - 1) / resident;
+        const double per_cta = static_cast<double>(waves) * kbps * rmm::kRowsBN * kBK * 2 / 55e9;
+        const double cost = std::max(per_cta, w_total / 6.0e12) * 1e6 + waves * 1.0 + (s > 1 ? 1.5 : 0.5);
+        if (cost < best - 1e-9) {
+            best = cost;
+            p.splits = s;
+            p.kb_per_split = kbps;
+            p.cluster = s > 1 ? 1 : 0;
+            p.stages = st;
+            p.grid = static_cast<int>(std::min<long>(units, resident));
+        }
+    }
+    if (p.cluster) p.grid = (p.grid / p.splits) * p.splits;
+    return p;
+}
+
+// The row-tile path serves every shape by default: for M <= 128 it streams W
+// with wide tiles and a cluster K split, which measured faster on GB300 than
+// the operand-swapped small-M path.  The small-M path stays available through
+// rmm_force_path(2) and backs rmsnorm_matmul_noalloc's split-K variant.
 int choose_path(int64_t M) {
+    (void)M;
     const int f = g_force_path.load();
     if (f == kPathRows || f == kPathCols) return f;
-    return M <= kColsMaxRowsAuto ? kPathCols : kPathRows;
+    return kPathRows;
 }
 
 // One launch of the tensor-core contraction, fused (RMSNorm folded in) or not.
@@ -257,7 +387,7 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
     }
     if (path == kPathCols) {
         if (M > rmm::kColsMaxMP) return RMM_ERR_INVALID_ARG;
-        const ColsPlan p = plan_cols(M, K, N, d);
+        const ColsPlan p = plan_cols(dev, fused, M, K, N, d, true);
         if (!map_2d(&tmX, X, M, K, p.MP)) return RMM_ERR_INTERNAL;
         if (!fused) tmG = tmX;  // unused by the kernel
         rmm::ColsLaunch a{};
@@ -272,12 +402,13 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
         a.kb_per_split = p.kb_per_split;
         a.stages = p.stages;
         a.grid = p.grid;
+        a.cluster = p.cluster;
         a.tmem_cols = p.tmem_cols;
-        if (p.splits > 1) {
+        if (p.splits > 1 && !p.cluster) {
             Workspace w;
             rc = get_workspace(dev, stream, static_cast<size_t>(p.splits) * M * N * sizeof(float),
                                static_cast<size_t>(p.n_tiles) * p.splits * rmm::kColsMaxMP * sizeof(float),
-                               static_cast<size_t>(p.n_tiles), &w);
+                               static_cast<size_t>(p.n_tiles) * 4, &w);
             if (rc != RMM_OK) return rc;
             a.ws_acc = w.acc;
             a.ws_ss = w.ss;
@@ -286,18 +417,24 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
         return rmm::launch_cols(fused, tmX, tmW, tmG, Y, a, stream) == cudaSuccess ? RMM_OK
                                                                                   : RMM_ERR_LAUNCH;
     }
-    if (!map_2d(&tmX, X, M, K, rmm::kRowsBM)) return RMM_ERR_INTERNAL;
+    const RowsPlan p = plan_rows(dev, fused, M, K, N, d);
+    if (!map_2d(&tmX, X, M, K, p.xrows)) return RMM_ERR_INTERNAL;
     if (!fused) tmG = tmX;
     rmm::RowsLaunch a{};
     a.M = static_cast<int>(M);
     a.N = static_cast<int>(N);
     a.K = static_cast<int>(K);
     a.eps = eps;
-    a.m_tiles = static_cast<int>((M + rmm::kRowsBM - 1) / rmm::kRowsBM);
-    a.n_tiles = static_cast<int>((N + rmm::kRowsBN - 1) / rmm::kRowsBN);
-    a.k_blocks = static_cast<int>((K + kBK - 1) / kBK);
-    const long tiles = static_cast<long>(a.m_tiles) * a.n_tiles;
-    a.grid = static_cast<int>(std::min<long>(tiles, d.sm_count));
+    a.m_tiles = p.m_tiles;
+    a.n_tiles = p.n_tiles;
+    a.k_blocks = p.k_blocks;
+    a.splits = p.splits;
+    a.kb_per_split = p.kb_per_split;
+    a.cluster = p.cluster;
+    a.xrows = p.xrows;
+    a.MP = p.MP;
+    a.stages = p.stages;
+    a.grid = p.grid;
     return rmm::launch_rows(fused, tmX, tmW, tmG, Y, a, stream) == cudaSuccess ? RMM_OK
                                                                               : RMM_ERR_LAUNCH;
 }
@@ -353,6 +490,37 @@ int rmm_force_path(int path) {
     return g_force_path.exchange(path);
 }
 
+int rmm_describe_plan(int64_t M, int64_t K, int64_t N, int fused, int* info) {
+    if (!info || M < 1 || K < 1 || N < 1) return RMM_ERR_INVALID_ARG;
+    int dev = 0;
+    DeviceInfo d;
+    int rc = current_device(&dev, &d);
+    if (rc != RMM_OK) return rc;
+    for (int i = 0; i < 8; ++i) info[i] = 0;
+    info[0] = choose_path(M);
+    if (info[0] == kPathCols) {
+        if (M > rmm::kColsMaxMP) return RMM_ERR_INVALID_ARG;
+        const ColsPlan p = plan_cols(dev, fused != 0, M, K, N, d, true);
+        info[1] = p.splits;
+        info[2] = p.cluster;
+        info[3] = p.grid;
+        info[4] = p.stages;
+        info[5] = p.MP;
+        info[6] = p.n_tiles;
+        info[7] = p.kb_per_split;
+    } else {
+        const RowsPlan p = plan_rows(dev, fused != 0, M, K, N, d);
+        info[1] = p.splits;
+        info[2] = p.cluster;
+        info[3] = p.grid;
+        info[4] = p.stages;
+        info[5] = p.xrows;
+        info[6] = p.m_tiles * p.n_tiles;
+        info[7] = p.kb_per_split;
+    }
+    return RMM_OK;
+}
+
 int rmm_dispatch_path(int64_t M, int64_t K, int64_t N) {
     (void)K;
     (void)N;
@@ -398,7 +566,7 @@ const char* rmm_status_string(int code) {
 namespace {
 
 constexpr size_t kScratchBytes = size_t(16) << 20;           // 16 MiB in total
-constexpr size_t kScratchCounterBytes = size_t(64) << 10;    // up to 16384 column tiles
+constexpr size_t kScratchCounterBytes = size_t(64) << 10;    // 4 counters per column tile
 constexpr size_t kScratchSsBytes = size_t(960) << 10;        // partial sums of squares
 constexpr size_t kScratchAccBytes = kScratchBytes - kScratchCounterBytes - kScratchSsBytes;
 
@@ -444,12 +612,12 @@ extern "C" int rmsnorm_matmul_noalloc(const void* X, const void* g, const void* 
     // The row-tile path and an unsplit small-M launch use no scratch at all.
     if (choose_path(M) == kPathRows) return run_contraction(true, X, g, W, Y, M, K, N, eps, stream);
     if (M > rmm::kColsMaxMP) return RMM_ERR_INVALID_ARG;
-    const ColsPlan p = plan_cols(M, K, N, d);
+    const ColsPlan p = plan_cols(dev, true, M, K, N, d, false);
     if (p.splits == 1) return run_contraction(true, X, g, W, Y, M, K, N, eps, stream);
 
     const size_t acc_bytes = static_cast<size_t>(p.splits) * M * N * sizeof(float);
     const size_t ss_bytes = static_cast<size_t>(p.n_tiles) * p.splits * rmm::kColsMaxMP * sizeof(float);
-    const size_t cnt_bytes = static_cast<size_t>(p.n_tiles) * sizeof(int);
+    const size_t cnt_bytes = static_cast<size_t>(p.n_tiles) * 4 * sizeof(int);
     if (acc_bytes > kScratchAccBytes || ss_bytes > kScratchSsBytes || cnt_bytes > kScratchCounterBytes)
         return RMM_ERR_SCRATCH_LIMIT;
     unsigned char* base = nullptr;

@@ -35,19 +35,21 @@ constexpr uint32_t kGBytes = kBK * 2;            // one g slice per stage: 128 B
 constexpr uint32_t kWBoxBytes = 64 * kBK * 2;    // one [64 k][64 n] W box: 8 KB
 
 // ------------------------------------------------------------ row-tile path
-constexpr int kRowsStages = 4;
-constexpr uint32_t kRowsXBytes = kRowsBM * kBK * 2;   // 16 KB
-constexpr uint32_t kRowsWBytes = kRowsBN * kBK * 2;   // 32 KB
-constexpr uint32_t kRowsOffX = 0;
-constexpr uint32_t kRowsOffW = kRowsOffX + kRowsStages * kRowsXBytes;
-constexpr uint32_t kRowsOffG = kRowsOffW + kRowsStages * kRowsWBytes;
-constexpr uint32_t kRowsOffBar = kRowsOffG + kRowsStages * kGBytes;
-// barriers: full[S], xform[S], empty[S], accfull[2], accempty[2], srfull[2], mmadone
-constexpr uint32_t kRowsNumBars = 3 * kRowsStages + 7;
-constexpr uint32_t kRowsOffSr = kRowsOffBar + ((kRowsNumBars * 8 + 15) / 16) * 16;
-constexpr uint32_t kRowsOffMisc = kRowsOffSr + 2 * kRowsBM * 4;
-constexpr uint32_t kRowsSmem = kRowsOffMisc + 16 + 1024;   // + alignment slack
-constexpr uint32_t kRowsTmemCols = 2 * kRowsBN;            // double-buffered accumulator
+constexpr uint32_t kRowsWBytes = kRowsBN * kBK * 2;   // 32 KB: four [64 k][64 n] W boxes
+constexpr uint32_t kRowsTmemCols = 2 * kRowsBN;       // double-buffered accumulator
+
+// Position in a ring of n pipeline stages: the slot and the parity of the
+// current pass over the ring (flips each time the slot wraps to 0).
+struct Ring {
+    uint32_t idx = 0, phase = 0, n;
+    __device__ explicit Ring(uint32_t n_) : n(n_) {}
+    __device__ __forceinline__ void advance() {
+        if (++idx == n) {
+            idx = 0;
+            phase ^= 1;
+        }
+    }
+};
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -86,40 +88,83 @@ __device__ __forceinline__ uint4 gain8(uint4 xv, uint4 gv, float& ss) {
     return o;
 }
 
-template <bool kFused>
+struct RowsLayout {
+    uint32_t xbytes, off_x, off_w, off_g, off_red, off_bar, off_sr, off_redss, off_rr, off_misc, total;
+};
+
+// Shared-memory layout of rows_kernel.  xrows: rows of X each stage loads
+// (128, or M rounded up to 16 when one row tile covers M).  X tiles come
+// first: the MMA always reads a 128-row window from an X tile, whose rows
+// past xrows (discarded results) fall on the following tiles.  red_slots:
+// with a cluster K split, split 0 gathers every split's partial rows (its own
+// included) as [splits][MP][256] fp32.
+__host__ __device__ inline RowsLayout rows_layout(int xrows, int stages, int red_slots, int MP) {
+    RowsLayout L;
+    L.xbytes = xrows * kBK * 2;
+    L.off_x = 0;
+    L.off_w = ((stages * L.xbytes + 1023) / 1024) * 1024;
+    L.off_g = L.off_w + stages * kRowsWBytes;
+    L.off_red = ((L.off_g + stages * kGBytes + 15) / 16) * 16;
+    L.off_bar = L.off_red + red_slots * MP * kRowsBN * 4;
+    const uint32_t nbars = 3 * kRowsMaxStages + 10;
+    L.off_sr = L.off_bar + ((nbars * 8 + 15) / 16) * 16;
+    L.off_redss = L.off_sr + 2 * kRowsBM * 4;
+    L.off_rr = L.off_redss + kClusterMaxSplits * kRowsBM * 4;
+    L.off_misc = L.off_rr + kRowsBM * 4;
+    L.total = L.off_misc + 16 + 1024;
+    return L;
+}
+
+template <bool kFused, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     rows_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                const __grid_constant__ CUtensorMap tmG, __nv_bfloat16* __restrict__ Y, int M,
-                int N, int K, float eps, int m_tiles, int n_tiles, int k_blocks) {
+                const __grid_constant__ CUtensorMap tmG, __nv_bfloat16* __restrict__ Y,
+                RowsLaunch a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
+    const int S = a.stages;
+    const int split = kSplit ? a.splits : 1;
+    const RowsLayout L = rows_layout(a.xrows, S, kSplit ? split : 0, a.MP);
+    const uint32_t xbytes = L.xbytes;
     const uint32_t sb = smem_u32(smem);
-    const uint32_t sx = sb + kRowsOffX, sw = sb + kRowsOffW, sg = sb + kRowsOffG;
-    const uint32_t bar0 = sb + kRowsOffBar;
+    const uint32_t sx = sb + L.off_x, sw = sb + L.off_w, sg = sb + L.off_g;
+    const uint32_t bar0 = sb + L.off_bar;
     auto full = [&](uint32_t s) { return bar0 + 8 * s; };
-    auto xform = [&](uint32_t s) { return bar0 + 8 * (kRowsStages + s); };
-    auto empty = [&](uint32_t s) { return bar0 + 8 * (2 * kRowsStages + s); };
-    auto accfull = [&](uint32_t b) { return bar0 + 8 * (3 * kRowsStages + b); };
-    auto accempty = [&](uint32_t b) { return bar0 + 8 * (3 * kRowsStages + 2 + b); };
-    auto srfull = [&](uint32_t b) { return bar0 + 8 * (3 * kRowsStages + 4 + b); };
-    const uint32_t mmadone = bar0 + 8 * (3 * kRowsStages + 6);
-    float* sr = reinterpret_cast<float*>(smem + kRowsOffSr);
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kRowsOffMisc);
-    volatile int* abort = reinterpret_cast<volatile int*>(smem + kRowsOffMisc + 4);
+    auto xform = [&](uint32_t s) { return bar0 + 8 * (kRowsMaxStages + s); };
+    auto empty = [&](uint32_t s) { return bar0 + 8 * (2 * kRowsMaxStages + s); };
+    auto accfull = [&](uint32_t b) { return bar0 + 8 * (3 * kRowsMaxStages + b); };
+    auto accempty = [&](uint32_t b) { return bar0 + 8 * (3 * kRowsMaxStages + 2 + b); };
+    auto srfull = [&](uint32_t b) { return bar0 + 8 * (3 * kRowsMaxStages + 4 + b); };
+    const uint32_t mmadone = bar0 + 8 * (3 * kRowsMaxStages + 6);
+    const uint32_t episync = bar0 + 8 * (3 * kRowsMaxStages + 7);
+    // split 0: every other split's partial rows have arrived; other splits:
+    // split 0 has consumed the partial rows this CTA pushed last
+    const uint32_t redfull = bar0 + 8 * (3 * kRowsMaxStages + 8);
+    const uint32_t redempty = bar0 + 8 * (3 * kRowsMaxStages + 9);
+    float* sr = reinterpret_cast<float*>(smem + L.off_sr);         // [2][128] row sums of squares
+    const uint32_t red_addr = sb + L.off_red, redss_addr = sb + L.off_redss;
+    const float* red = reinterpret_cast<const float*>(smem + L.off_red);      // [splits][MP][256]
+    const float* redss = reinterpret_cast<const float*>(smem + L.off_redss);  // [splits][128]
+    float* rr = reinterpret_cast<float*>(smem + L.off_rr);                     // [128]
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.off_misc);
+    volatile int* abort = reinterpret_cast<volatile int*>(smem + L.off_misc + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kRowsStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(full(s), 1);
-            mbar_init(xform(s), 128);
+            mbar_init(xform(s), 4);   // one elected lane per transform warp
             mbar_init(empty(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accfull(b), 1);
-            mbar_init(accempty(b), 128);
-            mbar_init(srfull(b), 128);
+            mbar_init(accempty(b), 4);  // one elected lane per epilogue warp
+            mbar_init(srfull(b), 4);    // one elected lane per transform warp
         }
         mbar_init(mmadone, 1);
+        mbar_init(episync, 4);
+        mbar_init(redfull, split > 1 ? (split - 1) * 128 : 1);
+        mbar_init(redempty, 1);
         *abort = 0;
         fence_mbar_init();
     }
@@ -135,60 +180,75 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // peers' barriers must be initialised before the first remote arrive
+    if (kSplit) cluster_sync_all();
+    // Set-up above overlaps the previous kernel on the stream; its writes are
+    // visible after grid_dep_wait().  The next kernel may then be scheduled.
+    grid_dep_wait();
+    if (threadIdx.x == 0) grid_dep_launch();
     const uint32_t tmem = *tmem_holder;
-    const int num_tiles = m_tiles * n_tiles;
+    // units = (tile, K split); with a cluster, blockIdx.x = cluster * splits +
+    // rank and the splits of one tile are the CTAs of one cluster
+    const int units = a.m_tiles * a.n_tiles * split;
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
             uint32_t it = 0;
+            Ring ring(S);
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+            for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+                const int t = u / split, sp = u - t * split;
+                const int kb0 = sp * a.kb_per_split, kb1 = min(a.k_blocks, kb0 + a.kb_per_split);
                 int mb, nb;
-                rows_tile_coords(t, m_tiles, n_tiles, mb, nb);
+                rows_tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
                 const int n0 = nb * kRowsBN;
-                const int nbox = min(4, (N - n0 + 63) / 64);
-                const uint32_t bytes = kRowsXBytes + nbox * kWBoxBytes + (kFused ? kGBytes : 0);
-                for (int kb = 0; kb < k_blocks; ++kb) {
-                    const uint32_t s = it % kRowsStages, ph = (it / kRowsStages) & 1;
+                const int nbox = min(4, (a.N - n0 + 63) / 64);
+                const uint32_t bytes = xbytes + nbox * kWBoxBytes + (kFused ? kGBytes : 0);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    const uint32_t s = ring.idx, ph = ring.phase;
                     if (!mbar_wait(empty(s), ph ^ 1, abort)) { ok = false; break; }
                     mbar_arrive_expect_tx(full(s), bytes);
-                    tma_load_2d_nohint(sx + s * kRowsXBytes, &tmX, full(s), kb * kBK, mb * kRowsBM);
+                    tma_load_2d_nohint(sx + s * xbytes, &tmX, full(s), kb * kBK, mb * kRowsBM);
                     for (int j = 0; j < nbox; ++j)
                         tma_load_2d_nohint(sw + s * kRowsWBytes + j * kWBoxBytes, &tmW, full(s),
                                            n0 + 64 * j, kb * kBK);
                     if (kFused) tma_load_1d(sg + s * kGBytes, &tmG, full(s), kb * kBK);
                     ++it;
+                    ring.advance();
                 }
             }
             // never leave with copies still landing in shared memory
-            const uint32_t pending = it < kRowsStages ? it : kRowsStages;
-            for (uint32_t i = it - pending; i < it; ++i)
-                mbar_wait_teardown(full(i % kRowsStages), (i / kRowsStages) & 1);
+            const uint32_t pending = it < static_cast<uint32_t>(S) ? it : S;
+            for (uint32_t i = it - pending; i < it; ++i) mbar_wait_teardown(full(i % S), (i / S) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(kRowsBM, kRowsBN, false, true);
             uint32_t it = 0, tl = 0;
+            Ring ring(S);
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++tl) {
+            for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++tl) {
+                const int t = u / split, sp = u - t * split;
+                const int kb0 = sp * a.kb_per_split, kb1 = min(a.k_blocks, kb0 + a.kb_per_split);
                 const uint32_t buf = tl & 1, use = tl >> 1;
                 if (!mbar_wait(accempty(buf), (use & 1) ^ 1, abort)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + buf * kRowsBN;
-                for (int kb = 0; kb < k_blocks; ++kb) {
-                    const uint32_t s = it % kRowsStages, ph = (it / kRowsStages) & 1;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    const uint32_t s = ring.idx, ph = ring.phase;
                     if (!mbar_wait(kFused ? xform(s) : full(s), ph, abort)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t a0 = sx + s * kRowsXBytes, b0 = sw + s * kRowsWBytes;
+                    const uint32_t a0 = sx + s * xbytes, b0 = sw + s * kRowsWBytes;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
                         mma_bf16_ss(d, sdesc_sw128(a0 + kk * 32, 16, 1024),
                                     sdesc_sw128(b0 + kk * 2048, kWBoxBytes, 1024), idesc,
-                                    (kb | kk) != 0);
+                                    (kb != kb0 || kk != 0));
                     mma_commit(empty(s));
                     ++it;
+                    ring.advance();
                 }
                 if (!ok) break;
                 mma_commit(accfull(buf));
@@ -203,31 +263,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             // row, so each warp access touches 4 whole rows (no bank conflicts).
             const int t = threadIdx.x - 128;
             const int kc = t & 7;           // chunk of the row
-            const int rb = t >> 3;          // rows rb + 16 i, i = 0..7
+            const int rb = t >> 3;          // rows rb + 16 i
+            const int groups = a.xrows / 16;
             const uint32_t swz_off = static_cast<uint32_t>((kc ^ (rb & 7)) << 4);
             uint32_t it = 0, tl = 0;
+            Ring ring(S);
             bool ok = true;
-            for (int t_ = blockIdx.x; ok && t_ < num_tiles; t_ += gridDim.x, ++tl) {
+            for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++tl) {
+                const int tt = u / split, sp = u - tt * split;
+                const int kb0 = sp * a.kb_per_split, kb1 = min(a.k_blocks, kb0 + a.kb_per_split);
                 const uint32_t buf = tl & 1, use = tl >> 1;
                 // sr[buf] is free once the epilogue released this accumulator
                 if (!warp_wait(accempty(buf), (use & 1) ^ 1, abort)) break;
                 float ss[kRowsBM / 16];
 #pragma unroll
                 for (int i = 0; i < kRowsBM / 16; ++i) ss[i] = 0.f;
-                for (int kb = 0; kb < k_blocks; ++kb) {
-                    const uint32_t s = it % kRowsStages, ph = (it / kRowsStages) & 1;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    const uint32_t s = ring.idx, ph = ring.phase;
                     if (!warp_wait(full(s), ph, abort)) { ok = false; break; }
                     const uint4 gv = lds128(sg + s * kGBytes + kc * 16);
-                    const uint32_t xt = sx + s * kRowsXBytes + swz_off;
+                    const uint32_t xt = sx + s * xbytes + swz_off;
+                    // rows rb + 16 i all have (row & 7) == (rb & 7)
+                    // all loads first, then the stores (the shared-memory
+                    // accesses keep program order), so the loads overlap
+                    uint4 xv[kRowsBM / 16];
 #pragma unroll
-                    for (int i = 0; i < kRowsBM / 16; ++i) {
-                        // row rb + 16 i has the same (row & 7) as rb
-                        const uint32_t a = xt + (rb + 16 * i) * 128;
-                        sts128(a, gain8(lds128(a), gv, ss[i]));
-                    }
+                    for (int i = 0; i < kRowsBM / 16; ++i)
+                        if (i < groups) xv[i] = lds128(xt + (rb + 16 * i) * 128);
+#pragma unroll
+                    for (int i = 0; i < kRowsBM / 16; ++i)
+                        if (i < groups) sts128(xt + (rb + 16 * i) * 128, gain8(xv[i], gv, ss[i]));
                     fence_proxy_async_smem();
-                    mbar_arrive(xform(s));
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xform(s));
                     ++it;
+                    ring.advance();
                 }
                 if (!ok) break;
 #pragma unroll
@@ -236,58 +306,137 @@ __global__ void __launch_bounds__(kThreads, 1)
                     v += __shfl_xor_sync(0xffffffffu, v, 1);
                     v += __shfl_xor_sync(0xffffffffu, v, 2);
                     v += __shfl_xor_sync(0xffffffffu, v, 4);
-                    if (kc == 0) sr[buf * kRowsBM + rb + 16 * i] = rsqrtf(v / static_cast<float>(K) + eps);
+                    if (kc == 0) sr[buf * kRowsBM + rb + 16 * i] = v;
                 }
-                mbar_arrive(srfull(buf));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(srfull(buf));
             }
         }
     } else if (warp >= 8) {
         // ------------------------------------------------ epilogue
         const int q = warp & 3;             // tensor-memory lane quarter of this warp
         const int row = q * 32 + lane;
+        const int e = threadIdx.x - 256;
+        const float inv_k = 1.f / static_cast<float>(a.K);
+        uint32_t ep = 0;
+        auto epi_sync = [&]() {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(episync);
+            return warp_wait(episync, (ep++) & 1, abort);
+        };
+        const uint32_t rank = kSplit ? cluster_ctarank() : 0;
+        uint32_t red_use = 0;
         uint32_t tl = 0;
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tl) {
+        for (int u = blockIdx.x; u < units; u += gridDim.x, ++tl) {
+            const int t = u / split;
             const uint32_t buf = tl & 1, use = tl >> 1;
             if (!warp_wait(accfull(buf), use & 1, abort)) break;
-            float r = 1.f;
-            if (kFused) {
-                if (!warp_wait(srfull(buf), use & 1, abort)) break;
-                r = sr[buf * kRowsBM + row];
-            }
+            if (kFused && !warp_wait(srfull(buf), use & 1, abort)) break;
             tc_fence_after();
             int mb, nb;
-            rows_tile_coords(t, m_tiles, n_tiles, mb, nb);
-            const int m = mb * kRowsBM + row;
+            rows_tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
             const int n0 = nb * kRowsBN;
-            const int ncols = min(kRowsBN, N - n0);
-            __nv_bfloat16* yrow = Y + static_cast<size_t>(m) * N + n0;
+            const int ncols = min(kRowsBN, a.N - n0);
+            const int rows_here = min(kRowsBM, a.M - mb * kRowsBM);   // valid rows of this tile
             const uint32_t taddr = tmem + buf * kRowsBN + (static_cast<uint32_t>(q * 32) << 16);
-            for (int c = 0; c < kRowsBN / 32; ++c) {
-                if (c * 32 >= ncols) break;   // warp-uniform
-                uint32_t v[32];
-                tmem_ld_32x32(taddr + c * 32, v);
-                if (m < M) {
+            const bool warp_has_rows = q * 32 < rows_here;              // warp-uniform
+            if (!kSplit) {
+                const int m = mb * kRowsBM + row;
+                const float r = kFused ? rsqrtf(sr[buf * kRowsBM + row] * inv_k + a.eps) : 1.f;
+                __nv_bfloat16* yrow = Y + static_cast<size_t>(m) * a.N + n0;
+                for (int c = 0; warp_has_rows && c < kRowsBN / 32; ++c) {
+                    if (c * 32 >= ncols) break;   // warp-uniform
+                    uint32_t v[32];
+                    tmem_ld_32x32(taddr + c * 32, v);
+                    if (row < rows_here) {
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const int col = c * 32 + g * 8;
-                        if (col < ncols) {
-                            uint4 o;
-                            o.x = pack_bf16x2(__uint_as_float(v[g * 8 + 0]) * r,
-                                              __uint_as_float(v[g * 8 + 1]) * r);
-                            o.y = pack_bf16x2(__uint_as_float(v[g * 8 + 2]) * r,
-                                              __uint_as_float(v[g * 8 + 3]) * r);
-                            o.z = pack_bf16x2(__uint_as_float(v[g * 8 + 4]) * r,
-                                              __uint_as_float(v[g * 8 + 5]) * r);
-                            o.w = pack_bf16x2(__uint_as_float(v[g * 8 + 6]) * r,
-                                              __uint_as_float(v[g * 8 + 7]) * r);
-                            *reinterpret_cast<uint4*>(yrow + col) = o;
+                        for (int g = 0; g < 4; ++g) {
+                            const int col = c * 32 + g * 8;
+                            if (col < ncols) {
+                                uint4 o;
+                                o.x = pack_bf16x2(__uint_as_float(v[g * 8 + 0]) * r,
+                                                  __uint_as_float(v[g * 8 + 1]) * r);
+                                o.y = pack_bf16x2(__uint_as_float(v[g * 8 + 2]) * r,
+                                                  __uint_as_float(v[g * 8 + 3]) * r);
+                                o.z = pack_bf16x2(__uint_as_float(v[g * 8 + 4]) * r,
+                                                  __uint_as_float(v[g * 8 + 5]) * r);
+                                o.w = pack_bf16x2(__uint_as_float(v[g * 8 + 6]) * r,
+                                                  __uint_as_float(v[g * 8 + 7]) * r);
+                                *reinterpret_cast<uint4*>(yrow + col) = o;
+                            }
                         }
                     }
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(accempty(buf));
+            } else {
+                // K split inside a cluster (one row tile, M <= 128): every split
+                // writes its partial rows (and row sums of squares) into split
+                // 0's shared memory, slot = split index; split 0 then adds the
+                // slots in split order and writes Y, column-parallel.
+                if (rank != 0 && !warp_wait_cluster(redempty, (red_use & 1) ^ 1, abort)) break;
+                const uint32_t slot = red_addr + rank * a.MP * kRowsBN * 4;
+                for (int c = 0; warp_has_rows && c < kRowsBN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32x32(taddr + c * 32, v);
+                    if (row < rows_here) {
+                        const uint32_t dst = slot + (row * kRowsBN + c * 32) * 4;
+#pragma unroll
+                        for (int g = 0; g < 8; ++g) {
+                            if (rank == 0)
+                                sts128(dst + g * 16, make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]));
+                            else
+                                st_dsmem_v4(mapa_shared(dst + g * 16, 0), make_uint4(v[4 * g], v[4 * g + 1],
+                                                                                      v[4 * g + 2], v[4 * g + 3]));
+                        }
+                    }
+                }
+                if (row < rows_here) {
+                    const float ssv = kFused ? sr[buf * kRowsBM + row] : 0.f;
+                    const uint32_t dst = redss_addr + (rank * kRowsBM + row) * 4;
+                    if (rank == 0)
+                        *reinterpret_cast<float*>(smem + L.off_redss + (rank * kRowsBM + row) * 4) = ssv;
+                    else
+                        st_dsmem_f32(mapa_shared(dst, 0), ssv);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(accempty(buf));
+                if (rank != 0) {
+                    mbar_arrive_remote(mapa_shared(redfull, 0));
+                } else {
+                    if (!epi_sync()) break;   // own slot written
+                    if (!warp_wait_cluster(redfull, red_use & 1, abort)) break;
+                    if (e < rows_here) {
+                        float tot = 0.f;
+                        for (int s2 = 0; s2 < split; ++s2) tot += redss[s2 * kRowsBM + e];
+                        rr[e] = kFused ? rsqrtf(tot * inv_k + a.eps) : 1.f;
+                    }
+                    if (!epi_sync()) break;
+                    const size_t slot_stride = static_cast<size_t>(a.MP) * kRowsBN;
+                    for (int m = 0; m < rows_here; ++m) {
+                        const float r = rr[m];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int col = e + 128 * h;
+                            float acc = 0.f;
+                            for (int s2 = 0; s2 < split; ++s2) acc += red[s2 * slot_stride + m * kRowsBN + col];
+                            if (col < ncols)
+                                Y[static_cast<size_t>(mb * kRowsBM + m) * a.N + n0 + col] =
+                                    __float2bfloat16_rn(acc * r);
+                        }
+                    }
+                    // every thread of split 0 is done with the slots: hand them back
+                    if (!epi_sync()) break;
+                    if (e == 0)
+                        for (int s2 = 1; s2 < split; ++s2) mbar_arrive_remote(mapa_shared(redempty, s2));
+                }
+                ++red_use;
             }
-            tc_fence_before();
-            mbar_arrive(accempty(buf));
         }
+        // split 0's last hand-back arrive must land before this CTA exits
+        if (kSplit && rank != 0 && red_use > 0) warp_wait_cluster(redempty, (red_use & 1) ^ 1, abort);
     }
 
     tc_fence_before();
@@ -300,19 +449,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------ small-M path
 struct ColsLayout {
-    uint32_t off_w, off_x, off_g, off_bar, off_ss, off_r, off_misc, total;
+    uint32_t off_w, off_x, off_g, off_red, off_bar, off_ss, off_r, off_redss, off_misc, total;
 };
 
-__host__ __device__ inline ColsLayout cols_layout(int MP, int stages) {
+// Shared-memory layout of cols_kernel.  With a cluster reduction, split 0's
+// CTA receives the other splits' fp32 partial tiles in `red`, as
+// [red_slots][MP rows][128 columns], and their row sums of squares in `redss`.
+__host__ __device__ inline ColsLayout cols_layout(int MP, int stages, int red_slots) {
     ColsLayout L;
     L.off_w = 0;
     L.off_x = L.off_w + stages * (kColsBN * kBK * 2);
     L.off_g = L.off_x + stages * (MP * kBK * 2);
-    L.off_bar = L.off_g + stages * kGBytes;
-    const uint32_t nbars = 3 * kColsMaxStages + 8;
+    L.off_red = L.off_g + stages * kGBytes;
+    L.off_bar = L.off_red + red_slots * MP * kColsBN * 4;
+    const uint32_t nbars = 3 * kColsMaxStages + 10;
     L.off_ss = L.off_bar + ((nbars * 8 + 15) / 16) * 16;
     L.off_r = L.off_ss + 2 * kColsMaxMP * 4;
-    L.off_misc = L.off_r + kColsMaxMP * 4;
+    L.off_redss = L.off_r;
+    L.off_misc = L.off_redss + (kClusterMaxSplits - 1) * kColsMaxMP * 4;
     L.total = L.off_misc + 16 + 1024;
     return L;
 }
@@ -325,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     const int MP = a.MP, S = a.stages;
-    const ColsLayout L = cols_layout(MP, S);
+    const ColsLayout L = cols_layout(MP, S, a.cluster ? a.splits - 1 : 0);
     const uint32_t sb = smem_u32(smem);
     const uint32_t sw = sb + L.off_w, sx = sb + L.off_x, sg = sb + L.off_g;
     const uint32_t xbytes = MP * kBK * 2;
@@ -339,28 +493,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto srfull = [&](uint32_t b) { return bar0 + 8 * (3 * kColsMaxStages + 4 + b); };
     const uint32_t mmadone = bar0 + 8 * (3 * kColsMaxStages + 6);
     const uint32_t episync = bar0 + 8 * (3 * kColsMaxStages + 7);
+    // split 0: the other splits' partials have arrived; other splits: split 0
+    // has consumed the previous partial this CTA pushed
+    const uint32_t redfull = bar0 + 8 * (3 * kColsMaxStages + 8);
+    const uint32_t redempty = bar0 + 8 * (3 * kColsMaxStages + 9);
+    const uint32_t red_addr = sb + L.off_red, redss_addr = sb + L.off_redss;
+    const float* red = reinterpret_cast<const float*>(smem + L.off_red);      // [splits-1][MP][128]
+    const float* redss = reinterpret_cast<const float*>(smem + L.off_redss);  // [splits-1][128]
     float* ss_s = reinterpret_cast<float*>(smem + L.off_ss);    // [2][128]
-    float* r_red = reinterpret_cast<float*>(smem + L.off_r);    // [128]
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.off_misc);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + L.off_misc + 4);
-    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L.off_misc + 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full(s), 1);
-            mbar_init(xform(s), 128);
+            mbar_init(xform(s), 4);   // one elected lane per transform warp
             mbar_init(empty(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accfull(b), 1);
-            mbar_init(accempty(b), 128);
-            mbar_init(srfull(b), 128);
+            mbar_init(accempty(b), 4);  // one elected lane per epilogue warp
+            mbar_init(srfull(b), 4);    // one elected lane per transform warp
         }
         mbar_init(mmadone, 1);
-        mbar_init(episync, 128);
+        mbar_init(episync, 4);
+        mbar_init(redfull, a.splits > 1 ? (a.splits - 1) * 128 : 1);
+        mbar_init(redempty, 1);
         *abort = 0;
-        *last_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -375,7 +535,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // peers' barriers must be initialised before the first remote arrive
+    if (a.cluster) cluster_sync_all();
+    // Set-up above overlaps the previous kernel on the stream; its writes are
+    // visible after grid_dep_wait().  The next kernel may then be scheduled.
+    grid_dep_wait();
+    if (threadIdx.x == 0) grid_dep_launch();
     const uint32_t tmem = *tmem_holder;
+    // With a cluster, the cluster's CTAs are the K splits of one column tile:
+    // blockIdx.x = cluster * splits + rank, and the unit walk below keeps them
+    // on the same tile.
     const int units = a.n_tiles * a.splits;
 
     if (warp == 0) {
@@ -384,6 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_w = policy_evict_first();   // W is read exactly once
             const uint64_t pol_x = policy_evict_last();    // X is re-read by every column tile
             uint32_t it = 0;
+            Ring ring(S);
             bool ok = true;
             for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
                 const int nt = u / a.splits, sp = u - nt * a.splits;
@@ -392,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nbox = min(2, (a.N - n0 + 63) / 64);
                 const uint32_t bytes = nbox * kWBoxBytes + xbytes + (kFused ? kGBytes : 0);
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    const uint32_t s = it % S, ph = (it / S) & 1;
+                    const uint32_t s = ring.idx, ph = ring.phase;
                     if (!mbar_wait(empty(s), ph ^ 1, abort)) { ok = false; break; }
                     mbar_arrive_expect_tx(full(s), bytes);
                     for (int j = 0; j < nbox; ++j)
@@ -401,6 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d(sx + s * xbytes, &tmX, full(s), kb * kBK, 0, pol_x);
                     if (kFused) tma_load_1d(sg + s * kGBytes, &tmG, full(s), kb * kBK);
                     ++it;
+                    ring.advance();
                 }
             }
             const uint32_t pending = it < static_cast<uint32_t>(S) ? it : S;
@@ -411,6 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(kColsBN, MP, true, false);
             uint32_t it = 0, tl = 0;
+            Ring ring(S);
             bool ok = true;
             for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++tl) {
                 const int nt = u / a.splits, sp = u - nt * a.splits;
@@ -420,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t d = tmem + buf * MP;
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    const uint32_t s = it % S, ph = (it / S) & 1;
+                    const uint32_t s = ring.idx, ph = ring.phase;
                     if (!mbar_wait(kFused ? xform(s) : full(s), ph, abort)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a0 = sw + s * wbytes, b0 = sx + s * xbytes;
@@ -431,6 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     (kb != kb0 || kk != 0));
                     mma_commit(empty(s));
                     ++it;
+                    ring.advance();
                 }
                 if (!ok) break;
                 mma_commit(accfull(buf));
@@ -447,6 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int groups = MP / 16;
             const uint32_t swz_off = static_cast<uint32_t>((kc ^ (rb & 7)) << 4);
             uint32_t it = 0, tl = 0;
+            Ring ring(S);
             bool ok = true;
             for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++tl) {
                 const int nt = u / a.splits, sp = u - nt * a.splits;
@@ -457,21 +631,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < kColsMaxMP / 16; ++i) ss[i] = 0.f;
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    const uint32_t s = it % S, ph = (it / S) & 1;
+                    const uint32_t s = ring.idx, ph = ring.phase;
                     if (!warp_wait(full(s), ph, abort)) { ok = false; break; }
                     const uint4 gv = lds128(sg + s * kGBytes + kc * 16);
                     const uint32_t xt = sx + s * xbytes;
+                    // all loads first, then the stores (see the row-tile path);
+                    // row = rb + 16 i has the same (row & 7) as rb
+                    uint4 xv[kColsMaxMP / 16];
 #pragma unroll
-                    for (int i = 0; i < kColsMaxMP / 16; ++i) {
-                        if (i < groups) {
-                            // row = rb + 16 i has the same (row & 7) as rb
-                            const uint32_t addr = xt + (rb + 16 * i) * 128 + swz_off;
-                            sts128(addr, gain8(lds128(addr), gv, ss[i]));
-                        }
-                    }
+                    for (int i = 0; i < kColsMaxMP / 16; ++i)
+                        if (i < groups) xv[i] = lds128(xt + (rb + 16 * i) * 128 + swz_off);
+#pragma unroll
+                    for (int i = 0; i < kColsMaxMP / 16; ++i)
+                        if (i < groups) sts128(xt + (rb + 16 * i) * 128 + swz_off, gain8(xv[i], gv, ss[i]));
                     fence_proxy_async_smem();
-                    mbar_arrive(xform(s));
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xform(s));
                     ++it;
+                    ring.advance();
                 }
                 if (!ok) break;
 #pragma unroll
@@ -482,7 +659,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     v += __shfl_xor_sync(0xffffffffu, v, 4);
                     if (i < groups && kc == 0) ss_s[buf * kColsMaxMP + rb + 16 * i] = v;
                 }
-                mbar_arrive(srfull(buf));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(srfull(buf));
             }
         }
     } else if (warp >= 8) {
@@ -493,9 +671,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // timeout elsewhere cannot leave a warp waiting forever)
         uint32_t ep = 0;
         auto epi_sync = [&]() {
-            mbar_arrive(episync);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(episync);
             return warp_wait(episync, (ep++) & 1, abort);
         };
+        const uint32_t rank = a.cluster ? cluster_ctarank() : 0;
+        uint32_t red_use = 0;
         uint32_t tl = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++tl) {
             const int nt = u / a.splits, sp = u - nt * a.splits;
@@ -525,11 +706,71 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 tc_fence_before();
-                mbar_arrive(accempty(buf));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(accempty(buf));
+            } else if (a.cluster) {
+                // Splits 1.. store their partial tile and row sums of squares
+                // straight into split 0's shared memory (one-way remote stores,
+                // then a release arrive); split 0 adds them in split order to
+                // its own partial, still in tensor memory, and writes Y.
+                if (rank != 0) {
+                    if (!warp_wait_cluster(redempty, (red_use & 1) ^ 1, abort)) break;
+                    const uint32_t dst =
+                        mapa_shared(red_addr + ((rank - 1) * MP * kColsBN + e) * 4, 0);
+                    for (int j = 0; j < jmax; ++j) {
+                        uint32_t v[16];
+                        tmem_ld_32x16(taddr + j * 16, v);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int m = j * 16 + i;
+                            if (m < a.M) st_dsmem_f32(dst + m * kColsBN * 4, __uint_as_float(v[i]));
+                        }
+                    }
+                    if (kFused && e < a.M)
+                        st_dsmem_f32(mapa_shared(redss_addr + ((rank - 1) * kColsMaxMP + e) * 4, 0),
+                                     ss_s[buf * kColsMaxMP + e]);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(accempty(buf));
+                    mbar_arrive_remote(mapa_shared(redfull, 0));
+                } else {
+                    if (!warp_wait_cluster(redfull, red_use & 1, abort)) break;
+                    for (int j = 0; j < jmax; ++j) {
+                        uint32_t v[16];
+                        tmem_ld_32x16(taddr + j * 16, v);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int m = j * 16 + i;
+                            if (m < a.M) {
+                                float acc = __uint_as_float(v[i]);
+                                float tot = kFused ? ss_s[buf * kColsMaxMP + m] : 0.f;
+                                for (int s2 = 1; s2 < a.splits; ++s2) {
+                                    acc += red[((s2 - 1) * MP + m) * kColsBN + e];
+                                    if (kFused) tot += redss[(s2 - 1) * kColsMaxMP + m];
+                                }
+                                const float r =
+                                    kFused ? rsqrtf(tot / static_cast<float>(a.K) + a.eps) : 1.f;
+                                if (n_ok) Y[static_cast<size_t>(m) * a.N + n] = __float2bfloat16_rn(acc * r);
+                            }
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(accempty(buf));
+                    // every thread of split 0 has read the slots: hand them back
+                    if (!epi_sync()) break;
+                    if (e == 0)
+                        for (int s2 = 1; s2 < a.splits; ++s2) mbar_arrive_remote(mapa_shared(redempty, s2));
+                }
+                ++red_use;
             } else {
-                // publish this split's partial sums, then the last CTA to finish
-                // the column tile adds all splits in split order (its own from
-                // tensor memory, which it still holds) and writes Y.
+                // Publish this split's partial sums (and its rows' partial sums
+                // of squares).  Then, per warp, the last of the splits' warps
+                // for these 32 columns adds all splits in split order (its own
+                // partial from tensor memory, which it still holds) and writes
+                // Y.  Counters are per (column tile, warp): no CTA-wide
+                // handshake follows the atomic, and the last warp issues all of
+                // its loads in one batch.
                 float* part = a.ws_acc + static_cast<size_t>(sp) * a.M * a.N;
                 for (int j = 0; j < jmax; ++j) {
                     uint32_t v[16];
@@ -545,57 +786,66 @@ __global__ void __launch_bounds__(kThreads, 1)
                     a.ws_ss[(static_cast<size_t>(nt) * a.splits + sp) * kColsMaxMP + e] =
                         ss_s[buf * kColsMaxMP + e];
                 __threadfence();
-                bool go = epi_sync();
-                if (go && e == 0) *last_flag = (atomicAdd(&a.counters[nt], 1) == a.splits - 1);
-                go = go && epi_sync();
-                if (go && *last_flag) {
+                // every thread's stores are globally visible before any warp counts
+                if (!epi_sync()) break;
+                int* counter = a.counters + nt * 4 + q;
+                uint32_t last = 0;
+                if (lane == 0) last = atomicAdd(counter, 1) == a.splits - 1;
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
                     __threadfence();
-                    if (kFused && e < a.M) {
-                        float tot = 0.f;
-#pragma unroll 4
-                        for (int s2 = 0; s2 < a.splits; ++s2)
-                            tot += __ldcg(&a.ws_ss[(static_cast<size_t>(nt) * a.splits + s2) *
-                                                       kColsMaxMP + e]);
-                        r_red[e] = rsqrtf(tot / static_cast<float>(a.K) + a.eps);
-                    }
-                    go = epi_sync();
-                    for (int j = 0; go && j < jmax; ++j) {
+                    float rr[kColsMaxMP / 32];
+                    for (int j = 0; j < jmax; ++j) {
                         uint32_t v[16];
                         tmem_ld_32x16(taddr + j * 16, v);
+                        if (j == 0) {
+                            // reciprocal RMS of rows lane, lane + 32, ... (loads
+                            // issued together with the first chunk's partials)
+#pragma unroll
+                            for (int i = 0; i < kColsMaxMP / 32; ++i) {
+                                const int m = lane + 32 * i;
+                                float tot = 0.f;
+                                if (kFused && m < a.M) {
+                                    const float* ssp =
+                                        a.ws_ss + static_cast<size_t>(nt) * a.splits * kColsMaxMP + m;
+#pragma unroll 4
+                                    for (int s2 = 0; s2 < a.splits; ++s2) tot += __ldcg(ssp + s2 * kColsMaxMP);
+                                }
+                                rr[i] = kFused ? rsqrtf(tot / static_cast<float>(a.K) + a.eps) : 1.f;
+                            }
+                        }
                         float acc[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-                        if (n_ok) {
-#pragma unroll 2
-                            for (int s2 = 0; s2 < a.splits; ++s2) {
-                                const float* p2 = a.ws_acc + static_cast<size_t>(s2) * a.M * a.N + n;
-                                float pv[16];
-#pragma unroll
-                                for (int i = 0; i < 16; ++i) {
-                                    const int m = j * 16 + i;
-                                    pv[i] = (s2 == sp) ? __uint_as_float(v[i])
-                                            : (m < a.M ? __ldcg(p2 + static_cast<size_t>(m) * a.N) : 0.f);
-                                }
-#pragma unroll
-                                for (int i = 0; i < 16; ++i) acc[i] += pv[i];
-                            }
+#pragma unroll 4
+                        for (int s2 = 0; s2 < a.splits; ++s2) {
+                            const float* p2 = a.ws_acc + static_cast<size_t>(s2) * a.M * a.N + n;
 #pragma unroll
                             for (int i = 0; i < 16; ++i) {
                                 const int m = j * 16 + i;
-                                if (m < a.M) {
-                                    const float r = kFused ? r_red[m] : 1.f;
-                                    Y[static_cast<size_t>(m) * a.N + n] = __float2bfloat16_rn(acc[i] * r);
-                                }
+                                acc[i] += (s2 == sp) ? __uint_as_float(v[i])
+                                          : ((m < a.M && n_ok) ? __ldcg(p2 + static_cast<size_t>(m) * a.N) : 0.f);
                             }
                         }
+                        const int jj = j >> 1;   // rows 16j .. 16j+15 sit in rr[j / 2]
+                        const float rsel = jj == 0 ? rr[0] : jj == 1 ? rr[1] : jj == 2 ? rr[2] : rr[3];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int m = j * 16 + i;
+                            const float r = __shfl_sync(0xffffffffu, rsel, ((j & 1) << 4) + i);
+                            if (m < a.M && n_ok)
+                                Y[static_cast<size_t>(m) * a.N + n] = __float2bfloat16_rn(acc[i] * r);
+                        }
                     }
-                    if (e == 0) a.counters[nt] = 0;
+                    if (lane == 0) *counter = 0;
                 }
                 tc_fence_before();
-                mbar_arrive(accempty(buf));
-                if (!go || !epi_sync()) break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(accempty(buf));
             }
         }
+        // split 0's last hand-back arrive must land before this CTA exits
+        if (a.cluster && rank != 0 && red_use > 0) warp_wait_cluster(redempty, (red_use & 1) ^ 1, abort);
     }
 
     tc_fence_before();
@@ -657,7 +907,7 @@ __global__ void __launch_bounds__(kNormThreads)
 // Raises a kernel's dynamic shared-memory limit to the device's opt-in
 // maximum, once per (kernel slot, device).
 cudaError_t ensure_smem_attr(const void* func, int slot) {
-    static int done[4][64] = {};
+    static int done[8][64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -672,46 +922,96 @@ cudaError_t ensure_smem_attr(const void* func, int slot) {
 
 }  // namespace
 
-size_t rows_smem_bytes() { return kRowsSmem; }
-size_t cols_smem_bytes(int MP, int stages) { return cols_layout(MP, stages).total; }
-size_t cols_fixed_smem_bytes() { return cols_layout(16, 0).total; }
+size_t rows_smem_bytes(int xrows, int stages, int red_slots, int MP) {
+    return rows_layout(xrows, stages, red_slots, MP).total;
+}
+size_t rows_stage_bytes(int xrows) { return xrows * kBK * 2 + kRowsWBytes + kGBytes; }
+size_t cols_smem_bytes(int MP, int stages, int red_slots) {
+    return cols_layout(MP, stages, red_slots).total;
+}
+size_t cols_fixed_smem_bytes(int MP, int red_slots) { return cols_layout(MP, 0, red_slots).total; }
 size_t cols_stage_bytes(int MP) { return kColsBN * kBK * 2 + MP * kBK * 2 + kGBytes; }
+
+// Launch with programmatic dependent launch (the kernel's set-up may overlap
+// the previous kernel on the stream) and, optionally, a 1-D cluster.
+template <typename... Args>
+cudaError_t launch_ex(void (*kern)(Args...), int grid, size_t smem, int cluster, cudaStream_t s,
+                      Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& tmW,
                         const CUtensorMap& tmG, void* Y, const RowsLaunch& a, cudaStream_t s) {
     auto* y = static_cast<__nv_bfloat16*>(Y);
-    cudaError_t e;
-    if (fused) {
-        e = ensure_smem_attr(reinterpret_cast<const void*>(rows_kernel<true>), 0);
-        if (e != cudaSuccess) return e;
-        rows_kernel<true><<<a.grid, kThreads, kRowsSmem, s>>>(tmX, tmW, tmG, y, a.M, a.N, a.K,
-                                                              a.eps, a.m_tiles, a.n_tiles,
-                                                              a.k_blocks);
-    } else {
-        e = ensure_smem_attr(reinterpret_cast<const void*>(rows_kernel<false>), 1);
-        if (e != cudaSuccess) return e;
-        rows_kernel<false><<<a.grid, kThreads, kRowsSmem, s>>>(tmX, tmW, tmG, y, a.M, a.N, a.K,
-                                                               a.eps, a.m_tiles, a.n_tiles,
-                                                               a.k_blocks);
-    }
+    const bool split = a.cluster != 0;
+    auto kern = fused ? (split ? rows_kernel<true, true> : rows_kernel<true, false>)
+                      : (split ? rows_kernel<false, true> : rows_kernel<false, false>);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), (fused ? 0 : 1) + (split ? 4 : 0));
+    if (e != cudaSuccess) return e;
+    const size_t smem = rows_smem_bytes(a.xrows, a.stages, split ? a.splits : 0, a.MP);
+    e = launch_ex(kern, a.grid, smem, split ? a.splits : 1, s, tmX, tmW, tmG, y, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 cudaError_t launch_cols(bool fused, const CUtensorMap& tmX, const CUtensorMap& tmW,
                         const CUtensorMap& tmG, void* Y, const ColsLaunch& a, cudaStream_t s) {
     auto* y = static_cast<__nv_bfloat16*>(Y);
-    const size_t smem = cols_smem_bytes(a.MP, a.stages);
-    cudaError_t e;
-    if (fused) {
-        e = ensure_smem_attr(reinterpret_cast<const void*>(cols_kernel<true>), 2);
-        if (e != cudaSuccess) return e;
-        cols_kernel<true><<<a.grid, kThreads, smem, s>>>(tmX, tmW, tmG, y, a);
-    } else {
-        e = ensure_smem_attr(reinterpret_cast<const void*>(cols_kernel<false>), 3);
-        if (e != cudaSuccess) return e;
-        cols_kernel<false><<<a.grid, kThreads, smem, s>>>(tmX, tmW, tmG, y, a);
-    }
+    auto kern = fused ? cols_kernel<true> : cols_kernel<false>;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), fused ? 2 : 3);
+    if (e != cudaSuccess) return e;
+    const size_t smem = cols_smem_bytes(a.MP, a.stages, a.cluster ? a.splits - 1 : 0);
+    e = launch_ex(kern, a.grid, smem, a.cluster ? a.splits : 1, s, tmX, tmW, tmG, y, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+template <typename Kern>
+int max_active_clusters(Kern kern, int slot, int splits, size_t smem) {
+    if (ensure_smem_attr(reinterpret_cast<const void*>(kern), slot) != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(splits);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = splits;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
+    return n;
+}
+
+int cols_max_active_clusters(bool fused, int splits, size_t smem) {
+    return fused ? max_active_clusters(cols_kernel<true>, 2, splits, smem)
+                 : max_active_clusters(cols_kernel<false>, 3, splits, smem);
+}
+
+int rows_max_active_clusters(bool fused, int splits, size_t smem) {
+    return fused ? max_active_clusters(rows_kernel<true, true>, 4, splits, smem)
+                 : max_active_clusters(rows_kernel<false, true>, 5, splits, smem);
 }
 
 cudaError_t launch_rmsnorm(const void* X, const void* g, void* Xn, int M, int K, float eps,

@@ -14,22 +14,36 @@ constexpr int kBK = 64;          // K extent of one pipeline stage (128 B of bf1
 // Row-tile path: CTA tile 128 (rows of X) x 256 (columns of W).
 constexpr int kRowsBM = 128;
 constexpr int kRowsBN = 256;
+constexpr int kRowsMaxStages = 6;
 
 // Small-M path: CTA tile 128 (columns of W) x MP (rows of X, padded to 16).
 constexpr int kColsBN = 128;
 constexpr int kColsMaxMP = 128;
-constexpr int kColsMaxStages = 8;
+constexpr int kColsMaxStages = 12;
+constexpr int kClusterMaxSplits = 8;   // portable cluster size
 constexpr int kColsMaxSplits = 16;
 
-size_t rows_smem_bytes();
-size_t cols_smem_bytes(int MP, int stages);
-size_t cols_fixed_smem_bytes();
+// Row-tile path shared memory: xrows = rows of X loaded per stage (128, or
+// M rounded up to 16 for a single row tile); red_slots = K splits reduced
+// through a cluster (0 without); MP = M rounded up to 16.
+size_t rows_smem_bytes(int xrows, int stages, int red_slots, int MP);
+size_t rows_stage_bytes(int xrows);
+int rows_max_active_clusters(bool fused, int splits, size_t smem);
+// red_slots = splits - 1 when the splits reduce through a cluster, else 0.
+size_t cols_smem_bytes(int MP, int stages, int red_slots);
+size_t cols_fixed_smem_bytes(int MP, int red_slots);
 size_t cols_stage_bytes(int MP);
+// Clusters of `splits` CTAs of cols_kernel that fit on the device at once
+// (0 if the configuration cannot be launched).
+int cols_max_active_clusters(bool fused, int splits, size_t smem);
 
 struct RowsLaunch {
     int M, N, K;
     float eps;
     int m_tiles, n_tiles, k_blocks;
+    int splits, kb_per_split;  // K split of each tile (splits > 1 needs m_tiles == 1)
+    int cluster;               // 1: the splits of a tile form a cluster
+    int xrows, MP, stages;
     int grid;
 };
 
@@ -37,10 +51,12 @@ struct ColsLaunch {
     int M, N, K;
     float eps;
     int MP, n_tiles, k_blocks, splits, kb_per_split, stages, grid;
+    int cluster;      // 1: the splits of a column tile form a cluster; splits > 0
+                      // push their partials into split 0's shared memory (ws_* unused)
     uint32_t tmem_cols;
-    float* ws_acc;    // [splits][M][N] fp32 partials (splits > 1 only)
+    float* ws_acc;    // [splits][M][N] fp32 partials (splits > 1 without a cluster)
     float* ws_ss;     // [n_tiles][splits][128] fp32 partial sums of squares
-    int* counters;    // [n_tiles] arrival counters, zero between launches
+    int* counters;    // [n_tiles][4] arrival counters (one per epilogue warp), zero between launches
 };
 
 cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& tmW,

@@ -51,11 +51,10 @@ def test_force_path_roundtrip(lib):
     assert rmm.force_path(rmm.PATH_AUTO) == rmm.PATH_AUTO
 
 
-def test_dispatch_by_rows(lib):
-    assert rmm.dispatch_path(1, 4096, 6144) == rmm.PATH_COLS
-    assert rmm.dispatch_path(64, 4096, 28672) == rmm.PATH_COLS
-    assert rmm.dispatch_path(65, 4096, 6144) == rmm.PATH_ROWS
-    assert rmm.dispatch_path(4096, 4096, 6144) == rmm.PATH_ROWS
+def test_default_dispatch_is_row_tile_path(lib):
+    # The row-tile path serves every shape unless a path is forced.
+    for M in (1, 16, 64, 65, 128, 4096):
+        assert rmm.dispatch_path(M, 4096, 6144) == rmm.PATH_ROWS
 
 
 A16 = 0x10000          # a 16-byte aligned fake address; never dereferenced

@@ -87,6 +87,8 @@ def test_workload_sampled_rows(rmm, name):
 RAGGED = [
     (1, 64, 8), (7, 72, 136), (16, 1024, 1000), (33, 520, 264), (64, 4096, 1032),
     (65, 256, 256), (129, 1032, 520), (255, 328, 392), (300, 2048, 2056),
+    # few column tiles and long K: more than 8 K splits (global-workspace reduction)
+    (16, 16384, 128), (48, 8192, 264),
 ]
 
 

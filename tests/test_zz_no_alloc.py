@@ -45,34 +45,45 @@ def _call(lib, fn, X, g, W, Y, eps):
 
 @pytest.mark.parametrize("name", ["decode_qkv_16x4096x6144", "decode_gatedmlp_64x4096x28672",
                                   "tiny_8x1024x1024", "prefill_qkv_4096x4096x6144"])
-def test_noalloc_matches_fused_on_two_calls(lib, name):
+@pytest.mark.parametrize("path", [0, 2])
+def test_noalloc_matches_fused_on_two_calls(lib, name, path):
+    # path 2 forces the small-M path, whose K split keeps its partial sums in
+    # the fixed scratch array; path 0 is the default (row-tile) dispatch.
     from sm_rmsnorm_matmul_gb300 import inputs
     w = inputs.WORKLOADS[name]
+    if path == 2 and w.M > 128:
+        pytest.skip("small-M path holds at most 128 rows")
     X, g, W = (t.cuda() for t in inputs.generate_workload(w))
-    ref = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
-    assert _call(lib, "rmsnorm_matmul", X, g, W, ref, w.eps) == 0
-    torch.cuda.synchronize()
-    ref_np = oracle.to_f64(ref.cpu())
-    for _ in range(2):
-        Y = torch.full((w.M, w.N), float("nan"), dtype=torch.bfloat16, device="cuda")
-        assert _call(lib, "rmsnorm_matmul_noalloc", X, g, W, Y, w.eps) == 0
+    prev = lib.rmm_force_path(path)
+    try:
+        ref = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
+        assert _call(lib, "rmsnorm_matmul", X, g, W, ref, w.eps) == 0
         torch.cuda.synchronize()
-        assert lib.rmm_device_status(torch.cuda.current_stream().cuda_stream) == 0
-        bad, max_abs, _ = oracle.tolerance_violations(Y.cpu(), ref_np, ATOL, RTOL)
-        assert bad == 0, f"{name}: {bad} elements differ from rmsnorm_matmul (max {max_abs:.3e})"
+        ref_np = oracle.to_f64(ref.cpu())
+        for _ in range(2):
+            Y = torch.full((w.M, w.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+            assert _call(lib, "rmsnorm_matmul_noalloc", X, g, W, Y, w.eps) == 0
+            torch.cuda.synchronize()
+            assert lib.rmm_device_status(torch.cuda.current_stream().cuda_stream) == 0
+            bad, max_abs, _ = oracle.tolerance_violations(Y.cpu(), ref_np, ATOL, RTOL)
+            assert bad == 0, f"{name}: {bad} elements differ from rmsnorm_matmul (max {max_abs:.3e})"
+    finally:
+        lib.rmm_force_path(prev)
 
 
 def test_noalloc_back_to_back_different_inputs(lib):
     # Two different problems in a row share the scratch array; neither may see
-    # the other's partial sums.
+    # the other's partial sums.  (Small-M path forced, so the array is used.)
     from sm_rmsnorm_matmul_gb300 import inputs
     outs = []
+    prev = lib.rmm_force_path(2)
     for seed in (11, 12):
         X, g, W = (t.cuda() for t in inputs.random_problem(16, 4096, 6144, seed=seed))
         Y = torch.empty((16, 6144), dtype=torch.bfloat16, device="cuda")
         assert _call(lib, "rmsnorm_matmul_noalloc", X, g, W, Y, 1e-6) == 0
         outs.append((X, g, W, Y))
     torch.cuda.synchronize()
+    lib.rmm_force_path(prev)
     for X, g, W, Y in outs:
         ref = torch.empty_like(Y)
         assert _call(lib, "rmsnorm_matmul", X, g, W, ref, 1e-6) == 0
