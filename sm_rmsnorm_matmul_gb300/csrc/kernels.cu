@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(mmadone, 1);
         mbar_init(episync, 4);
-        mbar_init(redfull, split > 1 ? (split - 1) * 128 : 1);
+        mbar_init(redfull, split > 1 ? split - 1 : 1);   // one arrive per other split (+ bytes)
         mbar_init(redempty, 1);
         *abort = 0;
         fence_mbar_init();
@@ -371,40 +371,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(accempty(buf));
             } else {
-                // K split inside a cluster (one row tile, M <= 128): every split
-                // writes its partial rows (and row sums of squares) into split
-                // 0's shared memory, slot = split index; split 0 then adds the
-                // slots in split order and writes Y, column-parallel.
+                // K split inside a cluster (one row tile, M <= 128).  Every
+                // split stages its partial rows (fp32, [row][256]) and row sums
+                // of squares in its own shared memory at slot = split index;
+                // splits 1.. then bulk-copy their slot into the same slot of
+                // split 0, which adds the slots in split order and writes Y.
                 if (rank != 0 && !warp_wait_cluster(redempty, (red_use & 1) ^ 1, abort)) break;
                 const uint32_t slot = red_addr + rank * a.MP * kRowsBN * 4;
+                const uint32_t ss_slot = redss_addr + rank * kRowsBM * 4;
                 for (int c = 0; warp_has_rows && c < kRowsBN / 32; ++c) {
                     uint32_t v[32];
                     tmem_ld_32x32(taddr + c * 32, v);
                     if (row < rows_here) {
                         const uint32_t dst = slot + (row * kRowsBN + c * 32) * 4;
 #pragma unroll
-                        for (int g = 0; g < 8; ++g) {
-                            if (rank == 0)
-                                sts128(dst + g * 16, make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]));
-                            else
-                                st_dsmem_v4(mapa_shared(dst + g * 16, 0), make_uint4(v[4 * g], v[4 * g + 1],
-                                                                                      v[4 * g + 2], v[4 * g + 3]));
-                        }
+                        for (int g = 0; g < 8; ++g)
+                            sts128(dst + g * 16, make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]));
                     }
                 }
-                if (row < rows_here) {
-                    const float ssv = kFused ? sr[buf * kRowsBM + row] : 0.f;
-                    const uint32_t dst = redss_addr + (rank * kRowsBM + row) * 4;
-                    if (rank == 0)
-                        *reinterpret_cast<float*>(smem + L.off_redss + (rank * kRowsBM + row) * 4) = ssv;
-                    else
-                        st_dsmem_f32(mapa_shared(dst, 0), ssv);
-                }
+                if (row < rows_here)
+                    *reinterpret_cast<float*>(smem + (ss_slot - sb) + row * 4) =
+                        kFused ? sr[buf * kRowsBM + row] : 0.f;
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(accempty(buf));
+                const uint32_t part_bytes = static_cast<uint32_t>(rows_here) * kRowsBN * 4;
+                const uint32_t ss_bytes = ((static_cast<uint32_t>(rows_here) * 4 + 15) / 16) * 16;
                 if (rank != 0) {
-                    mbar_arrive_remote(mapa_shared(redfull, 0));
+                    fence_proxy_async_smem();   // the bulk copy reads these writes
+                    if (!epi_sync()) break;
+                    if (e == 0) {
+                        const uint32_t bar = mapa_shared(redfull, 0);
+                        mbar_arrive_expect_tx_remote(bar, part_bytes + ss_bytes);
+                        bulk_copy_to_peer(mapa_shared(slot, 0), slot, part_bytes, bar);
+                        bulk_copy_to_peer(mapa_shared(ss_slot, 0), ss_slot, ss_bytes, bar);
+                    }
                 } else {
                     if (!epi_sync()) break;   // own slot written
                     if (!warp_wait_cluster(redfull, red_use & 1, abort)) break;
@@ -414,18 +415,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                         rr[e] = kFused ? rsqrtf(tot * inv_k + a.eps) : 1.f;
                     }
                     if (!epi_sync()) break;
+                    // thread e owns columns 2e, 2e+1; all splits' loads of a row
+                    // are issued together
+                    const int col = 2 * e;
                     const size_t slot_stride = static_cast<size_t>(a.MP) * kRowsBN;
+                    const float2* red2 = reinterpret_cast<const float2*>(red);
+                    __nv_bfloat16* yb = Y + static_cast<size_t>(mb * kRowsBM) * a.N + n0 + col;
+#pragma unroll 2
                     for (int m = 0; m < rows_here; ++m) {
-                        const float r = rr[m];
+                        float2 pv[kClusterMaxSplits];
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int col = e + 128 * h;
-                            float acc = 0.f;
-                            for (int s2 = 0; s2 < split; ++s2) acc += red[s2 * slot_stride + m * kRowsBN + col];
-                            if (col < ncols)
-                                Y[static_cast<size_t>(mb * kRowsBM + m) * a.N + n0 + col] =
-                                    __float2bfloat16_rn(acc * r);
-                        }
+                        for (int s2 = 0; s2 < kClusterMaxSplits; ++s2)
+                            if (s2 < split) pv[s2] = red2[(s2 * slot_stride + m * kRowsBN + col) / 2];
+                        float ax = 0.f, ay = 0.f;
+#pragma unroll
+                        for (int s2 = 0; s2 < kClusterMaxSplits; ++s2)
+                            if (s2 < split) {
+                                ax += pv[s2].x;
+                                ay += pv[s2].y;
+                            }
+                        const float r = rr[m];
+                        if (col < ncols)
+                            *reinterpret_cast<uint32_t*>(yb + static_cast<size_t>(m) * a.N) =
+                                pack_bf16x2(ax * r, ay * r);
                     }
                     // every thread of split 0 is done with the slots: hand them back
                     if (!epi_sync()) break;

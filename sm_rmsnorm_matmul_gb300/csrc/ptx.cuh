@@ -76,7 +76,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 
 // mbar_wait for roles that run as whole warps: every lane waits, and the
 // result is combined so that the warp leaves (or stays) together and its
-// .sync.aligned instructions never run on a partial warp.
+// .sync.aligned instructions never run on a partial warp.  (Polling from one
+// lane and broadcasting measured slower on GB300.)
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
     const bool ok = mbar_wait(bar, parity, abort);
     return __all_sync(0xffffffffu, ok);
@@ -150,6 +151,25 @@ __device__ __forceinline__ void st_dsmem_v4(uint32_t cluster_addr, uint4 v) {
                  "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
 }
+// arrive on a (possibly remote) barrier and raise its expected transaction
+// bytes, release semantics at cluster scope
+__device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t cluster_addr, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
+                     cluster_addr),
+                 "r"(bytes)
+                 : "memory");
+}
+// Copy `bytes` (multiple of 16, 16-byte aligned ends) from this CTA's shared
+// memory to another CTA's of the cluster; completes `bytes` of transaction
+// count on `bar` (an address in the destination CTA).
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
+                                                  uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst_cluster),
+        "r"(src), "r"(bytes), "r"(bar_cluster)
+        : "memory");
+}
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
@@ -216,6 +236,16 @@ __device__ __forceinline__ void tma_load_1d(uint32_t dst, const CUtensorMap* m, 
         " [%0], [%1, {%3}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0)
         : "memory");
+}
+
+// Prefetch a 2-D box into L2 (no shared memory, no completion).  Reads that
+// follow still go through L2, which stays coherent with any later writer, so
+// a prefetch can never make a reader see stale data.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* m, int c0, int c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
 }
 
 // Make this thread's generic-proxy shared-memory writes visible to the async
