@@ -459,6 +459,278 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ------------------------------------------- row-tile path, A in tensor memory
+// The fused kernel for several row tiles (prefill-like shapes).  The gain is
+// applied on the way from shared to tensor memory: each transform thread
+// reads its row of the X tile once, multiplies by g in bf16x2 and stores the
+// row straight into a tensor-memory A slot with tcgen05.st, and the MMA reads
+// A from there.  Compared with writing X*g back into shared memory for the
+// MMA to read, this removes two of the three passes over each X tile in
+// shared memory, whose bandwidth bounds this kernel.  X and W have separate
+// rings: an X slot is released as soon as its rows are in tensor memory.
+// Tensor memory: columns [0, 256) hold the accumulator (single buffer; the
+// epilogue holds it only while it reads it out), [256, 512) eight A slots of
+// 32 columns (128 rows x 64 bf16 each).
+constexpr int kTaXStages = 4;
+constexpr int kTaWStages = 4;
+constexpr int kTaAStages = 8;
+constexpr uint32_t kTaXBytes = kRowsBM * kBK * 2;    // 16 KB
+constexpr uint32_t kTaOffX = 0;
+constexpr uint32_t kTaOffW = kTaOffX + kTaXStages * kTaXBytes;
+constexpr uint32_t kTaOffG = kTaOffW + kTaWStages * kRowsWBytes;
+constexpr uint32_t kTaOffBar = kTaOffG + kTaXStages * kGBytes;
+// xfull, xempty, wfull, wempty, afull, aempty, accfull, accempty, srfull[2], srempty[2], mmadone
+constexpr uint32_t kTaNumBars = 2 * kTaXStages + 2 * kTaWStages + 2 * kTaAStages + 7;
+constexpr uint32_t kTaOffSr = kTaOffBar + ((kTaNumBars * 8 + 15) / 16) * 16;
+constexpr uint32_t kTaOffMisc = kTaOffSr + 2 * kRowsBM * 4;
+constexpr uint32_t kTaSmem = kTaOffMisc + 16 + 1024;
+constexpr uint32_t kTaAccCol = 0, kTaACol = 256;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    rows_ta_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                   const __grid_constant__ CUtensorMap tmG, __nv_bfloat16* __restrict__ Y,
+                   RowsLaunch a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t sx = sb + kTaOffX, sw = sb + kTaOffW, sg = sb + kTaOffG;
+    const uint32_t bar0 = sb + kTaOffBar;
+    uint32_t nb_ = 0;
+    const uint32_t xfull0 = bar0 + 8 * nb_; nb_ += kTaXStages;
+    const uint32_t xempty0 = bar0 + 8 * nb_; nb_ += kTaXStages;
+    const uint32_t wfull0 = bar0 + 8 * nb_; nb_ += kTaWStages;
+    const uint32_t wempty0 = bar0 + 8 * nb_; nb_ += kTaWStages;
+    const uint32_t afull0 = bar0 + 8 * nb_; nb_ += kTaAStages;
+    const uint32_t aempty0 = bar0 + 8 * nb_; nb_ += kTaAStages;
+    const uint32_t accfull = bar0 + 8 * nb_++;
+    const uint32_t accempty = bar0 + 8 * nb_++;
+    const uint32_t srfull0 = bar0 + 8 * nb_; nb_ += 2;
+    const uint32_t srempty0 = bar0 + 8 * nb_; nb_ += 2;
+    const uint32_t mmadone = bar0 + 8 * nb_++;
+    float* sr = reinterpret_cast<float*>(smem + kTaOffSr);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kTaOffMisc);
+    volatile int* abort = reinterpret_cast<volatile int*>(smem + kTaOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTaXStages; ++s) {
+            mbar_init(xfull0 + 8 * s, 1);
+            mbar_init(xempty0 + 8 * s, 4);
+        }
+        for (int s = 0; s < kTaWStages; ++s) {
+            mbar_init(wfull0 + 8 * s, 1);
+            mbar_init(wempty0 + 8 * s, 1);
+        }
+        for (int s = 0; s < kTaAStages; ++s) {
+            mbar_init(afull0 + 8 * s, 4);
+            mbar_init(aempty0 + 8 * s, 1);
+        }
+        mbar_init(accfull, 1);
+        mbar_init(accempty, 4);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(srfull0 + 8 * b, 4);
+            mbar_init(srempty0 + 8 * b, 4);
+        }
+        mbar_init(mmadone, 1);
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmX);
+        prefetch_tmap(&tmW);
+        prefetch_tmap(&tmG);
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(tmem_holder), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // Set-up above overlaps the previous kernel on the stream; its writes are
+    // visible after grid_dep_wait().  The next kernel may then be scheduled.
+    grid_dep_wait();
+    if (threadIdx.x == 0) grid_dep_launch();
+    const uint32_t tmem = *tmem_holder;
+    const int num_tiles = a.m_tiles * a.n_tiles;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            Ring xr(kTaXStages), wr(kTaWStages);
+            uint32_t xi = 0, wi = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+                int mb, nb;
+                rows_tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
+                const int n0 = nb * kRowsBN;
+                const int nbox = min(4, (a.N - n0 + 63) / 64);
+                for (int kb = 0; kb < a.k_blocks; ++kb) {
+                    if (!mbar_wait(xempty0 + 8 * xr.idx, xr.phase ^ 1, abort)) { ok = false; break; }
+                    const uint32_t xf = xfull0 + 8 * xr.idx;
+                    mbar_arrive_expect_tx(xf, kTaXBytes + kGBytes);
+                    tma_load_2d_nohint(sx + xr.idx * kTaXBytes, &tmX, xf, kb * kBK, mb * kRowsBM);
+                    tma_load_1d(sg + xr.idx * kGBytes, &tmG, xf, kb * kBK);
+                    xr.advance();
+                    ++xi;
+                    if (!mbar_wait(wempty0 + 8 * wr.idx, wr.phase ^ 1, abort)) { ok = false; break; }
+                    const uint32_t wf = wfull0 + 8 * wr.idx;
+                    mbar_arrive_expect_tx(wf, nbox * kWBoxBytes);
+                    for (int j = 0; j < nbox; ++j)
+                        tma_load_2d_nohint(sw + wr.idx * kRowsWBytes + j * kWBoxBytes, &tmW, wf,
+                                           n0 + 64 * j, kb * kBK);
+                    wr.advance();
+                    ++wi;
+                }
+            }
+            // never leave with copies still landing in shared memory
+            for (uint32_t i = xi > kTaXStages ? xi - kTaXStages : 0; i < xi; ++i)
+                mbar_wait_teardown(xfull0 + 8 * (i % kTaXStages), (i / kTaXStages) & 1);
+            for (uint32_t i = wi > kTaWStages ? wi - kTaWStages : 0; i < wi; ++i)
+                mbar_wait_teardown(wfull0 + 8 * (i % kTaWStages), (i / kTaWStages) & 1);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(kRowsBM, kRowsBN, false, true);
+            Ring wr(kTaWStages), ar(kTaAStages);
+            uint32_t tl = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++tl) {
+                if (!mbar_wait(accempty, (tl & 1) ^ 1, abort)) break;
+                tc_fence_after();
+                const uint32_t d = tmem + kTaAccCol;
+                for (int kb = 0; kb < a.k_blocks; ++kb) {
+                    if (!mbar_wait(wfull0 + 8 * wr.idx, wr.phase, abort)) { ok = false; break; }
+                    if (!mbar_wait(afull0 + 8 * ar.idx, ar.phase, abort)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a0 = tmem + kTaACol + ar.idx * 32;
+                    const uint32_t b0 = sw + wr.idx * kRowsWBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        mma_bf16_ts(d, a0 + kk * 8, sdesc_sw128(b0 + kk * 2048, kWBoxBytes, 1024), idesc,
+                                    (kb | kk) != 0);
+                    mma_commit(wempty0 + 8 * wr.idx);
+                    mma_commit(aempty0 + 8 * ar.idx);
+                    wr.advance();
+                    ar.advance();
+                }
+                if (!ok) break;
+                mma_commit(accfull);
+            }
+            mma_commit(mmadone);
+            mbar_wait_teardown(mmadone, 0);
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------ transform: X*g -> tensor memory
+        const int q = warp - 4;               // lane quarter this warp may access
+        const int row = q * 32 + lane;        // row of the X tile
+        const uint32_t xrow = static_cast<uint32_t>(row) * 128;
+        const uint32_t swz = static_cast<uint32_t>(row & 7);
+        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+        Ring xr(kTaXStages), ar(kTaAStages);
+        uint32_t tl = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++tl) {
+            const uint32_t buf = tl & 1, use = tl >> 1;
+            // sr[buf] is free once the epilogue read it for the tile two back
+            if (!warp_wait(srempty0 + 8 * buf, (use & 1) ^ 1, abort)) break;
+            float ss = 0.f;
+            for (int kb = 0; kb < a.k_blocks; ++kb) {
+                if (!warp_wait(xfull0 + 8 * xr.idx, xr.phase, abort)) { ok = false; break; }
+                const uint32_t xt = sx + xr.idx * kTaXBytes + xrow;
+                const uint32_t gt = sg + xr.idx * kGBytes;
+                uint4 xv[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) xv[c] = lds128(xt + ((c ^ swz) << 4));
+                uint32_t out[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 gv = lds128(gt + c * 16);
+                    const uint32_t xs[4] = {xv[c].x, xv[c].y, xv[c].z, xv[c].w};
+                    const uint32_t gs[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float x0 = bf16lo(xs[i]), x1 = bf16hi(xs[i]);
+                        ss = fmaf(x0, x0, ss);
+                        ss = fmaf(x1, x1, ss);
+                        out[c * 4 + i] = mul_bf16x2(xs[i], gs[i]);
+                    }
+                }
+                // the X slot has been read (values are in registers)
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xempty0 + 8 * xr.idx);
+                xr.advance();
+                if (!warp_wait(aempty0 + 8 * ar.idx, ar.phase ^ 1, abort)) { ok = false; break; }
+                tmem_st_32x32(tmem + kTaACol + ar.idx * 32 + lane_base, out);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(afull0 + 8 * ar.idx);
+                ar.advance();
+            }
+            if (!ok) break;
+            sr[buf * kRowsBM + row] = ss;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(srfull0 + 8 * buf);
+        }
+    } else if (warp >= 8) {
+        // ------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const float inv_k = 1.f / static_cast<float>(a.K);
+        uint32_t tl = 0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tl) {
+            const uint32_t buf = tl & 1, use = tl >> 1;
+            if (!warp_wait(accfull, tl & 1, abort)) break;
+            if (!warp_wait(srfull0 + 8 * buf, use & 1, abort)) break;
+            tc_fence_after();
+            const float r = rsqrtf(sr[buf * kRowsBM + row] * inv_k + a.eps);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(srempty0 + 8 * buf);
+            int mb, nb;
+            rows_tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
+            const int n0 = nb * kRowsBN;
+            const int ncols = min(kRowsBN, a.N - n0);
+            const int rows_here = min(kRowsBM, a.M - mb * kRowsBM);
+            const uint32_t taddr = tmem + kTaAccCol + (static_cast<uint32_t>(q * 32) << 16);
+            __nv_bfloat16* yrow = Y + static_cast<size_t>(mb * kRowsBM + row) * a.N + n0;
+            for (int c = 0; q * 32 < rows_here && c < kRowsBN / 32; ++c) {
+                if (c * 32 >= ncols) break;   // warp-uniform
+                uint32_t v[32];
+                tmem_ld_32x32(taddr + c * 32, v);
+                if (row < rows_here) {
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const int col = c * 32 + g * 8;
+                        if (col < ncols) {
+                            uint4 o;
+                            o.x = pack_bf16x2(__uint_as_float(v[g * 8 + 0]) * r,
+                                              __uint_as_float(v[g * 8 + 1]) * r);
+                            o.y = pack_bf16x2(__uint_as_float(v[g * 8 + 2]) * r,
+                                              __uint_as_float(v[g * 8 + 3]) * r);
+                            o.z = pack_bf16x2(__uint_as_float(v[g * 8 + 4]) * r,
+                                              __uint_as_float(v[g * 8 + 5]) * r);
+                            o.w = pack_bf16x2(__uint_as_float(v[g * 8 + 6]) * r,
+                                              __uint_as_float(v[g * 8 + 7]) * r);
+                            *reinterpret_cast<uint4*>(yrow + col) = o;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(accempty);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 // ------------------------------------------------------------ small-M path
 struct ColsLayout {
     uint32_t off_w, off_x, off_g, off_red, off_bar, off_ss, off_r, off_redss, off_misc, total;
@@ -975,6 +1247,13 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
                         const CUtensorMap& tmG, void* Y, const RowsLaunch& a, cudaStream_t s) {
     auto* y = static_cast<__nv_bfloat16*>(Y);
     const bool split = a.cluster != 0;
+    if (fused && !split && a.xrows == kRowsBM) {
+        cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(rows_ta_kernel), 6);
+        if (e != cudaSuccess) return e;
+        e = launch_ex(rows_ta_kernel, a.grid, kTaSmem, 1, s, tmX, tmW, tmG, y, a);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     auto kern = fused ? (split ? rows_kernel<true, true> : rows_kernel<true, false>)
                       : (split ? rows_kernel<false, true> : rows_kernel<false, false>);
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), (fused ? 0 : 1) + (split ? 4 : 0));
