@@ -90,6 +90,21 @@ bool map_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint3
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Row-major bf16 matrix [rows, cols] written in boxes of [128 rows, 32
+// columns] from shared memory with the 64-byte swizzle; writes outside the
+// matrix are dropped.
+bool map_2d_store(CUtensorMap* m, void* ptr, uint64_t rows, uint64_t cols) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {32, static_cast<cuuint32_t>(rmm::kRowsBM)};
+    const cuuint32_t estr[2] = {1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // bf16 vector [n] read in boxes of 64 elements.
 bool map_1d(CUtensorMap* m, const void* ptr, uint64_t n) {
     EncodeTiledFn f = encode_fn();
@@ -435,6 +450,11 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
     a.MP = p.MP;
     a.stages = p.stages;
     a.grid = p.grid;
+    CUtensorMap tmY;
+    if (fused && !p.cluster && p.xrows == rmm::kRowsBM) {
+        if (!map_2d_store(&tmY, Y, M, N)) return RMM_ERR_INTERNAL;
+        a.tmY = &tmY;
+    }
     return rmm::launch_rows(fused, tmX, tmW, tmG, Y, a, stream) == cudaSuccess ? RMM_OK
                                                                               : RMM_ERR_LAUNCH;
 }

@@ -471,16 +471,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Tensor memory: columns [0, 256) hold the accumulator (single buffer; the
 // epilogue holds it only while it reads it out), [256, 512) eight A slots of
 // 32 columns (128 rows x 64 bf16 each).
-constexpr int kTaXStages = 4;
+constexpr int kTaXStages = 3;
 constexpr int kTaWStages = 4;
 constexpr int kTaAStages = 8;
 constexpr uint32_t kTaXBytes = kRowsBM * kBK * 2;    // 16 KB
+constexpr uint32_t kTaStageOut = kRowsBM * 32 * 2;   // 8 KB: 128 rows x 32 bf16 of Y
 constexpr uint32_t kTaOffX = 0;
 constexpr uint32_t kTaOffW = kTaOffX + kTaXStages * kTaXBytes;
-constexpr uint32_t kTaOffG = kTaOffW + kTaWStages * kRowsWBytes;
+constexpr uint32_t kTaOffOut = kTaOffW + kTaWStages * kRowsWBytes;   // 2 staging buffers
+constexpr uint32_t kTaOffG = kTaOffOut + 2 * kTaStageOut;
 constexpr uint32_t kTaOffBar = kTaOffG + kTaXStages * kGBytes;
-// xfull, xempty, wfull, wempty, afull, aempty, accfull, accempty, srfull[2], srempty[2], mmadone
-constexpr uint32_t kTaNumBars = 2 * kTaXStages + 2 * kTaWStages + 2 * kTaAStages + 7;
+// xfull, xempty, wfull, wempty, afull, aempty, accfull, accempty, srfull[2], srempty[2],
+// mmadone, episync
+constexpr uint32_t kTaNumBars = 2 * kTaXStages + 2 * kTaWStages + 2 * kTaAStages + 8;
 constexpr uint32_t kTaOffSr = kTaOffBar + ((kTaNumBars * 8 + 15) / 16) * 16;
 constexpr uint32_t kTaOffMisc = kTaOffSr + 2 * kRowsBM * 4;
 constexpr uint32_t kTaSmem = kTaOffMisc + 16 + 1024;
@@ -488,7 +491,7 @@ constexpr uint32_t kTaAccCol = 0, kTaACol = 256;
 
 __global__ void __launch_bounds__(kThreads, 1)
     rows_ta_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                   const __grid_constant__ CUtensorMap tmG, __nv_bfloat16* __restrict__ Y,
+                   const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmY,
                    RowsLaunch a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
@@ -507,6 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t srfull0 = bar0 + 8 * nb_; nb_ += 2;
     const uint32_t srempty0 = bar0 + 8 * nb_; nb_ += 2;
     const uint32_t mmadone = bar0 + 8 * nb_++;
+    const uint32_t episync = bar0 + 8 * nb_++;
+    const uint32_t sout = sb + kTaOffOut;
     float* sr = reinterpret_cast<float*>(smem + kTaOffSr);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kTaOffMisc);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + kTaOffMisc + 4);
@@ -532,6 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(srempty0 + 8 * b, 4);
         }
         mbar_init(mmadone, 1);
+        mbar_init(episync, 4);
         *abort = 0;
         fence_mbar_init();
     }
@@ -539,6 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmX);
         prefetch_tmap(&tmW);
         prefetch_tmap(&tmG);
+        prefetch_tmap(&tmY);
     }
     if (warp == 2) {
         tmem_alloc(smem_u32(tmem_holder), 512);
@@ -635,7 +642,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t buf = tl & 1, use = tl >> 1;
             // sr[buf] is free once the epilogue read it for the tile two back
             if (!warp_wait(srempty0 + 8 * buf, (use & 1) ^ 1, abort)) break;
-            float ss = 0.f;
+            float ssp[8];   // independent partial sums: no long dependency chain
+#pragma unroll
+            for (int c = 0; c < 8; ++c) ssp[c] = 0.f;
             for (int kb = 0; kb < a.k_blocks; ++kb) {
                 if (!warp_wait(xfull0 + 8 * xr.idx, xr.phase, abort)) { ok = false; break; }
                 const uint32_t xt = sx + xr.idx * kTaXBytes + xrow;
@@ -652,8 +661,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const float x0 = bf16lo(xs[i]), x1 = bf16hi(xs[i]);
-                        ss = fmaf(x0, x0, ss);
-                        ss = fmaf(x1, x1, ss);
+                        ssp[c] = fmaf(x0, x0, ssp[c]);
+                        ssp[c] = fmaf(x1, x1, ssp[c]);
                         out[c * 4 + i] = mul_bf16x2(xs[i], gs[i]);
                     }
                 }
@@ -669,15 +678,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ar.advance();
             }
             if (!ok) break;
-            sr[buf * kRowsBM + row] = ss;
+            sr[buf * kRowsBM + row] = ((ssp[0] + ssp[1]) + (ssp[2] + ssp[3])) +
+                                      ((ssp[4] + ssp[5]) + (ssp[6] + ssp[7]));
             __syncwarp();
             if (lane == 0) mbar_arrive(srfull0 + 8 * buf);
         }
     } else if (warp >= 8) {
         // ------------------------------------------------ epilogue
+        // Read the whole accumulator row (scaled, bf16) into registers and
+        // release tensor memory at once; then store Y through two 8 KB
+        // staging buffers with TMA stores (64-byte swizzle: the 16-byte chunk
+        // j of row r sits at chunk j ^ ((r >> 1) & 3)), overlapped with the
+        // next tile's main loop.
         const int q = warp & 3;
         const int row = q * 32 + lane;
+        const int e = threadIdx.x - 256;
         const float inv_k = 1.f / static_cast<float>(a.K);
+        uint32_t ep = 0;
+        auto epi_sync = [&]() {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(episync);
+            return warp_wait(episync, (ep++) & 1, abort);
+        };
+        const uint32_t rswz = static_cast<uint32_t>((row >> 1) & 3);
+        uint32_t chunks = 0;   // staging buffer uses so far
         uint32_t tl = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tl) {
             const uint32_t buf = tl & 1, use = tl >> 1;
@@ -690,37 +714,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             int mb, nb;
             rows_tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
             const int n0 = nb * kRowsBN;
-            const int ncols = min(kRowsBN, a.N - n0);
-            const int rows_here = min(kRowsBM, a.M - mb * kRowsBM);
             const uint32_t taddr = tmem + kTaAccCol + (static_cast<uint32_t>(q * 32) << 16);
-            __nv_bfloat16* yrow = Y + static_cast<size_t>(mb * kRowsBM + row) * a.N + n0;
-            for (int c = 0; q * 32 < rows_here && c < kRowsBN / 32; ++c) {
-                if (c * 32 >= ncols) break;   // warp-uniform
-                uint32_t v[32];
-                tmem_ld_32x32(taddr + c * 32, v);
-                if (row < rows_here) {
+            uint32_t pk[kRowsBN / 2];   // the row, scaled and packed as bf16x2
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const int col = c * 32 + g * 8;
-                        if (col < ncols) {
-                            uint4 o;
-                            o.x = pack_bf16x2(__uint_as_float(v[g * 8 + 0]) * r,
-                                              __uint_as_float(v[g * 8 + 1]) * r);
-                            o.y = pack_bf16x2(__uint_as_float(v[g * 8 + 2]) * r,
-                                              __uint_as_float(v[g * 8 + 3]) * r);
-                            o.z = pack_bf16x2(__uint_as_float(v[g * 8 + 4]) * r,
-                                              __uint_as_float(v[g * 8 + 5]) * r);
-                            o.w = pack_bf16x2(__uint_as_float(v[g * 8 + 6]) * r,
-                                              __uint_as_float(v[g * 8 + 7]) * r);
-                            *reinterpret_cast<uint4*>(yrow + col) = o;
-                        }
-                    }
-                }
+            for (int c = 0; c < kRowsBN / 16; ++c) {
+                uint32_t v[16];
+                tmem_ld_32x16(taddr + c * 16, v);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    pk[c * 8 + i] = pack_bf16x2(__uint_as_float(v[2 * i]) * r,
+                                                __uint_as_float(v[2 * i + 1]) * r);
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(accempty);
+            if (lane == 0) mbar_arrive(accempty);   // the MMA may start the next tile
+            bool ok = true;
+#pragma unroll
+            for (int c = 0; c < kRowsBN / 32; ++c) {
+                if (n0 + c * 32 < a.N) {              // block-uniform
+                    const uint32_t sbuf = sout + (chunks & 1) * kTaStageOut;
+                    // the store issued two chunks ago must have read this buffer
+                    if (e == 0) bulk_wait_group_read<1>();
+                    if (!(ok = epi_sync())) break;
+                    const uint32_t rbase = sbuf + row * 64;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        sts128(rbase + ((j ^ rswz) << 4),
+                               make_uint4(pk[c * 16 + 4 * j], pk[c * 16 + 4 * j + 1],
+                                          pk[c * 16 + 4 * j + 2], pk[c * 16 + 4 * j + 3]));
+                    fence_proxy_async_smem();
+                    if (!(ok = epi_sync())) break;
+                    if (e == 0) {
+                        tma_store_2d(&tmY, sbuf, n0 + c * 32, mb * kRowsBM);
+                        bulk_commit_group();
+                    }
+                    ++chunks;
+                }
+            }
+            if (!ok) break;
         }
+        if (e == 0) bulk_wait_group_all();   // Y is written before the CTA exits
     }
 
     tc_fence_before();
@@ -1250,7 +1283,7 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
     if (fused && !split && a.xrows == kRowsBM) {
         cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(rows_ta_kernel), 6);
         if (e != cudaSuccess) return e;
-        e = launch_ex(rows_ta_kernel, a.grid, kTaSmem, 1, s, tmX, tmW, tmG, y, a);
+        e = launch_ex(rows_ta_kernel, a.grid, kTaSmem, 1, s, tmX, tmW, tmG, *a.tmY, a);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }

@@ -45,6 +45,8 @@ struct RowsLaunch {
     int cluster;               // 1: the splits of a tile form a cluster
     int xrows, MP, stages;
     int grid;
+    const CUtensorMap* tmY;    // Y in boxes of [128 rows][32 columns], 64-byte swizzle
+                               // (used by the fused kernel for several row tiles)
 };
 
 struct ColsLaunch {
