@@ -257,7 +257,8 @@ def bench_workload(torch, rmm, inputs, w, K, W_warm, device, stream, l2, with_un
     status = rmm.device_status(stream)
     del graphs
     res = {"secs": secs, "n_copies": n_copies, "status": status, "host": host,
-           "copies": copies, "path": rmm.dispatch_path(w.M, w.K, w.N)}
+           "copies": copies, "path": rmm.dispatch_path(w.M, w.K, w.N),
+           "plan": rmm.describe_plan(w.M, w.K, w.N)}
     if with_unfused:
         xn = [torch.empty((w.M, w.K), dtype=torch.bfloat16, device=device) for _ in range(n_copies)]
 
@@ -448,7 +449,7 @@ def main():
                 "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4)}
     roof["traffic"] = traffic_from_profile(w.name)
     roof["peak_source"] = peak_src
-    roof["kernel"] = "cols_kernel<fused>" if main_res["path"] == 2 else "rows_kernel<fused>"
+    roof["kernel"] = kernel_name(rmm, w)
     roof["algorithmic_bytes_per_launch"] = w.bytes_algorithmic
 
     out = {
@@ -467,6 +468,7 @@ def main():
         "config": {
             "workload": w.name, "M": w.M, "K": w.K, "N": w.N, "eps": w.eps, "seed": w.seed,
             "accumulate": "fp32", "path": "small-M (cols)" if main_res["path"] == 2 else "row-tile",
+            "plan": main_res["plan"],
             "l2": f"rotating input/output copies: {main_res['n_copies']} x "
                   f"{w.bytes_algorithmic / 1e6:.1f} MB > 3 x L2 ({l2 / 1e6:.0f} MB)"
                   if main_res["n_copies"] > 1 else
@@ -500,12 +502,25 @@ def main():
         pg.destroy_process_group()
 
 
+def kernel_name(rmm, w):
+    """Name of the kernel the fused call launches for this workload."""
+    plan = rmm.describe_plan(w.M, w.K, w.N)
+    if plan["path"] == 2:
+        return "cols_kernel<fused>"
+    if plan["cluster"]:
+        return f"rows_kernel<fused, K split x{plan['splits']} in a cluster>"
+    if w.M > 128:
+        return "rows_ta_kernel (A operand in tensor memory)"
+    return "rows_kernel<fused>"
+
+
 def shape_entry(w, t, r, peaks, k):
     tflops = w.flops / t / 1e12
     gbs = w.bytes_xwy / t / 1e9
     roof_t = max(w.flops / (peaks["bf16_tflops"] * 1e12), w.bytes_xwy / (peaks["hbm_gbs"] * 1e9))
     bound = "tensor" if w.flops / (peaks["bf16_tflops"] * 1e12) > w.bytes_xwy / (peaks["hbm_gbs"] * 1e9) else "hbm"
     e = {"workload": w.name, "path": "small-M (cols)" if r["path"] == 2 else "row-tile",
+         "plan": r.get("plan"),
          "steps": k, "us_per_call": round(t * 1e6, 3), "tflops": round(tflops, 2),
          "hbm_gbs": round(gbs, 1), "bound": bound, "roofline_frac": round(roof_t / t, 4),
          "copies": r["n_copies"], "device_status": r["status"]}

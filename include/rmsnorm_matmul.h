@@ -66,13 +66,14 @@ typedef enum {
  *   X  [M,K] bf16 input rows           g [K] bf16 gain
  *   W  [K,N] bf16 weights (N contiguous) Y [M,N] bf16 output (written)
  *   eps added to the mean square inside the square root.
- * A shape-based dispatcher picks the tensor-core row-tile path (large M:
- * X tiles are the MMA A operand) or the small-M weight-streaming path (W
- * tiles are the MMA A operand, split over K when N alone gives too few
- * tiles).  Both compute X*g and the row sum of squares in the same pass as
- * the contraction and apply r[m] in the epilogue.  The small-M path may use
- * a library-owned fp32 workspace per (device, stream), allocated on first
- * use (so make the first call outside any CUDA-graph capture).
+ * One launch of the tensor-core row-tile kernels: 128-row x 256-column tiles,
+ * X*g and the row sum of squares computed in the same pass as the
+ * contraction, r[m] applied in the epilogue.  For M <= 128 the K range may be
+ * split over up to 8 CTAs of a thread-block cluster whose partial sums are
+ * combined in shared memory, in a fixed order.  With rmm_force_path(2) the
+ * operand-swapped small-M kernel runs instead; its K split may use a
+ * library-owned fp32 workspace per (device, stream), allocated on first use
+ * (make that first call outside any CUDA-graph capture).
  * Returns an rmm_status.
  */
 int rmsnorm_matmul(const void* X, const void* g, const void* W, void* Y,
@@ -130,8 +131,9 @@ const char* rmm_status_string(int code);
  * array), held on every device where the library's device code is loaded
  * until the process exits.  Limit: splits x M x N x 4 bytes must fit in
  * 15 MiB (for example M = 64, N = 28672 with two K splits uses 14 MiB);
- * larger problems return RMM_ERR_SCRATCH_LIMIT.  The row-tile path (M > 64)
- * and unsplit small-M launches use no scratch.
+ * larger problems return RMM_ERR_SCRATCH_LIMIT.  The default row-tile path
+ * and unsplit small-M launches use no scratch; the small-M path's K split
+ * (rmm_force_path(2)) is the variant that uses the array.
  *
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
