@@ -86,6 +86,49 @@ def dist_env():
     return ws, rank, local
 
 
+class RankSync:
+    """Barrier and max-over-ranks for N replicas (one process per GPU).
+
+    The operation has no exchange step, so N GPUs run N independent replicas;
+    the only communication is this host-side barrier and the MAX of the
+    per-rank timings, over a gloo process group (no NCCL, no data-path
+    collective).  With one rank every call is a no-op.
+    """
+
+    def __init__(self, dist):
+        self.dist = dist
+
+    @classmethod
+    def create(cls, world_size: int):
+        if world_size <= 1:
+            return cls(None)
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        return cls(dist)
+
+    def __call__(self, val=None):
+        """Barrier; with a value, return the maximum of it over all ranks."""
+        if self.dist is None:
+            return val
+        if val is None:
+            self.dist.barrier()
+            return None
+        import torch
+        t = torch.tensor([float(val)], dtype=torch.float64)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.barrier()
+            self.dist.destroy_process_group()
+
+
+def whole_job_value(units_per_rank: float, world_size: int, max_secs: float) -> float:
+    """Units all ranks processed per second of the slowest rank (weak scaling)."""
+    return world_size * units_per_rank / max_secs
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
 
@@ -366,6 +409,8 @@ def main():
     ap.add_argument("--shapes", choices=["all", "none"], default="all")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--reference-budget", type=float, default=90.0,
+                    help="seconds of oracle work for the whole --impl reference run")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -381,21 +426,8 @@ def main():
     import sm_rmsnorm_matmul_gb300 as rmm
     rmm.lib()  # fail loudly if the CUDA library is missing
 
-    pg = None
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("gloo")
-        pg = dist
-
-    def barrier(val=None):
-        if pg is None:
-            return val
-        if val is None:
-            pg.barrier()
-            return None
-        t = torch.tensor([val], dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        return float(t.item())
+    sync = RankSync.create(ws)
+    barrier = sync if ws > 1 else None
 
     device = torch.device("cuda", local if ws > 1 else 0)
     torch.cuda.set_device(device)
@@ -412,12 +444,12 @@ def main():
     with ClockSampler(gpu_id) as sampler:
         main_res = bench_workload(torch, rmm, inputs, w, args.steps, args.warmup, device,
                                   stream, l2, with_unfused=True, sampler=sampler,
-                                  barrier=barrier if ws > 1 else None)
+                                  barrier=barrier)
         host = main_res["host"]
         e2e_steps = max(3, min(args.steps, 200))
         e2e_secs, h2d, d2h = e2e_bench(torch, rmm, w, host, device, stream, e2e_steps)
         if ws > 1:
-            e2e_secs = barrier(e2e_secs)
+            e2e_secs = sync(e2e_secs)
         del main_res["copies"]
         shapes = []
         if args.shapes == "all" and rank == 0:
@@ -437,7 +469,7 @@ def main():
     K = args.steps
     t_step = main_res["secs"] / K
     bytes_step = w.bytes_xwy
-    value = ws * bytes_step / t_step / 1e9
+    value = whole_job_value(bytes_step, ws, t_step) / 1e9
     achieved = w.bytes_algorithmic / t_step / 1e9
     bound = "hbm" if w.flops / w.bytes_xwy < 290 else "tensor"
     if bound == "hbm":
@@ -497,9 +529,7 @@ def main():
                                "secs_per_call": round(secs, 4)}
     if rank == 0:
         print(json.dumps(out), flush=True)
-    if pg is not None:
-        pg.barrier()
-        pg.destroy_process_group()
+    sync.close()
 
 
 def kernel_name(rmm, w):
@@ -536,7 +566,7 @@ def run_reference(args, w, ws, rank):
         return 0
     import oracle
     oracle.build()
-    budget = 90.0
+    budget = args.reference_budget
     K, Wm = args.steps, args.warmup
     # W untimed warm-up steps, then exactly K timed steps, each on a row sample
     # sized so that the whole run stays within the budget
