@@ -306,8 +306,11 @@ int rows_stages(int xrows, int red_slots, int MP, const DeviceInfo& d) {
     const size_t fixed = rmm::rows_smem_bytes(xrows, 0, red_slots, MP);
     const size_t per = rmm::rows_stage_bytes(xrows);
     const size_t avail = d.smem_optin > 0 ? static_cast<size_t>(d.smem_optin) : 227 * 1024;
-    const int st = avail > fixed ? static_cast<int>((avail - fixed) / per) : 0;
-    return std::min(rmm::kRowsMaxStages, st);
+    int st = avail > fixed ? static_cast<int>((avail - fixed) / per) : 0;
+    st = std::min(rmm::kRowsMaxStages, st);
+    // the X tiles are padded to 1 KB as a whole
+    while (st > 0 && rmm::rows_smem_bytes(xrows, st, red_slots, MP) > avail) --st;
+    return st;
 }
 
 std::mutex g_rows_occ_mu;

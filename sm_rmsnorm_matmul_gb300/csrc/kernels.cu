@@ -89,15 +89,23 @@ __device__ __forceinline__ uint4 gain8(uint4 xv, uint4 gv, float& ss) {
 }
 
 struct RowsLayout {
-    uint32_t xbytes, off_x, off_w, off_g, off_red, off_bar, off_sr, off_redss, off_rr, off_misc, total;
+    uint32_t xbytes, off_x, off_w, off_g, off_red, off_bar, off_sr, off_redss, off_misc, total;
 };
+
+// Column chunks of 32 in a row tile; with a cluster K split of S, chunk c is
+// reduced by CTA c % S, which therefore owns at most ceil(8 / S) chunks.
+constexpr int kRowsChunks = kRowsBN / 32;
+__host__ __device__ inline int rows_owned_max(int splits) {
+    return (kRowsChunks + splits - 1) / splits;
+}
 
 // Shared-memory layout of rows_kernel.  xrows: rows of X each stage loads
 // (128, or M rounded up to 16 when one row tile covers M).  X tiles come
 // first: the MMA always reads a 128-row window from an X tile, whose rows
 // past xrows (discarded results) fall on the following tiles.  red_slots:
-// with a cluster K split, split 0 gathers every split's partial rows (its own
-// included) as [splits][MP][256] fp32.
+// with a cluster K split of S = red_slots, each CTA receives, for the chunks
+// it owns, every split's partial rows as [S][ceil(8/S)][MP][32] fp32 (the
+// 16-byte pieces of a row rotated by row & 7 against bank conflicts).
 __host__ __device__ inline RowsLayout rows_layout(int xrows, int stages, int red_slots, int MP) {
     RowsLayout L;
     L.xbytes = xrows * kBK * 2;
@@ -105,12 +113,12 @@ __host__ __device__ inline RowsLayout rows_layout(int xrows, int stages, int red
     L.off_w = ((stages * L.xbytes + 1023) / 1024) * 1024;
     L.off_g = L.off_w + stages * kRowsWBytes;
     L.off_red = ((L.off_g + stages * kGBytes + 15) / 16) * 16;
-    L.off_bar = L.off_red + red_slots * MP * kRowsBN * 4;
+    const uint32_t red_bytes = red_slots > 0 ? red_slots * rows_owned_max(red_slots) * MP * 128 : 0;
+    L.off_bar = L.off_red + red_bytes;
     const uint32_t nbars = 3 * kRowsMaxStages + 10;
     L.off_sr = L.off_bar + ((nbars * 8 + 15) / 16) * 16;
     L.off_redss = L.off_sr + 2 * kRowsBM * 4;
-    L.off_rr = L.off_redss + kClusterMaxSplits * kRowsBM * 4;
-    L.off_misc = L.off_rr + kRowsBM * 4;
+    L.off_misc = L.off_redss + kClusterMaxSplits * kRowsBM * 4;
     L.total = L.off_misc + 16 + 1024;
     return L;
 }
@@ -137,15 +145,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto srfull = [&](uint32_t b) { return bar0 + 8 * (3 * kRowsMaxStages + 4 + b); };
     const uint32_t mmadone = bar0 + 8 * (3 * kRowsMaxStages + 6);
     const uint32_t episync = bar0 + 8 * (3 * kRowsMaxStages + 7);
-    // split 0: every other split's partial rows have arrived; other splits:
-    // split 0 has consumed the partial rows this CTA pushed last
+    // redfull: the other splits' partials of the chunks this CTA owns (and
+    // their row sums of squares) have arrived; redempty: every other split
+    // has added up its chunks of the previous tile, so its slots may be
+    // written again
     const uint32_t redfull = bar0 + 8 * (3 * kRowsMaxStages + 8);
     const uint32_t redempty = bar0 + 8 * (3 * kRowsMaxStages + 9);
     float* sr = reinterpret_cast<float*>(smem + L.off_sr);         // [2][128] row sums of squares
     const uint32_t red_addr = sb + L.off_red, redss_addr = sb + L.off_redss;
-    const float* red = reinterpret_cast<const float*>(smem + L.off_red);      // [splits][MP][256]
     const float* redss = reinterpret_cast<const float*>(smem + L.off_redss);  // [splits][128]
-    float* rr = reinterpret_cast<float*>(smem + L.off_rr);                     // [128]
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.off_misc);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + L.off_misc + 4);
 
@@ -163,8 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(mmadone, 1);
         mbar_init(episync, 4);
-        mbar_init(redfull, split > 1 ? split - 1 : 1);   // one arrive per other split (+ bytes)
-        mbar_init(redempty, 1);
+        mbar_init(redfull, 1);                            // own expect_tx (+ the peers' bytes)
+        mbar_init(redempty, split > 1 ? split - 1 : 1);   // one arrive per other split
         *abort = 0;
         fence_mbar_init();
     }
@@ -371,88 +379,110 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(accempty(buf));
             } else {
-                // K split inside a cluster (one row tile, M <= 128).  Every
-                // split stages its partial rows (fp32, [row][256]) and row sums
-                // of squares in its own shared memory at slot = split index;
-                // splits 1.. then bulk-copy their slot into the same slot of
-                // split 0, which adds the slots in split order and writes Y.
-                if (rank != 0 && !warp_wait_cluster(redempty, (red_use & 1) ^ 1, abort)) break;
-                const uint32_t slot = red_addr + rank * a.MP * kRowsBN * 4;
-                const uint32_t ss_slot = redss_addr + rank * kRowsBM * 4;
-                for (int c = 0; warp_has_rows && c < kRowsBN / 32; ++c) {
+                // K split inside a cluster (one row tile, M <= 128), reduced by
+                // scatter.  Chunk c of 32 columns belongs to CTA c % splits.
+                // Every CTA sends its partial rows of the chunks it does not
+                // own from registers straight into the owner's shared memory
+                // (st.async, whose bytes complete on the owner's redfull),
+                // keeps its own chunks in its own slot, and sends its row sums
+                // of squares to every peer.  Each owner then adds the slots in
+                // split order (fixed, whatever the arrival order), scales by
+                // 1/rms and writes its chunks of Y.
+                const int nchunks = (ncols + 31) / 32;
+                const int omax = rows_owned_max(split);
+                const int owned = nchunks > static_cast<int>(rank)
+                                      ? (nchunks - 1 - static_cast<int>(rank)) / split + 1 : 0;
+                if (e == 0)
+                    mbar_arrive_expect_tx(redfull, static_cast<uint32_t>((split - 1) * rows_here * (4 + owned * 128)));
+                // the owners must have added up the previous tile's slots
+                if (!warp_wait_cluster(redempty, (red_use & 1) ^ 1, abort)) break;
+                const uint32_t swz = static_cast<uint32_t>(row & 7);
+                for (int c = 0; warp_has_rows && c < nchunks; ++c) {
                     uint32_t v[32];
                     tmem_ld_32x32(taddr + c * 32, v);
                     if (row < rows_here) {
-                        const uint32_t dst = slot + (row * kRowsBN + c * 32) * 4;
+                        const int owner = c % split;
+                        const uint32_t dst = red_addr + ((rank * omax + c / split) * a.MP + row) * 128;
+                        if (owner == static_cast<int>(rank)) {
 #pragma unroll
-                        for (int g = 0; g < 8; ++g)
-                            sts128(dst + g * 16, make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]));
+                            for (int g = 0; g < 8; ++g)
+                                sts128(dst + ((g ^ swz) << 4),
+                                       make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]));
+                        } else {
+                            const uint32_t rdst = mapa_shared(dst, owner);
+                            const uint32_t rbar = mapa_shared(redfull, owner);
+#pragma unroll
+                            for (int g = 0; g < 8; ++g)
+                                st_async_v4(rdst + ((g ^ swz) << 4),
+                                            make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]), rbar);
+                        }
                     }
                 }
-                if (row < rows_here)
-                    *reinterpret_cast<float*>(smem + (ss_slot - sb) + row * 4) =
-                        kFused ? sr[buf * kRowsBM + row] : 0.f;
+                if (row < rows_here) {
+                    const float ssv = kFused ? sr[buf * kRowsBM + row] : 0.f;
+                    const uint32_t dst = redss_addr + (rank * kRowsBM + row) * 4;
+                    *reinterpret_cast<float*>(smem + (dst - sb)) = ssv;
+                    for (int p = 0; p < split; ++p)
+                        if (p != static_cast<int>(rank))
+                            st_async_b32(mapa_shared(dst, p), __float_as_uint(ssv), mapa_shared(redfull, p));
+                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(accempty(buf));
-                const uint32_t part_bytes = static_cast<uint32_t>(rows_here) * kRowsBN * 4;
-                const uint32_t ss_bytes = ((static_cast<uint32_t>(rows_here) * 4 + 15) / 16) * 16;
-                if (rank != 0) {
-                    fence_proxy_async_smem();   // the bulk copy reads these writes
-                    if (!epi_sync()) break;
-                    if (e == 0) {
-                        const uint32_t bar = mapa_shared(redfull, 0);
-                        mbar_arrive_expect_tx_remote(bar, part_bytes + ss_bytes);
-                        bulk_copy_to_peer(mapa_shared(slot, 0), slot, part_bytes, bar);
-                        bulk_copy_to_peer(mapa_shared(ss_slot, 0), ss_slot, ss_bytes, bar);
-                    }
-                } else {
-                    if (!epi_sync()) break;   // own slot written
-                    if (!warp_wait_cluster(redfull, red_use & 1, abort)) break;
-                    if (e < rows_here) {
-                        float tot = 0.f;
-                        for (int s2 = 0; s2 < split; ++s2) tot += redss[s2 * kRowsBM + e];
-                        rr[e] = kFused ? rsqrtf(tot * inv_k + a.eps) : 1.f;
-                    }
-                    if (!epi_sync()) break;
-                    // thread e owns columns 2e, 2e+1; all splits' loads of a row
-                    // are issued together
-                    const int col = 2 * e;
-                    const size_t slot_stride = static_cast<size_t>(a.MP) * kRowsBN;
-                    const float2* red2 = reinterpret_cast<const float2*>(red);
-                    __nv_bfloat16* yb = Y + static_cast<size_t>(mb * kRowsBM) * a.N + n0 + col;
-#pragma unroll 2
-                    for (int m = 0; m < rows_here; ++m) {
-                        float2 pv[kClusterMaxSplits];
+                if (!warp_wait_cluster(redfull, red_use & 1, abort)) break;
+                if (row < rows_here) {
+                    float tot = 0.f;
+                    for (int s2 = 0; s2 < split; ++s2) tot += redss[s2 * kRowsBM + row];
+                    const float r = kFused ? rsqrtf(tot * inv_k + a.eps) : 1.f;
+                    __nv_bfloat16* yrow = Y + static_cast<size_t>(mb * kRowsBM + row) * a.N + n0;
+                    for (int j = 0; j < owned; ++j) {
+                        const int c = static_cast<int>(rank) + j * split;
+                        float acc[32];
 #pragma unroll
-                        for (int s2 = 0; s2 < kClusterMaxSplits; ++s2)
-                            if (s2 < split) pv[s2] = red2[(s2 * slot_stride + m * kRowsBN + col) / 2];
-                        float ax = 0.f, ay = 0.f;
+                        for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+                        for (int s2 = 0; s2 < split; ++s2) {
+                            const uint32_t src = red_addr + ((s2 * omax + j) * a.MP + row) * 128;
 #pragma unroll
-                        for (int s2 = 0; s2 < kClusterMaxSplits; ++s2)
-                            if (s2 < split) {
-                                ax += pv[s2].x;
-                                ay += pv[s2].y;
+                            for (int g = 0; g < 8; ++g) {
+                                const uint4 t4 = lds128(src + ((g ^ swz) << 4));
+                                acc[4 * g] += __uint_as_float(t4.x);
+                                acc[4 * g + 1] += __uint_as_float(t4.y);
+                                acc[4 * g + 2] += __uint_as_float(t4.z);
+                                acc[4 * g + 3] += __uint_as_float(t4.w);
                             }
-                        const float r = rr[m];
-                        if (col < ncols)
-                            *reinterpret_cast<uint32_t*>(yb + static_cast<size_t>(m) * a.N) =
-                                pack_bf16x2(ax * r, ay * r);
+                        }
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            const int col = c * 32 + g * 8;
+                            if (col < ncols) {
+                                uint4 o;
+                                o.x = pack_bf16x2(acc[8 * g] * r, acc[8 * g + 1] * r);
+                                o.y = pack_bf16x2(acc[8 * g + 2] * r, acc[8 * g + 3] * r);
+                                o.z = pack_bf16x2(acc[8 * g + 4] * r, acc[8 * g + 5] * r);
+                                o.w = pack_bf16x2(acc[8 * g + 6] * r, acc[8 * g + 7] * r);
+                                *reinterpret_cast<uint4*>(yrow + col) = o;
+                            }
+                        }
                     }
-                    // every thread of split 0 is done with the slots: hand them back
+                }
+                // the next tile's partials may overwrite the slots once every
+                // epilogue thread here is done with them
+                if (u + static_cast<int>(gridDim.x) < units) {
                     if (!epi_sync()) break;
                     if (e == 0)
-                        for (int s2 = 1; s2 < split; ++s2) mbar_arrive_remote(mapa_shared(redempty, s2));
+                        for (int p = 0; p < split; ++p)
+                            if (p != static_cast<int>(rank)) mbar_arrive_remote(mapa_shared(redempty, p));
                 }
                 ++red_use;
             }
         }
-        // split 0's last hand-back arrive must land before this CTA exits
-        if (kSplit && rank != 0 && red_use > 0) warp_wait_cluster(redempty, (red_use & 1) ^ 1, abort);
     }
 
     tc_fence_before();
     __syncthreads();
+    // peers may still be storing into this CTA's shared memory until every
+    // CTA of the cluster has received all its partials
+    if (kSplit) cluster_sync_all();
     if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem, kRowsTmemCols);

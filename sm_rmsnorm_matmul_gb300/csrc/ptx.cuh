@@ -159,6 +159,22 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t cluster_ad
                  "r"(bytes)
                  : "memory");
 }
+// Store 16 bytes (or 4) into another CTA's shared memory; the store completes
+// as many bytes of transaction count on `bar_cluster`, a barrier in the
+// destination CTA.  The destination must not be this CTA.
+__device__ __forceinline__ void st_async_v4(uint32_t dst_cluster, uint4 v, uint32_t bar_cluster) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1,%2,%3,%4}, [%5];" ::"r"(
+            dst_cluster),
+        "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar_cluster)
+        : "memory");
+}
+__device__ __forceinline__ void st_async_b32(uint32_t dst_cluster, uint32_t v, uint32_t bar_cluster) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+                     dst_cluster),
+                 "r"(v), "r"(bar_cluster)
+                 : "memory");
+}
 // Copy `bytes` (multiple of 16, 16-byte aligned ends) from this CTA's shared
 // memory to another CTA's of the cluster; completes `bytes` of transaction
 // count on `bar` (an address in the destination CTA).
@@ -178,8 +194,9 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {
 __device__ __forceinline__ void fence_acq_rel_cluster() {
     asm volatile("fence.acq_rel.cluster;" ::: "memory");
 }
-// All threads of all CTAs of the cluster (used once, right after start-up,
-// when every CTA of the cluster is resident by construction).
+// All threads of all CTAs of the cluster (right after start-up, when every
+// CTA of the cluster is resident by construction, and before exit, so that no
+// CTA leaves while a peer may still write into its shared memory).
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
                      "memory");
