@@ -363,6 +363,8 @@ RowsPlan plan_rows(int dev, bool fused, int64_t M, int64_t K, int64_t N, const D
             if (resident <= 0) continue;
         }
         const long units = static_cast<long>(p.n_tiles) * s;
+        // a K split runs one (tile, split) unit per CTA, all resident at once
+        if (s > 1 && units > resident) continue;
         const long waves = (units + resident - 1) / resident;
         const double per_cta = static_cast<double>(waves) * kbps * rmm::kRowsBN * kBK * 2 / 55e9;
         const double cost = std::max(per_cta, w_total / 6.0e12) * 1e6 + waves * 1.0 + (s > 1 ? 1.5 : 0.5);

@@ -89,7 +89,7 @@ __device__ __forceinline__ uint4 gain8(uint4 xv, uint4 gv, float& ss) {
 }
 
 struct RowsLayout {
-    uint32_t xbytes, off_x, off_w, off_g, off_red, off_bar, off_sr, off_redss, off_misc, total;
+    uint32_t xbytes, off_x, off_w, off_g, off_red, red_block, off_bar, off_sr, off_misc, total;
 };
 
 // Column chunks of 32 in a row tile; with a cluster K split of S, chunk c is
@@ -103,9 +103,10 @@ __host__ __device__ inline int rows_owned_max(int splits) {
 // (128, or M rounded up to 16 when one row tile covers M).  X tiles come
 // first: the MMA always reads a 128-row window from an X tile, whose rows
 // past xrows (discarded results) fall on the following tiles.  red_slots:
-// with a cluster K split of S = red_slots, each CTA receives, for the chunks
-// it owns, every split's partial rows as [S][ceil(8/S)][MP][32] fp32 (the
-// 16-byte pieces of a row rotated by row & 7 against bank conflicts).
+// with a cluster K split of S = red_slots, each CTA receives one block per
+// split, [MP] fp32 row sums of squares followed by [ceil(8/S)][MP][32] fp32
+// partial rows of the chunks it owns (the 16-byte pieces of a row rotated by
+// row & 7 against bank conflicts).
 __host__ __device__ inline RowsLayout rows_layout(int xrows, int stages, int red_slots, int MP) {
     RowsLayout L;
     L.xbytes = xrows * kBK * 2;
@@ -113,15 +114,15 @@ __host__ __device__ inline RowsLayout rows_layout(int xrows, int stages, int red
     L.off_w = ((stages * L.xbytes + 1023) / 1024) * 1024;
     L.off_g = L.off_w + stages * kRowsWBytes;
     L.off_red = ((L.off_g + stages * kGBytes + 15) / 16) * 16;
-    const uint32_t red_bytes = red_slots > 0 ? red_slots * rows_owned_max(red_slots) * MP * 128 : 0;
-    L.off_bar = L.off_red + red_bytes;
+    L.red_block = red_slots > 0 ? MP * (4 + rows_owned_max(red_slots) * 128) : 0;
+    L.off_bar = L.off_red + red_slots * L.red_block;
     const uint32_t nbars = 3 * kRowsMaxStages + 10;
     L.off_sr = L.off_bar + ((nbars * 8 + 15) / 16) * 16;
-    L.off_redss = L.off_sr + 2 * kRowsBM * 4;
-    L.off_misc = L.off_redss + kClusterMaxSplits * kRowsBM * 4;
+    L.off_misc = L.off_sr + 2 * kRowsBM * 4;
     L.total = L.off_misc + 16 + 1024;
     return L;
 }
+
 
 template <bool kFused, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -144,16 +145,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto accempty = [&](uint32_t b) { return bar0 + 8 * (3 * kRowsMaxStages + 2 + b); };
     auto srfull = [&](uint32_t b) { return bar0 + 8 * (3 * kRowsMaxStages + 4 + b); };
     const uint32_t mmadone = bar0 + 8 * (3 * kRowsMaxStages + 6);
-    const uint32_t episync = bar0 + 8 * (3 * kRowsMaxStages + 7);
-    // redfull: the other splits' partials of the chunks this CTA owns (and
-    // their row sums of squares) have arrived; redempty: every other split
-    // has added up its chunks of the previous tile, so its slots may be
-    // written again
+    // the other splits' blocks (partials of the chunks this CTA owns, row
+    // sums of squares) have arrived
     const uint32_t redfull = bar0 + 8 * (3 * kRowsMaxStages + 8);
-    const uint32_t redempty = bar0 + 8 * (3 * kRowsMaxStages + 9);
     float* sr = reinterpret_cast<float*>(smem + L.off_sr);         // [2][128] row sums of squares
-    const uint32_t red_addr = sb + L.off_red, redss_addr = sb + L.off_redss;
-    const float* redss = reinterpret_cast<const float*>(smem + L.off_redss);  // [splits][128]
+    const uint32_t red_addr = sb + L.off_red;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.off_misc);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + L.off_misc + 4);
 
@@ -170,9 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(srfull(b), 4);    // one elected lane per transform warp
         }
         mbar_init(mmadone, 1);
-        mbar_init(episync, 4);
-        mbar_init(redfull, 1);                            // own expect_tx (+ the peers' bytes)
-        mbar_init(redempty, split > 1 ? split - 1 : 1);   // one arrive per other split
+        mbar_init(redfull, 1);   // own expect_tx (+ the peers' bytes)
         *abort = 0;
         fence_mbar_init();
     }
@@ -188,16 +182,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // peers' barriers must be initialised before the first remote arrive
-    if (kSplit) cluster_sync_all();
+    // peers' barriers must be initialised before the first remote access:
+    // announce it here, wait for the peers just before that access
+    if (kSplit) cluster_arrive();
     // Set-up above overlaps the previous kernel on the stream; its writes are
     // visible after grid_dep_wait().  The next kernel may then be scheduled.
     grid_dep_wait();
     if (threadIdx.x == 0) grid_dep_launch();
     const uint32_t tmem = *tmem_holder;
     // units = (tile, K split); with a cluster, blockIdx.x = cluster * splits +
-    // rank and the splits of one tile are the CTAs of one cluster
-    const int units = a.m_tiles * a.n_tiles * split;
+    // rank and the splits of one tile are the CTAs of one cluster, one unit
+    // per CTA (a launch that breaks this does no work and reports an
+    // internal error)
+    int units = a.m_tiles * a.n_tiles * split;
+    if (kSplit && units > static_cast<int>(gridDim.x)) {
+        if (threadIdx.x == 0) atomicCAS(&g_status, 0, kStatusInternal);
+        units = 0;
+    }
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -320,169 +321,176 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(srfull(buf));
             }
         }
-    } else if (warp >= 8) {
+    } else if (warp >= 8 && !kSplit) {
         // ------------------------------------------------ epilogue
         const int q = warp & 3;             // tensor-memory lane quarter of this warp
         const int row = q * 32 + lane;
-        const int e = threadIdx.x - 256;
         const float inv_k = 1.f / static_cast<float>(a.K);
-        uint32_t ep = 0;
-        auto epi_sync = [&]() {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(episync);
-            return warp_wait(episync, (ep++) & 1, abort);
-        };
-        const uint32_t rank = kSplit ? cluster_ctarank() : 0;
-        uint32_t red_use = 0;
         uint32_t tl = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++tl) {
-            const int t = u / split;
             const uint32_t buf = tl & 1, use = tl >> 1;
             if (!warp_wait(accfull(buf), use & 1, abort)) break;
             if (kFused && !warp_wait(srfull(buf), use & 1, abort)) break;
             tc_fence_after();
             int mb, nb;
-            rows_tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
+            rows_tile_coords(u, a.m_tiles, a.n_tiles, mb, nb);
             const int n0 = nb * kRowsBN;
             const int ncols = min(kRowsBN, a.N - n0);
             const int rows_here = min(kRowsBM, a.M - mb * kRowsBM);   // valid rows of this tile
             const uint32_t taddr = tmem + buf * kRowsBN + (static_cast<uint32_t>(q * 32) << 16);
             const bool warp_has_rows = q * 32 < rows_here;              // warp-uniform
-            if (!kSplit) {
-                const int m = mb * kRowsBM + row;
-                const float r = kFused ? rsqrtf(sr[buf * kRowsBM + row] * inv_k + a.eps) : 1.f;
-                __nv_bfloat16* yrow = Y + static_cast<size_t>(m) * a.N + n0;
-                for (int c = 0; warp_has_rows && c < kRowsBN / 32; ++c) {
-                    if (c * 32 >= ncols) break;   // warp-uniform
-                    uint32_t v[32];
-                    tmem_ld_32x32(taddr + c * 32, v);
-                    if (row < rows_here) {
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            const int col = c * 32 + g * 8;
-                            if (col < ncols) {
-                                uint4 o;
-                                o.x = pack_bf16x2(__uint_as_float(v[g * 8 + 0]) * r,
-                                                  __uint_as_float(v[g * 8 + 1]) * r);
-                                o.y = pack_bf16x2(__uint_as_float(v[g * 8 + 2]) * r,
-                                                  __uint_as_float(v[g * 8 + 3]) * r);
-                                o.z = pack_bf16x2(__uint_as_float(v[g * 8 + 4]) * r,
-                                                  __uint_as_float(v[g * 8 + 5]) * r);
-                                o.w = pack_bf16x2(__uint_as_float(v[g * 8 + 6]) * r,
-                                                  __uint_as_float(v[g * 8 + 7]) * r);
-                                *reinterpret_cast<uint4*>(yrow + col) = o;
-                            }
-                        }
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(accempty(buf));
-            } else {
-                // K split inside a cluster (one row tile, M <= 128), reduced by
-                // scatter.  Chunk c of 32 columns belongs to CTA c % splits.
-                // Every CTA sends its partial rows of the chunks it does not
-                // own from registers straight into the owner's shared memory
-                // (st.async, whose bytes complete on the owner's redfull),
-                // keeps its own chunks in its own slot, and sends its row sums
-                // of squares to every peer.  Each owner then adds the slots in
-                // split order (fixed, whatever the arrival order), scales by
-                // 1/rms and writes its chunks of Y.
-                const int nchunks = (ncols + 31) / 32;
-                const int omax = rows_owned_max(split);
-                const int owned = nchunks > static_cast<int>(rank)
-                                      ? (nchunks - 1 - static_cast<int>(rank)) / split + 1 : 0;
-                if (e == 0)
-                    mbar_arrive_expect_tx(redfull, static_cast<uint32_t>((split - 1) * rows_here * (4 + owned * 128)));
-                // the owners must have added up the previous tile's slots
-                if (!warp_wait_cluster(redempty, (red_use & 1) ^ 1, abort)) break;
-                const uint32_t swz = static_cast<uint32_t>(row & 7);
-                for (int c = 0; warp_has_rows && c < nchunks; ++c) {
-                    uint32_t v[32];
-                    tmem_ld_32x32(taddr + c * 32, v);
-                    if (row < rows_here) {
-                        const int owner = c % split;
-                        const uint32_t dst = red_addr + ((rank * omax + c / split) * a.MP + row) * 128;
-                        if (owner == static_cast<int>(rank)) {
-#pragma unroll
-                            for (int g = 0; g < 8; ++g)
-                                sts128(dst + ((g ^ swz) << 4),
-                                       make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]));
-                        } else {
-                            const uint32_t rdst = mapa_shared(dst, owner);
-                            const uint32_t rbar = mapa_shared(redfull, owner);
-#pragma unroll
-                            for (int g = 0; g < 8; ++g)
-                                st_async_v4(rdst + ((g ^ swz) << 4),
-                                            make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]), rbar);
-                        }
-                    }
-                }
+            const int m = mb * kRowsBM + row;
+            const float r = kFused ? rsqrtf(sr[buf * kRowsBM + row] * inv_k + a.eps) : 1.f;
+            __nv_bfloat16* yrow = Y + static_cast<size_t>(m) * a.N + n0;
+            for (int c = 0; warp_has_rows && c < kRowsBN / 32; ++c) {
+                if (c * 32 >= ncols) break;   // warp-uniform
+                uint32_t v[32];
+                tmem_ld_32x32(taddr + c * 32, v);
                 if (row < rows_here) {
-                    const float ssv = kFused ? sr[buf * kRowsBM + row] : 0.f;
-                    const uint32_t dst = redss_addr + (rank * kRowsBM + row) * 4;
-                    *reinterpret_cast<float*>(smem + (dst - sb)) = ssv;
-                    for (int p = 0; p < split; ++p)
-                        if (p != static_cast<int>(rank))
-                            st_async_b32(mapa_shared(dst, p), __float_as_uint(ssv), mapa_shared(redfull, p));
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(accempty(buf));
-                if (!warp_wait_cluster(redfull, red_use & 1, abort)) break;
-                if (row < rows_here) {
-                    float tot = 0.f;
-                    for (int s2 = 0; s2 < split; ++s2) tot += redss[s2 * kRowsBM + row];
-                    const float r = kFused ? rsqrtf(tot * inv_k + a.eps) : 1.f;
-                    __nv_bfloat16* yrow = Y + static_cast<size_t>(mb * kRowsBM + row) * a.N + n0;
-                    for (int j = 0; j < owned; ++j) {
-                        const int c = static_cast<int>(rank) + j * split;
-                        float acc[32];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-                        for (int s2 = 0; s2 < split; ++s2) {
-                            const uint32_t src = red_addr + ((s2 * omax + j) * a.MP + row) * 128;
-#pragma unroll
-                            for (int g = 0; g < 8; ++g) {
-                                const uint4 t4 = lds128(src + ((g ^ swz) << 4));
-                                acc[4 * g] += __uint_as_float(t4.x);
-                                acc[4 * g + 1] += __uint_as_float(t4.y);
-                                acc[4 * g + 2] += __uint_as_float(t4.z);
-                                acc[4 * g + 3] += __uint_as_float(t4.w);
-                            }
-                        }
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            const int col = c * 32 + g * 8;
-                            if (col < ncols) {
-                                uint4 o;
-                                o.x = pack_bf16x2(acc[8 * g] * r, acc[8 * g + 1] * r);
-                                o.y = pack_bf16x2(acc[8 * g + 2] * r, acc[8 * g + 3] * r);
-                                o.z = pack_bf16x2(acc[8 * g + 4] * r, acc[8 * g + 5] * r);
-                                o.w = pack_bf16x2(acc[8 * g + 6] * r, acc[8 * g + 7] * r);
-                                *reinterpret_cast<uint4*>(yrow + col) = o;
-                            }
+                    for (int g = 0; g < 4; ++g) {
+                        const int col = c * 32 + g * 8;
+                        if (col < ncols) {
+                            uint4 o;
+                            o.x = pack_bf16x2(__uint_as_float(v[g * 8 + 0]) * r,
+                                              __uint_as_float(v[g * 8 + 1]) * r);
+                            o.y = pack_bf16x2(__uint_as_float(v[g * 8 + 2]) * r,
+                                              __uint_as_float(v[g * 8 + 3]) * r);
+                            o.z = pack_bf16x2(__uint_as_float(v[g * 8 + 4]) * r,
+                                              __uint_as_float(v[g * 8 + 5]) * r);
+                            o.w = pack_bf16x2(__uint_as_float(v[g * 8 + 6]) * r,
+                                              __uint_as_float(v[g * 8 + 7]) * r);
+                            *reinterpret_cast<uint4*>(yrow + col) = o;
                         }
                     }
                 }
-                // the next tile's partials may overwrite the slots once every
-                // epilogue thread here is done with them
-                if (u + static_cast<int>(gridDim.x) < units) {
-                    if (!epi_sync()) break;
-                    if (e == 0)
-                        for (int p = 0; p < split; ++p)
-                            if (p != static_cast<int>(rank)) mbar_arrive_remote(mapa_shared(redempty, p));
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(accempty(buf));
+        }
+    }
+
+    if (kSplit) {
+        // ---------------------------------------- K split: reduce by scatter
+        // One (tile, split) unit per CTA, one row tile (M <= 128); the K
+        // splits of the tile are the CTAs of this cluster.  Chunk c of 32
+        // columns belongs to CTA c % splits.  Every warp takes part:
+        //  1. the warps of each tensor-memory lane quarter that holds rows
+        //     (three per quarter, taking every third chunk) read the
+        //     accumulator and store each chunk straight from registers into
+        //     its owner's receive block for this split (st.async; the bytes
+        //     complete on the owner's redfull) or, for their own chunks, into
+        //     their own block; with it go the row sums of squares;
+        //  2. once every split's block has arrived, all threads add the
+        //     blocks in split order (fixed, whatever the arrival order),
+        //     scale by 1/rms and write this CTA's chunks of Y.
+        // The 16-byte pieces of a row are rotated by row & 7 in the blocks,
+        // against bank conflicts.  The cluster barrier's second phase is
+        // entered once this CTA's blocks have all arrived (nothing is stored
+        // into it after that) and left before exit, so that no CTA leaves
+        // while its stores to a peer are in flight.
+        __syncwarp();
+        const int u = blockIdx.x;
+        const bool have = u < units;
+        const uint32_t rank = cluster_ctarank();
+        const int me = static_cast<int>(rank);
+        int mb = 0, nb = 0;
+        if (have) rows_tile_coords(u / split, a.m_tiles, a.n_tiles, mb, nb);
+        const int n0 = nb * kRowsBN;
+        const int ncols = min(kRowsBN, a.N - n0);
+        const int rows_here = min(kRowsBM, a.M - mb * kRowsBM);
+        const int nchunks = (ncols + 31) / 32;
+        const int owned = nchunks > me ? (nchunks - 1 - me) / split + 1 : 0;
+        const uint32_t blk = L.red_block;
+        const uint32_t my_block = red_addr + rank * blk;   // this split's block in every CTA
+        const int q = warp & 3, team = warp >> 2;
+        const int row = q * 32 + lane;
+        if (have && threadIdx.x == 0)
+            mbar_arrive_expect_tx(redfull, static_cast<uint32_t>((split - 1) * rows_here * (4 + owned * 128)));
+        cluster_wait();    // the peers' barriers are initialised
+        // 1. tensor memory -> owners
+        if (have && q * 32 < rows_here &&
+            warp_wait(accfull(0), 0, abort) && (!kFused || warp_wait(srfull(0), 0, abort))) {
+            tc_fence_after();
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+            const uint32_t swz = static_cast<uint32_t>(row & 7);
+            for (int c = team; c < nchunks; c += kThreads / 128) {
+                uint32_t v[32];
+                tmem_ld_32x32(taddr + c * 32, v);
+                if (row < rows_here) {
+                    const int owner = c % split;
+                    const uint32_t dst = my_block + a.MP * 4 + ((c / split) * a.MP + row) * 128;
+                    if (owner == me) {
+#pragma unroll
+                        for (int g = 0; g < 8; ++g)
+                            sts128(dst + ((g ^ swz) << 4),
+                                   make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]));
+                    } else {
+                        const uint32_t rdst = mapa_shared(dst, owner);
+                        const uint32_t rbar = mapa_shared(redfull, owner);
+#pragma unroll
+                        for (int g = 0; g < 8; ++g)
+                            st_async_v4(rdst + ((g ^ swz) << 4),
+                                        make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]), rbar);
+                    }
                 }
-                ++red_use;
+            }
+            if (team == 0 && row < rows_here) {
+                const float ssv = kFused ? sr[row] : 0.f;
+                const uint32_t dst = my_block + row * 4;
+                *reinterpret_cast<float*>(smem + (dst - sb)) = ssv;
+                for (int p = 0; p < split; ++p)
+                    if (p != me) st_async_b32(mapa_shared(dst, p), __float_as_uint(ssv), mapa_shared(redfull, p));
+            }
+        }
+        // 2. sum once every block has arrived (this CTA's own block: after
+        // the barrier below)
+        const bool ok = have && warp_wait_cluster(redfull, 0, abort);
+        cluster_arrive();
+        __syncthreads();
+        if (ok && !*abort) {
+            const float inv_k = 1.f / static_cast<float>(a.K);
+            const int n3 = rows_here * owned * 8;
+            for (int i = threadIdx.x; i < n3; i += kThreads) {
+                const int g = i & 7, j = (i >> 3) % owned, rr = (i >> 3) / owned;
+                const uint32_t piece = static_cast<uint32_t>((g ^ (rr & 7)) << 4);
+                // every split's piece and row sum in flight before the first add
+                float ssv[kClusterMaxSplits];
+                uint4 t4[kClusterMaxSplits];
+#pragma unroll
+                for (int s2 = 0; s2 < kClusterMaxSplits; ++s2)
+                    if (s2 < split) {
+                        ssv[s2] = *reinterpret_cast<const float*>(smem + L.off_red + s2 * blk + rr * 4);
+                        t4[s2] = lds128(red_addr + s2 * blk + a.MP * 4 + (j * a.MP + rr) * 128 + piece);
+                    }
+                float tot = 0.f;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int s2 = 0; s2 < kClusterMaxSplits; ++s2)
+                    if (s2 < split) {
+                        tot += ssv[s2];
+                        acc.x += __uint_as_float(t4[s2].x);
+                        acc.y += __uint_as_float(t4[s2].y);
+                        acc.z += __uint_as_float(t4[s2].z);
+                        acc.w += __uint_as_float(t4[s2].w);
+                    }
+                const float r = kFused ? rsqrtf(tot * inv_k + a.eps) : 1.f;
+                const int col = (me + j * split) * 32 + g * 4;
+                if (col < ncols) {
+                    uint2 o;
+                    o.x = pack_bf16x2(acc.x * r, acc.y * r);
+                    o.y = pack_bf16x2(acc.z * r, acc.w * r);
+                    *reinterpret_cast<uint2*>(Y + static_cast<size_t>(mb * kRowsBM + rr) * a.N + n0 + col) = o;
+                }
             }
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    // peers may still be storing into this CTA's shared memory until every
-    // CTA of the cluster has received all its partials
-    if (kSplit) cluster_sync_all();
+    // every CTA of the cluster has received all its blocks (the arrive above)
+    if (kSplit) cluster_wait();
     if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem, kRowsTmemCols);

@@ -41,7 +41,8 @@ struct RowsLaunch {
     int M, N, K;
     float eps;
     int m_tiles, n_tiles, k_blocks;
-    int splits, kb_per_split;  // K split of each tile (splits > 1 needs m_tiles == 1)
+    int splits, kb_per_split;  // K split of each tile (splits > 1 needs m_tiles == 1
+                               // and one (tile, split) unit per CTA)
     int cluster;               // 1: the splits of a tile form a cluster
     int xrows, MP, stages;
     int grid;
