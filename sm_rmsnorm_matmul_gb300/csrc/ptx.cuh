@@ -152,14 +152,6 @@ __device__ __forceinline__ void st_dsmem_v4(uint32_t cluster_addr, uint4 v) {
                  "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
 }
-// arrive on a (possibly remote) barrier and raise its expected transaction
-// bytes, release semantics at cluster scope
-__device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t cluster_addr, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
-                     cluster_addr),
-                 "r"(bytes)
-                 : "memory");
-}
 // Store 16 bytes (or 4) into another CTA's shared memory; the store completes
 // as many bytes of transaction count on `bar_cluster`, a barrier in the
 // destination CTA.  The destination must not be this CTA.
@@ -175,17 +167,6 @@ __device__ __forceinline__ void st_async_b32(uint32_t dst_cluster, uint32_t v, u
                      dst_cluster),
                  "r"(v), "r"(bar_cluster)
                  : "memory");
-}
-// Copy `bytes` (multiple of 16, 16-byte aligned ends) from this CTA's shared
-// memory to another CTA's of the cluster; completes `bytes` of transaction
-// count on `bar` (an address in the destination CTA).
-__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
-                                                  uint32_t bar_cluster) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            dst_cluster),
-        "r"(src), "r"(bytes), "r"(bar_cluster)
-        : "memory");
 }
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {
     float v;
@@ -370,29 +351,6 @@ __device__ __forceinline__ void tmem_ld_32x32(uint32_t taddr, uint32_t (&v)[32])
           "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
           "=r"(v[31])
         : "r"(taddr)
-        : "memory");
-}
-
-// Two 32-column loads issued back to back and one wait: 32 lanes x 64
-// consecutive 32-bit columns (the load latency is paid once).
-__device__ __forceinline__ void tmem_ld_32x64(uint32_t taddr, uint32_t (&v)[64]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-          "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]),
-          "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]),
-          "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31]), "=r"(v[32]), "=r"(v[33]), "=r"(v[34]),
-          "=r"(v[35]), "=r"(v[36]), "=r"(v[37]), "=r"(v[38]), "=r"(v[39]), "=r"(v[40]), "=r"(v[41]),
-          "=r"(v[42]), "=r"(v[43]), "=r"(v[44]), "=r"(v[45]), "=r"(v[46]), "=r"(v[47]), "=r"(v[48]),
-          "=r"(v[49]), "=r"(v[50]), "=r"(v[51]), "=r"(v[52]), "=r"(v[53]), "=r"(v[54]), "=r"(v[55]),
-          "=r"(v[56]), "=r"(v[57]), "=r"(v[58]), "=r"(v[59]), "=r"(v[60]), "=r"(v[61]), "=r"(v[62]),
-          "=r"(v[63])
-        : "r"(taddr), "r"(taddr + 32)
         : "memory");
 }
 
