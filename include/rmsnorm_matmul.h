@@ -70,10 +70,16 @@ typedef enum {
  * X*g and the row sum of squares computed in the same pass as the
  * contraction, r[m] applied in the epilogue.  For M <= 128 the K range may be
  * split over up to 8 CTAs of a thread-block cluster whose partial sums are
- * combined in shared memory, in a fixed order.  With rmm_force_path(2) the
- * operand-swapped small-M kernel runs instead; its K split may use a
- * library-owned fp32 workspace per (device, stream), allocated on first use
- * (make that first call outside any CUDA-graph capture).
+ * combined in shared memory, in a fixed order.  For more row tiles, when the
+ * tiles leave a last wave of CTAs at most half full, those last tiles are cut
+ * along K, one piece per CTA, and the pieces are combined, in a fixed order,
+ * through a library-owned fp32 workspace per (device, stream); the pieces of
+ * a tile wait for one another, so every CTA of the launch must be able to be
+ * resident at once (one per SM, which the grid size guarantees on a device
+ * not shared with other work).  With rmm_force_path(2) the operand-swapped
+ * small-M kernel runs instead; its K split may use the same workspace.  The
+ * workspace is allocated on first use of a shape that needs it (make that
+ * first call outside any CUDA-graph capture).
  * Returns an rmm_status.
  */
 int rmsnorm_matmul(const void* X, const void* g, const void* W, void* Y,
@@ -109,8 +115,11 @@ int rmm_force_path(int path);
  * Synchronises `stream`, then returns and clears the current device's
  * in-kernel status word: RMM_OK, or RMM_ERR_DEVICE_TIMEOUT if a bounded wait
  * inside a kernel gave up (that kernel then skipped its remaining work and
- * released its tensor memory).  RMM_ERR_LAUNCH if the synchronisation itself
- * failed.
+ * released its tensor memory), or RMM_ERR_INTERNAL if a kernel was launched
+ * with a configuration it does not support.  On either, the arrival counters
+ * of every workspace of the current device are cleared (synchronously), since
+ * a kernel that gave up may have left them set.  RMM_ERR_LAUNCH if the
+ * synchronisation itself failed.
  */
 int rmm_device_status(cudaStream_t stream);
 

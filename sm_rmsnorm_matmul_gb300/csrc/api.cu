@@ -206,6 +206,21 @@ int get_workspace(int dev, cudaStream_t s, size_t acc_bytes, size_t ss_bytes, si
     return RMM_OK;
 }
 
+// Zeroes the arrival counters of every workspace of the current device, after
+// a kernel that gave up may have left some of them set.  Synchronous.
+cudaError_t clear_workspace_counters() {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    for (auto& kv : g_ws) {
+        if (kv.first.first != dev || !kv.second.counters) continue;
+        e = cudaMemset(kv.second.counters, 0, kv.second.n_counters * sizeof(int));
+        if (e != cudaSuccess) return e;
+    }
+    return cudaDeviceSynchronize();
+}
+
 // ---------------------------------------------------------------- planning
 struct ColsPlan {
     int MP, n_tiles, k_blocks, splits, kb_per_split, stages, grid, cluster;
@@ -393,8 +408,9 @@ int choose_path(int64_t M) {
 }
 
 // One launch of the tensor-core contraction, fused (RMSNorm folded in) or not.
+// Without may_allocate, plans that need the per-stream workspace are avoided.
 int run_contraction(bool fused, const void* X, const void* g, const void* W, void* Y, int64_t M,
-                    int64_t K, int64_t N, float eps, cudaStream_t stream) {
+                    int64_t K, int64_t N, float eps, cudaStream_t stream, bool may_allocate = true) {
     int dev = 0;
     DeviceInfo d;
     int rc = current_device(&dev, &d);
@@ -456,9 +472,34 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
     a.stages = p.stages;
     a.grid = p.grid;
     CUtensorMap tmY;
+    a.tail_tiles = 0;
+    a.tail_pieces = 1;
+    a.tail_kbp = p.k_blocks;
     if (fused && !p.cluster && p.xrows == rmm::kRowsBM) {
         if (!map_2d_store(&tmY, Y, M, N)) return RMM_ERR_INTERNAL;
         a.tmY = &tmY;
+        // When the tiles leave a last wave at most half full, cut those tiles
+        // along K so that every CTA has a share of them.
+        const int tiles = p.m_tiles * p.n_tiles;
+        const int rem = tiles % p.grid;
+        if (may_allocate && tiles > p.grid && rem > 0 && 2 * rem <= p.grid && p.k_blocks >= 2) {
+            const int pmax = p.grid / rem;
+            const int kbp = (p.k_blocks + pmax - 1) / pmax;
+            const int pieces = (p.k_blocks + kbp - 1) / kbp;
+            if (pieces >= 2) {
+                Workspace w;
+                const size_t units = static_cast<size_t>(rem) * pieces;
+                rc = get_workspace(dev, stream, units * rmm::kRowsBM * rmm::kRowsBN * sizeof(float),
+                                   units * rmm::kRowsBM * sizeof(float), static_cast<size_t>(rem) * 2, &w);
+                if (rc != RMM_OK) return rc;
+                a.tail_tiles = rem;
+                a.tail_pieces = pieces;
+                a.tail_kbp = kbp;
+                a.ws_acc = w.acc;
+                a.ws_ss = w.ss;
+                a.ws_count = w.counters;
+            }
+        }
     }
     return rmm::launch_rows(fused, tmX, tmW, tmG, Y, a, stream) == cudaSuccess ? RMM_OK
                                                                               : RMM_ERR_LAUNCH;
@@ -556,6 +597,7 @@ int rmm_device_status(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return RMM_ERR_LAUNCH;
     int v = 0;
     if (rmm::read_and_clear_status(&v) != cudaSuccess) return RMM_ERR_LAUNCH;
+    if (v != RMM_OK && clear_workspace_counters() != cudaSuccess) return RMM_ERR_LAUNCH;
     return v;
 }
 
@@ -635,10 +677,10 @@ extern "C" int rmsnorm_matmul_noalloc(const void* X, const void* g, const void* 
     rc = current_device(&dev, &d);
     if (rc != RMM_OK) return rc;
     // The row-tile path and an unsplit small-M launch use no scratch at all.
-    if (choose_path(M) == kPathRows) return run_contraction(true, X, g, W, Y, M, K, N, eps, stream);
+    if (choose_path(M) == kPathRows) return run_contraction(true, X, g, W, Y, M, K, N, eps, stream, false);
     if (M > rmm::kColsMaxMP) return RMM_ERR_INVALID_ARG;
     const ColsPlan p = plan_cols(dev, true, M, K, N, d, false);
-    if (p.splits == 1) return run_contraction(true, X, g, W, Y, M, K, N, eps, stream);
+    if (p.splits == 1) return run_contraction(true, X, g, W, Y, M, K, N, eps, stream, false);
 
     const size_t acc_bytes = static_cast<size_t>(p.splits) * M * N * sizeof(float);
     const size_t ss_bytes = static_cast<size_t>(p.n_tiles) * p.splits * rmm::kColsMaxMP * sizeof(float);

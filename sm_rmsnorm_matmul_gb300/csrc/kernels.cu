@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Tensor memory: columns [0, 256) hold the accumulator (single buffer; the
 // epilogue holds it only while it reads it out), [256, 512) eight A slots of
 // 32 columns (128 rows x 64 bf16 each).
-constexpr int kTaXStages = 3;
+constexpr int kTaXStages = 4;
 constexpr int kTaWStages = 4;
 constexpr int kTaAStages = 8;
 constexpr uint32_t kTaXBytes = kRowsBM * kBK * 2;    // 16 KB
@@ -523,14 +523,41 @@ constexpr uint32_t kTaOffBar = kTaOffG + kTaXStages * kGBytes;
 // mmadone, episync
 constexpr uint32_t kTaNumBars = 2 * kTaXStages + 2 * kTaWStages + 2 * kTaAStages + 8;
 constexpr uint32_t kTaOffSr = kTaOffBar + ((kTaNumBars * 8 + 15) / 16) * 16;
-constexpr uint32_t kTaOffMisc = kTaOffSr + 2 * kRowsBM * 4;
+constexpr uint32_t kTaOffRr = kTaOffSr + 2 * kRowsBM * 4;    // 1/rms of a piece's rows
+constexpr uint32_t kTaOffMisc = kTaOffRr + kRowsBM * 4;
 constexpr uint32_t kTaSmem = kTaOffMisc + 16 + 1024;
 constexpr uint32_t kTaAccCol = 0, kTaACol = 256;
+
+// Work of CTA b of G in rows_ta_kernel, in order: whole tiles b, b + G, ...
+// below full = tiles - tail_tiles; then, if b < tail_tiles * tail_pieces, K
+// piece b % tail_pieces of tail tile b / tail_pieces (tile full + that).
+struct TaUnit {
+    int t, kb0, kb1, piece;   // piece < 0: the whole K range
+};
+__device__ __forceinline__ bool ta_unit(const RowsLaunch& a, int i, TaUnit& u) {
+    const int G = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+    const int full = a.m_tiles * a.n_tiles - a.tail_tiles;
+    const int t = b + i * G;
+    if (t < full) {
+        u.t = t;
+        u.kb0 = 0;
+        u.kb1 = a.k_blocks;
+        u.piece = -1;
+        return true;
+    }
+    const int whole = b < full ? (full - b + G - 1) / G : 0;
+    if (i != whole || b >= a.tail_tiles * a.tail_pieces) return false;
+    u.piece = b % a.tail_pieces;
+    u.t = full + b / a.tail_pieces;
+    u.kb0 = u.piece * a.tail_kbp;
+    u.kb1 = min(a.k_blocks, u.kb0 + a.tail_kbp);
+    return true;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     rows_ta_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmY,
-                   RowsLaunch a) {
+                   __nv_bfloat16* __restrict__ Y, RowsLaunch a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     const uint32_t sb = smem_u32(smem);
@@ -599,40 +626,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_holder;
     const int num_tiles = a.m_tiles * a.n_tiles;
 
-    if (warp == 0) {
-        // ------------------------------------------------ TMA producer
+    if (warp == 0 || warp == 3) {
+        // ------------------------------------------------ TMA producers
+        // Two threads, so that X (released as soon as it is in tensor memory)
+        // runs ahead on its own ring instead of behind the W ring: warp 0
+        // loads W, warp 3 loads X and g.
         if (lane == 0) {
-            Ring xr(kTaXStages), wr(kTaWStages);
-            uint32_t xi = 0, wi = 0;
+            const bool load_x = warp == 3;
+            Ring ring(load_x ? kTaXStages : kTaWStages);
+            uint32_t issued = 0;
+            const uint32_t full0 = load_x ? xfull0 : wfull0, empty0 = load_x ? xempty0 : wempty0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+            TaUnit un;
+            for (int i = 0; ok && ta_unit(a, i, un); ++i) {
                 int mb, nb;
-                rows_tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
+                rows_tile_coords(un.t, a.m_tiles, a.n_tiles, mb, nb);
                 const int n0 = nb * kRowsBN;
                 const int nbox = min(4, (a.N - n0 + 63) / 64);
-                for (int kb = 0; kb < a.k_blocks; ++kb) {
-                    if (!mbar_wait(xempty0 + 8 * xr.idx, xr.phase ^ 1, abort)) { ok = false; break; }
-                    const uint32_t xf = xfull0 + 8 * xr.idx;
-                    mbar_arrive_expect_tx(xf, kTaXBytes + kGBytes);
-                    tma_load_2d_nohint(sx + xr.idx * kTaXBytes, &tmX, xf, kb * kBK, mb * kRowsBM);
-                    tma_load_1d(sg + xr.idx * kGBytes, &tmG, xf, kb * kBK);
-                    xr.advance();
-                    ++xi;
-                    if (!mbar_wait(wempty0 + 8 * wr.idx, wr.phase ^ 1, abort)) { ok = false; break; }
-                    const uint32_t wf = wfull0 + 8 * wr.idx;
-                    mbar_arrive_expect_tx(wf, nbox * kWBoxBytes);
-                    for (int j = 0; j < nbox; ++j)
-                        tma_load_2d_nohint(sw + wr.idx * kRowsWBytes + j * kWBoxBytes, &tmW, wf,
-                                           n0 + 64 * j, kb * kBK);
-                    wr.advance();
-                    ++wi;
+                for (int kb = un.kb0; kb < un.kb1; ++kb) {
+                    if (!mbar_wait(empty0 + 8 * ring.idx, ring.phase ^ 1, abort)) { ok = false; break; }
+                    const uint32_t f = full0 + 8 * ring.idx;
+                    if (load_x) {
+                        mbar_arrive_expect_tx(f, kTaXBytes + kGBytes);
+                        tma_load_2d_nohint(sx + ring.idx * kTaXBytes, &tmX, f, kb * kBK, mb * kRowsBM);
+                        tma_load_1d(sg + ring.idx * kGBytes, &tmG, f, kb * kBK);
+                    } else {
+                        mbar_arrive_expect_tx(f, nbox * kWBoxBytes);
+                        for (int j = 0; j < nbox; ++j)
+                            tma_load_2d_nohint(sw + ring.idx * kRowsWBytes + j * kWBoxBytes, &tmW, f,
+                                               n0 + 64 * j, kb * kBK);
+                    }
+                    ring.advance();
+                    ++issued;
                 }
             }
             // never leave with copies still landing in shared memory
-            for (uint32_t i = xi > kTaXStages ? xi - kTaXStages : 0; i < xi; ++i)
-                mbar_wait_teardown(xfull0 + 8 * (i % kTaXStages), (i / kTaXStages) & 1);
-            for (uint32_t i = wi > kTaWStages ? wi - kTaWStages : 0; i < wi; ++i)
-                mbar_wait_teardown(wfull0 + 8 * (i % kTaWStages), (i / kTaWStages) & 1);
+            const uint32_t n = ring.n;
+            for (uint32_t i = issued > n ? issued - n : 0; i < issued; ++i)
+                mbar_wait_teardown(full0 + 8 * (i % n), (i / n) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
@@ -641,11 +672,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             Ring wr(kTaWStages), ar(kTaAStages);
             uint32_t tl = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++tl) {
+            TaUnit un;
+            for (int i = 0; ok && ta_unit(a, i, un); ++i, ++tl) {
                 if (!mbar_wait(accempty, (tl & 1) ^ 1, abort)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + kTaAccCol;
-                for (int kb = 0; kb < a.k_blocks; ++kb) {
+                for (int kb = un.kb0; kb < un.kb1; ++kb) {
                     if (!mbar_wait(wfull0 + 8 * wr.idx, wr.phase, abort)) { ok = false; break; }
                     if (!mbar_wait(afull0 + 8 * ar.idx, ar.phase, abort)) { ok = false; break; }
                     tc_fence_after();
@@ -654,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
                         mma_bf16_ts(d, a0 + kk * 8, sdesc_sw128(b0 + kk * 2048, kWBoxBytes, 1024), idesc,
-                                    (kb | kk) != 0);
+                                    kb != un.kb0 || kk != 0);
                     mma_commit(wempty0 + 8 * wr.idx);
                     mma_commit(aempty0 + 8 * ar.idx);
                     wr.advance();
@@ -676,14 +708,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         Ring xr(kTaXStages), ar(kTaAStages);
         uint32_t tl = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++tl) {
+        TaUnit un;
+        for (int i = 0; ok && ta_unit(a, i, un); ++i, ++tl) {
             const uint32_t buf = tl & 1, use = tl >> 1;
             // sr[buf] is free once the epilogue read it for the tile two back
             if (!warp_wait(srempty0 + 8 * buf, (use & 1) ^ 1, abort)) break;
             float ssp[8];   // independent partial sums: no long dependency chain
 #pragma unroll
             for (int c = 0; c < 8; ++c) ssp[c] = 0.f;
-            for (int kb = 0; kb < a.k_blocks; ++kb) {
+            for (int kb = un.kb0; kb < un.kb1; ++kb) {
                 if (!warp_wait(xfull0 + 8 * xr.idx, xr.phase, abort)) { ok = false; break; }
                 const uint32_t xt = sx + xr.idx * kTaXBytes + xrow;
                 const uint32_t gt = sg + xr.idx * kGBytes;
@@ -741,18 +774,102 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t rswz = static_cast<uint32_t>((row >> 1) & 3);
         uint32_t chunks = 0;   // staging buffer uses so far
         uint32_t tl = 0;
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tl) {
+        TaUnit un;
+        for (int i = 0; ta_unit(a, i, un); ++i, ++tl) {
             const uint32_t buf = tl & 1, use = tl >> 1;
             if (!warp_wait(accfull, tl & 1, abort)) break;
             if (!warp_wait(srfull0 + 8 * buf, use & 1, abort)) break;
             tc_fence_after();
-            const float r = rsqrtf(sr[buf * kRowsBM + row] * inv_k + a.eps);
+            const float ss_row = sr[buf * kRowsBM + row];
             __syncwarp();
             if (lane == 0) mbar_arrive(srempty0 + 8 * buf);
             int mb, nb;
-            rows_tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
+            rows_tile_coords(un.t, a.m_tiles, a.n_tiles, mb, nb);
             const int n0 = nb * kRowsBN;
             const uint32_t taddr = tmem + kTaAccCol + (static_cast<uint32_t>(q * 32) << 16);
+            if (un.piece >= 0) {
+                // A K piece of a tail tile: publish the fp32 partial and the
+                // partial row sums of squares, wait for the tile's other
+                // pieces, then reduce rows [r0, r1) of the tile over all
+                // pieces in piece order and write them to Y.
+                const int P = a.tail_pieces;
+                const int tail = un.t - (num_tiles - a.tail_tiles);
+                const size_t slot = static_cast<size_t>(tail) * P;
+                float* wrow = a.ws_acc + ((slot + un.piece) * kRowsBM + row) * kRowsBN;
+#pragma unroll 4
+                for (int c = 0; c < kRowsBN / 16; ++c) {
+                    uint32_t v[16];
+                    tmem_ld_32x16(taddr + c * 16, v);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        __stcg(reinterpret_cast<float4*>(wrow + c * 16 + 4 * j),
+                               make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                           __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])));
+                }
+                __stcg(a.ws_ss + (slot + un.piece) * kRowsBM + row, ss_row);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(accempty);
+                __threadfence();
+                int* cnt = a.ws_count + 2 * tail;
+                bool ok = epi_sync();
+                if (e == 0) {
+                    atomicAdd(cnt, 1);
+                    ok = spin_until_ge(cnt, P, abort) && ok;
+                }
+                ok = epi_sync() && ok && !*abort;
+                const int r0 = (un.piece * kRowsBM) / P, r1 = ((un.piece + 1) * kRowsBM) / P;
+                float* rr = reinterpret_cast<float*>(smem + kTaOffRr);
+                if (ok && e < r1 - r0) {
+                    float tot = 0.f;
+                    for (int p2 = 0; p2 < P; ++p2) tot += __ldcg(a.ws_ss + (slot + p2) * kRowsBM + r0 + e);
+                    rr[e] = rsqrtf(tot * inv_k + a.eps);
+                }
+                ok = epi_sync() && ok;
+                const int items = (r1 - r0) * (kRowsBN / 4);
+                for (int it = e; ok && it < items; it += 128) {
+                    const int rl = it / (kRowsBN / 4), col = (it % (kRowsBN / 4)) * 4;
+                    const int m = mb * kRowsBM + r0 + rl;
+                    const float* src = a.ws_acc + (slot * kRowsBM + r0 + rl) * kRowsBN + col;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    int p2 = 0;
+                    for (; p2 + 4 <= P; p2 += 4) {
+                        float4 t4[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            t4[j] = __ldcg(reinterpret_cast<const float4*>(src + static_cast<size_t>(p2 + j) * kRowsBM * kRowsBN));
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            acc.x += t4[j].x;
+                            acc.y += t4[j].y;
+                            acc.z += t4[j].z;
+                            acc.w += t4[j].w;
+                        }
+                    }
+                    for (; p2 < P; ++p2) {
+                        const float4 t4 = __ldcg(reinterpret_cast<const float4*>(src + static_cast<size_t>(p2) * kRowsBM * kRowsBN));
+                        acc.x += t4.x;
+                        acc.y += t4.y;
+                        acc.z += t4.z;
+                        acc.w += t4.w;
+                    }
+                    if (m < a.M && n0 + col < a.N) {
+                        const float r = rr[rl];
+                        uint2 o;
+                        o.x = pack_bf16x2(acc.x * r, acc.y * r);
+                        o.y = pack_bf16x2(acc.z * r, acc.w * r);
+                        *reinterpret_cast<uint2*>(Y + static_cast<size_t>(m) * a.N + n0 + col) = o;
+                    }
+                }
+                // the last piece through resets the tile's counters for the next launch
+                epi_sync();
+                if (e == 0 && atomicAdd(cnt + 1, 1) == P - 1) {
+                    atomicExch(cnt, 0);
+                    atomicExch(cnt + 1, 0);
+                }
+                continue;
+            }
+            const float r = rsqrtf(ss_row * inv_k + a.eps);
             uint32_t pk[kRowsBN / 2];   // the row, scaled and packed as bf16x2
 #pragma unroll
             for (int c = 0; c < kRowsBN / 16; ++c) {
@@ -1321,7 +1438,7 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
     if (fused && !split && a.xrows == kRowsBM) {
         cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(rows_ta_kernel), 6);
         if (e != cudaSuccess) return e;
-        e = launch_ex(rows_ta_kernel, a.grid, kTaSmem, 1, s, tmX, tmW, tmG, *a.tmY, a);
+        e = launch_ex(rows_ta_kernel, a.grid, kTaSmem, 1, s, tmX, tmW, tmG, *a.tmY, y, a);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }

@@ -48,6 +48,14 @@ struct RowsLaunch {
     int grid;
     const CUtensorMap* tmY;    // Y in boxes of [128 rows][32 columns], 64-byte swizzle
                                // (used by the fused kernel for several row tiles)
+    // Fused kernel for several row tiles: the last tail_tiles tiles (those a
+    // whole wave of CTAs would leave mostly idle) are cut along K into
+    // tail_pieces pieces of tail_kbp k-blocks, one per CTA, and reduced
+    // through global memory.  0 tail tiles: every tile is whole.
+    int tail_tiles, tail_pieces, tail_kbp;
+    float* ws_acc;             // [tail_tiles][tail_pieces][128][256] fp32 partials
+    float* ws_ss;              // [tail_tiles][tail_pieces][128] partial row sums of squares
+    int* ws_count;             // [tail_tiles][2] arrival counters, zero between launches
 };
 
 struct ColsLaunch {

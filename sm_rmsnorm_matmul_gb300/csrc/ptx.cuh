@@ -115,6 +115,29 @@ __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity,
     return __all_sync(0xffffffffu, ok);
 }
 
+// Global-memory flag with acquire semantics at GPU scope.
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+// Waits until *p >= target, bounded like mbar_wait (another CTA of the same
+// grid, resident at the same time, raises it).
+__device__ __forceinline__ bool spin_until_ge(const int* p, int target, volatile int* abort) {
+    if (ld_acquire_gpu(p) >= target) return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        __nanosleep(64);
+        if (ld_acquire_gpu(p) >= target) return true;
+        if (*abort) return false;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            atomicCAS(&g_status, 0, kStatusTimeout);
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
 // Bounded wait used during teardown; ignores the abort flag.
 __device__ __forceinline__ bool mbar_wait_teardown(uint32_t bar, uint32_t parity) {
     const uint64_t t0 = globaltimer();

@@ -105,6 +105,23 @@ def test_ragged(rmm, forced, M, K, N, path):
     assert_close(Y, ref, f"{M}x{K}x{N} path {path}")
 
 
+# Several row tiles whose last wave of CTAs would be at most half full: those
+# last tiles are cut along K, one piece per CTA, and the pieces are combined
+# through the workspace (here 160 tiles on 152 SMs leave 8; 170 leave 18, with
+# a partial row tile, a partial column tile and a partial K block).
+TAIL = [(1280, 1024, 4096), (1200, 1000, 4104)]
+
+
+@pytest.mark.parametrize("M,K,N", TAIL)
+def test_tail_tiles_cut_along_k(rmm, M, K, N):
+    from sm_rmsnorm_matmul_gb300 import inputs
+    X, g, W = inputs.random_problem(M, K, N, seed=M + K + N, x_kind="row_scaled")
+    Y = run_fused(rmm, X, g, W, 1e-6)
+    assert_close(Y, oracle.rmsnorm_matmul(X, g, W, 1e-6), f"{M}x{K}x{N}")
+    # the pieces are added in a fixed order: a second call gives the same bits
+    assert torch.equal(Y, run_fused(rmm, X, g, W, 1e-6))
+
+
 def test_small_m_rejects_large_m_when_forced(rmm, forced):
     forced(2)
     X = torch.zeros(129, 64, dtype=torch.bfloat16, device="cuda")
