@@ -154,7 +154,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort = reinterpret_cast<volatile int*>(smem + L.off_misc + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // units = (tile, K split); with a cluster, blockIdx.x = cluster * splits +
+    // rank and the splits of one tile are the CTAs of one cluster, one unit
+    // per CTA (a launch that breaks this does no work and reports an
+    // internal error)
+    int units = a.m_tiles * a.n_tiles * split;
+    const bool bad_launch = kSplit && units > static_cast<int>(gridDim.x);
+    if (bad_launch) units = 0;
+    // Loads of stage s = k-block kb of the unit whose tile starts at row block
+    // mb and column n0 (nbox W boxes of 64 columns).
+    auto issue = [&](uint32_t s, int kb, int mb, int n0, int nbox) {
+        mbar_arrive_expect_tx(full(s), xbytes + nbox * kWBoxBytes + (kFused ? kGBytes : 0));
+        tma_load_2d_nohint(sx + s * xbytes, &tmX, full(s), kb * kBK, mb * kRowsBM);
+        for (int j = 0; j < nbox; ++j)
+            tma_load_2d_nohint(sw + s * kRowsWBytes + j * kWBoxBytes, &tmW, full(s), n0 + 64 * j, kb * kBK);
+        if (kFused) tma_load_1d(sg + s * kGBytes, &tmG, full(s), kb * kBK);
+    };
+    // k-blocks of the first unit that thread 0 (the producer) issues before
+    // the CTA-wide set-up barrier, as soon as its barriers exist and the
+    // previous kernel on the stream has completed
+    uint32_t pro = 0;
     if (threadIdx.x == 0) {
+        if (bad_launch) atomicCAS(&g_status, 0, kStatusInternal);
         for (int s = 0; s < S; ++s) {
             mbar_init(full(s), 1);
             mbar_init(xform(s), 4);   // one elected lane per transform warp
@@ -169,11 +190,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(redfull, 1);   // own expect_tx (+ the peers' bytes)
         *abort = 0;
         fence_mbar_init();
-    }
-    if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmX);
         prefetch_tmap(&tmW);
         if (kFused) prefetch_tmap(&tmG);
+        // The previous kernel's writes are visible after grid_dep_wait(); the
+        // next kernel may then be scheduled (its set-up overlaps this one).
+        grid_dep_wait();
+        grid_dep_launch();
+        if (static_cast<int>(blockIdx.x) < units) {
+            const int u = blockIdx.x, t = u / split, sp = u - t * split;
+            const int kb0 = sp * a.kb_per_split, kb1 = min(a.k_blocks, kb0 + a.kb_per_split);
+            int mb, nb;
+            rows_tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
+            const int n0 = nb * kRowsBN;
+            pro = static_cast<uint32_t>(min(S, kb1 - kb0));
+            for (uint32_t i = 0; i < pro; ++i) issue(i, kb0 + static_cast<int>(i), mb, n0, min(4, (a.N - n0 + 63) / 64));
+        }
     }
     if (warp == 2) {
         tmem_alloc(smem_u32(tmem_holder), kRowsTmemCols);
@@ -185,26 +217,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // peers' barriers must be initialised before the first remote access:
     // announce it here, wait for the peers just before that access
     if (kSplit) cluster_arrive();
-    // Set-up above overlaps the previous kernel on the stream; its writes are
-    // visible after grid_dep_wait().  The next kernel may then be scheduled.
     grid_dep_wait();
-    if (threadIdx.x == 0) grid_dep_launch();
     const uint32_t tmem = *tmem_holder;
-    // units = (tile, K split); with a cluster, blockIdx.x = cluster * splits +
-    // rank and the splits of one tile are the CTAs of one cluster, one unit
-    // per CTA (a launch that breaks this does no work and reports an
-    // internal error)
-    int units = a.m_tiles * a.n_tiles * split;
-    if (kSplit && units > static_cast<int>(gridDim.x)) {
-        if (threadIdx.x == 0) atomicCAS(&g_status, 0, kStatusInternal);
-        units = 0;
-    }
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            uint32_t it = 0;
+            uint32_t it = pro;
             Ring ring(S);
+            for (uint32_t i = 0; i < pro; ++i) ring.advance();
             bool ok = true;
             for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
                 const int t = u / split, sp = u - t * split;
@@ -213,16 +234,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 rows_tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
                 const int n0 = nb * kRowsBN;
                 const int nbox = min(4, (a.N - n0 + 63) / 64);
-                const uint32_t bytes = xbytes + nbox * kWBoxBytes + (kFused ? kGBytes : 0);
-                for (int kb = kb0; kb < kb1; ++kb) {
+                const int first = kb0 + (u == static_cast<int>(blockIdx.x) ? static_cast<int>(pro) : 0);
+                for (int kb = first; kb < kb1; ++kb) {
                     const uint32_t s = ring.idx, ph = ring.phase;
                     if (!mbar_wait(empty(s), ph ^ 1, abort)) { ok = false; break; }
-                    mbar_arrive_expect_tx(full(s), bytes);
-                    tma_load_2d_nohint(sx + s * xbytes, &tmX, full(s), kb * kBK, mb * kRowsBM);
-                    for (int j = 0; j < nbox; ++j)
-                        tma_load_2d_nohint(sw + s * kRowsWBytes + j * kWBoxBytes, &tmW, full(s),
-                                           n0 + 64 * j, kb * kBK);
-                    if (kFused) tma_load_1d(sg + s * kGBytes, &tmG, full(s), kb * kBK);
+                    issue(s, kb, mb, n0, nbox);
                     ++it;
                     ring.advance();
                 }
