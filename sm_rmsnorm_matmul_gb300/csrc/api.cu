@@ -315,16 +315,17 @@ ColsPlan plan_cols(int dev, bool fused, int64_t M, int64_t K, int64_t N, const D
 
 struct RowsPlan {
     int m_tiles, n_tiles, k_blocks, splits, kb_per_split, cluster, xrows, MP, stages, grid;
+    int overlay;
 };
 
-int rows_stages(int xrows, int red_slots, int MP, const DeviceInfo& d) {
-    const size_t fixed = rmm::rows_smem_bytes(xrows, 0, red_slots, MP);
+int rows_stages(int xrows, int red_slots, int MP, const DeviceInfo& d, bool overlay = false) {
+    const size_t fixed = rmm::rows_smem_bytes(xrows, 0, red_slots, MP, overlay);
     const size_t per = rmm::rows_stage_bytes(xrows);
     const size_t avail = d.smem_optin > 0 ? static_cast<size_t>(d.smem_optin) : 227 * 1024;
     int st = avail > fixed ? static_cast<int>((avail - fixed) / per) : 0;
     st = std::min(rmm::kRowsMaxStages, st);
     // the X tiles are padded to 1 KB as a whole
-    while (st > 0 && rmm::rows_smem_bytes(xrows, st, red_slots, MP) > avail) --st;
+    while (st > 0 && rmm::rows_smem_bytes(xrows, st, red_slots, MP, overlay) > avail) --st;
     return st;
 }
 
@@ -370,11 +371,24 @@ RowsPlan plan_rows(int dev, bool fused, int64_t M, int64_t K, int64_t N, const D
         const int kbps = (p.k_blocks + s - 1) / s;
         if ((p.k_blocks + kbps - 1) / kbps != s) continue;
         const int red_slots = s > 1 ? s : 0;
-        const int st = rows_stages(p.xrows, red_slots, p.MP, d);
+        int st = rows_stages(p.xrows, red_slots, p.MP, d);
+        // A receive area of its own that leaves fewer than 3 stages: put the
+        // receive blocks over the pipeline buffers instead.  The extra
+        // handshake measured ~0.5 us, more than going from 3 to 5 stages
+        // bought (M = 64), less than going from 2 stages or none (M > 64).
+        bool overlay = false;
+        if (s > 1 && st < 3) {
+            const int so = rows_stages(p.xrows, red_slots, p.MP, d, true);
+            if (so > st && so >= 2 && rmm::rows_overlay_fits(p.xrows, so, s, p.MP)) {
+                st = so;
+                overlay = true;
+            }
+        }
         if (st < 2) continue;
         int resident = sms;
         if (s > 1) {
-            resident = rows_max_clusters(dev, fused, s, rmm::rows_smem_bytes(p.xrows, st, red_slots, p.MP)) * s;
+            resident = rows_max_clusters(dev, fused, s,
+                                         rmm::rows_smem_bytes(p.xrows, st, red_slots, p.MP, overlay)) * s;
             if (resident <= 0) continue;
         }
         const long units = static_cast<long>(p.n_tiles) * s;
@@ -382,13 +396,15 @@ RowsPlan plan_rows(int dev, bool fused, int64_t M, int64_t K, int64_t N, const D
         if (s > 1 && units > resident) continue;
         const long waves = (units + resident - 1) / resident;
         const double per_cta = static_cast<double>(waves) * kbps * rmm::kRowsBN * kBK * 2 / 55e9;
-        const double cost = std::max(per_cta, w_total / 6.0e12) * 1e6 + waves * 1.0 + (s > 1 ? 1.5 : 0.5);
+        const double cost = std::max(per_cta, w_total / 6.0e12) * 1e6 + waves * 1.0 + (s > 1 ? 1.5 : 0.5) +
+                            (overlay ? 0.7 : 0.0);
         if (cost < best - 1e-9) {
             best = cost;
             p.splits = s;
             p.kb_per_split = kbps;
             p.cluster = s > 1 ? 1 : 0;
             p.stages = st;
+            p.overlay = overlay ? 1 : 0;
             p.grid = static_cast<int>(std::min<long>(units, resident));
         }
     }
@@ -471,6 +487,7 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
     a.MP = p.MP;
     a.stages = p.stages;
     a.grid = p.grid;
+    a.red_overlay = p.overlay;
     CUtensorMap tmY;
     a.tail_tiles = 0;
     a.tail_pieces = 1;

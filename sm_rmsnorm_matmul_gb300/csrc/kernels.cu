@@ -106,16 +106,18 @@ __host__ __device__ inline int rows_owned_max(int splits) {
 // with a cluster K split of S = red_slots, each CTA receives one block per
 // split, [MP] fp32 row sums of squares followed by [ceil(8/S)][MP][32] fp32
 // partial rows of the chunks it owns (the 16-byte pieces of a row rotated by
-// row & 7 against bank conflicts).
-__host__ __device__ inline RowsLayout rows_layout(int xrows, int stages, int red_slots, int MP) {
+// row & 7 against bank conflicts).  With overlay, the receive blocks occupy
+// the start of the pipeline buffers, which are idle by the time they fill.
+__host__ __device__ inline RowsLayout rows_layout(int xrows, int stages, int red_slots, int MP,
+                                                  bool overlay = false) {
     RowsLayout L;
     L.xbytes = xrows * kBK * 2;
     L.off_x = 0;
     L.off_w = ((stages * L.xbytes + 1023) / 1024) * 1024;
     L.off_g = L.off_w + stages * kRowsWBytes;
-    L.off_red = ((L.off_g + stages * kGBytes + 15) / 16) * 16;
     L.red_block = red_slots > 0 ? MP * (4 + rows_owned_max(red_slots) * 128) : 0;
-    L.off_bar = L.off_red + red_slots * L.red_block;
+    L.off_red = overlay ? 0 : ((L.off_g + stages * kGBytes + 15) / 16) * 16;
+    L.off_bar = overlay ? ((L.off_g + stages * kGBytes + 15) / 16) * 16 : L.off_red + red_slots * L.red_block;
     const uint32_t nbars = 3 * kRowsMaxStages + 10;
     L.off_sr = L.off_bar + ((nbars * 8 + 15) / 16) * 16;
     L.off_misc = L.off_sr + 2 * kRowsBM * 4;
@@ -133,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = align1024(smem_raw);
     const int S = a.stages;
     const int split = kSplit ? a.splits : 1;
-    const RowsLayout L = rows_layout(a.xrows, S, kSplit ? split : 0, a.MP);
+    const RowsLayout L = rows_layout(a.xrows, S, kSplit ? split : 0, a.MP, kSplit && a.red_overlay);
     const uint32_t xbytes = L.xbytes;
     const uint32_t sb = smem_u32(smem);
     const uint32_t sx = sb + L.off_x, sw = sb + L.off_w, sg = sb + L.off_g;
@@ -148,6 +150,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the other splits' blocks (partials of the chunks this CTA owns, row
     // sums of squares) have arrived
     const uint32_t redfull = bar0 + 8 * (3 * kRowsMaxStages + 8);
+    // with the receive blocks over the pipeline buffers: every other split's
+    // buffers are idle, so its blocks may be stored
+    const uint32_t redgo = bar0 + 8 * (3 * kRowsMaxStages + 9);
     float* sr = reinterpret_cast<float*>(smem + L.off_sr);         // [2][128] row sums of squares
     const uint32_t red_addr = sb + L.off_red;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.off_misc);
@@ -159,7 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // per CTA (a launch that breaks this does no work and reports an
     // internal error)
     int units = a.m_tiles * a.n_tiles * split;
-    const bool bad_launch = kSplit && units > static_cast<int>(gridDim.x);
+    const bool bad_launch = kSplit && (units > static_cast<int>(gridDim.x) ||
+                                       (a.red_overlay && split * L.red_block > L.off_g));
     if (bad_launch) units = 0;
     // Loads of stage s = k-block kb of the unit whose tile starts at row block
     // mb and column n0 (nbox W boxes of 64 columns).
@@ -188,6 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(mmadone, 1);
         mbar_init(redfull, 1);   // own expect_tx (+ the peers' bytes)
+        mbar_init(redgo, split > 1 ? split - 1 : 1);   // one remote arrive per other split
         *abort = 0;
         fence_mbar_init();
         prefetch_tmap(&tmX);
@@ -427,7 +434,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         cluster_wait();    // the peers' barriers are initialised
         // 1. tensor memory -> owners
         if (have && q * 32 < rows_here &&
-            warp_wait(accfull(0), 0, abort) && (!kFused || warp_wait(srfull(0), 0, abort))) {
+            warp_wait(accfull(0), 0, abort) && (!kFused || warp_wait(srfull(0), 0, abort)) &&
+            (!a.red_overlay || [&] {
+                // The last MMA is done, so this CTA's pipeline buffers, which
+                // hold its receive blocks, are idle: tell the other splits,
+                // then wait until theirs are idle too.
+                if (threadIdx.x == 0)
+                    for (int p = 0; p < split; ++p)
+                        if (p != me) mbar_arrive_remote(mapa_shared(redgo, p));
+                return warp_wait_cluster(redgo, 0, abort);
+            }())) {
             tc_fence_after();
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
             const uint32_t swz = static_cast<uint32_t>(row & 7);
@@ -1410,8 +1426,12 @@ cudaError_t ensure_smem_attr(const void* func, int slot) {
 
 }  // namespace
 
-size_t rows_smem_bytes(int xrows, int stages, int red_slots, int MP) {
-    return rows_layout(xrows, stages, red_slots, MP).total;
+size_t rows_smem_bytes(int xrows, int stages, int red_slots, int MP, bool overlay) {
+    return rows_layout(xrows, stages, red_slots, MP, overlay).total;
+}
+bool rows_overlay_fits(int xrows, int stages, int splits, int MP) {
+    const RowsLayout L = rows_layout(xrows, stages, splits, MP, true);
+    return static_cast<uint32_t>(splits) * L.red_block <= L.off_g;
 }
 size_t rows_stage_bytes(int xrows) { return xrows * kBK * 2 + kRowsWBytes + kGBytes; }
 size_t cols_smem_bytes(int MP, int stages, int red_slots) {
@@ -1462,7 +1482,7 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
                       : (split ? rows_kernel<false, true> : rows_kernel<false, false>);
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), (fused ? 0 : 1) + (split ? 4 : 0));
     if (e != cudaSuccess) return e;
-    const size_t smem = rows_smem_bytes(a.xrows, a.stages, split ? a.splits : 0, a.MP);
+    const size_t smem = rows_smem_bytes(a.xrows, a.stages, split ? a.splits : 0, a.MP, split && a.red_overlay);
     e = launch_ex(kern, a.grid, smem, split ? a.splits : 1, s, tmX, tmW, tmG, y, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

@@ -25,8 +25,12 @@ constexpr int kColsMaxSplits = 16;
 
 // Row-tile path shared memory: xrows = rows of X loaded per stage (128, or
 // M rounded up to 16 for a single row tile); red_slots = K splits reduced
-// through a cluster (0 without); MP = M rounded up to 16.
-size_t rows_smem_bytes(int xrows, int stages, int red_slots, int MP);
+// through a cluster (0 without); MP = M rounded up to 16; overlay: the
+// splits' receive blocks reuse the pipeline buffers instead of an area of
+// their own.
+size_t rows_smem_bytes(int xrows, int stages, int red_slots, int MP, bool overlay = false);
+// The receive blocks of a K split over `splits` CTAs fit the pipeline buffers.
+bool rows_overlay_fits(int xrows, int stages, int splits, int MP);
 size_t rows_stage_bytes(int xrows);
 int rows_max_active_clusters(bool fused, int splits, size_t smem);
 // red_slots = splits - 1 when the splits reduce through a cluster, else 0.
@@ -43,6 +47,7 @@ struct RowsLaunch {
     int m_tiles, n_tiles, k_blocks;
     int splits, kb_per_split;  // K split of each tile (splits > 1 needs m_tiles == 1
                                // and one (tile, split) unit per CTA)
+    int red_overlay;           // 1: the splits' receive blocks reuse the pipeline buffers
     int cluster;               // 1: the splits of a tile form a cluster
     int xrows, MP, stages;
     int grid;

@@ -122,6 +122,21 @@ def test_tail_tiles_cut_along_k(rmm, M, K, N):
     assert torch.equal(Y, run_fused(rmm, X, g, W, 1e-6))
 
 
+# One row tile of 65..128 rows: the K-split receive blocks are too large to
+# sit beside the pipeline, so they reuse the pipeline buffers once every
+# split has finished its last MMA (handshake between the CTAs of a cluster).
+WIDE_DECODE = [(128, 4096, 6144), (100, 2048, 2056), (80, 1024, 512)]
+
+
+@pytest.mark.parametrize("M,K,N", WIDE_DECODE)
+def test_wide_decode_split_over_pipeline_buffers(rmm, M, K, N):
+    from sm_rmsnorm_matmul_gb300 import inputs
+    X, g, W = inputs.random_problem(M, K, N, seed=M * 5 + N, x_kind="outlier_entries")
+    Y = run_fused(rmm, X, g, W, 1e-5)
+    assert_close(Y, oracle.rmsnorm_matmul(X, g, W, 1e-5), f"{M}x{K}x{N}")
+    assert torch.equal(Y, run_fused(rmm, X, g, W, 1e-5))
+
+
 def test_small_m_rejects_large_m_when_forced(rmm, forced):
     forced(2)
     X = torch.zeros(129, 64, dtype=torch.bfloat16, device="cuda")
