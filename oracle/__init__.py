@@ -13,7 +13,10 @@ bit patterns exactly to float64, and marshals numpy arrays.
 Pins (tests/test_oracle_pins.py): the finite-field identity behind the
 rewrite, the rewritten and unfused forms agreeing, scale invariance,
 W = identity against torch's RMSNorm, constant rows against a closed form, a
-hand-worked 2x3x2 example, and the matmul part against numpy.
+hand-worked 2x3x2 example, and the matmul part against numpy.  The gated
+form is pinned by a zero gate giving zero, the exact odd part of SiLU
+(Y(W_gate) - Y(-W_gate) = Z_gate * Z_up), its two limits, and Y >= 0 when the
+gate and up projections coincide.
 """
 from __future__ import annotations
 
@@ -54,8 +57,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_matmul.argtypes = [dp, dp, dp, L, L, L, I]
     lib.oracle_rmsnorm_matmul.argtypes = [dp, dp, dp, dp, L, L, L, D, I]
     lib.oracle_rmsnorm_matmul_rewritten.argtypes = [dp, dp, dp, dp, L, L, L, D, I]
+    lib.oracle_rmsnorm_matmul_swiglu.argtypes = [dp, dp, dp, dp, L, L, L, D, I]
     for f in (lib.oracle_rmsnorm, lib.oracle_matmul, lib.oracle_rmsnorm_matmul,
-              lib.oracle_rmsnorm_matmul_rewritten, lib.oracle_max_threads):
+              lib.oracle_rmsnorm_matmul_rewritten, lib.oracle_rmsnorm_matmul_swiglu,
+              lib.oracle_max_threads):
         f.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     return lib
@@ -128,6 +133,18 @@ def rmsnorm_matmul_rewritten(X, g, W, eps: float, nthreads: int = 0, lib=None) -
     _check(lib.oracle_rmsnorm_matmul_rewritten(_ptr(X), _ptr(g), _ptr(W), _ptr(Y),
                                                M, K, N, float(eps), nthreads),
            "rmsnorm_matmul_rewritten")
+    return Y
+
+
+def rmsnorm_matmul_swiglu(X, g, W, eps: float, nthreads: int = 0, lib=None) -> np.ndarray:
+    """Y = silu(Z[:, :F]) * Z[:, F:] with Z = RMSNorm(X; g, eps) @ W, W [K, 2F], in fp64."""
+    lib = lib or load()
+    X, g, W = to_f64(X), to_f64(g), to_f64(W)
+    M, K = X.shape
+    N = W.shape[1]
+    Y = np.empty((M, N // 2), dtype=np.float64)
+    _check(lib.oracle_rmsnorm_matmul_swiglu(_ptr(X), _ptr(g), _ptr(W), _ptr(Y), M, K, N,
+                                            float(eps), nthreads), "rmsnorm_matmul_swiglu")
     return Y
 
 

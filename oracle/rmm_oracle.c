@@ -30,8 +30,17 @@
  *
  *   Y[m,n] = ( sum_k (X[m,k]*g[k]) * W[k,n] ) * r[m]
  *
+ * oracle_rmsnorm_matmul_swiglu() adds the gated MLP on top (GatedMLP is one
+ * of the review page's benchmark workloads, section 5 "experimental results",
+ * table of the six benchmarks; the pages give no formula for it).  Read as
+ * the gated MLP of the LLaMA family: W holds the gate projection in columns
+ * [0, F) and the up projection in columns [F, 2F), N = 2F, and
+ *
+ *   Z[m,n]  = RMSNorm(X)[m,:] . W[:,n]                    (as above)
+ *   Y[m,f]  = silu(Z[m,f]) * Z[m,F+f],  silu(z) = z / (1 + exp(-z)),  f < F.
+ *
  * Everything is double precision; nothing is rounded to bf16.  Row-major
- * layouts: X [M,K], g [K], W [K,N], Y [M,N].
+ * layouts: X [M,K], g [K], W [K,N], Y [M,N] (Y [M,F] for the gated form).
  */
 #include <math.h>
 #include <stdlib.h>
@@ -42,6 +51,7 @@
 
 #define ORACLE_OK 0
 #define ORACLE_ERR_ALLOC 1
+#define ORACLE_ERR_ARG 2
 
 /* Mean square of one row: (1/K) * sum_k x_k^2, summed in k order. */
 static double row_mean_square(const double *x, long K)
@@ -167,6 +177,34 @@ int oracle_rmsnorm_matmul_rewritten(const double *X, const double *g,
             y[n] *= r;
     }
     return ORACLE_OK;
+}
+
+/* Swish gate: silu(z) = z * sigmoid(z) = z / (1 + exp(-z)). */
+static double silu(double z)
+{
+    return z / (1.0 + exp(-z));
+}
+
+/* Gated MLP: Z = RMSNorm(X) @ W over N = 2F columns, then
+ * Y[m,f] = silu(Z[m,f]) * Z[m,F+f].  Y is [M, F]. */
+int oracle_rmsnorm_matmul_swiglu(const double *X, const double *g, const double *W,
+                                 double *Y, long M, long K, long N, double eps,
+                                 int nthreads)
+{
+    if (N % 2 != 0)
+        return ORACLE_ERR_ARG;
+    const long F = N / 2;
+    double *Z = (double *)malloc((size_t)(M * N > 0 ? M * N : 1) * sizeof(double));
+    if (!Z)
+        return ORACLE_ERR_ALLOC;
+    int rc = oracle_rmsnorm_matmul(X, g, W, Z, M, K, N, eps, nthreads);
+    if (rc == ORACLE_OK) {
+        for (long m = 0; m < M; ++m)
+            for (long f = 0; f < F; ++f)
+                Y[m * F + f] = silu(Z[m * N + f]) * Z[m * N + F + f];
+    }
+    free(Z);
+    return rc;
 }
 
 int oracle_max_threads(void)

@@ -224,6 +224,71 @@ def pin_permutations(lib, seed=17):
     return True, "ok"
 
 
+# ---------------------------------------------------------------------------
+# G: the gated MLP on top (review page, section 5, benchmark table: GatedMLP;
+# read as Y = silu(Z_gate) * Z_up with Z = RMSNorm(X) @ [W_gate | W_up]).
+# Z itself is the main oracle, pinned above; these pins tie the gate to facts
+# about silu(z) = z * sigmoid(z):
+#   G1 a zero gate gives exactly zero;
+#   G2 the odd part is exact: silu(z) - silu(-z) = z (sigmoid(z) + sigmoid(-z)
+#      = 1), so Y(W_gate) - Y(-W_gate) = Z_gate * Z_up;
+#   G3 silu(z) -> z for large z, G4 silu(z) -> 0 for large negative z;
+#   G5 with W_gate = W_up, Y = Z^2 sigmoid(Z) >= 0.
+# ---------------------------------------------------------------------------
+def _gated_problem(rng, M=5, K=24, F=7):
+    X = rng.standard_normal((M, K))
+    g = rng.uniform(0.5, 1.5, K)
+    Wg = rng.standard_normal((K, F))
+    Wu = rng.standard_normal((K, F))
+    return X, g, Wg, Wu
+
+
+def pin_gated_zero_gate(lib, seed=21):
+    X, g, _, Wu = _gated_problem(_rng(seed))
+    y = oracle.rmsnorm_matmul_swiglu(X, g, np.hstack([np.zeros_like(Wu), Wu]), 1e-6, lib=lib)
+    return (bool(np.all(y == 0.0)), "zero gate gives zero")
+
+
+def pin_gated_odd_part(lib, seed=22):
+    X, g, Wg, Wu = _gated_problem(_rng(seed))
+    yp = oracle.rmsnorm_matmul_swiglu(X, g, np.hstack([Wg, Wu]), 1e-6, lib=lib)
+    yn = oracle.rmsnorm_matmul_swiglu(X, g, np.hstack([-Wg, Wu]), 1e-6, lib=lib)
+    F = Wg.shape[1]
+    z = oracle.rmsnorm_matmul(X, g, np.hstack([Wg, Wu]), 1e-6, lib=lib)
+    ref = z[:, :F] * z[:, F:]
+    err = _rel_normwise(yp - yn, ref)
+    return (err <= 1e-12, f"odd part: normwise rel diff {err:.3e}")
+
+
+def pin_gated_limits(lib, seed=23):
+    rng = _rng(seed)
+    K, F = 16, 5
+    # constant rows: Z = sign(c) * (g @ W) / sqrt(1 + eps/c^2), here with a
+    # positive gate of at least 40 or a negative one of at most -40
+    X = np.full((2, K), 3.0)
+    g = rng.uniform(0.5, 1.5, K)
+    Wu = rng.standard_normal((K, F))
+    for sign in (1.0, -1.0):
+        Wg = sign * rng.uniform(5.0, 6.0, (K, F))
+        y = oracle.rmsnorm_matmul_swiglu(X, g, np.hstack([Wg, Wu]), 0.0, lib=lib)
+        zg, zu = g @ Wg, g @ Wu
+        if sign > 0:
+            err = _rel_normwise(y, np.broadcast_to(zg * zu, y.shape))
+            if not (zg.min() >= 40.0 and err <= 1e-14):
+                return False, f"large positive gate: rel diff {err:.3e}"
+        else:
+            bound = float(np.abs(zg * zu).max() * np.exp(-40.0))
+            if not (zg.max() <= -40.0 and float(np.abs(y).max()) <= bound):
+                return False, "large negative gate is not ~0"
+    return True, "ok"
+
+
+def pin_gated_equal_projections(lib, seed=24):
+    X, g, Wg, _ = _gated_problem(_rng(seed))
+    y = oracle.rmsnorm_matmul_swiglu(X, g, np.hstack([Wg, Wg]), 1e-6, lib=lib)
+    return (bool(np.all(y >= 0.0)) and bool(np.any(y > 0.0)), "gate = up gives y >= 0")
+
+
 ALL_PINS = {
     "rewrite_agrees": pin_rewrite_agrees,
     "scale_invariance": pin_scale_invariance,
@@ -232,4 +297,8 @@ ALL_PINS = {
     "hand_worked": pin_hand_worked,
     "matmul_part": pin_matmul_part,
     "permutations": pin_permutations,
+    "gated_zero_gate": pin_gated_zero_gate,
+    "gated_odd_part": pin_gated_odd_part,
+    "gated_limits": pin_gated_limits,
+    "gated_equal_projections": pin_gated_equal_projections,
 }

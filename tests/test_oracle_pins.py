@@ -64,6 +64,11 @@ def test_zero_row_gives_zero():
     assert np.array_equal(y, np.zeros((1, 3)))
 
 
+def test_gated_rejects_odd_width():
+    with pytest.raises(RuntimeError):
+        oracle.rmsnorm_matmul_swiglu(np.ones((1, 4)), np.ones(4), np.ones((4, 3)), 1e-6)
+
+
 def test_empty_rows():
     y = oracle.rmsnorm_matmul(np.zeros((0, 8)), np.ones(8), np.ones((8, 3)), 1e-6)
     assert y.shape == (0, 3)
@@ -91,6 +96,13 @@ MUTANTS = [
     ("last k dropped from the statistic", "for (long k = 0; k < K; ++k)\n        ss +=",
      "for (long k = 0; k < K - 1; ++k)\n        ss +="),
     ("statistic scaled by a constant", "ss += x[k] * x[k];", "ss += x[k] * x[k] * 1.25;"),
+    # the gated form
+    ("gate and up swapped", "silu(Z[m * N + f]) * Z[m * N + F + f]",
+     "silu(Z[m * N + F + f]) * Z[m * N + f]"),
+    ("sigmoid instead of silu", "return z / (1.0 + exp(-z));", "return 1.0 / (1.0 + exp(-z));"),
+    ("exponent sign flipped in silu", "return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
+    ("up column off by one", "* Z[m * N + F + f];", "* Z[m * N + F + f - (f > 0)];"),
+    ("gate not activated", "silu(Z[m * N + f]) * Z[m * N + F + f]", "Z[m * N + f] * Z[m * N + F + f]"),
 ]
 
 
