@@ -86,6 +86,24 @@ int rmsnorm_matmul(const void* X, const void* g, const void* W, void* Y,
                    int64_t M, int64_t K, int64_t N, float eps, cudaStream_t stream);
 
 /*
+ * Fused RMSNorm + MatMul + gated MLP, one launch (GatedMLP: one of the review
+ * page's benchmark workloads, section 5, "experimental results"; the pages
+ * give no formula, read here as the gated MLP of the LLaMA family):
+ *   W [K,N] holds the gate projection in columns [0, F) and the up projection
+ *   in columns [F, 2F), N = 2F;  Z = RMSNorm(X; g, eps) @ W as above (fp32
+ *   accumulation, never rounded to bf16);
+ *   Y [M,F] bf16:  Y[m,f] = silu(Z[m,f]) * Z[m,F+f],  silu(z) = z / (1 + e^-z).
+ * N must be a multiple of 16 (F a multiple of 8); the other rules are those of
+ * rmsnorm_matmul().  Always the row-tile kernels (rmm_force_path(2) does not
+ * apply); each 128 x 256 tile multiplies the gate columns f0..f0+127 and the
+ * matching up columns F+f0.., so the gate and up values of one output meet in
+ * the same accumulator row.  May use the per-(device, stream) workspace like
+ * rmsnorm_matmul().  Returns an rmm_status.
+ */
+int rmsnorm_matmul_swiglu(const void* X, const void* g, const void* W, void* Y,
+                          int64_t M, int64_t K, int64_t N, float eps, cudaStream_t stream);
+
+/*
  * Unfused RMSNorm alone (the first of the two kernels that the review page's
  * muGraph example says existing systems launch):
  *   Xn[m,k] = bf16( X[m,k] * g[k] * r[m] ),  X, Xn [M,K] bf16, g [K] bf16.
@@ -157,7 +175,8 @@ int rmsnorm_matmul_noalloc(const void* X, const void* g, const void* W, void* Y,
 /*
  * Launch plan the library would use for this shape on the current device
  * (introspection for tests and benchmarks; `fused` = 1 for rmsnorm_matmul,
- * 0 for matmul).  Fills info[0..7] with: path (1 row-tile, 2 small-M),
+ * 0 for matmul, 2 for rmsnorm_matmul_swiglu, whose N is the width of W).
+ * Fills info[0..7] with: path (1 row-tile, 2 small-M),
  * K splits, 1 if the splits reduce through a cluster's shared memory, grid
  * size, pipeline stages, padded rows MP, column tiles, k-blocks per split.
  * Queries device attributes; launches nothing.

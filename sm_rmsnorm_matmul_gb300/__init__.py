@@ -22,7 +22,8 @@ import threading
 from .build import LIB_PATH
 
 __all__ = [
-    "RmmError", "lib", "rmsnorm_matmul", "rmsnorm_matmul_noalloc", "rmsnorm", "matmul", "force_path",
+    "RmmError", "lib", "rmsnorm_matmul", "rmsnorm_matmul_noalloc", "rmsnorm_matmul_swiglu", "rmsnorm",
+    "matmul", "force_path",
     "dispatch_path", "describe_plan", "device_status", "status_string", "STATUS", "PATH_AUTO",
     "PATH_ROWS", "PATH_COLS", "ABI_FUNCTIONS",
 ]
@@ -37,7 +38,7 @@ PATH_AUTO, PATH_ROWS, PATH_COLS = 0, 1, 2
 # Every function declared in include/rmsnorm_matmul.h.
 ABI_FUNCTIONS = ("rmsnorm_matmul", "rmsnorm", "matmul", "rmm_force_path",
                  "rmm_device_status", "rmm_status_string", "rmm_dispatch_path",
-                 "rmsnorm_matmul_noalloc", "rmm_describe_plan")
+                 "rmsnorm_matmul_noalloc", "rmm_describe_plan", "rmsnorm_matmul_swiglu")
 
 
 class RmmError(RuntimeError):
@@ -54,6 +55,7 @@ def _bind(l: ctypes.CDLL) -> ctypes.CDLL:
     vp, i64, f32, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
     l.rmsnorm_matmul.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, vp]
     l.rmsnorm_matmul_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, vp]
+    l.rmsnorm_matmul_swiglu.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, vp]
     l.rmsnorm.argtypes = [vp, vp, vp, i64, i64, f32, vp]
     l.matmul.argtypes = [vp, vp, vp, i64, i64, i64, vp]
     l.rmm_force_path.argtypes = [i32]
@@ -62,8 +64,9 @@ def _bind(l: ctypes.CDLL) -> ctypes.CDLL:
     l.rmm_status_string.restype = ctypes.c_char_p
     l.rmm_dispatch_path.argtypes = [i64, i64, i64]
     l.rmm_describe_plan.argtypes = [i64, i64, i64, i32, ctypes.POINTER(ctypes.c_int)]
-    for name in ("rmsnorm_matmul", "rmsnorm_matmul_noalloc", "rmsnorm", "matmul", "rmm_force_path",
-                 "rmm_device_status", "rmm_dispatch_path", "rmm_describe_plan"):
+    for name in ("rmsnorm_matmul", "rmsnorm_matmul_noalloc", "rmsnorm_matmul_swiglu", "rmsnorm",
+                 "matmul", "rmm_force_path", "rmm_device_status", "rmm_dispatch_path",
+                 "rmm_describe_plan"):
         getattr(l, name).restype = i32
     return l
 
@@ -125,6 +128,30 @@ def rmsnorm_matmul(X, g, W, eps: float = 1e-6, out=None, stream=None):
             raise ValueError(f"out must have shape {(M, N)}")
     _raise(lib().rmsnorm_matmul(X.data_ptr(), g.data_ptr(), W.data_ptr(), out.data_ptr(),
                                 M, K, N, float(eps), _stream_ptr(stream)), "rmsnorm_matmul")
+    return out
+
+
+def rmsnorm_matmul_swiglu(X, g, W, eps: float = 1e-6, out=None, stream=None):
+    """Y[M,F] = silu(Z[:, :F]) * Z[:, F:] with Z = RMSNorm(X; g, eps) @ W, W [K, 2F]:
+    the gated MLP over the concatenated gate and up projections, one fused launch."""
+    import torch
+    _check_bf16("X", X, 2)
+    _check_bf16("g", g, 1)
+    _check_bf16("W", W, 2)
+    M, K = X.shape
+    if g.shape[0] != K or W.shape[0] != K or W.shape[1] % 2:
+        raise ValueError(f"shape mismatch: X {tuple(X.shape)}, g {tuple(g.shape)}, W {tuple(W.shape)}")
+    N = W.shape[1]
+    F = N // 2
+    if out is None:
+        out = torch.empty((M, F), dtype=torch.bfloat16, device=X.device)
+    else:
+        _check_bf16("out", out, 2)
+        if tuple(out.shape) != (M, F):
+            raise ValueError(f"out must have shape {(M, F)}")
+    _raise(lib().rmsnorm_matmul_swiglu(X.data_ptr(), g.data_ptr(), W.data_ptr(), out.data_ptr(),
+                                       M, K, N, float(eps), _stream_ptr(stream)),
+           "rmsnorm_matmul_swiglu")
     return out
 
 
@@ -202,10 +229,11 @@ def force_path(path: int) -> int:
 PLAN_FIELDS = ("path", "splits", "cluster", "grid", "stages", "MP", "tiles", "kb_per_split")
 
 
-def describe_plan(M: int, K: int, N: int, fused: bool = True) -> dict:
-    """The launch plan for this shape on the current device (no launch)."""
+def describe_plan(M: int, K: int, N: int, fused: bool = True, gated: bool = False) -> dict:
+    """The launch plan for this shape on the current device (no launch).
+    gated: the plan of rmsnorm_matmul_swiglu (N is then the width of W)."""
     info = (ctypes.c_int * 8)()
-    _raise(lib().rmm_describe_plan(M, K, N, int(fused), info), "rmm_describe_plan")
+    _raise(lib().rmm_describe_plan(M, K, N, 2 if gated else int(fused), info), "rmm_describe_plan")
     return dict(zip(PLAN_FIELDS, list(info)))
 
 

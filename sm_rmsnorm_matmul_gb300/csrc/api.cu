@@ -318,26 +318,27 @@ struct RowsPlan {
     int overlay;
 };
 
-int rows_stages(int xrows, int red_slots, int MP, const DeviceInfo& d, bool overlay = false) {
-    const size_t fixed = rmm::rows_smem_bytes(xrows, 0, red_slots, MP, overlay);
+int rows_stages(int xrows, int red_slots, int MP, const DeviceInfo& d, bool overlay = false,
+                bool glu = false) {
+    const size_t fixed = rmm::rows_smem_bytes(xrows, 0, red_slots, MP, overlay, glu);
     const size_t per = rmm::rows_stage_bytes(xrows);
     const size_t avail = d.smem_optin > 0 ? static_cast<size_t>(d.smem_optin) : 227 * 1024;
     int st = avail > fixed ? static_cast<int>((avail - fixed) / per) : 0;
     st = std::min(rmm::kRowsMaxStages, st);
     // the X tiles are padded to 1 KB as a whole
-    while (st > 0 && rmm::rows_smem_bytes(xrows, st, red_slots, MP, overlay) > avail) --st;
+    while (st > 0 && rmm::rows_smem_bytes(xrows, st, red_slots, MP, overlay, glu) > avail) --st;
     return st;
 }
 
 std::mutex g_rows_occ_mu;
-std::map<std::tuple<int, bool, int, size_t>, int> g_rows_occ;
+std::map<std::tuple<int, bool, int, size_t, bool>, int> g_rows_occ;
 
-int rows_max_clusters(int dev, bool fused, int splits, size_t smem) {
+int rows_max_clusters(int dev, bool fused, int splits, size_t smem, bool glu) {
     std::lock_guard<std::mutex> lk(g_rows_occ_mu);
-    auto key = std::make_tuple(dev, fused, splits, smem);
+    auto key = std::make_tuple(dev, fused, splits, smem, glu);
     auto it = g_rows_occ.find(key);
     if (it != g_rows_occ.end()) return it->second;
-    const int n = rmm::rows_max_active_clusters(fused, splits, smem);
+    const int n = rmm::rows_max_active_clusters(fused, splits, smem, glu);
     g_rows_occ[key] = n;
     return n;
 }
@@ -347,11 +348,14 @@ int rows_max_clusters(int dev, bool fused, int splits, size_t smem) {
 // 16 rows, and K split over 1..8 CTAs of a cluster chosen with a model of one
 // launch in microseconds (fitted to GB300 measurements): each CTA streams W at
 // about 55 GB/s, the GPU at about 6 TB/s, a unit costs about 1 us of fill and
-// drain, and the cluster reduction about 1.5 us.
-RowsPlan plan_rows(int dev, bool fused, int64_t M, int64_t K, int64_t N, const DeviceInfo& d) {
+// drain, and the cluster reduction about 1.5 us.  glu: the gated form, whose
+// tiles cover 128 output columns (256 columns of W, N = 2F).
+RowsPlan plan_rows(int dev, bool fused, int64_t M, int64_t K, int64_t N, const DeviceInfo& d,
+                   bool glu = false) {
     RowsPlan p{};
     p.m_tiles = static_cast<int>((M + rmm::kRowsBM - 1) / rmm::kRowsBM);
-    p.n_tiles = static_cast<int>((N + rmm::kRowsBN - 1) / rmm::kRowsBN);
+    p.n_tiles = glu ? static_cast<int>((N / 2 + rmm::kRowsBN / 2 - 1) / (rmm::kRowsBN / 2))
+                    : static_cast<int>((N + rmm::kRowsBN - 1) / rmm::kRowsBN);
     p.k_blocks = static_cast<int>((K + kBK - 1) / kBK);
     p.MP = static_cast<int>(std::min<int64_t>(rmm::kRowsBM, ((M + 15) / 16) * 16));
     const int sms = d.sm_count > 0 ? d.sm_count : 1;
@@ -371,15 +375,15 @@ RowsPlan plan_rows(int dev, bool fused, int64_t M, int64_t K, int64_t N, const D
         const int kbps = (p.k_blocks + s - 1) / s;
         if ((p.k_blocks + kbps - 1) / kbps != s) continue;
         const int red_slots = s > 1 ? s : 0;
-        int st = rows_stages(p.xrows, red_slots, p.MP, d);
+        int st = rows_stages(p.xrows, red_slots, p.MP, d, false, glu);
         // A receive area of its own that leaves fewer than 3 stages: put the
         // receive blocks over the pipeline buffers instead.  The extra
         // handshake measured ~0.5 us, more than going from 3 to 5 stages
         // bought (M = 64), less than going from 2 stages or none (M > 64).
         bool overlay = false;
         if (s > 1 && st < 3) {
-            const int so = rows_stages(p.xrows, red_slots, p.MP, d, true);
-            if (so > st && so >= 2 && rmm::rows_overlay_fits(p.xrows, so, s, p.MP)) {
+            const int so = rows_stages(p.xrows, red_slots, p.MP, d, true, glu);
+            if (so > st && so >= 2 && rmm::rows_overlay_fits(p.xrows, so, s, p.MP, glu)) {
                 st = so;
                 overlay = true;
             }
@@ -388,7 +392,8 @@ RowsPlan plan_rows(int dev, bool fused, int64_t M, int64_t K, int64_t N, const D
         int resident = sms;
         if (s > 1) {
             resident = rows_max_clusters(dev, fused, s,
-                                         rmm::rows_smem_bytes(p.xrows, st, red_slots, p.MP, overlay)) * s;
+                                         rmm::rows_smem_bytes(p.xrows, st, red_slots, p.MP, overlay, glu),
+                                         glu) * s;
             if (resident <= 0) continue;
         }
         const long units = static_cast<long>(p.n_tiles) * s;
@@ -425,13 +430,15 @@ int choose_path(int64_t M) {
 
 // One launch of the tensor-core contraction, fused (RMSNorm folded in) or not.
 // Without may_allocate, plans that need the per-stream workspace are avoided.
+// glu: the gated form (fused only; always the row-tile path), Y [M, N / 2].
 int run_contraction(bool fused, const void* X, const void* g, const void* W, void* Y, int64_t M,
-                    int64_t K, int64_t N, float eps, cudaStream_t stream, bool may_allocate = true) {
+                    int64_t K, int64_t N, float eps, cudaStream_t stream, bool may_allocate = true,
+                    bool glu = false) {
     int dev = 0;
     DeviceInfo d;
     int rc = current_device(&dev, &d);
     if (rc != RMM_OK) return rc;
-    const int path = choose_path(M);
+    const int path = glu ? static_cast<int>(kPathRows) : choose_path(M);
     CUtensorMap tmX, tmW, tmG;
     if (!map_2d(&tmW, W, K, N, kBK)) return RMM_ERR_INTERNAL;
     if (fused) {
@@ -469,7 +476,7 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
         return rmm::launch_cols(fused, tmX, tmW, tmG, Y, a, stream) == cudaSuccess ? RMM_OK
                                                                                   : RMM_ERR_LAUNCH;
     }
-    const RowsPlan p = plan_rows(dev, fused, M, K, N, d);
+    const RowsPlan p = plan_rows(dev, fused, M, K, N, d, glu);
     if (!map_2d(&tmX, X, M, K, p.xrows)) return RMM_ERR_INTERNAL;
     if (!fused) tmG = tmX;
     rmm::RowsLaunch a{};
@@ -488,12 +495,13 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
     a.stages = p.stages;
     a.grid = p.grid;
     a.red_overlay = p.overlay;
+    a.glu = glu ? 1 : 0;
     CUtensorMap tmY;
     a.tail_tiles = 0;
     a.tail_pieces = 1;
     a.tail_kbp = p.k_blocks;
     if (fused && !p.cluster && p.xrows == rmm::kRowsBM) {
-        if (!map_2d_store(&tmY, Y, M, N)) return RMM_ERR_INTERNAL;
+        if (!map_2d_store(&tmY, Y, M, glu ? N / 2 : N)) return RMM_ERR_INTERNAL;
         a.tmY = &tmY;
         // When the tiles leave a last wave at most half full, cut those tiles
         // along K so that every CTA has a share of them.
@@ -538,6 +546,19 @@ int rmsnorm_matmul(const void* X, const void* g, const void* W, void* Y, int64_t
     return run_contraction(true, X, g, W, Y, M, K, N, eps, stream);
 }
 
+int rmsnorm_matmul_swiglu(const void* X, const void* g, const void* W, void* Y, int64_t M,
+                          int64_t K, int64_t N, float eps, cudaStream_t stream) {
+    int rc = check_sizes(M, K, N, eps, true);
+    if (rc == kNoop) return RMM_OK;
+    if (rc != RMM_OK) return rc;
+    if (N % 16 != 0) return RMM_ERR_ALIGNMENT;   // F = N / 2 must be a multiple of 8
+    rc = check_ptrs(Y, static_cast<size_t>(M) * (N / 2) * 2,
+                    {{X, static_cast<size_t>(M) * K * 2}, {g, static_cast<size_t>(K) * 2},
+                     {W, static_cast<size_t>(K) * N * 2}});
+    if (rc != RMM_OK) return rc;
+    return run_contraction(true, X, g, W, Y, M, K, N, eps, stream, true, true);
+}
+
 int matmul(const void* A, const void* B, void* C, int64_t M, int64_t K, int64_t N,
            cudaStream_t stream) {
     int rc = check_sizes(M, K, N, 0.f, false);
@@ -574,13 +595,14 @@ int rmm_force_path(int path) {
 }
 
 int rmm_describe_plan(int64_t M, int64_t K, int64_t N, int fused, int* info) {
-    if (!info || M < 1 || K < 1 || N < 1) return RMM_ERR_INVALID_ARG;
+    if (!info || M < 1 || K < 1 || N < 1 || fused < 0 || fused > 2) return RMM_ERR_INVALID_ARG;
+    const bool glu = fused == 2;
     int dev = 0;
     DeviceInfo d;
     int rc = current_device(&dev, &d);
     if (rc != RMM_OK) return rc;
     for (int i = 0; i < 8; ++i) info[i] = 0;
-    info[0] = choose_path(M);
+    info[0] = glu ? static_cast<int>(kPathRows) : choose_path(M);
     if (info[0] == kPathCols) {
         if (M > rmm::kColsMaxMP) return RMM_ERR_INVALID_ARG;
         const ColsPlan p = plan_cols(dev, fused != 0, M, K, N, d, true);
@@ -592,7 +614,7 @@ int rmm_describe_plan(int64_t M, int64_t K, int64_t N, int fused, int* info) {
         info[6] = p.n_tiles;
         info[7] = p.kb_per_split;
     } else {
-        const RowsPlan p = plan_rows(dev, fused != 0, M, K, N, d);
+        const RowsPlan p = plan_rows(dev, fused != 0, M, K, N, d, glu);
         info[1] = p.splits;
         info[2] = p.cluster;
         info[3] = p.grid;

@@ -92,11 +92,23 @@ struct RowsLayout {
     uint32_t xbytes, off_x, off_w, off_g, off_red, red_block, off_bar, off_sr, off_misc, total;
 };
 
-// Column chunks of 32 in a row tile; with a cluster K split of S, chunk c is
-// reduced by CTA c % S, which therefore owns at most ceil(8 / S) chunks.
+// Column chunks of 32 in a row tile.  With a cluster K split of S, the
+// chunks are reduced in units: one chunk each, or, for the gated form, a
+// gate chunk and the up chunk 128 columns further (the tile's 256 columns are
+// 128 gate columns then the 128 matching up columns).  Unit u is reduced by
+// CTA u % S, which therefore owns at most ceil(units / S) units.
 constexpr int kRowsChunks = kRowsBN / 32;
-__host__ __device__ inline int rows_owned_max(int splits) {
-    return (kRowsChunks + splits - 1) / splits;
+__host__ __device__ inline int rows_red_units(bool glu) { return glu ? kRowsChunks / 2 : kRowsChunks; }
+__host__ __device__ inline int rows_owned_max(int splits, bool glu) {
+    return (rows_red_units(glu) + splits - 1) / splits;
+}
+
+// Swish gate, single precision: silu(z) = z / (1 + e^-z).
+__device__ __forceinline__ float silu_f(float z) { return z / (1.f + __expf(-z)); }
+// Output of the gated form from the gate and up accumulators of a row whose
+// reciprocal RMS is r.
+__device__ __forceinline__ float glu_out(float gate, float up, float r) {
+    return silu_f(gate * r) * (up * r);
 }
 
 // Shared-memory layout of rows_kernel.  xrows: rows of X each stage loads
@@ -104,18 +116,19 @@ __host__ __device__ inline int rows_owned_max(int splits) {
 // first: the MMA always reads a 128-row window from an X tile, whose rows
 // past xrows (discarded results) fall on the following tiles.  red_slots:
 // with a cluster K split of S = red_slots, each CTA receives one block per
-// split, [MP] fp32 row sums of squares followed by [ceil(8/S)][MP][32] fp32
-// partial rows of the chunks it owns (the 16-byte pieces of a row rotated by
-// row & 7 against bank conflicts).  With overlay, the receive blocks occupy
-// the start of the pipeline buffers, which are idle by the time they fill.
+// split, [MP] fp32 row sums of squares followed by [ceil(units/S)][1 or 2
+// chunks][MP][32] fp32 partial rows of the units it owns (the 16-byte pieces
+// of a row rotated by row & 7 against bank conflicts).  With overlay, the
+// receive blocks occupy the start of the pipeline buffers, which are idle by
+// the time they fill.
 __host__ __device__ inline RowsLayout rows_layout(int xrows, int stages, int red_slots, int MP,
-                                                  bool overlay = false) {
+                                                  bool overlay = false, bool glu = false) {
     RowsLayout L;
     L.xbytes = xrows * kBK * 2;
     L.off_x = 0;
     L.off_w = ((stages * L.xbytes + 1023) / 1024) * 1024;
     L.off_g = L.off_w + stages * kRowsWBytes;
-    L.red_block = red_slots > 0 ? MP * (4 + rows_owned_max(red_slots) * 128) : 0;
+    L.red_block = red_slots > 0 ? MP * (4 + rows_owned_max(red_slots, glu) * (glu ? 2 : 1) * 128) : 0;
     L.off_red = overlay ? 0 : ((L.off_g + stages * kGBytes + 15) / 16) * 16;
     L.off_bar = overlay ? ((L.off_g + stages * kGBytes + 15) / 16) * 16 : L.off_red + red_slots * L.red_block;
     const uint32_t nbars = 3 * kRowsMaxStages + 10;
@@ -126,7 +139,7 @@ __host__ __device__ inline RowsLayout rows_layout(int xrows, int stages, int red
 }
 
 
-template <bool kFused, bool kSplit>
+template <bool kFused, bool kSplit, bool kGlu>
 __global__ void __launch_bounds__(kThreads, 1)
     rows_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                 const __grid_constant__ CUtensorMap tmG, __nv_bfloat16* __restrict__ Y,
@@ -135,7 +148,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = align1024(smem_raw);
     const int S = a.stages;
     const int split = kSplit ? a.splits : 1;
-    const RowsLayout L = rows_layout(a.xrows, S, kSplit ? split : 0, a.MP, kSplit && a.red_overlay);
+    const RowsLayout L = rows_layout(a.xrows, S, kSplit ? split : 0, a.MP, kSplit && a.red_overlay, kGlu);
+    // Output columns: N, or F = N / 2 for the gated form, whose tile covers
+    // 128 output columns from two W column ranges (gate, then up).
+    const int Nout = kGlu ? a.N / 2 : a.N;
+    constexpr int kOutBN = kGlu ? kRowsBN / 2 : kRowsBN;
     const uint32_t xbytes = L.xbytes;
     const uint32_t sb = smem_u32(smem);
     const uint32_t sx = sb + L.off_x, sw = sb + L.off_w, sg = sb + L.off_g;
@@ -167,13 +184,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool bad_launch = kSplit && (units > static_cast<int>(gridDim.x) ||
                                        (a.red_overlay && split * L.red_block > L.off_g));
     if (bad_launch) units = 0;
+    // W boxes of 64 columns for the tile whose output columns start at n0:
+    // plain, the columns themselves (as many as fall inside N); gated, two
+    // boxes of gate columns n0.. and two of up columns Nout + n0.. (always
+    // four: a box past the gate half reads up columns, one past N reads
+    // zeros, and neither reaches an output column).
+    auto tile_nbox = [&](int n0) { return kGlu ? 4 : min(4, (a.N - n0 + 63) / 64); };
+    auto wcol = [&](int n0, int j) { return kGlu && j >= 2 ? Nout + n0 + 64 * (j - 2) : n0 + 64 * j; };
     // Loads of stage s = k-block kb of the unit whose tile starts at row block
-    // mb and column n0 (nbox W boxes of 64 columns).
+    // mb and output column n0.
     auto issue = [&](uint32_t s, int kb, int mb, int n0, int nbox) {
         mbar_arrive_expect_tx(full(s), xbytes + nbox * kWBoxBytes + (kFused ? kGBytes : 0));
         tma_load_2d_nohint(sx + s * xbytes, &tmX, full(s), kb * kBK, mb * kRowsBM);
         for (int j = 0; j < nbox; ++j)
-            tma_load_2d_nohint(sw + s * kRowsWBytes + j * kWBoxBytes, &tmW, full(s), n0 + 64 * j, kb * kBK);
+            tma_load_2d_nohint(sw + s * kRowsWBytes + j * kWBoxBytes, &tmW, full(s), wcol(n0, j), kb * kBK);
         if (kFused) tma_load_1d(sg + s * kGBytes, &tmG, full(s), kb * kBK);
     };
     // k-blocks of the first unit that thread 0 (the producer) issues before
@@ -209,9 +233,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int kb0 = sp * a.kb_per_split, kb1 = min(a.k_blocks, kb0 + a.kb_per_split);
             int mb, nb;
             rows_tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
-            const int n0 = nb * kRowsBN;
+            const int n0 = nb * kOutBN;
             pro = static_cast<uint32_t>(min(S, kb1 - kb0));
-            for (uint32_t i = 0; i < pro; ++i) issue(i, kb0 + static_cast<int>(i), mb, n0, min(4, (a.N - n0 + 63) / 64));
+            for (uint32_t i = 0; i < pro; ++i) issue(i, kb0 + static_cast<int>(i), mb, n0, tile_nbox(n0));
         }
     }
     if (warp == 2) {
@@ -239,8 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int kb0 = sp * a.kb_per_split, kb1 = min(a.k_blocks, kb0 + a.kb_per_split);
                 int mb, nb;
                 rows_tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
-                const int n0 = nb * kRowsBN;
-                const int nbox = min(4, (a.N - n0 + 63) / 64);
+                const int n0 = nb * kOutBN;
+                const int nbox = tile_nbox(n0);
                 const int first = kb0 + (u == static_cast<int>(blockIdx.x) ? static_cast<int>(pro) : 0);
                 for (int kb = first; kb < kb1; ++kb) {
                     const uint32_t s = ring.idx, ph = ring.phase;
@@ -357,32 +381,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             int mb, nb;
             rows_tile_coords(u, a.m_tiles, a.n_tiles, mb, nb);
-            const int n0 = nb * kRowsBN;
-            const int ncols = min(kRowsBN, a.N - n0);
+            const int n0 = nb * kOutBN;
+            const int ncols = min(kOutBN, Nout - n0);
             const int rows_here = min(kRowsBM, a.M - mb * kRowsBM);   // valid rows of this tile
             const uint32_t taddr = tmem + buf * kRowsBN + (static_cast<uint32_t>(q * 32) << 16);
             const bool warp_has_rows = q * 32 < rows_here;              // warp-uniform
             const int m = mb * kRowsBM + row;
             const float r = kFused ? rsqrtf(sr[buf * kRowsBM + row] * inv_k + a.eps) : 1.f;
-            __nv_bfloat16* yrow = Y + static_cast<size_t>(m) * a.N + n0;
-            for (int c = 0; warp_has_rows && c < kRowsBN / 32; ++c) {
+            __nv_bfloat16* yrow = Y + static_cast<size_t>(m) * Nout + n0;
+            for (int c = 0; warp_has_rows && c < kOutBN / 32; ++c) {
                 if (c * 32 >= ncols) break;   // warp-uniform
-                uint32_t v[32];
+                uint32_t v[32], w2[kGlu ? 32 : 1];
                 tmem_ld_32x32(taddr + c * 32, v);
+                if constexpr (kGlu) tmem_ld_32x32(taddr + kOutBN + c * 32, w2);
+                auto out = [&](int i) {
+                    if constexpr (kGlu) return glu_out(__uint_as_float(v[i]), __uint_as_float(w2[i]), r);
+                    else return __uint_as_float(v[i]) * r;
+                };
                 if (row < rows_here) {
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
                         const int col = c * 32 + g * 8;
                         if (col < ncols) {
                             uint4 o;
-                            o.x = pack_bf16x2(__uint_as_float(v[g * 8 + 0]) * r,
-                                              __uint_as_float(v[g * 8 + 1]) * r);
-                            o.y = pack_bf16x2(__uint_as_float(v[g * 8 + 2]) * r,
-                                              __uint_as_float(v[g * 8 + 3]) * r);
-                            o.z = pack_bf16x2(__uint_as_float(v[g * 8 + 4]) * r,
-                                              __uint_as_float(v[g * 8 + 5]) * r);
-                            o.w = pack_bf16x2(__uint_as_float(v[g * 8 + 6]) * r,
-                                              __uint_as_float(v[g * 8 + 7]) * r);
+                            o.x = pack_bf16x2(out(g * 8 + 0), out(g * 8 + 1));
+                            o.y = pack_bf16x2(out(g * 8 + 2), out(g * 8 + 3));
+                            o.z = pack_bf16x2(out(g * 8 + 4), out(g * 8 + 5));
+                            o.w = pack_bf16x2(out(g * 8 + 6), out(g * 8 + 7));
                             *reinterpret_cast<uint4*>(yrow + col) = o;
                         }
                     }
@@ -420,17 +445,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int me = static_cast<int>(rank);
         int mb = 0, nb = 0;
         if (have) rows_tile_coords(u / split, a.m_tiles, a.n_tiles, mb, nb);
-        const int n0 = nb * kRowsBN;
-        const int ncols = min(kRowsBN, a.N - n0);
+        const int n0 = nb * kOutBN;
+        const int ncols = min(kOutBN, Nout - n0);   // output columns of this tile
         const int rows_here = min(kRowsBM, a.M - mb * kRowsBM);
-        const int nchunks = (ncols + 31) / 32;
-        const int owned = nchunks > me ? (nchunks - 1 - me) / split + 1 : 0;
+        // reduction units of 32 output columns: accumulator chunk u, or (gated)
+        // gate chunk u with up chunk u + 4
+        constexpr int kUnitChunks = kGlu ? 2 : 1;
+        const int nunits = (ncols + 31) / 32;
+        const int owned = nunits > me ? (nunits - 1 - me) / split + 1 : 0;
         const uint32_t blk = L.red_block;
         const uint32_t my_block = red_addr + rank * blk;   // this split's block in every CTA
         const int q = warp & 3, team = warp >> 2;
         const int row = q * 32 + lane;
         if (have && threadIdx.x == 0)
-            mbar_arrive_expect_tx(redfull, static_cast<uint32_t>((split - 1) * rows_here * (4 + owned * 128)));
+            mbar_arrive_expect_tx(redfull,
+                                  static_cast<uint32_t>((split - 1) * rows_here * (4 + owned * kUnitChunks * 128)));
         cluster_wait();    // the peers' barriers are initialised
         // 1. tensor memory -> owners
         if (have && q * 32 < rows_here &&
@@ -447,12 +476,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
             const uint32_t swz = static_cast<uint32_t>(row & 7);
-            for (int c = team; c < nchunks; c += kThreads / 128) {
+            for (int c = team; c < kRowsChunks; c += kThreads / 128) {
+                const int unit = kGlu ? (c & (kRowsChunks / 2 - 1)) : c, half = kGlu ? c / (kRowsChunks / 2) : 0;
+                if (unit >= nunits) continue;   // warp-uniform
                 uint32_t v[32];
                 tmem_ld_32x32(taddr + c * 32, v);
                 if (row < rows_here) {
-                    const int owner = c % split;
-                    const uint32_t dst = my_block + a.MP * 4 + ((c / split) * a.MP + row) * 128;
+                    const int owner = unit % split;
+                    const uint32_t dst =
+                        my_block + a.MP * 4 + (((unit / split) * kUnitChunks + half) * a.MP + row) * 128;
                     if (owner == me) {
 #pragma unroll
                         for (int g = 0; g < 8; ++g)
@@ -487,33 +519,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = threadIdx.x; i < n3; i += kThreads) {
                 const int g = i & 7, j = (i >> 3) % owned, rr = (i >> 3) / owned;
                 const uint32_t piece = static_cast<uint32_t>((g ^ (rr & 7)) << 4);
-                // every split's piece and row sum in flight before the first add
+                // every split's pieces and row sum in flight before the first add
                 float ssv[kClusterMaxSplits];
-                uint4 t4[kClusterMaxSplits];
+                uint4 t4[kClusterMaxSplits][kUnitChunks];
 #pragma unroll
                 for (int s2 = 0; s2 < kClusterMaxSplits; ++s2)
                     if (s2 < split) {
                         ssv[s2] = *reinterpret_cast<const float*>(smem + L.off_red + s2 * blk + rr * 4);
-                        t4[s2] = lds128(red_addr + s2 * blk + a.MP * 4 + (j * a.MP + rr) * 128 + piece);
+#pragma unroll
+                        for (int h = 0; h < kUnitChunks; ++h)
+                            t4[s2][h] = lds128(red_addr + s2 * blk + a.MP * 4 +
+                                               ((j * kUnitChunks + h) * a.MP + rr) * 128 + piece);
                     }
                 float tot = 0.f;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                float4 acc[kUnitChunks];
+#pragma unroll
+                for (int h = 0; h < kUnitChunks; ++h) acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int s2 = 0; s2 < kClusterMaxSplits; ++s2)
                     if (s2 < split) {
                         tot += ssv[s2];
-                        acc.x += __uint_as_float(t4[s2].x);
-                        acc.y += __uint_as_float(t4[s2].y);
-                        acc.z += __uint_as_float(t4[s2].z);
-                        acc.w += __uint_as_float(t4[s2].w);
+#pragma unroll
+                        for (int h = 0; h < kUnitChunks; ++h) {
+                            acc[h].x += __uint_as_float(t4[s2][h].x);
+                            acc[h].y += __uint_as_float(t4[s2][h].y);
+                            acc[h].z += __uint_as_float(t4[s2][h].z);
+                            acc[h].w += __uint_as_float(t4[s2][h].w);
+                        }
                     }
                 const float r = kFused ? rsqrtf(tot * inv_k + a.eps) : 1.f;
                 const int col = (me + j * split) * 32 + g * 4;
                 if (col < ncols) {
+                    float o4[4];
+                    if constexpr (kGlu) {
+                        o4[0] = glu_out(acc[0].x, acc[kUnitChunks - 1].x, r);
+                        o4[1] = glu_out(acc[0].y, acc[kUnitChunks - 1].y, r);
+                        o4[2] = glu_out(acc[0].z, acc[kUnitChunks - 1].z, r);
+                        o4[3] = glu_out(acc[0].w, acc[kUnitChunks - 1].w, r);
+                    } else {
+                        o4[0] = acc[0].x * r;
+                        o4[1] = acc[0].y * r;
+                        o4[2] = acc[0].z * r;
+                        o4[3] = acc[0].w * r;
+                    }
                     uint2 o;
-                    o.x = pack_bf16x2(acc.x * r, acc.y * r);
-                    o.y = pack_bf16x2(acc.z * r, acc.w * r);
-                    *reinterpret_cast<uint2*>(Y + static_cast<size_t>(mb * kRowsBM + rr) * a.N + n0 + col) = o;
+                    o.x = pack_bf16x2(o4[0], o4[1]);
+                    o.y = pack_bf16x2(o4[2], o4[3]);
+                    *reinterpret_cast<uint2*>(Y + static_cast<size_t>(mb * kRowsBM + rr) * Nout + n0 + col) = o;
                 }
             }
         }
@@ -586,6 +638,7 @@ __device__ __forceinline__ bool ta_unit(const RowsLaunch& a, int i, TaUnit& u) {
     return true;
 }
 
+template <bool kGlu>
 __global__ void __launch_bounds__(kThreads, 1)
     rows_ta_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmY,
@@ -657,6 +710,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) grid_dep_launch();
     const uint32_t tmem = *tmem_holder;
     const int num_tiles = a.m_tiles * a.n_tiles;
+    // Output columns: N, or F = N / 2 for the gated form, whose tile covers
+    // 128 output columns read from gate columns n0.. and up columns F + n0..
+    const int Nout = kGlu ? a.N / 2 : a.N;
+    constexpr int kOutBN = kGlu ? kRowsBN / 2 : kRowsBN;
 
     if (warp == 0 || warp == 3) {
         // ------------------------------------------------ TMA producers
@@ -673,8 +730,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; ok && ta_unit(a, i, un); ++i) {
                 int mb, nb;
                 rows_tile_coords(un.t, a.m_tiles, a.n_tiles, mb, nb);
-                const int n0 = nb * kRowsBN;
-                const int nbox = min(4, (a.N - n0 + 63) / 64);
+                const int n0 = nb * kOutBN;
+                const int nbox = kGlu ? 4 : min(4, (a.N - n0 + 63) / 64);
                 for (int kb = un.kb0; kb < un.kb1; ++kb) {
                     if (!mbar_wait(empty0 + 8 * ring.idx, ring.phase ^ 1, abort)) { ok = false; break; }
                     const uint32_t f = full0 + 8 * ring.idx;
@@ -686,7 +743,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive_expect_tx(f, nbox * kWBoxBytes);
                         for (int j = 0; j < nbox; ++j)
                             tma_load_2d_nohint(sw + ring.idx * kRowsWBytes + j * kWBoxBytes, &tmW, f,
-                                               n0 + 64 * j, kb * kBK);
+                                               kGlu && j >= 2 ? Nout + n0 + 64 * (j - 2) : n0 + 64 * j,
+                                               kb * kBK);
                     }
                     ring.advance();
                     ++issued;
@@ -817,7 +875,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(srempty0 + 8 * buf);
             int mb, nb;
             rows_tile_coords(un.t, a.m_tiles, a.n_tiles, mb, nb);
-            const int n0 = nb * kRowsBN;
+            const int n0 = nb * kOutBN;
             const uint32_t taddr = tmem + kTaAccCol + (static_cast<uint32_t>(q * 32) << 16);
             if (un.piece >= 0) {
                 // A K piece of a tail tile: publish the fp32 partial and the
@@ -858,39 +916,65 @@ __global__ void __launch_bounds__(kThreads, 1)
                     rr[e] = rsqrtf(tot * inv_k + a.eps);
                 }
                 ok = epi_sync() && ok;
-                const int items = (r1 - r0) * (kRowsBN / 4);
+                // items: 4 output columns of one row; gated, from the gate
+                // partial at accumulator column col and the up partial 128
+                // columns further
+                constexpr int kHalves = kGlu ? 2 : 1;
+                const int items = (r1 - r0) * (kOutBN / 4);
                 for (int it = e; ok && it < items; it += 128) {
-                    const int rl = it / (kRowsBN / 4), col = (it % (kRowsBN / 4)) * 4;
+                    const int rl = it / (kOutBN / 4), col = (it % (kOutBN / 4)) * 4;
                     const int m = mb * kRowsBM + r0 + rl;
                     const float* src = a.ws_acc + (slot * kRowsBM + r0 + rl) * kRowsBN + col;
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    float4 acc[kHalves];
+#pragma unroll
+                    for (int h = 0; h < kHalves; ++h) acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
                     int p2 = 0;
                     for (; p2 + 4 <= P; p2 += 4) {
-                        float4 t4[4];
+                        float4 t4[4][kHalves];
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            t4[j] = __ldcg(reinterpret_cast<const float4*>(src + static_cast<size_t>(p2 + j) * kRowsBM * kRowsBN));
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            acc.x += t4[j].x;
-                            acc.y += t4[j].y;
-                            acc.z += t4[j].z;
-                            acc.w += t4[j].w;
+                            for (int h = 0; h < kHalves; ++h)
+                                t4[j][h] = __ldcg(reinterpret_cast<const float4*>(
+                                    src + static_cast<size_t>(p2 + j) * kRowsBM * kRowsBN + h * kOutBN));
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+#pragma unroll
+                            for (int h = 0; h < kHalves; ++h) {
+                                acc[h].x += t4[j][h].x;
+                                acc[h].y += t4[j][h].y;
+                                acc[h].z += t4[j][h].z;
+                                acc[h].w += t4[j][h].w;
+                            }
+                    }
+                    for (; p2 < P; ++p2)
+#pragma unroll
+                        for (int h = 0; h < kHalves; ++h) {
+                            const float4 t4 = __ldcg(reinterpret_cast<const float4*>(
+                                src + static_cast<size_t>(p2) * kRowsBM * kRowsBN + h * kOutBN));
+                            acc[h].x += t4.x;
+                            acc[h].y += t4.y;
+                            acc[h].z += t4.z;
+                            acc[h].w += t4.w;
                         }
-                    }
-                    for (; p2 < P; ++p2) {
-                        const float4 t4 = __ldcg(reinterpret_cast<const float4*>(src + static_cast<size_t>(p2) * kRowsBM * kRowsBN));
-                        acc.x += t4.x;
-                        acc.y += t4.y;
-                        acc.z += t4.z;
-                        acc.w += t4.w;
-                    }
-                    if (m < a.M && n0 + col < a.N) {
+                    if (m < a.M && n0 + col < Nout) {
                         const float r = rr[rl];
+                        float o4[4];
+                        if constexpr (kGlu) {
+                            o4[0] = glu_out(acc[0].x, acc[kHalves - 1].x, r);
+                            o4[1] = glu_out(acc[0].y, acc[kHalves - 1].y, r);
+                            o4[2] = glu_out(acc[0].z, acc[kHalves - 1].z, r);
+                            o4[3] = glu_out(acc[0].w, acc[kHalves - 1].w, r);
+                        } else {
+                            o4[0] = acc[0].x * r;
+                            o4[1] = acc[0].y * r;
+                            o4[2] = acc[0].z * r;
+                            o4[3] = acc[0].w * r;
+                        }
                         uint2 o;
-                        o.x = pack_bf16x2(acc.x * r, acc.y * r);
-                        o.y = pack_bf16x2(acc.z * r, acc.w * r);
-                        *reinterpret_cast<uint2*>(Y + static_cast<size_t>(m) * a.N + n0 + col) = o;
+                        o.x = pack_bf16x2(o4[0], o4[1]);
+                        o.y = pack_bf16x2(o4[2], o4[3]);
+                        *reinterpret_cast<uint2*>(Y + static_cast<size_t>(m) * Nout + n0 + col) = o;
                     }
                 }
                 // the last piece through resets the tile's counters for the next launch
@@ -902,23 +986,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
             const float r = rsqrtf(ss_row * inv_k + a.eps);
-            uint32_t pk[kRowsBN / 2];   // the row, scaled and packed as bf16x2
+            uint32_t pk[kOutBN / 2];   // the row's outputs, packed as bf16x2
 #pragma unroll
-            for (int c = 0; c < kRowsBN / 16; ++c) {
+            for (int c = 0; c < kOutBN / 16; ++c) {
                 uint32_t v[16];
                 tmem_ld_32x16(taddr + c * 16, v);
+                if constexpr (kGlu) {
+                    uint32_t w2[16];
+                    tmem_ld_32x16(taddr + kOutBN + c * 16, w2);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    pk[c * 8 + i] = pack_bf16x2(__uint_as_float(v[2 * i]) * r,
-                                                __uint_as_float(v[2 * i + 1]) * r);
+                    for (int i = 0; i < 8; ++i)
+                        pk[c * 8 + i] = pack_bf16x2(
+                            glu_out(__uint_as_float(v[2 * i]), __uint_as_float(w2[2 * i]), r),
+                            glu_out(__uint_as_float(v[2 * i + 1]), __uint_as_float(w2[2 * i + 1]), r));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        pk[c * 8 + i] = pack_bf16x2(__uint_as_float(v[2 * i]) * r,
+                                                    __uint_as_float(v[2 * i + 1]) * r);
+                }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(accempty);   // the MMA may start the next tile
             bool ok = true;
 #pragma unroll
-            for (int c = 0; c < kRowsBN / 32; ++c) {
-                if (n0 + c * 32 < a.N) {              // block-uniform
+            for (int c = 0; c < kOutBN / 32; ++c) {
+                if (n0 + c * 32 < Nout) {             // block-uniform
                     const uint32_t sbuf = sout + (chunks & 1) * kTaStageOut;
                     // the store issued two chunks ago must have read this buffer
                     if (e == 0) bulk_wait_group_read<1>();
@@ -1411,7 +1505,7 @@ __global__ void __launch_bounds__(kNormThreads)
 // Raises a kernel's dynamic shared-memory limit to the device's opt-in
 // maximum, once per (kernel slot, device).
 cudaError_t ensure_smem_attr(const void* func, int slot) {
-    static int done[8][64] = {};
+    static int done[16][64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -1426,11 +1520,11 @@ cudaError_t ensure_smem_attr(const void* func, int slot) {
 
 }  // namespace
 
-size_t rows_smem_bytes(int xrows, int stages, int red_slots, int MP, bool overlay) {
-    return rows_layout(xrows, stages, red_slots, MP, overlay).total;
+size_t rows_smem_bytes(int xrows, int stages, int red_slots, int MP, bool overlay, bool glu) {
+    return rows_layout(xrows, stages, red_slots, MP, overlay, glu).total;
 }
-bool rows_overlay_fits(int xrows, int stages, int splits, int MP) {
-    const RowsLayout L = rows_layout(xrows, stages, splits, MP, true);
+bool rows_overlay_fits(int xrows, int stages, int splits, int MP, bool glu) {
+    const RowsLayout L = rows_layout(xrows, stages, splits, MP, true, glu);
     return static_cast<uint32_t>(splits) * L.red_block <= L.off_g;
 }
 size_t rows_stage_bytes(int xrows) { return xrows * kBK * 2 + kRowsWBytes + kGBytes; }
@@ -1471,18 +1565,23 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
                         const CUtensorMap& tmG, void* Y, const RowsLaunch& a, cudaStream_t s) {
     auto* y = static_cast<__nv_bfloat16*>(Y);
     const bool split = a.cluster != 0;
+    const bool glu = a.glu != 0;
+    if (glu && !fused) return cudaErrorInvalidValue;
     if (fused && !split && a.xrows == kRowsBM) {
-        cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(rows_ta_kernel), 6);
+        auto ta = glu ? rows_ta_kernel<true> : rows_ta_kernel<false>;
+        cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(ta), glu ? 9 : 6);
         if (e != cudaSuccess) return e;
-        e = launch_ex(rows_ta_kernel, a.grid, kTaSmem, 1, s, tmX, tmW, tmG, *a.tmY, y, a);
+        e = launch_ex(ta, a.grid, kTaSmem, 1, s, tmX, tmW, tmG, *a.tmY, y, a);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
-    auto kern = fused ? (split ? rows_kernel<true, true> : rows_kernel<true, false>)
-                      : (split ? rows_kernel<false, true> : rows_kernel<false, false>);
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), (fused ? 0 : 1) + (split ? 4 : 0));
+    auto kern = glu ? (split ? rows_kernel<true, true, true> : rows_kernel<true, false, true>)
+            : fused ? (split ? rows_kernel<true, true, false> : rows_kernel<true, false, false>)
+                    : (split ? rows_kernel<false, true, false> : rows_kernel<false, false, false>);
+    const int slot = glu ? (split ? 8 : 7) : (fused ? 0 : 1) + (split ? 4 : 0);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), slot);
     if (e != cudaSuccess) return e;
-    const size_t smem = rows_smem_bytes(a.xrows, a.stages, split ? a.splits : 0, a.MP, split && a.red_overlay);
+    const size_t smem = rows_smem_bytes(a.xrows, a.stages, split ? a.splits : 0, a.MP, split && a.red_overlay, glu);
     e = launch_ex(kern, a.grid, smem, split ? a.splits : 1, s, tmX, tmW, tmG, y, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -1524,9 +1623,10 @@ int cols_max_active_clusters(bool fused, int splits, size_t smem) {
                  : max_active_clusters(cols_kernel<false>, 3, splits, smem);
 }
 
-int rows_max_active_clusters(bool fused, int splits, size_t smem) {
-    return fused ? max_active_clusters(rows_kernel<true, true>, 4, splits, smem)
-                 : max_active_clusters(rows_kernel<false, true>, 5, splits, smem);
+int rows_max_active_clusters(bool fused, int splits, size_t smem, bool glu) {
+    if (glu) return max_active_clusters(rows_kernel<true, true, true>, 8, splits, smem);
+    return fused ? max_active_clusters(rows_kernel<true, true, false>, 4, splits, smem)
+                 : max_active_clusters(rows_kernel<false, true, false>, 5, splits, smem);
 }
 
 cudaError_t launch_rmsnorm(const void* X, const void* g, void* Xn, int M, int K, float eps,

@@ -28,11 +28,13 @@ constexpr int kColsMaxSplits = 16;
 // through a cluster (0 without); MP = M rounded up to 16; overlay: the
 // splits' receive blocks reuse the pipeline buffers instead of an area of
 // their own.
-size_t rows_smem_bytes(int xrows, int stages, int red_slots, int MP, bool overlay = false);
+// glu: the gated form (reduction units of two chunks).
+size_t rows_smem_bytes(int xrows, int stages, int red_slots, int MP, bool overlay = false,
+                       bool glu = false);
 // The receive blocks of a K split over `splits` CTAs fit the pipeline buffers.
-bool rows_overlay_fits(int xrows, int stages, int splits, int MP);
+bool rows_overlay_fits(int xrows, int stages, int splits, int MP, bool glu = false);
 size_t rows_stage_bytes(int xrows);
-int rows_max_active_clusters(bool fused, int splits, size_t smem);
+int rows_max_active_clusters(bool fused, int splits, size_t smem, bool glu = false);
 // red_slots = splits - 1 when the splits reduce through a cluster, else 0.
 size_t cols_smem_bytes(int MP, int stages, int red_slots);
 size_t cols_fixed_smem_bytes(int MP, int red_slots);
@@ -48,6 +50,8 @@ struct RowsLaunch {
     int splits, kb_per_split;  // K split of each tile (splits > 1 needs m_tiles == 1
                                // and one (tile, split) unit per CTA)
     int red_overlay;           // 1: the splits' receive blocks reuse the pipeline buffers
+    int glu;                   // 1: gated form: W [K, N = 2F] holds gate then up columns,
+                               // Y [M, F] = silu(gate) * up; output tiles of 128 columns
     int cluster;               // 1: the splits of a tile form a cluster
     int xrows, MP, stages;
     int grid;

@@ -88,6 +88,16 @@ def test_fused_validation(lib, args, expect):
     assert lib.rmsnorm_matmul(X, g, W, Y, M, K, N, eps, None) == expect
 
 
+def test_gated_validation(lib):
+    f = lib.rmsnorm_matmul_swiglu
+    assert f(A16, B16, C16, D16, 8, 64, 24, 1e-6, None) == 2      # N % 16 (F = 12)
+    assert f(A16, B16, C16, D16, 8, 64, 20, 1e-6, None) == 2      # N % 8
+    assert f(A16, B16, C16, 0, 8, 64, 32, 1e-6, None) == 1        # NULL Y
+    assert f(A16, B16, C16, A16 + 64, 8, 64, 32, 1e-6, None) == 1 # Y overlaps X
+    assert f(A16, B16, C16, D16, 8, 64, 32, -1.0, None) == 1      # eps < 0
+    assert f(0, 0, 0, 0, 0, 64, 32, 1e-6, None) == 0              # M = 0: no-op
+
+
 def test_unfused_validation(lib):
     assert lib.rmsnorm(0, B16, D16, 8, 64, 1e-6, None) == 1
     assert lib.rmsnorm(A16, B16, D16, 8, 63, 1e-6, None) == 2

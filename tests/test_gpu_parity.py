@@ -137,6 +137,61 @@ def test_wide_decode_split_over_pipeline_buffers(rmm, M, K, N):
     assert torch.equal(Y, run_fused(rmm, X, g, W, 1e-5))
 
 
+# ------------------------------------------------------- gated MLP on top
+# rmsnorm_matmul_swiglu: W [K, 2F] = [gate | up], Y [M, F] = silu(Z_gate) * Z_up.
+GATED = [
+    (64, 4096, 28672),   # decode gate|up, the benchmark shape
+    (16, 1032, 2000),    # F = 1000: a partial output tile, K split over a cluster
+    (1, 64, 16),         # one row, one k-block, F = 8
+    (100, 2048, 2064),   # 100 rows: receive blocks over the pipeline buffers
+    (300, 520, 528),     # several row tiles (prefill kernel), ragged everywhere
+    (1280, 1024, 8192),  # 320 tiles: the last 16 cut along K (prefill kernel's tail)
+]
+
+
+def assert_gated_close(Y, X, g, W, eps, what):
+    """Y = silu(Z_gate) * Z_up against the oracle, with the tolerance of the
+    ungated output Z (|dz| <= 1e-2 + 1e-2 |z|) carried through silu(a) * b to
+    first order, plus the second-order term and Y's own bf16 rounding:
+      |dy| <= |silu'(zg)| e_g |zu| + |silu(zg)| e_u + e_g e_u + 2^-8 |y|.
+    The gate multiplies Z's errors (chiefly the bf16 rounding of X*g before
+    the tensor cores) by |z_up|, so the ungated bound does not hold for Y."""
+    F = W.shape[1] // 2
+    ref = oracle.rmsnorm_matmul_swiglu(X, g, W, eps)
+    Z = oracle.rmsnorm_matmul(X, g, W, eps)
+    zg, zu = Z[:, :F], Z[:, F:]
+    eg, eu = ATOL + RTOL * np.abs(zg), ATOL + RTOL * np.abs(zu)
+    sig = 1.0 / (1.0 + np.exp(-zg))
+    dsilu = sig * (1.0 + zg * (1.0 - sig))
+    tol = np.abs(dsilu) * eg * np.abs(zu) + np.abs(zg * sig) * eu + eg * eu + 2.0 ** -8 * np.abs(ref)
+    y = oracle.to_f64(Y)
+    bad = ~(np.abs(y - ref) <= tol)   # NaN fails
+    assert not bad.any(), f"{what}: {int(bad.sum())} of {ref.size} outside the propagated tolerance"
+
+
+@pytest.mark.parametrize("M,K,N", GATED)
+def test_gated(rmm, M, K, N):
+    from sm_rmsnorm_matmul_gb300 import inputs
+    X, g, W = inputs.random_problem(M, K, N, seed=M + 3 * K + N, x_kind="row_scaled")
+    Y = rmm.rmsnorm_matmul_swiglu(X.cuda(), g.cuda(), W.cuda(), 1e-5)
+    torch.cuda.synchronize()
+    assert rmm.device_status() == 0
+    assert Y.shape == (M, N // 2)
+    assert_gated_close(Y.cpu(), X, g, W, 1e-5, f"gated {M}x{K}x{N}")
+    assert torch.equal(Y, rmm.rmsnorm_matmul_swiglu(X.cuda(), g.cuda(), W.cuda(), 1e-5))
+
+
+def test_gated_prefill_sampled_rows(rmm):
+    from sm_rmsnorm_matmul_gb300 import inputs
+    M, K, N = 4096, 4096, 12288
+    X, g, W = inputs.random_problem(M, K, N, seed=99, x_kind="row_scaled")
+    Y = rmm.rmsnorm_matmul_swiglu(X.cuda(), g.cuda(), W.cuda(), 1e-6)
+    torch.cuda.synchronize()
+    assert rmm.device_status() == 0
+    rows = inputs.sample_rows(M, 256)
+    assert_gated_close(Y.cpu()[rows], X[rows], g, W, 1e-6, "gated prefill")
+
+
 def test_small_m_rejects_large_m_when_forced(rmm, forced):
     forced(2)
     X = torch.zeros(129, 64, dtype=torch.bfloat16, device="cuda")
