@@ -224,7 +224,7 @@ def traffic_from_profile(workload: str):
 
 
 # --------------------------------------------------------------- GPU timing
-def make_copies(w, n_copies, device, torch, inputs):
+def make_copies(w, n_copies, device, torch, inputs, out_cols=None):
     X, g, W = inputs.generate_workload(w)
     Xd, gd, Wd = X.to(device), g.to(device), W.to(device)
     copies = []
@@ -233,7 +233,7 @@ def make_copies(w, n_copies, device, torch, inputs):
             xs, gs, ws = Xd, gd, Wd
         else:
             xs, gs, ws = Xd.clone(), gd.clone(), Wd.clone()
-        ys = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device)
+        ys = torch.empty((w.M, out_cols or w.N), dtype=torch.bfloat16, device=device)
         copies.append((xs, gs, ws, ys))
     return (X, g, W), copies
 
@@ -274,13 +274,16 @@ def time_graph(torch, stream, step_fn, n_copies, K, chunk=500):
 
 
 def bench_workload(torch, rmm, inputs, w, K, W_warm, device, stream, l2, with_unfused=True,
-                   sampler=None, barrier=None):
+                   sampler=None, barrier=None, gated=False):
+    """gated: time rmsnorm_matmul_swiglu (Y [M, N/2]) instead of rmsnorm_matmul."""
     n_copies = n_rotating_copies(w, l2)
-    host, copies = make_copies(w, n_copies, device, torch, inputs)
+    F = w.N // 2
+    host, copies = make_copies(w, n_copies, device, torch, inputs, out_cols=F if gated else None)
+    fused = rmm.rmsnorm_matmul_swiglu if gated else rmm.rmsnorm_matmul
 
     def step(i):
         x, g, wt, y = copies[i]
-        rmm.rmsnorm_matmul(x, g, wt, w.eps, out=y, stream=stream)
+        fused(x, g, wt, w.eps, out=y, stream=stream)
 
     with torch.cuda.stream(stream):
         for i in range(max(W_warm, 1)):
@@ -300,15 +303,24 @@ def bench_workload(torch, rmm, inputs, w, K, W_warm, device, stream, l2, with_un
     status = rmm.device_status(stream)
     del graphs
     res = {"secs": secs, "n_copies": n_copies, "status": status, "host": host,
-           "copies": copies, "path": rmm.dispatch_path(w.M, w.K, w.N),
-           "plan": rmm.describe_plan(w.M, w.K, w.N)}
+           "copies": copies, "path": 1 if gated else rmm.dispatch_path(w.M, w.K, w.N),
+           "plan": rmm.describe_plan(w.M, w.K, w.N, gated=gated)}
     if with_unfused:
         xn = [torch.empty((w.M, w.K), dtype=torch.bfloat16, device=device) for _ in range(n_copies)]
+        zs = [torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device) for _ in range(n_copies)] \
+            if gated else None
 
         def step_unfused(i):
+            # the separate kernels: RMSNorm, MatMul (and, gated, torch's
+            # elementwise silu(gate) * up on the bf16 product)
             x, g, wt, y = copies[i]
             rmm.rmsnorm(x, g, w.eps, out=xn[i], stream=stream)
-            rmm.matmul(xn[i], wt, out=y, stream=stream)
+            if gated:
+                rmm.matmul(xn[i], wt, out=zs[i], stream=stream)
+                with torch.cuda.stream(stream):
+                    torch.mul(torch.nn.functional.silu(zs[i][:, :F]), zs[i][:, F:], out=y)
+            else:
+                rmm.matmul(xn[i], wt, out=y, stream=stream)
 
         with torch.cuda.stream(stream):
             for i in range(2):
@@ -317,7 +329,7 @@ def bench_workload(torch, rmm, inputs, w, K, W_warm, device, stream, l2, with_un
         ku = max(1, min(K, 200))
         s_unf, _, g2 = time_graph(torch, stream, step_unfused, n_copies, ku)
         res["unfused_secs_per_step"] = s_unf / ku
-        del g2, xn
+        del g2, xn, zs
     return res
 
 
@@ -464,6 +476,19 @@ def main():
                 shapes.append(shape_entry(ww, t, r, peaks, k))
                 del r
                 torch.cuda.empty_cache()
+            # the gated MLP on top (rmsnorm_matmul_swiglu), on the gate|up shape
+            # and on a prefill-sized one
+            gated_prefill = inputs.Workload(name="prefill_gatedmlp_4096x4096x28672", M=4096, K=4096,
+                                            N=28672, eps=1e-5, seed=6, w_std=1 / 64, x_kind="row_scaled")
+            for ww in (inputs.WORKLOADS["decode_gatedmlp_64x4096x28672"], gated_prefill):
+                est = max(ww.flops / (peaks["bf16_tflops"] * 1e12),
+                          gated_bytes(ww) / (peaks["hbm_gbs"] * 1e9))
+                k = int(min(5000, max(20, 0.2 / max(est, 1e-7))))
+                r = bench_workload(torch, rmm, inputs, ww, k, 3, device, stream, l2,
+                                   with_unfused=True, sampler=sampler, gated=True)
+                shapes.append(shape_entry(ww, r["secs"] / k, r, peaks, k, gated=True))
+                del r
+                torch.cuda.empty_cache()
     clocks = sampler.summary()
 
     K = args.steps
@@ -544,12 +569,19 @@ def kernel_name(rmm, w):
     return "rows_kernel<fused>"
 
 
-def shape_entry(w, t, r, peaks, k):
+def gated_bytes(w):
+    """X + W + Y bytes of the gated form (Y has N/2 columns)."""
+    return 2 * (w.M * w.K + w.K * w.N + w.M * (w.N // 2))
+
+
+def shape_entry(w, t, r, peaks, k, gated=False):
+    nbytes = gated_bytes(w) if gated else w.bytes_xwy
     tflops = w.flops / t / 1e12
-    gbs = w.bytes_xwy / t / 1e9
-    roof_t = max(w.flops / (peaks["bf16_tflops"] * 1e12), w.bytes_xwy / (peaks["hbm_gbs"] * 1e9))
-    bound = "tensor" if w.flops / (peaks["bf16_tflops"] * 1e12) > w.bytes_xwy / (peaks["hbm_gbs"] * 1e9) else "hbm"
-    e = {"workload": w.name, "path": "small-M (cols)" if r["path"] == 2 else "row-tile",
+    gbs = nbytes / t / 1e9
+    roof_t = max(w.flops / (peaks["bf16_tflops"] * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9))
+    bound = "tensor" if w.flops / (peaks["bf16_tflops"] * 1e12) > nbytes / (peaks["hbm_gbs"] * 1e9) else "hbm"
+    e = {"workload": w.name + (" (gated: silu(gate) * up)" if gated else ""),
+         "path": "small-M (cols)" if r["path"] == 2 else "row-tile",
          "plan": r.get("plan"),
          "steps": k, "us_per_call": round(t * 1e6, 3), "tflops": round(tflops, 2),
          "hbm_gbs": round(gbs, 1), "bound": bound, "roofline_frac": round(roof_t / t, 4),
@@ -557,7 +589,7 @@ def shape_entry(w, t, r, peaks, k):
     if bound == "tensor":
         e["frac_of_tensor_peak_sustained"] = round(tflops / peaks["bf16_tflops_sustained"], 4)
     if "unfused_secs_per_step" in r:
-        e["unfused_pair_us"] = round(r["unfused_secs_per_step"] * 1e6, 3)
+        e["unfused_us" if gated else "unfused_pair_us"] = round(r["unfused_secs_per_step"] * 1e6, 3)
     return e
 
 
