@@ -103,6 +103,26 @@ int rmsnorm_matmul(const void* X, const void* g, const void* W, void* Y,
 int rmsnorm_matmul_swiglu(const void* X, const void* g, const void* W, void* Y,
                           int64_t M, int64_t K, int64_t N, float eps, cudaStream_t stream);
 
+/* Flags of rmsnorm_matmul_ex(). */
+enum {
+    RMM_WEIGHT_NK = 1u,   /* W is stored [N, K] (K contiguous: a linear layer's weight),
+                             not [K, N]; Y = RMSNorm(X) @ W^T */
+    RMM_GATED_SILU = 2u   /* the gated form of rmsnorm_matmul_swiglu(): the N rows (or
+                             columns) of W are gate then up, Y is [M, N/2] */
+};
+
+/*
+ * rmsnorm_matmul() with options: any combination of the flags above (0 is
+ * rmsnorm_matmul() itself, RMM_GATED_SILU is rmsnorm_matmul_swiglu()).  With
+ * RMM_WEIGHT_NK, W [N, K] is row-major with K contiguous and the tensor cores
+ * read it K-major; every other rule (sizes, alignment, no overlap, results)
+ * is that of the flagless form.  Always the row-tile kernels.  Unknown flag
+ * bits return RMM_ERR_INVALID_ARG.  Returns an rmm_status.
+ */
+int rmsnorm_matmul_ex(const void* X, const void* g, const void* W, void* Y,
+                      int64_t M, int64_t K, int64_t N, float eps, unsigned flags,
+                      cudaStream_t stream);
+
 /*
  * Unfused RMSNorm alone (the first of the two kernels that the review page's
  * muGraph example says existing systems launch):
@@ -175,7 +195,8 @@ int rmsnorm_matmul_noalloc(const void* X, const void* g, const void* W, void* Y,
 /*
  * Launch plan the library would use for this shape on the current device
  * (introspection for tests and benchmarks; `fused` = 1 for rmsnorm_matmul,
- * 0 for matmul, 2 for rmsnorm_matmul_swiglu, whose N is the width of W).
+ * 0 for matmul, 2 for rmsnorm_matmul_swiglu, whose N is the width of W; the
+ * plan does not depend on RMM_WEIGHT_NK).
  * Fills info[0..7] with: path (1 row-tile, 2 small-M),
  * K splits, 1 if the splits reduce through a cluster's shared memory, grid
  * size, pipeline stages, padded rows MP, column tiles, k-blocks per split.

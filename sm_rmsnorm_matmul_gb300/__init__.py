@@ -22,8 +22,8 @@ import threading
 from .build import LIB_PATH
 
 __all__ = [
-    "RmmError", "lib", "rmsnorm_matmul", "rmsnorm_matmul_noalloc", "rmsnorm_matmul_swiglu", "rmsnorm",
-    "matmul", "force_path",
+    "RmmError", "lib", "rmsnorm_matmul", "rmsnorm_matmul_noalloc", "rmsnorm_matmul_swiglu",
+    "rmsnorm_matmul_ex", "WEIGHT_NK", "GATED_SILU", "rmsnorm", "matmul", "force_path",
     "dispatch_path", "describe_plan", "device_status", "status_string", "STATUS", "PATH_AUTO",
     "PATH_ROWS", "PATH_COLS", "ABI_FUNCTIONS",
 ]
@@ -34,11 +34,13 @@ STATUS = {
     5: "RMM_ERR_DEVICE_TIMEOUT", 6: "RMM_ERR_INTERNAL", 7: "RMM_ERR_SCRATCH_LIMIT",
 }
 PATH_AUTO, PATH_ROWS, PATH_COLS = 0, 1, 2
+WEIGHT_NK, GATED_SILU = 1, 2   # flags of rmsnorm_matmul_ex
 
 # Every function declared in include/rmsnorm_matmul.h.
 ABI_FUNCTIONS = ("rmsnorm_matmul", "rmsnorm", "matmul", "rmm_force_path",
                  "rmm_device_status", "rmm_status_string", "rmm_dispatch_path",
-                 "rmsnorm_matmul_noalloc", "rmm_describe_plan", "rmsnorm_matmul_swiglu")
+                 "rmsnorm_matmul_noalloc", "rmm_describe_plan", "rmsnorm_matmul_swiglu",
+                 "rmsnorm_matmul_ex")
 
 
 class RmmError(RuntimeError):
@@ -56,6 +58,7 @@ def _bind(l: ctypes.CDLL) -> ctypes.CDLL:
     l.rmsnorm_matmul.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, vp]
     l.rmsnorm_matmul_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, vp]
     l.rmsnorm_matmul_swiglu.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, vp]
+    l.rmsnorm_matmul_ex.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, ctypes.c_uint, vp]
     l.rmsnorm.argtypes = [vp, vp, vp, i64, i64, f32, vp]
     l.matmul.argtypes = [vp, vp, vp, i64, i64, i64, vp]
     l.rmm_force_path.argtypes = [i32]
@@ -64,7 +67,8 @@ def _bind(l: ctypes.CDLL) -> ctypes.CDLL:
     l.rmm_status_string.restype = ctypes.c_char_p
     l.rmm_dispatch_path.argtypes = [i64, i64, i64]
     l.rmm_describe_plan.argtypes = [i64, i64, i64, i32, ctypes.POINTER(ctypes.c_int)]
-    for name in ("rmsnorm_matmul", "rmsnorm_matmul_noalloc", "rmsnorm_matmul_swiglu", "rmsnorm",
+    for name in ("rmsnorm_matmul", "rmsnorm_matmul_noalloc", "rmsnorm_matmul_swiglu", "rmsnorm_matmul_ex",
+                 "rmsnorm",
                  "matmul", "rmm_force_path", "rmm_device_status", "rmm_dispatch_path",
                  "rmm_describe_plan"):
         getattr(l, name).restype = i32
@@ -152,6 +156,32 @@ def rmsnorm_matmul_swiglu(X, g, W, eps: float = 1e-6, out=None, stream=None):
     _raise(lib().rmsnorm_matmul_swiglu(X.data_ptr(), g.data_ptr(), W.data_ptr(), out.data_ptr(),
                                        M, K, N, float(eps), _stream_ptr(stream)),
            "rmsnorm_matmul_swiglu")
+    return out
+
+
+def rmsnorm_matmul_ex(X, g, W, eps: float = 1e-6, weight_nk: bool = False, gated: bool = False,
+                      out=None, stream=None):
+    """rmsnorm_matmul() with options.  weight_nk: W is [N, K] (a linear layer's
+    weight, K contiguous) and Y = RMSNorm(X) @ W.T; gated: Y = silu(Z[:, :F]) *
+    Z[:, F:] with F = N / 2, as rmsnorm_matmul_swiglu()."""
+    import torch
+    _check_bf16("X", X, 2)
+    _check_bf16("g", g, 1)
+    _check_bf16("W", W, 2)
+    M, K = X.shape
+    N = W.shape[0] if weight_nk else W.shape[1]
+    if g.shape[0] != K or W.shape[1 if weight_nk else 0] != K or (gated and N % 2):
+        raise ValueError(f"shape mismatch: X {tuple(X.shape)}, g {tuple(g.shape)}, W {tuple(W.shape)}")
+    cols = N // 2 if gated else N
+    if out is None:
+        out = torch.empty((M, cols), dtype=torch.bfloat16, device=X.device)
+    else:
+        _check_bf16("out", out, 2)
+        if tuple(out.shape) != (M, cols):
+            raise ValueError(f"out must have shape {(M, cols)}")
+    flags = (WEIGHT_NK if weight_nk else 0) | (GATED_SILU if gated else 0)
+    _raise(lib().rmsnorm_matmul_ex(X.data_ptr(), g.data_ptr(), W.data_ptr(), out.data_ptr(),
+                                   M, K, N, float(eps), flags, _stream_ptr(stream)), "rmsnorm_matmul_ex")
     return out
 
 

@@ -331,14 +331,14 @@ int rows_stages(int xrows, int red_slots, int MP, const DeviceInfo& d, bool over
 }
 
 std::mutex g_rows_occ_mu;
-std::map<std::tuple<int, bool, int, size_t, bool>, int> g_rows_occ;
+std::map<std::tuple<int, bool, int, size_t, bool, bool>, int> g_rows_occ;
 
-int rows_max_clusters(int dev, bool fused, int splits, size_t smem, bool glu) {
+int rows_max_clusters(int dev, bool fused, int splits, size_t smem, bool glu, bool wnk) {
     std::lock_guard<std::mutex> lk(g_rows_occ_mu);
-    auto key = std::make_tuple(dev, fused, splits, smem, glu);
+    auto key = std::make_tuple(dev, fused, splits, smem, glu, wnk);
     auto it = g_rows_occ.find(key);
     if (it != g_rows_occ.end()) return it->second;
-    const int n = rmm::rows_max_active_clusters(fused, splits, smem, glu);
+    const int n = rmm::rows_max_active_clusters(fused, splits, smem, glu, wnk);
     g_rows_occ[key] = n;
     return n;
 }
@@ -351,7 +351,7 @@ int rows_max_clusters(int dev, bool fused, int splits, size_t smem, bool glu) {
 // drain, and the cluster reduction about 1.5 us.  glu: the gated form, whose
 // tiles cover 128 output columns (256 columns of W, N = 2F).
 RowsPlan plan_rows(int dev, bool fused, int64_t M, int64_t K, int64_t N, const DeviceInfo& d,
-                   bool glu = false) {
+                   bool glu = false, bool wnk = false) {
     RowsPlan p{};
     p.m_tiles = static_cast<int>((M + rmm::kRowsBM - 1) / rmm::kRowsBM);
     p.n_tiles = glu ? static_cast<int>((N / 2 + rmm::kRowsBN / 2 - 1) / (rmm::kRowsBN / 2))
@@ -393,7 +393,7 @@ RowsPlan plan_rows(int dev, bool fused, int64_t M, int64_t K, int64_t N, const D
         if (s > 1) {
             resident = rows_max_clusters(dev, fused, s,
                                          rmm::rows_smem_bytes(p.xrows, st, red_slots, p.MP, overlay, glu),
-                                         glu) * s;
+                                         glu, wnk) * s;
             if (resident <= 0) continue;
         }
         const long units = static_cast<long>(p.n_tiles) * s;
@@ -431,16 +431,20 @@ int choose_path(int64_t M) {
 // One launch of the tensor-core contraction, fused (RMSNorm folded in) or not.
 // Without may_allocate, plans that need the per-stream workspace are avoided.
 // glu: the gated form (fused only; always the row-tile path), Y [M, N / 2].
+// wnk: W stored [N, K] (fused only; always the row-tile path).
 int run_contraction(bool fused, const void* X, const void* g, const void* W, void* Y, int64_t M,
                     int64_t K, int64_t N, float eps, cudaStream_t stream, bool may_allocate = true,
-                    bool glu = false) {
+                    bool glu = false, bool wnk = false) {
     int dev = 0;
     DeviceInfo d;
     int rc = current_device(&dev, &d);
     if (rc != RMM_OK) return rc;
-    const int path = glu ? static_cast<int>(kPathRows) : choose_path(M);
+    const int path = glu || wnk ? static_cast<int>(kPathRows) : choose_path(M);
     CUtensorMap tmX, tmW, tmG;
-    if (!map_2d(&tmW, W, K, N, kBK)) return RMM_ERR_INTERNAL;
+    // [K, N]: boxes of [64 k][64 n]; [N, K]: boxes of [256 n][64 k], or 128 rows
+    // each for the gate and up halves of the gated form
+    if (!(wnk ? map_2d(&tmW, W, N, K, glu ? rmm::kRowsBN / 2 : rmm::kRowsBN) : map_2d(&tmW, W, K, N, kBK)))
+        return RMM_ERR_INTERNAL;
     if (fused) {
         if (!map_1d(&tmG, g, K)) return RMM_ERR_INTERNAL;
     }
@@ -476,7 +480,7 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
         return rmm::launch_cols(fused, tmX, tmW, tmG, Y, a, stream) == cudaSuccess ? RMM_OK
                                                                                   : RMM_ERR_LAUNCH;
     }
-    const RowsPlan p = plan_rows(dev, fused, M, K, N, d, glu);
+    const RowsPlan p = plan_rows(dev, fused, M, K, N, d, glu, wnk);
     if (!map_2d(&tmX, X, M, K, p.xrows)) return RMM_ERR_INTERNAL;
     if (!fused) tmG = tmX;
     rmm::RowsLaunch a{};
@@ -496,6 +500,7 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
     a.grid = p.grid;
     a.red_overlay = p.overlay;
     a.glu = glu ? 1 : 0;
+    a.w_nk = wnk ? 1 : 0;
     CUtensorMap tmY;
     a.tail_tiles = 0;
     a.tail_pieces = 1;
@@ -546,17 +551,25 @@ int rmsnorm_matmul(const void* X, const void* g, const void* W, void* Y, int64_t
     return run_contraction(true, X, g, W, Y, M, K, N, eps, stream);
 }
 
-int rmsnorm_matmul_swiglu(const void* X, const void* g, const void* W, void* Y, int64_t M,
-                          int64_t K, int64_t N, float eps, cudaStream_t stream) {
+int rmsnorm_matmul_ex(const void* X, const void* g, const void* W, void* Y, int64_t M, int64_t K,
+                      int64_t N, float eps, unsigned flags, cudaStream_t stream) {
+    if (flags & ~static_cast<unsigned>(RMM_WEIGHT_NK | RMM_GATED_SILU)) return RMM_ERR_INVALID_ARG;
+    const bool glu = (flags & RMM_GATED_SILU) != 0, wnk = (flags & RMM_WEIGHT_NK) != 0;
     int rc = check_sizes(M, K, N, eps, true);
     if (rc == kNoop) return RMM_OK;
     if (rc != RMM_OK) return rc;
-    if (N % 16 != 0) return RMM_ERR_ALIGNMENT;   // F = N / 2 must be a multiple of 8
-    rc = check_ptrs(Y, static_cast<size_t>(M) * (N / 2) * 2,
+    if (glu && N % 16 != 0) return RMM_ERR_ALIGNMENT;   // F = N / 2 must be a multiple of 8
+    const int64_t out_cols = glu ? N / 2 : N;
+    rc = check_ptrs(Y, static_cast<size_t>(M) * out_cols * 2,
                     {{X, static_cast<size_t>(M) * K * 2}, {g, static_cast<size_t>(K) * 2},
                      {W, static_cast<size_t>(K) * N * 2}});
     if (rc != RMM_OK) return rc;
-    return run_contraction(true, X, g, W, Y, M, K, N, eps, stream, true, true);
+    return run_contraction(true, X, g, W, Y, M, K, N, eps, stream, true, glu, wnk);
+}
+
+int rmsnorm_matmul_swiglu(const void* X, const void* g, const void* W, void* Y, int64_t M,
+                          int64_t K, int64_t N, float eps, cudaStream_t stream) {
+    return rmsnorm_matmul_ex(X, g, W, Y, M, K, N, eps, RMM_GATED_SILU, stream);
 }
 
 int matmul(const void* A, const void* B, void* C, int64_t M, int64_t K, int64_t N,

@@ -121,6 +121,42 @@ __device__ __forceinline__ float glu_out(float gate, float up, float r) {
     return silu_f(gate * r) * (up * r);
 }
 
+// One W stage: k-block kb by the tile's 256 accumulator columns, into the
+// 32 KB slot at dst.  Weights stored [K, N] (N contiguous): [64 k][64 n] boxes,
+// N-major for the MMA, as many as fall inside N.  Weights stored [N, K] (K
+// contiguous, the layout of a linear layer's weight): one [256 n][64 k] box,
+// K-major, rows past N read as zeros.  Gated: accumulator columns 0..127 come
+// from the gate columns n0.. and 128..255 from the up columns Nout + n0.. (a
+// box past the gate half reads up columns, one past N zeros; neither reaches
+// an output).  w_stage_bytes() gives the bytes the copies deliver.
+template <bool kGlu, bool kWnk>
+__device__ __forceinline__ uint32_t w_stage_bytes(int n0, int N) {
+    if constexpr (kWnk || kGlu) return kRowsWBytes;
+    else return static_cast<uint32_t>(min(4, (N - n0 + 63) / 64)) * kWBoxBytes;
+}
+template <bool kGlu, bool kWnk>
+__device__ __forceinline__ void load_w_stage(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int n0,
+                                             int kb, int N, int Nout) {
+    if constexpr (kWnk) {
+        if constexpr (kGlu) {
+            tma_load_2d_nohint(dst, tm, bar, kb * kBK, n0);
+            tma_load_2d_nohint(dst + kRowsWBytes / 2, tm, bar, kb * kBK, Nout + n0);
+        } else {
+            tma_load_2d_nohint(dst, tm, bar, kb * kBK, n0);
+        }
+    } else {
+        const int nbox = static_cast<int>(w_stage_bytes<kGlu, kWnk>(n0, N) / kWBoxBytes);
+        for (int j = 0; j < nbox; ++j)
+            tma_load_2d_nohint(dst + j * kWBoxBytes, tm, bar, kGlu && j >= 2 ? Nout + n0 + 64 * (j - 2) : n0 + 64 * j,
+                               kb * kBK);
+    }
+}
+// Shared-memory descriptor of the W stage at b0 for the MMA's k-step kk.
+template <bool kWnk>
+__device__ __forceinline__ uint64_t w_desc(uint32_t b0, int kk) {
+    return kWnk ? sdesc_sw128(b0 + kk * 32, 16, 1024) : sdesc_sw128(b0 + kk * 2048, kWBoxBytes, 1024);
+}
+
 // Shared-memory layout of rows_kernel.  xrows: rows of X each stage loads
 // (128, or M rounded up to 16 when one row tile covers M).  X tiles come
 // first: the MMA always reads a 128-row window from an X tile, whose rows
@@ -149,7 +185,7 @@ __host__ __device__ inline RowsLayout rows_layout(int xrows, int stages, int red
 }
 
 
-template <bool kFused, bool kSplit, bool kGlu>
+template <bool kFused, bool kSplit, bool kGlu, bool kWnk>
 __global__ void __launch_bounds__(kThreads, 1)
     rows_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                 const __grid_constant__ CUtensorMap tmG, __nv_bfloat16* __restrict__ Y,
@@ -199,15 +235,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // boxes of gate columns n0.. and two of up columns Nout + n0.. (always
     // four: a box past the gate half reads up columns, one past N reads
     // zeros, and neither reaches an output column).
-    auto tile_nbox = [&](int n0) { return kGlu ? 4 : min(4, (a.N - n0 + 63) / 64); };
-    auto wcol = [&](int n0, int j) { return kGlu && j >= 2 ? Nout + n0 + 64 * (j - 2) : n0 + 64 * j; };
     // Loads of stage s = k-block kb of the unit whose tile starts at row block
     // mb and output column n0.
-    auto issue = [&](uint32_t s, int kb, int mb, int n0, int nbox) {
-        mbar_arrive_expect_tx(full(s), xbytes + nbox * kWBoxBytes + (kFused ? kGBytes : 0));
+    auto issue = [&](uint32_t s, int kb, int mb, int n0) {
+        mbar_arrive_expect_tx(full(s), xbytes + w_stage_bytes<kGlu, kWnk>(n0, a.N) + (kFused ? kGBytes : 0));
         tma_load_2d_nohint(sx + s * xbytes, &tmX, full(s), kb * kBK, mb * kRowsBM);
-        for (int j = 0; j < nbox; ++j)
-            tma_load_2d_nohint(sw + s * kRowsWBytes + j * kWBoxBytes, &tmW, full(s), wcol(n0, j), kb * kBK);
+        load_w_stage<kGlu, kWnk>(sw + s * kRowsWBytes, &tmW, full(s), n0, kb, a.N, Nout);
         if (kFused) tma_load_1d(sg + s * kGBytes, &tmG, full(s), kb * kBK);
     };
     // k-blocks of the first unit that thread 0 (the producer) issues before
@@ -245,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             rows_tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
             const int n0 = nb * kOutBN;
             pro = static_cast<uint32_t>(min(S, kb1 - kb0));
-            for (uint32_t i = 0; i < pro; ++i) issue(i, kb0 + static_cast<int>(i), mb, n0, tile_nbox(n0));
+            for (uint32_t i = 0; i < pro; ++i) issue(i, kb0 + static_cast<int>(i), mb, n0);
         }
     }
     if (warp == 2) {
@@ -274,12 +307,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int mb, nb;
                 rows_tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
                 const int n0 = nb * kOutBN;
-                const int nbox = tile_nbox(n0);
                 const int first = kb0 + (u == static_cast<int>(blockIdx.x) ? static_cast<int>(pro) : 0);
                 for (int kb = first; kb < kb1; ++kb) {
                     const uint32_t s = ring.idx, ph = ring.phase;
                     if (!mbar_wait(empty(s), ph ^ 1, abort)) { ok = false; break; }
-                    issue(s, kb, mb, n0, nbox);
+                    issue(s, kb, mb, n0);
                     ++it;
                     ring.advance();
                 }
@@ -291,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(kRowsBM, kRowsBN, false, true);
+            constexpr uint32_t idesc = idesc_bf16_f32(kRowsBM, kRowsBN, false, !kWnk);
             uint32_t it = 0, tl = 0;
             Ring ring(S);
             bool ok = true;
@@ -309,8 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t a0 = sx + s * xbytes, b0 = sw + s * kRowsWBytes;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
-                        mma_bf16_ss(d, sdesc_sw128(a0 + kk * 32, 16, 1024),
-                                    sdesc_sw128(b0 + kk * 2048, kWBoxBytes, 1024), idesc,
+                        mma_bf16_ss(d, sdesc_sw128(a0 + kk * 32, 16, 1024), w_desc<kWnk>(b0, kk), idesc,
                                     (kb != kb0 || kk != 0));
                     mma_commit(empty(s));
                     ++it;
@@ -648,7 +679,7 @@ __device__ __forceinline__ bool ta_unit(const RowsLaunch& a, int i, TaUnit& u) {
     return true;
 }
 
-template <bool kGlu>
+template <bool kGlu, bool kWnk>
 __global__ void __launch_bounds__(kThreads, 1)
     rows_ta_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmY,
@@ -741,7 +772,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int mb, nb;
                 rows_tile_coords(un.t, a.m_tiles, a.n_tiles, mb, nb);
                 const int n0 = nb * kOutBN;
-                const int nbox = kGlu ? 4 : min(4, (a.N - n0 + 63) / 64);
                 for (int kb = un.kb0; kb < un.kb1; ++kb) {
                     if (!mbar_wait(empty0 + 8 * ring.idx, ring.phase ^ 1, abort)) { ok = false; break; }
                     const uint32_t f = full0 + 8 * ring.idx;
@@ -750,11 +780,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_2d_nohint(sx + ring.idx * kTaXBytes, &tmX, f, kb * kBK, mb * kRowsBM);
                         tma_load_1d(sg + ring.idx * kGBytes, &tmG, f, kb * kBK);
                     } else {
-                        mbar_arrive_expect_tx(f, nbox * kWBoxBytes);
-                        for (int j = 0; j < nbox; ++j)
-                            tma_load_2d_nohint(sw + ring.idx * kRowsWBytes + j * kWBoxBytes, &tmW, f,
-                                               kGlu && j >= 2 ? Nout + n0 + 64 * (j - 2) : n0 + 64 * j,
-                                               kb * kBK);
+                        mbar_arrive_expect_tx(f, w_stage_bytes<kGlu, kWnk>(n0, a.N));
+                        load_w_stage<kGlu, kWnk>(sw + ring.idx * kRowsWBytes, &tmW, f, n0, kb, a.N, Nout);
                     }
                     ring.advance();
                     ++issued;
@@ -768,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(kRowsBM, kRowsBN, false, true);
+            constexpr uint32_t idesc = idesc_bf16_f32(kRowsBM, kRowsBN, false, !kWnk);
             Ring wr(kTaWStages), ar(kTaAStages);
             uint32_t tl = 0;
             bool ok = true;
@@ -785,8 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t b0 = sw + wr.idx * kRowsWBytes;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
-                        mma_bf16_ts(d, a0 + kk * 8, sdesc_sw128(b0 + kk * 2048, kWBoxBytes, 1024), idesc,
-                                    kb != un.kb0 || kk != 0);
+                        mma_bf16_ts(d, a0 + kk * 8, w_desc<kWnk>(b0, kk), idesc, kb != un.kb0 || kk != 0);
                     mma_commit(wempty0 + 8 * wr.idx);
                     mma_commit(aempty0 + 8 * ar.idx);
                     wr.advance();
@@ -1575,20 +1601,31 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
                         const CUtensorMap& tmG, void* Y, const RowsLaunch& a, cudaStream_t s) {
     auto* y = static_cast<__nv_bfloat16*>(Y);
     const bool split = a.cluster != 0;
-    const bool glu = a.glu != 0;
-    if (glu && !fused) return cudaErrorInvalidValue;
+    const bool glu = a.glu != 0, wnk = a.w_nk != 0;
+    if ((glu || wnk) && !fused) return cudaErrorInvalidValue;
     if (fused && !split && a.xrows == kRowsBM) {
-        auto ta = glu ? rows_ta_kernel<true> : rows_ta_kernel<false>;
-        cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(ta), glu ? 9 : 6);
+        auto ta = wnk ? (glu ? rows_ta_kernel<true, true> : rows_ta_kernel<false, true>)
+                      : (glu ? rows_ta_kernel<true, false> : rows_ta_kernel<false, false>);
+        cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(ta), wnk ? (glu ? 15 : 14) : (glu ? 9 : 6));
         if (e != cudaSuccess) return e;
         e = launch_ex(ta, a.grid, kTaSmem, 1, s, tmX, tmW, tmG, *a.tmY, y, a);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
-    auto kern = glu ? (split ? rows_kernel<true, true, true> : rows_kernel<true, false, true>)
-            : fused ? (split ? rows_kernel<true, true, false> : rows_kernel<true, false, false>)
-                    : (split ? rows_kernel<false, true, false> : rows_kernel<false, false, false>);
-    const int slot = glu ? (split ? 8 : 7) : (fused ? 0 : 1) + (split ? 4 : 0);
+    decltype(&rows_kernel<true, true, true, true>) kern;
+    int slot;
+    if (wnk) {
+        kern = glu ? (split ? rows_kernel<true, true, true, true> : rows_kernel<true, false, true, true>)
+                   : (split ? rows_kernel<true, true, false, true> : rows_kernel<true, false, false, true>);
+        slot = 10 + (glu ? 2 : 0) + (split ? 1 : 0);
+    } else if (glu) {
+        kern = split ? rows_kernel<true, true, true, false> : rows_kernel<true, false, true, false>;
+        slot = split ? 8 : 7;
+    } else {
+        kern = fused ? (split ? rows_kernel<true, true, false, false> : rows_kernel<true, false, false, false>)
+                     : (split ? rows_kernel<false, true, false, false> : rows_kernel<false, false, false, false>);
+        slot = (fused ? 0 : 1) + (split ? 4 : 0);
+    }
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), slot);
     if (e != cudaSuccess) return e;
     const size_t smem = rows_smem_bytes(a.xrows, a.stages, split ? a.splits : 0, a.MP, split && a.red_overlay, glu);
@@ -1633,10 +1670,13 @@ int cols_max_active_clusters(bool fused, int splits, size_t smem) {
                  : max_active_clusters(cols_kernel<false>, 3, splits, smem);
 }
 
-int rows_max_active_clusters(bool fused, int splits, size_t smem, bool glu) {
-    if (glu) return max_active_clusters(rows_kernel<true, true, true>, 8, splits, smem);
-    return fused ? max_active_clusters(rows_kernel<true, true, false>, 4, splits, smem)
-                 : max_active_clusters(rows_kernel<false, true, false>, 5, splits, smem);
+int rows_max_active_clusters(bool fused, int splits, size_t smem, bool glu, bool wnk) {
+    if (wnk)
+        return glu ? max_active_clusters(rows_kernel<true, true, true, true>, 13, splits, smem)
+                   : max_active_clusters(rows_kernel<true, true, false, true>, 11, splits, smem);
+    if (glu) return max_active_clusters(rows_kernel<true, true, true, false>, 8, splits, smem);
+    return fused ? max_active_clusters(rows_kernel<true, true, false, false>, 4, splits, smem)
+                 : max_active_clusters(rows_kernel<false, true, false, false>, 5, splits, smem);
 }
 
 cudaError_t launch_rmsnorm(const void* X, const void* g, void* Xn, int M, int K, float eps,

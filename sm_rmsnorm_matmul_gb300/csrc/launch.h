@@ -34,7 +34,7 @@ size_t rows_smem_bytes(int xrows, int stages, int red_slots, int MP, bool overla
 // The receive blocks of a K split over `splits` CTAs fit the pipeline buffers.
 bool rows_overlay_fits(int xrows, int stages, int splits, int MP, bool glu = false);
 size_t rows_stage_bytes(int xrows);
-int rows_max_active_clusters(bool fused, int splits, size_t smem, bool glu = false);
+int rows_max_active_clusters(bool fused, int splits, size_t smem, bool glu = false, bool wnk = false);
 // red_slots = splits - 1 when the splits reduce through a cluster, else 0.
 size_t cols_smem_bytes(int MP, int stages, int red_slots);
 size_t cols_fixed_smem_bytes(int MP, int red_slots);
@@ -52,6 +52,7 @@ struct RowsLaunch {
     int red_overlay;           // 1: the splits' receive blocks reuse the pipeline buffers
     int glu;                   // 1: gated form: W [K, N = 2F] holds gate then up columns,
                                // Y [M, F] = silu(gate) * up; output tiles of 128 columns
+    int w_nk;                  // 1: W stored [N, K] (K contiguous), read K-major
     int cluster;               // 1: the splits of a tile form a cluster
     int xrows, MP, stages;
     int grid;

@@ -98,6 +98,15 @@ def test_gated_validation(lib):
     assert f(0, 0, 0, 0, 0, 64, 32, 1e-6, None) == 0              # M = 0: no-op
 
 
+def test_ex_validation(lib):
+    f = lib.rmsnorm_matmul_ex
+    assert f(A16, B16, C16, D16, 8, 64, 64, 1e-6, 4, None) == 1      # unknown flag bit
+    assert f(A16, B16, C16, D16, 8, 64, 24, 1e-6, 2, None) == 2      # gated: N % 16
+    assert f(A16, B16, C16, D16, 8, 60, 64, 1e-6, 1, None) == 2      # K % 8
+    assert f(A16, B16, C16, C16, 8, 64, 64, 1e-6, 1, None) == 1      # Y aliases W
+    assert f(0, 0, 0, 0, 8, 64, 0, 1e-6, 3, None) == 0               # N = 0: no-op
+
+
 def test_unfused_validation(lib):
     assert lib.rmsnorm(0, B16, D16, 8, 64, 1e-6, None) == 1
     assert lib.rmsnorm(A16, B16, D16, 8, 63, 1e-6, None) == 2

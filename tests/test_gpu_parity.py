@@ -192,6 +192,33 @@ def test_gated_prefill_sampled_rows(rmm):
     assert_gated_close(Y.cpu()[rows], X[rows], g, W, 1e-6, "gated prefill")
 
 
+# ------------------------------------------- weights stored [N, K] (K-major)
+# rmsnorm_matmul_ex(weight_nk=True): W as a linear layer stores it, Y = RMSNorm(X) @ W^T.
+WEIGHT_NK = [
+    (16, 4096, 6144, False),   # decode QKV: K split over a cluster
+    (64, 4096, 28672, False),  # decode gate|up: one CTA per column tile
+    (7, 72, 136, False),       # ragged rows, K and N
+    (1280, 1024, 4096, False), # prefill kernel with the K-split tail
+    (300, 520, 264, False),    # several row tiles, ragged
+    (16, 1032, 2000, True),    # gated, K split
+    (300, 520, 528, True),     # gated, prefill kernel
+]
+
+
+@pytest.mark.parametrize("M,K,N,gated", WEIGHT_NK)
+def test_weight_nk(rmm, M, K, N, gated):
+    from sm_rmsnorm_matmul_gb300 import inputs
+    X, g, W = inputs.random_problem(M, K, N, seed=2 * M + K + 5 * N, x_kind="outlier_entries")
+    Wt = W.t().contiguous()   # [N, K]
+    Y = rmm.rmsnorm_matmul_ex(X.cuda(), g.cuda(), Wt.cuda(), 1e-6, weight_nk=True, gated=gated)
+    torch.cuda.synchronize()
+    assert rmm.device_status() == 0
+    if gated:
+        assert_gated_close(Y.cpu(), X, g, W, 1e-6, f"[N,K] gated {M}x{K}x{N}")
+    else:
+        assert_close(Y.cpu(), oracle.rmsnorm_matmul(X, g, W, 1e-6), f"[N,K] {M}x{K}x{N}")
+
+
 def test_small_m_rejects_large_m_when_forced(rmm, forced):
     forced(2)
     X = torch.zeros(129, 64, dtype=torch.bfloat16, device="cuda")
