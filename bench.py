@@ -224,8 +224,10 @@ def traffic_from_profile(workload: str):
 
 
 # --------------------------------------------------------------- GPU timing
-def make_copies(w, n_copies, device, torch, inputs, out_cols=None):
+def make_copies(w, n_copies, device, torch, inputs, out_cols=None, weight_nk=False):
     X, g, W = inputs.generate_workload(w)
+    if weight_nk:
+        W = W.t().contiguous()   # [N, K], a linear layer's layout
     Xd, gd, Wd = X.to(device), g.to(device), W.to(device)
     copies = []
     for i in range(n_copies):
@@ -274,16 +276,19 @@ def time_graph(torch, stream, step_fn, n_copies, K, chunk=500):
 
 
 def bench_workload(torch, rmm, inputs, w, K, W_warm, device, stream, l2, with_unfused=True,
-                   sampler=None, barrier=None, gated=False):
-    """gated: time rmsnorm_matmul_swiglu (Y [M, N/2]) instead of rmsnorm_matmul."""
+                   sampler=None, barrier=None, gated=False, weight_nk=False):
+    """gated: time the gated form (Y [M, N/2]); weight_nk: W stored [N, K]."""
     n_copies = n_rotating_copies(w, l2)
     F = w.N // 2
-    host, copies = make_copies(w, n_copies, device, torch, inputs, out_cols=F if gated else None)
-    fused = rmm.rmsnorm_matmul_swiglu if gated else rmm.rmsnorm_matmul
+    host, copies = make_copies(w, n_copies, device, torch, inputs, out_cols=F if gated else None,
+                               weight_nk=weight_nk)
 
     def step(i):
         x, g, wt, y = copies[i]
-        fused(x, g, wt, w.eps, out=y, stream=stream)
+        if gated or weight_nk:
+            rmm.rmsnorm_matmul_ex(x, g, wt, w.eps, weight_nk=weight_nk, gated=gated, out=y, stream=stream)
+        else:
+            rmm.rmsnorm_matmul(x, g, wt, w.eps, out=y, stream=stream)
 
     with torch.cuda.stream(stream):
         for i in range(max(W_warm, 1)):
@@ -487,6 +492,18 @@ def main():
                 r = bench_workload(torch, rmm, inputs, ww, k, 3, device, stream, l2,
                                    with_unfused=True, sampler=sampler, gated=True)
                 shapes.append(shape_entry(ww, r["secs"] / k, r, peaks, k, gated=True))
+                del r
+                torch.cuda.empty_cache()
+            # weights stored [N, K] (a linear layer's layout, read K-major)
+            for name in ("decode_qkv_16x4096x6144", "prefill_qkv_4096x4096x6144"):
+                ww = inputs.WORKLOADS[name]
+                est = max(ww.flops / (peaks["bf16_tflops"] * 1e12), ww.bytes_xwy / (peaks["hbm_gbs"] * 1e9))
+                k = int(min(5000, max(20, 0.2 / max(est, 1e-7))))
+                r = bench_workload(torch, rmm, inputs, ww, k, 3, device, stream, l2,
+                                   with_unfused=False, sampler=sampler, weight_nk=True)
+                e = shape_entry(ww, r["secs"] / k, r, peaks, k)
+                e["workload"] += " (W stored [N, K])"
+                shapes.append(e)
                 del r
                 torch.cuda.empty_cache()
     clocks = sampler.summary()
