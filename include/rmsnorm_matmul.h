@@ -161,6 +161,18 @@ int rmm_force_path(int path);
  */
 int rmm_device_status(cudaStream_t stream);
 
+/*
+ * Test hook, not for production use (the timeout path, exercised without any
+ * fault).  wait_limit_ns > 0 sets the limit of every bounded in-kernel wait
+ * (default 2 s; 0 restores it).  skip_sends != 0 makes the row-tile kernels'
+ * K-split reduction skip the stores of its partials, so that each owning CTA's
+ * wait for them runs out: the kernel then records RMM_ERR_DEVICE_TIMEOUT,
+ * skips its remaining work, frees its tensor memory and exits normally, and
+ * rmm_device_status() reports it.  Applies to the current device; synchronous.
+ * Returns RMM_ERR_INVALID_ARG for a negative limit.
+ */
+int rmm_test_hooks(int skip_sends, int64_t wait_limit_ns);
+
 /* Static, NUL-terminated name of a status code ("RMM_OK", ...). */
 const char* rmm_status_string(int code);
 

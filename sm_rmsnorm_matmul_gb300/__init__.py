@@ -40,7 +40,7 @@ WEIGHT_NK, GATED_SILU = 1, 2   # flags of rmsnorm_matmul_ex
 ABI_FUNCTIONS = ("rmsnorm_matmul", "rmsnorm", "matmul", "rmm_force_path",
                  "rmm_device_status", "rmm_status_string", "rmm_dispatch_path",
                  "rmsnorm_matmul_noalloc", "rmm_describe_plan", "rmsnorm_matmul_swiglu",
-                 "rmsnorm_matmul_ex")
+                 "rmsnorm_matmul_ex", "rmm_test_hooks")
 
 
 class RmmError(RuntimeError):
@@ -67,10 +67,11 @@ def _bind(l: ctypes.CDLL) -> ctypes.CDLL:
     l.rmm_status_string.restype = ctypes.c_char_p
     l.rmm_dispatch_path.argtypes = [i64, i64, i64]
     l.rmm_describe_plan.argtypes = [i64, i64, i64, i32, ctypes.POINTER(ctypes.c_int)]
+    l.rmm_test_hooks.argtypes = [i32, i64]
     for name in ("rmsnorm_matmul", "rmsnorm_matmul_noalloc", "rmsnorm_matmul_swiglu", "rmsnorm_matmul_ex",
                  "rmsnorm",
                  "matmul", "rmm_force_path", "rmm_device_status", "rmm_dispatch_path",
-                 "rmm_describe_plan"):
+                 "rmm_describe_plan", "rmm_test_hooks"):
         getattr(l, name).restype = i32
     return l
 

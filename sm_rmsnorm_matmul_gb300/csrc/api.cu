@@ -653,6 +653,17 @@ int rmm_device_status(cudaStream_t stream) {
     return v;
 }
 
+int rmm_test_hooks(int skip_sends, int64_t wait_limit_ns) {
+    if (wait_limit_ns < 0) return RMM_ERR_INVALID_ARG;
+    int dev = 0;
+    DeviceInfo d;
+    int rc = current_device(&dev, &d);
+    if (rc != RMM_OK) return rc;
+    const unsigned long long limit = wait_limit_ns > 0 ? static_cast<unsigned long long>(wait_limit_ns)
+                                                       : 2000000000ull;
+    return rmm::set_test_hooks(skip_sends != 0, limit) == cudaSuccess ? RMM_OK : RMM_ERR_LAUNCH;
+}
+
 const char* rmm_status_string(int code) {
     switch (code) {
         case RMM_OK: return "RMM_OK";

@@ -498,6 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t my_block = red_addr + rank * blk;   // this split's block in every CTA
         const int q = warp & 3, team = warp >> 2;
         const int row = q * 32 + lane;
+        const bool send = g_test_skip_sends == 0;
         if (have && threadIdx.x == 0)
             mbar_arrive_expect_tx(redfull,
                                   static_cast<uint32_t>((split - 1) * rows_here * (4 + owned * kUnitChunks * 128)));
@@ -531,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int g = 0; g < 8; ++g)
                             sts128(dst + ((g ^ swz) << 4),
                                    make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]));
-                    } else {
+                    } else if (send) {
                         const uint32_t rdst = mapa_shared(dst, owner);
                         const uint32_t rbar = mapa_shared(redfull, owner);
 #pragma unroll
@@ -545,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float ssv = kFused ? sr[row] : 0.f;
                 const uint32_t dst = my_block + row * 4;
                 *reinterpret_cast<float*>(smem + (dst - sb)) = ssv;
-                for (int p = 0; p < split; ++p)
+                for (int p = 0; p < split && send; ++p)
                     if (p != me) st_async_b32(mapa_shared(dst, p), __float_as_uint(ssv), mapa_shared(redfull, p));
             }
         }
@@ -1685,6 +1686,14 @@ cudaError_t launch_rmsnorm(const void* X, const void* g, void* Xn, int M, int K,
                                              static_cast<const __nv_bfloat16*>(g),
                                              static_cast<__nv_bfloat16*>(Xn), K, eps);
     return cudaGetLastError();
+}
+
+cudaError_t set_test_hooks(int skip_sends, unsigned long long wait_limit_ns) {
+    cudaError_t e = cudaMemcpyToSymbol(g_test_skip_sends, &skip_sends, sizeof(int));
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyToSymbol(g_wait_limit_ns, &wait_limit_ns, sizeof(wait_limit_ns));
+    if (e != cudaSuccess) return e;
+    return cudaDeviceSynchronize();
 }
 
 cudaError_t read_and_clear_status(int* out) {

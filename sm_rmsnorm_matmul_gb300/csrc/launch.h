@@ -89,5 +89,8 @@ cudaError_t launch_rmsnorm(const void* X, const void* g, void* Xn, int M, int K,
 
 // Copies the in-kernel status word to *out and clears it (synchronous).
 cudaError_t read_and_clear_status(int* out);
+// Test hooks of the current device (synchronous): skip the K-split sends,
+// and the limit of every bounded in-kernel wait.
+cudaError_t set_test_hooks(int skip_sends, unsigned long long wait_limit_ns);
 
 }  // namespace rmm

@@ -1,0 +1,50 @@
+"""The bounded in-kernel waits, run out on purpose without any fault.
+
+A test hook makes the row-tile kernel's K-split reduction skip the stores of
+its partials, so that every owning CTA's wait for them runs out (after a
+shortened limit).  The kernel must then record RMM_ERR_DEVICE_TIMEOUT, skip
+its remaining work, free its tensor memory and exit; rmm_device_status()
+reports it; and the next call on the same context runs normally.
+"""
+import pytest
+
+import oracle
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rmm():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sm_rmsnorm_matmul_gb300 as m
+    from sm_rmsnorm_matmul_gb300 import build
+    build.build()
+    m.lib()
+    return m
+
+
+def test_timeout_is_reported_and_the_context_recovers(rmm):
+    from sm_rmsnorm_matmul_gb300 import inputs
+    M, K, N = 16, 4096, 6144
+    plan = rmm.describe_plan(M, K, N)
+    assert plan["splits"] > 1 and plan["cluster"] == 1   # the K-split reduction runs
+    X, g, W = (t.cuda() for t in inputs.random_problem(M, K, N, seed=31))
+    l = rmm.lib()
+    assert rmm.device_status() == 0
+    assert l.rmm_test_hooks(1, 50_000_000) == 0          # skip the sends; 50 ms per wait
+    try:
+        rmm.rmsnorm_matmul(X, g, W, 1e-6)
+        assert rmm.device_status() == 5                  # RMM_ERR_DEVICE_TIMEOUT
+    finally:
+        assert l.rmm_test_hooks(0, 0) == 0               # normal operation, 2 s limit
+    Y = rmm.rmsnorm_matmul(X, g, W, 1e-6)
+    torch.cuda.synchronize()
+    assert rmm.device_status() == 0
+    bad, max_abs, _ = oracle.tolerance_violations(Y.cpu(), oracle.rmsnorm_matmul(X.cpu(), g.cpu(), W.cpu(), 1e-6))
+    assert bad == 0, max_abs
+
+
+def test_hook_rejects_negative_limit(rmm):
+    assert rmm.lib().rmm_test_hooks(0, -1) == 1
