@@ -16,7 +16,9 @@ W = identity against torch's RMSNorm, constant rows against a closed form, a
 hand-worked 2x3x2 example, and the matmul part against numpy.  The gated
 form is pinned by a zero gate giving zero, the exact odd part of SiLU
 (Y(W_gate) - Y(-W_gate) = Z_gate * Z_up), its two limits, and Y >= 0 when the
-gate and up projections coincide.
+gate and up projections coincide.  The LoRA form is pinned by a zero adapter
+giving the plain result bitwise, a zero W against the associativity of
+(RMSNorm(X) @ A) @ B in numpy, and a rank-one adapter against its closed form.
 """
 from __future__ import annotations
 
@@ -58,9 +60,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_rmsnorm_matmul.argtypes = [dp, dp, dp, dp, L, L, L, D, I]
     lib.oracle_rmsnorm_matmul_rewritten.argtypes = [dp, dp, dp, dp, L, L, L, D, I]
     lib.oracle_rmsnorm_matmul_swiglu.argtypes = [dp, dp, dp, dp, L, L, L, D, I]
+    lib.oracle_rmsnorm_matmul_lora.argtypes = [dp, dp, dp, dp, dp, dp, L, L, L, L, D, I]
     for f in (lib.oracle_rmsnorm, lib.oracle_matmul, lib.oracle_rmsnorm_matmul,
               lib.oracle_rmsnorm_matmul_rewritten, lib.oracle_rmsnorm_matmul_swiglu,
-              lib.oracle_max_threads):
+              lib.oracle_rmsnorm_matmul_lora, lib.oracle_max_threads):
         f.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     return lib
@@ -145,6 +148,20 @@ def rmsnorm_matmul_swiglu(X, g, W, eps: float, nthreads: int = 0, lib=None) -> n
     Y = np.empty((M, N // 2), dtype=np.float64)
     _check(lib.oracle_rmsnorm_matmul_swiglu(_ptr(X), _ptr(g), _ptr(W), _ptr(Y), M, K, N,
                                             float(eps), nthreads), "rmsnorm_matmul_swiglu")
+    return Y
+
+
+def rmsnorm_matmul_lora(X, g, W, A, B, eps: float, nthreads: int = 0, lib=None) -> np.ndarray:
+    """Y = RMSNorm(X; g, eps) @ (W + A @ B) in fp64; A [K, R], B [R, N]."""
+    lib = lib or load()
+    X, g, W, A, B = to_f64(X), to_f64(g), to_f64(W), to_f64(A), to_f64(B)
+    M, K = X.shape
+    N = W.shape[1]
+    R = A.shape[1]
+    assert A.shape == (K, R) and B.shape == (R, N)
+    Y = np.empty((M, N), dtype=np.float64)
+    _check(lib.oracle_rmsnorm_matmul_lora(_ptr(X), _ptr(g), _ptr(W), _ptr(A), _ptr(B), _ptr(Y),
+                                          M, K, N, R, float(eps), nthreads), "rmsnorm_matmul_lora")
     return Y
 
 

@@ -39,6 +39,14 @@
  *   Z[m,n]  = RMSNorm(X)[m,:] . W[:,n]                    (as above)
  *   Y[m,f]  = silu(Z[m,f]) * Z[m,F+f],  silu(z) = z / (1 + exp(-z)),  f < F.
  *
+ * oracle_rmsnorm_matmul_lora() is the LoRA variant (LoRA is another of the
+ * review page's benchmark workloads, section 5 table; no formula is given).
+ * Read as the standard low-rank adapter: A [K,R], B [R,N] with the scaling
+ * folded into B, and the effective weight W + A.B:
+ *
+ *   Weff[k,n] = W[k,n] + sum_j A[k,j] * B[j,n]
+ *   Y[m,n]    = RMSNorm(X)[m,:] . Weff[:,n]
+ *
  * Everything is double precision; nothing is rounded to bf16.  Row-major
  * layouts: X [M,K], g [K], W [K,N], Y [M,N] (Y [M,F] for the gated form).
  */
@@ -204,6 +212,31 @@ int oracle_rmsnorm_matmul_swiglu(const double *X, const double *g, const double 
                 Y[m * F + f] = silu(Z[m * N + f]) * Z[m * N + F + f];
     }
     free(Z);
+    return rc;
+}
+
+/* LoRA: Y = RMSNorm(X) @ (W + A @ B).  A [K,R], B [R,N]. */
+int oracle_rmsnorm_matmul_lora(const double *X, const double *g, const double *W,
+                               const double *A, const double *B, double *Y, long M,
+                               long K, long N, long R, double eps, int nthreads)
+{
+    double *Weff = (double *)malloc((size_t)(K * N > 0 ? K * N : 1) * sizeof(double));
+    if (!Weff)
+        return ORACLE_ERR_ALLOC;
+    /* the effective weight, W + A @ B, loop order k, j, n */
+    for (long k = 0; k < K; ++k) {
+        double *wk = Weff + k * N;
+        for (long n = 0; n < N; ++n)
+            wk[n] = W[k * N + n];
+        for (long j = 0; j < R; ++j) {
+            const double akj = A[k * R + j];
+            const double *bj = B + j * N;
+            for (long n = 0; n < N; ++n)
+                wk[n] += akj * bj[n];
+        }
+    }
+    int rc = oracle_rmsnorm_matmul(X, g, Weff, Y, M, K, N, eps, nthreads);
+    free(Weff);
     return rc;
 }
 

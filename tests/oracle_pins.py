@@ -289,6 +289,49 @@ def pin_gated_equal_projections(lib, seed=24):
     return (bool(np.all(y >= 0.0)) and bool(np.any(y > 0.0)), "gate = up gives y >= 0")
 
 
+# ---------------------------------------------------------------------------
+# L: LoRA (review page, section 5, benchmark table; read as
+# Y = RMSNorm(X) @ (W + A @ B)).  Pinned by
+#   L1 a zero adapter (A = 0, or B = 0) gives the plain oracle bitwise;
+#   L2 W = 0: Y = (RMSNorm(X) @ A) @ B, numpy's matmuls on the pinned RMSNorm;
+#   L3 a rank-one adapter a b^T with W = 0 has the closed form
+#      Y[m,n] = (sum_k Xn[m,k] a[k]) * b[n].
+# ---------------------------------------------------------------------------
+def _lora_problem(rng, M=6, K=20, N=9, R=4):
+    X = rng.standard_normal((M, K))
+    g = rng.uniform(0.5, 1.5, K)
+    W = rng.standard_normal((K, N))
+    A = rng.standard_normal((K, R))
+    B = rng.standard_normal((R, N))
+    return X, g, W, A, B
+
+
+def pin_lora_zero_adapter(lib, seed=31):
+    X, g, W, A, B = _lora_problem(_rng(seed))
+    y = oracle.rmsnorm_matmul(X, g, W, 1e-6, lib=lib)
+    ya = oracle.rmsnorm_matmul_lora(X, g, W, np.zeros_like(A), B, 1e-6, lib=lib)
+    yb = oracle.rmsnorm_matmul_lora(X, g, W, A, np.zeros_like(B), 1e-6, lib=lib)
+    return (bool(np.array_equal(ya, y) and np.array_equal(yb, y)), "zero adapter")
+
+
+def pin_lora_adapter_alone(lib, seed=32):
+    X, g, W, A, B = _lora_problem(_rng(seed))
+    y = oracle.rmsnorm_matmul_lora(X, g, np.zeros_like(W), A, B, 1e-6, lib=lib)
+    ref = (oracle.rmsnorm(X, g, 1e-6, lib=lib) @ A) @ B
+    err = _rel_normwise(y, ref)
+    return (err <= 1e-13, f"W = 0: normwise rel diff {err:.3e}")
+
+
+def pin_lora_rank_one(lib, seed=33):
+    X, g, W, A, B = _lora_problem(_rng(seed), R=1)
+    y = oracle.rmsnorm_matmul_lora(X, g, np.zeros_like(W), A, B, 0.0, lib=lib)
+    ms = (X * X).mean(axis=1)
+    xn = X * g[None, :] / np.sqrt(ms)[:, None]
+    ref = np.outer(xn @ A[:, 0], B[0])
+    err = _rel_normwise(y, ref)
+    return (err <= 1e-13, f"rank one: normwise rel diff {err:.3e}")
+
+
 ALL_PINS = {
     "rewrite_agrees": pin_rewrite_agrees,
     "scale_invariance": pin_scale_invariance,
@@ -301,4 +344,7 @@ ALL_PINS = {
     "gated_odd_part": pin_gated_odd_part,
     "gated_limits": pin_gated_limits,
     "gated_equal_projections": pin_gated_equal_projections,
+    "lora_zero_adapter": pin_lora_zero_adapter,
+    "lora_adapter_alone": pin_lora_adapter_alone,
+    "lora_rank_one": pin_lora_rank_one,
 }

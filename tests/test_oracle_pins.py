@@ -103,6 +103,14 @@ MUTANTS = [
     ("exponent sign flipped in silu", "return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
     ("up column off by one", "* Z[m * N + F + f];", "* Z[m * N + F + f - (f > 0)];"),
     ("gate not activated", "silu(Z[m * N + f]) * Z[m * N + F + f]", "Z[m * N + f] * Z[m * N + F + f]"),
+    # the LoRA form
+    ("adapter subtracted", "wk[n] += akj * bj[n];", "wk[n] -= akj * bj[n];"),
+    ("adapter doubled", "wk[n] += akj * bj[n];", "wk[n] += 2.0 * akj * bj[n];"),
+    ("adapter B read transposed", "const double *bj = B + j * N;", "const double *bj = B + j; /* mutant */"),
+    ("adapter A row and column swapped", "const double akj = A[k * R + j];",
+     "const double akj = A[(j * K + k) % (K * R)];"),
+    ("last adapter rank dropped", "for (long j = 0; j < R; ++j) {\n            const double akj",
+     "for (long j = 0; j < R - 1; ++j) {\n            const double akj"),
 ]
 
 
@@ -115,6 +123,9 @@ def test_pins_catch_mutant(tmp_path, desc, orig, repl):
     if desc == "W read transposed":
         # read W as if stored [N,K]: element (k,n) at n*K + k (stays in bounds)
         mutated = mutated.replace("y[n] += a * w[n];", "y[n] += a * w[n * K];")
+    if desc == "adapter B read transposed":
+        # read B as if stored [N,R]: element (j,n) at n*R + j (stays in bounds)
+        mutated = mutated.replace("wk[n] += akj * bj[n];", "wk[n] += akj * bj[n * R];")
     path = tmp_path / "mutant.c"
     path.write_text(mutated)
     so = tmp_path / "libmutant.so"
