@@ -124,6 +124,24 @@ int rmsnorm_matmul_ex(const void* X, const void* g, const void* W, void* Y,
                       cudaStream_t stream);
 
 /*
+ * RMSNorm + MatMul with a low-rank adapter (LoRA: another of the review page's
+ * benchmark workloads, section 5 table; no formula given, read as the standard
+ * adapter with its scaling folded into B):
+ *   Y [M,N] = RMSNorm(X; g, eps) @ (W + A @ B),  A [K,R], B [R,N] bf16,
+ *   1 <= R <= 64, R a multiple of 8; the other rules are those of
+ *   rmsnorm_matmul().
+ * Two launches of the row-tile kernels: T = bf16((X*g) @ A) [M,R] into a
+ * library-owned buffer per (device, stream) (allocated on first use; make that
+ * first call outside any CUDA-graph capture), then the main contraction with
+ * one more 64-deep stage per tile whose operands are T and B, so that
+ * Y = r * ((X*g) @ W + T @ B) with one division by the row RMS.  Returns an
+ * rmm_status.
+ */
+int rmsnorm_matmul_lora(const void* X, const void* g, const void* W, const void* A,
+                        const void* B, void* Y, int64_t M, int64_t K, int64_t N, int64_t R,
+                        float eps, cudaStream_t stream);
+
+/*
  * Unfused RMSNorm alone (the first of the two kernels that the review page's
  * muGraph example says existing systems launch):
  *   Xn[m,k] = bf16( X[m,k] * g[k] * r[m] ),  X, Xn [M,K] bf16, g [K] bf16.

@@ -23,7 +23,8 @@ from .build import LIB_PATH
 
 __all__ = [
     "RmmError", "lib", "rmsnorm_matmul", "rmsnorm_matmul_noalloc", "rmsnorm_matmul_swiglu",
-    "rmsnorm_matmul_ex", "WEIGHT_NK", "GATED_SILU", "rmsnorm", "matmul", "force_path",
+    "rmsnorm_matmul_ex", "rmsnorm_matmul_lora", "WEIGHT_NK", "GATED_SILU", "rmsnorm", "matmul",
+    "force_path",
     "dispatch_path", "describe_plan", "device_status", "status_string", "STATUS", "PATH_AUTO",
     "PATH_ROWS", "PATH_COLS", "ABI_FUNCTIONS",
 ]
@@ -40,7 +41,7 @@ WEIGHT_NK, GATED_SILU = 1, 2   # flags of rmsnorm_matmul_ex
 ABI_FUNCTIONS = ("rmsnorm_matmul", "rmsnorm", "matmul", "rmm_force_path",
                  "rmm_device_status", "rmm_status_string", "rmm_dispatch_path",
                  "rmsnorm_matmul_noalloc", "rmm_describe_plan", "rmsnorm_matmul_swiglu",
-                 "rmsnorm_matmul_ex", "rmm_test_hooks")
+                 "rmsnorm_matmul_ex", "rmm_test_hooks", "rmsnorm_matmul_lora")
 
 
 class RmmError(RuntimeError):
@@ -68,10 +69,11 @@ def _bind(l: ctypes.CDLL) -> ctypes.CDLL:
     l.rmm_dispatch_path.argtypes = [i64, i64, i64]
     l.rmm_describe_plan.argtypes = [i64, i64, i64, i32, ctypes.POINTER(ctypes.c_int)]
     l.rmm_test_hooks.argtypes = [i32, i64]
+    l.rmsnorm_matmul_lora.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, f32, vp]
     for name in ("rmsnorm_matmul", "rmsnorm_matmul_noalloc", "rmsnorm_matmul_swiglu", "rmsnorm_matmul_ex",
                  "rmsnorm",
                  "matmul", "rmm_force_path", "rmm_device_status", "rmm_dispatch_path",
-                 "rmm_describe_plan", "rmm_test_hooks"):
+                 "rmm_describe_plan", "rmm_test_hooks", "rmsnorm_matmul_lora"):
         getattr(l, name).restype = i32
     return l
 
@@ -183,6 +185,30 @@ def rmsnorm_matmul_ex(X, g, W, eps: float = 1e-6, weight_nk: bool = False, gated
     flags = (WEIGHT_NK if weight_nk else 0) | (GATED_SILU if gated else 0)
     _raise(lib().rmsnorm_matmul_ex(X.data_ptr(), g.data_ptr(), W.data_ptr(), out.data_ptr(),
                                    M, K, N, float(eps), flags, _stream_ptr(stream)), "rmsnorm_matmul_ex")
+    return out
+
+
+def rmsnorm_matmul_lora(X, g, W, A, B, eps: float = 1e-6, out=None, stream=None):
+    """Y[M,N] = RMSNorm(X; g, eps) @ (W + A @ B) with a low-rank adapter A [K,R],
+    B [R,N] (R <= 64, a multiple of 8)."""
+    import torch
+    for name, t in (("X", X), ("g", g), ("W", W), ("A", A), ("B", B)):
+        _check_bf16(name, t, 1 if name == "g" else 2)
+    M, K = X.shape
+    N = W.shape[1]
+    R = A.shape[1]
+    if g.shape[0] != K or W.shape[0] != K or A.shape[0] != K or tuple(B.shape) != (R, N):
+        raise ValueError(f"shape mismatch: X {tuple(X.shape)}, W {tuple(W.shape)}, A {tuple(A.shape)}, "
+                         f"B {tuple(B.shape)}")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    else:
+        _check_bf16("out", out, 2)
+        if tuple(out.shape) != (M, N):
+            raise ValueError(f"out must have shape {(M, N)}")
+    _raise(lib().rmsnorm_matmul_lora(X.data_ptr(), g.data_ptr(), W.data_ptr(), A.data_ptr(), B.data_ptr(),
+                                     out.data_ptr(), M, K, N, R, float(eps), _stream_ptr(stream)),
+           "rmsnorm_matmul_lora")
     return out
 
 

@@ -157,6 +157,8 @@ struct Workspace {
     size_t ss_bytes = 0;
     int* counters = nullptr;
     size_t n_counters = 0;
+    void* lora_t = nullptr;   // the low-rank adapter's T = bf16((X*g) @ A), [M, R]
+    size_t lora_t_bytes = 0;
 };
 
 std::mutex g_ws_mu;
@@ -219,6 +221,27 @@ cudaError_t clear_workspace_counters() {
         if (e != cudaSuccess) return e;
     }
     return cudaDeviceSynchronize();
+}
+
+// The T buffer of (dev, stream) for the low-rank adapter, grown to `bytes`.
+// Growing synchronises the stream and is refused during capture.
+int get_lora_buffer(int dev, cudaStream_t s, size_t bytes, void** out) {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    Workspace& w = g_ws[{dev, s}];
+    if (w.lora_t_bytes < bytes) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+            return RMM_ERR_INTERNAL;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return RMM_ERR_LAUNCH;
+        void* p = nullptr;
+        const size_t n = round_up_pow2(bytes);
+        if (cudaMalloc(&p, n) != cudaSuccess) return RMM_ERR_INTERNAL;
+        if (w.lora_t) cudaFree(w.lora_t);
+        w.lora_t = p;
+        w.lora_t_bytes = n;
+    }
+    *out = w.lora_t;
+    return RMM_OK;
 }
 
 // ---------------------------------------------------------------- planning
@@ -432,14 +455,19 @@ int choose_path(int64_t M) {
 // Without may_allocate, plans that need the per-stream workspace are avoided.
 // glu: the gated form (fused only; always the row-tile path), Y [M, N / 2].
 // wnk: W stored [N, K] (fused only; always the row-tile path).
+// unscaled: no division by the row RMS.  lora_t, lora_b: the low-rank
+// adapter's T [M, R] and B [R, N], added as one more stage per tile (row-tile
+// path).
 int run_contraction(bool fused, const void* X, const void* g, const void* W, void* Y, int64_t M,
                     int64_t K, int64_t N, float eps, cudaStream_t stream, bool may_allocate = true,
-                    bool glu = false, bool wnk = false) {
+                    bool glu = false, bool wnk = false, bool unscaled = false,
+                    const void* lora_t = nullptr, const void* lora_b = nullptr, int64_t R = 0) {
+    const bool lora = lora_t != nullptr;
     int dev = 0;
     DeviceInfo d;
     int rc = current_device(&dev, &d);
     if (rc != RMM_OK) return rc;
-    const int path = glu || wnk ? static_cast<int>(kPathRows) : choose_path(M);
+    const int path = glu || wnk || lora || unscaled ? static_cast<int>(kPathRows) : choose_path(M);
     CUtensorMap tmX, tmW, tmG;
     // [K, N]: boxes of [64 k][64 n]; [N, K]: boxes of [256 n][64 k], or 128 rows
     // each for the gate and up halves of the gated form
@@ -501,6 +529,12 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
     a.red_overlay = p.overlay;
     a.glu = glu ? 1 : 0;
     a.w_nk = wnk ? 1 : 0;
+    a.unscaled = unscaled ? 1 : 0;
+    a.lora = lora ? 1 : 0;
+    CUtensorMap tmT = tmX, tmB = tmW;   // unused without the adapter
+    if (lora) {
+        if (!map_2d(&tmT, lora_t, M, R, p.xrows) || !map_2d(&tmB, lora_b, R, N, kBK)) return RMM_ERR_INTERNAL;
+    }
     CUtensorMap tmY;
     a.tail_tiles = 0;
     a.tail_pieces = 1;
@@ -531,7 +565,7 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
             }
         }
     }
-    return rmm::launch_rows(fused, tmX, tmW, tmG, Y, a, stream) == cudaSuccess ? RMM_OK
+    return rmm::launch_rows(fused, tmX, tmW, tmG, tmT, tmB, Y, a, stream) == cudaSuccess ? RMM_OK
                                                                               : RMM_ERR_LAUNCH;
 }
 
@@ -565,6 +599,33 @@ int rmsnorm_matmul_ex(const void* X, const void* g, const void* W, void* Y, int6
                      {W, static_cast<size_t>(K) * N * 2}});
     if (rc != RMM_OK) return rc;
     return run_contraction(true, X, g, W, Y, M, K, N, eps, stream, true, glu, wnk);
+}
+
+int rmsnorm_matmul_lora(const void* X, const void* g, const void* W, const void* A, const void* B,
+                        void* Y, int64_t M, int64_t K, int64_t N, int64_t R, float eps,
+                        cudaStream_t stream) {
+    int rc = check_sizes(M, K, N, eps, true);
+    if (rc == kNoop) return RMM_OK;
+    if (rc != RMM_OK) return rc;
+    if (R < 1 || R > kBK) return RMM_ERR_INVALID_ARG;
+    if (R % 8 != 0) return RMM_ERR_ALIGNMENT;
+    rc = check_ptrs(Y, static_cast<size_t>(M) * N * 2,
+                    {{X, static_cast<size_t>(M) * K * 2}, {g, static_cast<size_t>(K) * 2},
+                     {W, static_cast<size_t>(K) * N * 2}, {A, static_cast<size_t>(K) * R * 2},
+                     {B, static_cast<size_t>(R) * N * 2}});
+    if (rc != RMM_OK) return rc;
+    int dev = 0;
+    DeviceInfo d;
+    rc = current_device(&dev, &d);
+    if (rc != RMM_OK) return rc;
+    void* T = nullptr;
+    rc = get_lora_buffer(dev, stream, static_cast<size_t>(M) * R * 2, &T);
+    if (rc != RMM_OK) return rc;
+    // T = bf16((X*g) @ A): the same gained, bf16-rounded rows the MMA sees,
+    // without the division by the RMS (applied once, to the sum, below)
+    rc = run_contraction(true, X, g, A, T, M, K, R, eps, stream, true, false, false, true);
+    if (rc != RMM_OK) return rc;
+    return run_contraction(true, X, g, W, Y, M, K, N, eps, stream, true, false, false, false, T, B, R);
 }
 
 int rmsnorm_matmul_swiglu(const void* X, const void* g, const void* W, void* Y, int64_t M,

@@ -188,8 +188,8 @@ __host__ __device__ inline RowsLayout rows_layout(int xrows, int stages, int red
 template <bool kFused, bool kSplit, bool kGlu, bool kWnk>
 __global__ void __launch_bounds__(kThreads, 1)
     rows_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                const __grid_constant__ CUtensorMap tmG, __nv_bfloat16* __restrict__ Y,
-                RowsLaunch a) {
+                const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmT,
+                const __grid_constant__ CUtensorMap tmB, __nv_bfloat16* __restrict__ Y, RowsLaunch a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     const int S = a.stages;
@@ -235,13 +235,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // boxes of gate columns n0.. and two of up columns Nout + n0.. (always
     // four: a box past the gate half reads up columns, one past N reads
     // zeros, and neither reaches an output column).
+    // Low-rank adapter: the unit holding split 0 of a tile runs one more
+    // stage after its k-blocks, at k-block index k_blocks, whose A tile is
+    // T = bf16((X*g) @ A) (rows of tmT, R <= 64 columns, zeros past R) and
+    // whose B tile is the adapter's B (rows of tmB, zeros past R); it gets
+    // no gain and adds nothing to the row statistic.
+    // (compiled into the plain [K, N] form only, the one the adapter API uses)
+    constexpr bool kAdapter = kFused && !kGlu && !kWnk;
+    auto lora_extra = [&](int sp) { return kAdapter && a.lora && sp == 0 ? 1 : 0; };
     // Loads of stage s = k-block kb of the unit whose tile starts at row block
-    // mb and output column n0.
+    // mb and output column n0 (kb == k_blocks: the adapter stage).
     auto issue = [&](uint32_t s, int kb, int mb, int n0) {
-        mbar_arrive_expect_tx(full(s), xbytes + w_stage_bytes<kGlu, kWnk>(n0, a.N) + (kFused ? kGBytes : 0));
-        tma_load_2d_nohint(sx + s * xbytes, &tmX, full(s), kb * kBK, mb * kRowsBM);
-        load_w_stage<kGlu, kWnk>(sw + s * kRowsWBytes, &tmW, full(s), n0, kb, a.N, Nout);
-        if (kFused) tma_load_1d(sg + s * kGBytes, &tmG, full(s), kb * kBK);
+        const bool ext = kb >= a.k_blocks;
+        mbar_arrive_expect_tx(full(s), xbytes + w_stage_bytes<kGlu, kWnk>(n0, a.N) +
+                                           (kFused && !ext ? kGBytes : 0));
+        tma_load_2d_nohint(sx + s * xbytes, ext ? &tmT : &tmX, full(s), ext ? 0 : kb * kBK, mb * kRowsBM);
+        load_w_stage<kGlu, kWnk>(sw + s * kRowsWBytes, ext ? &tmB : &tmW, full(s), n0, ext ? 0 : kb, a.N, Nout);
+        if (kFused && !ext) tma_load_1d(sg + s * kGBytes, &tmG, full(s), kb * kBK);
     };
     // k-blocks of the first unit that thread 0 (the producer) issues before
     // the CTA-wide set-up barrier, as soon as its barriers exist and the
@@ -277,8 +287,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             int mb, nb;
             rows_tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
             const int n0 = nb * kOutBN;
-            pro = static_cast<uint32_t>(min(S, kb1 - kb0));
-            for (uint32_t i = 0; i < pro; ++i) issue(i, kb0 + static_cast<int>(i), mb, n0);
+            const int kend = kb1 + lora_extra(sp);
+            pro = static_cast<uint32_t>(min(S, kend - kb0));
+            for (uint32_t i = 0; i < pro; ++i) {
+                const int kb = kb0 + static_cast<int>(i);
+                issue(i, kb < kb1 ? kb : a.k_blocks, mb, n0);
+            }
         }
     }
     if (warp == 2) {
@@ -308,10 +322,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 rows_tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
                 const int n0 = nb * kOutBN;
                 const int first = kb0 + (u == static_cast<int>(blockIdx.x) ? static_cast<int>(pro) : 0);
-                for (int kb = first; kb < kb1; ++kb) {
+                const int kend = kb1 + lora_extra(sp);
+                for (int kb = first; kb < kend; ++kb) {
                     const uint32_t s = ring.idx, ph = ring.phase;
                     if (!mbar_wait(empty(s), ph ^ 1, abort)) { ok = false; break; }
-                    issue(s, kb, mb, n0);
+                    issue(s, kb < kb1 ? kb : a.k_blocks, mb, n0);
                     ++it;
                     ring.advance();
                 }
@@ -334,7 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(accempty(buf), (use & 1) ^ 1, abort)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + buf * kRowsBN;
-                for (int kb = kb0; kb < kb1; ++kb) {
+                const int kend = kb1 + lora_extra(sp);
+                for (int kb = kb0; kb < kend; ++kb) {
                     const uint32_t s = ring.idx, ph = ring.phase;
                     if (!mbar_wait(kFused ? xform(s) : full(s), ph, abort)) { ok = false; break; }
                     tc_fence_after();
@@ -375,21 +391,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float ss[kRowsBM / 16];
 #pragma unroll
                 for (int i = 0; i < kRowsBM / 16; ++i) ss[i] = 0.f;
-                for (int kb = kb0; kb < kb1; ++kb) {
+                const int kend = kb1 + lora_extra(sp);
+                for (int kb = kb0; kb < kend; ++kb) {
                     const uint32_t s = ring.idx, ph = ring.phase;
                     if (!warp_wait(full(s), ph, abort)) { ok = false; break; }
-                    const uint4 gv = lds128(sg + s * kGBytes + kc * 16);
-                    const uint32_t xt = sx + s * xbytes + swz_off;
-                    // rows rb + 16 i all have (row & 7) == (rb & 7)
-                    // all loads first, then the stores (the shared-memory
-                    // accesses keep program order), so the loads overlap
-                    uint4 xv[kRowsBM / 16];
+                    if (kb < kb1) {   // (the adapter stage needs no transform)
+                        const uint4 gv = lds128(sg + s * kGBytes + kc * 16);
+                        const uint32_t xt = sx + s * xbytes + swz_off;
+                        // rows rb + 16 i all have (row & 7) == (rb & 7)
+                        // all loads first, then the stores (the shared-memory
+                        // accesses keep program order), so the loads overlap
+                        uint4 xv[kRowsBM / 16];
 #pragma unroll
-                    for (int i = 0; i < kRowsBM / 16; ++i)
-                        if (i < groups) xv[i] = lds128(xt + (rb + 16 * i) * 128);
+                        for (int i = 0; i < kRowsBM / 16; ++i)
+                            if (i < groups) xv[i] = lds128(xt + (rb + 16 * i) * 128);
 #pragma unroll
-                    for (int i = 0; i < kRowsBM / 16; ++i)
-                        if (i < groups) sts128(xt + (rb + 16 * i) * 128, gain8(xv[i], gv, ss[i]));
+                        for (int i = 0; i < kRowsBM / 16; ++i)
+                            if (i < groups) sts128(xt + (rb + 16 * i) * 128, gain8(xv[i], gv, ss[i]));
+                    }
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(xform(s));
@@ -428,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t taddr = tmem + buf * kRowsBN + (static_cast<uint32_t>(q * 32) << 16);
             const bool warp_has_rows = q * 32 < rows_here;              // warp-uniform
             const int m = mb * kRowsBM + row;
-            const float r = kFused ? rsqrtf(sr[buf * kRowsBM + row] * inv_k + a.eps) : 1.f;
+            const float r = kFused && !a.unscaled ? rsqrtf(sr[buf * kRowsBM + row] * inv_k + a.eps) : 1.f;
             __nv_bfloat16* yrow = Y + static_cast<size_t>(m) * Nout + n0;
             for (int c = 0; warp_has_rows && c < kOutBN / 32; ++c) {
                 if (c * 32 >= ncols) break;   // warp-uniform
@@ -589,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             acc[h].w += __uint_as_float(t4[s2][h].w);
                         }
                     }
-                const float r = kFused ? rsqrtf(tot * inv_k + a.eps) : 1.f;
+                const float r = kFused && !a.unscaled ? rsqrtf(tot * inv_k + a.eps) : 1.f;
                 const int col = (me + j * split) * 32 + g * 4;
                 if (col < ncols) {
                     float o4[4];
@@ -659,6 +678,7 @@ constexpr uint32_t kTaAccCol = 0, kTaACol = 256;
 // piece b % tail_pieces of tail tile b / tail_pieces (tile full + that).
 struct TaUnit {
     int t, kb0, kb1, piece;   // piece < 0: the whole K range
+    int extra;                // 1: the low-rank adapter stage follows (whole tile, or piece 0)
 };
 __device__ __forceinline__ bool ta_unit(const RowsLaunch& a, int i, TaUnit& u) {
     const int G = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
@@ -669,6 +689,7 @@ __device__ __forceinline__ bool ta_unit(const RowsLaunch& a, int i, TaUnit& u) {
         u.kb0 = 0;
         u.kb1 = a.k_blocks;
         u.piece = -1;
+        u.extra = a.lora ? 1 : 0;
         return true;
     }
     const int whole = b < full ? (full - b + G - 1) / G : 0;
@@ -677,13 +698,15 @@ __device__ __forceinline__ bool ta_unit(const RowsLaunch& a, int i, TaUnit& u) {
     u.t = full + b / a.tail_pieces;
     u.kb0 = u.piece * a.tail_kbp;
     u.kb1 = min(a.k_blocks, u.kb0 + a.tail_kbp);
+    u.extra = a.lora && u.piece == 0 ? 1 : 0;
     return true;
 }
 
 template <bool kGlu, bool kWnk>
 __global__ void __launch_bounds__(kThreads, 1)
     rows_ta_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                   const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmY,
+                   const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmT,
+                   const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmY,
                    __nv_bfloat16* __restrict__ Y, RowsLaunch a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
@@ -756,6 +779,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 128 output columns read from gate columns n0.. and up columns F + n0..
     const int Nout = kGlu ? a.N / 2 : a.N;
     constexpr int kOutBN = kGlu ? kRowsBN / 2 : kRowsBN;
+    // the low-rank adapter stage exists in the plain [K, N] form only
+    constexpr bool kAdapter = !kGlu && !kWnk;
 
     if (warp == 0 || warp == 3) {
         // ------------------------------------------------ TMA producers
@@ -773,16 +798,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int mb, nb;
                 rows_tile_coords(un.t, a.m_tiles, a.n_tiles, mb, nb);
                 const int n0 = nb * kOutBN;
-                for (int kb = un.kb0; kb < un.kb1; ++kb) {
+                for (int kb = un.kb0; kb < un.kb1 + (kAdapter ? un.extra : 0); ++kb) {
+                    const bool ext = kAdapter && kb >= un.kb1;   // the adapter stage: T and B
                     if (!mbar_wait(empty0 + 8 * ring.idx, ring.phase ^ 1, abort)) { ok = false; break; }
                     const uint32_t f = full0 + 8 * ring.idx;
                     if (load_x) {
-                        mbar_arrive_expect_tx(f, kTaXBytes + kGBytes);
-                        tma_load_2d_nohint(sx + ring.idx * kTaXBytes, &tmX, f, kb * kBK, mb * kRowsBM);
-                        tma_load_1d(sg + ring.idx * kGBytes, &tmG, f, kb * kBK);
+                        mbar_arrive_expect_tx(f, kTaXBytes + (ext ? 0 : kGBytes));
+                        tma_load_2d_nohint(sx + ring.idx * kTaXBytes, ext ? &tmT : &tmX, f, ext ? 0 : kb * kBK,
+                                           mb * kRowsBM);
+                        if (!ext) tma_load_1d(sg + ring.idx * kGBytes, &tmG, f, kb * kBK);
                     } else {
                         mbar_arrive_expect_tx(f, w_stage_bytes<kGlu, kWnk>(n0, a.N));
-                        load_w_stage<kGlu, kWnk>(sw + ring.idx * kRowsWBytes, &tmW, f, n0, kb, a.N, Nout);
+                        load_w_stage<kGlu, kWnk>(sw + ring.idx * kRowsWBytes, ext ? &tmB : &tmW, f, n0,
+                                                 ext ? 0 : kb, a.N, Nout);
                     }
                     ring.advance();
                     ++issued;
@@ -805,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(accempty, (tl & 1) ^ 1, abort)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + kTaAccCol;
-                for (int kb = un.kb0; kb < un.kb1; ++kb) {
+                for (int kb = un.kb0; kb < un.kb1 + (kAdapter ? un.extra : 0); ++kb) {
                     if (!mbar_wait(wfull0 + 8 * wr.idx, wr.phase, abort)) { ok = false; break; }
                     if (!mbar_wait(afull0 + 8 * ar.idx, ar.phase, abort)) { ok = false; break; }
                     tc_fence_after();
@@ -843,7 +871,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             float ssp[8];   // independent partial sums: no long dependency chain
 #pragma unroll
             for (int c = 0; c < 8; ++c) ssp[c] = 0.f;
-            for (int kb = un.kb0; kb < un.kb1; ++kb) {
+            for (int kb = un.kb0; kb < un.kb1 + (kAdapter ? un.extra : 0); ++kb) {
+                const bool ext = kAdapter && kb >= un.kb1;   // the adapter stage: T rows, no gain, no statistic
                 if (!warp_wait(xfull0 + 8 * xr.idx, xr.phase, abort)) { ok = false; break; }
                 const uint32_t xt = sx + xr.idx * kTaXBytes + xrow;
                 const uint32_t gt = sg + xr.idx * kGBytes;
@@ -853,8 +882,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t out[32];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    const uint4 gv = lds128(gt + c * 16);
                     const uint32_t xs[4] = {xv[c].x, xv[c].y, xv[c].z, xv[c].w};
+                    if (ext) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) out[c * 4 + i] = xs[i];
+                        continue;
+                    }
+                    const uint4 gv = lds128(gt + c * 16);
                     const uint32_t gs[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -950,7 +984,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok && e < r1 - r0) {
                     float tot = 0.f;
                     for (int p2 = 0; p2 < P; ++p2) tot += __ldcg(a.ws_ss + (slot + p2) * kRowsBM + r0 + e);
-                    rr[e] = rsqrtf(tot * inv_k + a.eps);
+                    rr[e] = a.unscaled ? 1.f : rsqrtf(tot * inv_k + a.eps);
                 }
                 ok = epi_sync() && ok;
                 // items: 4 output columns of one row; gated, from the gate
@@ -1022,7 +1056,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 continue;
             }
-            const float r = rsqrtf(ss_row * inv_k + a.eps);
+            const float r = a.unscaled ? 1.f : rsqrtf(ss_row * inv_k + a.eps);
             uint32_t pk[kOutBN / 2];   // the row's outputs, packed as bf16x2
 #pragma unroll
             for (int c = 0; c < kOutBN / 16; ++c) {
@@ -1599,7 +1633,8 @@ cudaError_t launch_ex(void (*kern)(Args...), int grid, size_t smem, int cluster,
 }
 
 cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& tmW,
-                        const CUtensorMap& tmG, void* Y, const RowsLaunch& a, cudaStream_t s) {
+                        const CUtensorMap& tmG, const CUtensorMap& tmT, const CUtensorMap& tmB, void* Y,
+                        const RowsLaunch& a, cudaStream_t s) {
     auto* y = static_cast<__nv_bfloat16*>(Y);
     const bool split = a.cluster != 0;
     const bool glu = a.glu != 0, wnk = a.w_nk != 0;
@@ -1609,7 +1644,7 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
                       : (glu ? rows_ta_kernel<true, false> : rows_ta_kernel<false, false>);
         cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(ta), wnk ? (glu ? 15 : 14) : (glu ? 9 : 6));
         if (e != cudaSuccess) return e;
-        e = launch_ex(ta, a.grid, kTaSmem, 1, s, tmX, tmW, tmG, *a.tmY, y, a);
+        e = launch_ex(ta, a.grid, kTaSmem, 1, s, tmX, tmW, tmG, tmT, tmB, *a.tmY, y, a);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
@@ -1630,7 +1665,7 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), slot);
     if (e != cudaSuccess) return e;
     const size_t smem = rows_smem_bytes(a.xrows, a.stages, split ? a.splits : 0, a.MP, split && a.red_overlay, glu);
-    e = launch_ex(kern, a.grid, smem, split ? a.splits : 1, s, tmX, tmW, tmG, y, a);
+    e = launch_ex(kern, a.grid, smem, split ? a.splits : 1, s, tmX, tmW, tmG, tmT, tmB, y, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -53,6 +53,8 @@ struct RowsLaunch {
     int glu;                   // 1: gated form: W [K, N = 2F] holds gate then up columns,
                                // Y [M, F] = silu(gate) * up; output tiles of 128 columns
     int w_nk;                  // 1: W stored [N, K] (K contiguous), read K-major
+    int unscaled;              // 1: no division by the row RMS (Y = (X*g) @ W)
+    int lora;                  // 1: one more stage per tile from the adapter's T and B
     int cluster;               // 1: the splits of a tile form a cluster
     int xrows, MP, stages;
     int grid;
@@ -80,8 +82,10 @@ struct ColsLaunch {
     int* counters;    // [n_tiles][4] arrival counters (one per epilogue warp), zero between launches
 };
 
+// tmT, tmB: the low-rank adapter's T [M, R] and B [R, N] (used with a.lora).
 cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& tmW,
-                        const CUtensorMap& tmG, void* Y, const RowsLaunch& a, cudaStream_t s);
+                        const CUtensorMap& tmG, const CUtensorMap& tmT, const CUtensorMap& tmB, void* Y,
+                        const RowsLaunch& a, cudaStream_t s);
 cudaError_t launch_cols(bool fused, const CUtensorMap& tmX, const CUtensorMap& tmW,
                         const CUtensorMap& tmG, void* Y, const ColsLaunch& a, cudaStream_t s);
 cudaError_t launch_rmsnorm(const void* X, const void* g, void* Xn, int M, int K, float eps,

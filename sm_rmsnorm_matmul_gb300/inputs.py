@@ -113,3 +113,14 @@ def generate_workload(w: Workload):
 def random_problem(M: int, K: int, N: int, seed: int, x_kind: str = "normal"):
     """A ragged-shape problem with the same distributions (W std 1/sqrt(K))."""
     return generate(M, K, N, seed=seed, w_std=1.0 / math.sqrt(K), x_kind=x_kind)
+
+
+def lora_adapter(K: int, N: int, R: int, seed: int):
+    """A low-rank adapter (A [K,R], B [R,N]) as contiguous bf16 CPU tensors:
+    A ~ N(0, 1/sqrt(K)), B ~ N(0, 1/sqrt(R)), so that the adapter's share of
+    the output is of the same order as W's for unit-RMS rows."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    a = torch.randn(K, R, generator=gen, dtype=torch.float32) / math.sqrt(K)
+    b = torch.randn(R, N, generator=gen, dtype=torch.float32) / math.sqrt(R)
+    return a.to(torch.bfloat16).contiguous(), b.to(torch.bfloat16).contiguous()

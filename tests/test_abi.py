@@ -107,6 +107,17 @@ def test_ex_validation(lib):
     assert f(0, 0, 0, 0, 8, 64, 0, 1e-6, 3, None) == 0               # N = 0: no-op
 
 
+def test_lora_validation(lib):
+    f = lib.rmsnorm_matmul_lora
+    E16 = 0x70000000
+    assert f(A16, B16, C16, D16, E16, D16 + 0x100000, 8, 64, 64, 0, 1e-6, None) == 1    # R = 0
+    assert f(A16, B16, C16, D16, E16, D16 + 0x100000, 8, 64, 64, 72, 1e-6, None) == 1   # R > 64
+    assert f(A16, B16, C16, D16, E16, D16 + 0x100000, 8, 64, 64, 12, 1e-6, None) == 2   # R % 8
+    assert f(A16, B16, C16, D16, 0, D16 + 0x100000, 8, 64, 64, 16, 1e-6, None) == 1     # NULL B
+    assert f(A16, B16, C16, D16, E16, D16, 8, 64, 64, 16, 1e-6, None) == 1              # Y aliases A
+    assert f(0, 0, 0, 0, 0, 0, 0, 64, 64, 16, 1e-6, None) == 0                          # M = 0: no-op
+
+
 def test_unfused_validation(lib):
     assert lib.rmsnorm(0, B16, D16, 8, 64, 1e-6, None) == 1
     assert lib.rmsnorm(A16, B16, D16, 8, 63, 1e-6, None) == 2

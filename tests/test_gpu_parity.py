@@ -219,6 +219,48 @@ def test_weight_nk(rmm, M, K, N, gated):
         assert_close(Y.cpu(), oracle.rmsnorm_matmul(X, g, W, 1e-6), f"[N,K] {M}x{K}x{N}")
 
 
+# ------------------------------------------------------- low-rank adapter
+# rmsnorm_matmul_lora: Y = RMSNorm(X) @ (W + A @ B), A [K,R], B [R,N].
+LORA = [
+    (16, 4096, 6144, 16),    # decode QKV shape: K split, the adapter stage in split 0
+    (64, 4096, 28672, 64),   # one CTA per column tile
+    (7, 72, 136, 8),         # ragged rows, K and N; a single k-block plus the adapter
+    (1280, 1024, 4096, 32),  # prefill kernel: whole tiles and K pieces (piece 0 adds it)
+    (300, 520, 264, 24),     # several row tiles, ragged
+]
+
+
+def assert_lora_close(Y, X, g, W, A, B, eps, what):
+    """Y = RMSNorm(X) @ (W + A @ B) against the oracle.  The tensor cores take
+    the adapter's intermediate T = (X*g) @ A as bf16, one rounding per element
+    (relative error <= 2^-8) that the K-sum does not average out, so the bound
+    adds that rounding carried through r[m] * T @ B to the ungated one:
+      |dy| <= 1e-2 + 1e-2 |y| + r[m] * 2^-8 * sum_j |T[m,j]| |B[j,n]|."""
+    ref = oracle.rmsnorm_matmul_lora(X, g, W, A, B, eps)
+    Xf, gf, Af, Bf = (oracle.to_f64(t) for t in (X, g, A, B))
+    r = 1.0 / np.sqrt((Xf * Xf).mean(axis=1) + eps)
+    T = (Xf * gf[None, :]) @ Af
+    tol = ATOL + RTOL * np.abs(ref) + r[:, None] * 2.0 ** -8 * (np.abs(T) @ np.abs(Bf))
+    y = oracle.to_f64(Y)
+    bad = ~(np.abs(y - ref) <= tol)   # NaN fails
+    assert not bad.any(), f"{what}: {int(bad.sum())} of {ref.size} outside the bound"
+
+
+@pytest.mark.parametrize("M,K,N,R", LORA)
+def test_lora(rmm, M, K, N, R):
+    from sm_rmsnorm_matmul_gb300 import inputs
+    X, g, W = inputs.random_problem(M, K, N, seed=M + K + N + R, x_kind="row_scaled")
+    A, B = inputs.lora_adapter(K, N, R, seed=R + 1)
+    Y = rmm.rmsnorm_matmul_lora(X.cuda(), g.cuda(), W.cuda(), A.cuda(), B.cuda(), 1e-5)
+    torch.cuda.synchronize()
+    assert rmm.device_status() == 0
+    assert_lora_close(Y.cpu(), X, g, W, A, B, 1e-5, f"lora {M}x{K}x{N} R={R}")
+    # a zero adapter gives the plain result
+    Y0 = rmm.rmsnorm_matmul_lora(X.cuda(), g.cuda(), W.cuda(), torch.zeros_like(A).cuda(), B.cuda(), 1e-5)
+    torch.cuda.synchronize()
+    assert_close(Y0.cpu(), oracle.rmsnorm_matmul(X, g, W, 1e-5), f"lora zero adapter {M}x{K}x{N}")
+
+
 def test_small_m_rejects_large_m_when_forced(rmm, forced):
     forced(2)
     X = torch.zeros(129, 64, dtype=torch.bfloat16, device="cuda")
