@@ -276,16 +276,21 @@ def time_graph(torch, stream, step_fn, n_copies, K, chunk=500):
 
 
 def bench_workload(torch, rmm, inputs, w, K, W_warm, device, stream, l2, with_unfused=True,
-                   sampler=None, barrier=None, gated=False, weight_nk=False):
-    """gated: time the gated form (Y [M, N/2]); weight_nk: W stored [N, K]."""
+                   sampler=None, barrier=None, gated=False, weight_nk=False, lora_r=0):
+    """gated: time the gated form (Y [M, N/2]); weight_nk: W stored [N, K];
+    lora_r > 0: the low-rank adapter form with rank lora_r."""
     n_copies = n_rotating_copies(w, l2)
     F = w.N // 2
     host, copies = make_copies(w, n_copies, device, torch, inputs, out_cols=F if gated else None,
                                weight_nk=weight_nk)
+    if lora_r:
+        A, B = (t.to(device) for t in inputs.lora_adapter(w.K, w.N, lora_r, seed=w.seed + 100))
 
     def step(i):
         x, g, wt, y = copies[i]
-        if gated or weight_nk:
+        if lora_r:
+            rmm.rmsnorm_matmul_lora(x, g, wt, A, B, w.eps, out=y, stream=stream)
+        elif gated or weight_nk:
             rmm.rmsnorm_matmul_ex(x, g, wt, w.eps, weight_nk=weight_nk, gated=gated, out=y, stream=stream)
         else:
             rmm.rmsnorm_matmul(x, g, wt, w.eps, out=y, stream=stream)
@@ -313,14 +318,22 @@ def bench_workload(torch, rmm, inputs, w, K, W_warm, device, stream, l2, with_un
     if with_unfused:
         xn = [torch.empty((w.M, w.K), dtype=torch.bfloat16, device=device) for _ in range(n_copies)]
         zs = [torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device) for _ in range(n_copies)] \
-            if gated else None
+            if gated or lora_r else None
+        ts = torch.empty((w.M, lora_r), dtype=torch.bfloat16, device=device) if lora_r else None
 
         def step_unfused(i):
             # the separate kernels: RMSNorm, MatMul (and, gated, torch's
-            # elementwise silu(gate) * up on the bf16 product)
+            # elementwise silu(gate) * up on the bf16 product; with an
+            # adapter, Xn @ A, T @ B and torch's elementwise add)
             x, g, wt, y = copies[i]
             rmm.rmsnorm(x, g, w.eps, out=xn[i], stream=stream)
-            if gated:
+            if lora_r:
+                rmm.matmul(xn[i], wt, out=y, stream=stream)
+                rmm.matmul(xn[i], A, out=ts, stream=stream)
+                rmm.matmul(ts, B, out=zs[i], stream=stream)
+                with torch.cuda.stream(stream):
+                    y.add_(zs[i])
+            elif gated:
                 rmm.matmul(xn[i], wt, out=zs[i], stream=stream)
                 with torch.cuda.stream(stream):
                     torch.mul(torch.nn.functional.silu(zs[i][:, :F]), zs[i][:, F:], out=y)
@@ -334,7 +347,7 @@ def bench_workload(torch, rmm, inputs, w, K, W_warm, device, stream, l2, with_un
         ku = max(1, min(K, 200))
         s_unf, _, g2 = time_graph(torch, stream, step_unfused, n_copies, ku)
         res["unfused_secs_per_step"] = s_unf / ku
-        del g2, xn, zs
+        del g2, xn, zs, ts
     return res
 
 
@@ -506,6 +519,16 @@ def main():
                 shapes.append(e)
                 del r
                 torch.cuda.empty_cache()
+            # the low-rank adapter form
+            for name, lora_rank in (("decode_qkv_16x4096x6144", 16), ("prefill_qkv_4096x4096x6144", 64)):
+                ww = inputs.WORKLOADS[name]
+                est = max(ww.flops / (peaks["bf16_tflops"] * 1e12), ww.bytes_xwy / (peaks["hbm_gbs"] * 1e9))
+                k = int(min(5000, max(20, 0.2 / max(est, 1e-7))))
+                r = bench_workload(torch, rmm, inputs, ww, k, 3, device, stream, l2,
+                                   with_unfused=True, sampler=sampler, lora_r=lora_rank)
+                shapes.append(shape_entry(ww, r["secs"] / k, r, peaks, k, lora_r=lora_rank))
+                del r
+                torch.cuda.empty_cache()
     clocks = sampler.summary()
 
     K = args.steps
@@ -591,13 +614,18 @@ def gated_bytes(w):
     return 2 * (w.M * w.K + w.K * w.N + w.M * (w.N // 2))
 
 
-def shape_entry(w, t, r, peaks, k, gated=False):
+def shape_entry(w, t, r, peaks, k, gated=False, lora_r=0):
     nbytes = gated_bytes(w) if gated else w.bytes_xwy
-    tflops = w.flops / t / 1e12
+    flops = w.flops
+    if lora_r:   # + A, B, and T written and read back; + (X*g) @ A and T @ B
+        nbytes += 2 * (w.K * lora_r + lora_r * w.N + 2 * w.M * lora_r)
+        flops += 2 * w.M * lora_r * (w.K + w.N)
+    tflops = flops / t / 1e12
     gbs = nbytes / t / 1e9
-    roof_t = max(w.flops / (peaks["bf16_tflops"] * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9))
-    bound = "tensor" if w.flops / (peaks["bf16_tflops"] * 1e12) > nbytes / (peaks["hbm_gbs"] * 1e9) else "hbm"
-    e = {"workload": w.name + (" (gated: silu(gate) * up)" if gated else ""),
+    roof_t = max(flops / (peaks["bf16_tflops"] * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9))
+    bound = "tensor" if flops / (peaks["bf16_tflops"] * 1e12) > nbytes / (peaks["hbm_gbs"] * 1e9) else "hbm"
+    e = {"workload": w.name + (" (gated: silu(gate) * up)" if gated else "") +
+         (f" (low-rank adapter, R = {lora_r})" if lora_r else ""),
          "path": "small-M (cols)" if r["path"] == 2 else "row-tile",
          "plan": r.get("plan"),
          "steps": k, "us_per_call": round(t * 1e6, 3), "tflops": round(tflops, 2),
@@ -606,7 +634,7 @@ def shape_entry(w, t, r, peaks, k, gated=False):
     if bound == "tensor":
         e["frac_of_tensor_peak_sustained"] = round(tflops / peaks["bf16_tflops_sustained"], 4)
     if "unfused_secs_per_step" in r:
-        e["unfused_us" if gated else "unfused_pair_us"] = round(r["unfused_secs_per_step"] * 1e6, 3)
+        e["unfused_us" if gated or lora_r else "unfused_pair_us"] = round(r["unfused_secs_per_step"] * 1e6, 3)
     return e
 
 

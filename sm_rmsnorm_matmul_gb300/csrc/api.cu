@@ -354,14 +354,14 @@ int rows_stages(int xrows, int red_slots, int MP, const DeviceInfo& d, bool over
 }
 
 std::mutex g_rows_occ_mu;
-std::map<std::tuple<int, bool, int, size_t, bool, bool>, int> g_rows_occ;
+std::map<std::tuple<int, bool, int, size_t, bool, bool, bool>, int> g_rows_occ;
 
-int rows_max_clusters(int dev, bool fused, int splits, size_t smem, bool glu, bool wnk) {
+int rows_max_clusters(int dev, bool fused, int splits, size_t smem, bool glu, bool wnk, bool lora) {
     std::lock_guard<std::mutex> lk(g_rows_occ_mu);
-    auto key = std::make_tuple(dev, fused, splits, smem, glu, wnk);
+    auto key = std::make_tuple(dev, fused, splits, smem, glu, wnk, lora);
     auto it = g_rows_occ.find(key);
     if (it != g_rows_occ.end()) return it->second;
-    const int n = rmm::rows_max_active_clusters(fused, splits, smem, glu, wnk);
+    const int n = rmm::rows_max_active_clusters(fused, splits, smem, glu, wnk, lora);
     g_rows_occ[key] = n;
     return n;
 }
@@ -374,7 +374,7 @@ int rows_max_clusters(int dev, bool fused, int splits, size_t smem, bool glu, bo
 // drain, and the cluster reduction about 1.5 us.  glu: the gated form, whose
 // tiles cover 128 output columns (256 columns of W, N = 2F).
 RowsPlan plan_rows(int dev, bool fused, int64_t M, int64_t K, int64_t N, const DeviceInfo& d,
-                   bool glu = false, bool wnk = false) {
+                   bool glu = false, bool wnk = false, bool lora = false) {
     RowsPlan p{};
     p.m_tiles = static_cast<int>((M + rmm::kRowsBM - 1) / rmm::kRowsBM);
     p.n_tiles = glu ? static_cast<int>((N / 2 + rmm::kRowsBN / 2 - 1) / (rmm::kRowsBN / 2))
@@ -416,7 +416,7 @@ RowsPlan plan_rows(int dev, bool fused, int64_t M, int64_t K, int64_t N, const D
         if (s > 1) {
             resident = rows_max_clusters(dev, fused, s,
                                          rmm::rows_smem_bytes(p.xrows, st, red_slots, p.MP, overlay, glu),
-                                         glu, wnk) * s;
+                                         glu, wnk, lora) * s;
             if (resident <= 0) continue;
         }
         const long units = static_cast<long>(p.n_tiles) * s;
@@ -508,7 +508,7 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
         return rmm::launch_cols(fused, tmX, tmW, tmG, Y, a, stream) == cudaSuccess ? RMM_OK
                                                                                   : RMM_ERR_LAUNCH;
     }
-    const RowsPlan p = plan_rows(dev, fused, M, K, N, d, glu, wnk);
+    const RowsPlan p = plan_rows(dev, fused, M, K, N, d, glu, wnk, lora);
     if (!map_2d(&tmX, X, M, K, p.xrows)) return RMM_ERR_INTERNAL;
     if (!fused) tmG = tmX;
     rmm::RowsLaunch a{};

@@ -185,7 +185,7 @@ __host__ __device__ inline RowsLayout rows_layout(int xrows, int stages, int red
 }
 
 
-template <bool kFused, bool kSplit, bool kGlu, bool kWnk>
+template <bool kFused, bool kSplit, bool kGlu, bool kWnk, bool kLora>
 __global__ void __launch_bounds__(kThreads, 1)
     rows_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                 const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmT,
@@ -240,13 +240,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // T = bf16((X*g) @ A) (rows of tmT, R <= 64 columns, zeros past R) and
     // whose B tile is the adapter's B (rows of tmB, zeros past R); it gets
     // no gain and adds nothing to the row statistic.
-    // (compiled into the plain [K, N] form only, the one the adapter API uses)
-    constexpr bool kAdapter = kFused && !kGlu && !kWnk;
-    auto lora_extra = [&](int sp) { return kAdapter && a.lora && sp == 0 ? 1 : 0; };
+    // (its own instantiations: kLora, fused [K, N] form only; the others
+    // carry none of it)
+    static_assert(!kLora || (kFused && !kGlu && !kWnk), "the adapter stage is for the plain fused form");
+    auto lora_extra = [&](int sp) { return kLora && sp == 0 ? 1 : 0; };
     // Loads of stage s = k-block kb of the unit whose tile starts at row block
     // mb and output column n0 (kb == k_blocks: the adapter stage).
     auto issue = [&](uint32_t s, int kb, int mb, int n0) {
-        const bool ext = kb >= a.k_blocks;
+        const bool ext = kLora && kb >= a.k_blocks;
         mbar_arrive_expect_tx(full(s), xbytes + w_stage_bytes<kGlu, kWnk>(n0, a.N) +
                                            (kFused && !ext ? kGBytes : 0));
         tma_load_2d_nohint(sx + s * xbytes, ext ? &tmT : &tmX, full(s), ext ? 0 : kb * kBK, mb * kRowsBM);
@@ -395,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = kb0; kb < kend; ++kb) {
                     const uint32_t s = ring.idx, ph = ring.phase;
                     if (!warp_wait(full(s), ph, abort)) { ok = false; break; }
-                    if (kb < kb1) {   // (the adapter stage needs no transform)
+                    if (!kLora || kb < kb1) {   // (the adapter stage needs no transform)
                         const uint4 gv = lds128(sg + s * kGBytes + kc * 16);
                         const uint32_t xt = sx + s * xbytes + swz_off;
                         // rows rb + 16 i all have (row & 7) == (rb & 7)
@@ -702,7 +703,7 @@ __device__ __forceinline__ bool ta_unit(const RowsLaunch& a, int i, TaUnit& u) {
     return true;
 }
 
-template <bool kGlu, bool kWnk>
+template <bool kGlu, bool kWnk, bool kLora>
 __global__ void __launch_bounds__(kThreads, 1)
     rows_ta_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmT,
@@ -779,8 +780,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 128 output columns read from gate columns n0.. and up columns F + n0..
     const int Nout = kGlu ? a.N / 2 : a.N;
     constexpr int kOutBN = kGlu ? kRowsBN / 2 : kRowsBN;
-    // the low-rank adapter stage exists in the plain [K, N] form only
-    constexpr bool kAdapter = !kGlu && !kWnk;
+    // the low-rank adapter stage: its own instantiations (kLora), plain [K, N] form only
+    static_assert(!kLora || (!kGlu && !kWnk), "the adapter stage is for the plain form");
 
     if (warp == 0 || warp == 3) {
         // ------------------------------------------------ TMA producers
@@ -798,8 +799,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int mb, nb;
                 rows_tile_coords(un.t, a.m_tiles, a.n_tiles, mb, nb);
                 const int n0 = nb * kOutBN;
-                for (int kb = un.kb0; kb < un.kb1 + (kAdapter ? un.extra : 0); ++kb) {
-                    const bool ext = kAdapter && kb >= un.kb1;   // the adapter stage: T and B
+                for (int kb = un.kb0; kb < un.kb1 + (kLora ? un.extra : 0); ++kb) {
+                    const bool ext = kLora && kb >= un.kb1;   // the adapter stage: T and B
                     if (!mbar_wait(empty0 + 8 * ring.idx, ring.phase ^ 1, abort)) { ok = false; break; }
                     const uint32_t f = full0 + 8 * ring.idx;
                     if (load_x) {
@@ -833,7 +834,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(accempty, (tl & 1) ^ 1, abort)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + kTaAccCol;
-                for (int kb = un.kb0; kb < un.kb1 + (kAdapter ? un.extra : 0); ++kb) {
+                for (int kb = un.kb0; kb < un.kb1 + (kLora ? un.extra : 0); ++kb) {
                     if (!mbar_wait(wfull0 + 8 * wr.idx, wr.phase, abort)) { ok = false; break; }
                     if (!mbar_wait(afull0 + 8 * ar.idx, ar.phase, abort)) { ok = false; break; }
                     tc_fence_after();
@@ -871,8 +872,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             float ssp[8];   // independent partial sums: no long dependency chain
 #pragma unroll
             for (int c = 0; c < 8; ++c) ssp[c] = 0.f;
-            for (int kb = un.kb0; kb < un.kb1 + (kAdapter ? un.extra : 0); ++kb) {
-                const bool ext = kAdapter && kb >= un.kb1;   // the adapter stage: T rows, no gain, no statistic
+            for (int kb = un.kb0; kb < un.kb1 + (kLora ? un.extra : 0); ++kb) {
+                const bool ext = kLora && kb >= un.kb1;   // the adapter stage: T rows, no gain, no statistic
                 if (!warp_wait(xfull0 + 8 * xr.idx, xr.phase, abort)) { ok = false; break; }
                 const uint32_t xt = sx + xr.idx * kTaXBytes + xrow;
                 const uint32_t gt = sg + xr.idx * kGBytes;
@@ -880,22 +881,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 8; ++c) xv[c] = lds128(xt + ((c ^ swz) << 4));
                 uint32_t out[32];
+                if (!ext) {
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint32_t xs[4] = {xv[c].x, xv[c].y, xv[c].z, xv[c].w};
-                    if (ext) {
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 gv = lds128(gt + c * 16);
+                        const uint32_t xs[4] = {xv[c].x, xv[c].y, xv[c].z, xv[c].w};
+                        const uint32_t gs[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) out[c * 4 + i] = xs[i];
-                        continue;
+                        for (int i = 0; i < 4; ++i) {
+                            const float x0 = bf16lo(xs[i]), x1 = bf16hi(xs[i]);
+                            ssp[c] = fmaf(x0, x0, ssp[c]);
+                            ssp[c] = fmaf(x1, x1, ssp[c]);
+                            out[c * 4 + i] = mul_bf16x2(xs[i], gs[i]);
+                        }
                     }
-                    const uint4 gv = lds128(gt + c * 16);
-                    const uint32_t gs[4] = {gv.x, gv.y, gv.z, gv.w};
+                } else {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float x0 = bf16lo(xs[i]), x1 = bf16hi(xs[i]);
-                        ssp[c] = fmaf(x0, x0, ssp[c]);
-                        ssp[c] = fmaf(x1, x1, ssp[c]);
-                        out[c * 4 + i] = mul_bf16x2(xs[i], gs[i]);
+                    for (int c = 0; c < 8; ++c) {
+                        out[c * 4 + 0] = xv[c].x;
+                        out[c * 4 + 1] = xv[c].y;
+                        out[c * 4 + 2] = xv[c].z;
+                        out[c * 4 + 3] = xv[c].w;
                     }
                 }
                 // the X slot has been read (values are in registers)
@@ -1576,7 +1582,7 @@ __global__ void __launch_bounds__(kNormThreads)
 // Raises a kernel's dynamic shared-memory limit to the device's opt-in
 // maximum, once per (kernel slot, device).
 cudaError_t ensure_smem_attr(const void* func, int slot) {
-    static int done[16][64] = {};
+    static int done[24][64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -1637,29 +1643,35 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
                         const RowsLaunch& a, cudaStream_t s) {
     auto* y = static_cast<__nv_bfloat16*>(Y);
     const bool split = a.cluster != 0;
-    const bool glu = a.glu != 0, wnk = a.w_nk != 0;
-    if ((glu || wnk) && !fused) return cudaErrorInvalidValue;
+    const bool glu = a.glu != 0, wnk = a.w_nk != 0, lora = a.lora != 0;
+    if ((glu || wnk || lora) && !fused) return cudaErrorInvalidValue;
+    if (lora && (glu || wnk)) return cudaErrorInvalidValue;
     if (fused && !split && a.xrows == kRowsBM) {
-        auto ta = wnk ? (glu ? rows_ta_kernel<true, true> : rows_ta_kernel<false, true>)
-                      : (glu ? rows_ta_kernel<true, false> : rows_ta_kernel<false, false>);
-        cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(ta), wnk ? (glu ? 15 : 14) : (glu ? 9 : 6));
+        auto ta = lora ? rows_ta_kernel<false, false, true>
+                : wnk  ? (glu ? rows_ta_kernel<true, true, false> : rows_ta_kernel<false, true, false>)
+                       : (glu ? rows_ta_kernel<true, false, false> : rows_ta_kernel<false, false, false>);
+        cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(ta),
+                                         lora ? 18 : wnk ? (glu ? 15 : 14) : (glu ? 9 : 6));
         if (e != cudaSuccess) return e;
         e = launch_ex(ta, a.grid, kTaSmem, 1, s, tmX, tmW, tmG, tmT, tmB, *a.tmY, y, a);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
-    decltype(&rows_kernel<true, true, true, true>) kern;
+    decltype(&rows_kernel<true, true, true, true, false>) kern;
     int slot;
-    if (wnk) {
-        kern = glu ? (split ? rows_kernel<true, true, true, true> : rows_kernel<true, false, true, true>)
-                   : (split ? rows_kernel<true, true, false, true> : rows_kernel<true, false, false, true>);
+    if (lora) {
+        kern = split ? rows_kernel<true, true, false, false, true> : rows_kernel<true, false, false, false, true>;
+        slot = split ? 17 : 16;
+    } else if (wnk) {
+        kern = glu ? (split ? rows_kernel<true, true, true, true, false> : rows_kernel<true, false, true, true, false>)
+                   : (split ? rows_kernel<true, true, false, true, false> : rows_kernel<true, false, false, true, false>);
         slot = 10 + (glu ? 2 : 0) + (split ? 1 : 0);
     } else if (glu) {
-        kern = split ? rows_kernel<true, true, true, false> : rows_kernel<true, false, true, false>;
+        kern = split ? rows_kernel<true, true, true, false, false> : rows_kernel<true, false, true, false, false>;
         slot = split ? 8 : 7;
     } else {
-        kern = fused ? (split ? rows_kernel<true, true, false, false> : rows_kernel<true, false, false, false>)
-                     : (split ? rows_kernel<false, true, false, false> : rows_kernel<false, false, false, false>);
+        kern = fused ? (split ? rows_kernel<true, true, false, false, false> : rows_kernel<true, false, false, false, false>)
+                     : (split ? rows_kernel<false, true, false, false, false> : rows_kernel<false, false, false, false, false>);
         slot = (fused ? 0 : 1) + (split ? 4 : 0);
     }
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), slot);
@@ -1706,13 +1718,14 @@ int cols_max_active_clusters(bool fused, int splits, size_t smem) {
                  : max_active_clusters(cols_kernel<false>, 3, splits, smem);
 }
 
-int rows_max_active_clusters(bool fused, int splits, size_t smem, bool glu, bool wnk) {
+int rows_max_active_clusters(bool fused, int splits, size_t smem, bool glu, bool wnk, bool lora) {
+    if (lora) return max_active_clusters(rows_kernel<true, true, false, false, true>, 17, splits, smem);
     if (wnk)
-        return glu ? max_active_clusters(rows_kernel<true, true, true, true>, 13, splits, smem)
-                   : max_active_clusters(rows_kernel<true, true, false, true>, 11, splits, smem);
-    if (glu) return max_active_clusters(rows_kernel<true, true, true, false>, 8, splits, smem);
-    return fused ? max_active_clusters(rows_kernel<true, true, false, false>, 4, splits, smem)
-                 : max_active_clusters(rows_kernel<false, true, false, false>, 5, splits, smem);
+        return glu ? max_active_clusters(rows_kernel<true, true, true, true, false>, 13, splits, smem)
+                   : max_active_clusters(rows_kernel<true, true, false, true, false>, 11, splits, smem);
+    if (glu) return max_active_clusters(rows_kernel<true, true, true, false, false>, 8, splits, smem);
+    return fused ? max_active_clusters(rows_kernel<true, true, false, false, false>, 4, splits, smem)
+                 : max_active_clusters(rows_kernel<false, true, false, false, false>, 5, splits, smem);
 }
 
 cudaError_t launch_rmsnorm(const void* X, const void* g, void* Xn, int M, int K, float eps,

@@ -34,7 +34,8 @@ size_t rows_smem_bytes(int xrows, int stages, int red_slots, int MP, bool overla
 // The receive blocks of a K split over `splits` CTAs fit the pipeline buffers.
 bool rows_overlay_fits(int xrows, int stages, int splits, int MP, bool glu = false);
 size_t rows_stage_bytes(int xrows);
-int rows_max_active_clusters(bool fused, int splits, size_t smem, bool glu = false, bool wnk = false);
+int rows_max_active_clusters(bool fused, int splits, size_t smem, bool glu = false, bool wnk = false,
+                             bool lora = false);
 // red_slots = splits - 1 when the splits reduce through a cluster, else 0.
 size_t cols_smem_bytes(int MP, int stages, int red_slots);
 size_t cols_fixed_smem_bytes(int MP, int red_slots);
