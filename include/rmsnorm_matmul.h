@@ -182,12 +182,15 @@ int rmm_device_status(cudaStream_t stream);
 /*
  * Test hook, not for production use (the timeout path, exercised without any
  * fault).  wait_limit_ns > 0 sets the limit of every bounded in-kernel wait
- * (default 2 s; 0 restores it).  skip_sends != 0 makes the row-tile kernels'
- * K-split reduction skip the stores of its partials, so that each owning CTA's
- * wait for them runs out: the kernel then records RMM_ERR_DEVICE_TIMEOUT,
- * skips its remaining work, frees its tensor memory and exits normally, and
- * rmm_device_status() reports it.  Applies to the current device; synchronous.
- * Returns RMM_ERR_INVALID_ARG for a negative limit.
+ * (microsecond resolution, at most the 2 s default; 0 restores the default).
+ * skip_sends != 0 makes the row-tile kernels' K-split reduction skip the
+ * stores of its partials, so that each owning CTA's wait for them runs out:
+ * the kernel then records RMM_ERR_DEVICE_TIMEOUT, skips its remaining work,
+ * frees its tensor memory and exits normally, and rmm_device_status() reports
+ * it.  Both settings are process-wide host state, passed to every later
+ * launch as kernel parameters (no device memory is written; launches already
+ * enqueued keep their values).  Returns RMM_ERR_INVALID_ARG for a negative
+ * limit.
  */
 int rmm_test_hooks(int skip_sends, int64_t wait_limit_ns);
 

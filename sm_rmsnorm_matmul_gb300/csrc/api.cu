@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -22,6 +23,11 @@ namespace {
 using rmm::kBK;
 
 std::atomic<int> g_force_path{0};
+// Test hooks (rmm_test_hooks): the limit of one bounded in-kernel wait and
+// whether the K-split reduction skips its stores; passed in every launch.
+constexpr int64_t kDefaultWaitUs = 2000000;
+std::atomic<int> g_wait_limit_us{static_cast<int>(kDefaultWaitUs)};
+std::atomic<int> g_skip_sends{0};
 
 constexpr int kPathRows = 1;
 constexpr int kPathCols = 2;
@@ -493,6 +499,7 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
         a.kb_per_split = p.kb_per_split;
         a.stages = p.stages;
         a.grid = p.grid;
+        a.wait_limit_us = g_wait_limit_us.load();
         a.cluster = p.cluster;
         a.tmem_cols = p.tmem_cols;
         if (p.splits > 1 && !p.cluster) {
@@ -531,6 +538,8 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
     a.w_nk = wnk ? 1 : 0;
     a.unscaled = unscaled ? 1 : 0;
     a.lora = lora ? 1 : 0;
+    a.wait_limit_us = g_wait_limit_us.load();
+    a.test_skip_sends = g_skip_sends.load();
     CUtensorMap tmT = tmX, tmB = tmW;   // unused without the adapter
     if (lora) {
         if (!map_2d(&tmT, lora_t, M, R, p.xrows) || !map_2d(&tmB, lora_b, R, N, kBK)) return RMM_ERR_INTERNAL;
@@ -716,13 +725,10 @@ int rmm_device_status(cudaStream_t stream) {
 
 int rmm_test_hooks(int skip_sends, int64_t wait_limit_ns) {
     if (wait_limit_ns < 0) return RMM_ERR_INVALID_ARG;
-    int dev = 0;
-    DeviceInfo d;
-    int rc = current_device(&dev, &d);
-    if (rc != RMM_OK) return rc;
-    const unsigned long long limit = wait_limit_ns > 0 ? static_cast<unsigned long long>(wait_limit_ns)
-                                                       : 2000000000ull;
-    return rmm::set_test_hooks(skip_sends != 0, limit) == cudaSuccess ? RMM_OK : RMM_ERR_LAUNCH;
+    const int64_t us = wait_limit_ns > 0 ? std::max<int64_t>(1, wait_limit_ns / 1000) : kDefaultWaitUs;
+    g_wait_limit_us.store(static_cast<int>(std::min<int64_t>(us, kDefaultWaitUs)));
+    g_skip_sends.store(skip_sends != 0 ? 1 : 0);
+    return RMM_OK;
 }
 
 const char* rmm_status_string(int code) {
@@ -836,6 +842,7 @@ extern "C" int rmsnorm_matmul_noalloc(const void* X, const void* g, const void* 
     a.stages = p.stages;
     a.grid = p.grid;
     a.tmem_cols = p.tmem_cols;
+    a.wait_limit_us = g_wait_limit_us.load();
     a.ws_acc = acc;
     a.ws_ss = ss;
     a.counters = counters;

@@ -273,7 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(mmadone, 1);
         mbar_init(redfull, 1);   // own expect_tx (+ the peers' bytes)
         mbar_init(redgo, split > 1 ? split - 1 : 1);   // one remote arrive per other split
-        *abort = 0;
+        abort[0] = 0;
+        abort[1] = a.wait_limit_us;
         fence_mbar_init();
         prefetch_tmap(&tmX);
         prefetch_tmap(&tmW);
@@ -518,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t my_block = red_addr + rank * blk;   // this split's block in every CTA
         const int q = warp & 3, team = warp >> 2;
         const int row = q * 32 + lane;
-        const bool send = g_test_skip_sends == 0;
+        const bool send = a.test_skip_sends == 0;
         if (have && threadIdx.x == 0)
             mbar_arrive_expect_tx(redfull,
                                   static_cast<uint32_t>((split - 1) * rows_here * (4 + owned * kUnitChunks * 128)));
@@ -754,7 +755,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(mmadone, 1);
         mbar_init(episync, 4);
-        *abort = 0;
+        abort[0] = 0;
+        abort[1] = a.wait_limit_us;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -1195,7 +1197,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(episync, 4);
         mbar_init(redfull, a.splits > 1 ? (a.splits - 1) * 128 : 1);
         mbar_init(redempty, 1);
-        *abort = 0;
+        abort[0] = 0;
+        abort[1] = a.wait_limit_us;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -1734,14 +1737,6 @@ cudaError_t launch_rmsnorm(const void* X, const void* g, void* Xn, int M, int K,
                                              static_cast<const __nv_bfloat16*>(g),
                                              static_cast<__nv_bfloat16*>(Xn), K, eps);
     return cudaGetLastError();
-}
-
-cudaError_t set_test_hooks(int skip_sends, unsigned long long wait_limit_ns) {
-    cudaError_t e = cudaMemcpyToSymbol(g_test_skip_sends, &skip_sends, sizeof(int));
-    if (e != cudaSuccess) return e;
-    e = cudaMemcpyToSymbol(g_wait_limit_ns, &wait_limit_ns, sizeof(wait_limit_ns));
-    if (e != cudaSuccess) return e;
-    return cudaDeviceSynchronize();
 }
 
 cudaError_t read_and_clear_status(int* out) {

@@ -56,6 +56,8 @@ struct RowsLaunch {
     int w_nk;                  // 1: W stored [N, K] (K contiguous), read K-major
     int unscaled;              // 1: no division by the row RMS (Y = (X*g) @ W)
     int lora;                  // 1: one more stage per tile from the adapter's T and B
+    int wait_limit_us;         // limit of one bounded in-kernel wait
+    int test_skip_sends;       // test hook: the K-split reduction skips its stores
     int cluster;               // 1: the splits of a tile form a cluster
     int xrows, MP, stages;
     int grid;
@@ -81,6 +83,7 @@ struct ColsLaunch {
     float* ws_acc;    // [splits][M][N] fp32 partials (splits > 1 without a cluster)
     float* ws_ss;     // [n_tiles][splits][128] fp32 partial sums of squares
     int* counters;    // [n_tiles][4] arrival counters (one per epilogue warp), zero between launches
+    int wait_limit_us;   // limit of one bounded in-kernel wait
 };
 
 // tmT, tmB: the low-rank adapter's T [M, R] and B [R, N] (used with a.lora).
@@ -94,8 +97,6 @@ cudaError_t launch_rmsnorm(const void* X, const void* g, void* Xn, int M, int K,
 
 // Copies the in-kernel status word to *out and clears it (synchronous).
 cudaError_t read_and_clear_status(int* out);
-// Test hooks of the current device (synchronous): skip the K-split sends,
-// and the limit of every bounded in-kernel wait.
-cudaError_t set_test_hooks(int skip_sends, unsigned long long wait_limit_ns);
+
 
 }  // namespace rmm

@@ -16,14 +16,14 @@ __device__ int g_status = 0;
 
 constexpr int kStatusTimeout = 5;                     // RMM_ERR_DEVICE_TIMEOUT
 constexpr int kStatusInternal = 6;                    // RMM_ERR_INTERNAL (launch not as planned)
-constexpr uint64_t kWaitLimitNs = 2000000000ull;      // 2 s per wait (default)
+constexpr int kWaitLimitUs = 2000000;                 // 2 s per wait (default)
 constexpr uint64_t kTeardownLimitNs = 200000000ull;   // 0.2 s per teardown wait
-// Limit of one bounded wait, kWaitLimitNs unless a test shortens it.
-__device__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
-// Test hook, 0 in normal use: nonzero makes the row-tile K-split reduction
-// skip the stores of its partials, so that the owners' waits run out and the
-// timeout path runs without any fault.
-__device__ int g_test_skip_sends = 0;
+// Every kernel keeps its abort flag at abort[0] and the limit of one bounded
+// wait, in microseconds, at abort[1] (shared memory, set at start-up from the
+// launch parameters: kWaitLimitUs unless a test shortens it).
+__device__ __forceinline__ uint64_t wait_limit_ns(volatile int* abort) {
+    return static_cast<uint64_t>(abort[1]) * 1000ull;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -62,7 +62,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase of parity `parity` to complete.  Gives up (returns
-// false) when another role has set *abort, or after g_wait_limit_ns, in which
+// false) when another role has set *abort, or after the wait limit, in which
 // case it records the timeout in g_status and sets *abort so that every role
 // of the CTA leaves its loop.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
@@ -73,7 +73,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         for (int i = 0; i < 16; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (globaltimer() - t0 > g_wait_limit_ns) {
+        if (globaltimer() - t0 > wait_limit_ns(abort)) {
             atomicCAS(&g_status, 0, kStatusTimeout);
             *abort = 1;
             return false;
@@ -111,7 +111,7 @@ __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity,
         for (;;) {
             if (mbar_try_wait_cluster(bar, parity)) { ok = true; break; }
             if (*abort) break;
-            if (globaltimer() - t0 > g_wait_limit_ns) {
+            if (globaltimer() - t0 > wait_limit_ns(abort)) {
                 atomicCAS(&g_status, 0, kStatusTimeout);
                 *abort = 1;
                 break;
@@ -136,7 +136,7 @@ __device__ __forceinline__ bool spin_until_ge(const int* p, int target, volatile
         __nanosleep(64);
         if (ld_acquire_gpu(p) >= target) return true;
         if (*abort) return false;
-        if (globaltimer() - t0 > g_wait_limit_ns) {
+        if (globaltimer() - t0 > wait_limit_ns(abort)) {
             atomicCAS(&g_status, 0, kStatusTimeout);
             *abort = 1;
             return false;
