@@ -61,9 +61,14 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_rmsnorm_matmul_rewritten.argtypes = [dp, dp, dp, dp, L, L, L, D, I]
     lib.oracle_rmsnorm_matmul_swiglu.argtypes = [dp, dp, dp, dp, L, L, L, D, I]
     lib.oracle_rmsnorm_matmul_lora.argtypes = [dp, dp, dp, dp, dp, dp, L, L, L, L, D, I]
+    lp = ctypes.POINTER(ctypes.c_long)
+    lib.oracle_attention.argtypes = [dp, dp, dp, dp, L, L, L, L, L, D, I, lp, L, I]
+    lib.oracle_qknorm_attention.argtypes = [dp, dp, dp, dp, dp, dp, L, L, L, L, L, D, D, I,
+                                            lp, L, I]
     for f in (lib.oracle_rmsnorm, lib.oracle_matmul, lib.oracle_rmsnorm_matmul,
               lib.oracle_rmsnorm_matmul_rewritten, lib.oracle_rmsnorm_matmul_swiglu,
-              lib.oracle_rmsnorm_matmul_lora, lib.oracle_max_threads):
+              lib.oracle_rmsnorm_matmul_lora, lib.oracle_attention, lib.oracle_qknorm_attention,
+              lib.oracle_max_threads):
         f.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     return lib
@@ -185,6 +190,59 @@ def matmul(A, B, nthreads: int = 0, lib=None) -> np.ndarray:
     C = np.empty((M, N), dtype=np.float64)
     _check(lib.oracle_matmul(_ptr(A), _ptr(B), _ptr(C), M, K, N, nthreads), "matmul")
     return C
+
+
+def _heads(t, name):
+    a = to_f64(t)
+    if a.ndim != 4:
+        raise ValueError(f"{name} must be [B, S, heads, D]")
+    return np.ascontiguousarray(a)
+
+
+def _positions(qpos, S):
+    if qpos is None:
+        return None, S
+    q = np.ascontiguousarray(np.asarray(qpos, dtype=np.int64)).astype(ctypes.c_long)
+    return q, len(q)
+
+
+def attention(Q, K, V, scale: float, causal: bool = True, qpos=None, nthreads: int = 0,
+              lib=None) -> np.ndarray:
+    """Scaled dot-product attention in fp64.  Q [B,S,Hq,D], K and V [B,S,Hkv,D];
+    returns O [B, len(qpos) or S, Hq, D] for the query positions qpos."""
+    lib = lib or load()
+    Q, K, V = _heads(Q, "Q"), _heads(K, "K"), _heads(V, "V")
+    B, S, Hq, D = Q.shape
+    Hkv = K.shape[2]
+    assert K.shape == (B, S, Hkv, D) and V.shape == K.shape
+    q, nq = _positions(qpos, S)
+    O = np.empty((B, nq, Hq, D), dtype=np.float64)
+    qp = q.ctypes.data_as(ctypes.POINTER(ctypes.c_long)) if q is not None else None
+    _check(lib.oracle_attention(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), B, S, Hq, Hkv, D,
+                                float(scale), int(bool(causal)), qp, nq, nthreads), "attention")
+    return O
+
+
+def qknorm_attention(Q, K, V, gq, gk, eps: float, scale: float | None = None,
+                     causal: bool = True, qpos=None, nthreads: int = 0, lib=None) -> np.ndarray:
+    """RMSNorm(Q; gq) and RMSNorm(K; gk) over the head dimension, then
+    attention with scale 1/sqrt(D) unless given; fp64."""
+    lib = lib or load()
+    Q, K, V = _heads(Q, "Q"), _heads(K, "K"), _heads(V, "V")
+    gq, gk = to_f64(gq), to_f64(gk)
+    B, S, Hq, D = Q.shape
+    Hkv = K.shape[2]
+    assert K.shape == (B, S, Hkv, D) and V.shape == K.shape
+    assert gq.shape == (D,) and gk.shape == (D,)
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    q, nq = _positions(qpos, S)
+    O = np.empty((B, nq, Hq, D), dtype=np.float64)
+    qp = q.ctypes.data_as(ctypes.POINTER(ctypes.c_long)) if q is not None else None
+    _check(lib.oracle_qknorm_attention(_ptr(Q), _ptr(K), _ptr(V), _ptr(gq), _ptr(gk), _ptr(O),
+                                       B, S, Hq, Hkv, D, float(eps), float(scale),
+                                       int(bool(causal)), qp, nq, nthreads), "qknorm_attention")
+    return O
 
 
 def max_threads(lib=None) -> int:

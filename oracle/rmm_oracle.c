@@ -47,8 +47,23 @@
  *   Weff[k,n] = W[k,n] + sum_j A[k,j] * B[j,n]
  *   Y[m,n]    = RMSNorm(X)[m,:] . Weff[:,n]
  *
+ * oracle_attention() and oracle_qknorm_attention() are the QKNorm + Attention
+ * workload (another row of the review page's section 5 benchmark table; the
+ * pages give only its name).  Read as the query/key normalisation of recent
+ * decoder models: RMSNorm with a gain over the head dimension D, applied to
+ * every query head and every key head, then scaled dot-product attention,
+ * causal or not, with grouped key/value heads (query head h reads key/value
+ * head h / (Hq / Hkv)):
+ *
+ *   Qn[b,i,h,:] = RMSNorm(Q[b,i,h,:]; gq, eps)            (over d < D)
+ *   Kn[b,j,c,:] = RMSNorm(K[b,j,c,:]; gk, eps)
+ *   s_j         = scale * sum_d Qn[b,i,h,d] * Kn[b,j,c,d]  (c = h / (Hq/Hkv);
+ *                                                          j < S, j <= i if causal)
+ *   O[b,i,h,:]  = sum_j softmax(s)_j * V[b,j,c,:]
+ *
  * Everything is double precision; nothing is rounded to bf16.  Row-major
- * layouts: X [M,K], g [K], W [K,N], Y [M,N] (Y [M,F] for the gated form).
+ * layouts: X [M,K], g [K], W [K,N], Y [M,N] (Y [M,F] for the gated form);
+ * Q and O [B,S,Hq,D], K and V [B,S,Hkv,D].
  */
 #include <math.h>
 #include <stdlib.h>
@@ -237,6 +252,94 @@ int oracle_rmsnorm_matmul_lora(const double *X, const double *g, const double *W
     }
     int rc = oracle_rmsnorm_matmul(X, g, Weff, Y, M, K, N, eps, nthreads);
     free(Weff);
+    return rc;
+}
+
+/* Attention for the query positions qpos[0..nq) of every sequence (all S
+ * positions, in order, when qpos is NULL; nq must then be S).  O is
+ * [B, nq, Hq, D].  The softmax subtracts the row maximum before exp, which
+ * changes nothing in exact arithmetic and keeps exp in range. */
+int oracle_attention(const double *Q, const double *K, const double *V, double *O,
+                     long B, long S, long Hq, long Hkv, long D, double scale, int causal,
+                     const long *qpos, long nq, int nthreads)
+{
+    if (B < 0 || S < 0 || Hq < 1 || Hkv < 1 || D < 1 || Hq % Hkv != 0)
+        return ORACLE_ERR_ARG;
+    if (!qpos && nq != S)
+        return ORACLE_ERR_ARG;
+    for (long t = 0; qpos && t < nq; ++t)
+        if (qpos[t] < 0 || qpos[t] >= S)
+            return ORACLE_ERR_ARG;
+    const long group = Hq / Hkv;
+    int nt = resolve_threads(nthreads);
+    (void)nt;
+    int rc = ORACLE_OK;
+#pragma omp parallel for num_threads(nt) schedule(dynamic, 4)
+    for (long row = 0; row < B * nq * Hq; ++row) {
+        const long b = row / (nq * Hq);
+        const long t = (row / Hq) % nq;
+        const long h = row % Hq;
+        const long c = h / group;                 /* key/value head of query head h */
+        const long i = qpos ? qpos[t] : t;        /* query position */
+        const long nkeys = causal ? i + 1 : S;    /* keys j < nkeys take part */
+        const double *q = Q + ((b * S + i) * Hq + h) * D;
+        double *o = O + ((b * nq + t) * Hq + h) * D;
+        double *sc = (double *)malloc((size_t)(nkeys > 0 ? nkeys : 1) * sizeof(double));
+        if (!sc) {
+#pragma omp atomic write
+            rc = ORACLE_ERR_ALLOC;
+            continue;
+        }
+        double smax = -INFINITY;
+        for (long j = 0; j < nkeys; ++j) {
+            const double *k = K + ((b * S + j) * Hkv + c) * D;
+            double dot = 0.0;
+            for (long d = 0; d < D; ++d)
+                dot += q[d] * k[d];
+            sc[j] = scale * dot;
+            if (sc[j] > smax)
+                smax = sc[j];
+        }
+        double denom = 0.0;
+        for (long j = 0; j < nkeys; ++j) {
+            sc[j] = exp(sc[j] - smax);
+            denom += sc[j];
+        }
+        for (long d = 0; d < D; ++d)
+            o[d] = 0.0;
+        for (long j = 0; j < nkeys; ++j) {
+            const double *v = V + ((b * S + j) * Hkv + c) * D;
+            const double pj = sc[j] / denom;
+            for (long d = 0; d < D; ++d)
+                o[d] += pj * v[d];
+        }
+        free(sc);
+    }
+    return rc;
+}
+
+/* QK-normalised attention: the RMSNorm above over every query and key head
+ * (rows of length D), then oracle_attention().  scale is taken as given
+ * (callers pass 1/sqrt(D) for the usual scaled dot product). */
+int oracle_qknorm_attention(const double *Q, const double *K, const double *V,
+                            const double *gq, const double *gk, double *O, long B, long S,
+                            long Hq, long Hkv, long D, double eps, double scale, int causal,
+                            const long *qpos, long nq, int nthreads)
+{
+    if (B < 0 || S < 0 || Hq < 1 || Hkv < 1 || D < 1)
+        return ORACLE_ERR_ARG;
+    const size_t nqe = (size_t)(B * S * Hq * D), nke = (size_t)(B * S * Hkv * D);
+    double *Qn = (double *)malloc((nqe > 0 ? nqe : 1) * sizeof(double));
+    double *Kn = (double *)malloc((nke > 0 ? nke : 1) * sizeof(double));
+    int rc = (Qn && Kn) ? ORACLE_OK : ORACLE_ERR_ALLOC;
+    if (rc == ORACLE_OK)
+        rc = oracle_rmsnorm(Q, gq, Qn, B * S * Hq, D, eps, nthreads);
+    if (rc == ORACLE_OK)
+        rc = oracle_rmsnorm(K, gk, Kn, B * S * Hkv, D, eps, nthreads);
+    if (rc == ORACLE_OK)
+        rc = oracle_attention(Qn, Kn, V, O, B, S, Hq, Hkv, D, scale, causal, qpos, nq, nthreads);
+    free(Qn);
+    free(Kn);
     return rc;
 }
 

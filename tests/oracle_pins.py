@@ -332,6 +332,127 @@ def pin_lora_rank_one(lib, seed=33):
     return (err <= 1e-13, f"rank one: normwise rel diff {err:.3e}")
 
 
+# ---------------------------------------------------------------------------
+# A: QKNorm + Attention (review page, section 5, benchmark table; read as
+# per-head RMSNorm with gains on queries and keys, then softmax attention with
+# grouped key/value heads).  Pinned by
+#   A1 torch's rms_norm and scaled_dot_product_attention (library routines,
+#      float64 on the CPU), causal and not, grouped heads expanded with
+#      repeat_interleave, a small and a large eps;
+#   A2 the first query of a causal row sees one key: O = V[0] of its group, bitwise;
+#   A3 equal keys give uniform weights: O[i] = mean of V over the visible keys;
+#   A4 with eps = 0, scaling query rows by 2^3 and key rows by 2^-5 changes
+#      nothing (bitwise: the normalisation removes any row scale);
+#   A5 values constant along the sequence come back unchanged (weights sum to 1);
+#   A6 grouped heads equal full multi-head attention with repeated key/value heads;
+#   A7 a 2-token, D = 2 case worked out by hand.
+# ---------------------------------------------------------------------------
+def _attn_problem(rng, B=2, S=23, Hq=4, Hkv=2, D=8):
+    Q = rng.standard_normal((B, S, Hq, D)) * rng.uniform(0.1, 10, (B, S, Hq, 1))
+    K = rng.standard_normal((B, S, Hkv, D)) * rng.uniform(0.1, 10, (B, S, Hkv, 1))
+    V = rng.standard_normal((B, S, Hkv, D))
+    gq = rng.uniform(0.5, 1.5, D)
+    gk = rng.uniform(0.5, 1.5, D)
+    return Q, K, V, gq, gk
+
+
+def pin_attn_library(lib, seed=41):
+    import torch
+    F = torch.nn.functional
+    Q, K, V, gq, gk = _attn_problem(_rng(seed))
+    B, S, Hq, D = Q.shape
+    rep = Hq // K.shape[2]
+    worst = 0.0
+    for causal in (True, False):
+        for eps in (1e-6, 0.5):
+            o = oracle.qknorm_attention(Q, K, V, gq, gk, eps, causal=causal, lib=lib)
+            qn = F.rms_norm(torch.tensor(Q), (D,), torch.tensor(gq), eps)
+            kn = F.rms_norm(torch.tensor(K), (D,), torch.tensor(gk), eps)
+            kr = kn.repeat_interleave(rep, dim=2)
+            vr = torch.tensor(V).repeat_interleave(rep, dim=2)
+            ref = F.scaled_dot_product_attention(qn.transpose(1, 2), kr.transpose(1, 2),
+                                                 vr.transpose(1, 2), is_causal=causal)
+            ref = ref.transpose(1, 2).numpy()
+            worst = max(worst, float(np.abs(o - ref).max()))
+    return (worst <= 1e-12, f"vs torch rms_norm + sdpa: max abs diff {worst:.3e}")
+
+
+def pin_attn_single_key(lib, seed=42):
+    Q, K, V, gq, gk = _attn_problem(_rng(seed))
+    B, S, Hq, D = Q.shape
+    rep = Hq // K.shape[2]
+    o = oracle.qknorm_attention(Q, K, V, gq, gk, 1e-6, causal=True, qpos=[0], lib=lib)
+    ref = np.repeat(V[:, 0:1], rep, axis=2)
+    return (bool(np.array_equal(o, ref)), "first causal query = V[0] of its group")
+
+
+def pin_attn_equal_keys(lib, seed=43):
+    Q, K, V, gq, gk = _attn_problem(_rng(seed))
+    B, S, Hq, D = Q.shape
+    rep = Hq // K.shape[2]
+    K = np.repeat(K[:, :1], S, axis=1)   # every key equal to the first
+    o = oracle.qknorm_attention(Q, K, V, gq, gk, 1e-6, causal=True, lib=lib)
+    prefix_mean = np.cumsum(V, axis=1) / np.arange(1, S + 1)[None, :, None, None]
+    ref = np.repeat(prefix_mean, rep, axis=2)
+    err = float(np.abs(o - ref).max())
+    o2 = oracle.qknorm_attention(Q, K, V, gq, gk, 1e-6, causal=False, lib=lib)
+    ref2 = np.repeat(np.repeat(V.mean(axis=1, keepdims=True), S, axis=1), rep, axis=2)
+    err = max(err, float(np.abs(o2 - ref2).max()))
+    return (err <= 1e-13, f"equal keys: max abs diff from the mean {err:.3e}")
+
+
+def pin_attn_scale_invariance(lib, seed=44):
+    Q, K, V, gq, gk = _attn_problem(_rng(seed))
+    a = oracle.qknorm_attention(Q, K, V, gq, gk, 0.0, causal=True, lib=lib)
+    b = oracle.qknorm_attention(Q * 8.0, K / 32.0, V, gq, gk, 0.0, causal=True, lib=lib)
+    return (bool(np.array_equal(a, b)), "row scale removed by the normalisation (bitwise)")
+
+
+def pin_attn_constant_values(lib, seed=45):
+    rng = _rng(seed)
+    Q, K, V, gq, gk = _attn_problem(rng)
+    c = rng.standard_normal((V.shape[0], 1, V.shape[2], V.shape[3]))
+    V = np.repeat(c, V.shape[1], axis=1)
+    rep = Q.shape[2] // K.shape[2]
+    worst = 0.0
+    for causal in (True, False):
+        o = oracle.qknorm_attention(Q, K, V, gq, gk, 1e-6, causal=causal, lib=lib)
+        ref = np.repeat(V, rep, axis=2)
+        worst = max(worst, float(np.abs(o - ref).max()))
+    return (worst <= 1e-14, f"constant values: max abs diff {worst:.3e}")
+
+
+def pin_attn_gqa_is_repeated_mha(lib, seed=46):
+    Q, K, V, gq, gk = _attn_problem(_rng(seed))
+    rep = Q.shape[2] // K.shape[2]
+    g = oracle.qknorm_attention(Q, K, V, gq, gk, 1e-6, causal=True, lib=lib)
+    m = oracle.qknorm_attention(Q, np.repeat(K, rep, axis=2), np.repeat(V, rep, axis=2), gq, gk,
+                                1e-6, causal=True, lib=lib)
+    return (bool(np.array_equal(g, m)), "grouped heads = repeated key/value heads (bitwise)")
+
+
+def pin_attn_hand_worked(lib):
+    # D = 2, unit gains, eps = 0, scale 1/sqrt(2).  Queries (1, -1) and (3, 3)
+    # normalise to (1, -1) and (1, 1); keys (2, 2) and (1, -1) to (1, 1) and
+    # (1, -1).  Scores: position 0 against keys 0, 1: 0 and sqrt(2); position 1:
+    # sqrt(2) and 0.  With V = (1, 0), (0, 4) and e = exp(sqrt(2)):
+    #   causal:     O0 = (1, 0),                O1 = (e, 4) / (e + 1)
+    #   not causal: O0 = (1, 4e) / (1 + e),     O1 = (e, 4) / (e + 1)
+    Q = np.array([[1.0, -1.0], [3.0, 3.0]]).reshape(1, 2, 1, 2)
+    K = np.array([[2.0, 2.0], [1.0, -1.0]]).reshape(1, 2, 1, 2)
+    V = np.array([[1.0, 0.0], [0.0, 4.0]]).reshape(1, 2, 1, 2)
+    one = np.ones(2)
+    e = math.exp(math.sqrt(2.0))
+    o1 = np.array([e / (e + 1.0), 4.0 / (e + 1.0)])
+    want = {True: np.array([[1.0, 0.0], o1]),
+            False: np.array([[1.0 / (1.0 + e), 4.0 * e / (1.0 + e)], o1])}
+    worst = 0.0
+    for causal in (True, False):
+        o = oracle.qknorm_attention(Q, K, V, one, one, 0.0, causal=causal, lib=lib)
+        worst = max(worst, float(np.abs(o.reshape(2, 2) - want[causal]).max()))
+    return (worst <= 1e-15, f"hand-worked case: max abs diff {worst:.3e}")
+
+
 ALL_PINS = {
     "rewrite_agrees": pin_rewrite_agrees,
     "scale_invariance": pin_scale_invariance,
@@ -347,4 +468,11 @@ ALL_PINS = {
     "lora_zero_adapter": pin_lora_zero_adapter,
     "lora_adapter_alone": pin_lora_adapter_alone,
     "lora_rank_one": pin_lora_rank_one,
+    "attn_library": pin_attn_library,
+    "attn_single_key": pin_attn_single_key,
+    "attn_equal_keys": pin_attn_equal_keys,
+    "attn_scale_invariance": pin_attn_scale_invariance,
+    "attn_constant_values": pin_attn_constant_values,
+    "attn_gqa_is_repeated_mha": pin_attn_gqa_is_repeated_mha,
+    "attn_hand_worked": pin_attn_hand_worked,
 }

@@ -111,6 +111,19 @@ MUTANTS = [
      "const double akj = A[(j * K + k) % (K * R)];"),
     ("last adapter rank dropped", "for (long j = 0; j < R; ++j) {\n            const double akj",
      "for (long j = 0; j < R - 1; ++j) {\n            const double akj"),
+    # QKNorm + Attention
+    ("attention scale dropped", "sc[j] = scale * dot;", "sc[j] = dot;"),
+    ("causal mask hides the diagonal", "const long nkeys = causal ? i + 1 : S;",
+     "const long nkeys = causal ? i : S;"),
+    ("causal mask shows one key too many", "const long nkeys = causal ? i + 1 : S;",
+     "const long nkeys = causal ? (i + 2 < S ? i + 2 : S) : S;"),
+    ("key/value head taken modulo Hkv", "const long c = h / group;", "const long c = h % Hkv;"),
+    ("keys not normalised", "rc = oracle_rmsnorm(K, gk, Kn, B * S * Hkv, D, eps, nthreads);",
+     "memcpy(Kn, K, nke * sizeof(double));"),
+    ("query and key gains swapped", "oracle_rmsnorm(Q, gq, Qn,", "oracle_rmsnorm(Q, gk, Qn,"),
+    ("softmax not normalised", "const double pj = sc[j] / denom;", "const double pj = sc[j];"),
+    ("values read in reverse order", "const double *v = V + ((b * S + j) * Hkv + c) * D;",
+     "const double *v = V + ((b * S + nkeys - 1 - j) * Hkv + c) * D;"),
 ]
 
 
@@ -140,3 +153,21 @@ def test_pins_catch_mutant(tmp_path, desc, orig, repl):
         if not ok:
             failed.append(name)
     assert failed, f"no pin caught the mutant: {desc}"
+
+
+def test_attention_rejects_bad_arguments():
+    Q = np.zeros((1, 4, 3, 8))
+    K = np.zeros((1, 4, 2, 8))
+    with pytest.raises(RuntimeError):          # 3 query heads over 2 key/value heads
+        oracle.attention(Q, K, K, 1.0)
+    Q = np.zeros((1, 4, 2, 8))
+    with pytest.raises(RuntimeError):          # query position outside the sequence
+        oracle.attention(Q, K, K, 1.0, qpos=[4])
+
+
+def test_attention_positions_select_rows(lib):
+    rng = np.random.default_rng(7)
+    Q, K, V = (rng.standard_normal((2, 9, h, 8)) for h in (4, 2, 2))
+    full = oracle.attention(Q, K, V, 0.3, causal=True, lib=lib)
+    part = oracle.attention(Q, K, V, 0.3, causal=True, qpos=[8, 0, 3], lib=lib)
+    assert np.array_equal(part, full[:, [8, 0, 3]])
