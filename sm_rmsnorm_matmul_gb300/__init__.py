@@ -26,7 +26,7 @@ __all__ = [
     "rmsnorm_matmul_ex", "rmsnorm_matmul_lora", "WEIGHT_NK", "GATED_SILU", "rmsnorm", "matmul",
     "force_path",
     "dispatch_path", "describe_plan", "device_status", "status_string", "STATUS", "PATH_AUTO",
-    "PATH_ROWS", "PATH_COLS", "ABI_FUNCTIONS",
+    "PATH_ROWS", "PATH_COLS", "ABI_FUNCTIONS", "rmsnorm_heads", "qknorm_attention",
 ]
 
 STATUS = {
@@ -37,11 +37,12 @@ STATUS = {
 PATH_AUTO, PATH_ROWS, PATH_COLS = 0, 1, 2
 WEIGHT_NK, GATED_SILU = 1, 2   # flags of rmsnorm_matmul_ex
 
-# Every function declared in include/rmsnorm_matmul.h.
+# Every function declared in include/rmsnorm_matmul.h and include/qknorm_attention.h.
 ABI_FUNCTIONS = ("rmsnorm_matmul", "rmsnorm", "matmul", "rmm_force_path",
                  "rmm_device_status", "rmm_status_string", "rmm_dispatch_path",
                  "rmsnorm_matmul_noalloc", "rmm_describe_plan", "rmsnorm_matmul_swiglu",
-                 "rmsnorm_matmul_ex", "rmm_test_hooks", "rmsnorm_matmul_lora")
+                 "rmsnorm_matmul_ex", "rmm_test_hooks", "rmsnorm_matmul_lora",
+                 "rmsnorm_heads", "qknorm_attention")
 
 
 class RmmError(RuntimeError):
@@ -70,10 +71,14 @@ def _bind(l: ctypes.CDLL) -> ctypes.CDLL:
     l.rmm_describe_plan.argtypes = [i64, i64, i64, i32, ctypes.POINTER(ctypes.c_int)]
     l.rmm_test_hooks.argtypes = [i32, i64]
     l.rmsnorm_matmul_lora.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, f32, vp]
+    l.rmsnorm_heads.argtypes = [vp, i64, vp, vp, i64, i64, i64, i64, f32, vp]
+    l.qknorm_attention.argtypes = [vp, i64, vp, i64, vp, i64, vp, vp, vp, i64,
+                                   i64, i64, i64, i64, i64, f32, f32, i32, vp]
     for name in ("rmsnorm_matmul", "rmsnorm_matmul_noalloc", "rmsnorm_matmul_swiglu", "rmsnorm_matmul_ex",
                  "rmsnorm",
                  "matmul", "rmm_force_path", "rmm_device_status", "rmm_dispatch_path",
-                 "rmm_describe_plan", "rmm_test_hooks", "rmsnorm_matmul_lora"):
+                 "rmm_describe_plan", "rmm_test_hooks", "rmsnorm_matmul_lora",
+                 "rmsnorm_heads", "qknorm_attention"):
         getattr(l, name).restype = i32
     return l
 
@@ -209,6 +214,65 @@ def rmsnorm_matmul_lora(X, g, W, A, B, eps: float = 1e-6, out=None, stream=None)
     _raise(lib().rmsnorm_matmul_lora(X.data_ptr(), g.data_ptr(), W.data_ptr(), A.data_ptr(), B.data_ptr(),
                                      out.data_ptr(), M, K, N, R, float(eps), _stream_ptr(stream)),
            "rmsnorm_matmul_lora")
+    return out
+
+
+def _check_heads(name, t):
+    """A bf16 CUDA tensor [B, S, H, D] whose heads are contiguous and whose
+    tokens are a constant stride apart (a column block of a [B*S, width]
+    matrix qualifies).  Returns that token stride in elements."""
+    import torch
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
+        raise TypeError(f"{name} must be a bfloat16 CUDA tensor")
+    if t.dim() != 4:
+        raise ValueError(f"{name} must be [B, S, heads, D], got shape {tuple(t.shape)}")
+    B, S, H, D = t.shape
+    st = t.stride()
+    if st[3] != 1 or (H > 1 and st[2] != D) or (B > 1 and st[0] != S * st[1]):
+        raise ValueError(f"{name}: heads must be contiguous and tokens evenly spaced, "
+                         f"got strides {st}")
+    return st[1] if S > 1 else H * D
+
+
+def rmsnorm_heads(X, g, eps: float = 1e-6, out=None, stream=None):
+    """Y[t,h,:] = RMSNorm(X[t,h,:]; g, eps) over the last dimension for X [T, H, D]
+    (heads contiguous, rows evenly spaced)."""
+    import torch
+    _check_bf16("g", g, 1)
+    ldx = _check_heads("X", X.unsqueeze(0))
+    T, H, D = X.shape
+    if g.shape[0] != D:
+        raise ValueError(f"g must have {D} elements")
+    if out is None:
+        out = torch.empty((T, H, D), dtype=torch.bfloat16, device=X.device)
+    ldy = _check_heads("out", out.unsqueeze(0))
+    _raise(lib().rmsnorm_heads(X.data_ptr(), ldx, g.data_ptr(), out.data_ptr(), ldy, T, H, D,
+                               float(eps), _stream_ptr(stream)), "rmsnorm_heads")
+    return out
+
+
+def qknorm_attention(Q, K, V, gq, gk, eps: float = 1e-6, scale: float | None = None,
+                     causal: bool = True, out=None, stream=None):
+    """O = softmax(scale * RMSNorm(Q; gq) RMSNorm(K; gk)^T) V per head (causal by
+    default), grouped key/value heads.  Q [B,S,Hq,D], K and V [B,S,Hkv,D]; views
+    of a fused QKV projection output are accepted as they are.  O [B,S,Hq,D]."""
+    import torch
+    ldq, ldk, ldv = _check_heads("Q", Q), _check_heads("K", K), _check_heads("V", V)
+    _check_bf16("gq", gq, 1)
+    _check_bf16("gk", gk, 1)
+    B, S, Hq, D = Q.shape
+    Hkv = K.shape[2]
+    if tuple(K.shape) != (B, S, Hkv, D) or tuple(V.shape) != (B, S, Hkv, D):
+        raise ValueError(f"shape mismatch: Q {tuple(Q.shape)}, K {tuple(K.shape)}, V {tuple(V.shape)}")
+    if out is None:
+        out = torch.empty((B, S, Hq, D), dtype=torch.bfloat16, device=Q.device)
+    if tuple(out.shape) != (B, S, Hq, D):
+        raise ValueError(f"out must have shape {(B, S, Hq, D)}")
+    ldo = _check_heads("out", out)
+    _raise(lib().qknorm_attention(Q.data_ptr(), ldq, K.data_ptr(), ldk, V.data_ptr(), ldv,
+                                  gq.data_ptr(), gk.data_ptr(), out.data_ptr(), ldo, B, S, Hq, Hkv, D,
+                                  float(eps), float(scale or 0.0), int(bool(causal)),
+                                  _stream_ptr(stream)), "qknorm_attention")
     return out
 
 

@@ -16,6 +16,7 @@
 #include <utility>
 
 #include "launch.h"
+#include "qknorm_attention.h"
 #include "rmsnorm_matmul.h"
 
 namespace {
@@ -124,6 +125,22 @@ bool map_1d(CUtensorMap* m, const void* ptr, uint64_t n) {
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 tensor [B][S][width] with row stride ld (elements) and sequence
+// stride S * ld, read or written in boxes of [box_rows][64] with the
+// 128-byte swizzle; outside the tensor loads read zero and stores are dropped.
+bool map_3d(CUtensorMap* m, const void* ptr, uint64_t B, uint64_t S, uint64_t width, uint64_t ld,
+            uint32_t box_rows) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    const cuuint64_t dims[3] = {width, S, B};
+    const cuuint64_t strides[2] = {ld * 2, S * ld * 2};
+    const cuuint32_t box[3] = {64, box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // -------------------------------------------------------------- validation
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
     const auto pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
@@ -165,6 +182,8 @@ struct Workspace {
     size_t n_counters = 0;
     void* lora_t = nullptr;   // the low-rank adapter's T = bf16((X*g) @ A), [M, R]
     size_t lora_t_bytes = 0;
+    void* khat = nullptr;     // normalised keys of qknorm_attention, [B, S, Hkv, D]
+    size_t khat_bytes = 0;
 };
 
 std::mutex g_ws_mu;
@@ -247,6 +266,25 @@ int get_lora_buffer(int dev, cudaStream_t s, size_t bytes, void** out) {
         w.lora_t_bytes = n;
     }
     *out = w.lora_t;
+    return RMM_OK;
+}
+
+int get_khat_buffer(int dev, cudaStream_t s, size_t bytes, void** out) {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    Workspace& w = g_ws[{dev, s}];
+    if (w.khat_bytes < bytes) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+            return RMM_ERR_INTERNAL;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return RMM_ERR_LAUNCH;
+        void* p = nullptr;
+        const size_t n = round_up_pow2(bytes);
+        if (cudaMalloc(&p, n) != cudaSuccess) return RMM_ERR_INTERNAL;
+        if (w.khat) cudaFree(w.khat);
+        w.khat = p;
+        w.khat_bytes = n;
+    }
+    *out = w.khat;
     return RMM_OK;
 }
 
@@ -717,10 +755,88 @@ int rmm_dispatch_path(int64_t M, int64_t K, int64_t N) {
 
 int rmm_device_status(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return RMM_ERR_LAUNCH;
-    int v = 0;
+    int v = 0, va = 0;
     if (rmm::read_and_clear_status(&v) != cudaSuccess) return RMM_ERR_LAUNCH;
+    if (rmm::attn_read_and_clear_status(&va) != cudaSuccess) return RMM_ERR_LAUNCH;
+    if (v == RMM_OK) v = va;
     if (v != RMM_OK && clear_workspace_counters() != cudaSuccess) return RMM_ERR_LAUNCH;
     return v;
+}
+
+int rmsnorm_heads(const void* X, int64_t ldx, const void* g, void* Y, int64_t ldy, int64_t T,
+                  int64_t H, int64_t D, float eps, cudaStream_t stream) {
+    if (T < 0 || H < 1 || D < 8 || D > 256 || D % 8 != 0) return RMM_ERR_INVALID_ARG;
+    if (!std::isfinite(eps) || eps < 0.f) return RMM_ERR_INVALID_ARG;
+    if (H > INT32_MAX / D || ldx < H * D || ldy < H * D) return RMM_ERR_INVALID_ARG;
+    if (T == 0) return RMM_OK;
+    if (ldx % 8 != 0 || ldy % 8 != 0) return RMM_ERR_ALIGNMENT;
+    const size_t xb = static_cast<size_t>((T - 1) * ldx + H * D) * 2;
+    const size_t yb = static_cast<size_t>((T - 1) * ldy + H * D) * 2;
+    int rc = check_ptrs(Y, yb, {{X, xb}, {g, static_cast<size_t>(D) * 2}});
+    if (rc != RMM_OK) return rc;
+    int dev = 0;
+    DeviceInfo d;
+    rc = current_device(&dev, &d);
+    if (rc != RMM_OK) return rc;
+    return rmm::launch_rmsnorm_heads(X, ldx, g, Y, ldy, T, static_cast<int>(H), static_cast<int>(D),
+                                     eps, stream) == cudaSuccess
+               ? RMM_OK
+               : RMM_ERR_LAUNCH;
+}
+
+int qknorm_attention(const void* Q, int64_t ldq, const void* K, int64_t ldk, const void* V,
+                     int64_t ldv, const void* gq, const void* gk, void* O, int64_t ldo, int64_t B,
+                     int64_t S, int64_t Hq, int64_t Hkv, int64_t D, float eps, float scale,
+                     int causal, cudaStream_t stream) {
+    if (B < 0 || S < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return RMM_ERR_INVALID_ARG;
+    if (D != rmm::kAttD) return RMM_ERR_INVALID_ARG;
+    if (!std::isfinite(eps) || eps < 0.f || !std::isfinite(scale)) return RMM_ERR_INVALID_ARG;
+    if (Hq > 4096 || ldq < Hq * D || ldo < Hq * D || ldk < Hkv * D || ldv < Hkv * D)
+        return RMM_ERR_INVALID_ARG;
+    if (B == 0 || S == 0) return RMM_OK;
+    if (S > INT32_MAX / 2 || B * Hq > INT32_MAX) return RMM_ERR_INVALID_ARG;
+    const int64_t n_qt = (S + rmm::kAttBM - 1) / rmm::kAttBM;
+    if (n_qt * B * Hq > INT32_MAX) return RMM_ERR_INVALID_ARG;
+    if (ldq % 8 != 0 || ldk % 8 != 0 || ldv % 8 != 0 || ldo % 8 != 0) return RMM_ERR_ALIGNMENT;
+    auto span = [&](int64_t ld, int64_t heads) {
+        return static_cast<size_t>((B * S - 1) * ld + heads * D) * 2;
+    };
+    int rc = check_ptrs(O, span(ldo, Hq),
+                        {{Q, span(ldq, Hq)}, {K, span(ldk, Hkv)}, {V, span(ldv, Hkv)},
+                         {gq, static_cast<size_t>(D) * 2}, {gk, static_cast<size_t>(D) * 2}});
+    if (rc != RMM_OK) return rc;
+    int dev = 0;
+    DeviceInfo d;
+    rc = current_device(&dev, &d);
+    if (rc != RMM_OK) return rc;
+    if (static_cast<size_t>(d.smem_optin) < rmm::attn_smem_bytes()) return RMM_ERR_UNSUPPORTED_DEVICE;
+    void* khat = nullptr;
+    rc = get_khat_buffer(dev, stream, static_cast<size_t>(B * S * Hkv * D) * 2, &khat);
+    if (rc != RMM_OK) return rc;
+    CUtensorMap tmQ, tmK, tmV, tmO;
+    if (!map_3d(&tmQ, Q, B, S, Hq * D, ldq, rmm::kAttBM) ||
+        !map_3d(&tmK, khat, B, S, Hkv * D, Hkv * D, rmm::kAttBN) ||
+        !map_3d(&tmV, V, B, S, Hkv * D, ldv, 64) || !map_3d(&tmO, O, B, S, Hq * D, ldo, rmm::kAttBM))
+        return RMM_ERR_INTERNAL;
+    // the keys once: Kn = RMSNorm(K; gk) per head, into the workspace
+    if (rmm::launch_rmsnorm_heads(K, ldk, gk, khat, Hkv * D, B * S, static_cast<int>(Hkv),
+                                  static_cast<int>(D), eps, stream) != cudaSuccess)
+        return RMM_ERR_LAUNCH;
+    rmm::AttnLaunch a{};
+    a.S = static_cast<int>(S);
+    a.Hq = static_cast<int>(Hq);
+    a.group = static_cast<int>(Hq / Hkv);
+    a.n_qt = static_cast<int>(n_qt);
+    a.n_hb = static_cast<int>(B * Hq);
+    a.causal = causal != 0;
+    a.grid = static_cast<int>(n_qt * B * Hq);
+    a.eps = eps;
+    const double sc = scale > 0.f ? static_cast<double>(scale) : 1.0 / std::sqrt(static_cast<double>(D));
+    a.qscale = static_cast<float>(sc * 1.4426950408889634);   // log2(e)
+    a.wait_limit_us = g_wait_limit_us.load();
+    return rmm::launch_qknorm_attention(tmQ, tmK, tmV, tmO, gq, a, stream) == cudaSuccess
+               ? RMM_OK
+               : RMM_ERR_LAUNCH;
 }
 
 int rmm_test_hooks(int skip_sends, int64_t wait_limit_ns) {

@@ -98,5 +98,34 @@ cudaError_t launch_rmsnorm(const void* X, const void* g, void* Xn, int M, int K,
 // Copies the in-kernel status word to *out and clears it (synchronous).
 cudaError_t read_and_clear_status(int* out);
 
+// ------------------------------------------------ QK-normalised attention (attention.cu)
+constexpr int kAttD = 128;    // head dimension
+constexpr int kAttBM = 128;   // query rows per CTA
+constexpr int kAttBN = 128;   // keys per tile
+
+struct AttnLaunch {
+    int S;            // sequence length (queries and keys)
+    int Hq, group;    // query heads; query heads per key/value head
+    int n_qt;         // query tiles per sequence, ceil(S / 128)
+    int n_hb;         // Hq * B
+    int causal;
+    int grid;         // n_qt * n_hb
+    float eps;
+    float qscale;     // scale * log2(e), folded into the normalised queries
+    int wait_limit_us;
+};
+
+// Y[t,h,:] = RMSNorm(X[t,h,:]; g, eps) for T rows of H heads of D (8..256).
+cudaError_t launch_rmsnorm_heads(const void* X, int64_t ldx, const void* g, void* Y, int64_t ldy,
+                                 int64_t T, int H, int D, float eps, cudaStream_t s);
+// tmQ, tmK (normalised keys), tmV: 3-D maps [B][S][heads*128] read in boxes
+// of [128 rows][64] (V: [64][64]); tmO: the same geometry as tmQ, stored.
+cudaError_t launch_qknorm_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                                    const CUtensorMap& tmV, const CUtensorMap& tmO,
+                                    const void* gq, const AttnLaunch& a, cudaStream_t s);
+size_t attn_smem_bytes();
+// The attention translation unit's own status word (as read_and_clear_status).
+cudaError_t attn_read_and_clear_status(int* out);
+
 
 }  // namespace rmm

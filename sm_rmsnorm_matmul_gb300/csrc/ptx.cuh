@@ -10,9 +10,12 @@
 namespace rmm {
 
 // In-kernel status word: 0, or the rmm_status code of the first bounded wait
-// that ran out.  Read and cleared by rmm_device_status().  This header is
-// included by exactly one translation unit (kernels.cu), which owns it.
+// that ran out.  Internal linkage: every translation unit that includes this
+// header has its own word and a host function that reads and clears it;
+// rmm_device_status() combines them.
+namespace {
 __device__ int g_status = 0;
+}
 
 constexpr int kStatusTimeout = 5;                     // RMM_ERR_DEVICE_TIMEOUT
 constexpr int kStatusInternal = 6;                    // RMM_ERR_INTERNAL (launch not as planned)
@@ -277,6 +280,28 @@ __device__ __forceinline__ void tma_load_1d(uint32_t dst, const CUtensorMap* m, 
         : "memory");
 }
 
+// 3-D tiled load: box at (c0 = innermost, c1, c2) -> smem, completes `bytes`
+// of transaction count on `bar`.  c0 * element size must be a multiple of 16.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                            int c0, int c1, int c2, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+        : "memory");
+}
+
+// 3-D tiled store smem -> global, clipped to the tensor's bounds; part of
+// this thread's current bulk group.  Coordinates are never negative here.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src, int c0, int c1,
+                                             int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(m)),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
 // Prefetch a 2-D box into L2 (no shared memory, no completion).  Reads that
 // follow still go through L2, which stays coherent with any later writer, so
 // a prefetch can never make a reader see stale data.
@@ -453,6 +478,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
+}
+// 2^x on the special-function unit (the PTX ex2.approx instruction; -inf -> 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 __device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }

@@ -124,3 +124,62 @@ def lora_adapter(K: int, N: int, R: int, seed: int):
     a = torch.randn(K, R, generator=gen, dtype=torch.float32) / math.sqrt(K)
     b = torch.randn(R, N, generator=gen, dtype=torch.float32) / math.sqrt(R)
     return a.to(torch.bfloat16).contiguous(), b.to(torch.bfloat16).contiguous()
+
+
+@dataclass(frozen=True)
+class AttentionWorkload:
+    """QK-normalised attention over the output of a fused QKV projection:
+    B sequences of S tokens, Hq query heads and Hkv key/value heads of D."""
+    name: str
+    B: int
+    S: int
+    Hq: int
+    Hkv: int
+    D: int
+    eps: float
+    causal: bool
+    seed: int
+
+    @property
+    def flops(self) -> float:
+        """2 S D per query-key pair for each of the two products; causal
+        attention visits S (S + 1) / 2 pairs per head, full attention S^2."""
+        pairs = self.S * (self.S + 1) / 2 if self.causal else self.S * self.S
+        return 4.0 * self.B * self.Hq * self.D * pairs
+
+    @property
+    def bytes_algorithmic(self) -> int:
+        """Q, K, V read once, O written once, bf16."""
+        return 2 * self.B * self.S * self.D * (2 * self.Hq + 2 * self.Hkv)
+
+
+# The prefill QKV projection's output (4096 tokens x 6144 columns) read as
+# 32 query heads and 8 key/value heads of 128 (grouped-query attention).
+ATTENTION_WORKLOADS = {
+    "prefill_attention_1x4096_h32_kv8_d128_causal": AttentionWorkload(
+        "prefill_attention_1x4096_h32_kv8_d128_causal", B=1, S=4096, Hq=32, Hkv=8, D=128,
+        eps=1e-6, causal=True, seed=5),
+}
+
+
+def attention_inputs(B: int, S: int, Hq: int, Hkv: int, D: int, seed: int):
+    """A fused QKV projection output [B*S, (Hq + 2*Hkv)*D] as a contiguous bf16
+    CPU tensor, and the gains gq, gk [D]: entries N(0, 1), every token's row
+    scaled by one LogUniform(0.1, 10) factor (the spread of row norms the
+    normalisation has to remove), gains U(0.5, 1.5)."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    width = (Hq + 2 * Hkv) * D
+    qkv = torch.randn(B * S, width, generator=gen, dtype=torch.float32)
+    u = torch.rand(B * S, 1, generator=gen, dtype=torch.float32)
+    qkv *= torch.exp(math.log(0.1) + u * (math.log(10.0) - math.log(0.1)))
+    gq = 0.5 + torch.rand(D, generator=gen, dtype=torch.float32)
+    gk = 0.5 + torch.rand(D, generator=gen, dtype=torch.float32)
+    return (qkv.to(torch.bfloat16).contiguous(), gq.to(torch.bfloat16).contiguous(),
+            gk.to(torch.bfloat16).contiguous())
+
+
+def split_qkv(qkv, B: int, S: int, Hq: int, Hkv: int, D: int):
+    """Views Q [B,S,Hq,D], K and V [B,S,Hkv,D] of a fused QKV tensor."""
+    t = qkv.view(B, S, Hq + 2 * Hkv, D)
+    return t[:, :, :Hq], t[:, :, Hq:Hq + Hkv], t[:, :, Hq + Hkv:]

@@ -9,7 +9,7 @@ import pytest
 import sm_rmsnorm_matmul_gb300 as rmm
 from sm_rmsnorm_matmul_gb300 import build as rbuild
 
-HEADER = os.path.join(rbuild.INCLUDE, "rmsnorm_matmul.h")
+HEADERS = [os.path.join(rbuild.INCLUDE, h) for h in ("rmsnorm_matmul.h", "qknorm_attention.h")]
 
 
 @pytest.fixture(scope="module")
@@ -19,8 +19,10 @@ def lib():
 
 
 def declared_functions():
-    with open(HEADER) as f:
-        src = f.read()
+    src = ""
+    for h in HEADERS:
+        with open(h) as f:
+            src += f.read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return set(re.findall(r"^\s*(?:int|const char\*)\s+(\w+)\s*\(", src, flags=re.M))
 
@@ -116,6 +118,41 @@ def test_lora_validation(lib):
     assert f(A16, B16, C16, D16, 0, D16 + 0x100000, 8, 64, 64, 16, 1e-6, None) == 1     # NULL B
     assert f(A16, B16, C16, D16, E16, D16, 8, 64, 64, 16, 1e-6, None) == 1              # Y aliases A
     assert f(0, 0, 0, 0, 0, 0, 0, 64, 64, 16, 1e-6, None) == 0                          # M = 0: no-op
+
+
+def test_attention_validation(lib):
+    f = lib.qknorm_attention
+    E16, F16 = 0x70000000, 0x7000_0000_0
+    # (Q, ldq, K, ldk, V, ldv, gq, gk, O, ldo, B, S, Hq, Hkv, D, eps, scale, causal)
+    ok = [A16, 6144, A16 + 8192, 6144, A16 + 10240, 6144, B16, B16 + 256, F16, 4096,
+          1, 256, 32, 8, 128, 1e-6, 0.0, 1]
+
+    def call(**kw):
+        a = list(ok)
+        names = ["Q", "ldq", "K", "ldk", "V", "ldv", "gq", "gk", "O", "ldo", "B", "S", "Hq",
+                 "Hkv", "D", "eps", "scale", "causal"]
+        for k, v in kw.items():
+            a[names.index(k)] = v
+        return f(*a, None)
+
+    assert call(D=64) == 1                 # head dimension other than 128
+    assert call(Hq=12) == 1                # Hq not a multiple of Hkv
+    assert call(ldq=4000) == 1             # row stride narrower than the heads
+    assert call(ldo=4100) == 2             # row stride not a multiple of 8
+    assert call(Q=A16 + 4) == 2            # misaligned pointer
+    assert call(O=0) == 1                  # NULL output
+    assert call(O=A16 + 4096) == 1         # output overlaps the inputs
+    assert call(eps=-1.0) == 1
+    assert call(scale=float("nan")) == 1
+    assert call(S=0) == 0 and call(B=0) == 0   # no-ops
+    h = lib.rmsnorm_heads
+    assert h(A16, 1024, B16, D16, 1024, 4, 8, 128, 1e-6, None) != 1   # valid (fails later without a GPU)
+    assert h(A16, 1024, B16, D16, 1024, 4, 8, 100, 1e-6, None) == 1   # D % 8
+    assert h(A16, 1024, B16, D16, 1024, 4, 2, 512, 1e-6, None) == 1   # D > 256
+    assert h(A16, 1000, B16, D16, 1024, 4, 8, 128, 1e-6, None) == 1   # ldx < H * D
+    assert h(A16, 1028, B16, D16, 1028, 4, 8, 128, 1e-6, None) == 2   # ld % 8
+    assert h(A16, 1024, B16, A16, 1024, 4, 8, 128, 1e-6, None) == 1   # Y aliases X
+    assert h(0, 1024, 0, 0, 1024, 0, 8, 128, 1e-6, None) == 0         # T = 0: no-op
 
 
 def test_unfused_validation(lib):

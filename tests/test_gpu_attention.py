@@ -1,0 +1,198 @@
+"""QK-normalised attention on the GPU against the fp64 oracle, through the C ABI.
+
+The device rounds the normalised queries (with scale * log2(e) folded in) and
+the normalised keys to bf16 before the tensor cores.  The reference applies
+the same two roundings to the oracle's own RMSNorm (fp64) and then runs the
+oracle's fp64 attention with base-2 exponentials (scale ln 2), so that what is
+left to compare is the device's softmax and products.  What remains on the
+device side, per output element, and the bound used here:
+
+  * P rounded to bf16 (relative 2^-9 per weight), ex2.approx (relative ~2^-22),
+    fp32 sums over at most a few thousand keys (~2^-12), and the rare element
+    of the bf16 operands whose fp32 statistic put it on the other side of a
+    rounding boundary: together below 2^-8 * sum_j p_j |v_jd|;
+  * O rounded to bf16 once: 2^-9 |o|, taken as 2^-8 |o|.
+
+  |O - O_ref| <= 2^-8 * sum_j p_j |v_jd| + 2^-8 |O_ref| + 1e-5
+
+sum_j p_j |v_jd| is the oracle's attention with |V| as the values.  A second
+check compares with the fully exact oracle (no rounding anywhere) under the
+first-order bound of the two operand roundings.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+LN2 = math.log(2.0)
+LOG2E = 1.0 / LN2
+
+
+@pytest.fixture(scope="module")
+def rmm():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sm_rmsnorm_matmul_gb300 as m
+    m.lib()
+    return m
+
+
+def bf16_round(x):
+    """fp64 -> fp32 -> bf16 (nearest even) -> fp64: the device computes its
+    operands in fp32 and rounds them once."""
+    return torch.from_numpy(np.ascontiguousarray(x)).to(torch.float32).to(torch.bfloat16).double().numpy()
+
+
+def references(Q, K, V, gq, gk, eps, causal, qpos=None):
+    B, S, Hq, D = Q.shape
+    Hkv = K.shape[2]
+    qn = oracle.rmsnorm(Q.reshape(-1, D), gq, eps).reshape(B, S, Hq, D)
+    kn = oracle.rmsnorm(K.reshape(-1, D), gk, eps).reshape(B, S, Hkv, D)
+    qd = bf16_round(qn * (LOG2E / math.sqrt(D)))
+    kd = bf16_round(kn)
+    Vf = oracle.to_f64(V)
+    ref = oracle.attention(qd, kd, Vf, LN2, causal=causal, qpos=qpos)
+    wabs = oracle.attention(qd, kd, np.abs(Vf), LN2, causal=causal, qpos=qpos)
+    return ref, wabs, qn, kn
+
+
+def assert_attention_close(O, Q, K, V, gq, gk, eps, causal, what, qpos=None):
+    ref, wabs, qn, kn = references(Q, K, V, gq, gk, eps, causal, qpos)
+    o = oracle.to_f64(O)
+    if qpos is not None:
+        o = o[:, qpos]
+    tol = 2.0 ** -8 * wabs + 2.0 ** -8 * np.abs(ref) + 1e-5
+    err = np.abs(o - ref)
+    bad = ~(err <= tol)   # NaN fails
+    assert not bad.any(), (f"{what}: {int(bad.sum())} of {ref.size} outside the bound, "
+                           f"max err {float(np.nanmax(err)):.3e}")
+    # the exact oracle (no rounding): operand roundings move every score by at
+    # most 2^-8 * scale * sum_d |qn_d kn_d| (relative 2^-9 on each operand);
+    # to first order the output moves by at most twice the largest such
+    # shift times sum_j p_j |v_jd - o_d| <= 2 * sum_j p_j |v_jd|
+    exact = oracle.qknorm_attention(Q, K, V, gq, gk, eps, causal=causal, qpos=qpos)
+    D = Q.shape[3]
+    rep = Q.shape[2] // K.shape[2]
+    qs = np.abs(qn if qpos is None else qn[:, qpos])
+    ks = np.repeat(np.abs(kn), rep, axis=2).max(axis=1, keepdims=True)
+    shift = 2.0 ** -8 / math.sqrt(D) * (qs * ks).sum(axis=3, keepdims=True)
+    tol_e = 1.25 * (2 * shift * 2 * wabs) + tol
+    bad = ~(np.abs(o - exact) <= tol_e)
+    assert not bad.any(), f"{what}: {int(bad.sum())} outside the bound of the exact oracle"
+
+
+def run(rmm, B, S, Hq, Hkv, causal, seed, eps=1e-6, D=128, qkv=None):
+    from sm_rmsnorm_matmul_gb300 import inputs
+    if qkv is None:
+        qkv, gq, gk = inputs.attention_inputs(B, S, Hq, Hkv, D, seed)
+    else:
+        _, gq, gk = inputs.attention_inputs(B, 1, Hq, Hkv, D, seed)
+    Q, K, V = inputs.split_qkv(qkv, B, S, Hq, Hkv, D)
+    Qd, Kd, Vd = inputs.split_qkv(qkv.cuda(), B, S, Hq, Hkv, D)
+    O = rmm.qknorm_attention(Qd, Kd, Vd, gq.cuda(), gk.cuda(), eps, causal=causal)
+    torch.cuda.synchronize()
+    assert rmm.device_status() == 0
+    return O.cpu(), Q, K, V, gq, gk
+
+
+ATTN = [
+    # (B, S, Hq, Hkv, causal)
+    (1, 256, 4, 2, True),      # two query tiles, two key tiles, diagonal masks
+    (2, 300, 4, 1, True),      # ragged sequence, two sequences, four query heads per key head
+    (1, 200, 2, 2, False),     # full attention over a ragged last key tile
+    (1, 1, 2, 1, True),        # one token
+    (1, 1100, 2, 1, True),     # nine key tiles
+    (3, 130, 8, 8, False),     # multi-head, full, two tiles with a 2-key tail
+]
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,causal", ATTN)
+def test_qknorm_attention(rmm, B, S, Hq, Hkv, causal):
+    O, Q, K, V, gq, gk = run(rmm, B, S, Hq, Hkv, causal, seed=B * 1000 + S + Hq)
+    assert_attention_close(O, Q, K, V, gq, gk, 1e-6, causal, f"attention {B}x{S} {Hq}/{Hkv}")
+
+
+def test_first_causal_row_is_first_value(rmm):
+    # one visible key: softmax weight exactly 1, O = bf16(V[0]) exactly
+    O, Q, K, V, gq, gk = run(rmm, 1, 64, 4, 2, True, seed=9)
+    rep = 2
+    want = V[:, 0].repeat_interleave(rep, dim=1)
+    assert torch.equal(O[:, 0], want)
+
+
+def test_rescaled_rows(rmm):
+    # every query of a head equals one direction u and so does one late key:
+    # that key's score dwarfs the first tile's, so the running maximum jumps
+    # by far more than 2^8 and the accumulator is rescaled
+    from sm_rmsnorm_matmul_gb300 import inputs
+    B, S, Hq, Hkv, D = 1, 700, 2, 1, 128
+    qkv, gq, gk = inputs.attention_inputs(B, S, Hq, Hkv, D, 21)
+    gq = torch.full((D,), 1.5, dtype=torch.bfloat16)
+    gk = torch.full((D,), 1.5, dtype=torch.bfloat16)
+    t = qkv.view(B * S, Hq + 2 * Hkv, D)
+    u = torch.randn(D, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
+    t[:, 0] = u
+    t[:, 1] = -u
+    t[:, Hq] = -u                   # every key points away ...
+    t[450, Hq] = u                  # ... except one, late in the sequence
+    t[451:, Hq] = torch.randn(S - 451, D, generator=torch.Generator().manual_seed(4)).to(torch.bfloat16)
+    Q, K, V = inputs.split_qkv(qkv, B, S, Hq, Hkv, D)
+    Qd, Kd, Vd = inputs.split_qkv(qkv.cuda(), B, S, Hq, Hkv, D)
+    O = rmm.qknorm_attention(Qd, Kd, Vd, gq.cuda(), gk.cuda(), 1e-6, causal=True)
+    torch.cuda.synchronize()
+    assert rmm.device_status() == 0
+    assert_attention_close(O.cpu(), Q, K, V, gq, gk, 1e-6, True, "rescaled rows")
+
+
+def test_explicit_scale_and_eps(rmm):
+    from sm_rmsnorm_matmul_gb300 import inputs
+    B, S, Hq, Hkv, D = 1, 150, 2, 1, 128
+    qkv, gq, gk = inputs.attention_inputs(B, S, Hq, Hkv, D, 33)
+    Q, K, V = inputs.split_qkv(qkv, B, S, Hq, Hkv, D)
+    Qd, Kd, Vd = inputs.split_qkv(qkv.cuda(), B, S, Hq, Hkv, D)
+    O = rmm.qknorm_attention(Qd, Kd, Vd, gq.cuda(), gk.cuda(), 0.25, scale=1.0 / 16, causal=False)
+    torch.cuda.synchronize()
+    qn = oracle.rmsnorm(Q.reshape(-1, D), gq, 0.25).reshape(B, S, Hq, D)
+    kn = oracle.rmsnorm(K.reshape(-1, D), gk, 0.25).reshape(B, S, Hkv, D)
+    qd = bf16_round(qn * (LOG2E / 16))
+    kd = bf16_round(kn)
+    ref = oracle.attention(qd, kd, oracle.to_f64(V), LN2, causal=False)
+    wabs = oracle.attention(qd, kd, np.abs(oracle.to_f64(V)), LN2, causal=False)
+    err = np.abs(oracle.to_f64(O.cpu()) - ref)
+    assert (err <= 2.0 ** -8 * wabs + 2.0 ** -8 * np.abs(ref) + 1e-5).all()
+
+
+def test_full_size_sampled_rows(rmm):
+    # the benchmark's workload (one 4096-token sequence, 32 query heads over
+    # 8 key/value heads, causal), sampled query positions checked one by one
+    from sm_rmsnorm_matmul_gb300 import inputs
+    w = inputs.ATTENTION_WORKLOADS["prefill_attention_1x4096_h32_kv8_d128_causal"]
+    qkv, gq, gk = inputs.attention_inputs(w.B, w.S, w.Hq, w.Hkv, w.D, w.seed)
+    Q, K, V = inputs.split_qkv(qkv, w.B, w.S, w.Hq, w.Hkv, w.D)
+    Qd, Kd, Vd = inputs.split_qkv(qkv.cuda(), w.B, w.S, w.Hq, w.Hkv, w.D)
+    O = rmm.qknorm_attention(Qd, Kd, Vd, gq.cuda(), gk.cuda(), w.eps, causal=w.causal)
+    torch.cuda.synchronize()
+    assert rmm.device_status() == 0
+    qpos = sorted({0, 1, 127, 128, 129, 2047, 2048, 4094, 4095} |
+                  set(inputs.sample_rows(w.S, 24)))
+    assert_attention_close(O.cpu(), Q, K, V, gq, gk, w.eps, w.causal, "full size", qpos=qpos)
+
+
+def test_rmsnorm_heads_matches_oracle(rmm):
+    from sm_rmsnorm_matmul_gb300 import inputs
+    B, S, Hq, Hkv, D = 1, 333, 4, 2, 128
+    qkv, gq, gk = inputs.attention_inputs(B, S, Hq, Hkv, D, 44)
+    K = qkv.view(B * S, Hq + 2 * Hkv, D)[:, Hq:Hq + Hkv]
+    Y = rmm.rmsnorm_heads(K.cuda(), gk.cuda(), 1e-6).cpu()
+    ref = oracle.rmsnorm(K.reshape(-1, D), gk, 1e-6).reshape(S, Hkv, D)
+    y = oracle.to_f64(Y)
+    # one rounding of an fp32 value: the nearest bf16 or, at a boundary, its neighbour
+    assert (np.abs(y - ref) <= 2.0 ** -7 * np.abs(ref) + 1e-30).all()
+    same = (y == bf16_round(ref)).mean()
+    assert same > 0.99, same
