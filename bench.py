@@ -351,6 +351,73 @@ def bench_workload(torch, rmm, inputs, w, K, W_warm, device, stream, l2, with_un
     return res
 
 
+def bench_attention(torch, rmm, inputs, w, K, device, stream, l2, sampler=None):
+    """Time qknorm_attention on one AttentionWorkload: K back-to-back calls in
+    CUDA graphs, each on its own copy of the fused QKV tensor (copies rotate
+    so that every call misses L2), and torch's rms_norm + scaled dot-product
+    attention on the same inputs as context."""
+    per = w.bytes_algorithmic
+    n_copies = max(1, math.ceil(3 * l2 / per) + 1) if per < 3 * l2 else 1
+    qkv, gq, gk = inputs.attention_inputs(w.B, w.S, w.Hq, w.Hkv, w.D, w.seed)
+    gq, gk = gq.to(device), gk.to(device)
+    copies = []
+    for _ in range(n_copies):
+        t = qkv.to(device)
+        o = torch.empty((w.B, w.S, w.Hq, w.D), dtype=torch.bfloat16, device=device)
+        copies.append((inputs.split_qkv(t, w.B, w.S, w.Hq, w.Hkv, w.D), o))
+
+    def step(i):
+        (q, k, v), o = copies[i]
+        rmm.qknorm_attention(q, k, v, gq, gk, w.eps, causal=w.causal, out=o, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            step(i % n_copies)
+    stream.synchronize()
+    if rmm.device_status(stream) != 0:
+        raise RuntimeError("device status not clean after warm-up")
+    secs, window, graphs = time_graph(torch, stream, step, n_copies, K)
+    if sampler:
+        sampler.mark(*window)
+    del graphs
+    status = rmm.device_status(stream)
+    F = torch.nn.functional
+
+    def step_torch(i):
+        (q, k, v), _ = copies[i]
+        qn = F.rms_norm(q, (w.D,), gq, w.eps)
+        kn = F.rms_norm(k, (w.D,), gk, w.eps)
+        F.scaled_dot_product_attention(qn.transpose(1, 2), kn.transpose(1, 2), v.transpose(1, 2),
+                                       is_causal=w.causal, enable_gqa=True)
+
+    unfused = None
+    try:
+        with torch.cuda.stream(stream):
+            for i in range(2):
+                step_torch(i % n_copies)
+        ku = max(3, K // 4)
+        s_u, _, g2 = time_graph(torch, stream, step_torch, n_copies, ku)
+        del g2
+        unfused = s_u / ku
+    except (RuntimeError, TypeError):   # an older torch without enable_gqa or rms_norm
+        unfused = None
+    del copies
+    return {"secs": secs, "n_copies": n_copies, "status": status, "unfused_secs_per_step": unfused}
+
+
+def attention_entry(w, t, r, peaks, k):
+    tflops = w.flops / t / 1e12
+    e = {"workload": w.name + " (QK-normalised attention)", "path": "qknorm_attention (tcgen05)",
+         "steps": k, "us_per_call": round(t * 1e6, 3), "tflops": round(tflops, 2),
+         "hbm_gbs": round(w.bytes_algorithmic / t / 1e9, 1), "bound": "tensor",
+         "roofline_frac": round(tflops / peaks["bf16_tflops"], 4),
+         "frac_of_tensor_peak_sustained": round(tflops / peaks["bf16_tflops_sustained"], 4),
+         "copies": r["n_copies"], "device_status": r["status"]}
+    if r.get("unfused_secs_per_step"):
+        e["torch_rms_norm_sdpa_us"] = round(r["unfused_secs_per_step"] * 1e6, 3)
+    return e
+
+
 def e2e_bench(torch, rmm, w, host, device, stream, K):
     """Pinned host X, g, W -> device, fused call, Y -> pinned host, per step."""
     X, g, W = host
@@ -446,8 +513,11 @@ def main():
         args.warmup = 3
 
     from sm_rmsnorm_matmul_gb300 import inputs
-    w = inputs.WORKLOADS[args.workload]
     ws, rank, local = dist_env()
+    if args.workload in inputs.ATTENTION_WORKLOADS:
+        # one attention line alone (profiling and quick checks)
+        return run_attention_only(args, inputs.ATTENTION_WORKLOADS[args.workload], rank)
+    w = inputs.WORKLOADS[args.workload]
 
     if args.impl == "reference":
         return run_reference(args, w, ws, rank)
@@ -529,6 +599,13 @@ def main():
                 shapes.append(shape_entry(ww, r["secs"] / k, r, peaks, k, lora_r=lora_rank))
                 del r
                 torch.cuda.empty_cache()
+            # QK-normalised attention over the prefill QKV projection's output
+            for aw in inputs.ATTENTION_WORKLOADS.values():
+                k = int(min(2000, max(20, 0.3 / (aw.flops / (peaks["bf16_tflops"] * 1e12) * 3))))
+                r = bench_attention(torch, rmm, inputs, aw, k, device, stream, l2, sampler=sampler)
+                shapes.append(attention_entry(aw, r["secs"] / k, r, peaks, k))
+                del r
+                torch.cuda.empty_cache()
     clocks = sampler.summary()
 
     K = args.steps
@@ -595,6 +672,25 @@ def main():
     if rank == 0:
         print(json.dumps(out), flush=True)
     sync.close()
+
+
+def run_attention_only(args, aw, rank):
+    """`--workload <attention workload>`: time qknorm_attention alone for
+    --steps calls and print its shape entry as one JSON line."""
+    import torch
+    import sm_rmsnorm_matmul_gb300 as rmm
+    from sm_rmsnorm_matmul_gb300 import inputs
+    rmm.lib()
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 1024 * 1024))
+    peaks, _ = load_peaks()
+    stream = torch.cuda.Stream(device=device)
+    r = bench_attention(torch, rmm, inputs, aw, args.steps, device, stream, l2)
+    e = attention_entry(aw, r["secs"] / args.steps, r, peaks, args.steps)
+    if rank == 0:
+        print(json.dumps(e), flush=True)
 
 
 def kernel_name(rmm, w):

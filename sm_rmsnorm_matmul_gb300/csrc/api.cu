@@ -795,8 +795,8 @@ int qknorm_attention(const void* Q, int64_t ldq, const void* K, int64_t ldk, con
         return RMM_ERR_INVALID_ARG;
     if (B == 0 || S == 0) return RMM_OK;
     if (S > INT32_MAX / 2 || B * Hq > INT32_MAX) return RMM_ERR_INVALID_ARG;
-    const int64_t n_qt = (S + rmm::kAttBM - 1) / rmm::kAttBM;
-    if (n_qt * B * Hq > INT32_MAX) return RMM_ERR_INVALID_ARG;
+    const int64_t n_qb = (S + 2 * rmm::kAttBM - 1) / (2 * rmm::kAttBM);
+    if (n_qb * B * Hq > INT32_MAX) return RMM_ERR_INVALID_ARG;
     if (ldq % 8 != 0 || ldk % 8 != 0 || ldv % 8 != 0 || ldo % 8 != 0) return RMM_ERR_ALIGNMENT;
     auto span = [&](int64_t ld, int64_t heads) {
         return static_cast<size_t>((B * S - 1) * ld + heads * D) * 2;
@@ -826,10 +826,10 @@ int qknorm_attention(const void* Q, int64_t ldq, const void* K, int64_t ldk, con
     a.S = static_cast<int>(S);
     a.Hq = static_cast<int>(Hq);
     a.group = static_cast<int>(Hq / Hkv);
-    a.n_qt = static_cast<int>(n_qt);
+    a.n_qb = static_cast<int>(n_qb);
     a.n_hb = static_cast<int>(B * Hq);
     a.causal = causal != 0;
-    a.grid = static_cast<int>(n_qt * B * Hq);
+    a.grid = static_cast<int>(n_qb * B * Hq);
     a.eps = eps;
     const double sc = scale > 0.f ? static_cast<double>(scale) : 1.0 / std::sqrt(static_cast<double>(D));
     a.qscale = static_cast<float>(sc * 1.4426950408889634);   // log2(e)

@@ -7,12 +7,12 @@
 //
 //   rmsnorm_heads_kernel    normalises every key head once (memory-bound; one
 //                           warp per head row), into a bf16 workspace;
-//   qknorm_attention_kernel one CTA per 128-row query tile of one head:
-//                           normalises the query tile in shared memory (with
-//                           scale * log2(e) folded in), then for each 128-key
-//                           tile S = Qn Kn^T and O += P V on the tensor cores
-//                           (tcgen05, accumulators in tensor memory), with the
-//                           online softmax between them.
+//   qknorm_attention_kernel one CTA per 256 query rows of one head (two
+//                           128-row tiles): normalises the query tiles in shared
+//                           memory (with scale * log2(e) folded in), then for
+//                           each 128-key tile S = Qn Kn^T and O += P V on the
+//                           tensor cores (tcgen05, accumulators in tensor
+//                           memory), with the online softmax between them.
 //
 // Normalising each key once, not once per query tile that reads it, is the
 // choice for GB300: a key tile is read by S/128 query tiles of every head in
@@ -89,23 +89,28 @@ __global__ void __launch_bounds__(kHeadsWarps * 32)
 }
 
 // ------------------------------------------------------- attention kernel
-constexpr int kAttThreads = 256;     // warp 0 TMA, 1 MMA, 2 TMEM, 3 idle, 4-7 rows
-constexpr int kAttKStages = 3;
-constexpr int kAttVStages = 2;
+// One CTA per block of 256 query rows of one head: two 128-row query tiles,
+// A (rows q0 .. q0 + 127) and B (q0 + 128 .. q0 + 255), each with its own
+// score buffer, output accumulator and group of four softmax warps.  The MMA
+// issuer alternates between them, so the tensor cores work on one tile's
+// products while the other tile's softmax runs; both read the same K and V
+// tiles, loaded once.
+constexpr int kAttThreads = 320;    // warp 0 TMA, 1 MMA + TMEM, 2-5 tile A, 6-9 tile B
+constexpr int kAttStages = 2;       // K and V rings
 constexpr uint32_t kAttTile = kAttBM * kAttD * 2;   // 32 KB: a Q, K or V tile
 constexpr uint32_t kAttHalf = kAttTile / 2;         // 64 columns of a tile (SW128 box)
-constexpr uint32_t kAttOffQ = 0;                    // Q tile, later the O staging
-constexpr uint32_t kAttOffK = kAttOffQ + kAttTile;
-constexpr uint32_t kAttOffV = kAttOffK + kAttKStages * kAttTile;
-constexpr uint32_t kAttOffG = kAttOffV + kAttVStages * kAttTile;   // gq as fp32 [128]
+constexpr uint32_t kAttOffQ = 0;                    // Q tiles A and B, later the O staging
+constexpr uint32_t kAttOffK = kAttOffQ + 2 * kAttTile;
+constexpr uint32_t kAttOffV = kAttOffK + kAttStages * kAttTile;
+constexpr uint32_t kAttOffG = kAttOffV + kAttStages * kAttTile;   // gq as fp32 [128]
 constexpr uint32_t kAttOffBar = kAttOffG + kAttD * 4;
 constexpr uint32_t kAttNumBars = 18;
 constexpr uint32_t kAttOffMisc = kAttOffBar + 256;
 constexpr uint32_t kAttSmem = kAttOffMisc + 16 + 1024;   // + alignment slack
 static_assert(kAttNumBars * 8 <= 256, "barrier area");
-// Tensor memory: two S buffers (P overwrites the first 64 columns of its S
-// buffer, two bf16 per column) and the O accumulator.
-constexpr uint32_t kAttColS = 0, kAttColO = 256, kAttTmemCols = 512;
+// Tensor memory, per query tile X (columns X * 256 ..): the score buffer S
+// (P overwrites its first 64 columns, two bf16 per column), then O.
+constexpr uint32_t kAttColO = 128, kAttTmemCols = 512;
 constexpr float kAttRescale = 8.f;   // rescale O only when the row max grows by > 2^8
 
 __global__ void __launch_bounds__(kAttThreads, 1)
@@ -122,45 +127,52 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     const uint32_t sq = sbase + kAttOffQ, sk = sbase + kAttOffK, sv = sbase + kAttOffV;
     float* sg = reinterpret_cast<float*>(smem + kAttOffG);
     const uint32_t bar0 = sbase + kAttOffBar;
-    const uint32_t q_full = bar0, q_ready = bar0 + 8;
-    auto k_full = [&](uint32_t i) { return bar0 + 16 + 8 * i; };
+    const uint32_t q_full = bar0;
+    auto q_ready = [&](int x) { return bar0 + 8 + 8 * x; };
+    auto k_full = [&](uint32_t i) { return bar0 + 24 + 8 * i; };
     auto k_empty = [&](uint32_t i) { return bar0 + 40 + 8 * i; };
-    auto v_full = [&](uint32_t i) { return bar0 + 64 + 8 * i; };
-    auto v_empty = [&](uint32_t i) { return bar0 + 80 + 8 * i; };
-    auto s_full = [&](uint32_t i) { return bar0 + 96 + 8 * i; };
-    auto p_full = [&](uint32_t i) { return bar0 + 112 + 8 * i; };
-    const uint32_t o_done = bar0 + 128, mmadone = bar0 + 136;
+    auto v_full = [&](uint32_t i) { return bar0 + 56 + 8 * i; };
+    auto v_empty = [&](uint32_t i) { return bar0 + 72 + 8 * i; };
+    auto s_full = [&](int x) { return bar0 + 88 + 8 * x; };
+    auto p_full = [&](int x) { return bar0 + 104 + 8 * x; };
+    auto o_final = [&](int x) { return bar0 + 120 + 8 * x; };
+    const uint32_t mmadone = bar0 + 136;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kAttOffMisc);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + kAttOffMisc + 4);
 
-    // the tile: query rows [q0, q0 + 128) of head h in sequence b; causal
-    // launches take the longest rows (the last query tiles) first
+    // the block: query rows [q0, q0 + 256) of head h in sequence b; causal
+    // launches take the longest rows (the last blocks) first
     const int bid = blockIdx.x;
-    const int qt = a.causal ? a.n_qt - 1 - bid / a.n_hb : bid / a.n_hb;
+    const int qb = a.causal ? a.n_qb - 1 - bid / a.n_hb : bid / a.n_hb;
     const int hb = bid % a.n_hb;
     const int h = hb % a.Hq, b = hb / a.Hq;
     const int c = h / a.group;
-    const int q0 = qt * kAttBM;
+    const int q0 = qb * 2 * kAttBM;
     const int n_kv_all = (a.S + kAttBN - 1) / kAttBN;
-    const int n_kv = a.causal ? min(qt + 1, n_kv_all) : n_kv_all;
+    // key tiles each query tile visits (tile B may lie past the sequence end)
+    int n_x[2];
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+        const int qt = 2 * qb + x;
+        n_x[x] = q0 + x * kAttBM >= a.S ? 0 : a.causal ? min(qt + 1, n_kv_all) : n_kv_all;
+    }
+    const int n_kv = max(n_x[0], n_x[1]);
 
     if (threadIdx.x == 0) {
         if (blockDim.x != kAttThreads) atomicCAS(&g_status, 0, kStatusInternal);
         mbar_init(q_full, 1);
-        mbar_init(q_ready, 4);   // one elected lane per row warp
-        for (int i = 0; i < kAttKStages; ++i) {
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(q_ready(x), 4);   // one elected lane per softmax warp
+            mbar_init(s_full(x), 1);
+            mbar_init(p_full(x), 4);
+            mbar_init(o_final(x), 1);
+        }
+        for (int i = 0; i < kAttStages; ++i) {
             mbar_init(k_full(i), 1);
             mbar_init(k_empty(i), 1);
-        }
-        for (int i = 0; i < kAttVStages; ++i) {
             mbar_init(v_full(i), 1);
             mbar_init(v_empty(i), 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(s_full(i), 1);
-            mbar_init(p_full(i), 4);
-        }
-        mbar_init(o_done, 1);
         mbar_init(mmadone, 1);
         abort[0] = blockDim.x != kAttThreads;
         abort[1] = a.wait_limit_us;
@@ -170,7 +182,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         prefetch_tmap(&tmV);
         prefetch_tmap(&tmO);
     }
-    if (warp == 2) {
+    if (warp == 1) {
         tmem_alloc(smem_u32(tmem_holder), kAttTmemCols);
         tmem_relinquish();
     }
@@ -187,11 +199,15 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         // ------------------------------------------------ TMA producer
         if (lane == 0 && !*abort) {
             const uint64_t keep = policy_evict_last();   // K and V tiles are re-read
-            const uint64_t once = policy_evict_first();  // the query tile is read once
-            mbar_arrive_expect_tx(q_full, kAttTile);
-            tma_load_3d(sq, &tmQ, q_full, h * kAttD, q0, b, once);
-            tma_load_3d(sq + kAttHalf, &tmQ, q_full, h * kAttD + 64, q0, b, once);
-            Ring kr(kAttKStages), vr(kAttVStages);
+            const uint64_t once = policy_evict_first();  // the query tiles are read once
+            mbar_arrive_expect_tx(q_full, 2 * kAttTile);
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                tma_load_3d(sq + x * kAttTile, &tmQ, q_full, h * kAttD, q0 + x * kAttBM, b, once);
+                tma_load_3d(sq + x * kAttTile + kAttHalf, &tmQ, q_full, h * kAttD + 64,
+                            q0 + x * kAttBM, b, once);
+            }
+            Ring kr(kAttStages), vr(kAttStages);
             int k_issued = 0, v_issued = 0;
             for (int j = 0; j < n_kv; ++j) {
                 if (!mbar_wait(k_empty(kr.idx), kr.phase ^ 1, abort)) break;
@@ -216,72 +232,87 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             }
             // never leave with copies still landing in shared memory
             mbar_wait_teardown(q_full, 0);
-            for (int i = k_issued > kAttKStages ? k_issued - kAttKStages : 0; i < k_issued; ++i)
-                mbar_wait_teardown(k_full(i % kAttKStages), (i / kAttKStages) & 1);
-            for (int i = v_issued > kAttVStages ? v_issued - kAttVStages : 0; i < v_issued; ++i)
-                mbar_wait_teardown(v_full(i % kAttVStages), (i / kAttVStages) & 1);
+            for (int i = k_issued > kAttStages ? k_issued - kAttStages : 0; i < k_issued; ++i)
+                mbar_wait_teardown(k_full(i % kAttStages), (i / kAttStages) & 1);
+            for (int i = v_issued > kAttStages ? v_issued - kAttStages : 0; i < v_issued; ++i)
+                mbar_wait_teardown(v_full(i % kAttStages), (i / kAttStages) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(kAttBM, kAttBN, false, false);
             constexpr uint32_t idesc_o = idesc_bf16_f32(kAttBM, kAttD, false, true);
-            Ring kr(kAttKStages), vr(kAttVStages);
-            // S_j = Qn K_j^T into S buffer j & 1: A and B K-major, 8 steps of 16 dims
-            auto issue_s = [&](int j) -> bool {
-                if (!mbar_wait(k_full(kr.idx), kr.phase, abort)) return false;
-                tc_fence_after();
-                const uint32_t d = tmem + kAttColS + (j & 1) * kAttBN;
-                const uint32_t kb = sk + kr.idx * kAttTile;
+            // S_x = Qn_x K^T into tile x's score buffer: A and B K-major, 8 steps of 16 dims
+            auto issue_s = [&](int x, uint32_t kslot) {
+                const uint32_t d = tmem + x * 256;
+                const uint32_t qa = sq + x * kAttTile, kb = sk + kslot * kAttTile;
 #pragma unroll
                 for (int kk = 0; kk < kAttD / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kAttHalf + (kk & 3) * 32;
-                    mma_bf16_ss(d, sdesc_sw128(sq + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                    mma_bf16_ss(d, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
                                 idesc_s, kk > 0);
                 }
-                mma_commit(k_empty(kr.idx));
-                mma_commit(s_full(j & 1));
-                kr.advance();
-                return true;
+                mma_commit(s_full(x));
             };
-            bool ok = mbar_wait(q_ready, 0, abort);
-            if (ok) {
-                tc_fence_after();
-                ok = issue_s(0);
-            }
-            for (int j = 0; ok && j < n_kv; ++j) {
-                // the next scores first, so the softmax of tile j + 1 overlaps P_j V_j
-                if (j + 1 < n_kv && !issue_s(j + 1)) break;
-                if (!mbar_wait(p_full(j & 1), (j >> 1) & 1, abort)) break;
-                if (!mbar_wait(v_full(vr.idx), vr.phase, abort)) break;
-                tc_fence_after();
-                // O += P_j V_j: A = P from tensor memory (keys 16kk.. in columns
-                // 8kk..), B = V MN-major (dims contiguous), 8 steps of 16 keys
-                const uint32_t pa = tmem + kAttColS + (j & 1) * kAttBN;
-                const uint32_t vb = sv + vr.idx * kAttTile;
+            // O_x += P_x V: A = P from tensor memory (keys 16kk.. in columns
+            // 8kk..), B = V MN-major (dims contiguous), 8 steps of 16 keys
+            auto issue_pv = [&](int x, uint32_t vslot, bool acc) {
+                const uint32_t pa = tmem + x * 256, vb = sv + vslot * kAttTile;
 #pragma unroll
                 for (int kk = 0; kk < kAttBN / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * (kAttTile / 2) + (kk & 3) * 2048;
-                    mma_bf16_ts(tmem + kAttColO, pa + kk * 8, sdesc_sw128(vb + off, kAttTile / 4, 1024),
-                                idesc_o, j > 0 || kk > 0);
+                    mma_bf16_ts(pa + kAttColO, pa + kk * 8, sdesc_sw128(vb + off, kAttTile / 4, 1024),
+                                idesc_o, acc || kk > 0);
                 }
+            };
+            Ring kr(kAttStages), vr(kAttStages);
+            bool ok = n_kv > 0 && mbar_wait(k_full(kr.idx), kr.phase, abort);
+            for (int x = 0; ok && x < 2; ++x) {
+                if (n_x[x] == 0) continue;
+                if (!mbar_wait(q_ready(x), 0, abort)) { ok = false; break; }
+                tc_fence_after();
+                issue_s(x, kr.idx);
+            }
+            if (ok) {
+                mma_commit(k_empty(kr.idx));
+                kr.advance();
+            }
+            for (int j = 0; ok && j < n_kv; ++j) {
+                const bool next = j + 1 < n_kv;
+                if (!mbar_wait(v_full(vr.idx), vr.phase, abort)) break;
+                if (next && !mbar_wait(k_full(kr.idx), kr.phase, abort)) break;
+                for (int x = 0; x < 2; ++x) {
+                    if (j >= n_x[x]) continue;
+                    if (!mbar_wait(p_full(x), j & 1, abort)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_pv(x, vr.idx, j > 0);
+                    if (j + 1 < n_x[x]) issue_s(x, kr.idx);
+                    else mma_commit(o_final(x));
+                }
+                if (!ok) break;
                 mma_commit(v_empty(vr.idx));
-                mma_commit(o_done);
                 vr.advance();
+                if (next) {
+                    mma_commit(k_empty(kr.idx));
+                    kr.advance();
+                }
             }
             mma_commit(mmadone);
             mbar_wait_teardown(mmadone, 0);
         }
-    } else if (warp >= 4) {
-        // ------------------------------------------------ rows: norm, softmax, epilogue
-        const int q = warp - 4;                  // lane quarter of tensor memory
+    } else {
+        // ------------------------------------------------ softmax warps of tile x
+        const int x = (warp - 2) >> 2;          // 0: tile A (warps 2-5), 1: tile B (6-9)
+        const int q = warp & 3;                  // lane quarter of tensor memory
         const int row = q * 32 + lane;           // query row of the tile
-        const int qpos = q0 + row;
+        const int qt = 2 * qb + x;
+        const int qpos = qt * kAttBM + row;
+        const int n = n_x[x];
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t swz = static_cast<uint32_t>(row & 7);
-        const uint32_t srow = sq + static_cast<uint32_t>(row) * 128;
-        sg[row] = __bfloat162float(gq[row]);
-        named_bar_sync(1, 128);
+        const uint32_t srow = sq + x * kAttTile + static_cast<uint32_t>(row) * 128;
+        if (x == 0) sg[row] = __bfloat162float(gq[row]);
+        named_bar_sync(1, 256);
         bool ok = warp_wait(q_full, 0, abort);
         if (ok) {
             // Qn * scale * log2(e) in place, bf16 (the swizzled K-major tile layout)
@@ -316,25 +347,19 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                 }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(q_ready);
+            if (lane == 0) mbar_arrive(q_ready(x));
         }
-        const uint32_t obuf = tmem + kAttColO + lane_base;
+        const uint32_t sbuf = tmem + x * 256 + lane_base;
+        const uint32_t obuf = sbuf + kAttColO;
         float m_ref = 0.f, l = 0.f;
-        for (int j = 0; ok && j < n_kv; ++j) {
-            if (!warp_wait(s_full(j & 1), (j >> 1) & 1, abort)) {
+        for (int j = 0; ok && j < n; ++j) {
+            if (!warp_wait(s_full(x), j & 1, abort)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t sbuf = tmem + kAttColS + (j & 1) * kAttBN + lane_base;
-            float s[kAttBN];
-#pragma unroll
-            for (int cc = 0; cc < kAttBN / 32; ++cc) {
-                uint32_t v[32];
-                tmem_ld_32x32(sbuf + cc * 32, v);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(v[i]);
-            }
+            uint32_t v[kAttBN];
+            tmem_ld_32x32_x128(sbuf, v);
             // keys past the sequence end, and after the query when causal
             const int kbase = j * kAttBN;
             int lim = min(kAttBN, a.S - kbase);
@@ -342,15 +367,15 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             if (lim < kAttBN) {
 #pragma unroll
                 for (int i = 0; i < kAttBN; ++i)
-                    if (i >= lim) s[i] = -INFINITY;
+                    if (i >= lim) v[i] = 0xff800000u;   // -inf
             }
             float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int i = 0; i < kAttBN; i += 4) {
-                mx[0] = fmaxf(mx[0], s[i]);
-                mx[1] = fmaxf(mx[1], s[i + 1]);
-                mx[2] = fmaxf(mx[2], s[i + 2]);
-                mx[3] = fmaxf(mx[3], s[i + 3]);
+            for (int i = 0; i < kAttBN; i += 8) {
+                mx[0] = max3f(mx[0], __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+                mx[1] = max3f(mx[1], __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                mx[2] = max3f(mx[2], __uint_as_float(v[i + 4]), __uint_as_float(v[i + 5]));
+                mx[3] = max3f(mx[3], __uint_as_float(v[i + 6]), __uint_as_float(v[i + 7]));
             }
             const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
             float alpha = 1.f;
@@ -365,81 +390,73 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                 l *= alpha;
                 rescale = true;
             }
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint64_t negm = pack_f32x2(-m_ref, -m_ref);
+            uint64_t acc[4] = {0, 0, 0, 0};   // packed partial row sums (0.0f pairs)
+            uint32_t pk[kAttBN / 2];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float p0 = ex2_approx(s[half * 64 + 2 * i] - m_ref);
-                    const float p1 = ex2_approx(s[half * 64 + 2 * i + 1] - m_ref);
-                    ls[i & 3] += p0 + p1;
-                    pk[i] = pack_bf16x2(p0, p1);
-                }
-                tmem_st_32x32(sbuf + half * 32, pk);
+            for (int i = 0; i < kAttBN / 2; ++i) {
+                const uint64_t d = add_f32x2(pack_f32x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
+                                             negm);
+                const float p0 = ex2_approx(lo_f32(d)), p1 = ex2_approx(hi_f32(d));
+                acc[i & 3] = add_f32x2(acc[i & 3], pack_f32x2(p0, p1));
+                pk[i] = pack_bf16x2(p0, p1);
             }
-            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            tmem_st_32x32_x64(sbuf, pk);
+            const uint64_t t = add_f32x2(add_f32x2(acc[0], acc[1]), add_f32x2(acc[2], acc[3]));
+            l += lo_f32(t) + hi_f32(t);
             if (__any_sync(0xffffffffu, rescale)) {
-                // O holds P_0..P_{j-1} V: wait for the last product, then scale.
-                // S_j completed, and it was issued after P_{j-2} V, so o_done is
-                // at most one phase behind: the parity wait is exact.
-                if (!warp_wait(o_done, (j - 1) & 1, abort)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
+                // O holds P_0..P_{j-1} V, complete: S_j was issued after the
+                // last of those products and has completed
 #pragma unroll 1
                 for (int cc = 0; cc < kAttD / 32; ++cc) {
-                    uint32_t v[32];
-                    tmem_ld_32x32(obuf + cc * 32, v);
+                    uint32_t o[32];
+                    tmem_ld_32x32(obuf + cc * 32, o);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-                    tmem_st_32x32(obuf + cc * 32, v);
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st_32x32(obuf + cc * 32, o);
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full(j & 1));
+            if (lane == 0) mbar_arrive(p_full(x));
         }
         // ------------------------------------------------ epilogue: O / l -> bf16 -> TMA store
-        // The last product's completion, from the single-use barrier the MMA
-        // issuer commits after its last instruction: a parity wait on o_done
-        // could be two phases behind here (S_{n-1} is issued before P_{n-2} V).
-        if (ok) ok = warp_wait(mmadone, 0, abort);
-        if (ok) {
+        if (ok && n > 0) ok = warp_wait(o_final(x), 0, abort);
+        if (ok && n > 0) {
             tc_fence_after();
             const float inv_l = 1.f / l;
-            // staging in the Q area (every MMA that read it has completed):
-            // 128-byte swizzle, two 64-column halves
+            // staging in this tile's Q area (every MMA that read it has
+            // completed): 128-byte swizzle, two 64-column halves
 #pragma unroll
             for (int cc = 0; cc < kAttD / 32; ++cc) {
-                uint32_t v[32];
-                tmem_ld_32x32(obuf + cc * 32, v);
+                uint32_t o[32];
+                tmem_ld_32x32(obuf + cc * 32, o);
                 const uint32_t dst = srow + (cc >> 1) * kAttHalf;
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
                     uint32_t o4[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        o4[i] = pack_bf16x2(__uint_as_float(v[8 * t + 2 * i]) * inv_l,
-                                            __uint_as_float(v[8 * t + 2 * i + 1]) * inv_l);
+                        o4[i] = pack_bf16x2(__uint_as_float(o[8 * t + 2 * i]) * inv_l,
+                                            __uint_as_float(o[8 * t + 2 * i + 1]) * inv_l);
                     const uint32_t chunk = static_cast<uint32_t>((cc & 1) * 4 + t);
                     sts128(dst + ((chunk ^ swz) << 4), make_uint4(o4[0], o4[1], o4[2], o4[3]));
                 }
             }
             fence_proxy_async_smem();
         }
-        named_bar_sync(1, 128);
-        if (row == 0 && !*abort) {
-            tma_store_3d(&tmO, sq, h * kAttD, q0, b);
-            tma_store_3d(&tmO, sq + kAttHalf, h * kAttD + 64, q0, b);
+        named_bar_sync(2 + x, 128);
+        if (row == 0 && n > 0 && !*abort) {
+            const uint32_t src = sq + x * kAttTile;
+            tma_store_3d(&tmO, src, h * kAttD, qt * kAttBM, b);
+            tma_store_3d(&tmO, src + kAttHalf, h * kAttD + 64, qt * kAttBM, b);
             bulk_commit_group();
             bulk_wait_group_all();
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 2) {
+    if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kAttTmemCols);
     }

@@ -106,10 +106,10 @@ constexpr int kAttBN = 128;   // keys per tile
 struct AttnLaunch {
     int S;            // sequence length (queries and keys)
     int Hq, group;    // query heads; query heads per key/value head
-    int n_qt;         // query tiles per sequence, ceil(S / 128)
+    int n_qb;         // blocks of 256 query rows per sequence, ceil(S / 256)
     int n_hb;         // Hq * B
     int causal;
-    int grid;         // n_qt * n_hb
+    int grid;         // n_qb * n_hb
     float eps;
     float qscale;     // scale * log2(e), folded into the normalised queries
     int wait_limit_us;
