@@ -91,12 +91,17 @@ __global__ void __launch_bounds__(kHeadsWarps * 32)
 // ------------------------------------------------------- attention kernel
 // One CTA per block of 256 query rows of one head: two 128-row query tiles,
 // A (rows q0 .. q0 + 127) and B (q0 + 128 .. q0 + 255), each with its own
-// score buffer, output accumulator and group of four softmax warps.  The MMA
-// issuer alternates between them, so the tensor cores work on one tile's
-// products while the other tile's softmax runs; both read the same K and V
-// tiles, loaded once.
-constexpr int kAttThreads = 320;    // warp 0 TMA, 1 MMA + TMEM, 2-5 tile A, 6-9 tile B
-constexpr int kAttStages = 2;       // K and V rings
+// score buffer, output accumulator and group of four softmax warps.  One
+// thread issues the MMAs of both, alternating A then B for every key tile,
+// which keeps the two tiles half a period apart: the tensor cores work on
+// one tile's products while the other tile's softmax runs.  (Two issuing
+// threads, one per tile, drift into step with each other, and then both
+// softmaxes run while the tensor pipe idles.)  Both tiles read the same K
+// and V tiles, loaded once: stage j of the ring holds V_j and K_{j+1} (K_0
+// has a barrier of its own), so the issuer waits once and releases once per
+// key tile.
+constexpr int kAttThreads = 320;    // warp 0 TMA, 1 MMA + TMEM, 2-5 softmax A, 6-9 softmax B
+constexpr int kAttStages = 2;       // K and V slots
 constexpr uint32_t kAttTile = kAttBM * kAttD * 2;   // 32 KB: a Q, K or V tile
 constexpr uint32_t kAttHalf = kAttTile / 2;         // 64 columns of a tile (SW128 box)
 constexpr uint32_t kAttOffQ = 0;                    // Q tiles A and B, later the O staging
@@ -104,7 +109,7 @@ constexpr uint32_t kAttOffK = kAttOffQ + 2 * kAttTile;
 constexpr uint32_t kAttOffV = kAttOffK + kAttStages * kAttTile;
 constexpr uint32_t kAttOffG = kAttOffV + kAttStages * kAttTile;   // gq as fp32 [128]
 constexpr uint32_t kAttOffBar = kAttOffG + kAttD * 4;
-constexpr uint32_t kAttNumBars = 18;
+constexpr uint32_t kAttNumBars = 15;
 constexpr uint32_t kAttOffMisc = kAttOffBar + 256;
 constexpr uint32_t kAttSmem = kAttOffMisc + 16 + 1024;   // + alignment slack
 static_assert(kAttNumBars * 8 <= 256, "barrier area");
@@ -127,16 +132,14 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     const uint32_t sq = sbase + kAttOffQ, sk = sbase + kAttOffK, sv = sbase + kAttOffV;
     float* sg = reinterpret_cast<float*>(smem + kAttOffG);
     const uint32_t bar0 = sbase + kAttOffBar;
-    const uint32_t q_full = bar0;
-    auto q_ready = [&](int x) { return bar0 + 8 + 8 * x; };
-    auto k_full = [&](uint32_t i) { return bar0 + 24 + 8 * i; };
-    auto k_empty = [&](uint32_t i) { return bar0 + 40 + 8 * i; };
-    auto v_full = [&](uint32_t i) { return bar0 + 56 + 8 * i; };
-    auto v_empty = [&](uint32_t i) { return bar0 + 72 + 8 * i; };
-    auto s_full = [&](int x) { return bar0 + 88 + 8 * x; };
-    auto p_full = [&](int x) { return bar0 + 104 + 8 * x; };
-    auto o_final = [&](int x) { return bar0 + 120 + 8 * x; };
-    const uint32_t mmadone = bar0 + 136;
+    const uint32_t q_full = bar0, k0_full = bar0 + 8;
+    auto q_ready = [&](int x) { return bar0 + 16 + 8 * x; };
+    auto kv_full = [&](uint32_t i) { return bar0 + 32 + 8 * i; };
+    auto kv_empty = [&](uint32_t i) { return bar0 + 48 + 8 * i; };
+    auto s_full = [&](int x) { return bar0 + 64 + 8 * x; };
+    auto p_full = [&](int x) { return bar0 + 80 + 8 * x; };
+    auto o_final = [&](int x) { return bar0 + 96 + 8 * x; };
+    const uint32_t mmadone = bar0 + 112;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kAttOffMisc);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + kAttOffMisc + 4);
 
@@ -150,17 +153,18 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     const int q0 = qb * 2 * kAttBM;
     const int n_kv_all = (a.S + kAttBN - 1) / kAttBN;
     // key tiles each query tile visits (tile B may lie past the sequence end)
-    int n_x[2];
-#pragma unroll
-    for (int x = 0; x < 2; ++x) {
+    auto tiles_of = [&](int x) {
         const int qt = 2 * qb + x;
-        n_x[x] = q0 + x * kAttBM >= a.S ? 0 : a.causal ? min(qt + 1, n_kv_all) : n_kv_all;
-    }
-    const int n_kv = max(n_x[0], n_x[1]);
+        return q0 + x * kAttBM >= a.S ? 0 : a.causal ? min(qt + 1, n_kv_all) : n_kv_all;
+    };
+    const int n_a = tiles_of(0), n_b = tiles_of(1);
+    auto n_x = [&](int x) { return x ? n_b : n_a; };
+    const int n_kv = max(n_a, n_b);
 
     if (threadIdx.x == 0) {
         if (blockDim.x != kAttThreads) atomicCAS(&g_status, 0, kStatusInternal);
         mbar_init(q_full, 1);
+        mbar_init(k0_full, 1);
         for (int x = 0; x < 2; ++x) {
             mbar_init(q_ready(x), 4);   // one elected lane per softmax warp
             mbar_init(s_full(x), 1);
@@ -168,10 +172,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             mbar_init(o_final(x), 1);
         }
         for (int i = 0; i < kAttStages; ++i) {
-            mbar_init(k_full(i), 1);
-            mbar_init(k_empty(i), 1);
-            mbar_init(v_full(i), 1);
-            mbar_init(v_empty(i), 1);
+            mbar_init(kv_full(i), 1);
+            mbar_init(kv_empty(i), 1);
         }
         mbar_init(mmadone, 1);
         abort[0] = blockDim.x != kAttThreads;
@@ -207,95 +209,98 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                 tma_load_3d(sq + x * kAttTile + kAttHalf, &tmQ, q_full, h * kAttD + 64,
                             q0 + x * kAttBM, b, once);
             }
-            Ring kr(kAttStages), vr(kAttStages);
-            int k_issued = 0, v_issued = 0;
+            mbar_arrive_expect_tx(k0_full, kAttTile);
+            tma_load_3d(sk, &tmK, k0_full, c * kAttD, 0, b, keep);
+            tma_load_3d(sk + kAttHalf, &tmK, k0_full, c * kAttD + 64, 0, b, keep);
+            int issued = 0;
             for (int j = 0; j < n_kv; ++j) {
-                if (!mbar_wait(k_empty(kr.idx), kr.phase ^ 1, abort)) break;
-                mbar_arrive_expect_tx(k_full(kr.idx), kAttTile);
-                const uint32_t kd = sk + kr.idx * kAttTile;
-                tma_load_3d(kd, &tmK, k_full(kr.idx), c * kAttD, j * kAttBN, b, keep);
-                tma_load_3d(kd + kAttHalf, &tmK, k_full(kr.idx), c * kAttD + 64, j * kAttBN, b, keep);
-                kr.advance();
-                ++k_issued;
-                if (!mbar_wait(v_empty(vr.idx), vr.phase ^ 1, abort)) break;
-                mbar_arrive_expect_tx(v_full(vr.idx), kAttTile);
-                const uint32_t vd = sv + vr.idx * kAttTile;
+                const uint32_t st = j & 1;
+                // V slot j & 1 held V_{j-2} and K slot (j+1) & 1 held K_{j-1};
+                // both are released by the issuers' commits after key tile
+                // j - 2 (for j = 1: after S(0), which read K_0)
+                if (j >= 1) {
+                    const uint32_t par = (j & 1) ? ((j - 1) >> 1) & 1 : ((j >> 1) - 1) & 1;
+                    if (!mbar_wait(kv_empty(st), par, abort)) break;
+                }
+                const bool kn = j + 1 < n_kv;
+                mbar_arrive_expect_tx(kv_full(st), kn ? 2 * kAttTile : kAttTile);
+                const uint32_t vd = sv + st * kAttTile;
                 // four boxes of [64 keys][64 dims]: box (kk, n) at (2 kk + n) * 8 KB
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk)
 #pragma unroll
                     for (int n = 0; n < 2; ++n)
-                        tma_load_3d(vd + (2 * kk + n) * (kAttTile / 4), &tmV, v_full(vr.idx),
+                        tma_load_3d(vd + (2 * kk + n) * (kAttTile / 4), &tmV, kv_full(st),
                                     c * kAttD + n * 64, j * kAttBN + kk * 64, b, keep);
-                vr.advance();
-                ++v_issued;
+                if (kn) {
+                    const uint32_t kd = sk + ((j + 1) & 1) * kAttTile;
+                    tma_load_3d(kd, &tmK, kv_full(st), c * kAttD, (j + 1) * kAttBN, b, keep);
+                    tma_load_3d(kd + kAttHalf, &tmK, kv_full(st), c * kAttD + 64, (j + 1) * kAttBN, b,
+                                keep);
+                }
+                ++issued;
             }
             // never leave with copies still landing in shared memory
             mbar_wait_teardown(q_full, 0);
-            for (int i = k_issued > kAttStages ? k_issued - kAttStages : 0; i < k_issued; ++i)
-                mbar_wait_teardown(k_full(i % kAttStages), (i / kAttStages) & 1);
-            for (int i = v_issued > kAttStages ? v_issued - kAttStages : 0; i < v_issued; ++i)
-                mbar_wait_teardown(v_full(i % kAttStages), (i / kAttStages) & 1);
+            mbar_wait_teardown(k0_full, 0);
+            for (int i = issued > kAttStages ? issued - kAttStages : 0; i < issued; ++i)
+                mbar_wait_teardown(kv_full(i & 1), (i >> 1) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(kAttBM, kAttBN, false, false);
             constexpr uint32_t idesc_o = idesc_bf16_f32(kAttBM, kAttD, false, true);
+            // Descriptors are built once; a step adds its byte offset >> 4 to
+            // the start-address field (every tile lies below 256 KB, so the
+            // 14-bit field never carries).
+            const uint64_t dq0 = sdesc_sw128(sq, 16, 1024), dq1 = sdesc_sw128(sq + kAttTile, 16, 1024);
+            const uint64_t dk0 = sdesc_sw128(sk, 16, 1024), dk1 = sdesc_sw128(sk + kAttTile, 16, 1024);
+            const uint64_t dv0 = sdesc_sw128(sv, kAttTile / 4, 1024);
+            const uint64_t dv1 = sdesc_sw128(sv + kAttTile, kAttTile / 4, 1024);
             // S_x = Qn_x K^T into tile x's score buffer: A and B K-major, 8 steps of 16 dims
             auto issue_s = [&](int x, uint32_t kslot) {
                 const uint32_t d = tmem + x * 256;
-                const uint32_t qa = sq + x * kAttTile, kb = sk + kslot * kAttTile;
+                const uint64_t a0 = x ? dq1 : dq0, b0 = kslot ? dk1 : dk0;
 #pragma unroll
                 for (int kk = 0; kk < kAttD / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kAttHalf + (kk & 3) * 32;
-                    mma_bf16_ss(d, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                                idesc_s, kk > 0);
+                    const uint64_t off = ((kk >> 2) * kAttHalf + (kk & 3) * 32) >> 4;
+                    mma_bf16_ss(d, a0 + off, b0 + off, idesc_s, kk > 0);
                 }
                 mma_commit(s_full(x));
             };
             // O_x += P_x V: A = P from tensor memory (keys 16kk.. in columns
             // 8kk..), B = V MN-major (dims contiguous), 8 steps of 16 keys
             auto issue_pv = [&](int x, uint32_t vslot, bool acc) {
-                const uint32_t pa = tmem + x * 256, vb = sv + vslot * kAttTile;
+                const uint32_t pa = tmem + x * 256;
+                const uint64_t b0 = vslot ? dv1 : dv0;
 #pragma unroll
                 for (int kk = 0; kk < kAttBN / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * (kAttTile / 2) + (kk & 3) * 2048;
-                    mma_bf16_ts(pa + kAttColO, pa + kk * 8, sdesc_sw128(vb + off, kAttTile / 4, 1024),
-                                idesc_o, acc || kk > 0);
+                    const uint64_t off = ((kk >> 2) * (kAttTile / 2) + (kk & 3) * 2048) >> 4;
+                    mma_bf16_ts(pa + kAttColO, pa + kk * 8, b0 + off, idesc_o, acc || kk > 0);
                 }
             };
-            Ring kr(kAttStages), vr(kAttStages);
-            bool ok = n_kv > 0 && mbar_wait(k_full(kr.idx), kr.phase, abort);
+            bool ok = mbar_wait(k0_full, 0, abort);
             for (int x = 0; ok && x < 2; ++x) {
-                if (n_x[x] == 0) continue;
+                if (n_x(x) == 0) continue;
                 if (!mbar_wait(q_ready(x), 0, abort)) { ok = false; break; }
                 tc_fence_after();
-                issue_s(x, kr.idx);
+                issue_s(x, 0);
             }
-            if (ok) {
-                mma_commit(k_empty(kr.idx));
-                kr.advance();
-            }
+            if (ok) mma_commit(kv_empty(1));   // K_0 read: "key tile -1" of stage 1
             for (int j = 0; ok && j < n_kv; ++j) {
-                const bool next = j + 1 < n_kv;
-                if (!mbar_wait(v_full(vr.idx), vr.phase, abort)) break;
-                if (next && !mbar_wait(k_full(kr.idx), kr.phase, abort)) break;
+                const uint32_t st = j & 1;
+                if (!mbar_wait(kv_full(st), (j >> 1) & 1, abort)) break;
                 for (int x = 0; x < 2; ++x) {
-                    if (j >= n_x[x]) continue;
+                    if (j >= n_x(x)) continue;
                     if (!mbar_wait(p_full(x), j & 1, abort)) { ok = false; break; }
                     tc_fence_after();
-                    issue_pv(x, vr.idx, j > 0);
-                    if (j + 1 < n_x[x]) issue_s(x, kr.idx);
+                    issue_pv(x, st, j > 0);
+                    if (j + 1 < n_x(x)) issue_s(x, (j + 1) & 1);
                     else mma_commit(o_final(x));
                 }
                 if (!ok) break;
-                mma_commit(v_empty(vr.idx));
-                vr.advance();
-                if (next) {
-                    mma_commit(k_empty(kr.idx));
-                    kr.advance();
-                }
+                mma_commit(kv_empty(st));
             }
             mma_commit(mmadone);
             mbar_wait_teardown(mmadone, 0);
@@ -307,7 +312,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         const int row = q * 32 + lane;           // query row of the tile
         const int qt = 2 * qb + x;
         const int qpos = qt * kAttBM + row;
-        const int n = n_x[x];
+        const int n = n_x(x);
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t swz = static_cast<uint32_t>(row & 7);
         const uint32_t srow = sq + x * kAttTile + static_cast<uint32_t>(row) * 128;
