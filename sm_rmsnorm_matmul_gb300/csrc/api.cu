@@ -778,8 +778,8 @@ int rmsnorm_heads(const void* X, int64_t ldx, const void* g, void* Y, int64_t ld
     DeviceInfo d;
     rc = current_device(&dev, &d);
     if (rc != RMM_OK) return rc;
-    return rmm::launch_rmsnorm_heads(X, ldx, g, Y, ldy, T, static_cast<int>(H), static_cast<int>(D),
-                                     eps, stream) == cudaSuccess
+    return rmm::launch_rmsnorm_heads(X, ldx, g, nullptr, Y, ldy, T, static_cast<int>(H),
+                                     static_cast<int>(D), eps, stream) == cudaSuccess
                ? RMM_OK
                : RMM_ERR_LAUNCH;
 }
@@ -818,8 +818,9 @@ int qknorm_attention(const void* Q, int64_t ldq, const void* K, int64_t ldk, con
         !map_3d(&tmK, khat, B, S, Hkv * D, Hkv * D, rmm::kAttBN) ||
         !map_3d(&tmV, V, B, S, Hkv * D, ldv, 64) || !map_3d(&tmO, O, B, S, Hq * D, ldo, rmm::kAttBM))
         return RMM_ERR_INTERNAL;
-    // the keys once: Kn = RMSNorm(K; gk) per head, into the workspace
-    if (rmm::launch_rmsnorm_heads(K, ldk, gk, khat, Hkv * D, B * S, static_cast<int>(Hkv),
+    // the keys once: RMSNorm(K; gk) * gq per head, into the workspace (the
+    // query gain moves onto the keys; the query rows keep only their 1/RMS)
+    if (rmm::launch_rmsnorm_heads(K, ldk, gk, gq, khat, Hkv * D, B * S, static_cast<int>(Hkv),
                                   static_cast<int>(D), eps, stream) != cudaSuccess)
         return RMM_ERR_LAUNCH;
     rmm::AttnLaunch a{};
@@ -834,7 +835,7 @@ int qknorm_attention(const void* Q, int64_t ldq, const void* K, int64_t ldk, con
     const double sc = scale > 0.f ? static_cast<double>(scale) : 1.0 / std::sqrt(static_cast<double>(D));
     a.qscale = static_cast<float>(sc * 1.4426950408889634);   // log2(e)
     a.wait_limit_us = g_wait_limit_us.load();
-    return rmm::launch_qknorm_attention(tmQ, tmK, tmV, tmO, gq, a, stream) == cudaSuccess
+    return rmm::launch_qknorm_attention(tmQ, tmK, tmV, tmO, a, stream) == cudaSuccess
                ? RMM_OK
                : RMM_ERR_LAUNCH;
 }

@@ -6,17 +6,22 @@
 // key/value heads.  Two kernels:
 //
 //   rmsnorm_heads_kernel    normalises every key head once (memory-bound; one
-//                           warp per head row), into a bf16 workspace;
+//                           warp per head row), into a bf16 workspace, with
+//                           the query gain gq folded in: Kg = bf16(Kn * gq);
 //   qknorm_attention_kernel one CTA per 256 query rows of one head (two
-//                           128-row tiles): normalises the query tiles in shared
-//                           memory (with scale * log2(e) folded in), then for
-//                           each 128-key tile S = Qn Kn^T and O += P V on the
-//                           tensor cores (tcgen05, accumulators in tensor
-//                           memory), with the online softmax between them.
+//                           128-row tiles): for each 128-key tile S' = Q Kg^T
+//                           (the raw bf16 queries) and O += P V on the tensor
+//                           cores (tcgen05, accumulators in tensor memory),
+//                           with the online softmax between them.
 //
-// Normalising each key once, not once per query tile that reads it, is the
-// choice for GB300: a key tile is read by S/128 query tiles of every head in
-// its group, and the workspace round trip costs two reads of K.
+// The query normalisation is a row scale: <Qn_i, Kn_j> = r_i <Q_i * gq, Kn_j>
+// = r_i <Q_i, Kg_j> with r_i = 1 / sqrt(mean(Q_i^2) + eps), so the kernel
+// multiplies row i of S' by r_i * scale * log2(e) inside the softmax (one
+// fused multiply-add that also subtracts the running maximum), and the MMA
+// reads the query tile as it was loaded.  Normalising each key once, not
+// once per query tile that reads it, is the choice for GB300: a key tile is
+// read by S/128 query tiles of every head in its group, and the workspace
+// round trip costs two reads of K.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -44,13 +49,15 @@ struct Ring {   // index and phase of a circular buffer of mbarrier-guarded slot
 // ------------------------------------------------------------ key rmsnorm
 constexpr int kHeadsWarps = 8;
 
-// Y[t,h,:] = bf16(X[t,h,:] * g * rsqrt(mean(X[t,h,:]^2) + eps)), one warp per
-// (t, h).  D is a multiple of 8 and at most 256: lane l holds elements
-// [8l, 8l + 8) when 8l < D.
+// Y[t,h,:] = bf16(X[t,h,:] * g * g2 * rsqrt(mean(X[t,h,:]^2) + eps)), one
+// warp per (t, h); g2 is an optional second gain (nullptr: none), the
+// products in fp32 and one rounding.  D is a multiple of 8 and at most 256:
+// lane l holds elements [8l, 8l + 8) when 8l < D.
 __global__ void __launch_bounds__(kHeadsWarps * 32)
     rmsnorm_heads_kernel(const __nv_bfloat16* __restrict__ X, int64_t ldx,
-                         const __nv_bfloat16* __restrict__ g, __nv_bfloat16* __restrict__ Y,
-                         int64_t ldy, int64_t T, int H, int D, float eps) {
+                         const __nv_bfloat16* __restrict__ g, const __nv_bfloat16* __restrict__ g2,
+                         __nv_bfloat16* __restrict__ Y, int64_t ldy, int64_t T, int H, int D,
+                         float eps) {
     // X may be the output of the previous kernel on the stream
     grid_dep_wait();
     grid_dep_launch();
@@ -78,11 +85,19 @@ __global__ void __launch_bounds__(kHeadsWarps * 32)
     const float r = rsqrtf(ss / static_cast<float>(D) + eps);
     if (active) {
         const uint4 gu = __ldg(reinterpret_cast<const uint4*>(g + lane * 8));
-        const uint32_t gw[4] = {gu.x, gu.y, gu.z, gu.w};
+        float gf[8] = {bf16lo(gu.x), bf16hi(gu.x), bf16lo(gu.y), bf16hi(gu.y),
+                       bf16lo(gu.z), bf16hi(gu.z), bf16lo(gu.w), bf16hi(gu.w)};
+        if (g2 != nullptr) {
+            const uint4 hu = __ldg(reinterpret_cast<const uint4*>(g2 + lane * 8));
+            const float hf[8] = {bf16lo(hu.x), bf16hi(hu.x), bf16lo(hu.y), bf16hi(hu.y),
+                                 bf16lo(hu.z), bf16hi(hu.z), bf16lo(hu.w), bf16hi(hu.w)};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) gf[i] *= hf[i];
+        }
         uint32_t out[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            out[i] = pack_bf16x2(v[2 * i] * bf16lo(gw[i]) * r, v[2 * i + 1] * bf16hi(gw[i]) * r);
+            out[i] = pack_bf16x2(v[2 * i] * gf[2 * i] * r, v[2 * i + 1] * gf[2 * i + 1] * r);
         *reinterpret_cast<uint4*>(Y + t * ldy + h * D + lane * 8) =
             make_uint4(out[0], out[1], out[2], out[3]);
     }
@@ -107,8 +122,7 @@ constexpr uint32_t kAttHalf = kAttTile / 2;         // 64 columns of a tile (SW1
 constexpr uint32_t kAttOffQ = 0;                    // Q tiles A and B, later the O staging
 constexpr uint32_t kAttOffK = kAttOffQ + 2 * kAttTile;
 constexpr uint32_t kAttOffV = kAttOffK + kAttStages * kAttTile;
-constexpr uint32_t kAttOffG = kAttOffV + kAttStages * kAttTile;   // gq as fp32 [128]
-constexpr uint32_t kAttOffBar = kAttOffG + kAttD * 4;
+constexpr uint32_t kAttOffBar = kAttOffV + kAttStages * kAttTile;
 constexpr uint32_t kAttNumBars = 15;
 constexpr uint32_t kAttOffMisc = kAttOffBar + 256;
 constexpr uint32_t kAttSmem = kAttOffMisc + 16 + 1024;   // + alignment slack
@@ -122,18 +136,15 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     qknorm_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                             const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV,
-                            const __grid_constant__ CUtensorMap tmO,
-                            const __nv_bfloat16* __restrict__ gq, AttnLaunch a) {
+                            const __grid_constant__ CUtensorMap tmO, AttnLaunch a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sq = sbase + kAttOffQ, sk = sbase + kAttOffK, sv = sbase + kAttOffV;
-    float* sg = reinterpret_cast<float*>(smem + kAttOffG);
     const uint32_t bar0 = sbase + kAttOffBar;
     const uint32_t q_full = bar0, k0_full = bar0 + 8;
-    auto q_ready = [&](int x) { return bar0 + 16 + 8 * x; };
     auto kv_full = [&](uint32_t i) { return bar0 + 32 + 8 * i; };
     auto kv_empty = [&](uint32_t i) { return bar0 + 48 + 8 * i; };
     auto s_full = [&](int x) { return bar0 + 64 + 8 * x; };
@@ -166,7 +177,6 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         mbar_init(q_full, 1);
         mbar_init(k0_full, 1);
         for (int x = 0; x < 2; ++x) {
-            mbar_init(q_ready(x), 4);   // one elected lane per softmax warp
             mbar_init(s_full(x), 1);
             mbar_init(p_full(x), 4);
             mbar_init(o_final(x), 1);
@@ -280,13 +290,10 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                     mma_bf16_ts(pa + kAttColO, pa + kk * 8, b0 + off, idesc_o, acc || kk > 0);
                 }
             };
-            bool ok = mbar_wait(k0_full, 0, abort);
-            for (int x = 0; ok && x < 2; ++x) {
-                if (n_x(x) == 0) continue;
-                if (!mbar_wait(q_ready(x), 0, abort)) { ok = false; break; }
-                tc_fence_after();
-                issue_s(x, 0);
-            }
+            bool ok = mbar_wait(k0_full, 0, abort) && mbar_wait(q_full, 0, abort);
+            if (ok) tc_fence_after();
+            for (int x = 0; ok && x < 2; ++x)
+                if (n_x(x) > 0) issue_s(x, 0);
             if (ok) mma_commit(kv_empty(1));   // K_0 read: "key tile -1" of stage 1
             for (int j = 0; ok && j < n_kv; ++j) {
                 const uint32_t st = j & 1;
@@ -316,12 +323,11 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t swz = static_cast<uint32_t>(row & 7);
         const uint32_t srow = sq + x * kAttTile + static_cast<uint32_t>(row) * 128;
-        if (x == 0) sg[row] = __bfloat162float(gq[row]);
-        named_bar_sync(1, 256);
         bool ok = warp_wait(q_full, 0, abort);
+        // the row's scale r * scale * log2(e) (the query tile is only read:
+        // the first products run on it meanwhile)
+        float ss[4] = {0.f, 0.f, 0.f, 0.f};
         if (ok) {
-            // Qn * scale * log2(e) in place, bf16 (the swizzled K-major tile layout)
-            float ss = 0.f;
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
@@ -330,30 +336,13 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        ss = fmaf(bf16lo(w[i]), bf16lo(w[i]), ss);
-                        ss = fmaf(bf16hi(w[i]), bf16hi(w[i]), ss);
+                        ss[i] = fmaf(bf16lo(w[i]), bf16lo(w[i]), ss[i]);
+                        ss[i] = fmaf(bf16hi(w[i]), bf16hi(w[i]), ss[i]);
                     }
                 }
-            const float f = rsqrtf(ss * (1.f / kAttD) + a.eps) * a.qscale;
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    const uint32_t addr = srow + hf * kAttHalf + ((cc ^ swz) << 4);
-                    const uint4 u = lds128(addr);
-                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-                    const float* gg = sg + hf * 64 + cc * 8;
-                    uint32_t o4[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        o4[i] = pack_bf16x2(bf16lo(w[i]) * gg[2 * i] * f,
-                                            bf16hi(w[i]) * gg[2 * i + 1] * f);
-                    sts128(addr, make_uint4(o4[0], o4[1], o4[2], o4[3]));
-                }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(q_ready(x));
         }
+        const float rc = rsqrtf(((ss[0] + ss[1]) + (ss[2] + ss[3])) * (1.f / kAttD) + a.eps) * a.qscale;
+        const uint64_t rc2 = pack_f32x2(rc, rc);
         const uint32_t sbuf = tmem + x * 256 + lane_base;
         const uint32_t obuf = sbuf + kAttColO;
         float m_ref = 0.f, l = 0.f;
@@ -382,7 +371,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                 mx[2] = max3f(mx[2], __uint_as_float(v[i + 4]), __uint_as_float(v[i + 5]));
                 mx[3] = max3f(mx[3], __uint_as_float(v[i + 6]), __uint_as_float(v[i + 7]));
             }
-            const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            // rc > 0: the maximum of the scaled scores is rc times the maximum
+            const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * rc;
             float alpha = 1.f;
             bool rescale = false;
             if (j == 0) {
@@ -400,8 +390,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             uint32_t pk[kAttBN / 2];
 #pragma unroll
             for (int i = 0; i < kAttBN / 2; ++i) {
-                const uint64_t d = add_f32x2(pack_f32x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
-                                             negm);
+                const uint64_t d = fma_f32x2(pack_f32x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
+                                             rc2, negm);
                 const float p0 = ex2_approx(lo_f32(d)), p1 = ex2_approx(hi_f32(d));
                 acc[i & 3] = add_f32x2(acc[i & 3], pack_f32x2(p0, p1));
                 pk[i] = pack_bf16x2(p0, p1);
@@ -456,7 +446,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             tma_store_3d(&tmO, src, h * kAttD, qt * kAttBM, b);
             tma_store_3d(&tmO, src + kAttHalf, h * kAttD + 64, qt * kAttBM, b);
             bulk_commit_group();
-            bulk_wait_group_all();
+            bulk_wait_group_read<0>();   // the staging area is read; the writes complete on their own
         }
     }
     tc_fence_before();
@@ -487,21 +477,21 @@ cudaError_t launch_pdl(void (*kern)(Args...), int grid, int block, size_t smem, 
 
 size_t attn_smem_bytes() { return kAttSmem; }
 
-cudaError_t launch_rmsnorm_heads(const void* X, int64_t ldx, const void* g, void* Y, int64_t ldy,
-                                 int64_t T, int H, int D, float eps, cudaStream_t s) {
+cudaError_t launch_rmsnorm_heads(const void* X, int64_t ldx, const void* g, const void* g2, void* Y,
+                                 int64_t ldy, int64_t T, int H, int D, float eps, cudaStream_t s) {
     const int64_t items = T * H;
     if (items <= 0) return cudaSuccess;
     const int64_t grid = (items + kHeadsWarps - 1) / kHeadsWarps;
     if (grid > INT32_MAX) return cudaErrorInvalidValue;
     return launch_pdl(rmsnorm_heads_kernel, static_cast<int>(grid), kHeadsWarps * 32, 0, s,
                       static_cast<const __nv_bfloat16*>(X), ldx,
-                      static_cast<const __nv_bfloat16*>(g), static_cast<__nv_bfloat16*>(Y), ldy, T,
-                      H, D, eps);
+                      static_cast<const __nv_bfloat16*>(g), static_cast<const __nv_bfloat16*>(g2),
+                      static_cast<__nv_bfloat16*>(Y), ldy, T, H, D, eps);
 }
 
 cudaError_t launch_qknorm_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                     const CUtensorMap& tmV, const CUtensorMap& tmO,
-                                    const void* gq, const AttnLaunch& a, cudaStream_t s) {
+                                    const AttnLaunch& a, cudaStream_t s) {
     // the shared-memory limit is a per-device attribute of the function
     static std::atomic<bool> attr_set[64];
     int dev = 0;
@@ -514,8 +504,7 @@ cudaError_t launch_qknorm_attention(const CUtensorMap& tmQ, const CUtensorMap& t
         if (e != cudaSuccess) return e;
         attr_set[dev].store(true);
     }
-    return launch_pdl(qknorm_attention_kernel, a.grid, kAttThreads, kAttSmem, s, tmQ, tmK, tmV, tmO,
-                      static_cast<const __nv_bfloat16*>(gq), a);
+    return launch_pdl(qknorm_attention_kernel, a.grid, kAttThreads, kAttSmem, s, tmQ, tmK, tmV, tmO, a);
 }
 
 cudaError_t attn_read_and_clear_status(int* out) {

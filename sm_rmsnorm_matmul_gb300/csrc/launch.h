@@ -111,18 +111,19 @@ struct AttnLaunch {
     int causal;
     int grid;         // n_qb * n_hb
     float eps;
-    float qscale;     // scale * log2(e), folded into the normalised queries
+    float qscale;     // scale * log2(e), applied with each query row's 1/RMS to its scores
     int wait_limit_us;
 };
 
-// Y[t,h,:] = RMSNorm(X[t,h,:]; g, eps) for T rows of H heads of D (8..256).
-cudaError_t launch_rmsnorm_heads(const void* X, int64_t ldx, const void* g, void* Y, int64_t ldy,
-                                 int64_t T, int H, int D, float eps, cudaStream_t s);
-// tmQ, tmK (normalised keys), tmV: 3-D maps [B][S][heads*128] read in boxes
-// of [128 rows][64] (V: [64][64]); tmO: the same geometry as tmQ, stored.
+// Y[t,h,:] = RMSNorm(X[t,h,:]; g, eps) * g2 for T rows of H heads of D
+// (8..256); g2 may be nullptr (no second gain).
+cudaError_t launch_rmsnorm_heads(const void* X, int64_t ldx, const void* g, const void* g2, void* Y,
+                                 int64_t ldy, int64_t T, int H, int D, float eps, cudaStream_t s);
+// tmQ, tmK (normalised keys times gq), tmV: 3-D maps [B][S][heads*128] read
+// in boxes of [128 rows][64] (V: [64][64]); tmO: the same geometry as tmQ, stored.
 cudaError_t launch_qknorm_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                     const CUtensorMap& tmV, const CUtensorMap& tmO,
-                                    const void* gq, const AttnLaunch& a, cudaStream_t s);
+                                    const AttnLaunch& a, cudaStream_t s);
 size_t attn_smem_bytes();
 // The attention translation unit's own status word (as read_and_clear_status).
 cudaError_t attn_read_and_clear_status(int* out);

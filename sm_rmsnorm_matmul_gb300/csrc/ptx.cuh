@@ -467,6 +467,12 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
+// Two fp32 fused multiply-adds in one instruction (a * b + c, pairwise).
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
 __device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
     return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
 }

@@ -1,23 +1,26 @@
 """QK-normalised attention on the GPU against the fp64 oracle, through the C ABI.
 
-The device rounds the normalised queries (with scale * log2(e) folded in) and
-the normalised keys to bf16 before the tensor cores.  The reference applies
-the same two roundings to the oracle's own RMSNorm (fp64) and then runs the
-oracle's fp64 attention with base-2 exponentials (scale ln 2), so that what is
-left to compare is the device's softmax and products.  What remains on the
-device side, per output element, and the bound used here:
+The device multiplies the raw bf16 queries with keys normalised once and
+multiplied by the query gain, Kg = bf16(RMSNorm(K; gk) * gq) (the only
+operand rounding), and scales each query row's scores by its 1/RMS times
+scale * log2(e) in fp32.  The reference applies the same rounding to the
+oracle's own RMSNorm (fp64), takes the queries as Q * r * scale * log2(e)
+unrounded, and runs the oracle's fp64 attention with base-2 exponentials
+(scale ln 2), so that what is left to compare is the device's softmax and
+products.  What remains on the device side, per output element, and the
+bound used here:
 
   * P rounded to bf16 (relative 2^-9 per weight), ex2.approx (relative ~2^-22),
-    fp32 sums over at most a few thousand keys (~2^-12), and the rare element
-    of the bf16 operands whose fp32 statistic put it on the other side of a
-    rounding boundary: together below 2^-8 * sum_j p_j |v_jd|;
+    fp32 scores and sums, and the rare key element whose fp32 statistic put
+    it on the other side of a rounding boundary: together below
+    2^-8 * sum_j p_j |v_jd|;
   * O rounded to bf16 once: 2^-9 |o|, taken as 2^-8 |o|.
 
   |O - O_ref| <= 2^-8 * sum_j p_j |v_jd| + 2^-8 |O_ref| + 1e-5
 
 sum_j p_j |v_jd| is the oracle's attention with |V| as the values.  A second
 check compares with the fully exact oracle (no rounding anywhere) under the
-first-order bound of the two operand roundings.
+first-order bound of the key rounding.
 """
 import math
 
@@ -49,16 +52,18 @@ def bf16_round(x):
     return torch.from_numpy(np.ascontiguousarray(x)).to(torch.float32).to(torch.bfloat16).double().numpy()
 
 
-def references(Q, K, V, gq, gk, eps, causal, qpos=None):
+def references(Q, K, V, gq, gk, eps, causal, qpos=None, scale=None):
     B, S, Hq, D = Q.shape
     Hkv = K.shape[2]
-    qn = oracle.rmsnorm(Q.reshape(-1, D), gq, eps).reshape(B, S, Hq, D)
+    c = (1.0 / math.sqrt(D) if scale is None else scale) * LOG2E
+    qr = oracle.rmsnorm(Q.reshape(-1, D), np.ones(D), eps).reshape(B, S, Hq, D)   # Q * r
     kn = oracle.rmsnorm(K.reshape(-1, D), gk, eps).reshape(B, S, Hkv, D)
-    qd = bf16_round(qn * (LOG2E / math.sqrt(D)))
-    kd = bf16_round(kn)
+    qd = qr * c
+    kd = bf16_round(kn * oracle.to_f64(gq))
     Vf = oracle.to_f64(V)
     ref = oracle.attention(qd, kd, Vf, LN2, causal=causal, qpos=qpos)
     wabs = oracle.attention(qd, kd, np.abs(Vf), LN2, causal=causal, qpos=qpos)
+    qn = qr * oracle.to_f64(gq)
     return ref, wabs, qn, kn
 
 
@@ -72,10 +77,10 @@ def assert_attention_close(O, Q, K, V, gq, gk, eps, causal, what, qpos=None):
     bad = ~(err <= tol)   # NaN fails
     assert not bad.any(), (f"{what}: {int(bad.sum())} of {ref.size} outside the bound, "
                            f"max err {float(np.nanmax(err)):.3e}")
-    # the exact oracle (no rounding): operand roundings move every score by at
-    # most 2^-8 * scale * sum_d |qn_d kn_d| (relative 2^-9 on each operand);
-    # to first order the output moves by at most twice the largest such
-    # shift times sum_j p_j |v_jd - o_d| <= 2 * sum_j p_j |v_jd|
+    # the exact oracle (no rounding): the key rounding moves every score by at
+    # most 2^-9 * scale * sum_d |qn_d kn_d| (taken as 2^-8 below); to first
+    # order the output moves by at most twice the largest such shift times
+    # sum_j p_j |v_jd - o_d| <= 2 * sum_j p_j |v_jd|
     exact = oracle.qknorm_attention(Q, K, V, gq, gk, eps, causal=causal, qpos=qpos)
     D = Q.shape[3]
     rep = Q.shape[2] // K.shape[2]
@@ -158,12 +163,7 @@ def test_explicit_scale_and_eps(rmm):
     Qd, Kd, Vd = inputs.split_qkv(qkv.cuda(), B, S, Hq, Hkv, D)
     O = rmm.qknorm_attention(Qd, Kd, Vd, gq.cuda(), gk.cuda(), 0.25, scale=1.0 / 16, causal=False)
     torch.cuda.synchronize()
-    qn = oracle.rmsnorm(Q.reshape(-1, D), gq, 0.25).reshape(B, S, Hq, D)
-    kn = oracle.rmsnorm(K.reshape(-1, D), gk, 0.25).reshape(B, S, Hkv, D)
-    qd = bf16_round(qn * (LOG2E / 16))
-    kd = bf16_round(kn)
-    ref = oracle.attention(qd, kd, oracle.to_f64(V), LN2, causal=False)
-    wabs = oracle.attention(qd, kd, np.abs(oracle.to_f64(V)), LN2, causal=False)
+    ref, wabs, _, _ = references(Q, K, V, gq, gk, 0.25, False, scale=1.0 / 16)
     err = np.abs(oracle.to_f64(O.cpu()) - ref)
     assert (err <= 2.0 ** -8 * wabs + 2.0 ** -8 * np.abs(ref) + 1e-5).all()
 
