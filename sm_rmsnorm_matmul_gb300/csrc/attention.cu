@@ -106,16 +106,17 @@ __global__ void __launch_bounds__(kHeadsWarps * 32)
 // ------------------------------------------------------- attention kernel
 // One CTA per block of 256 query rows of one head: two 128-row query tiles,
 // A (rows q0 .. q0 + 127) and B (q0 + 128 .. q0 + 255), each with its own
-// score buffer, output accumulator and group of four softmax warps.  One
-// thread issues the MMAs of both, alternating A then B for every key tile,
-// which keeps the two tiles half a period apart: the tensor cores work on
-// one tile's products while the other tile's softmax runs.  (Two issuing
-// threads, one per tile, drift into step with each other, and then both
-// softmaxes run while the tensor pipe idles.)  Both tiles read the same K
-// and V tiles, loaded once: stage j of the ring holds V_j and K_{j+1} (K_0
-// has a barrier of its own), so the issuer waits once and releases once per
-// key tile.
-constexpr int kAttThreads = 320;    // warp 0 TMA, 1 MMA + TMEM, 2-5 softmax A, 6-9 softmax B
+// score buffer, output accumulator, group of four softmax warps and MMA
+// issuing thread.  The issuers take turns, A then B for every key tile
+// (a pair of turn barriers): that keeps the two tiles half a period apart, so
+// the tensor cores work on one tile's products while the other tile's
+// softmax runs, and each issuer does its waits and releases while the other
+// one issues (an issuing thread stalls whenever the tensor pipe's queue is
+// full, so a single issuer's own waits leave the pipe idle).  Without the
+// turns the two issuers drift into step and both softmaxes run while the
+// pipe idles.  Both tiles read the same K and V tiles, loaded once: stage j
+// of the ring holds V_j and K_{j+1} (K_0 has a barrier of its own).
+constexpr int kAttThreads = 352;    // warp 0 TMA, 1 MMA A + TMEM, 2-5 softmax A, 6-9 softmax B, 10 MMA B
 constexpr int kAttStages = 2;       // K and V slots
 constexpr uint32_t kAttTile = kAttBM * kAttD * 2;   // 32 KB: a Q, K or V tile
 constexpr uint32_t kAttHalf = kAttTile / 2;         // 64 columns of a tile (SW128 box)
@@ -145,6 +146,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     const uint32_t sq = sbase + kAttOffQ, sk = sbase + kAttOffK, sv = sbase + kAttOffV;
     const uint32_t bar0 = sbase + kAttOffBar;
     const uint32_t q_full = bar0, k0_full = bar0 + 8;
+    auto turn = [&](int x) { return bar0 + 16 + 8 * x; };   // issuer x may issue
     auto kv_full = [&](uint32_t i) { return bar0 + 32 + 8 * i; };
     auto kv_empty = [&](uint32_t i) { return bar0 + 48 + 8 * i; };
     auto s_full = [&](int x) { return bar0 + 64 + 8 * x; };
@@ -183,9 +185,11 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         }
         for (int i = 0; i < kAttStages; ++i) {
             mbar_init(kv_full(i), 1);
-            mbar_init(kv_empty(i), 1);
+            mbar_init(kv_empty(i), 2);   // one commit per issuer
         }
-        mbar_init(mmadone, 1);
+        mbar_init(turn(0), 1);
+        mbar_init(turn(1), 1);
+        mbar_init(mmadone, 2);
         abort[0] = blockDim.x != kAttThreads;
         abort[1] = a.wait_limit_us;
         fence_mbar_init();
@@ -256,57 +260,64 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             for (int i = issued > kAttStages ? issued - kAttStages : 0; i < issued; ++i)
                 mbar_wait_teardown(kv_full(i & 1), (i >> 1) & 1);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == 10) {
+        // ------------------------------------------------ MMA issuer of tile x
         if (lane == 0) {
+            const int x = warp == 1 ? 0 : 1;
+            const int n = n_x(x);
             constexpr uint32_t idesc_s = idesc_bf16_f32(kAttBM, kAttBN, false, false);
             constexpr uint32_t idesc_o = idesc_bf16_f32(kAttBM, kAttD, false, true);
             // Descriptors are built once; a step adds its byte offset >> 4 to
             // the start-address field (every tile lies below 256 KB, so the
             // 14-bit field never carries).
-            const uint64_t dq0 = sdesc_sw128(sq, 16, 1024), dq1 = sdesc_sw128(sq + kAttTile, 16, 1024);
+            const uint64_t dq = sdesc_sw128(sq + x * kAttTile, 16, 1024);
             const uint64_t dk0 = sdesc_sw128(sk, 16, 1024), dk1 = sdesc_sw128(sk + kAttTile, 16, 1024);
             const uint64_t dv0 = sdesc_sw128(sv, kAttTile / 4, 1024);
             const uint64_t dv1 = sdesc_sw128(sv + kAttTile, kAttTile / 4, 1024);
-            // S_x = Qn_x K^T into tile x's score buffer: A and B K-major, 8 steps of 16 dims
-            auto issue_s = [&](int x, uint32_t kslot) {
-                const uint32_t d = tmem + x * 256;
-                const uint64_t a0 = x ? dq1 : dq0, b0 = kslot ? dk1 : dk0;
+            const uint32_t dS = tmem + x * 256;
+            // S = Q_x Kg^T into the tile's score buffer: A and B K-major, 8 steps of 16 dims
+            auto issue_s = [&](uint32_t kslot) {
+                const uint64_t b0 = kslot ? dk1 : dk0;
 #pragma unroll
                 for (int kk = 0; kk < kAttD / 16; ++kk) {
                     const uint64_t off = ((kk >> 2) * kAttHalf + (kk & 3) * 32) >> 4;
-                    mma_bf16_ss(d, a0 + off, b0 + off, idesc_s, kk > 0);
+                    mma_bf16_ss(dS, dq + off, b0 + off, idesc_s, kk > 0);
                 }
                 mma_commit(s_full(x));
             };
-            // O_x += P_x V: A = P from tensor memory (keys 16kk.. in columns
+            // O_x += P V: A = P from tensor memory (keys 16kk.. in columns
             // 8kk..), B = V MN-major (dims contiguous), 8 steps of 16 keys
-            auto issue_pv = [&](int x, uint32_t vslot, bool acc) {
-                const uint32_t pa = tmem + x * 256;
+            auto issue_pv = [&](uint32_t vslot, bool acc) {
                 const uint64_t b0 = vslot ? dv1 : dv0;
 #pragma unroll
                 for (int kk = 0; kk < kAttBN / 16; ++kk) {
                     const uint64_t off = ((kk >> 2) * (kAttTile / 2) + (kk & 3) * 2048) >> 4;
-                    mma_bf16_ts(pa + kAttColO, pa + kk * 8, b0 + off, idesc_o, acc || kk > 0);
+                    mma_bf16_ts(dS + kAttColO, dS + kk * 8, b0 + off, idesc_o, acc || kk > 0);
                 }
             };
             bool ok = mbar_wait(k0_full, 0, abort) && mbar_wait(q_full, 0, abort);
-            if (ok) tc_fence_after();
-            for (int x = 0; ok && x < 2; ++x)
-                if (n_x(x) > 0) issue_s(x, 0);
-            if (ok) mma_commit(kv_empty(1));   // K_0 read: "key tile -1" of stage 1
+            if (ok) {
+                tc_fence_after();
+                if (n > 0) issue_s(0);
+                mma_commit(kv_empty(1));   // K_0 read: "key tile -1" of stage 1
+            }
+            // Each issuer waits for stage j before releasing it, so neither
+            // releases a stage twice before the other released it once.  The
+            // turn passes A -> B -> A every key tile, also through an issuer
+            // that has nothing left to issue.
             for (int j = 0; ok && j < n_kv; ++j) {
                 const uint32_t st = j & 1;
                 if (!mbar_wait(kv_full(st), (j >> 1) & 1, abort)) break;
-                for (int x = 0; x < 2; ++x) {
-                    if (j >= n_x(x)) continue;
-                    if (!mbar_wait(p_full(x), j & 1, abort)) { ok = false; break; }
+                if (j < n && !mbar_wait(p_full(x), j & 1, abort)) break;
+                // A's turn for tile j is B's hand-back from tile j - 1 (none for j = 0)
+                if ((x == 1 || j > 0) && !mbar_wait(turn(x), (x == 0 ? j - 1 : j) & 1, abort)) break;
+                if (j < n) {
                     tc_fence_after();
-                    issue_pv(x, st, j > 0);
-                    if (j + 1 < n_x(x)) issue_s(x, (j + 1) & 1);
+                    issue_pv(st, j > 0);
+                    if (j + 1 < n) issue_s((j + 1) & 1);
                     else mma_commit(o_final(x));
                 }
-                if (!ok) break;
+                mbar_arrive(turn(x ^ 1));
                 mma_commit(kv_empty(st));
             }
             mma_commit(mmadone);
