@@ -813,10 +813,10 @@ int qknorm_attention(const void* Q, int64_t ldq, const void* K, int64_t ldk, con
     void* khat = nullptr;
     rc = get_khat_buffer(dev, stream, static_cast<size_t>(B * S * Hkv * D) * 2, &khat);
     if (rc != RMM_OK) return rc;
-    CUtensorMap tmQ, tmK, tmV, tmO;
+    CUtensorMap tmQ, tmK, tmV;
     if (!map_3d(&tmQ, Q, B, S, Hq * D, ldq, rmm::kAttBM) ||
         !map_3d(&tmK, khat, B, S, Hkv * D, Hkv * D, rmm::kAttBN) ||
-        !map_3d(&tmV, V, B, S, Hkv * D, ldv, 64) || !map_3d(&tmO, O, B, S, Hq * D, ldo, rmm::kAttBM))
+        !map_3d(&tmV, V, B, S, Hkv * D, ldv, 64))
         return RMM_ERR_INTERNAL;
     // the keys once: RMSNorm(K; gk) * gq per head, into the workspace (the
     // query gain moves onto the keys; the query rows keep only their 1/RMS)
@@ -830,12 +830,15 @@ int qknorm_attention(const void* Q, int64_t ldq, const void* K, int64_t ldk, con
     a.n_qb = static_cast<int>(n_qb);
     a.n_hb = static_cast<int>(B * Hq);
     a.causal = causal != 0;
-    a.grid = static_cast<int>(n_qb * B * Hq);
+    a.n_blocks = static_cast<int>(n_qb * B * Hq);
+    a.grid = std::min(a.n_blocks, d.sm_count);
     a.eps = eps;
     const double sc = scale > 0.f ? static_cast<double>(scale) : 1.0 / std::sqrt(static_cast<double>(D));
     a.qscale = static_cast<float>(sc * 1.4426950408889634);   // log2(e)
     a.wait_limit_us = g_wait_limit_us.load();
-    return rmm::launch_qknorm_attention(tmQ, tmK, tmV, tmO, a, stream) == cudaSuccess
+    a.O = O;
+    a.ldo = ldo;
+    return rmm::launch_qknorm_attention(tmQ, tmK, tmV, a, stream) == cudaSuccess
                ? RMM_OK
                : RMM_ERR_LAUNCH;
 }

@@ -8,11 +8,12 @@
 //   rmsnorm_heads_kernel    normalises every key head once (memory-bound; one
 //                           warp per head row), into a bf16 workspace, with
 //                           the query gain gq folded in: Kg = bf16(Kn * gq);
-//   qknorm_attention_kernel one CTA per 256 query rows of one head (two
-//                           128-row tiles): for each 128-key tile S' = Q Kg^T
-//                           (the raw bf16 queries) and O += P V on the tensor
-//                           cores (tcgen05, accumulators in tensor memory),
-//                           with the online softmax between them.
+//   qknorm_attention_kernel persistent, one CTA per SM walking blocks of 256
+//                           query rows of one head (two 128-row tiles): for
+//                           each 128-key tile S' = Q Kg^T (the raw bf16
+//                           queries) and O += P V on the tensor cores
+//                           (tcgen05, accumulators in tensor memory), with
+//                           the online softmax between them.
 //
 // The query normalisation is a row scale: <Qn_i, Kn_j> = r_i <Q_i * gq, Kn_j>
 // = r_i <Q_i, Kg_j> with r_i = 1 / sqrt(mean(Q_i^2) + eps), so the kernel
@@ -104,40 +105,79 @@ __global__ void __launch_bounds__(kHeadsWarps * 32)
 }
 
 // ------------------------------------------------------- attention kernel
-// One CTA per block of 256 query rows of one head: two 128-row query tiles,
-// A (rows q0 .. q0 + 127) and B (q0 + 128 .. q0 + 255), each with its own
-// score buffer, output accumulator, group of four softmax warps and MMA
-// issuing thread.  The issuers take turns, A then B for every key tile
-// (a pair of turn barriers): that keeps the two tiles half a period apart, so
-// the tensor cores work on one tile's products while the other tile's
-// softmax runs, and each issuer does its waits and releases while the other
-// one issues (an issuing thread stalls whenever the tensor pipe's queue is
-// full, so a single issuer's own waits leave the pipe idle).  Without the
-// turns the two issuers drift into step and both softmaxes run while the
-// pipe idles.  Both tiles read the same K and V tiles, loaded once: stage j
-// of the ring holds V_j and K_{j+1} (K_0 has a barrier of its own).
+// A persistent CTA per SM walks its blocks of 256 query rows.  Blocks are
+// numbered longest first when causal; CTA c of G takes block r G + c from
+// each even band r of G blocks and (r + 1) G - 1 - c from each odd band (a
+// zig-zag, so that every CTA gets a similar total of key tiles: a plain
+// stride left the heaviest CTA 30% above the mean).  A block holds
+// two 128-row query tiles, A (rows q0 .. q0 + 127) and B (q0 + 128 ..), each
+// with its own score buffer, output accumulator, group of four softmax warps
+// and MMA issuing thread.  The issuers take turns, A then B for every key
+// tile (a pair of turn barriers): that keeps the two tiles half a period
+// apart, so the tensor cores work on one tile's products while the other
+// tile's softmax runs, and each issuer does its waits and releases while the
+// other one issues (an issuing thread stalls whenever the tensor pipe's queue
+// is full).  Without the turns the two issuers drift into step and both
+// softmaxes run while the pipe idles.
+//
+// Both tiles read the same K and V tiles, loaded once, as one stream across
+// the CTA's blocks: stage g of a two-deep ring holds V_j of the current
+// block and the next K tile of the stream, K_{j+1}, or for the block's last
+// stage the next block's K_0 (the very first K_0 has a barrier of its own).
+// The next block's query tiles load as soon as the current block's last
+// score products have completed and its row norms have been read, during the
+// block's last key tile; an issuer starts the next block's first products
+// right after its last ones of the current block, and O leaves through plain
+// stores from the softmax threads, so blocks follow each other without a
+// gap.  Every barrier's parity is a count kept by the roles that use it.
 constexpr int kAttThreads = 352;    // warp 0 TMA, 1 MMA A + TMEM, 2-5 softmax A, 6-9 softmax B, 10 MMA B
 constexpr int kAttStages = 2;       // K and V slots
 constexpr uint32_t kAttTile = kAttBM * kAttD * 2;   // 32 KB: a Q, K or V tile
 constexpr uint32_t kAttHalf = kAttTile / 2;         // 64 columns of a tile (SW128 box)
-constexpr uint32_t kAttOffQ = 0;                    // Q tiles A and B, later the O staging
+constexpr uint32_t kAttOffQ = 0;                    // query tiles A and B
 constexpr uint32_t kAttOffK = kAttOffQ + 2 * kAttTile;
 constexpr uint32_t kAttOffV = kAttOffK + kAttStages * kAttTile;
 constexpr uint32_t kAttOffBar = kAttOffV + kAttStages * kAttTile;
-constexpr uint32_t kAttNumBars = 15;
+constexpr uint32_t kAttNumBars = 18;
 constexpr uint32_t kAttOffMisc = kAttOffBar + 256;
 constexpr uint32_t kAttSmem = kAttOffMisc + 16 + 1024;   // + alignment slack
 static_assert(kAttNumBars * 8 <= 256, "barrier area");
-// Tensor memory, per query tile X (columns X * 256 ..): the score buffer S
+// Tensor memory, per query tile x (columns x * 256 ..): the score buffer S
 // (P overwrites its first 64 columns, two bf16 per column), then O.
 constexpr uint32_t kAttColO = 128, kAttTmemCols = 512;
 constexpr float kAttRescale = 8.f;   // rescale O only when the row max grows by > 2^8
 
+// One block of 256 query rows of one head of one sequence.
+struct AttnBlock {
+    int qb, h, b, c, q0;
+    int n0, n1;  // key tiles query tiles A and B visit (0: tile past the sequence end)
+    int nkv;     // max(n0, n1)
+    __device__ __forceinline__ int n(int x) const { return x ? n1 : n0; }
+};
+
+__device__ __forceinline__ AttnBlock attn_block(const AttnLaunch& a, int k) {
+    AttnBlock B;
+    B.qb = a.causal ? a.n_qb - 1 - k / a.n_hb : k / a.n_hb;
+    const int hb = k % a.n_hb;
+    B.h = hb % a.Hq;
+    B.b = hb / a.Hq;
+    B.c = B.h / a.group;
+    B.q0 = B.qb * 2 * kAttBM;
+    const int n_all = (a.S + kAttBN - 1) / kAttBN;
+    auto tiles = [&](int x) {
+        const int qt = 2 * B.qb + x;
+        return B.q0 + x * kAttBM >= a.S ? 0 : a.causal ? min(qt + 1, n_all) : n_all;
+    };
+    B.n0 = tiles(0);
+    B.n1 = tiles(1);
+    B.nkv = max(B.n0, B.n1);
+    return B;
+}
+
 __global__ void __launch_bounds__(kAttThreads, 1)
     qknorm_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                             const __grid_constant__ CUtensorMap tmK,
-                            const __grid_constant__ CUtensorMap tmV,
-                            const __grid_constant__ CUtensorMap tmO, AttnLaunch a) {
+                            const __grid_constant__ CUtensorMap tmV, AttnLaunch a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -145,50 +185,38 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sq = sbase + kAttOffQ, sk = sbase + kAttOffK, sv = sbase + kAttOffV;
     const uint32_t bar0 = sbase + kAttOffBar;
-    const uint32_t q_full = bar0, k0_full = bar0 + 8;
-    auto turn = [&](int x) { return bar0 + 16 + 8 * x; };   // issuer x may issue
-    auto kv_full = [&](uint32_t i) { return bar0 + 32 + 8 * i; };
-    auto kv_empty = [&](uint32_t i) { return bar0 + 48 + 8 * i; };
-    auto s_full = [&](int x) { return bar0 + 64 + 8 * x; };
-    auto p_full = [&](int x) { return bar0 + 80 + 8 * x; };
-    auto o_final = [&](int x) { return bar0 + 96 + 8 * x; };
-    const uint32_t mmadone = bar0 + 112;
+    const uint32_t q_full = bar0, q_empty = bar0 + 8, k0_full = bar0 + 16;
+    auto kv_full = [&](uint32_t i) { return bar0 + 24 + 8 * i; };
+    auto kv_empty = [&](uint32_t i) { return bar0 + 40 + 8 * i; };
+    auto turn = [&](int x) { return bar0 + 56 + 8 * x; };      // issuer x may issue
+    auto s_full = [&](int x) { return bar0 + 72 + 8 * x; };
+    auto p_full = [&](int x) { return bar0 + 88 + 8 * x; };
+    auto o_final = [&](int x) { return bar0 + 104 + 8 * x; };
+    auto o_empty = [&](int x) { return bar0 + 120 + 8 * x; };
+    const uint32_t mmadone = bar0 + 136;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kAttOffMisc);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + kAttOffMisc + 4);
-
-    // the block: query rows [q0, q0 + 256) of head h in sequence b; causal
-    // launches take the longest rows (the last blocks) first
-    const int bid = blockIdx.x;
-    const int qb = a.causal ? a.n_qb - 1 - bid / a.n_hb : bid / a.n_hb;
-    const int hb = bid % a.n_hb;
-    const int h = hb % a.Hq, b = hb / a.Hq;
-    const int c = h / a.group;
-    const int q0 = qb * 2 * kAttBM;
-    const int n_kv_all = (a.S + kAttBN - 1) / kAttBN;
-    // key tiles each query tile visits (tile B may lie past the sequence end)
-    auto tiles_of = [&](int x) {
-        const int qt = 2 * qb + x;
-        return q0 + x * kAttBM >= a.S ? 0 : a.causal ? min(qt + 1, n_kv_all) : n_kv_all;
+    // the CTA's r-th block, or -1 (once a band has none, no later band has)
+    auto block_id = [&](int r) {
+        const int G = gridDim.x, c = blockIdx.x;
+        const int k = (r & 1) ? (r + 1) * G - 1 - c : r * G + c;
+        return k < a.n_blocks ? k : -1;
     };
-    const int n_a = tiles_of(0), n_b = tiles_of(1);
-    auto n_x = [&](int x) { return x ? n_b : n_a; };
-    const int n_kv = max(n_a, n_b);
 
     if (threadIdx.x == 0) {
         if (blockDim.x != kAttThreads) atomicCAS(&g_status, 0, kStatusInternal);
         mbar_init(q_full, 1);
+        mbar_init(q_empty, 2 + 8);   // a commit per issuer + one lane per softmax warp
         mbar_init(k0_full, 1);
         for (int x = 0; x < 2; ++x) {
+            mbar_init(kv_full(x), 1);
+            mbar_init(kv_empty(x), 2);   // one commit per issuer
+            mbar_init(turn(x), 1);
             mbar_init(s_full(x), 1);
-            mbar_init(p_full(x), 4);
+            mbar_init(p_full(x), 4);     // one lane per softmax warp
             mbar_init(o_final(x), 1);
+            mbar_init(o_empty(x), 4);
         }
-        for (int i = 0; i < kAttStages; ++i) {
-            mbar_init(kv_full(i), 1);
-            mbar_init(kv_empty(i), 2);   // one commit per issuer
-        }
-        mbar_init(turn(0), 1);
-        mbar_init(turn(1), 1);
         mbar_init(mmadone, 2);
         abort[0] = blockDim.x != kAttThreads;
         abort[1] = a.wait_limit_us;
@@ -196,7 +224,6 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         prefetch_tmap(&tmQ);
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
-        prefetch_tmap(&tmO);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_holder), kAttTmemCols);
@@ -213,58 +240,73 @@ __global__ void __launch_bounds__(kAttThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
-        if (lane == 0 && !*abort) {
+        if (lane == 0 && !*abort && block_id(0) >= 0) {
             const uint64_t keep = policy_evict_last();   // K and V tiles are re-read
             const uint64_t once = policy_evict_first();  // the query tiles are read once
-            mbar_arrive_expect_tx(q_full, 2 * kAttTile);
+            auto load_q = [&](const AttnBlock& B) {
+                mbar_arrive_expect_tx(q_full, 2 * kAttTile);
 #pragma unroll
-            for (int x = 0; x < 2; ++x) {
-                tma_load_3d(sq + x * kAttTile, &tmQ, q_full, h * kAttD, q0 + x * kAttBM, b, once);
-                tma_load_3d(sq + x * kAttTile + kAttHalf, &tmQ, q_full, h * kAttD + 64,
-                            q0 + x * kAttBM, b, once);
-            }
+                for (int x = 0; x < 2; ++x) {
+                    tma_load_3d(sq + x * kAttTile, &tmQ, q_full, B.h * kAttD, B.q0 + x * kAttBM, B.b, once);
+                    tma_load_3d(sq + x * kAttTile + kAttHalf, &tmQ, q_full, B.h * kAttD + 64,
+                                B.q0 + x * kAttBM, B.b, once);
+                }
+            };
+            AttnBlock cur = attn_block(a, block_id(0));
+            load_q(cur);
             mbar_arrive_expect_tx(k0_full, kAttTile);
-            tma_load_3d(sk, &tmK, k0_full, c * kAttD, 0, b, keep);
-            tma_load_3d(sk + kAttHalf, &tmK, k0_full, c * kAttD + 64, 0, b, keep);
-            int issued = 0;
-            for (int j = 0; j < n_kv; ++j) {
-                const uint32_t st = j & 1;
-                // V slot j & 1 held V_{j-2} and K slot (j+1) & 1 held K_{j-1};
-                // both are released by the issuers' commits after key tile
-                // j - 2 (for j = 1: after S(0), which read K_0)
-                if (j >= 1) {
-                    const uint32_t par = (j & 1) ? ((j - 1) >> 1) & 1 : ((j >> 1) - 1) & 1;
-                    if (!mbar_wait(kv_empty(st), par, abort)) break;
-                }
-                const bool kn = j + 1 < n_kv;
-                mbar_arrive_expect_tx(kv_full(st), kn ? 2 * kAttTile : kAttTile);
-                const uint32_t vd = sv + st * kAttTile;
-                // four boxes of [64 keys][64 dims]: box (kk, n) at (2 kk + n) * 8 KB
+            tma_load_3d(sk, &tmK, k0_full, cur.c * kAttD, 0, cur.b, keep);
+            tma_load_3d(sk + kAttHalf, &tmK, k0_full, cur.c * kAttD + 64, 0, cur.b, keep);
+            uint32_t g = 0;   // stages issued
+            uint32_t t = 0;   // blocks begun
+            bool ok = true;
+            for (int r = 0; ok && block_id(r) >= 0; ++r, ++t) {
+                const bool has_next = block_id(r + 1) >= 0;
+                const AttnBlock nxt = has_next ? attn_block(a, block_id(r + 1)) : cur;
+                for (int j = 0; j < cur.nkv; ++j, ++g) {
+                    const uint32_t st = g & 1;
+                    // V slot g & 1 held the V of stage g - 2 and K slot (g+1) & 1
+                    // the K of stage g - 2 (the first K_0 for g = 1): both are
+                    // released by the issuers' commits after stage g - 2
+                    if (g >= 1) {
+                        const uint32_t par = (g & 1) ? ((g - 1) >> 1) & 1 : ((g >> 1) - 1) & 1;
+                        if (!mbar_wait(kv_empty(st), par, abort)) { ok = false; break; }
+                    }
+                    const bool last = j + 1 == cur.nkv;
+                    const bool kn = !last || has_next;
+                    mbar_arrive_expect_tx(kv_full(st), kn ? 2 * kAttTile : kAttTile);
+                    const uint32_t vd = sv + st * kAttTile;
+                    // four boxes of [64 keys][64 dims]: box (kk, n) at (2 kk + n) * 8 KB
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk)
+                    for (int kk = 0; kk < 2; ++kk)
 #pragma unroll
-                    for (int n = 0; n < 2; ++n)
-                        tma_load_3d(vd + (2 * kk + n) * (kAttTile / 4), &tmV, kv_full(st),
-                                    c * kAttD + n * 64, j * kAttBN + kk * 64, b, keep);
-                if (kn) {
-                    const uint32_t kd = sk + ((j + 1) & 1) * kAttTile;
-                    tma_load_3d(kd, &tmK, kv_full(st), c * kAttD, (j + 1) * kAttBN, b, keep);
-                    tma_load_3d(kd + kAttHalf, &tmK, kv_full(st), c * kAttD + 64, (j + 1) * kAttBN, b,
-                                keep);
+                        for (int n = 0; n < 2; ++n)
+                            tma_load_3d(vd + (2 * kk + n) * (kAttTile / 4), &tmV, kv_full(st),
+                                        cur.c * kAttD + n * 64, j * kAttBN + kk * 64, cur.b, keep);
+                    if (kn) {
+                        const uint32_t kd = sk + ((g + 1) & 1) * kAttTile;
+                        const int kc = last ? nxt.c : cur.c, kj = last ? 0 : j + 1, kb = last ? nxt.b : cur.b;
+                        tma_load_3d(kd, &tmK, kv_full(st), kc * kAttD, kj * kAttBN, kb, keep);
+                        tma_load_3d(kd + kAttHalf, &tmK, kv_full(st), kc * kAttD + 64, kj * kAttBN, kb, keep);
+                    }
                 }
-                ++issued;
+                if (!ok || !has_next) break;
+                // the next block's query tiles, once this block's score
+                // products have completed and its row norms have been read
+                if (!mbar_wait(q_empty, t & 1, abort)) break;
+                load_q(nxt);
+                cur = nxt;
             }
             // never leave with copies still landing in shared memory
-            mbar_wait_teardown(q_full, 0);
+            mbar_wait_teardown(q_full, t & 1);
             mbar_wait_teardown(k0_full, 0);
-            for (int i = issued > kAttStages ? issued - kAttStages : 0; i < issued; ++i)
+            for (uint32_t i = g > kAttStages ? g - kAttStages : 0; i < g; ++i)
                 mbar_wait_teardown(kv_full(i & 1), (i >> 1) & 1);
         }
     } else if (warp == 1 || warp == 10) {
         // ------------------------------------------------ MMA issuer of tile x
         if (lane == 0) {
             const int x = warp == 1 ? 0 : 1;
-            const int n = n_x(x);
             constexpr uint32_t idesc_s = idesc_bf16_f32(kAttBM, kAttBN, false, false);
             constexpr uint32_t idesc_o = idesc_bf16_f32(kAttBM, kAttD, false, true);
             // Descriptors are built once; a step adds its byte offset >> 4 to
@@ -295,50 +337,92 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                     mma_bf16_ts(dS + kAttColO, dS + kk * 8, b0 + off, idesc_o, acc || kk > 0);
                 }
             };
-            bool ok = mbar_wait(k0_full, 0, abort) && mbar_wait(q_full, 0, abort);
+            // the first score product of a block; a query tile with at most
+            // one key tile has then read its query tile for the last time
+            auto begin_block = [&](const AttnBlock& B, uint32_t kslot) {
+                if (B.n(x) > 0) issue_s(kslot);
+                if (B.n(x) <= 1) mma_commit(q_empty);
+            };
+            uint32_t g = 0, t = 0, pi = 0;   // stages, blocks, P tiles consumed
+            const bool any = block_id(0) >= 0;
+            AttnBlock cur = attn_block(a, any ? block_id(0) : 0);
+            bool ok = any && mbar_wait(k0_full, 0, abort) && mbar_wait(q_full, 0, abort);
             if (ok) {
                 tc_fence_after();
-                if (n > 0) issue_s(0);
-                mma_commit(kv_empty(1));   // K_0 read: "key tile -1" of stage 1
+                begin_block(cur, 0);
+                mma_commit(kv_empty(1));   // the first K_0 read: "stage -1" of slot 1
             }
-            // Each issuer waits for stage j before releasing it, so neither
+            // Each issuer waits for stage g before releasing it, so neither
             // releases a stage twice before the other released it once.  The
-            // turn passes A -> B -> A every key tile, also through an issuer
-            // that has nothing left to issue.
-            for (int j = 0; ok && j < n_kv; ++j) {
-                const uint32_t st = j & 1;
-                if (!mbar_wait(kv_full(st), (j >> 1) & 1, abort)) break;
-                if (j < n && !mbar_wait(p_full(x), j & 1, abort)) break;
-                // A's turn for tile j is B's hand-back from tile j - 1 (none for j = 0)
-                if ((x == 1 || j > 0) && !mbar_wait(turn(x), (x == 0 ? j - 1 : j) & 1, abort)) break;
-                if (j < n) {
+            // turn passes A -> B -> A every stage, also through an issuer that
+            // has nothing to issue in it.
+            for (int r = 0; ok && block_id(r) >= 0; ++r, ++t) {
+                const bool has_next = block_id(r + 1) >= 0;
+                const AttnBlock nxt = has_next ? attn_block(a, block_id(r + 1)) : cur;
+                const int n = cur.n(x);
+                for (int j = 0; j < cur.nkv; ++j, ++g) {
+                    const uint32_t st = g & 1;
+                    if (!mbar_wait(kv_full(st), (g >> 1) & 1, abort)) { ok = false; break; }
+                    if (j < n && !mbar_wait(p_full(x), pi & 1, abort)) { ok = false; break; }
+                    // the first P V of a block overwrites O: the previous
+                    // block's epilogue has read it (one arrival per block)
+                    if (j == 0 && n > 0 && t > 0 && !mbar_wait(o_empty(x), (t - 1) & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    // A's turn at stage g is B's hand-back from stage g - 1 (none at g = 0)
+                    if ((x == 1 || g > 0) && !mbar_wait(turn(x), (x == 0 ? g - 1 : g) & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
-                    issue_pv(st, j > 0);
-                    if (j + 1 < n) issue_s((j + 1) & 1);
-                    else mma_commit(o_final(x));
+                    if (j < n) {
+                        ++pi;
+                        issue_pv(st, j > 0);
+                        if (j + 1 < n) {
+                            issue_s((g + 1) & 1);
+                            if (j + 2 == n) mma_commit(q_empty);   // that was the last score product
+                        } else {
+                            mma_commit(o_final(x));
+                        }
+                    }
+                    mbar_arrive(turn(x ^ 1));
+                    if (j + 1 == cur.nkv && has_next) {
+                        // the next block's first product (after the turn is
+                        // handed over, so the other tile's last products do
+                        // not wait for the load): its query tiles, loaded
+                        // during this stage, and its K_0, in this stage
+                        if (!mbar_wait(q_full, (t + 1) & 1, abort)) { ok = false; break; }
+                        tc_fence_after();
+                        begin_block(nxt, (g + 1) & 1);
+                    }
+                    mma_commit(kv_empty(st));
                 }
-                mbar_arrive(turn(x ^ 1));
-                mma_commit(kv_empty(st));
+                cur = nxt;
             }
             mma_commit(mmadone);
             mbar_wait_teardown(mmadone, 0);
         }
-    } else {
+    } else if (warp >= 2 && warp < 10) {
         // ------------------------------------------------ softmax warps of tile x
         const int x = (warp - 2) >> 2;          // 0: tile A (warps 2-5), 1: tile B (6-9)
         const int q = warp & 3;                  // lane quarter of tensor memory
         const int row = q * 32 + lane;           // query row of the tile
-        const int qt = 2 * qb + x;
-        const int qpos = qt * kAttBM + row;
-        const int n = n_x(x);
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t swz = static_cast<uint32_t>(row & 7);
         const uint32_t srow = sq + x * kAttTile + static_cast<uint32_t>(row) * 128;
-        bool ok = warp_wait(q_full, 0, abort);
-        // the row's scale r * scale * log2(e) (the query tile is only read:
-        // the first products run on it meanwhile)
-        float ss[4] = {0.f, 0.f, 0.f, 0.f};
-        if (ok) {
+        const uint32_t sbuf = tmem + x * 256 + lane_base;
+        const uint32_t obuf = sbuf + kAttColO;
+        uint32_t t = 0, si = 0, ob = 0;   // blocks, S tiles consumed, blocks with output
+        bool ok = true;
+        for (int r = 0; ok && block_id(r) >= 0; ++r, ++t) {
+            const AttnBlock B = attn_block(a, block_id(r));
+            const int n = B.n(x);
+            const int qt = 2 * B.qb + x;
+            const int qpos = qt * kAttBM + row;
+            if (!warp_wait(q_full, t & 1, abort)) break;
+            // the row's scale r * scale * log2(e); the query tile is only read
+            float ss[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
@@ -351,113 +435,111 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                         ss[i] = fmaf(bf16hi(w[i]), bf16hi(w[i]), ss[i]);
                     }
                 }
-        }
-        const float rc = rsqrtf(((ss[0] + ss[1]) + (ss[2] + ss[3])) * (1.f / kAttD) + a.eps) * a.qscale;
-        const uint64_t rc2 = pack_f32x2(rc, rc);
-        const uint32_t sbuf = tmem + x * 256 + lane_base;
-        const uint32_t obuf = sbuf + kAttColO;
-        float m_ref = 0.f, l = 0.f;
-        for (int j = 0; ok && j < n; ++j) {
-            if (!warp_wait(s_full(x), j & 1, abort)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            uint32_t v[kAttBN];
-            tmem_ld_32x32_x128(sbuf, v);
-            // keys past the sequence end, and after the query when causal
-            const int kbase = j * kAttBN;
-            int lim = min(kAttBN, a.S - kbase);
-            if (a.causal && j == qt) lim = min(lim, qpos - kbase + 1);
-            if (lim < kAttBN) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_empty);
+            const float rc = rsqrtf(((ss[0] + ss[1]) + (ss[2] + ss[3])) * (1.f / kAttD) + a.eps) * a.qscale;
+            const uint64_t rc2 = pack_f32x2(rc, rc);
+            float m_ref = 0.f, l = 0.f;
+            for (int j = 0; j < n; ++j, ++si) {
+                if (!warp_wait(s_full(x), si & 1, abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t v[kAttBN];
+                tmem_ld_32x32_x128(sbuf, v);
+                // keys past the sequence end, and after the query when causal
+                const int kbase = j * kAttBN;
+                int lim = min(kAttBN, a.S - kbase);
+                if (a.causal && j == qt) lim = min(lim, qpos - kbase + 1);
+                if (lim < kAttBN) {
 #pragma unroll
-                for (int i = 0; i < kAttBN; ++i)
-                    if (i >= lim) v[i] = 0xff800000u;   // -inf
-            }
-            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                    for (int i = 0; i < kAttBN; ++i)
+                        if (i >= lim) v[i] = 0xff800000u;   // -inf
+                }
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int i = 0; i < kAttBN; i += 8) {
-                mx[0] = max3f(mx[0], __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
-                mx[1] = max3f(mx[1], __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
-                mx[2] = max3f(mx[2], __uint_as_float(v[i + 4]), __uint_as_float(v[i + 5]));
-                mx[3] = max3f(mx[3], __uint_as_float(v[i + 6]), __uint_as_float(v[i + 7]));
-            }
-            // rc > 0: the maximum of the scaled scores is rc times the maximum
-            const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * rc;
-            float alpha = 1.f;
-            bool rescale = false;
-            if (j == 0) {
-                m_ref = m_tile == -INFINITY ? 0.f : m_tile;
-            } else if (m_tile > m_ref + kAttRescale) {
-                // weights stay below 2^8 relative to m_ref; beyond that the
-                // reference moves and O and l are scaled down to it
-                alpha = ex2_approx(m_ref - m_tile);
-                m_ref = m_tile;
-                l *= alpha;
-                rescale = true;
-            }
-            const uint64_t negm = pack_f32x2(-m_ref, -m_ref);
-            uint64_t acc[4] = {0, 0, 0, 0};   // packed partial row sums (0.0f pairs)
-            uint32_t pk[kAttBN / 2];
+                for (int i = 0; i < kAttBN; i += 8) {
+                    mx[0] = max3f(mx[0], __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+                    mx[1] = max3f(mx[1], __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                    mx[2] = max3f(mx[2], __uint_as_float(v[i + 4]), __uint_as_float(v[i + 5]));
+                    mx[3] = max3f(mx[3], __uint_as_float(v[i + 6]), __uint_as_float(v[i + 7]));
+                }
+                // rc > 0: the maximum of the scaled scores is rc times the maximum
+                const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * rc;
+                float alpha = 1.f;
+                bool rescale = false;
+                if (j == 0) {
+                    m_ref = m_tile == -INFINITY ? 0.f : m_tile;
+                } else if (m_tile > m_ref + kAttRescale) {
+                    // weights stay below 2^8 relative to m_ref; beyond that the
+                    // reference moves and O and l are scaled down to it
+                    alpha = ex2_approx(m_ref - m_tile);
+                    m_ref = m_tile;
+                    l *= alpha;
+                    rescale = true;
+                }
+                const uint64_t negm = pack_f32x2(-m_ref, -m_ref);
+                uint64_t acc[4] = {0, 0, 0, 0};   // packed partial row sums (0.0f pairs)
+                uint32_t pk[kAttBN / 2];
 #pragma unroll
-            for (int i = 0; i < kAttBN / 2; ++i) {
-                const uint64_t d = fma_f32x2(pack_f32x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
-                                             rc2, negm);
-                const float p0 = ex2_approx(lo_f32(d)), p1 = ex2_approx(hi_f32(d));
-                acc[i & 3] = add_f32x2(acc[i & 3], pack_f32x2(p0, p1));
-                pk[i] = pack_bf16x2(p0, p1);
-            }
-            tmem_st_32x32_x64(sbuf, pk);
-            const uint64_t t = add_f32x2(add_f32x2(acc[0], acc[1]), add_f32x2(acc[2], acc[3]));
-            l += lo_f32(t) + hi_f32(t);
-            if (__any_sync(0xffffffffu, rescale)) {
-                // O holds P_0..P_{j-1} V, complete: S_j was issued after the
-                // last of those products and has completed
+                for (int i = 0; i < kAttBN / 2; ++i) {
+                    const uint64_t d = fma_f32x2(pack_f32x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
+                                                 rc2, negm);
+                    const float p0 = ex2_approx(lo_f32(d)), p1 = ex2_approx(hi_f32(d));
+                    acc[i & 3] = add_f32x2(acc[i & 3], pack_f32x2(p0, p1));
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
+                tmem_st_32x32_x64(sbuf, pk);
+                const uint64_t tsum = add_f32x2(add_f32x2(acc[0], acc[1]), add_f32x2(acc[2], acc[3]));
+                l += lo_f32(tsum) + hi_f32(tsum);
+                if (__any_sync(0xffffffffu, rescale)) {
+                    // O holds this block's P_0..P_{j-1} V, complete: S_j was
+                    // issued after the last of those products and has completed
 #pragma unroll 1
+                    for (int cc = 0; cc < kAttD / 32; ++cc) {
+                        uint32_t o[32];
+                        tmem_ld_32x32(obuf + cc * 32, o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st_32x32(obuf + cc * 32, o);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full(x));
+            }
+            if (!ok) break;
+            // ------------------------------------------------ epilogue: O / l -> bf16 -> global
+            if (n > 0) {
+                if (!warp_wait(o_final(x), ob & 1, abort)) break;
+                ++ob;
+                tc_fence_after();
+                const float inv_l = 1.f / l;
+                __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.O) +
+                                      (static_cast<int64_t>(B.b) * a.S + qpos) * a.ldo + B.h * kAttD;
+                const bool valid = qpos < a.S;
+#pragma unroll
                 for (int cc = 0; cc < kAttD / 32; ++cc) {
                     uint32_t o[32];
                     tmem_ld_32x32(obuf + cc * 32, o);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st_32x32(obuf + cc * 32, o);
+                    for (int t4 = 0; t4 < 4; ++t4) {
+                        uint32_t o4[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            o4[i] = pack_bf16x2(__uint_as_float(o[8 * t4 + 2 * i]) * inv_l,
+                                                __uint_as_float(o[8 * t4 + 2 * i + 1]) * inv_l);
+                        if (valid)
+                            *reinterpret_cast<uint4*>(orow + cc * 32 + t4 * 8) =
+                                make_uint4(o4[0], o4[1], o4[2], o4[3]);
+                    }
                 }
+                tc_fence_before();
             }
-            tc_fence_before();
+            // O of this tile is free for the next block's first product
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full(x));
-        }
-        // ------------------------------------------------ epilogue: O / l -> bf16 -> TMA store
-        if (ok && n > 0) ok = warp_wait(o_final(x), 0, abort);
-        if (ok && n > 0) {
-            tc_fence_after();
-            const float inv_l = 1.f / l;
-            // staging in this tile's Q area (every MMA that read it has
-            // completed): 128-byte swizzle, two 64-column halves
-#pragma unroll
-            for (int cc = 0; cc < kAttD / 32; ++cc) {
-                uint32_t o[32];
-                tmem_ld_32x32(obuf + cc * 32, o);
-                const uint32_t dst = srow + (cc >> 1) * kAttHalf;
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    uint32_t o4[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        o4[i] = pack_bf16x2(__uint_as_float(o[8 * t + 2 * i]) * inv_l,
-                                            __uint_as_float(o[8 * t + 2 * i + 1]) * inv_l);
-                    const uint32_t chunk = static_cast<uint32_t>((cc & 1) * 4 + t);
-                    sts128(dst + ((chunk ^ swz) << 4), make_uint4(o4[0], o4[1], o4[2], o4[3]));
-                }
-            }
-            fence_proxy_async_smem();
-        }
-        named_bar_sync(2 + x, 128);
-        if (row == 0 && n > 0 && !*abort) {
-            const uint32_t src = sq + x * kAttTile;
-            tma_store_3d(&tmO, src, h * kAttD, qt * kAttBM, b);
-            tma_store_3d(&tmO, src + kAttHalf, h * kAttD + 64, qt * kAttBM, b);
-            bulk_commit_group();
-            bulk_wait_group_read<0>();   // the staging area is read; the writes complete on their own
+            if (lane == 0) mbar_arrive(o_empty(x));
         }
     }
     tc_fence_before();
@@ -501,8 +583,7 @@ cudaError_t launch_rmsnorm_heads(const void* X, int64_t ldx, const void* g, cons
 }
 
 cudaError_t launch_qknorm_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                                    const CUtensorMap& tmV, const CUtensorMap& tmO,
-                                    const AttnLaunch& a, cudaStream_t s) {
+                                    const CUtensorMap& tmV, const AttnLaunch& a, cudaStream_t s) {
     // the shared-memory limit is a per-device attribute of the function
     static std::atomic<bool> attr_set[64];
     int dev = 0;
@@ -515,7 +596,7 @@ cudaError_t launch_qknorm_attention(const CUtensorMap& tmQ, const CUtensorMap& t
         if (e != cudaSuccess) return e;
         attr_set[dev].store(true);
     }
-    return launch_pdl(qknorm_attention_kernel, a.grid, kAttThreads, kAttSmem, s, tmQ, tmK, tmV, tmO, a);
+    return launch_pdl(qknorm_attention_kernel, a.grid, kAttThreads, kAttSmem, s, tmQ, tmK, tmV, a);
 }
 
 cudaError_t attn_read_and_clear_status(int* out) {

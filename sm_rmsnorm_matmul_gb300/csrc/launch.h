@@ -109,10 +109,13 @@ struct AttnLaunch {
     int n_qb;         // blocks of 256 query rows per sequence, ceil(S / 256)
     int n_hb;         // Hq * B
     int causal;
-    int grid;         // n_qb * n_hb
+    int n_blocks;     // n_qb * n_hb
+    int grid;         // persistent CTAs, min(n_blocks, SMs)
     float eps;
     float qscale;     // scale * log2(e), applied with each query row's 1/RMS to its scores
     int wait_limit_us;
+    void* O;          // output [B, S, Hq, 128], row stride ldo elements
+    long long ldo;
 };
 
 // Y[t,h,:] = RMSNorm(X[t,h,:]; g, eps) * g2 for T rows of H heads of D
@@ -120,10 +123,9 @@ struct AttnLaunch {
 cudaError_t launch_rmsnorm_heads(const void* X, int64_t ldx, const void* g, const void* g2, void* Y,
                                  int64_t ldy, int64_t T, int H, int D, float eps, cudaStream_t s);
 // tmQ, tmK (normalised keys times gq), tmV: 3-D maps [B][S][heads*128] read
-// in boxes of [128 rows][64] (V: [64][64]); tmO: the same geometry as tmQ, stored.
+// in boxes of [128 rows][64] (V: [64][64]).
 cudaError_t launch_qknorm_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                                    const CUtensorMap& tmV, const CUtensorMap& tmO,
-                                    const AttnLaunch& a, cudaStream_t s);
+                                    const CUtensorMap& tmV, const AttnLaunch& a, cudaStream_t s);
 size_t attn_smem_bytes();
 // The attention translation unit's own status word (as read_and_clear_status).
 cudaError_t attn_read_and_clear_status(int* out);
