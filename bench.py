@@ -495,6 +495,49 @@ def cpu_oracle_run(w, budget_s, steps=None, warmup=0):
     return secs, nbytes, sample, threads, len(idx), reps
 
 
+def cpu_oracle_table(one_thread_secs: float = 2.0):
+    """The fp64 oracle on every workload, on the host cores: all rows of the
+    workloads up to 4096 rows, the 256-row sample of the larger one (its
+    full-size time extrapolated from the sample, and labelled so), with every
+    OpenMP thread, and with one thread on a row sample of about
+    `one_thread_secs`."""
+    import numpy as np
+    import oracle
+    from sm_rmsnorm_matmul_gb300 import inputs
+    lib = oracle.load()
+    threads = oracle.max_threads(lib)
+    rows_out = []
+    for name in inputs.WORKLOAD_ORDER:
+        w = inputs.WORKLOADS[name]
+        X, g, W = inputs.generate_workload(w)
+        Xf, gf, Wf = oracle.to_f64(X), oracle.to_f64(g), oracle.to_f64(W)
+        del X, W
+        full = w.M <= 4096
+        idx = list(range(w.M)) if full else inputs.sample_rows(w.M, 256)
+        Xs = np.ascontiguousarray(Xf[idx])
+        t = time.perf_counter()
+        oracle.rmsnorm_matmul(Xs, gf, Wf, w.eps, lib=lib)
+        secs = time.perf_counter() - t
+        flops = 2.0 * len(idx) * w.K * w.N
+        per_row_one = secs * threads / len(idx)       # estimate for one thread
+        n1 = max(1, min(len(idx), int(one_thread_secs / max(per_row_one, 1e-9))))
+        idx1 = inputs.sample_rows(w.M, n1) if n1 < w.M else list(range(w.M))
+        X1 = np.ascontiguousarray(Xf[idx1])
+        t = time.perf_counter()
+        oracle.rmsnorm_matmul(X1, gf, Wf, w.eps, nthreads=1, lib=lib)
+        s1 = time.perf_counter() - t
+        e = {"workload": name, "rows": len(idx), "rows_of": w.M, "threads": threads,
+             "secs": round(secs, 4), "gflops_f64": round(flops / secs / 1e9, 2),
+             "one_thread": {"rows": len(idx1), "secs": round(s1, 4),
+                            "gflops_f64": round(2.0 * len(idx1) * w.K * w.N / s1 / 1e9, 2)}}
+        if not full:
+            e["full_size_secs_extrapolated"] = round(secs * w.M / len(idx), 2)
+        rows_out.append(e)
+        del Xf, Wf, Xs, X1
+    return {"nproc": os.cpu_count(), "openmp_threads": threads, "kind": "oracle",
+            "workloads": rows_out}
+
+
 # ---------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -669,6 +712,8 @@ def main():
         out["cpu_baseline"] = {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s",
                                "cores": threads, "kind": "oracle", "sample": sample,
                                "secs_per_call": round(secs, 4)}
+        if args.shapes == "all":
+            out["cpu_oracle_table"] = cpu_oracle_table()
     if rank == 0:
         print(json.dumps(out), flush=True)
     sync.close()
