@@ -317,22 +317,26 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             const uint64_t dv0 = sdesc_sw128(sv, kAttTile / 4, 1024);
             const uint64_t dv1 = sdesc_sw128(sv + kAttTile, kAttTile / 4, 1024);
             const uint32_t dS = tmem + x * 256;
-            // S = Q_x Kg^T into the tile's score buffer: A and B K-major, 8 steps of 16 dims
-            auto issue_s = [&](uint32_t kslot) {
+            // S = Q_x Kg^T into the tile's score buffer: A and B K-major, steps
+            // k0 .. k1 - 1 of 8 (16 dims each)
+            auto s_steps = [&](uint32_t kslot, int k0, int k1) {
                 const uint64_t b0 = kslot ? dk1 : dk0;
 #pragma unroll
-                for (int kk = 0; kk < kAttD / 16; ++kk) {
+                for (int kk = k0; kk < k1; ++kk) {
                     const uint64_t off = ((kk >> 2) * kAttHalf + (kk & 3) * 32) >> 4;
                     mma_bf16_ss(dS, dq + off, b0 + off, idesc_s, kk > 0);
                 }
+            };
+            auto issue_s = [&](uint32_t kslot) {
+                s_steps(kslot, 0, kAttD / 16);
                 mma_commit(s_full(x));
             };
             // O_x += P V: A = P from tensor memory (keys 16kk.. in columns
-            // 8kk..), B = V MN-major (dims contiguous), 8 steps of 16 keys
-            auto issue_pv = [&](uint32_t vslot, bool acc) {
+            // 8kk..), B = V MN-major (dims contiguous), steps k0 .. k1 - 1 of 8
+            auto pv_steps = [&](uint32_t vslot, bool acc, int k0, int k1) {
                 const uint64_t b0 = vslot ? dv1 : dv0;
 #pragma unroll
-                for (int kk = 0; kk < kAttBN / 16; ++kk) {
+                for (int kk = k0; kk < k1; ++kk) {
                     const uint64_t off = ((kk >> 2) * (kAttTile / 2) + (kk & 3) * 2048) >> 4;
                     mma_bf16_ts(dS + kAttColO, dS + kk * 8, b0 + off, idesc_o, acc || kk > 0);
                 }
@@ -376,17 +380,27 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                         break;
                     }
                     tc_fence_after();
+                    // The turn passes four MMAs before the end of this issuer's
+                    // work for the stage: the other issuer wakes while they
+                    // are issued (its own MMAs do not depend on these).
                     if (j < n) {
                         ++pi;
-                        issue_pv(st, j > 0);
                         if (j + 1 < n) {
-                            issue_s((g + 1) & 1);
+                            pv_steps(st, j > 0, 0, kAttBN / 16);
+                            s_steps((g + 1) & 1, 0, 4);
+                            mbar_arrive(turn(x ^ 1));
+                            s_steps((g + 1) & 1, 4, kAttD / 16);
+                            mma_commit(s_full(x));
                             if (j + 2 == n) mma_commit(q_empty);   // that was the last score product
                         } else {
+                            pv_steps(st, j > 0, 0, 4);
+                            mbar_arrive(turn(x ^ 1));
+                            pv_steps(st, j > 0, 4, kAttBN / 16);
                             mma_commit(o_final(x));
                         }
+                    } else {
+                        mbar_arrive(turn(x ^ 1));
                     }
-                    mbar_arrive(turn(x ^ 1));
                     if (j + 1 == cur.nkv && has_next) {
                         // the next block's first product (after the turn is
                         // handed over, so the other tile's last products do
