@@ -104,6 +104,69 @@ __global__ void __launch_bounds__(kHeadsWarps * 32)
     }
 }
 
+// The same for head dimensions D = 8 << s (D / 8 chunks of 16 bytes divide
+// a warp's 32 lanes): one warp per row t, all H heads at once.  The row's
+// H * D elements are contiguous; lane l takes chunks l, l + 32, ... (so
+// every 512 bytes of the row are one coalesced warp access, and all of a
+// lane's loads are issued before any arithmetic), and a head's D / 8 chunks
+// sit in D / 8 consecutive lanes, summed with xor shuffles inside that group.
+template <int kChunksMax>
+__global__ void __launch_bounds__(kHeadsWarps * 32)
+    rmsnorm_rows_kernel(const __nv_bfloat16* __restrict__ X, int64_t ldx,
+                        const __nv_bfloat16* __restrict__ g, const __nv_bfloat16* __restrict__ g2,
+                        __nv_bfloat16* __restrict__ Y, int64_t ldy, int64_t T, int H, int D,
+                        float eps) {
+    grid_dep_wait();
+    grid_dep_launch();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * kHeadsWarps + warp;
+    if (t >= T) return;
+    const int gsz = D >> 3;                    // lanes (chunks) per head: 1 .. 32
+    const int n_chunks = H * gsz;
+    const int n_iter = (n_chunks + 31) >> 5;   // <= kChunksMax
+    const __nv_bfloat16* x = X + t * ldx;
+    __nv_bfloat16* y = Y + t * ldy;
+    uint4 u[kChunksMax];
+#pragma unroll
+    for (int i = 0; i < kChunksMax; ++i) {
+        const int ch = lane + 32 * i;
+        u[i] = (i < n_iter && ch < n_chunks) ? __ldg(reinterpret_cast<const uint4*>(x) + ch)
+                                             : make_uint4(0, 0, 0, 0);
+    }
+    const float inv_d = 1.f / static_cast<float>(D);
+#pragma unroll
+    for (int i = 0; i < kChunksMax; ++i) {
+        if (i >= n_iter) break;
+        const int ch = lane + 32 * i;
+        const uint32_t w[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
+        float ss = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            ss = fmaf(bf16lo(w[k]), bf16lo(w[k]), ss);
+            ss = fmaf(bf16hi(w[k]), bf16hi(w[k]), ss);
+        }
+        for (int o = 1; o < gsz; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (ch >= n_chunks) continue;
+        const float r = rsqrtf(ss * inv_d + eps);
+        const int d0 = (ch % gsz) * 8;        // position of the chunk within its head
+        const uint4 gu = __ldg(reinterpret_cast<const uint4*>(g + d0));
+        float gf[8] = {bf16lo(gu.x), bf16hi(gu.x), bf16lo(gu.y), bf16hi(gu.y),
+                       bf16lo(gu.z), bf16hi(gu.z), bf16lo(gu.w), bf16hi(gu.w)};
+        if (g2 != nullptr) {
+            const uint4 hu = __ldg(reinterpret_cast<const uint4*>(g2 + d0));
+            const float hf[8] = {bf16lo(hu.x), bf16hi(hu.x), bf16lo(hu.y), bf16hi(hu.y),
+                                 bf16lo(hu.z), bf16hi(hu.z), bf16lo(hu.w), bf16hi(hu.w)};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) gf[k] *= hf[k];
+        }
+        uint32_t out[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            out[k] = pack_bf16x2(bf16lo(w[k]) * gf[2 * k] * r, bf16hi(w[k]) * gf[2 * k + 1] * r);
+        reinterpret_cast<uint4*>(y)[ch] = make_uint4(out[0], out[1], out[2], out[3]);
+    }
+}
+
 // ------------------------------------------------------- attention kernel
 // A persistent CTA per SM walks its blocks of 256 query rows.  Blocks are
 // numbered longest first when causal; CTA c of G takes block r G + c from
@@ -588,6 +651,17 @@ cudaError_t launch_rmsnorm_heads(const void* X, int64_t ldx, const void* g, cons
                                  int64_t ldy, int64_t T, int H, int D, float eps, cudaStream_t s) {
     const int64_t items = T * H;
     if (items <= 0) return cudaSuccess;
+    // D a power of two from 8 to 256 and a row of at most 8 warp-wide chunks:
+    // one warp per row (the common case, e.g. 8 key heads of 128)
+    const bool pow2 = D >= 8 && D <= 256 && (D & (D - 1)) == 0;
+    if (pow2 && (static_cast<int64_t>(H) * (D / 8) + 31) / 32 <= 8) {
+        const int64_t grid_r = (T + kHeadsWarps - 1) / kHeadsWarps;
+        if (grid_r > INT32_MAX) return cudaErrorInvalidValue;
+        return launch_pdl(rmsnorm_rows_kernel<8>, static_cast<int>(grid_r), kHeadsWarps * 32, 0, s,
+                          static_cast<const __nv_bfloat16*>(X), ldx,
+                          static_cast<const __nv_bfloat16*>(g), static_cast<const __nv_bfloat16*>(g2),
+                          static_cast<__nv_bfloat16*>(Y), ldy, T, H, D, eps);
+    }
     const int64_t grid = (items + kHeadsWarps - 1) / kHeadsWarps;
     if (grid > INT32_MAX) return cudaErrorInvalidValue;
     return launch_pdl(rmsnorm_heads_kernel, static_cast<int>(grid), kHeadsWarps * 32, 0, s,

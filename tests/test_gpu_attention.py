@@ -184,13 +184,22 @@ def test_full_size_sampled_rows(rmm):
     assert_attention_close(O.cpu(), Q, K, V, gq, gk, w.eps, w.causal, "full size", qpos=qpos)
 
 
-def test_rmsnorm_heads_matches_oracle(rmm):
-    from sm_rmsnorm_matmul_gb300 import inputs
-    B, S, Hq, Hkv, D = 1, 333, 4, 2, 128
-    qkv, gq, gk = inputs.attention_inputs(B, S, Hq, Hkv, D, 44)
-    K = qkv.view(B * S, Hq + 2 * Hkv, D)[:, Hq:Hq + Hkv]
-    Y = rmm.rmsnorm_heads(K.cuda(), gk.cuda(), 1e-6).cpu()
-    ref = oracle.rmsnorm(K.reshape(-1, D), gk, 1e-6).reshape(S, Hkv, D)
+@pytest.mark.parametrize("T,H,D,pad", [
+    (333, 2, 128, 0),     # one warp per row (two heads of 128)
+    (130, 8, 128, 16),    # eight heads, row stride wider than the heads
+    (64, 8, 256, 0),      # the widest row the one-warp kernel takes (8 chunks per lane)
+    (77, 5, 64, 8),
+    (50, 3, 96, 0),       # D not a power of two: one warp per head
+    (20, 40, 64, 0),      # a row too wide for one warp: one warp per head
+])
+def test_rmsnorm_heads_matches_oracle(rmm, T, H, D, pad):
+    g = torch.Generator().manual_seed(T + H + D)
+    X = (torch.randn(T, H * D + pad, generator=g) * torch.exp(torch.randn(T, 1, generator=g))).to(torch.bfloat16)
+    gain = (0.5 + torch.rand(D, generator=g)).to(torch.bfloat16)
+    Xv = X[:, :H * D].view(T, H, D)
+    Y = rmm.rmsnorm_heads(X.cuda()[:, :H * D].view(T, H, D), gain.cuda(), 1e-6).cpu()
+    assert rmm.device_status() == 0
+    ref = oracle.rmsnorm(Xv.reshape(-1, D), gain, 1e-6).reshape(T, H, D)
     y = oracle.to_f64(Y)
     # one rounding of an fp32 value: the nearest bf16 or, at a boundary, its neighbour
     assert (np.abs(y - ref) <= 2.0 ** -7 * np.abs(ref) + 1e-30).all()
