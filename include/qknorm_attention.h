@@ -57,14 +57,16 @@ int rmsnorm_heads(const void* X, int64_t ldx, const void* g, void* Y, int64_t ld
  * at least the width of its tensor's heads; all pointers 16-byte aligned;
  * O may not overlap any input.  B = 0 or S = 0 is a no-op.
  *
- * Device arithmetic: the keys are normalised once into a library workspace
- * (per device and stream, grown on demand; a growing call synchronises the
- * stream and may not run under stream capture), each query tile is
- * normalised in shared memory with the scale and log2(e) folded in; both are
- * rounded to bf16 before the tensor cores.  Scores accumulate in fp32 in
- * tensor memory, the softmax weights are rounded to bf16 for the second
- * product, the output accumulates in fp32 and is rounded once.
- * Two kernel launches on `stream`.
+ * Device arithmetic: the keys are normalised once, with both gains, into a
+ * library workspace, Kg = bf16(RMSNorm(K; gk) * gq) (per device and stream,
+ * grown on demand; a growing call synchronises the stream and may not run
+ * under stream capture).  The raw bf16 queries enter the tensor cores, and
+ * each query row's scores are multiplied by its 1/RMS times scale * log2(e)
+ * in fp32 (the query normalisation is a row scale of the scores), so Kg is
+ * the only rounded operand.  Scores accumulate in fp32 in tensor memory, the
+ * softmax weights are rounded to bf16 for the second product, the output
+ * accumulates in fp32 and is rounded once.  Two kernel launches on `stream`:
+ * the key pass and a persistent attention kernel (one CTA per SM).
  */
 int qknorm_attention(const void* Q, int64_t ldq, const void* K, int64_t ldk, const void* V,
                      int64_t ldv, const void* gq, const void* gk, void* O, int64_t ldo,
