@@ -402,7 +402,10 @@ def bench_attention(torch, rmm, inputs, w, K, device, stream, l2, sampler=None):
     except (RuntimeError, TypeError):   # an older torch without enable_gqa or rms_norm
         unfused = None
     del copies
-    return {"secs": secs, "n_copies": n_copies, "status": status, "unfused_secs_per_step": unfused}
+    return {"secs": secs, "n_copies": n_copies, "status": status, "unfused_secs_per_step": unfused,
+            "l2": (f"rotating input/output copies: {n_copies} x {per / 1e6:.1f} MB > 3 x L2 "
+                   f"({l2 / 1e6:.0f} MB)") if n_copies > 1 else
+                  f"inputs ({per / 1e6:.0f} MB) larger than L2 ({l2 / 1e6:.0f} MB)"}
 
 
 def attention_entry(w, t, r, peaks, k):
@@ -412,7 +415,7 @@ def attention_entry(w, t, r, peaks, k):
          "hbm_gbs": round(w.bytes_algorithmic / t / 1e9, 1), "bound": "tensor",
          "roofline_frac": round(tflops / peaks["bf16_tflops"], 4),
          "frac_of_tensor_peak_sustained": round(tflops / peaks["bf16_tflops_sustained"], 4),
-         "copies": r["n_copies"], "device_status": r["status"]}
+         "copies": r["n_copies"], "l2": r["l2"], "device_status": r["status"]}
     if r.get("unfused_secs_per_step"):
         e["torch_rms_norm_sdpa_us"] = round(r["unfused_secs_per_step"] * 1e6, 3)
     return e

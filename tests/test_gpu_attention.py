@@ -168,6 +168,23 @@ def test_explicit_scale_and_eps(rmm):
     assert (err <= 2.0 ** -8 * wabs + 2.0 ** -8 * np.abs(ref) + 1e-5).all()
 
 
+@pytest.mark.parametrize("B,S,Hq,Hkv,causal", [
+    (2, 2048, 16, 4, False),   # full attention, two sequences
+    (1, 3000, 32, 8, True),    # ragged length: the last block half past the end, a partial last band
+])
+def test_large_sampled_rows(rmm, B, S, Hq, Hkv, causal):
+    from sm_rmsnorm_matmul_gb300 import inputs
+    D = 128
+    qkv, gq, gk = inputs.attention_inputs(B, S, Hq, Hkv, D, seed=S + Hq)
+    Q, K, V = inputs.split_qkv(qkv, B, S, Hq, Hkv, D)
+    Qd, Kd, Vd = inputs.split_qkv(qkv.cuda(), B, S, Hq, Hkv, D)
+    O = rmm.qknorm_attention(Qd, Kd, Vd, gq.cuda(), gk.cuda(), 1e-6, causal=causal)
+    torch.cuda.synchronize()
+    assert rmm.device_status() == 0
+    qpos = sorted({0, 127, 128, 255, 256, S - 129, S - 128, S - 1} | set(inputs.sample_rows(S, 24)))
+    assert_attention_close(O.cpu(), Q, K, V, gq, gk, 1e-6, causal, f"{B}x{S} {Hq}/{Hkv}", qpos=qpos)
+
+
 def test_full_size_sampled_rows(rmm):
     # the benchmark's workload (one 4096-token sequence, 32 query heads over
     # 8 key/value heads, causal), sampled query positions checked one by one
