@@ -185,6 +185,23 @@ def test_large_sampled_rows(rmm, B, S, Hq, Hkv, causal):
     assert_attention_close(O.cpu(), Q, K, V, gq, gk, 1e-6, causal, f"{B}x{S} {Hq}/{Hkv}", qpos=qpos)
 
 
+def test_output_row_stride(rmm):
+    # O written into the first Hq * D columns of a wider buffer (row stride
+    # Hq * D + 64): the same values as a dense output, the padding untouched
+    from sm_rmsnorm_matmul_gb300 import inputs
+    B, S, Hq, Hkv, D = 2, 300, 4, 2, 128
+    qkv, gq, gk = inputs.attention_inputs(B, S, Hq, Hkv, D, 61)
+    Qd, Kd, Vd = inputs.split_qkv(qkv.cuda(), B, S, Hq, Hkv, D)
+    dense = rmm.qknorm_attention(Qd, Kd, Vd, gq.cuda(), gk.cuda(), 1e-6, causal=True)
+    wide = torch.full((B * S, Hq * D + 64), 7.0, dtype=torch.bfloat16, device="cuda")
+    view = wide[:, :Hq * D].view(B, S, Hq, D)
+    rmm.qknorm_attention(Qd, Kd, Vd, gq.cuda(), gk.cuda(), 1e-6, causal=True, out=view)
+    torch.cuda.synchronize()
+    assert rmm.device_status() == 0
+    assert torch.equal(view.cpu(), dense.cpu())
+    assert bool((wide[:, Hq * D:] == 7.0).all())
+
+
 def test_full_size_sampled_rows(rmm):
     # the benchmark's workload (one 4096-token sequence, 32 query heads over
     # 8 key/value heads, causal), sampled query positions checked one by one
