@@ -281,7 +281,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kFused) prefetch_tmap(&tmG);
         // The previous kernel's writes are visible after grid_dep_wait(); the
         // next kernel may then be scheduled (its set-up overlaps this one).
-        grid_dep_wait();
+        // With the adapter the previous kernel is the launch that computes T,
+        // which itself waited for its own predecessor before letting this one
+        // start: X, g, W and B are then visible already, and only the adapter
+        // stage (which reads T) waits for it.
+        if (!kLora) grid_dep_wait();
         grid_dep_launch();
         if (static_cast<int>(blockIdx.x) < units) {
             const int u = blockIdx.x, t = u / split, sp = u - t * split;
@@ -293,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pro = static_cast<uint32_t>(min(S, kend - kb0));
             for (uint32_t i = 0; i < pro; ++i) {
                 const int kb = kb0 + static_cast<int>(i);
+                if (kLora && kb >= kb1) grid_dep_wait();
                 issue(i, kb < kb1 ? kb : a.k_blocks, mb, n0);
             }
         }
@@ -307,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // peers' barriers must be initialised before the first remote access:
     // announce it here, wait for the peers just before that access
     if (kSplit) cluster_arrive();
-    grid_dep_wait();
+    if (!kLora) grid_dep_wait();   // with the adapter only the producer reads T (see above)
     const uint32_t tmem = *tmem_holder;
 
     if (warp == 0) {
@@ -328,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = first; kb < kend; ++kb) {
                     const uint32_t s = ring.idx, ph = ring.phase;
                     if (!mbar_wait(empty(s), ph ^ 1, abort)) { ok = false; break; }
+                    if (kLora && kb >= kb1) grid_dep_wait();   // the adapter stage reads T
                     issue(s, kb < kb1 ? kb : a.k_blocks, mb, n0);
                     ++it;
                     ring.advance();
