@@ -590,11 +590,18 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
         if (!map_2d_store(&tmY, Y, M, glu ? N / 2 : N)) return RMM_ERR_INTERNAL;
         a.tmY = &tmY;
         // When the tiles leave a last wave at most half full, cut those tiles
-        // along K so that every CTA has a share of them.
+        // along K so that every CTA has a share of them.  When all the tiles
+        // fill at most half the SMs (one partial wave, e.g. a contraction with
+        // a narrow N such as the adapter's T), cut every tile, one piece per
+        // CTA, up to one CTA per SM (all resident at once, as the pieces'
+        // reduction needs).
         const int tiles = p.m_tiles * p.n_tiles;
-        const int rem = tiles % p.grid;
-        if (may_allocate && tiles > p.grid && rem > 0 && 2 * rem <= p.grid && p.k_blocks >= 2) {
-            const int pmax = p.grid / rem;
+        const int sms = d.sm_count > 0 ? d.sm_count : 1;
+        const bool few = tiles <= p.grid && 2 * tiles <= sms;
+        const int grid = few ? sms : p.grid;
+        const int rem = tiles % grid;
+        if (may_allocate && (tiles > grid || few) && rem > 0 && 2 * rem <= grid && p.k_blocks >= 2) {
+            const int pmax = grid / rem;
             const int kbp = (p.k_blocks + pmax - 1) / pmax;
             const int pieces = (p.k_blocks + kbp - 1) / kbp;
             if (pieces >= 2) {
@@ -609,6 +616,8 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
                 a.ws_acc = w.acc;
                 a.ws_ss = w.ss;
                 a.ws_count = w.counters;
+                // every tile cut: one CTA per piece
+                if (few) a.grid = tiles * pieces;
             }
         }
     }
