@@ -3,11 +3,13 @@
 // The operation is the "QKNorm + Attention" workload of the Mirage review
 // page's benchmark table (section 5): per-head RMSNorm with a gain on every
 // query and key head, then softmax attention (causal or full) with grouped
-// key/value heads.  Two kernels:
+// key/value heads.  Two launches:
 //
-//   rmsnorm_heads_kernel    normalises every key head once (memory-bound; one
-//                           warp per head row), into a bf16 workspace, with
-//                           the query gain gq folded in: Kg = bf16(Kn * gq);
+//   rmsnorm_rows_kernel     normalises every key head once (memory-bound; one
+//   (rmsnorm_heads_kernel   warp per token and all its heads, or one warp per
+//    for other D)           head when D is not a power of two), into a bf16
+//                           workspace, with the query gain gq folded in:
+//                           Kg = bf16(Kn * gq);
 //   qknorm_attention_kernel persistent, one CTA per SM walking blocks of 256
 //                           query rows of one head (two 128-row tiles): for
 //                           each 128-key tile S' = Q Kg^T (the raw bf16
@@ -22,7 +24,7 @@
 // reads the query tile as it was loaded.  Normalising each key once, not
 // once per query tile that reads it, is the choice for GB300: a key tile is
 // read by S/128 query tiles of every head in its group, and the workspace
-// round trip costs two reads of K.
+// round trip costs one write and one read of the normalised keys.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
