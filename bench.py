@@ -247,7 +247,8 @@ def n_rotating_copies(w, l2_bytes):
 
 def time_graph(torch, stream, step_fn, n_copies, K, chunk=500):
     """Capture K back-to-back steps (step i uses copy i % n_copies) in CUDA
-    graphs of at most `chunk` steps, replay them once, return seconds."""
+    graphs of at most `chunk` steps, replay them once, return seconds, the
+    wall-clock window and the graphs (which replay_times can run again)."""
     graphs = []
     done = 0
     while done < K:
@@ -275,10 +276,28 @@ def time_graph(torch, stream, step_fn, n_copies, K, chunk=500):
     return start.elapsed_time(end) / 1e3, (t0, t1), graphs
 
 
+def replay_times(torch, stream, graphs, n):
+    """Replay the captured K steps n more times; seconds of each replay."""
+    out = []
+    for _ in range(n):
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for gr in graphs:
+                gr.replay()
+            end.record(stream)
+        end.synchronize()
+        out.append(start.elapsed_time(end) / 1e3)
+    return out
+
+
 def bench_workload(torch, rmm, inputs, w, K, W_warm, device, stream, l2, with_unfused=True,
-                   sampler=None, barrier=None, gated=False, weight_nk=False, lora_r=0):
+                   sampler=None, barrier=None, gated=False, weight_nk=False, lora_r=0, replays=0):
     """gated: time the gated form (Y [M, N/2]); weight_nk: W stored [N, K];
-    lora_r > 0: the low-rank adapter form with rank lora_r."""
+    lora_r > 0: the low-rank adapter form with rank lora_r; replays > 0: replay
+    the timed steps that many more times (reported beside the timed run, which
+    alone gives the result)."""
     n_copies = n_rotating_copies(w, l2)
     F = w.N // 2
     host, copies = make_copies(w, n_copies, device, torch, inputs, out_cols=F if gated else None,
@@ -310,9 +329,10 @@ def bench_workload(torch, rmm, inputs, w, K, W_warm, device, stream, l2, with_un
         secs = barrier(secs)
     if sampler:
         sampler.mark(*window)
+    extra = replay_times(torch, stream, graphs, replays) if replays else []
     status = rmm.device_status(stream)
     del graphs
-    res = {"secs": secs, "n_copies": n_copies, "status": status, "host": host,
+    res = {"secs": secs, "n_copies": n_copies, "status": status, "host": host, "replays": [secs] + extra,
            "copies": copies, "path": 1 if gated else rmm.dispatch_path(w.M, w.K, w.N),
            "plan": rmm.describe_plan(w.M, w.K, w.N, gated=gated)}
     if with_unfused:
@@ -590,7 +610,7 @@ def main():
     with ClockSampler(gpu_id) as sampler:
         main_res = bench_workload(torch, rmm, inputs, w, args.steps, args.warmup, device,
                                   stream, l2, with_unfused=True, sampler=sampler,
-                                  barrier=barrier)
+                                  barrier=barrier, replays=4 if ws == 1 else 0)
         host = main_res["host"]
         e2e_steps = max(3, min(args.steps, 200))
         e2e_secs, h2d, d2h = e2e_bench(torch, rmm, w, host, device, stream, e2e_steps)
@@ -705,6 +725,11 @@ def main():
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_secs / e2e_steps * 1e3, 4), "steps": e2e_steps},
         "gpu_launches": K,
+        # the same K steps replayed again (the timed run first): spread of the measurement
+        "graph_replays": {"count": len(main_res["replays"]),
+                          "median_ms_per_step": round(statistics.median(main_res["replays"]) / K * 1e3, 6),
+                          "min_ms_per_step": round(min(main_res["replays"]) / K * 1e3, 6),
+                          "max_ms_per_step": round(max(main_res["replays"]) / K * 1e3, 6)},
         "clocks": clocks,
         "device_status": main_res["status"],
     }
