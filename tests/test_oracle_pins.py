@@ -171,3 +171,59 @@ def test_attention_positions_select_rows(lib):
     full = oracle.attention(Q, K, V, 0.3, causal=True, lib=lib)
     part = oracle.attention(Q, K, V, 0.3, causal=True, qpos=[8, 0, 3], lib=lib)
     assert np.array_equal(part, full[:, [8, 0, 3]])
+
+
+# Random shapes against torch's float64 library routines (an implementation
+# the oracle does not call): every form, several sizes, causal and full.
+def _torch():
+    return pytest.importorskip("torch")
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_forms_match_torch_on_random_shapes(lib, seed):
+    torch = _torch()
+    F = torch.nn.functional
+    rng = np.random.default_rng(100 + seed)
+    M, K, N, R = (int(v) for v in rng.integers(1, 40, 4))
+    N += N % 2   # the gated form needs an even width
+    eps = float(10.0 ** rng.uniform(-6, 0))
+    X = rng.standard_normal((M, K)) * np.exp(rng.standard_normal((M, 1)))
+    g = rng.uniform(0.5, 1.5, K)
+    W = rng.standard_normal((K, N))
+    A, B = rng.standard_normal((K, R)), rng.standard_normal((R, N))
+    Xn = F.rms_norm(torch.tensor(X), (K,), torch.tensor(g), eps)
+    Z = Xn @ torch.tensor(W)
+    ref = Z.numpy()
+    assert np.abs(oracle.rmsnorm_matmul(X, g, W, eps, lib=lib) - ref).max() <= 1e-12 * (1 + np.abs(ref).max())
+    half = N // 2
+    gated = (F.silu(Z[:, :half]) * Z[:, half:]).numpy()
+    got = oracle.rmsnorm_matmul_swiglu(X, g, W, eps, lib=lib)
+    assert np.abs(got - gated).max() <= 1e-12 * (1 + np.abs(gated).max())
+    lora = (Xn @ (torch.tensor(W) + torch.tensor(A) @ torch.tensor(B))).numpy()
+    got = oracle.rmsnorm_matmul_lora(X, g, W, A, B, eps, lib=lib)
+    assert np.abs(got - lora).max() <= 1e-12 * (1 + np.abs(lora).max())
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_attention_matches_torch_on_random_shapes(lib, seed):
+    torch = _torch()
+    F = torch.nn.functional
+    rng = np.random.default_rng(200 + seed)
+    Hkv = int(rng.integers(1, 4))
+    Hq = Hkv * int(rng.integers(1, 4))
+    B, S, D = int(rng.integers(1, 3)), int(rng.integers(1, 40)), int(rng.integers(2, 24))
+    causal = bool(seed % 2)
+    eps = float(10.0 ** rng.uniform(-6, -1))
+    scale = float(rng.uniform(0.05, 1.0))
+    Q = rng.standard_normal((B, S, Hq, D)) * np.exp(rng.standard_normal((B, S, Hq, 1)))
+    K = rng.standard_normal((B, S, Hkv, D)) * np.exp(rng.standard_normal((B, S, Hkv, 1)))
+    V = rng.standard_normal((B, S, Hkv, D))
+    gq, gk = rng.uniform(0.5, 1.5, D), rng.uniform(0.5, 1.5, D)
+    o = oracle.qknorm_attention(Q, K, V, gq, gk, eps, scale=scale, causal=causal, lib=lib)
+    qn = F.rms_norm(torch.tensor(Q), (D,), torch.tensor(gq), eps)
+    kn = F.rms_norm(torch.tensor(K), (D,), torch.tensor(gk), eps)
+    rep = Hq // Hkv
+    ref = F.scaled_dot_product_attention(qn.transpose(1, 2), kn.repeat_interleave(rep, dim=2).transpose(1, 2),
+                                         torch.tensor(V).repeat_interleave(rep, dim=2).transpose(1, 2),
+                                         is_causal=causal, scale=scale).transpose(1, 2).numpy()
+    assert np.abs(o - ref).max() <= 1e-12 * (1 + np.abs(ref).max())
