@@ -847,6 +847,7 @@ int qknorm_attention(const void* Q, int64_t ldq, const void* K, int64_t ldk, con
     a.wait_limit_us = g_wait_limit_us.load();
     a.O = O;
     a.ldo = ldo;
+    a.test_skip_loads = g_skip_sends.load();
     return rmm::launch_qknorm_attention(tmQ, tmK, tmV, a, stream) == cudaSuccess
                ? RMM_OK
                : RMM_ERR_LAUNCH;

@@ -337,6 +337,9 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                         const uint32_t par = (g & 1) ? ((g - 1) >> 1) & 1 : ((g >> 1) - 1) & 1;
                         if (!mbar_wait(kv_empty(st), par, abort)) { ok = false; break; }
                     }
+                    // test hook: leave out the first stage, so that the issuers'
+                    // waits for it run out (the timeout path, without a fault)
+                    if (a.test_skip_loads && g == 0) continue;
                     const bool last = j + 1 == cur.nkv;
                     const bool kn = !last || has_next;
                     mbar_arrive_expect_tx(kv_full(st), kn ? 2 * kAttTile : kAttTile);

@@ -116,6 +116,7 @@ struct AttnLaunch {
     int wait_limit_us;
     void* O;          // output [B, S, Hq, 128], row stride ldo elements
     long long ldo;
+    int test_skip_loads;   // test hook: the producer leaves out its first K/V stage
 };
 
 // Y[t,h,:] = RMSNorm(X[t,h,:]; g, eps) * g2 for T rows of H heads of D

@@ -2,7 +2,8 @@
 
 A test hook makes the row-tile kernel's K-split reduction skip the stores of
 its partials, so that every owning CTA's wait for them runs out (after a
-shortened limit).  The kernel must then record RMM_ERR_DEVICE_TIMEOUT, skip
+shortened limit); for the attention kernel it makes the loader leave out its
+first key/value stage.  The kernel must then record RMM_ERR_DEVICE_TIMEOUT, skip
 its remaining work, free its tensor memory and exit; rmm_device_status()
 reports it; and the next call on the same context runs normally.
 """
@@ -48,3 +49,28 @@ def test_timeout_is_reported_and_the_context_recovers(rmm):
 
 def test_hook_rejects_negative_limit(rmm):
     assert rmm.lib().rmm_test_hooks(0, -1) == 1
+
+
+def test_attention_timeout_is_reported_and_the_context_recovers(rmm):
+    # the same hook makes the attention loader leave out its first key/value
+    # stage: both MMA issuers' waits for it run out, every role leaves its
+    # loop, and the CTA frees its tensor memory and exits
+    from sm_rmsnorm_matmul_gb300 import inputs
+    B, S, Hq, Hkv, D = 1, 512, 4, 2, 128
+    qkv, gq, gk = inputs.attention_inputs(B, S, Hq, Hkv, D, seed=7)
+    Qd, Kd, Vd = inputs.split_qkv(qkv.cuda(), B, S, Hq, Hkv, D)
+    l = rmm.lib()
+    assert rmm.device_status() == 0
+    assert l.rmm_test_hooks(1, 50_000_000) == 0
+    try:
+        rmm.qknorm_attention(Qd, Kd, Vd, gq.cuda(), gk.cuda(), 1e-6, causal=True)
+        assert rmm.device_status() == 5                  # RMM_ERR_DEVICE_TIMEOUT
+    finally:
+        assert l.rmm_test_hooks(0, 0) == 0
+    O = rmm.qknorm_attention(Qd, Kd, Vd, gq.cuda(), gk.cuda(), 1e-6, causal=True)
+    torch.cuda.synchronize()
+    assert rmm.device_status() == 0
+    Q, K, V = inputs.split_qkv(qkv, B, S, Hq, Hkv, D)
+    ref = oracle.qknorm_attention(Q, K, V, gq, gk, 1e-6, causal=True)
+    bad, max_abs, _ = oracle.tolerance_violations(O.cpu(), ref, atol=3e-2, rtol=3e-2)
+    assert bad == 0, max_abs
