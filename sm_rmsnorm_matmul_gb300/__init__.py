@@ -222,8 +222,12 @@ def _check_heads(name, t):
     tokens are a constant stride apart (a column block of a [B*S, width]
     matrix qualifies).  Returns that token stride in elements."""
     import torch
-    if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
-        raise TypeError(f"{name} must be a bfloat16 CUDA tensor")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
     if t.dim() != 4:
         raise ValueError(f"{name} must be [B, S, heads, D], got shape {tuple(t.shape)}")
     B, S, H, D = t.shape

@@ -187,3 +187,27 @@ def test_no_oracle_in_product_path():
                     src = fh.read()
                 assert not re.search(r"^\s*(import|from)\s+oracle", src, flags=re.M), f
                 assert "rmm_oracle" not in src, f
+
+
+def test_attention_binding_checks_tensors(lib):
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 8, 4, 128, dtype=torch.bfloat16)
+    k = torch.zeros(1, 8, 2, 128, dtype=torch.bfloat16)
+    g = torch.ones(128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        rmm.qknorm_attention(q, k, k, g, g)                       # CPU tensors
+    with pytest.raises(TypeError, match="bfloat16"):
+        rmm.qknorm_attention(q.float(), k, k, g, g)
+    with pytest.raises(ValueError, match="CUDA"):
+        rmm.rmsnorm_heads(q[0], g)                                 # CPU tensor
+    with pytest.raises(TypeError, match="torch.Tensor"):
+        rmm.qknorm_attention([0], k, k, g, g)
+
+
+def test_attention_abi_rejects_grouping_and_head_dim(lib):
+    f = lib.qknorm_attention
+    # (Q, ldq, K, ldk, V, ldv, gq, gk, O, ldo, B, S, Hq, Hkv, D, eps, scale, causal)
+    assert f(A16, 768, A16 + 512, 768, A16 + 768, 768, B16, B16 + 256, C16, 512,
+             1, 16, 5, 2, 128, 1e-6, 0.0, 1, None) == 1               # 5 query heads over 2
+    assert f(A16, 384, A16 + 256, 384, A16 + 320, 384, B16, B16 + 256, C16, 256,
+             1, 16, 4, 1, 64, 1e-6, 0.0, 1, None) == 1                # D = 64 is not built
