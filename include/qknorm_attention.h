@@ -53,7 +53,7 @@ int rmsnorm_heads(const void* X, int64_t ldx, const void* g, void* Y, int64_t ld
  * are [D].  scale <= 0 selects 1/sqrt(D).  causal != 0 restricts query i to
  * keys j <= i.
  *
- * Requirements: D = 128; Hq a multiple of Hkv; every ld a multiple of 8 and
+ * Requirements: D = 64 or 128; Hq a multiple of Hkv; every ld a multiple of 8 and
  * at least the width of its tensor's heads; all pointers 16-byte aligned;
  * O may not overlap any input.  B = 0 or S = 0 is a no-op.
  *

@@ -798,7 +798,7 @@ int qknorm_attention(const void* Q, int64_t ldq, const void* K, int64_t ldk, con
                      int64_t S, int64_t Hq, int64_t Hkv, int64_t D, float eps, float scale,
                      int causal, cudaStream_t stream) {
     if (B < 0 || S < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return RMM_ERR_INVALID_ARG;
-    if (D != rmm::kAttD) return RMM_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return RMM_ERR_INVALID_ARG;
     if (!std::isfinite(eps) || eps < 0.f || !std::isfinite(scale)) return RMM_ERR_INVALID_ARG;
     if (Hq > 4096 || ldq < Hq * D || ldo < Hq * D || ldk < Hkv * D || ldv < Hkv * D)
         return RMM_ERR_INVALID_ARG;
@@ -818,7 +818,8 @@ int qknorm_attention(const void* Q, int64_t ldq, const void* K, int64_t ldk, con
     DeviceInfo d;
     rc = current_device(&dev, &d);
     if (rc != RMM_OK) return rc;
-    if (static_cast<size_t>(d.smem_optin) < rmm::attn_smem_bytes()) return RMM_ERR_UNSUPPORTED_DEVICE;
+    if (static_cast<size_t>(d.smem_optin) < rmm::attn_smem_bytes(static_cast<int>(D)))
+        return RMM_ERR_UNSUPPORTED_DEVICE;
     void* khat = nullptr;
     rc = get_khat_buffer(dev, stream, static_cast<size_t>(B * S * Hkv * D) * 2, &khat);
     if (rc != RMM_OK) return rc;
@@ -834,6 +835,7 @@ int qknorm_attention(const void* Q, int64_t ldq, const void* K, int64_t ldk, con
         return RMM_ERR_LAUNCH;
     rmm::AttnLaunch a{};
     a.S = static_cast<int>(S);
+    a.D = static_cast<int>(D);
     a.Hq = static_cast<int>(Hq);
     a.group = static_cast<int>(Hq / Hkv);
     a.n_qb = static_cast<int>(n_qb);

@@ -197,18 +197,16 @@ __global__ void __launch_bounds__(kHeadsWarps * 32)
 // gap.  Every barrier's parity is a count kept by the roles that use it.
 constexpr int kAttThreads = 352;    // warp 0 TMA, 1 MMA A + TMEM, 2-5 softmax A, 6-9 softmax B, 10 MMA B
 constexpr int kAttStages = 2;       // K and V slots
-constexpr uint32_t kAttTile = kAttBM * kAttD * 2;   // 32 KB: a Q, K or V tile
-constexpr uint32_t kAttHalf = kAttTile / 2;         // 64 columns of a tile (SW128 box)
-constexpr uint32_t kAttOffQ = 0;                    // query tiles A and B
-constexpr uint32_t kAttOffK = kAttOffQ + 2 * kAttTile;
-constexpr uint32_t kAttOffV = kAttOffK + kAttStages * kAttTile;
-constexpr uint32_t kAttOffBar = kAttOffV + kAttStages * kAttTile;
+constexpr uint32_t kAttBox = kAttBM * 64 * 2;      // 16 KB: [128 rows][64 columns], one SW128 box
 constexpr uint32_t kAttNumBars = 18;
-constexpr uint32_t kAttOffMisc = kAttOffBar + 256;
-constexpr uint32_t kAttSmem = kAttOffMisc + 16 + 1024;   // + alignment slack
 static_assert(kAttNumBars * 8 <= 256, "barrier area");
+// Shared memory for head dimension D: query tiles A and B, two K and two V
+// tiles (each [128][D]), barriers, the TMEM address and abort words.
+constexpr uint32_t att_tile_bytes(int D) { return kAttBM * D * 2; }
+constexpr uint32_t att_off_bar(int D) { return (2 + 2 * kAttStages) * att_tile_bytes(D); }
+constexpr uint32_t att_smem_bytes(int D) { return att_off_bar(D) + 256 + 16 + 1024; }   // + alignment slack
 // Tensor memory, per query tile x (columns x * 256 ..): the score buffer S
-// (P overwrites its first 64 columns, two bf16 per column), then O.
+// (P overwrites its first 64 columns, two bf16 per column), then O (D columns).
 constexpr uint32_t kAttColO = 128, kAttTmemCols = 512;
 constexpr float kAttRescale = 8.f;   // rescale O only when the row max grows by > 2^8
 
@@ -239,17 +237,23 @@ __device__ __forceinline__ AttnBlock attn_block(const AttnLaunch& a, int k) {
     return B;
 }
 
+template <int kD>   // head dimension: 64 or 128
 __global__ void __launch_bounds__(kAttThreads, 1)
     qknorm_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                             const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV, AttnLaunch a) {
+    static_assert(kD == 64 || kD == 128, "head dimension");
+    constexpr uint32_t kTile = att_tile_bytes(kD);   // a Q, K or V tile
+    constexpr int kBoxes = kD / 64;                  // SW128 boxes of 64 columns per tile
+    constexpr uint32_t kOffK = 2 * kTile, kOffV = kOffK + kAttStages * kTile;
+    constexpr uint32_t kOffBar = att_off_bar(kD), kOffMisc = kOffBar + 256;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t sq = sbase + kAttOffQ, sk = sbase + kAttOffK, sv = sbase + kAttOffV;
-    const uint32_t bar0 = sbase + kAttOffBar;
+    const uint32_t sq = sbase, sk = sbase + kOffK, sv = sbase + kOffV;
+    const uint32_t bar0 = sbase + kOffBar;
     const uint32_t q_full = bar0, q_empty = bar0 + 8, k0_full = bar0 + 16;
     auto kv_full = [&](uint32_t i) { return bar0 + 24 + 8 * i; };
     auto kv_empty = [&](uint32_t i) { return bar0 + 40 + 8 * i; };
@@ -259,8 +263,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     auto o_final = [&](int x) { return bar0 + 104 + 8 * x; };
     auto o_empty = [&](int x) { return bar0 + 120 + 8 * x; };
     const uint32_t mmadone = bar0 + 136;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kAttOffMisc);
-    volatile int* abort = reinterpret_cast<volatile int*>(smem + kAttOffMisc + 4);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+    volatile int* abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
     // the CTA's r-th block, or -1 (once a band has none, no later band has)
     auto block_id = [&](int r) {
         const int G = gridDim.x, c = blockIdx.x;
@@ -309,19 +313,20 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             const uint64_t keep = policy_evict_last();   // K and V tiles are re-read
             const uint64_t once = policy_evict_first();  // the query tiles are read once
             auto load_q = [&](const AttnBlock& B) {
-                mbar_arrive_expect_tx(q_full, 2 * kAttTile);
+                mbar_arrive_expect_tx(q_full, 2 * kTile);
 #pragma unroll
-                for (int x = 0; x < 2; ++x) {
-                    tma_load_3d(sq + x * kAttTile, &tmQ, q_full, B.h * kAttD, B.q0 + x * kAttBM, B.b, once);
-                    tma_load_3d(sq + x * kAttTile + kAttHalf, &tmQ, q_full, B.h * kAttD + 64,
-                                B.q0 + x * kAttBM, B.b, once);
-                }
+                for (int x = 0; x < 2; ++x)
+#pragma unroll
+                    for (int bx = 0; bx < kBoxes; ++bx)
+                        tma_load_3d(sq + x * kTile + bx * kAttBox, &tmQ, q_full, B.h * kD + bx * 64,
+                                    B.q0 + x * kAttBM, B.b, once);
             };
             AttnBlock cur = attn_block(a, block_id(0));
             load_q(cur);
-            mbar_arrive_expect_tx(k0_full, kAttTile);
-            tma_load_3d(sk, &tmK, k0_full, cur.c * kAttD, 0, cur.b, keep);
-            tma_load_3d(sk + kAttHalf, &tmK, k0_full, cur.c * kAttD + 64, 0, cur.b, keep);
+            mbar_arrive_expect_tx(k0_full, kTile);
+#pragma unroll
+            for (int bx = 0; bx < kBoxes; ++bx)
+                tma_load_3d(sk + bx * kAttBox, &tmK, k0_full, cur.c * kD + bx * 64, 0, cur.b, keep);
             uint32_t g = 0;   // stages issued
             uint32_t t = 0;   // blocks begun
             bool ok = true;
@@ -342,20 +347,22 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                     if (a.test_skip_loads && g == 0) continue;
                     const bool last = j + 1 == cur.nkv;
                     const bool kn = !last || has_next;
-                    mbar_arrive_expect_tx(kv_full(st), kn ? 2 * kAttTile : kAttTile);
-                    const uint32_t vd = sv + st * kAttTile;
-                    // four boxes of [64 keys][64 dims]: box (kk, n) at (2 kk + n) * 8 KB
+                    mbar_arrive_expect_tx(kv_full(st), kn ? 2 * kTile : kTile);
+                    const uint32_t vd = sv + st * kTile;
+                    // boxes of [64 keys][64 dims]: box (kk, n) at (kBoxes kk + n) * 8 KB
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk)
 #pragma unroll
-                        for (int n = 0; n < 2; ++n)
-                            tma_load_3d(vd + (2 * kk + n) * (kAttTile / 4), &tmV, kv_full(st),
-                                        cur.c * kAttD + n * 64, j * kAttBN + kk * 64, cur.b, keep);
+                        for (int n = 0; n < kBoxes; ++n)
+                            tma_load_3d(vd + (kBoxes * kk + n) * (kAttBox / 2), &tmV, kv_full(st),
+                                        cur.c * kD + n * 64, j * kAttBN + kk * 64, cur.b, keep);
                     if (kn) {
-                        const uint32_t kd = sk + ((g + 1) & 1) * kAttTile;
+                        const uint32_t kd = sk + ((g + 1) & 1) * kTile;
                         const int kc = last ? nxt.c : cur.c, kj = last ? 0 : j + 1, kb = last ? nxt.b : cur.b;
-                        tma_load_3d(kd, &tmK, kv_full(st), kc * kAttD, kj * kAttBN, kb, keep);
-                        tma_load_3d(kd + kAttHalf, &tmK, kv_full(st), kc * kAttD + 64, kj * kAttBN, kb, keep);
+#pragma unroll
+                        for (int bx = 0; bx < kBoxes; ++bx)
+                            tma_load_3d(kd + bx * kAttBox, &tmK, kv_full(st), kc * kD + bx * 64, kj * kAttBN,
+                                        kb, keep);
                     }
                 }
                 if (!ok || !has_next) break;
@@ -376,14 +383,14 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         if (lane == 0) {
             const int x = warp == 1 ? 0 : 1;
             constexpr uint32_t idesc_s = idesc_bf16_f32(kAttBM, kAttBN, false, false);
-            constexpr uint32_t idesc_o = idesc_bf16_f32(kAttBM, kAttD, false, true);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(kAttBM, kD, false, true);
             // Descriptors are built once; a step adds its byte offset >> 4 to
             // the start-address field (every tile lies below 256 KB, so the
             // 14-bit field never carries).
-            const uint64_t dq = sdesc_sw128(sq + x * kAttTile, 16, 1024);
-            const uint64_t dk0 = sdesc_sw128(sk, 16, 1024), dk1 = sdesc_sw128(sk + kAttTile, 16, 1024);
-            const uint64_t dv0 = sdesc_sw128(sv, kAttTile / 4, 1024);
-            const uint64_t dv1 = sdesc_sw128(sv + kAttTile, kAttTile / 4, 1024);
+            const uint64_t dq = sdesc_sw128(sq + x * kTile, 16, 1024);
+            const uint64_t dk0 = sdesc_sw128(sk, 16, 1024), dk1 = sdesc_sw128(sk + kTile, 16, 1024);
+            const uint64_t dv0 = sdesc_sw128(sv, kAttBox / 2, 1024);
+            const uint64_t dv1 = sdesc_sw128(sv + kTile, kAttBox / 2, 1024);
             const uint32_t dS = tmem + x * 256;
             // S = Q_x Kg^T into the tile's score buffer: A and B K-major, steps
             // k0 .. k1 - 1 of 8 (16 dims each)
@@ -391,12 +398,12 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                 const uint64_t b0 = kslot ? dk1 : dk0;
 #pragma unroll
                 for (int kk = k0; kk < k1; ++kk) {
-                    const uint64_t off = ((kk >> 2) * kAttHalf + (kk & 3) * 32) >> 4;
+                    const uint64_t off = ((kk >> 2) * kAttBox + (kk & 3) * 32) >> 4;
                     mma_bf16_ss(dS, dq + off, b0 + off, idesc_s, kk > 0);
                 }
             };
             auto issue_s = [&](uint32_t kslot) {
-                s_steps(kslot, 0, kAttD / 16);
+                s_steps(kslot, 0, kD / 16);
                 mma_commit(s_full(x));
             };
             // O_x += P V: A = P from tensor memory (keys 16kk.. in columns
@@ -405,7 +412,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                 const uint64_t b0 = vslot ? dv1 : dv0;
 #pragma unroll
                 for (int kk = k0; kk < k1; ++kk) {
-                    const uint64_t off = ((kk >> 2) * (kAttTile / 2) + (kk & 3) * 2048) >> 4;
+                    const uint64_t off = ((kk >> 2) * (kTile / 2) + (kk & 3) * 2048) >> 4;
                     mma_bf16_ts(dS + kAttColO, dS + kk * 8, b0 + off, idesc_o, acc || kk > 0);
                 }
             };
@@ -457,7 +464,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                             pv_steps(st, j > 0, 0, kAttBN / 16);
                             s_steps((g + 1) & 1, 0, 4);
                             mbar_arrive(turn(x ^ 1));
-                            s_steps((g + 1) & 1, 4, kAttD / 16);
+                            s_steps((g + 1) & 1, 4, kD / 16);
                             mma_commit(s_full(x));
                             if (j + 2 == n) mma_commit(q_empty);   // that was the last score product
                         } else {
@@ -492,7 +499,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         const int row = q * 32 + lane;           // query row of the tile
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t swz = static_cast<uint32_t>(row & 7);
-        const uint32_t srow = sq + x * kAttTile + static_cast<uint32_t>(row) * 128;
+        const uint32_t srow = sq + x * kTile + static_cast<uint32_t>(row) * 128;
         const uint32_t sbuf = tmem + x * 256 + lane_base;
         const uint32_t obuf = sbuf + kAttColO;
         uint32_t t = 0, si = 0, ob = 0;   // blocks, S tiles consumed, blocks with output
@@ -506,10 +513,10 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             // the row's scale r * scale * log2(e); the query tile is only read
             float ss[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf)
+            for (int hf = 0; hf < kBoxes; ++hf)
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc) {
-                    const uint4 u = lds128(srow + hf * kAttHalf + ((cc ^ swz) << 4));
+                    const uint4 u = lds128(srow + hf * kAttBox + ((cc ^ swz) << 4));
                     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -519,7 +526,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                 }
             __syncwarp();
             if (lane == 0) mbar_arrive(q_empty);
-            const float rc = rsqrtf(((ss[0] + ss[1]) + (ss[2] + ss[3])) * (1.f / kAttD) + a.eps) * a.qscale;
+            const float rc = rsqrtf(((ss[0] + ss[1]) + (ss[2] + ss[3])) * (1.f / kD) + a.eps) * a.qscale;
             const uint64_t rc2 = pack_f32x2(rc, rc);
             float m_ref = 0.f, l = 0.f;
             for (int j = 0; j < n; ++j, ++si) {
@@ -579,7 +586,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                     // O holds this block's P_0..P_{j-1} V, complete: S_j was
                     // issued after the last of those products and has completed
 #pragma unroll 1
-                    for (int cc = 0; cc < kAttD / 32; ++cc) {
+                    for (int cc = 0; cc < kD / 32; ++cc) {
                         uint32_t o[32];
                         tmem_ld_32x32(obuf + cc * 32, o);
 #pragma unroll
@@ -599,10 +606,10 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                 tc_fence_after();
                 const float inv_l = 1.f / l;
                 __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.O) +
-                                      (static_cast<int64_t>(B.b) * a.S + qpos) * a.ldo + B.h * kAttD;
+                                      (static_cast<int64_t>(B.b) * a.S + qpos) * a.ldo + B.h * kD;
                 const bool valid = qpos < a.S;
 #pragma unroll
-                for (int cc = 0; cc < kAttD / 32; ++cc) {
+                for (int cc = 0; cc < kD / 32; ++cc) {
                     uint32_t o[32];
                     tmem_ld_32x32(obuf + cc * 32, o);
 #pragma unroll
@@ -650,7 +657,7 @@ cudaError_t launch_pdl(void (*kern)(Args...), int grid, int block, size_t smem, 
 
 }  // namespace
 
-size_t attn_smem_bytes() { return kAttSmem; }
+size_t attn_smem_bytes(int D) { return att_smem_bytes(D); }
 
 cudaError_t launch_rmsnorm_heads(const void* X, int64_t ldx, const void* g, const void* g2, void* Y,
                                  int64_t ldy, int64_t T, int H, int D, float eps, cudaStream_t s) {
@@ -677,19 +684,22 @@ cudaError_t launch_rmsnorm_heads(const void* X, int64_t ldx, const void* g, cons
 
 cudaError_t launch_qknorm_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                     const CUtensorMap& tmV, const AttnLaunch& a, cudaStream_t s) {
-    // the shared-memory limit is a per-device attribute of the function
-    static std::atomic<bool> attr_set[64];
+    // the shared-memory limit is a per-device attribute of each function
+    static std::atomic<bool> attr_set[2][64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev].load()) {
-        e = cudaFuncSetAttribute(qknorm_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kAttSmem);
+    if (a.D != 64 && a.D != 128) return cudaErrorInvalidValue;
+    const int v = a.D == 128;
+    auto kern = v ? qknorm_attention_kernel<128> : qknorm_attention_kernel<64>;
+    const uint32_t smem = att_smem_bytes(a.D);
+    if (!attr_set[v][dev].load()) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        attr_set[dev].store(true);
+        attr_set[v][dev].store(true);
     }
-    return launch_pdl(qknorm_attention_kernel, a.grid, kAttThreads, kAttSmem, s, tmQ, tmK, tmV, a);
+    return launch_pdl(kern, a.grid, kAttThreads, smem, s, tmQ, tmK, tmV, a);
 }
 
 cudaError_t attn_read_and_clear_status(int* out) {

@@ -99,12 +99,12 @@ cudaError_t launch_rmsnorm(const void* X, const void* g, void* Xn, int M, int K,
 cudaError_t read_and_clear_status(int* out);
 
 // ------------------------------------------------ QK-normalised attention (attention.cu)
-constexpr int kAttD = 128;    // head dimension
-constexpr int kAttBM = 128;   // query rows per CTA
+constexpr int kAttBM = 128;   // query rows per tile
 constexpr int kAttBN = 128;   // keys per tile
 
 struct AttnLaunch {
     int S;            // sequence length (queries and keys)
+    int D;            // head dimension, 64 or 128
     int Hq, group;    // query heads; query heads per key/value head
     int n_qb;         // blocks of 256 query rows per sequence, ceil(S / 256)
     int n_hb;         // Hq * B
@@ -114,7 +114,7 @@ struct AttnLaunch {
     float eps;
     float qscale;     // scale * log2(e), applied with each query row's 1/RMS to its scores
     int wait_limit_us;
-    void* O;          // output [B, S, Hq, 128], row stride ldo elements
+    void* O;          // output [B, S, Hq, D], row stride ldo elements
     long long ldo;
     int test_skip_loads;   // test hook: the producer leaves out its first K/V stage
 };
@@ -127,7 +127,7 @@ cudaError_t launch_rmsnorm_heads(const void* X, int64_t ldx, const void* g, cons
 // in boxes of [128 rows][64] (V: [64][64]).
 cudaError_t launch_qknorm_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                     const CUtensorMap& tmV, const AttnLaunch& a, cudaStream_t s);
-size_t attn_smem_bytes();
+size_t attn_smem_bytes(int D);
 // The attention translation unit's own status word (as read_and_clear_status).
 cudaError_t attn_read_and_clear_status(int* out);
 

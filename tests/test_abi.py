@@ -135,7 +135,7 @@ def test_attention_validation(lib):
             a[names.index(k)] = v
         return f(*a, None)
 
-    assert call(D=64) == 1                 # head dimension other than 128
+    assert call(D=96) == 1                 # head dimension other than 64 or 128
     assert call(Hq=12) == 1                # Hq not a multiple of Hkv
     assert call(ldq=4000) == 1             # row stride narrower than the heads
     assert call(ldo=4100) == 2             # row stride not a multiple of 8
@@ -209,5 +209,5 @@ def test_attention_abi_rejects_grouping_and_head_dim(lib):
     # (Q, ldq, K, ldk, V, ldv, gq, gk, O, ldo, B, S, Hq, Hkv, D, eps, scale, causal)
     assert f(A16, 768, A16 + 512, 768, A16 + 768, 768, B16, B16 + 256, C16, 512,
              1, 16, 5, 2, 128, 1e-6, 0.0, 1, None) == 1               # 5 query heads over 2
-    assert f(A16, 384, A16 + 256, 384, A16 + 320, 384, B16, B16 + 256, C16, 256,
-             1, 16, 4, 1, 64, 1e-6, 0.0, 1, None) == 1                # D = 64 is not built
+    assert f(A16, 480, A16 + 320, 480, A16 + 400, 480, B16, B16 + 256, C16, 320,
+             1, 16, 4, 1, 80, 1e-6, 0.0, 1, None) == 1                # D = 80 is not built

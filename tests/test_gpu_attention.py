@@ -123,6 +123,21 @@ def test_qknorm_attention(rmm, B, S, Hq, Hkv, causal):
     assert_attention_close(O, Q, K, V, gq, gk, 1e-6, causal, f"attention {B}x{S} {Hq}/{Hkv}")
 
 
+ATTN_D64 = [
+    # (B, S, Hq, Hkv, causal), head dimension 64
+    (1, 256, 4, 2, True),
+    (2, 300, 4, 1, True),      # ragged, two sequences, 4:1 grouping
+    (1, 200, 2, 2, False),     # full attention, ragged last key tile
+    (1, 1100, 2, 1, True),     # nine key tiles
+]
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,causal", ATTN_D64)
+def test_qknorm_attention_head_dim_64(rmm, B, S, Hq, Hkv, causal):
+    O, Q, K, V, gq, gk = run(rmm, B, S, Hq, Hkv, causal, seed=B * 977 + S + Hq, D=64)
+    assert_attention_close(O, Q, K, V, gq, gk, 1e-6, causal, f"D=64 attention {B}x{S} {Hq}/{Hkv}")
+
+
 def test_first_causal_row_is_first_value(rmm):
     # one visible key: softmax weight exactly 1, O = bf16(V[0]) exactly
     O, Q, K, V, gq, gk = run(rmm, 1, 64, 4, 2, True, seed=9)
