@@ -159,6 +159,10 @@ ATTENTION_WORKLOADS = {
     "prefill_attention_1x4096_h32_kv8_d128_causal": AttentionWorkload(
         "prefill_attention_1x4096_h32_kv8_d128_causal", B=1, S=4096, Hq=32, Hkv=8, D=128,
         eps=1e-6, causal=True, seed=5),
+    # the same sequence and heads with head dimension 64
+    "prefill_attention_1x4096_h32_kv8_d64_causal": AttentionWorkload(
+        "prefill_attention_1x4096_h32_kv8_d64_causal", B=1, S=4096, Hq=32, Hkv=8, D=64,
+        eps=1e-6, causal=True, seed=6),
 }
 
 
