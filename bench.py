@@ -733,8 +733,6 @@ def main():
         "clocks": clocks,
         "device_status": main_res["status"],
     }
-    if shapes:
-        out["shapes"] = shapes
     if rank == 0 and not args.no_cpu_baseline:
         secs, nbytes, sample, threads, _, _ = cpu_oracle_run(w, args.cpu_budget)
         out["cpu_baseline"] = {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s",
@@ -742,6 +740,12 @@ def main():
                                "secs_per_call": round(secs, 4)}
         if args.shapes == "all":
             out["cpu_oracle_table"] = cpu_oracle_table()
+    if shapes:
+        out["shapes"] = shapes
+        # compact copies of every line, last on the line (a reader that keeps
+        # only its tail still sees each workload's result)
+        out["other_lines"] = [compact(e) for e in shapes if e["workload"] not in inputs.WORKLOADS]
+        out["per_config"] = [compact(e) for e in shapes if e["workload"] in inputs.WORKLOADS]
     if rank == 0:
         print(json.dumps(out), flush=True)
     sync.close()
@@ -778,6 +782,17 @@ def kernel_name(rmm, w):
     return "rows_kernel<fused>"
 
 
+def compact(e):
+    """A short form of one shape entry: time, rates, fraction of its roofline
+    (of the measured burst peak) and, where timed, the unfused kernels' time."""
+    c = {"w": e["workload"].replace(" (", "(")[:48], "us": round(e["us_per_call"], 2), "tf": round(e["tflops"], 1),
+         "gbs": round(e["hbm_gbs"]), "frac": round(e["roofline_frac"], 3), "of": e["bound"]}
+    for k in ("unfused_pair_us", "unfused_us", "torch_rms_norm_sdpa_us"):
+        if k in e:
+            c["unf_us"] = round(e[k], 1)
+    return c
+
+
 def gated_bytes(w):
     """X + W + Y bytes of the gated form (Y has N/2 columns)."""
     return 2 * (w.M * w.K + w.K * w.N + w.M * (w.N // 2))
@@ -786,8 +801,8 @@ def gated_bytes(w):
 def shape_entry(w, t, r, peaks, k, gated=False, lora_r=0):
     nbytes = gated_bytes(w) if gated else w.bytes_xwy
     flops = w.flops
-    if lora_r:   # + A, B, and T written and read back; + (X*g) @ A and T @ B
-        nbytes += 2 * (w.K * lora_r + lora_r * w.N + 2 * w.M * lora_r)
+    if lora_r:   # + A and B; + (X*g) @ A and T @ B (the intermediate T is not algorithmic)
+        nbytes += 2 * (w.K * lora_r + lora_r * w.N)
         flops += 2 * w.M * lora_r * (w.K + w.N)
     tflops = flops / t / 1e12
     gbs = nbytes / t / 1e9

@@ -74,9 +74,10 @@ typedef enum {
  * tiles leave a last wave of CTAs at most half full, those last tiles are cut
  * along K, one piece per CTA, and the pieces are combined, in a fixed order,
  * through a library-owned fp32 workspace per (device, stream); the pieces of
- * a tile wait for one another, so every CTA of the launch must be able to be
- * resident at once (one per SM, which the grid size guarantees on a device
- * not shared with other work).  With rmm_force_path(2) the operand-swapped
+ * a tile wait for one another, so such a launch is cooperative: all its CTAs
+ * (at most one per SM) are resident at once, or the launch fails with
+ * RMM_ERR_LAUNCH (for example on a device partition with fewer SMs than the
+ * device reports).  With rmm_force_path(2) the operand-swapped
  * small-M kernel runs instead; its K split may use the same workspace.  The
  * workspace is allocated on first use of a shape that needs it (make that
  * first call outside any CUDA-graph capture).
@@ -130,12 +131,15 @@ int rmsnorm_matmul_ex(const void* X, const void* g, const void* W, void* Y,
  *   Y [M,N] = RMSNorm(X; g, eps) @ (W + A @ B),  A [K,R], B [R,N] bf16,
  *   1 <= R <= 64, R a multiple of 8; the other rules are those of
  *   rmsnorm_matmul().
- * Two launches of the row-tile kernels: T = bf16((X*g) @ A) [M,R] into a
- * library-owned buffer per (device, stream) (allocated on first use; make that
- * first call outside any CUDA-graph capture), then the main contraction with
- * one more 64-deep stage per tile whose operands are T and B, so that
- * Y = r * ((X*g) @ W + T @ B) with one division by the row RMS.  Returns an
- * rmm_status.
+ * Two launches of the row-tile kernels.  The first computes T = (X*g) @ A
+ * (fp32 accumulation, no division by the RMS) and stores it as a pair of bf16
+ * matrices, T_hi = bf16(T) and T_lo = bf16(T - T_hi), [M, 2 x 64] in a
+ * library-owned buffer per (device, stream) (allocated on first use; make
+ * that first call outside any CUDA-graph capture).  The second is the main
+ * contraction with two more 64-deep stages per tile, T_hi @ B and T_lo @ B,
+ * so that Y = r * ((X*g) @ W + T @ B) with one division by the row RMS and T
+ * carried to about 2^-16 relative (no rounding beyond that of the plain
+ * form's operands).  Returns an rmm_status.
  */
 int rmsnorm_matmul_lora(const void* X, const void* g, const void* W, const void* A,
                         const void* B, void* Y, int64_t M, int64_t K, int64_t N, int64_t R,
@@ -201,27 +205,35 @@ const char* rmm_status_string(int code);
 /*
  * rmsnorm_matmul_noalloc -- the same computation, arguments and results as
  * rmsnorm_matmul(), for callers that cannot let a library allocate device
- * memory: code being captured into a CUDA graph (where cudaMalloc is
- * refused), runtimes and plugin hosts that own all device memory and forbid
- * allocation inside their enqueue call, and processes with a fixed memory
- * budget.  It calls no cudaMalloc, cudaFree or allocating library routine.
- * The paper has no counterpart to this entry point.
+ * memory during a call: inference runtimes and plugin hosts that own all
+ * device memory through their own pool and forbid allocation inside their
+ * enqueue step, processes that fix their device-memory budget at start-up,
+ * and latency-critical paths where cudaMalloc (which may synchronise the
+ * device) is not acceptable.  It calls no cudaMalloc, cudaFree or allocating
+ * library routine.  The paper has no counterpart to this entry point.
  *
- * Scratch: where the small-M path splits K, its fp32 partial sums live in one
- * fixed 16 MiB device array inside this library (a file-scope __device__
- * array), held on every device where the library's device code is loaded
- * until the process exits.  Limit: splits x M x N x 4 bytes must fit in
- * 15 MiB (for example M = 64, N = 28672 with two K splits uses 14 MiB);
- * larger problems return RMM_ERR_SCRATCH_LIMIT.  The default row-tile path
- * and unsplit small-M launches use no scratch; the small-M path's K split
- * (rmm_force_path(2)) is the variant that uses the array.
+ * It runs the same kernels with the same launch plan as rmsnorm_matmul()
+ * (results agree bit for bit), but the K-split partial sums that
+ * rmsnorm_matmul() keeps in a workspace allocated on first use -- the tail
+ * pieces of the prefill kernel, and the global split of the small-M path under
+ * rmm_force_path(2) -- live in one fixed 20 MiB device array inside this
+ * library (a file-scope __device__ array), held on every device where the
+ * library's device code is loaded until the process exits.  Limit: the plan's
+ * partials (fp32 sums plus row sums of squares) must fit in 20 MiB - 64 KiB
+ * and its arrival counters in 64 KiB; the tail pieces of any shape fit on a
+ * device of up to 152 SMs (at most one 128 x 256 fp32 piece per SM), and a
+ * plan that needs more returns RMM_ERR_SCRATCH_LIMIT before any launch.
+ * Plans without a K split through memory (decode shapes, which split K inside
+ * a cluster) use no scratch.
  *
  * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  Every call shares the one array, which keeps the previous call's
- * contents; each call clears its arrival counters on `stream` before its
- * kernel.  Calls whose kernels overlap on the GPU (for example on two streams
- * at once) race on the array: order them on one stream or with events.
+ * device, with that device current) and keeps it for the life of the process;
+ * make that first call before any stream capture, and do not reset the device
+ * while the library is in use.  Every call shares the one array, which keeps
+ * the previous call's contents; each call that uses it clears its arrival
+ * counters on `stream` before its kernel.  Calls whose kernels overlap on the
+ * GPU (for example on two streams at once) race on the array: order them on
+ * one stream or with events.
  */
 int rmsnorm_matmul_noalloc(const void* X, const void* g, const void* W, void* Y,
                            int64_t M, int64_t K, int64_t N, float eps, cudaStream_t stream);
@@ -234,6 +246,10 @@ int rmsnorm_matmul_noalloc(const void* X, const void* g, const void* W, void* Y,
  * Fills info[0..7] with: path (1 row-tile, 2 small-M),
  * K splits, 1 if the splits reduce through a cluster's shared memory, grid
  * size, pipeline stages, padded rows MP, column tiles, k-blocks per split.
+ * For the fused kernel over several row tiles, the K splits and k-blocks per
+ * split are those of its tail tiles (1 split: every tile whole), and splits
+ * without a cluster mean partial sums in the workspace.  The plan described is
+ * rmsnorm_matmul()'s, which rmsnorm_matmul_noalloc() runs too.
  * Queries device attributes; launches nothing.
  */
 int rmm_describe_plan(int64_t M, int64_t K, int64_t N, int fused, int* info);

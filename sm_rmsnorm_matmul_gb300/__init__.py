@@ -282,13 +282,14 @@ def qknorm_attention(Q, K, V, gq, gk, eps: float = 1e-6, scale: float | None = N
 
 def rmsnorm_matmul_noalloc(X, g, W, eps: float = 1e-6, out=None, stream=None):
     """rmsnorm_matmul() for callers that cannot let the library allocate device
-    memory (graph capture, runtimes that own all device memory, fixed budgets).
+    memory during a call (runtimes that own all device memory, fixed budgets,
+    latency-critical paths).
 
-    The library allocates nothing: split-K partial sums use a fixed 16 MiB
-    array inside the library.  `out` must be given, since allocating it here
-    would defeat the purpose.  Calls that overlap on the GPU share that array
-    and race; problems needing more than 15 MiB of partials raise
-    RmmError(RMM_ERR_SCRATCH_LIMIT).
+    The library allocates nothing: it runs rmsnorm_matmul()'s plan with the
+    K-split partial sums in a fixed 20 MiB array inside the library.  `out`
+    must be given, since allocating it here would defeat the purpose.  Calls
+    that overlap on the GPU share that array and race; a plan whose partials do
+    not fit raises RmmError(RMM_ERR_SCRATCH_LIMIT).
     """
     _check_bf16("X", X, 2)
     _check_bf16("g", g, 1)

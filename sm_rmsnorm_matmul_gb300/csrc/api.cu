@@ -180,7 +180,7 @@ struct Workspace {
     size_t ss_bytes = 0;
     int* counters = nullptr;
     size_t n_counters = 0;
-    void* lora_t = nullptr;   // the low-rank adapter's T = bf16((X*g) @ A), [M, R]
+    void* lora_t = nullptr;   // the low-rank adapter's T = (X*g) @ A as bf16 hi | lo, [M, 128]
     size_t lora_t_bytes = 0;
     void* khat = nullptr;     // normalised keys of qknorm_attention, [B, S, Hkv, D]
     size_t khat_bytes = 0;
@@ -484,6 +484,38 @@ RowsPlan plan_rows(int dev, bool fused, int64_t M, int64_t K, int64_t N, const D
     return p;
 }
 
+// K split of the last tiles of the fused kernel for several row tiles.  When
+// the tiles leave a last wave at most half full, those tiles are cut along K
+// so that every CTA has a share of them.  When all the tiles fill at most half
+// the SMs (one partial wave, e.g. a contraction with a narrow N such as the
+// adapter's T), every tile is cut, one piece per CTA, up to one CTA per SM.
+// The pieces of a tile wait for one another, so the launch is cooperative.
+struct TailPlan {
+    int tiles = 0;    // tail tiles (0: every tile whole)
+    int pieces = 1;   // K pieces per tail tile
+    int kbp = 0;      // k-blocks per piece
+    int grid = 0;     // CTAs of the launch
+};
+TailPlan plan_tail(const RowsPlan& p, const DeviceInfo& d) {
+    TailPlan t;
+    t.grid = p.grid;
+    const int tiles = p.m_tiles * p.n_tiles;
+    const int sms = d.sm_count > 0 ? d.sm_count : 1;
+    const bool few = tiles <= p.grid && 2 * tiles <= sms;
+    const int grid = few ? sms : p.grid;
+    const int rem = tiles % grid;
+    if (!((tiles > grid || few) && rem > 0 && 2 * rem <= grid && p.k_blocks >= 2)) return t;
+    const int pmax = grid / rem;
+    const int kbp = (p.k_blocks + pmax - 1) / pmax;
+    const int pieces = (p.k_blocks + kbp - 1) / kbp;
+    if (pieces < 2) return t;
+    t.tiles = rem;
+    t.pieces = pieces;
+    t.kbp = kbp;
+    if (few) t.grid = tiles * pieces;   // every tile cut: one CTA per piece
+    return t;
+}
+
 // The row-tile path serves every shape by default: for M <= 128 it streams W
 // with wide tiles and a cluster K split, which measured faster on GB300 than
 // the operand-swapped small-M path.  The small-M path stays available through
@@ -495,17 +527,43 @@ int choose_path(int64_t M) {
     return kPathRows;
 }
 
+// Device memory for K-split partials that the caller provides instead of the
+// per-(device, stream) workspace: a fixed area with its capacities.  The plan
+// is the one the workspace would get; a plan whose partials do not fit is
+// refused with RMM_ERR_SCRATCH_LIMIT.  The arrival counters are cleared on the
+// stream before each launch that uses them (the area keeps the previous
+// call's contents).
+struct FixedScratch {
+    unsigned char* area;   // fp32 partial sums, then the partial row sums of squares
+    size_t area_bytes;
+    int* counters;
+    size_t counter_bytes;
+    // The partials of a plan (acc_bytes of sums, then ss_bytes) placed in
+    // `area`; false if they do not fit.
+    bool place(size_t acc_bytes, size_t ss_bytes, float** acc, float** ss) const {
+        const size_t ss_off = (acc_bytes + 255) / 256 * 256;
+        if (ss_off + ss_bytes > area_bytes) return false;
+        *acc = reinterpret_cast<float*>(area);
+        *ss = reinterpret_cast<float*>(area + ss_off);
+        return true;
+    }
+};
+
 // One launch of the tensor-core contraction, fused (RMSNorm folded in) or not.
-// Without may_allocate, plans that need the per-stream workspace are avoided.
+// fixed: never allocate; K-split partials go to that area (RMM_ERR_SCRATCH_LIMIT
+// if the plan's partials do not fit).
 // glu: the gated form (fused only; always the row-tile path), Y [M, N / 2].
 // wnk: W stored [N, K] (fused only; always the row-tile path).
-// unscaled: no division by the row RMS.  lora_t, lora_b: the low-rank
-// adapter's T [M, R] and B [R, N], added as one more stage per tile (row-tile
+// unscaled: no division by the row RMS; hilo (with unscaled, N <= 64): Y is
+// [M, 128], each output written as the bf16 pair hi (columns [0, 64)) and lo
+// (columns [64, 128)).  lora_t, lora_b: the low-rank adapter's T [M, 128] (a
+// hilo output) and B [R, N], added as two more stages per tile (row-tile
 // path).
 int run_contraction(bool fused, const void* X, const void* g, const void* W, void* Y, int64_t M,
-                    int64_t K, int64_t N, float eps, cudaStream_t stream, bool may_allocate = true,
+                    int64_t K, int64_t N, float eps, cudaStream_t stream, const FixedScratch* fixed = nullptr,
                     bool glu = false, bool wnk = false, bool unscaled = false,
-                    const void* lora_t = nullptr, const void* lora_b = nullptr, int64_t R = 0) {
+                    const void* lora_t = nullptr, const void* lora_b = nullptr, int64_t R = 0,
+                    bool hilo = false) {
     const bool lora = lora_t != nullptr;
     int dev = 0;
     DeviceInfo d;
@@ -541,14 +599,24 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
         a.cluster = p.cluster;
         a.tmem_cols = p.tmem_cols;
         if (p.splits > 1 && !p.cluster) {
-            Workspace w;
-            rc = get_workspace(dev, stream, static_cast<size_t>(p.splits) * M * N * sizeof(float),
-                               static_cast<size_t>(p.n_tiles) * p.splits * rmm::kColsMaxMP * sizeof(float),
-                               static_cast<size_t>(p.n_tiles) * 4, &w);
-            if (rc != RMM_OK) return rc;
-            a.ws_acc = w.acc;
-            a.ws_ss = w.ss;
-            a.counters = w.counters;
+            const size_t acc_bytes = static_cast<size_t>(p.splits) * M * N * sizeof(float);
+            const size_t ss_bytes = static_cast<size_t>(p.n_tiles) * p.splits * rmm::kColsMaxMP * sizeof(float);
+            const size_t ncount = static_cast<size_t>(p.n_tiles) * 4;
+            if (fixed) {
+                if (!fixed->place(acc_bytes, ss_bytes, &a.ws_acc, &a.ws_ss) ||
+                    ncount * sizeof(int) > fixed->counter_bytes)
+                    return RMM_ERR_SCRATCH_LIMIT;
+                if (cudaMemsetAsync(fixed->counters, 0, ncount * sizeof(int), stream) != cudaSuccess)
+                    return RMM_ERR_LAUNCH;
+                a.counters = fixed->counters;
+            } else {
+                Workspace w;
+                rc = get_workspace(dev, stream, acc_bytes, ss_bytes, ncount, &w);
+                if (rc != RMM_OK) return rc;
+                a.ws_acc = w.acc;
+                a.ws_ss = w.ss;
+                a.counters = w.counters;
+            }
         }
         return rmm::launch_cols(fused, tmX, tmW, tmG, Y, a, stream) == cudaSuccess ? RMM_OK
                                                                                   : RMM_ERR_LAUNCH;
@@ -575,49 +643,50 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
     a.glu = glu ? 1 : 0;
     a.w_nk = wnk ? 1 : 0;
     a.unscaled = unscaled ? 1 : 0;
+    a.hilo = hilo ? 1 : 0;
     a.lora = lora ? 1 : 0;
     a.wait_limit_us = g_wait_limit_us.load();
     a.test_skip_sends = g_skip_sends.load();
     CUtensorMap tmT = tmX, tmB = tmW;   // unused without the adapter
     if (lora) {
-        if (!map_2d(&tmT, lora_t, M, R, p.xrows) || !map_2d(&tmB, lora_b, R, N, kBK)) return RMM_ERR_INTERNAL;
+        if (!map_2d(&tmT, lora_t, M, 2 * kBK, p.xrows) || !map_2d(&tmB, lora_b, R, N, kBK))
+            return RMM_ERR_INTERNAL;
     }
     CUtensorMap tmY;
     a.tail_tiles = 0;
     a.tail_pieces = 1;
     a.tail_kbp = p.k_blocks;
     if (fused && !p.cluster && p.xrows == rmm::kRowsBM) {
-        if (!map_2d_store(&tmY, Y, M, glu ? N / 2 : N)) return RMM_ERR_INTERNAL;
+        if (!map_2d_store(&tmY, Y, M, hilo ? 2 * kBK : glu ? N / 2 : N)) return RMM_ERR_INTERNAL;
         a.tmY = &tmY;
-        // When the tiles leave a last wave at most half full, cut those tiles
-        // along K so that every CTA has a share of them.  When all the tiles
-        // fill at most half the SMs (one partial wave, e.g. a contraction with
-        // a narrow N such as the adapter's T), cut every tile, one piece per
-        // CTA, up to one CTA per SM (all resident at once, as the pieces'
-        // reduction needs).
-        const int tiles = p.m_tiles * p.n_tiles;
-        const int sms = d.sm_count > 0 ? d.sm_count : 1;
-        const bool few = tiles <= p.grid && 2 * tiles <= sms;
-        const int grid = few ? sms : p.grid;
-        const int rem = tiles % grid;
-        if (may_allocate && (tiles > grid || few) && rem > 0 && 2 * rem <= grid && p.k_blocks >= 2) {
-            const int pmax = grid / rem;
-            const int kbp = (p.k_blocks + pmax - 1) / pmax;
-            const int pieces = (p.k_blocks + kbp - 1) / kbp;
-            if (pieces >= 2) {
-                Workspace w;
+        const TailPlan t = plan_tail(p, d);
+        if (t.tiles > 0) {
+            const int rem = t.tiles, pieces = t.pieces;
+            {
+                constexpr size_t kPieceBytes = static_cast<size_t>(rmm::kRowsBM) * rmm::kRowsBN * sizeof(float);
                 const size_t units = static_cast<size_t>(rem) * pieces;
-                rc = get_workspace(dev, stream, units * rmm::kRowsBM * rmm::kRowsBN * sizeof(float),
-                                   units * rmm::kRowsBM * sizeof(float), static_cast<size_t>(rem) * 2, &w);
-                if (rc != RMM_OK) return rc;
+                if (fixed) {
+                    if (!fixed->place(units * kPieceBytes, units * rmm::kRowsBM * sizeof(float), &a.ws_acc,
+                                      &a.ws_ss) ||
+                        static_cast<size_t>(rem) * 2 * sizeof(int) > fixed->counter_bytes)
+                        return RMM_ERR_SCRATCH_LIMIT;
+                    if (cudaMemsetAsync(fixed->counters, 0, static_cast<size_t>(rem) * 2 * sizeof(int), stream) !=
+                        cudaSuccess)
+                        return RMM_ERR_LAUNCH;
+                    a.ws_count = fixed->counters;
+                } else {
+                    Workspace w;
+                    rc = get_workspace(dev, stream, units * kPieceBytes, units * rmm::kRowsBM * sizeof(float),
+                                       static_cast<size_t>(rem) * 2, &w);
+                    if (rc != RMM_OK) return rc;
+                    a.ws_acc = w.acc;
+                    a.ws_ss = w.ss;
+                    a.ws_count = w.counters;
+                }
                 a.tail_tiles = rem;
                 a.tail_pieces = pieces;
-                a.tail_kbp = kbp;
-                a.ws_acc = w.acc;
-                a.ws_ss = w.ss;
-                a.ws_count = w.counters;
-                // every tile cut: one CTA per piece
-                if (few) a.grid = tiles * pieces;
+                a.tail_kbp = t.kbp;
+                a.grid = t.grid;
             }
         }
     }
@@ -654,7 +723,7 @@ int rmsnorm_matmul_ex(const void* X, const void* g, const void* W, void* Y, int6
                     {{X, static_cast<size_t>(M) * K * 2}, {g, static_cast<size_t>(K) * 2},
                      {W, static_cast<size_t>(K) * N * 2}});
     if (rc != RMM_OK) return rc;
-    return run_contraction(true, X, g, W, Y, M, K, N, eps, stream, true, glu, wnk);
+    return run_contraction(true, X, g, W, Y, M, K, N, eps, stream, nullptr, glu, wnk);
 }
 
 int rmsnorm_matmul_lora(const void* X, const void* g, const void* W, const void* A, const void* B,
@@ -675,13 +744,15 @@ int rmsnorm_matmul_lora(const void* X, const void* g, const void* W, const void*
     rc = current_device(&dev, &d);
     if (rc != RMM_OK) return rc;
     void* T = nullptr;
-    rc = get_lora_buffer(dev, stream, static_cast<size_t>(M) * R * 2, &T);
+    rc = get_lora_buffer(dev, stream, static_cast<size_t>(M) * 2 * kBK * 2, &T);
     if (rc != RMM_OK) return rc;
-    // T = bf16((X*g) @ A): the same gained, bf16-rounded rows the MMA sees,
-    // without the division by the RMS (applied once, to the sum, below)
-    rc = run_contraction(true, X, g, A, T, M, K, R, eps, stream, true, false, false, true);
+    // T = (X*g) @ A over the same gained, bf16-rounded rows the MMA sees,
+    // without the division by the RMS (applied once, to the sum, below),
+    // kept as the bf16 pair hi = bf16(T), lo = bf16(T - hi): [M, 128]
+    rc = run_contraction(true, X, g, A, T, M, K, R, eps, stream, nullptr, false, false, true, nullptr, nullptr, 0,
+                         true);
     if (rc != RMM_OK) return rc;
-    return run_contraction(true, X, g, W, Y, M, K, N, eps, stream, true, false, false, false, T, B, R);
+    return run_contraction(true, X, g, W, Y, M, K, N, eps, stream, nullptr, false, false, false, T, B, R);
 }
 
 int rmsnorm_matmul_swiglu(const void* X, const void* g, const void* W, void* Y, int64_t M,
@@ -752,6 +823,15 @@ int rmm_describe_plan(int64_t M, int64_t K, int64_t N, int fused, int* info) {
         info[5] = p.xrows;
         info[6] = p.m_tiles * p.n_tiles;
         info[7] = p.kb_per_split;
+        if (fused != 0 && !p.cluster && p.xrows == rmm::kRowsBM) {
+            // the fused kernel for several row tiles: its tail tiles' K pieces
+            const TailPlan t = plan_tail(p, d);
+            if (t.tiles > 0) {
+                info[1] = t.pieces;
+                info[3] = t.grid;
+                info[7] = t.kbp;
+            }
+        }
     }
     return RMM_OK;
 }
@@ -882,22 +962,23 @@ const char* rmm_status_string(int code) {
 // ============================================================================
 // Allocation-free variant of rmsnorm_matmul().
 //
-// Some callers cannot let a library allocate device memory: code that is being
-// captured into a CUDA graph (cudaMalloc is not a stream operation and is
-// refused there), inference runtimes and plugin hosts that own every byte of
-// device memory and forbid allocation inside their enqueue call, and
-// processes with a fixed memory budget set at start-up.  For them,
-// rmsnorm_matmul_noalloc() runs the same kernels; where the small-M path
-// splits K, its fp32 partial sums, partial row sums of squares and arrival
-// counters live in the fixed array below instead of a workspace allocated on
-// first use.
+// Some callers cannot let a library allocate device memory during a call:
+// inference runtimes and plugin hosts that own every byte of device memory
+// through their own pool and forbid allocation inside their enqueue step;
+// processes that fix their device-memory budget at start-up; and
+// latency-critical paths where cudaMalloc, which may synchronise the device,
+// is not acceptable.  rmsnorm_matmul_noalloc() runs the same kernels with the
+// same plans, but the K-split partial sums that rmsnorm_matmul() keeps in a
+// workspace allocated on first use (the prefill kernel's tail pieces, the
+// small-M path's global split) live in the fixed array below.  20 MiB holds
+// the tail pieces of any shape on a 152-SM device (at most one 128 x 256
+// fp32 piece per SM: 19.1 MiB); a plan that needs more is refused.
 // ============================================================================
 namespace {
 
-constexpr size_t kScratchBytes = size_t(16) << 20;           // 16 MiB in total
-constexpr size_t kScratchCounterBytes = size_t(64) << 10;    // 4 counters per column tile
-constexpr size_t kScratchSsBytes = size_t(960) << 10;        // partial sums of squares
-constexpr size_t kScratchAccBytes = kScratchBytes - kScratchCounterBytes - kScratchSsBytes;
+constexpr size_t kScratchBytes = size_t(20) << 20;          // 20 MiB in total
+constexpr size_t kScratchCounterBytes = size_t(64) << 10;   // arrival counters first
+constexpr size_t kScratchAreaBytes = kScratchBytes - kScratchCounterBytes;
 
 // Held on every device where this module is loaded, until the process exits.
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
@@ -907,7 +988,8 @@ std::map<int, unsigned char*> g_scratch_addr;
 
 // Device address of g_scratch on `dev`, which must be the current device.
 // Looked up once per device (the first call may load this library's device
-// code on that device).
+// code on that device) and kept for the life of the process: a device reset
+// while the library is in use leaves it (like the workspaces) dangling.
 int scratch_address(int dev, unsigned char** out) {
     std::lock_guard<std::mutex> lk(g_scratch_mu);
     auto it = g_scratch_addr.find(dev);
@@ -938,46 +1020,10 @@ extern "C" int rmsnorm_matmul_noalloc(const void* X, const void* g, const void* 
     DeviceInfo d;
     rc = current_device(&dev, &d);
     if (rc != RMM_OK) return rc;
-    // The row-tile path and an unsplit small-M launch use no scratch at all.
-    if (choose_path(M) == kPathRows) return run_contraction(true, X, g, W, Y, M, K, N, eps, stream, false);
-    if (M > rmm::kColsMaxMP) return RMM_ERR_INVALID_ARG;
-    const ColsPlan p = plan_cols(dev, true, M, K, N, d, false);
-    if (p.splits == 1) return run_contraction(true, X, g, W, Y, M, K, N, eps, stream, false);
-
-    const size_t acc_bytes = static_cast<size_t>(p.splits) * M * N * sizeof(float);
-    const size_t ss_bytes = static_cast<size_t>(p.n_tiles) * p.splits * rmm::kColsMaxMP * sizeof(float);
-    const size_t cnt_bytes = static_cast<size_t>(p.n_tiles) * 4 * sizeof(int);
-    if (acc_bytes > kScratchAccBytes || ss_bytes > kScratchSsBytes || cnt_bytes > kScratchCounterBytes)
-        return RMM_ERR_SCRATCH_LIMIT;
     unsigned char* base = nullptr;
     rc = scratch_address(dev, &base);
     if (rc != RMM_OK) return rc;
-    int* counters = reinterpret_cast<int*>(base);
-    float* ss = reinterpret_cast<float*>(base + kScratchCounterBytes);
-    float* acc = reinterpret_cast<float*>(base + kScratchCounterBytes + kScratchSsBytes);
-    // The array keeps the previous call's contents; the counters must start at 0.
-    if (cudaMemsetAsync(counters, 0, cnt_bytes, stream) != cudaSuccess) return RMM_ERR_LAUNCH;
-
-    CUtensorMap tmX, tmW, tmG;
-    if (!map_2d(&tmW, W, K, N, kBK) || !map_1d(&tmG, g, K) || !map_2d(&tmX, X, M, K, p.MP))
-        return RMM_ERR_INTERNAL;
-    rmm::ColsLaunch a{};
-    a.M = static_cast<int>(M);
-    a.N = static_cast<int>(N);
-    a.K = static_cast<int>(K);
-    a.eps = eps;
-    a.MP = p.MP;
-    a.n_tiles = p.n_tiles;
-    a.k_blocks = p.k_blocks;
-    a.splits = p.splits;
-    a.kb_per_split = p.kb_per_split;
-    a.stages = p.stages;
-    a.grid = p.grid;
-    a.tmem_cols = p.tmem_cols;
-    a.wait_limit_us = g_wait_limit_us.load();
-    a.ws_acc = acc;
-    a.ws_ss = ss;
-    a.counters = counters;
-    return rmm::launch_cols(true, tmX, tmW, tmG, Y, a, stream) == cudaSuccess ? RMM_OK
-                                                                            : RMM_ERR_LAUNCH;
+    const FixedScratch f{base + kScratchCounterBytes, kScratchAreaBytes, reinterpret_cast<int*>(base),
+                         kScratchCounterBytes};
+    return run_contraction(true, X, g, W, Y, M, K, N, eps, stream, &f);
 }

@@ -88,6 +88,27 @@ __device__ __forceinline__ uint4 gain8(uint4 xv, uint4 gv, float& ss) {
     return o;
 }
 
+// The low-rank adapter's T enters the contraction as two bf16 stages, its hi
+// and lo halves.
+constexpr int kLoraStages = 2;
+
+// Two outputs a, b as bf16 pairs: hi = bf16(v) and lo = bf16(v - hi) (v - hi
+// is exact in fp32), so that hi + lo carries v to about 2^-16 relative.
+__device__ __forceinline__ void hilo_pack(float a, float b, uint32_t& hi, uint32_t& lo) {
+    hi = pack_bf16x2(a, b);
+    lo = pack_bf16x2(a - bf16lo(hi), b - bf16hi(hi));
+}
+// Four consecutive outputs of a row at column col (< 64) of a hilo output
+// [rows][128]: hi at col, lo at 64 + col.
+__device__ __forceinline__ void store_hilo4(__nv_bfloat16* yrow, int col, float v0, float v1, float v2,
+                                            float v3) {
+    uint2 h, l;
+    hilo_pack(v0, v1, h.x, l.x);
+    hilo_pack(v2, v3, h.y, l.y);
+    *reinterpret_cast<uint2*>(yrow + col) = h;
+    *reinterpret_cast<uint2*>(yrow + kBK + col) = l;
+}
+
 struct RowsLayout {
     uint32_t xbytes, off_x, off_w, off_g, off_red, red_block, off_bar, off_sr, off_misc, total;
 };
@@ -235,22 +256,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     // boxes of gate columns n0.. and two of up columns Nout + n0.. (always
     // four: a box past the gate half reads up columns, one past N reads
     // zeros, and neither reaches an output column).
-    // Low-rank adapter: the unit holding split 0 of a tile runs one more
-    // stage after its k-blocks, at k-block index k_blocks, whose A tile is
-    // T = bf16((X*g) @ A) (rows of tmT, R <= 64 columns, zeros past R) and
-    // whose B tile is the adapter's B (rows of tmB, zeros past R); it gets
-    // no gain and adds nothing to the row statistic.
+    // Low-rank adapter: the unit holding split 0 of a tile runs two more
+    // stages after its k-blocks, at k-block indices k_blocks + e, e = 0, 1,
+    // whose A tiles are the hi (e = 0) and lo (e = 1) halves of T = (X*g) @ A
+    // (columns [64e, 64e + 64) of tmT, zeros past R in each half) and whose B
+    // tile is the adapter's B both times (rows of tmB, zeros past R); they get
+    // no gain and add nothing to the row statistic.  T_hi @ B + T_lo @ B
+    // carries T to about 2^-16 relative, far below the output's rounding.
     // (its own instantiations: kLora, fused [K, N] form only; the others
     // carry none of it)
     static_assert(!kLora || (kFused && !kGlu && !kWnk), "the adapter stage is for the plain fused form");
-    auto lora_extra = [&](int sp) { return kLora && sp == 0 ? 1 : 0; };
+    auto lora_extra = [&](int sp) { return kLora && sp == 0 ? kLoraStages : 0; };
     // Loads of stage s = k-block kb of the unit whose tile starts at row block
-    // mb and output column n0 (kb == k_blocks: the adapter stage).
+    // mb and output column n0 (kb >= k_blocks: adapter stage kb - k_blocks).
     auto issue = [&](uint32_t s, int kb, int mb, int n0) {
         const bool ext = kLora && kb >= a.k_blocks;
         mbar_arrive_expect_tx(full(s), xbytes + w_stage_bytes<kGlu, kWnk>(n0, a.N) +
                                            (kFused && !ext ? kGBytes : 0));
-        tma_load_2d_nohint(sx + s * xbytes, ext ? &tmT : &tmX, full(s), ext ? 0 : kb * kBK, mb * kRowsBM);
+        tma_load_2d_nohint(sx + s * xbytes, ext ? &tmT : &tmX, full(s), (ext ? kb - a.k_blocks : kb) * kBK,
+                           mb * kRowsBM);
         load_w_stage<kGlu, kWnk>(sw + s * kRowsWBytes, ext ? &tmB : &tmW, full(s), n0, ext ? 0 : kb, a.N, Nout);
         if (kFused && !ext) tma_load_1d(sg + s * kGBytes, &tmG, full(s), kb * kBK);
     };
@@ -298,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (uint32_t i = 0; i < pro; ++i) {
                 const int kb = kb0 + static_cast<int>(i);
                 if (kLora && kb >= kb1) grid_dep_wait();
-                issue(i, kb < kb1 ? kb : a.k_blocks, mb, n0);
+                issue(i, kb < kb1 ? kb : a.k_blocks + (kb - kb1), mb, n0);
             }
         }
     }
@@ -334,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t s = ring.idx, ph = ring.phase;
                     if (!mbar_wait(empty(s), ph ^ 1, abort)) { ok = false; break; }
                     if (kLora && kb >= kb1) grid_dep_wait();   // the adapter stage reads T
-                    issue(s, kb < kb1 ? kb : a.k_blocks, mb, n0);
+                    issue(s, kb < kb1 ? kb : a.k_blocks + (kb - kb1), mb, n0);
                     ++it;
                     ring.advance();
                 }
@@ -456,7 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool warp_has_rows = q * 32 < rows_here;              // warp-uniform
             const int m = mb * kRowsBM + row;
             const float r = kFused && !a.unscaled ? rsqrtf(sr[buf * kRowsBM + row] * inv_k + a.eps) : 1.f;
-            __nv_bfloat16* yrow = Y + static_cast<size_t>(m) * Nout + n0;
+            const int ldy = !kGlu && a.hilo ? 2 * kBK : Nout;   // row stride of Y
+            __nv_bfloat16* yrow = Y + static_cast<size_t>(m) * ldy + n0;
             for (int c = 0; warp_has_rows && c < kOutBN / 32; ++c) {
                 if (c * 32 >= ncols) break;   // warp-uniform
                 uint32_t v[32], w2[kGlu ? 32 : 1];
@@ -471,6 +496,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int g = 0; g < 4; ++g) {
                         const int col = c * 32 + g * 8;
                         if (col < ncols) {
+                            if (!kGlu && a.hilo) {
+                                store_hilo4(yrow, col, out(g * 8 + 0), out(g * 8 + 1), out(g * 8 + 2),
+                                            out(g * 8 + 3));
+                                store_hilo4(yrow, col + 4, out(g * 8 + 4), out(g * 8 + 5), out(g * 8 + 6),
+                                            out(g * 8 + 7));
+                                continue;
+                            }
                             uint4 o;
                             o.x = pack_bf16x2(out(g * 8 + 0), out(g * 8 + 1));
                             o.y = pack_bf16x2(out(g * 8 + 2), out(g * 8 + 3));
@@ -630,6 +662,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         o4[1] = acc[0].y * r;
                         o4[2] = acc[0].z * r;
                         o4[3] = acc[0].w * r;
+                        if (a.hilo) {
+                            store_hilo4(Y + static_cast<size_t>(mb * kRowsBM + rr) * (2 * kBK), col, o4[0], o4[1],
+                                        o4[2], o4[3]);
+                            continue;
+                        }
                     }
                     uint2 o;
                     o.x = pack_bf16x2(o4[0], o4[1]);
@@ -686,7 +723,7 @@ constexpr uint32_t kTaAccCol = 0, kTaACol = 256;
 // piece b % tail_pieces of tail tile b / tail_pieces (tile full + that).
 struct TaUnit {
     int t, kb0, kb1, piece;   // piece < 0: the whole K range
-    int extra;                // 1: the low-rank adapter stage follows (whole tile, or piece 0)
+    int extra;                // adapter stages that follow (whole tile, or piece 0 of a tail tile)
 };
 __device__ __forceinline__ bool ta_unit(const RowsLaunch& a, int i, TaUnit& u) {
     const int G = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
@@ -697,7 +734,7 @@ __device__ __forceinline__ bool ta_unit(const RowsLaunch& a, int i, TaUnit& u) {
         u.kb0 = 0;
         u.kb1 = a.k_blocks;
         u.piece = -1;
-        u.extra = a.lora ? 1 : 0;
+        u.extra = a.lora ? kLoraStages : 0;
         return true;
     }
     const int whole = b < full ? (full - b + G - 1) / G : 0;
@@ -706,7 +743,7 @@ __device__ __forceinline__ bool ta_unit(const RowsLaunch& a, int i, TaUnit& u) {
     u.t = full + b / a.tail_pieces;
     u.kb0 = u.piece * a.tail_kbp;
     u.kb1 = min(a.k_blocks, u.kb0 + a.tail_kbp);
-    u.extra = a.lora && u.piece == 0 ? 1 : 0;
+    u.extra = a.lora && u.piece == 0 ? kLoraStages : 0;
     return true;
 }
 
@@ -808,13 +845,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 rows_tile_coords(un.t, a.m_tiles, a.n_tiles, mb, nb);
                 const int n0 = nb * kOutBN;
                 for (int kb = un.kb0; kb < un.kb1 + (kLora ? un.extra : 0); ++kb) {
-                    const bool ext = kLora && kb >= un.kb1;   // the adapter stage: T and B
+                    const bool ext = kLora && kb >= un.kb1;   // the adapter stages: T (hi, lo) and B
                     if (!mbar_wait(empty0 + 8 * ring.idx, ring.phase ^ 1, abort)) { ok = false; break; }
                     const uint32_t f = full0 + 8 * ring.idx;
                     if (load_x) {
                         mbar_arrive_expect_tx(f, kTaXBytes + (ext ? 0 : kGBytes));
-                        tma_load_2d_nohint(sx + ring.idx * kTaXBytes, ext ? &tmT : &tmX, f, ext ? 0 : kb * kBK,
-                                           mb * kRowsBM);
+                        tma_load_2d_nohint(sx + ring.idx * kTaXBytes, ext ? &tmT : &tmX, f,
+                                           (ext ? kb - un.kb1 : kb) * kBK, mb * kRowsBM);
                         if (!ext) tma_load_1d(sg + ring.idx * kGBytes, &tmG, f, kb * kBK);
                     } else {
                         mbar_arrive_expect_tx(f, w_stage_bytes<kGlu, kWnk>(n0, a.N));
@@ -1055,6 +1092,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             o4[1] = acc[0].y * r;
                             o4[2] = acc[0].z * r;
                             o4[3] = acc[0].w * r;
+                            if (a.hilo) {
+                                store_hilo4(Y + static_cast<size_t>(m) * (2 * kBK), col, o4[0], o4[1], o4[2], o4[3]);
+                                continue;
+                            }
                         }
                         uint2 o;
                         o.x = pack_bf16x2(o4[0], o4[1]);
@@ -1072,8 +1113,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float r = a.unscaled ? 1.f : rsqrtf(ss_row * inv_k + a.eps);
             uint32_t pk[kOutBN / 2];   // the row's outputs, packed as bf16x2
+            // a hilo output: the first 64 accumulator columns as hi (words
+            // 0..31, columns 0..63 of Y) and lo (words 32..63, columns 64..127)
+            const bool hilo = !kGlu && a.hilo;
+            if (hilo) {
+#pragma unroll
+                for (int c = 0; c < kBK / 16; ++c) {
+                    uint32_t v[16];
+                    tmem_ld_32x16(taddr + c * 16, v);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        hilo_pack(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]), pk[c * 8 + i],
+                                  pk[kBK / 2 + c * 8 + i]);
+                }
+            }
 #pragma unroll
             for (int c = 0; c < kOutBN / 16; ++c) {
+                if (hilo) break;
                 uint32_t v[16];
                 tmem_ld_32x16(taddr + c * 16, v);
                 if constexpr (kGlu) {
@@ -1095,9 +1151,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(accempty);   // the MMA may start the next tile
             bool ok = true;
+            const int nstore = hilo ? 2 * kBK : Nout;   // columns of Y
 #pragma unroll
             for (int c = 0; c < kOutBN / 32; ++c) {
-                if (n0 + c * 32 < Nout) {             // block-uniform
+                if (n0 + c * 32 < nstore) {             // block-uniform
                     const uint32_t sbuf = sout + (chunks & 1) * kTaStageOut;
                     // the store issued two chunks ago must have read this buffer
                     if (e == 0) bulk_wait_group_read<1>();
@@ -1621,20 +1678,26 @@ size_t cols_fixed_smem_bytes(int MP, int red_slots) { return cols_layout(MP, 0, 
 size_t cols_stage_bytes(int MP) { return kColsBN * kBK * 2 + MP * kBK * 2 + kGBytes; }
 
 // Launch with programmatic dependent launch (the kernel's set-up may overlap
-// the previous kernel on the stream) and, optionally, a 1-D cluster.
+// the previous kernel on the stream) and, optionally, a 1-D cluster, or as a
+// cooperative grid (all CTAs resident at once, or the launch fails).
 template <typename... Args>
 cudaError_t launch_ex(void (*kern)(Args...), int grid, size_t smem, int cluster, cudaStream_t s,
-                      Args... args) {
+                      bool cooperative, Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[3];
     int n = 0;
     attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[n].val.programmaticStreamSerializationAllowed = 1;
     ++n;
+    if (cooperative) {
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n].val.cooperative = 1;
+        ++n;
+    }
     if (cluster > 1) {
         attr[n].id = cudaLaunchAttributeClusterDimension;
         attr[n].val.clusterDim.x = cluster;
@@ -1662,7 +1725,10 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
         cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(ta),
                                          lora ? 18 : wnk ? (glu ? 15 : 14) : (glu ? 9 : 6));
         if (e != cudaSuccess) return e;
-        e = launch_ex(ta, a.grid, kTaSmem, 1, s, tmX, tmW, tmG, tmT, tmB, *a.tmY, y, a);
+        // The pieces of a tail tile wait for one another: launched as a
+        // cooperative grid, every CTA is resident at once (or the launch
+        // fails), whatever else shares the device.
+        e = launch_ex(ta, a.grid, kTaSmem, 1, s, a.tail_tiles > 0, tmX, tmW, tmG, tmT, tmB, *a.tmY, y, a);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
@@ -1686,7 +1752,7 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), slot);
     if (e != cudaSuccess) return e;
     const size_t smem = rows_smem_bytes(a.xrows, a.stages, split ? a.splits : 0, a.MP, split && a.red_overlay, glu);
-    e = launch_ex(kern, a.grid, smem, split ? a.splits : 1, s, tmX, tmW, tmG, tmT, tmB, y, a);
+    e = launch_ex(kern, a.grid, smem, split ? a.splits : 1, s, false, tmX, tmW, tmG, tmT, tmB, y, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -1698,7 +1764,7 @@ cudaError_t launch_cols(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), fused ? 2 : 3);
     if (e != cudaSuccess) return e;
     const size_t smem = cols_smem_bytes(a.MP, a.stages, a.cluster ? a.splits - 1 : 0);
-    e = launch_ex(kern, a.grid, smem, a.cluster ? a.splits : 1, s, tmX, tmW, tmG, y, a);
+    e = launch_ex(kern, a.grid, smem, a.cluster ? a.splits : 1, s, false, tmX, tmW, tmG, y, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

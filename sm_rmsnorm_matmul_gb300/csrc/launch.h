@@ -55,7 +55,11 @@ struct RowsLaunch {
                                // Y [M, F] = silu(gate) * up; output tiles of 128 columns
     int w_nk;                  // 1: W stored [N, K] (K contiguous), read K-major
     int unscaled;              // 1: no division by the row RMS (Y = (X*g) @ W)
-    int lora;                  // 1: one more stage per tile from the adapter's T and B
+    int hilo;                  // 1 (with unscaled, N <= 64): each output v is written as the
+                               // bf16 pair hi = bf16(v), lo = bf16(v - hi), Y [M, 128] with
+                               // hi in columns [0, 64) and lo in [64, 128) (zeros past N)
+    int lora;                  // 1: two more stages per tile, the adapter's T (hi, then lo
+                               // columns of a hilo output) times B
     int wait_limit_us;         // limit of one bounded in-kernel wait
     int test_skip_sends;       // test hook: the K-split reduction skips its stores
     int cluster;               // 1: the splits of a tile form a cluster

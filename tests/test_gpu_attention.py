@@ -67,8 +67,8 @@ def references(Q, K, V, gq, gk, eps, causal, qpos=None, scale=None):
     return ref, wabs, qn, kn
 
 
-def assert_attention_close(O, Q, K, V, gq, gk, eps, causal, what, qpos=None):
-    ref, wabs, qn, kn = references(Q, K, V, gq, gk, eps, causal, qpos)
+def assert_attention_close(O, Q, K, V, gq, gk, eps, causal, what, qpos=None, scale=None):
+    ref, wabs, qn, kn = references(Q, K, V, gq, gk, eps, causal, qpos, scale=scale)
     o = oracle.to_f64(O)
     if qpos is not None:
         o = o[:, qpos]
@@ -77,17 +77,23 @@ def assert_attention_close(O, Q, K, V, gq, gk, eps, causal, what, qpos=None):
     bad = ~(err <= tol)   # NaN fails
     assert not bad.any(), (f"{what}: {int(bad.sum())} of {ref.size} outside the bound, "
                            f"max err {float(np.nanmax(err)):.3e}")
-    # the exact oracle (no rounding): the key rounding moves every score by at
-    # most 2^-9 * scale * sum_d |qn_d kn_d| (taken as 2^-8 below); to first
-    # order the output moves by at most twice the largest such shift times
-    # sum_j p_j |v_jd - o_d| <= 2 * sum_j p_j |v_jd|
-    exact = oracle.qknorm_attention(Q, K, V, gq, gk, eps, causal=causal, qpos=qpos)
-    D = Q.shape[3]
+    # The exact oracle (no rounding anywhere).  The reference differs from it
+    # only in the keys: kd = bf16(fp32(kn * gq)) is within (2^-9 + 2^-23) of
+    # kn * gq relatively (one fp32 and one bf16 rounding to nearest), so every
+    # score moves by |delta_j| <= Delta = (2^-9 + 2^-23) * scale *
+    # sum_d |qn_d| max_j |kn_jd|.  Each softmax weight then changes by the
+    # factor e^delta_j / sum_i p_i e^delta_i, within [e^-2Delta, e^2Delta], so
+    # |p'_j - p_j| <= (e^2Delta - 1) p_j <= (e^2Delta - 1) e^2Delta p'_j and
+    # |O_ref - O_exact| <= (e^2Delta - 1) e^2Delta sum_j p'_j |v_jd|, where
+    # sum_j p'_j |v_jd| is wabs (the reference's weights).  No first-order
+    # step: the bound holds for any Delta.
+    exact = oracle.qknorm_attention(Q, K, V, gq, gk, eps, scale=scale, causal=causal, qpos=qpos)
     rep = Q.shape[2] // K.shape[2]
     qs = np.abs(qn if qpos is None else qn[:, qpos])
     ks = np.repeat(np.abs(kn), rep, axis=2).max(axis=1, keepdims=True)
-    shift = 2.0 ** -8 / math.sqrt(D) * (qs * ks).sum(axis=3, keepdims=True)
-    tol_e = 1.25 * (2 * shift * 2 * wabs) + tol
+    c = (1.0 / math.sqrt(Q.shape[3]) if scale is None else scale)
+    delta = (2.0 ** -9 + 2.0 ** -23) * c * (qs * ks).sum(axis=3, keepdims=True)
+    tol_e = tol + np.expm1(2 * delta) * np.exp(2 * delta) * wabs
     bad = ~(np.abs(o - exact) <= tol_e)
     assert not bad.any(), f"{what}: {int(bad.sum())} outside the bound of the exact oracle"
 
@@ -178,9 +184,8 @@ def test_explicit_scale_and_eps(rmm):
     Qd, Kd, Vd = inputs.split_qkv(qkv.cuda(), B, S, Hq, Hkv, D)
     O = rmm.qknorm_attention(Qd, Kd, Vd, gq.cuda(), gk.cuda(), 0.25, scale=1.0 / 16, causal=False)
     torch.cuda.synchronize()
-    ref, wabs, _, _ = references(Q, K, V, gq, gk, 0.25, False, scale=1.0 / 16)
-    err = np.abs(oracle.to_f64(O.cpu()) - ref)
-    assert (err <= 2.0 ** -8 * wabs + 2.0 ** -8 * np.abs(ref) + 1e-5).all()
+    assert rmm.device_status() == 0
+    assert_attention_close(O.cpu(), Q, K, V, gq, gk, 0.25, False, "explicit scale and eps", scale=1.0 / 16)
 
 
 @pytest.mark.parametrize("B,S,Hq,Hkv,causal", [

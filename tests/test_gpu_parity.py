@@ -222,28 +222,14 @@ def test_weight_nk(rmm, M, K, N, gated):
 # ------------------------------------------------------- low-rank adapter
 # rmsnorm_matmul_lora: Y = RMSNorm(X) @ (W + A @ B), A [K,R], B [R,N].
 LORA = [
-    (16, 4096, 6144, 16),    # decode QKV shape: K split, the adapter stage in split 0
+    (16, 4096, 6144, 16),    # decode QKV shape: K split, the adapter stages in split 0
     (64, 4096, 28672, 64),   # one CTA per column tile
     (7, 72, 136, 8),         # ragged rows, K and N; a single k-block plus the adapter
     (1280, 1024, 4096, 32),  # prefill kernel: whole tiles and K pieces (piece 0 adds it)
     (300, 520, 264, 24),     # several row tiles, ragged
+    (4096, 4096, 6144, 64),  # prefill QKV shape (the benchmark's adapter line): T's launch cut along K
+    (20000, 1024, 512, 56),  # 157 row tiles for T's launch: whole tiles (TMA stores) and a K-cut tail
 ]
-
-
-def assert_lora_close(Y, X, g, W, A, B, eps, what):
-    """Y = RMSNorm(X) @ (W + A @ B) against the oracle.  The tensor cores take
-    the adapter's intermediate T = (X*g) @ A as bf16, one rounding per element
-    (relative error <= 2^-8) that the K-sum does not average out, so the bound
-    adds that rounding carried through r[m] * T @ B to the ungated one:
-      |dy| <= 1e-2 + 1e-2 |y| + r[m] * 2^-8 * sum_j |T[m,j]| |B[j,n]|."""
-    ref = oracle.rmsnorm_matmul_lora(X, g, W, A, B, eps)
-    Xf, gf, Af, Bf = (oracle.to_f64(t) for t in (X, g, A, B))
-    r = 1.0 / np.sqrt((Xf * Xf).mean(axis=1) + eps)
-    T = (Xf * gf[None, :]) @ Af
-    tol = ATOL + RTOL * np.abs(ref) + r[:, None] * 2.0 ** -8 * (np.abs(T) @ np.abs(Bf))
-    y = oracle.to_f64(Y)
-    bad = ~(np.abs(y - ref) <= tol)   # NaN fails
-    assert not bad.any(), f"{what}: {int(bad.sum())} of {ref.size} outside the bound"
 
 
 @pytest.mark.parametrize("M,K,N,R", LORA)
@@ -254,7 +240,9 @@ def test_lora(rmm, M, K, N, R):
     Y = rmm.rmsnorm_matmul_lora(X.cuda(), g.cuda(), W.cuda(), A.cuda(), B.cuda(), 1e-5)
     torch.cuda.synchronize()
     assert rmm.device_status() == 0
-    assert_lora_close(Y.cpu(), X, g, W, A, B, 1e-5, f"lora {M}x{K}x{N} R={R}")
+    # the plain bound of every other form: the adapter's intermediate T is
+    # carried as a bf16 hi/lo pair, so no rounding beyond the plain form's
+    assert_close(Y.cpu(), oracle.rmsnorm_matmul_lora(X, g, W, A, B, 1e-5), f"lora {M}x{K}x{N} R={R}")
     # a zero adapter gives the plain result
     Y0 = rmm.rmsnorm_matmul_lora(X.cuda(), g.cuda(), W.cuda(), torch.zeros_like(A).cuda(), B.cuda(), 1e-5)
     torch.cuda.synchronize()
