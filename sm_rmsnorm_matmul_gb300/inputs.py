@@ -115,15 +115,25 @@ def random_problem(M: int, K: int, N: int, seed: int, x_kind: str = "normal"):
     return generate(M, K, N, seed=seed, w_std=1.0 / math.sqrt(K), x_kind=x_kind)
 
 
-def lora_adapter(K: int, N: int, R: int, seed: int):
+def lora_adapter(K: int, N: int, R: int, seed: int, share: float = 1.0):
     """A low-rank adapter (A [K,R], B [R,N]) as contiguous bf16 CPU tensors:
-    A ~ N(0, 1/sqrt(K)), B ~ N(0, 1/sqrt(R)), so that the adapter's share of
-    the output is of the same order as W's for unit-RMS rows."""
+    A ~ N(0, 1/sqrt(K)), B ~ N(0, sqrt(share/R)), so that each element of
+    A @ B has variance share/K: with share = 1 the adapter's part of the output
+    is of the same order as that of a W of std 1/sqrt(K)."""
     gen = torch.Generator(device="cpu")
     gen.manual_seed(seed)
     a = torch.randn(K, R, generator=gen, dtype=torch.float32) / math.sqrt(K)
-    b = torch.randn(R, N, generator=gen, dtype=torch.float32) / math.sqrt(R)
+    b = torch.randn(R, N, generator=gen, dtype=torch.float32) * math.sqrt(share / R)
     return a.to(torch.bfloat16).contiguous(), b.to(torch.bfloat16).contiguous()
+
+
+def lora_problem(M: int, K: int, N: int, R: int, seed: int, x_kind: str = "row_scaled"):
+    """X, g, W, A, B for RMSNorm(X) @ (W + A @ B) with unit-RMS outputs, like
+    every workload above: W ~ N(0, 1/sqrt(2K)) and an adapter of share 1/2, so
+    that W + A @ B has the per-element variance 1/K of a plain workload's W."""
+    X, g, W = generate(M, K, N, seed=seed, w_std=1.0 / math.sqrt(2 * K), x_kind=x_kind)
+    A, B = lora_adapter(K, N, R, seed=seed + 1, share=0.5)
+    return X, g, W, A, B
 
 
 @dataclass(frozen=True)
