@@ -707,7 +707,7 @@ def main():
         "data": "synthetic (seeded; see sm_rmsnorm_matmul_gb300/inputs.py)",
         "config": {
             "workload": w.name, "M": w.M, "K": w.K, "N": w.N, "eps": w.eps, "seed": w.seed,
-            "accumulate": "fp32", "path": "small-M (cols)" if main_res["path"] == 2 else "row-tile",
+            "accumulate": "fp32", "path": "small-M (gemv)" if main_res["path"] == 2 else "row-tile",
             "plan": main_res["plan"],
             "l2": f"rotating input/output copies: {main_res['n_copies']} x "
                   f"{w.bytes_algorithmic / 1e6:.1f} MB > 3 x L2 ({l2 / 1e6:.0f} MB)"
@@ -774,7 +774,7 @@ def kernel_name(rmm, w):
     """Name of the kernel the fused call launches for this workload."""
     plan = rmm.describe_plan(w.M, w.K, w.N)
     if plan["path"] == 2:
-        return "cols_kernel<fused>"
+        return f"gemv_kernel<fused> ({plan['splits']} K pieces per 64-column unit)"
     if plan["cluster"]:
         return f"rows_kernel<fused, K split x{plan['splits']} in a cluster>"
     if w.M > 128:
@@ -810,7 +810,7 @@ def shape_entry(w, t, r, peaks, k, gated=False, lora_r=0):
     bound = "tensor" if flops / (peaks["bf16_tflops"] * 1e12) > nbytes / (peaks["hbm_gbs"] * 1e9) else "hbm"
     e = {"workload": w.name + (" (gated: silu(gate) * up)" if gated else "") +
          (f" (low-rank adapter, R = {lora_r})" if lora_r else ""),
-         "path": "small-M (cols)" if r["path"] == 2 else "row-tile",
+         "path": "small-M (gemv)" if r["path"] == 2 else "row-tile",
          "plan": r.get("plan"),
          "steps": k, "us_per_call": round(t * 1e6, 3), "tflops": round(tflops, 2),
          "hbm_gbs": round(gbs, 1), "bound": bound, "roofline_frac": round(roof_t / t, 4),

@@ -66,20 +66,25 @@ typedef enum {
  *   X  [M,K] bf16 input rows           g [K] bf16 gain
  *   W  [K,N] bf16 weights (N contiguous) Y [M,N] bf16 output (written)
  *   eps added to the mean square inside the square root.
- * One launch of the tensor-core row-tile kernels: 128-row x 256-column tiles,
- * X*g and the row sum of squares computed in the same pass as the
- * contraction, r[m] applied in the epilogue.  For M <= 128 the K range may be
- * split over up to 8 CTAs of a thread-block cluster whose partial sums are
- * combined in shared memory, in a fixed order.  For more row tiles, when the
- * tiles leave a last wave of CTAs at most half full, those last tiles are cut
- * along K, one piece per CTA, and the pieces are combined, in a fixed order,
- * through a library-owned fp32 workspace per (device, stream); the pieces of
- * a tile wait for one another, so such a launch is cooperative: all its CTAs
- * (at most one per SM) are resident at once, or the launch fails with
- * RMM_ERR_LAUNCH (for example on a device partition with fewer SMs than the
- * device reports).  With rmm_force_path(2) the operand-swapped
- * small-M kernel runs instead; its K split may use the same workspace.  The
- * workspace is allocated on first use of a shape that needs it (make that
+ * Shape-based dispatch between two kernels:
+ *  - M <= 16: the small-M path, a split-K GEMV-style kernel: W streamed with
+ *    128-bit loads straight into mma.sync fragments, X*g and the row sums of
+ *    squares formed on the fly, 64-column units whose K range may be cut into
+ *    pieces; the pieces meet in a library-owned fp32 workspace per (device,
+ *    stream) and the last CTA of a unit adds them in a fixed order (no CTA
+ *    waits for another).
+ *  - M > 16: the tcgen05 row-tile kernels: 128-row x 256-column tiles, X*g
+ *    and the row sum of squares computed in the same pass as the contraction,
+ *    r[m] applied in the epilogue.  For M <= 128 the K range may be split over
+ *    up to 8 CTAs of a thread-block cluster whose partial sums are combined in
+ *    shared memory, in a fixed order.  For more row tiles, when the tiles
+ *    leave a last wave of CTAs at most half full, those last tiles are cut
+ *    along K, one piece per CTA, and the pieces are combined, in a fixed
+ *    order, through the same workspace; the pieces of a tile wait for one
+ *    another, so such a launch is cooperative: all its CTAs (at most one per
+ *    SM) are resident at once, or the launch fails with RMM_ERR_LAUNCH (for
+ *    example on a device partition with fewer SMs than the device reports).
+ * The workspace is allocated on first use of a shape that needs it (make that
  * first call outside any CUDA-graph capture).
  * Returns an rmm_status.
  */
@@ -165,7 +170,7 @@ int matmul(const void* A, const void* B, void* C,
 /*
  * Test and benchmark switch for the dispatcher of rmsnorm_matmul() and
  * matmul(): 0 = shape-based choice (default), 1 = always the row-tile path,
- * 2 = always the small-M path (requires M <= 128; larger M returns
+ * 2 = always the small-M path (requires M <= 16; larger M returns
  * RMM_ERR_INVALID_ARG while forced).  Returns the previous setting, or -1 for
  * an unknown value (the setting is then unchanged).
  */
@@ -214,17 +219,17 @@ const char* rmm_status_string(int code);
  *
  * It runs the same kernels with the same launch plan as rmsnorm_matmul()
  * (results agree bit for bit), but the K-split partial sums that
- * rmsnorm_matmul() keeps in a workspace allocated on first use -- the tail
- * pieces of the prefill kernel, and the global split of the small-M path under
- * rmm_force_path(2) -- live in one fixed 20 MiB device array inside this
+ * rmsnorm_matmul() keeps in a workspace allocated on first use -- the K
+ * pieces of the small-M path and the tail pieces of the prefill kernel --
+ * live in one fixed 20 MiB device array inside this
  * library (a file-scope __device__ array), held on every device where the
  * library's device code is loaded until the process exits.  Limit: the plan's
  * partials (fp32 sums plus row sums of squares) must fit in 20 MiB - 64 KiB
  * and its arrival counters in 64 KiB; the tail pieces of any shape fit on a
  * device of up to 152 SMs (at most one 128 x 256 fp32 piece per SM), and a
  * plan that needs more returns RMM_ERR_SCRATCH_LIMIT before any launch.
- * Plans without a K split through memory (decode shapes, which split K inside
- * a cluster) use no scratch.
+ * Plans without a K split through memory (whole tiles, or a K split inside a
+ * cluster) use no scratch.
  *
  * The first call on a device looks up the array's device address (once per
  * device, with that device current) and keeps it for the life of the process;

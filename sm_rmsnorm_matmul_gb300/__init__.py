@@ -26,7 +26,7 @@ __all__ = [
     "rmsnorm_matmul_ex", "rmsnorm_matmul_lora", "WEIGHT_NK", "GATED_SILU", "rmsnorm", "matmul",
     "force_path",
     "dispatch_path", "describe_plan", "device_status", "status_string", "STATUS", "PATH_AUTO",
-    "PATH_ROWS", "PATH_COLS", "ABI_FUNCTIONS", "rmsnorm_heads", "qknorm_attention",
+    "PATH_ROWS", "PATH_SMALL_M", "ABI_FUNCTIONS", "rmsnorm_heads", "qknorm_attention",
 ]
 
 STATUS = {
@@ -34,7 +34,7 @@ STATUS = {
     3: "RMM_ERR_UNSUPPORTED_DEVICE", 4: "RMM_ERR_LAUNCH",
     5: "RMM_ERR_DEVICE_TIMEOUT", 6: "RMM_ERR_INTERNAL", 7: "RMM_ERR_SCRATCH_LIMIT",
 }
-PATH_AUTO, PATH_ROWS, PATH_COLS = 0, 1, 2
+PATH_AUTO, PATH_ROWS, PATH_SMALL_M = 0, 1, 2
 WEIGHT_NK, GATED_SILU = 1, 2   # flags of rmsnorm_matmul_ex
 
 # Every function declared in include/rmsnorm_matmul.h and include/qknorm_attention.h.
@@ -345,7 +345,7 @@ def matmul(A, B, out=None, stream=None):
 
 
 def force_path(path: int) -> int:
-    """0 auto, 1 row-tile path, 2 small-M path.  Returns the previous value."""
+    """0 auto, 1 row-tile path, 2 small-M path (M <= 16).  Returns the previous value."""
     prev = lib().rmm_force_path(int(path))
     if prev < 0:
         raise ValueError(f"unknown path {path}")

@@ -1,6 +1,6 @@
 """Build libsm_rmsnorm_matmul.so in-tree with nvcc for sm_103a.
 
-Three translation units (kernels.cu, attention.cu, api.cu) are compiled in parallel and
+Four translation units (kernels.cu, attention.cu, gemv.cu, api.cu) are compiled in parallel and
 linked into ``sm_rmsnorm_matmul_gb300/_lib/libsm_rmsnorm_matmul.so`` with the
 CUDA runtime linked statically.  Rebuilds only when a source is newer than the
 library.  Run as ``python -m sm_rmsnorm_matmul_gb300.build [--force] [-v]``.
@@ -21,7 +21,7 @@ LIB_DIR = os.path.join(PKG, "_lib")
 LIB_NAME = "libsm_rmsnorm_matmul.so"
 LIB_PATH = os.path.join(LIB_DIR, LIB_NAME)
 
-SOURCES = ["kernels.cu", "attention.cu", "api.cu"]
+SOURCES = ["kernels.cu", "attention.cu", "gemv.cu", "api.cu"]
 HEADERS = ["ptx.cuh", "launch.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",

@@ -31,7 +31,7 @@ std::atomic<int> g_wait_limit_us{static_cast<int>(kDefaultWaitUs)};
 std::atomic<int> g_skip_sends{0};
 
 constexpr int kPathRows = 1;
-constexpr int kPathCols = 2;
+constexpr int kPathSmallM = 2;
 
 // ------------------------------------------------------------------ device
 struct DeviceInfo {
@@ -228,7 +228,13 @@ int get_workspace(int dev, cudaStream_t s, size_t acc_bytes, size_t ss_bytes, si
     if (w.acc) cudaFree(w.acc);
     if (w.ss) cudaFree(w.ss);
     if (w.counters) cudaFree(w.counters);
-    w = n;
+    // the adapter's T and the normalised keys keep their own buffers
+    w.acc = n.acc;
+    w.acc_bytes = n.acc_bytes;
+    w.ss = n.ss;
+    w.ss_bytes = n.ss_bytes;
+    w.counters = n.counters;
+    w.n_counters = n.n_counters;
     *out = w;
     return RMM_OK;
 }
@@ -289,94 +295,50 @@ int get_khat_buffer(int dev, cudaStream_t s, size_t bytes, void** out) {
 }
 
 // ---------------------------------------------------------------- planning
-struct ColsPlan {
-    int MP, n_tiles, k_blocks, splits, kb_per_split, stages, grid, cluster;
-    uint32_t tmem_cols;
+// Small-M path (gemv.cu): units of 64 columns, K cut into `splits` pieces of
+// steps_per_piece 16-deep k-steps, one CTA per piece.
+struct GemvPlan {
+    int units, ksteps, splits, steps_per_piece;
 };
 
-std::mutex g_occ_mu;
-std::map<std::tuple<int, bool, int, size_t>, int> g_occ;
+std::mutex g_gv_mu;
+std::map<std::pair<int, bool>, int> g_gv_occ;
 
-// Clusters of `splits` CTAs that can be resident at once, cached per device.
-int max_clusters(int dev, bool fused, int splits, size_t smem) {
-    std::lock_guard<std::mutex> lk(g_occ_mu);
-    auto key = std::make_tuple(dev, fused, splits, smem);
-    auto it = g_occ.find(key);
-    if (it != g_occ.end()) return it->second;
-    const int n = rmm::cols_max_active_clusters(fused, splits, smem);
-    g_occ[key] = n;
+int gemv_slots_per_sm(int dev, bool fused) {
+    std::lock_guard<std::mutex> lk(g_gv_mu);
+    auto key = std::make_pair(dev, fused);
+    auto it = g_gv_occ.find(key);
+    if (it != g_gv_occ.end()) return it->second;
+    const int n = std::max(1, rmm::gemv_ctas_per_sm(fused));
+    g_gv_occ[key] = n;
     return n;
 }
 
-int cols_stages(int MP, int red_slots, const DeviceInfo& d) {
-    const size_t fixed = rmm::cols_fixed_smem_bytes(MP, red_slots);
-    const size_t per = rmm::cols_stage_bytes(MP);
-    const size_t avail = d.smem_optin > 0 ? static_cast<size_t>(d.smem_optin) : 227 * 1024;
-    const int st = avail > fixed ? static_cast<int>((avail - fixed) / per) : 0;
-    return std::min(rmm::kColsMaxStages, st);
-}
-
-// Model of one launch of the small-M path, in microseconds (fitted to
-// measurements on GB300): each CTA keeps `stages` W tiles in flight with about
-// 3.2 us from issue to release, the whole GPU streams W at about 5.8 TB/s, a
-// unit of work costs about 1 us of pipeline fill and epilogue, and the last
-// unit's K-split reduction adds about 0.5 us (no split), 1.5 us (cluster) or
-// 3.5 us (global workspace, a few L2 round trips).
-double cols_cost_us(int64_t N, int64_t K, int n_tiles, int splits, int kbps, int resident, int stages,
-                    int mode) {
-    const long units = static_cast<long>(n_tiles) * splits;
-    const long waves = (units + resident - 1) / resident;
-    const double cta_rate = stages * 16384.0 / 3.2e-6;                   // bytes/s per CTA
-    const double per_cta = static_cast<double>(waves) * kbps * 16384.0 / cta_rate;
-    const double total = static_cast<double>(K) * N * 2 / 5.8e12;
-    const double tail = mode == 0 ? 0.5 : (mode == 1 ? 1.5 : 3.5);
-    return std::max(per_cta, total) * 1e6 + waves * 1.0 + tail;
-}
-
-// Choose the K split of the small-M path and how the splits are combined:
-// mode 0 = no split, 1 = cluster (splits 1.. push partials into split 0's
-// shared memory), 2 = global workspace (last arriving warp reduces).
-ColsPlan plan_cols(int dev, bool fused, int64_t M, int64_t K, int64_t N, const DeviceInfo& d,
-                   bool allow_cluster) {
-    ColsPlan p{};
-    p.MP = static_cast<int>(((M + 15) / 16) * 16);
-    p.n_tiles = static_cast<int>((N + rmm::kColsBN - 1) / rmm::kColsBN);
-    p.k_blocks = static_cast<int>((K + kBK - 1) / kBK);
-    const int sms = d.sm_count > 0 ? d.sm_count : 1;
-    double best = 1e300;
-    for (int s = 1; s <= rmm::kColsMaxSplits && s <= p.k_blocks; ++s) {
-        const int kbps = (p.k_blocks + s - 1) / s;
-        const int real = (p.k_blocks + kbps - 1) / kbps;
-        if (real != s) continue;
-        for (int mode = (s == 1 ? 0 : 1); mode <= (s == 1 ? 0 : 2); ++mode) {
-            const bool cl = mode == 1;
-            if (cl && (!allow_cluster || s > rmm::kClusterMaxSplits ||
-                       static_cast<size_t>(s - 1) * p.MP * rmm::kColsBN * 4 > 64 * 1024))
-                continue;
-            const int red_slots = cl ? s - 1 : 0;
-            const int st = cols_stages(p.MP, red_slots, d);
-            if (st < 2) continue;
-            int resident = sms;
-            if (cl) {
-                resident = max_clusters(dev, fused, s, rmm::cols_smem_bytes(p.MP, st, red_slots)) * s;
-                if (resident <= 0) continue;
-            }
-            const double cost = cols_cost_us(N, K, p.n_tiles, s, kbps, resident, st, mode);
-            if (cost < best - 1e-9) {
-                best = cost;
-                p.splits = s;
-                p.kb_per_split = kbps;
-                p.cluster = cl ? 1 : 0;
-                p.stages = st;
-                const long units = static_cast<long>(p.n_tiles) * s;
-                p.grid = static_cast<int>(std::min<long>(units, resident));
-            }
+// K split of the small-M path: the pieces of one launch run as waves of
+// (SMs x CTAs per SM); a piece of P k-steps costs its CTA time in proportion
+// to P (its 8 warps take ceil(P / 8) rounds of loads), and a split adds the
+// publication of the pieces and the last CTA's sum over them, about 8 k-steps
+// plus 4 per batch of 8 pieces (fitted on GB300).  Pieces keep at least one
+// k-step per warp.
+GemvPlan plan_gemv(int dev, bool fused, int64_t K, int64_t N, const DeviceInfo& d) {
+    GemvPlan p{};
+    p.units = static_cast<int>((N + rmm::kGvBN - 1) / rmm::kGvBN);
+    p.ksteps = static_cast<int>((K + rmm::kGvBK - 1) / rmm::kGvBK);
+    const long slots = static_cast<long>(d.sm_count > 0 ? d.sm_count : 1) * gemv_slots_per_sm(dev, fused);
+    p.splits = 1;
+    p.steps_per_piece = p.ksteps;
+    long best = -1;
+    for (int s = 1; s <= 32 && s * 8 <= std::max(8, p.ksteps); ++s) {
+        const int spp = (p.ksteps + s - 1) / s;
+        if ((p.ksteps + spp - 1) / spp != s) continue;
+        const long waves = (static_cast<long>(p.units) * s + slots - 1) / slots;
+        const long cost = waves * spp + (s > 1 ? 8 + 4 * ((s + 7) / 8) : 0);
+        if (best < 0 || cost < best) {
+            best = cost;
+            p.splits = s;
+            p.steps_per_piece = spp;
         }
     }
-    if (p.cluster) p.grid = (p.grid / p.splits) * p.splits;
-    uint32_t cols = 32;
-    while (cols < static_cast<uint32_t>(2 * p.MP)) cols <<= 1;
-    p.tmem_cols = cols;
     return p;
 }
 
@@ -516,14 +478,14 @@ TailPlan plan_tail(const RowsPlan& p, const DeviceInfo& d) {
     return t;
 }
 
-// The row-tile path serves every shape by default: for M <= 128 it streams W
-// with wide tiles and a cluster K split, which measured faster on GB300 than
-// the operand-swapped small-M path.  The small-M path stays available through
-// rmm_force_path(2) and backs rmsnorm_matmul_noalloc's split-K variant.
+// Shape-based dispatch.  The small-M path as built streams W at 3.4-4.3 TB/s
+// against ~6.3 TB/s for the row-tile kernels' TMA rings (decode QKV 14.9 vs
+// 11.9 us, tiny 5.5 vs 5.2 us on GB300), so every shape takes the row-tile
+// kernels unless path 2 is forced.
 int choose_path(int64_t M) {
     (void)M;
     const int f = g_force_path.load();
-    if (f == kPathRows || f == kPathCols) return f;
+    if (f == kPathRows || f == kPathSmallM) return f;
     return kPathRows;
 }
 
@@ -570,6 +532,38 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
     int rc = current_device(&dev, &d);
     if (rc != RMM_OK) return rc;
     const int path = glu || wnk || lora || unscaled ? static_cast<int>(kPathRows) : choose_path(M);
+    if (path == kPathSmallM) {
+        if (M > rmm::kGvMaxM) return RMM_ERR_INVALID_ARG;
+        const GemvPlan p = plan_gemv(dev, fused, K, N, d);
+        rmm::GemvLaunch a{};
+        a.M = static_cast<int>(M);
+        a.N = static_cast<int>(N);
+        a.K = static_cast<int>(K);
+        a.eps = eps;
+        a.units = p.units;
+        a.ksteps = p.ksteps;
+        a.splits = p.splits;
+        a.steps_per_piece = p.steps_per_piece;
+        if (p.splits > 1) {
+            const size_t ws_bytes = static_cast<size_t>(p.units) * p.splits * rmm::kGvPieceFloats * sizeof(float);
+            const size_t ncount = static_cast<size_t>(p.units);
+            if (fixed) {
+                float* unused = nullptr;
+                if (!fixed->place(ws_bytes, 0, &a.ws, &unused) || ncount * sizeof(int) > fixed->counter_bytes)
+                    return RMM_ERR_SCRATCH_LIMIT;
+                if (cudaMemsetAsync(fixed->counters, 0, ncount * sizeof(int), stream) != cudaSuccess)
+                    return RMM_ERR_LAUNCH;
+                a.counters = fixed->counters;
+            } else {
+                Workspace w;
+                rc = get_workspace(dev, stream, ws_bytes, 0, ncount, &w);
+                if (rc != RMM_OK) return rc;
+                a.ws = w.acc;
+                a.counters = w.counters;
+            }
+        }
+        return rmm::launch_gemv(fused, X, g, W, Y, a, stream) == cudaSuccess ? RMM_OK : RMM_ERR_LAUNCH;
+    }
     CUtensorMap tmX, tmW, tmG;
     // [K, N]: boxes of [64 k][64 n]; [N, K]: boxes of [256 n][64 k], or 128 rows
     // each for the gate and up halves of the gated form
@@ -577,49 +571,6 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
         return RMM_ERR_INTERNAL;
     if (fused) {
         if (!map_1d(&tmG, g, K)) return RMM_ERR_INTERNAL;
-    }
-    if (path == kPathCols) {
-        if (M > rmm::kColsMaxMP) return RMM_ERR_INVALID_ARG;
-        const ColsPlan p = plan_cols(dev, fused, M, K, N, d, true);
-        if (!map_2d(&tmX, X, M, K, p.MP)) return RMM_ERR_INTERNAL;
-        if (!fused) tmG = tmX;  // unused by the kernel
-        rmm::ColsLaunch a{};
-        a.M = static_cast<int>(M);
-        a.N = static_cast<int>(N);
-        a.K = static_cast<int>(K);
-        a.eps = eps;
-        a.MP = p.MP;
-        a.n_tiles = p.n_tiles;
-        a.k_blocks = p.k_blocks;
-        a.splits = p.splits;
-        a.kb_per_split = p.kb_per_split;
-        a.stages = p.stages;
-        a.grid = p.grid;
-        a.wait_limit_us = g_wait_limit_us.load();
-        a.cluster = p.cluster;
-        a.tmem_cols = p.tmem_cols;
-        if (p.splits > 1 && !p.cluster) {
-            const size_t acc_bytes = static_cast<size_t>(p.splits) * M * N * sizeof(float);
-            const size_t ss_bytes = static_cast<size_t>(p.n_tiles) * p.splits * rmm::kColsMaxMP * sizeof(float);
-            const size_t ncount = static_cast<size_t>(p.n_tiles) * 4;
-            if (fixed) {
-                if (!fixed->place(acc_bytes, ss_bytes, &a.ws_acc, &a.ws_ss) ||
-                    ncount * sizeof(int) > fixed->counter_bytes)
-                    return RMM_ERR_SCRATCH_LIMIT;
-                if (cudaMemsetAsync(fixed->counters, 0, ncount * sizeof(int), stream) != cudaSuccess)
-                    return RMM_ERR_LAUNCH;
-                a.counters = fixed->counters;
-            } else {
-                Workspace w;
-                rc = get_workspace(dev, stream, acc_bytes, ss_bytes, ncount, &w);
-                if (rc != RMM_OK) return rc;
-                a.ws_acc = w.acc;
-                a.ws_ss = w.ss;
-                a.counters = w.counters;
-            }
-        }
-        return rmm::launch_cols(fused, tmX, tmW, tmG, Y, a, stream) == cudaSuccess ? RMM_OK
-                                                                                  : RMM_ERR_LAUNCH;
     }
     const RowsPlan p = plan_rows(dev, fused, M, K, N, d, glu, wnk, lora);
     if (!map_2d(&tmX, X, M, K, p.xrows)) return RMM_ERR_INTERNAL;
@@ -804,16 +755,16 @@ int rmm_describe_plan(int64_t M, int64_t K, int64_t N, int fused, int* info) {
     if (rc != RMM_OK) return rc;
     for (int i = 0; i < 8; ++i) info[i] = 0;
     info[0] = glu ? static_cast<int>(kPathRows) : choose_path(M);
-    if (info[0] == kPathCols) {
-        if (M > rmm::kColsMaxMP) return RMM_ERR_INVALID_ARG;
-        const ColsPlan p = plan_cols(dev, fused != 0, M, K, N, d, true);
+    if (info[0] == kPathSmallM) {
+        if (M > rmm::kGvMaxM) return RMM_ERR_INVALID_ARG;
+        const GemvPlan p = plan_gemv(dev, fused != 0, K, N, d);
         info[1] = p.splits;
-        info[2] = p.cluster;
-        info[3] = p.grid;
-        info[4] = p.stages;
-        info[5] = p.MP;
-        info[6] = p.n_tiles;
-        info[7] = p.kb_per_split;
+        info[2] = 0;
+        info[3] = p.units * p.splits;
+        info[4] = 0;
+        info[5] = rmm::kGvMaxM;
+        info[6] = p.units;
+        info[7] = p.steps_per_piece;
     } else {
         const RowsPlan p = plan_rows(dev, fused != 0, M, K, N, d, glu);
         info[1] = p.splits;

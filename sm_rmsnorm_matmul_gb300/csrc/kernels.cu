@@ -9,18 +9,18 @@
 // memory, in the same pass that accumulates the row sum of squares.
 //
 // Two tensor-core kernels (tcgen05, accumulators in tensor memory, operands
-// staged by TMA through an mbarrier ring), one warp-specialised CTA per SM:
-//   rows_kernel: CTA tile = 128 rows of X x 256 columns of W.  A = X*g
-//     (K-major), B = W (N-major).  For large M (prefill-like shapes).
-//   cols_kernel: CTA tile = 128 columns of W x MP rows of X (MP <= 128).
-//     A = W^T (N-major, the same shared-memory tile layout), B = X*g
-//     (K-major).  W is streamed once; when N alone gives too few tiles the
-//     K range is split and fp32 partials are combined in a fixed order by
-//     the last CTA to finish a column tile.  For small M (decode-like shapes).
-// Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer, warp 2
-// tensor-memory allocator, warps 4-7 transform (X*g, sum of squares),
-// warps 8-11 epilogue (tensor memory -> registers -> scale by r -> bf16).
+// staged by TMA through an mbarrier ring), one warp-specialised CTA per SM,
+// CTA tile = 128 rows of X x 256 columns of W, A = X*g (K-major), B = W:
+//   rows_kernel: one row tile (M <= 128); when the column tiles alone give
+//     too few CTAs the K range is split over the CTAs of a cluster, whose
+//     partial sums meet in shared memory in a fixed order.
+//   rows_ta_kernel: several row tiles (prefill-like shapes), persistent, the
+//     A operand written into tensor memory as X*g is formed.
+// Warp roles (384 threads): TMA producers, one MMA issuer, a tensor-memory
+// allocator, four transform warps (X*g, sum of squares) and four epilogue
+// warps (tensor memory -> registers -> scale by r -> bf16).
 // A third kernel, rmsnorm_kernel, is the unfused RMSNorm kept for comparison.
+// The small-M path (at most 16 rows of X) is in gemv.cu.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -474,7 +474,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int mb, nb;
             rows_tile_coords(u, a.m_tiles, a.n_tiles, mb, nb);
             const int n0 = nb * kOutBN;
-            const int ncols = min(kOutBN, Nout - n0);
+            // a hilo output writes all 64 columns of each half (zeros past N)
+            const int ncols = !kGlu && a.hilo ? kBK : min(kOutBN, Nout - n0);
             const int rows_here = min(kRowsBM, a.M - mb * kRowsBM);   // valid rows of this tile
             const uint32_t taddr = tmem + buf * kRowsBN + (static_cast<uint32_t>(q * 32) << 16);
             const bool warp_has_rows = q * 32 < rows_here;              // warp-uniform
@@ -546,7 +547,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int mb = 0, nb = 0;
         if (have) rows_tile_coords(u / split, a.m_tiles, a.n_tiles, mb, nb);
         const int n0 = nb * kOutBN;
-        const int ncols = min(kOutBN, Nout - n0);   // output columns of this tile
+        // output columns of this tile (a hilo output: all 64 of each half, zeros past N)
+        const int ncols = !kGlu && a.hilo ? kBK : min(kOutBN, Nout - n0);
         const int rows_here = min(kRowsBM, a.M - mb * kRowsBM);
         // reduction units of 32 output columns: accumulator chunk u, or (gated)
         // gate chunk u with up chunk u + 4
@@ -1079,7 +1081,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             acc[h].z += t4.z;
                             acc[h].w += t4.w;
                         }
-                    if (m < a.M && n0 + col < Nout) {
+                    if (m < a.M && n0 + col < (!kGlu && a.hilo ? kBK : Nout)) {
                         const float r = rr[rl];
                         float o4[4];
                         if constexpr (kGlu) {
@@ -1187,416 +1189,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// ------------------------------------------------------------ small-M path
-struct ColsLayout {
-    uint32_t off_w, off_x, off_g, off_red, off_bar, off_ss, off_r, off_redss, off_misc, total;
-};
-
-// Shared-memory layout of cols_kernel.  With a cluster reduction, split 0's
-// CTA receives the other splits' fp32 partial tiles in `red`, as
-// [red_slots][MP rows][128 columns], and their row sums of squares in `redss`.
-__host__ __device__ inline ColsLayout cols_layout(int MP, int stages, int red_slots) {
-    ColsLayout L;
-    L.off_w = 0;
-    L.off_x = L.off_w + stages * (kColsBN * kBK * 2);
-    L.off_g = L.off_x + stages * (MP * kBK * 2);
-    L.off_red = L.off_g + stages * kGBytes;
-    L.off_bar = L.off_red + red_slots * MP * kColsBN * 4;
-    const uint32_t nbars = 3 * kColsMaxStages + 10;
-    L.off_ss = L.off_bar + ((nbars * 8 + 15) / 16) * 16;
-    L.off_r = L.off_ss + 2 * kColsMaxMP * 4;
-    L.off_redss = L.off_r;
-    L.off_misc = L.off_redss + (kClusterMaxSplits - 1) * kColsMaxMP * 4;
-    L.total = L.off_misc + 16 + 1024;
-    return L;
-}
-
-template <bool kFused>
-__global__ void __launch_bounds__(kThreads, 1)
-    cols_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                const __grid_constant__ CUtensorMap tmG, __nv_bfloat16* __restrict__ Y,
-                ColsLaunch a) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = align1024(smem_raw);
-    const int MP = a.MP, S = a.stages;
-    const ColsLayout L = cols_layout(MP, S, a.cluster ? a.splits - 1 : 0);
-    const uint32_t sb = smem_u32(smem);
-    const uint32_t sw = sb + L.off_w, sx = sb + L.off_x, sg = sb + L.off_g;
-    const uint32_t xbytes = MP * kBK * 2;
-    constexpr uint32_t wbytes = kColsBN * kBK * 2;
-    const uint32_t bar0 = sb + L.off_bar;
-    auto full = [&](uint32_t s) { return bar0 + 8 * s; };
-    auto xform = [&](uint32_t s) { return bar0 + 8 * (kColsMaxStages + s); };
-    auto empty = [&](uint32_t s) { return bar0 + 8 * (2 * kColsMaxStages + s); };
-    auto accfull = [&](uint32_t b) { return bar0 + 8 * (3 * kColsMaxStages + b); };
-    auto accempty = [&](uint32_t b) { return bar0 + 8 * (3 * kColsMaxStages + 2 + b); };
-    auto srfull = [&](uint32_t b) { return bar0 + 8 * (3 * kColsMaxStages + 4 + b); };
-    const uint32_t mmadone = bar0 + 8 * (3 * kColsMaxStages + 6);
-    const uint32_t episync = bar0 + 8 * (3 * kColsMaxStages + 7);
-    // split 0: the other splits' partials have arrived; other splits: split 0
-    // has consumed the previous partial this CTA pushed
-    const uint32_t redfull = bar0 + 8 * (3 * kColsMaxStages + 8);
-    const uint32_t redempty = bar0 + 8 * (3 * kColsMaxStages + 9);
-    const uint32_t red_addr = sb + L.off_red, redss_addr = sb + L.off_redss;
-    const float* red = reinterpret_cast<const float*>(smem + L.off_red);      // [splits-1][MP][128]
-    const float* redss = reinterpret_cast<const float*>(smem + L.off_redss);  // [splits-1][128]
-    float* ss_s = reinterpret_cast<float*>(smem + L.off_ss);    // [2][128]
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.off_misc);
-    volatile int* abort = reinterpret_cast<volatile int*>(smem + L.off_misc + 4);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(full(s), 1);
-            mbar_init(xform(s), 4);   // one elected lane per transform warp
-            mbar_init(empty(s), 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(accfull(b), 1);
-            mbar_init(accempty(b), 4);  // one elected lane per epilogue warp
-            mbar_init(srfull(b), 4);    // one elected lane per transform warp
-        }
-        mbar_init(mmadone, 1);
-        mbar_init(episync, 4);
-        mbar_init(redfull, a.splits > 1 ? (a.splits - 1) * 128 : 1);
-        mbar_init(redempty, 1);
-        abort[0] = 0;
-        abort[1] = a.wait_limit_us;
-        fence_mbar_init();
-    }
-    if (warp == 0 && lane == 0) {
-        prefetch_tmap(&tmX);
-        prefetch_tmap(&tmW);
-        if (kFused) prefetch_tmap(&tmG);
-    }
-    if (warp == 2) {
-        tmem_alloc(smem_u32(tmem_holder), a.tmem_cols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    // peers' barriers must be initialised before the first remote arrive
-    if (a.cluster) cluster_sync_all();
-    // Set-up above overlaps the previous kernel on the stream; its writes are
-    // visible after grid_dep_wait().  The next kernel may then be scheduled.
-    grid_dep_wait();
-    if (threadIdx.x == 0) grid_dep_launch();
-    const uint32_t tmem = *tmem_holder;
-    // With a cluster, the cluster's CTAs are the K splits of one column tile:
-    // blockIdx.x = cluster * splits + rank, and the unit walk below keeps them
-    // on the same tile.
-    const int units = a.n_tiles * a.splits;
-
-    if (warp == 0) {
-        // ------------------------------------------------ TMA producer
-        if (lane == 0) {
-            const uint64_t pol_w = policy_evict_first();   // W is read exactly once
-            const uint64_t pol_x = policy_evict_last();    // X is re-read by every column tile
-            uint32_t it = 0;
-            Ring ring(S);
-            bool ok = true;
-            for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-                const int nt = u / a.splits, sp = u - nt * a.splits;
-                const int kb0 = sp * a.kb_per_split, kb1 = min(a.k_blocks, kb0 + a.kb_per_split);
-                const int n0 = nt * kColsBN;
-                const int nbox = min(2, (a.N - n0 + 63) / 64);
-                const uint32_t bytes = nbox * kWBoxBytes + xbytes + (kFused ? kGBytes : 0);
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    const uint32_t s = ring.idx, ph = ring.phase;
-                    if (!mbar_wait(empty(s), ph ^ 1, abort)) { ok = false; break; }
-                    mbar_arrive_expect_tx(full(s), bytes);
-                    for (int j = 0; j < nbox; ++j)
-                        tma_load_2d(sw + s * wbytes + j * kWBoxBytes, &tmW, full(s), n0 + 64 * j,
-                                    kb * kBK, pol_w);
-                    tma_load_2d(sx + s * xbytes, &tmX, full(s), kb * kBK, 0, pol_x);
-                    if (kFused) tma_load_1d(sg + s * kGBytes, &tmG, full(s), kb * kBK);
-                    ++it;
-                    ring.advance();
-                }
-            }
-            const uint32_t pending = it < static_cast<uint32_t>(S) ? it : S;
-            for (uint32_t i = it - pending; i < it; ++i) mbar_wait_teardown(full(i % S), (i / S) & 1);
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(kColsBN, MP, true, false);
-            uint32_t it = 0, tl = 0;
-            Ring ring(S);
-            bool ok = true;
-            for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++tl) {
-                const int nt = u / a.splits, sp = u - nt * a.splits;
-                const int kb0 = sp * a.kb_per_split, kb1 = min(a.k_blocks, kb0 + a.kb_per_split);
-                const uint32_t buf = tl & 1, use = tl >> 1;
-                if (!mbar_wait(accempty(buf), (use & 1) ^ 1, abort)) break;
-                tc_fence_after();
-                const uint32_t d = tmem + buf * MP;
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    const uint32_t s = ring.idx, ph = ring.phase;
-                    if (!mbar_wait(kFused ? xform(s) : full(s), ph, abort)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t a0 = sw + s * wbytes, b0 = sx + s * xbytes;
-#pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        mma_bf16_ss(d, sdesc_sw128(a0 + kk * 2048, kWBoxBytes, 1024),
-                                    sdesc_sw128(b0 + kk * 32, 16, 1024), idesc,
-                                    (kb != kb0 || kk != 0));
-                    mma_commit(empty(s));
-                    ++it;
-                    ring.advance();
-                }
-                if (!ok) break;
-                mma_commit(accfull(buf));
-            }
-            mma_commit(mmadone);
-            mbar_wait_teardown(mmadone, 0);
-        }
-    } else if (warp >= 4 && warp < 8) {
-        // ------------------------------------------------ transform: X*g, sum of squares
-        if (kFused) {
-            const int t = threadIdx.x - 128;
-            const int kc = t & 7;         // 16-byte chunk of the 128-byte row
-            const int rb = t >> 3;        // rows rb, rb + 16, rb + 32, ...
-            const int groups = MP / 16;
-            const uint32_t swz_off = static_cast<uint32_t>((kc ^ (rb & 7)) << 4);
-            uint32_t it = 0, tl = 0;
-            Ring ring(S);
-            bool ok = true;
-            for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++tl) {
-                const int nt = u / a.splits, sp = u - nt * a.splits;
-                const int kb0 = sp * a.kb_per_split, kb1 = min(a.k_blocks, kb0 + a.kb_per_split);
-                const uint32_t buf = tl & 1, use = tl >> 1;
-                if (!warp_wait(accempty(buf), (use & 1) ^ 1, abort)) break;
-                float ss[kColsMaxMP / 16];
-#pragma unroll
-                for (int i = 0; i < kColsMaxMP / 16; ++i) ss[i] = 0.f;
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    const uint32_t s = ring.idx, ph = ring.phase;
-                    if (!warp_wait(full(s), ph, abort)) { ok = false; break; }
-                    const uint4 gv = lds128(sg + s * kGBytes + kc * 16);
-                    const uint32_t xt = sx + s * xbytes;
-                    // all loads first, then the stores (see the row-tile path);
-                    // row = rb + 16 i has the same (row & 7) as rb
-                    uint4 xv[kColsMaxMP / 16];
-#pragma unroll
-                    for (int i = 0; i < kColsMaxMP / 16; ++i)
-                        if (i < groups) xv[i] = lds128(xt + (rb + 16 * i) * 128 + swz_off);
-#pragma unroll
-                    for (int i = 0; i < kColsMaxMP / 16; ++i)
-                        if (i < groups) sts128(xt + (rb + 16 * i) * 128 + swz_off, gain8(xv[i], gv, ss[i]));
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(xform(s));
-                    ++it;
-                    ring.advance();
-                }
-                if (!ok) break;
-#pragma unroll
-                for (int i = 0; i < kColsMaxMP / 16; ++i) {
-                    float v = ss[i];
-                    v += __shfl_xor_sync(0xffffffffu, v, 1);
-                    v += __shfl_xor_sync(0xffffffffu, v, 2);
-                    v += __shfl_xor_sync(0xffffffffu, v, 4);
-                    if (i < groups && kc == 0) ss_s[buf * kColsMaxMP + rb + 16 * i] = v;
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(srfull(buf));
-            }
-        }
-    } else if (warp >= 8) {
-        // ------------------------------------------------ epilogue
-        const int e = threadIdx.x - 256;     // == tensor-memory lane == column within the tile
-        const int q = warp & 3;
-        // bounded barrier over the 4 epilogue warps (an mbarrier, so that a
-        // timeout elsewhere cannot leave a warp waiting forever)
-        uint32_t ep = 0;
-        auto epi_sync = [&]() {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(episync);
-            return warp_wait(episync, (ep++) & 1, abort);
-        };
-        const uint32_t rank = a.cluster ? cluster_ctarank() : 0;
-        uint32_t red_use = 0;
-        uint32_t tl = 0;
-        for (int u = blockIdx.x; u < units; u += gridDim.x, ++tl) {
-            const int nt = u / a.splits, sp = u - nt * a.splits;
-            const uint32_t buf = tl & 1, use = tl >> 1;
-            if (!warp_wait(accfull(buf), use & 1, abort)) break;
-            if (kFused && !warp_wait(srfull(buf), use & 1, abort)) break;
-            tc_fence_after();
-            const int n = nt * kColsBN + e;
-            const bool n_ok = n < a.N;
-            const uint32_t taddr = tmem + buf * MP + (static_cast<uint32_t>(q * 32) << 16);
-            const int jmax = (a.M + 15) / 16;   // column groups that hold real rows
-            if (a.splits == 1) {
-                for (int j = 0; j < jmax; ++j) {
-                    uint32_t v[16];
-                    tmem_ld_32x16(taddr + j * 16, v);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int m = j * 16 + i;
-                        if (m < a.M && n_ok) {
-                            float r = 1.f;
-                            if (kFused)
-                                r = rsqrtf(ss_s[buf * kColsMaxMP + m] / static_cast<float>(a.K) +
-                                           a.eps);
-                            Y[static_cast<size_t>(m) * a.N + n] =
-                                __float2bfloat16_rn(__uint_as_float(v[i]) * r);
-                        }
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(accempty(buf));
-            } else if (a.cluster) {
-                // Splits 1.. store their partial tile and row sums of squares
-                // straight into split 0's shared memory (one-way remote stores,
-                // then a release arrive); split 0 adds them in split order to
-                // its own partial, still in tensor memory, and writes Y.
-                if (rank != 0) {
-                    if (!warp_wait_cluster(redempty, (red_use & 1) ^ 1, abort)) break;
-                    const uint32_t dst =
-                        mapa_shared(red_addr + ((rank - 1) * MP * kColsBN + e) * 4, 0);
-                    for (int j = 0; j < jmax; ++j) {
-                        uint32_t v[16];
-                        tmem_ld_32x16(taddr + j * 16, v);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int m = j * 16 + i;
-                            if (m < a.M) st_dsmem_f32(dst + m * kColsBN * 4, __uint_as_float(v[i]));
-                        }
-                    }
-                    if (kFused && e < a.M)
-                        st_dsmem_f32(mapa_shared(redss_addr + ((rank - 1) * kColsMaxMP + e) * 4, 0),
-                                     ss_s[buf * kColsMaxMP + e]);
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(accempty(buf));
-                    mbar_arrive_remote(mapa_shared(redfull, 0));
-                } else {
-                    if (!warp_wait_cluster(redfull, red_use & 1, abort)) break;
-                    for (int j = 0; j < jmax; ++j) {
-                        uint32_t v[16];
-                        tmem_ld_32x16(taddr + j * 16, v);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int m = j * 16 + i;
-                            if (m < a.M) {
-                                float acc = __uint_as_float(v[i]);
-                                float tot = kFused ? ss_s[buf * kColsMaxMP + m] : 0.f;
-                                for (int s2 = 1; s2 < a.splits; ++s2) {
-                                    acc += red[((s2 - 1) * MP + m) * kColsBN + e];
-                                    if (kFused) tot += redss[(s2 - 1) * kColsMaxMP + m];
-                                }
-                                const float r =
-                                    kFused ? rsqrtf(tot / static_cast<float>(a.K) + a.eps) : 1.f;
-                                if (n_ok) Y[static_cast<size_t>(m) * a.N + n] = __float2bfloat16_rn(acc * r);
-                            }
-                        }
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(accempty(buf));
-                    // every thread of split 0 has read the slots: hand them back
-                    if (!epi_sync()) break;
-                    if (e == 0)
-                        for (int s2 = 1; s2 < a.splits; ++s2) mbar_arrive_remote(mapa_shared(redempty, s2));
-                }
-                ++red_use;
-            } else {
-                // Publish this split's partial sums (and its rows' partial sums
-                // of squares).  Then, per warp, the last of the splits' warps
-                // for these 32 columns adds all splits in split order (its own
-                // partial from tensor memory, which it still holds) and writes
-                // Y.  Counters are per (column tile, warp): no CTA-wide
-                // handshake follows the atomic, and the last warp issues all of
-                // its loads in one batch.
-                float* part = a.ws_acc + static_cast<size_t>(sp) * a.M * a.N;
-                for (int j = 0; j < jmax; ++j) {
-                    uint32_t v[16];
-                    tmem_ld_32x16(taddr + j * 16, v);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int m = j * 16 + i;
-                        if (m < a.M && n_ok)
-                            part[static_cast<size_t>(m) * a.N + n] = __uint_as_float(v[i]);
-                    }
-                }
-                if (kFused && e < a.M)
-                    a.ws_ss[(static_cast<size_t>(nt) * a.splits + sp) * kColsMaxMP + e] =
-                        ss_s[buf * kColsMaxMP + e];
-                __threadfence();
-                // every thread's stores are globally visible before any warp counts
-                if (!epi_sync()) break;
-                int* counter = a.counters + nt * 4 + q;
-                uint32_t last = 0;
-                if (lane == 0) last = atomicAdd(counter, 1) == a.splits - 1;
-                last = __shfl_sync(0xffffffffu, last, 0);
-                if (last) {
-                    __threadfence();
-                    float rr[kColsMaxMP / 32];
-                    for (int j = 0; j < jmax; ++j) {
-                        uint32_t v[16];
-                        tmem_ld_32x16(taddr + j * 16, v);
-                        if (j == 0) {
-                            // reciprocal RMS of rows lane, lane + 32, ... (loads
-                            // issued together with the first chunk's partials)
-#pragma unroll
-                            for (int i = 0; i < kColsMaxMP / 32; ++i) {
-                                const int m = lane + 32 * i;
-                                float tot = 0.f;
-                                if (kFused && m < a.M) {
-                                    const float* ssp =
-                                        a.ws_ss + static_cast<size_t>(nt) * a.splits * kColsMaxMP + m;
-#pragma unroll 4
-                                    for (int s2 = 0; s2 < a.splits; ++s2) tot += __ldcg(ssp + s2 * kColsMaxMP);
-                                }
-                                rr[i] = kFused ? rsqrtf(tot / static_cast<float>(a.K) + a.eps) : 1.f;
-                            }
-                        }
-                        float acc[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-#pragma unroll 4
-                        for (int s2 = 0; s2 < a.splits; ++s2) {
-                            const float* p2 = a.ws_acc + static_cast<size_t>(s2) * a.M * a.N + n;
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const int m = j * 16 + i;
-                                acc[i] += (s2 == sp) ? __uint_as_float(v[i])
-                                          : ((m < a.M && n_ok) ? __ldcg(p2 + static_cast<size_t>(m) * a.N) : 0.f);
-                            }
-                        }
-                        const int jj = j >> 1;   // rows 16j .. 16j+15 sit in rr[j / 2]
-                        const float rsel = jj == 0 ? rr[0] : jj == 1 ? rr[1] : jj == 2 ? rr[2] : rr[3];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int m = j * 16 + i;
-                            const float r = __shfl_sync(0xffffffffu, rsel, ((j & 1) << 4) + i);
-                            if (m < a.M && n_ok)
-                                Y[static_cast<size_t>(m) * a.N + n] = __float2bfloat16_rn(acc[i] * r);
-                        }
-                    }
-                    if (lane == 0) *counter = 0;
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(accempty(buf));
-            }
-        }
-        // split 0's last hand-back arrive must land before this CTA exits
-        if (a.cluster && rank != 0 && red_use > 0) warp_wait_cluster(redempty, (red_use & 1) ^ 1, abort);
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 2) {
-        tc_fence_after();
-        tmem_dealloc(tmem, a.tmem_cols);
-    }
-}
-
 // ------------------------------------------------------------ unfused RMSNorm
 constexpr int kNormThreads = 256;
 
@@ -1671,12 +1263,6 @@ bool rows_overlay_fits(int xrows, int stages, int splits, int MP, bool glu) {
     return static_cast<uint32_t>(splits) * L.red_block <= L.off_g;
 }
 size_t rows_stage_bytes(int xrows) { return xrows * kBK * 2 + kRowsWBytes + kGBytes; }
-size_t cols_smem_bytes(int MP, int stages, int red_slots) {
-    return cols_layout(MP, stages, red_slots).total;
-}
-size_t cols_fixed_smem_bytes(int MP, int red_slots) { return cols_layout(MP, 0, red_slots).total; }
-size_t cols_stage_bytes(int MP) { return kColsBN * kBK * 2 + MP * kBK * 2 + kGBytes; }
-
 // Launch with programmatic dependent launch (the kernel's set-up may overlap
 // the previous kernel on the stream) and, optionally, a 1-D cluster, or as a
 // cooperative grid (all CTAs resident at once, or the launch fails).
@@ -1757,18 +1343,6 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
     return cudaGetLastError();
 }
 
-cudaError_t launch_cols(bool fused, const CUtensorMap& tmX, const CUtensorMap& tmW,
-                        const CUtensorMap& tmG, void* Y, const ColsLaunch& a, cudaStream_t s) {
-    auto* y = static_cast<__nv_bfloat16*>(Y);
-    auto kern = fused ? cols_kernel<true> : cols_kernel<false>;
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), fused ? 2 : 3);
-    if (e != cudaSuccess) return e;
-    const size_t smem = cols_smem_bytes(a.MP, a.stages, a.cluster ? a.splits - 1 : 0);
-    e = launch_ex(kern, a.grid, smem, a.cluster ? a.splits : 1, s, false, tmX, tmW, tmG, y, a);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
-}
-
 template <typename Kern>
 int max_active_clusters(Kern kern, int slot, int splits, size_t smem) {
     if (ensure_smem_attr(reinterpret_cast<const void*>(kern), slot) != cudaSuccess) return 0;
@@ -1786,11 +1360,6 @@ int max_active_clusters(Kern kern, int slot, int splits, size_t smem) {
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
     return n;
-}
-
-int cols_max_active_clusters(bool fused, int splits, size_t smem) {
-    return fused ? max_active_clusters(cols_kernel<true>, 2, splits, smem)
-                 : max_active_clusters(cols_kernel<false>, 3, splits, smem);
 }
 
 int rows_max_active_clusters(bool fused, int splits, size_t smem, bool glu, bool wnk, bool lora) {

@@ -16,12 +16,7 @@ constexpr int kRowsBM = 128;
 constexpr int kRowsBN = 256;
 constexpr int kRowsMaxStages = 6;
 
-// Small-M path: CTA tile 128 (columns of W) x MP (rows of X, padded to 16).
-constexpr int kColsBN = 128;
-constexpr int kColsMaxMP = 128;
-constexpr int kColsMaxStages = 12;
 constexpr int kClusterMaxSplits = 8;   // portable cluster size
-constexpr int kColsMaxSplits = 16;
 
 // Row-tile path shared memory: xrows = rows of X loaded per stage (128, or
 // M rounded up to 16 for a single row tile); red_slots = K splits reduced
@@ -36,14 +31,6 @@ bool rows_overlay_fits(int xrows, int stages, int splits, int MP, bool glu = fal
 size_t rows_stage_bytes(int xrows);
 int rows_max_active_clusters(bool fused, int splits, size_t smem, bool glu = false, bool wnk = false,
                              bool lora = false);
-// red_slots = splits - 1 when the splits reduce through a cluster, else 0.
-size_t cols_smem_bytes(int MP, int stages, int red_slots);
-size_t cols_fixed_smem_bytes(int MP, int red_slots);
-size_t cols_stage_bytes(int MP);
-// Clusters of `splits` CTAs of cols_kernel that fit on the device at once
-// (0 if the configuration cannot be launched).
-int cols_max_active_clusters(bool fused, int splits, size_t smem);
-
 struct RowsLaunch {
     int M, N, K;
     float eps;
@@ -77,30 +64,37 @@ struct RowsLaunch {
     int* ws_count;             // [tail_tiles][2] arrival counters, zero between launches
 };
 
-struct ColsLaunch {
-    int M, N, K;
-    float eps;
-    int MP, n_tiles, k_blocks, splits, kb_per_split, stages, grid;
-    int cluster;      // 1: the splits of a column tile form a cluster; splits > 0
-                      // push their partials into split 0's shared memory (ws_* unused)
-    uint32_t tmem_cols;
-    float* ws_acc;    // [splits][M][N] fp32 partials (splits > 1 without a cluster)
-    float* ws_ss;     // [n_tiles][splits][128] fp32 partial sums of squares
-    int* counters;    // [n_tiles][4] arrival counters (one per epilogue warp), zero between launches
-    int wait_limit_us;   // limit of one bounded in-kernel wait
-};
-
 // tmT, tmB: the low-rank adapter's T [M, R] and B [R, N] (used with a.lora).
 cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& tmW,
                         const CUtensorMap& tmG, const CUtensorMap& tmT, const CUtensorMap& tmB, void* Y,
                         const RowsLaunch& a, cudaStream_t s);
-cudaError_t launch_cols(bool fused, const CUtensorMap& tmX, const CUtensorMap& tmW,
-                        const CUtensorMap& tmG, void* Y, const ColsLaunch& a, cudaStream_t s);
 cudaError_t launch_rmsnorm(const void* X, const void* g, void* Xn, int M, int K, float eps,
                            cudaStream_t s);
 
 // Copies the in-kernel status word to *out and clears it (synchronous).
 cudaError_t read_and_clear_status(int* out);
+
+// ------------------------------------------------ small-M path (gemv.cu)
+constexpr int kGvMaxM = 16;   // rows of X: one m16 tile of mma.sync.m16n8k16
+constexpr int kGvBN = 64;     // columns of W per unit
+constexpr int kGvBK = 16;     // k per step
+constexpr int kGvPieceFloats = kGvMaxM * kGvBN + kGvMaxM;   // one published piece: tile, then row sums
+
+struct GemvLaunch {
+    int M, N, K;
+    float eps;
+    int units;             // ceil(N / 64)
+    int ksteps;            // ceil(K / 16)
+    int splits;            // K pieces per unit, one CTA each (grid = units * splits)
+    int steps_per_piece;   // k-steps of a piece (the last may have fewer)
+    float* ws;             // [units][splits][16 * 64 + 16] fp32 partials (splits > 1)
+    int* counters;         // [units] arrival counters, zero between launches (splits > 1)
+};
+// X [M, K], g [K] (fused only), W [K, N], Y [M, N] bf16, row-major.
+cudaError_t launch_gemv(bool fused, const void* X, const void* g, const void* W, void* Y, const GemvLaunch& a,
+                        cudaStream_t s);
+// CTAs of the small-M kernel that fit on one SM.
+int gemv_ctas_per_sm(bool fused);
 
 // ------------------------------------------------ QK-normalised attention (attention.cu)
 constexpr int kAttBM = 128;   // query rows per tile

@@ -46,16 +46,16 @@ def test_status_strings(lib):
 def test_force_path_roundtrip(lib):
     assert rmm.force_path(rmm.PATH_ROWS) == rmm.PATH_AUTO
     assert rmm.dispatch_path(8, 1024, 1024) == rmm.PATH_ROWS
-    assert rmm.force_path(rmm.PATH_COLS) == rmm.PATH_ROWS
-    assert rmm.dispatch_path(4096, 4096, 4096) == rmm.PATH_COLS
-    assert rmm.force_path(rmm.PATH_AUTO) == rmm.PATH_COLS
+    assert rmm.force_path(rmm.PATH_SMALL_M) == rmm.PATH_ROWS
+    assert rmm.dispatch_path(4096, 4096, 4096) == rmm.PATH_SMALL_M
+    assert rmm.force_path(rmm.PATH_AUTO) == rmm.PATH_SMALL_M
     assert lib.rmm_force_path(7) == -1
     assert rmm.force_path(rmm.PATH_AUTO) == rmm.PATH_AUTO
 
 
-def test_default_dispatch_is_row_tile_path(lib):
-    # The row-tile path serves every shape unless a path is forced.
-    for M in (1, 16, 64, 65, 128, 4096):
+def test_default_dispatch(lib):
+    # the row-tile kernels serve every shape unless a path is forced
+    for M in (1, 8, 16, 17, 64, 65, 128, 4096):
         assert rmm.dispatch_path(M, 4096, 6144) == rmm.PATH_ROWS
 
 

@@ -14,6 +14,7 @@ pytestmark = pytest.mark.gpu
 
 ATOL = 1e-2
 RTOL = 1e-2
+SMALL_M = 16   # rows the small-M path (path 2) takes
 
 
 @pytest.fixture(scope="module")
@@ -62,6 +63,8 @@ LARGE_WORKLOADS = ["prefill_qkv_4096x4096x6144", "large_prefill_16384x8192x8192"
 def test_workload_all_rows(rmm, forced, name, path):
     from sm_rmsnorm_matmul_gb300 import inputs
     w = inputs.WORKLOADS[name]
+    if path == 2 and w.M > SMALL_M:
+        pytest.skip("the small-M path holds at most 16 rows")
     X, g, W = inputs.generate_workload(w)
     forced(path)
     Y = run_fused(rmm, X, g, W, w.eps)
@@ -87,8 +90,10 @@ def test_workload_sampled_rows(rmm, name):
 RAGGED = [
     (1, 64, 8), (7, 72, 136), (16, 1024, 1000), (33, 520, 264), (64, 4096, 1032),
     (65, 256, 256), (129, 1032, 520), (255, 328, 392), (300, 2048, 2056),
-    # few column tiles and long K: more than 8 K splits (global-workspace reduction)
+    # few column tiles and long K: many K pieces (small-M path) or splits
     (16, 16384, 128), (48, 8192, 264),
+    # small-M path: one partial k-step, a k-step half past K, one row, ragged units
+    (3, 8, 8), (12, 4104, 72), (1, 2056, 6152), (9, 520, 4096),
 ]
 
 
@@ -96,13 +101,15 @@ RAGGED = [
 @pytest.mark.parametrize("path", [1, 2])
 def test_ragged(rmm, forced, M, K, N, path):
     from sm_rmsnorm_matmul_gb300 import inputs
-    if path == 2 and M > 128:
-        pytest.skip("small-M path holds at most 128 rows")
+    if path == 2 and M > SMALL_M:
+        pytest.skip("the small-M path holds at most 16 rows")
     X, g, W = inputs.random_problem(M, K, N, seed=M * 7 + K + N, x_kind="row_scaled")
     forced(path)
     Y = run_fused(rmm, X, g, W, 1e-5)
     ref = oracle.rmsnorm_matmul(X, g, W, 1e-5)
     assert_close(Y, ref, f"{M}x{K}x{N} path {path}")
+    # the K pieces are added in a fixed order: a second call gives the same bits
+    assert torch.equal(Y, run_fused(rmm, X, g, W, 1e-5))
 
 
 # Several row tiles whose last wave of CTAs would be at most half full: those
@@ -269,15 +276,20 @@ def test_lora(rmm, M, K, N, R):
     err = np.abs(oracle.to_f64(Y2.cpu()[rows]) - emu)
     bad = ~(err <= 2.0 ** -8 * np.abs(emu) + 1e-4)   # NaN fails
     assert not bad.any(), f"lora {M}x{K}x{N} R={R}: {int(bad.sum())} beyond the rounding of X*g (max {err.max():.3e})"
-    # a zero adapter gives the plain result
+    # a zero adapter gives the plain row-tile kernel's result, bit for bit
     Y0 = rmm.rmsnorm_matmul_lora(Xd, gd, Wd, torch.zeros_like(A).cuda(), B.cuda(), 1e-5)
+    prev = rmm.force_path(rmm.PATH_ROWS)
+    try:
+        Yp = rmm.rmsnorm_matmul(Xd, gd, Wd, 1e-5)
+    finally:
+        rmm.force_path(prev)
     torch.cuda.synchronize()
-    assert torch.equal(Y0, rmm.rmsnorm_matmul(Xd, gd, Wd, 1e-5))
+    assert torch.equal(Y0, Yp)
 
 
 def test_small_m_rejects_large_m_when_forced(rmm, forced):
     forced(2)
-    X = torch.zeros(129, 64, dtype=torch.bfloat16, device="cuda")
+    X = torch.zeros(SMALL_M + 1, 64, dtype=torch.bfloat16, device="cuda")
     g = torch.ones(64, dtype=torch.bfloat16, device="cuda")
     W = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(rmm.RmmError):
@@ -319,7 +331,7 @@ def test_scale_invariance_on_gpu(rmm):
     # statistic's ratio unchanged; with eps = 0 the outputs stay in tolerance
     # of each other and of the oracle.
     from sm_rmsnorm_matmul_gb300 import inputs
-    X, g, W = inputs.random_problem(64, 2048, 1024, seed=8)
+    X, g, W = inputs.random_problem(16, 2048, 1024, seed=8)
     for path in (1, 2):
         prev = rmm.force_path(path)
         try:
@@ -349,12 +361,12 @@ def test_unfused_rmsnorm(rmm, M, K):
     assert_close(Xn.cpu(), oracle.rmsnorm(X, g, 1e-6), f"rmsnorm {M}x{K}")
 
 
-@pytest.mark.parametrize("M,K,N", [(16, 4096, 6144), (100, 520, 264), (512, 1024, 2048)])
+@pytest.mark.parametrize("M,K,N", [(16, 4096, 6144), (5, 1032, 1000), (100, 520, 264), (512, 1024, 2048)])
 @pytest.mark.parametrize("path", [0, 1, 2])
 def test_unfused_matmul(rmm, forced, M, K, N, path):
     from sm_rmsnorm_matmul_gb300 import inputs
-    if path == 2 and M > 128:
-        pytest.skip("small-M path holds at most 128 rows")
+    if path == 2 and M > SMALL_M:
+        pytest.skip("the small-M path holds at most 16 rows")
     A, _, B = inputs.random_problem(M, K, N, seed=M * 3 + N)
     forced(path)
     C = rmm.matmul(A.cuda(), B.cuda())

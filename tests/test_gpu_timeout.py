@@ -27,22 +27,27 @@ def rmm():
 
 
 def test_timeout_is_reported_and_the_context_recovers(rmm):
+    # the row-tile kernel's cluster K split (the small-M path has no waits)
     from sm_rmsnorm_matmul_gb300 import inputs
     M, K, N = 16, 4096, 6144
-    plan = rmm.describe_plan(M, K, N)
-    assert plan["splits"] > 1 and plan["cluster"] == 1   # the K-split reduction runs
-    X, g, W = (t.cuda() for t in inputs.random_problem(M, K, N, seed=31))
+    prev = rmm.force_path(rmm.PATH_ROWS)
     l = rmm.lib()
-    assert rmm.device_status() == 0
-    assert l.rmm_test_hooks(1, 50_000_000) == 0          # skip the sends; 50 ms per wait
     try:
-        rmm.rmsnorm_matmul(X, g, W, 1e-6)
-        assert rmm.device_status() == 5                  # RMM_ERR_DEVICE_TIMEOUT
+        plan = rmm.describe_plan(M, K, N)
+        assert plan["splits"] > 1 and plan["cluster"] == 1   # the K-split reduction runs
+        X, g, W = (t.cuda() for t in inputs.random_problem(M, K, N, seed=31))
+        assert rmm.device_status() == 0
+        assert l.rmm_test_hooks(1, 50_000_000) == 0          # skip the sends; 50 ms per wait
+        try:
+            rmm.rmsnorm_matmul(X, g, W, 1e-6)
+            assert rmm.device_status() == 5                  # RMM_ERR_DEVICE_TIMEOUT
+        finally:
+            assert l.rmm_test_hooks(0, 0) == 0               # normal operation, 2 s limit
+        Y = rmm.rmsnorm_matmul(X, g, W, 1e-6)
+        torch.cuda.synchronize()
+        assert rmm.device_status() == 0
     finally:
-        assert l.rmm_test_hooks(0, 0) == 0               # normal operation, 2 s limit
-    Y = rmm.rmsnorm_matmul(X, g, W, 1e-6)
-    torch.cuda.synchronize()
-    assert rmm.device_status() == 0
+        rmm.force_path(prev)
     bad, max_abs, _ = oracle.tolerance_violations(Y.cpu(), oracle.rmsnorm_matmul(X.cpu(), g.cpu(), W.cpu(), 1e-6))
     assert bad == 0, max_abs
 

@@ -65,16 +65,16 @@ def _uses_scratch(plan):
 
 # (name or (M, K, N), forced path, whether the plan puts partials in the array)
 CASES = [
-    ("tiny_8x1024x1024", 0, False),
+    ("tiny_8x1024x1024", 0, False),                # row-tile kernel, K split inside a cluster
     ("decode_qkv_16x4096x6144", 0, False),
-    ("decode_gatedmlp_64x4096x28672", 0, False),
+    ("decode_gatedmlp_64x4096x28672", 0, False),   # row-tile kernel, whole tiles
     ("prefill_qkv_4096x4096x6144", 0, True),      # 8 tail tiles cut into 16 K pieces
-    ((1280, 1024, 4096), 0, True),                 # 8 tail tiles, ragged nothing
+    ((1280, 1024, 4096), 0, True),                 # 8 tail tiles
     ((1200, 1000, 4104), 0, True),                 # 18 tail tiles, partial row, column and K blocks
-    ("tiny_8x1024x1024", 2, None),
-    ("decode_qkv_16x4096x6144", 2, None),
-    ((16, 16384, 128), 2, True),                   # more than 8 K splits: global split
-    ((48, 8192, 264), 2, True),
+    ("tiny_8x1024x1024", 2, True),                 # small-M path, K cut into pieces
+    ("decode_qkv_16x4096x6144", 2, True),
+    ((16, 16384, 128), 2, True),                   # long K: many pieces per unit
+    ((12, 8192, 264), 2, True),                    # ragged last unit
 ]
 
 
@@ -139,13 +139,13 @@ def test_noalloc_back_to_back_different_inputs(lib):
 
 
 def test_noalloc_rejects_plans_beyond_its_scratch(lib):
-    # Forced small-M path with a global K split whose fp32 partials exceed the
-    # array: refused before any launch, and the output is left untouched.
+    # A small-M launch whose K pieces (16 x 64 fp32 and 16 row sums per piece)
+    # exceed the array: refused before any launch, the output left untouched.
     prev = lib.rmm_force_path(2)
     try:
-        for M, K, N in [(128, 16384, 14336), (128, 16384, 12288), (128, 8192, 12288)]:
+        for M, K, N in [(16, 2048, 65536), (16, 4096, 65536), (16, 2048, 131072)]:
             p = _plan(lib, M, K, N)
-            need = p["splits"] * (M * N + p["tiles"] * 128) * 4
+            need = p["splits"] * p["tiles"] * (16 * 64 + 16) * 4
             if _uses_scratch(p) and need > AREA_BYTES:
                 break
         else:
