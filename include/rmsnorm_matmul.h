@@ -67,13 +67,16 @@ typedef enum {
  *   W  [K,N] bf16 weights (N contiguous) Y [M,N] bf16 output (written)
  *   eps added to the mean square inside the square root.
  * Shape-based dispatch between two kernels:
- *  - M <= 16: the small-M path, a split-K GEMV-style kernel: W streamed with
- *    128-bit loads straight into mma.sync fragments, X*g and the row sums of
- *    squares formed on the fly, 64-column units whose K range may be cut into
- *    pieces; the pieces meet in a library-owned fp32 workspace per (device,
- *    stream) and the last CTA of a unit adds them in a fixed order (no CTA
- *    waits for another).
- *  - M > 16: the tcgen05 row-tile kernels: 128-row x 256-column tiles, X*g
+ *  - M <= 16 and a W that the row-tile kernel, whose 256-column tiles take
+ *    at most 8 K splits, would stream more slowly (a long K over a narrow N:
+ *    a model of both kernels' streaming rates decides): the small-M path, a
+ *    split-K GEMV-style kernel: W, X and g streamed by TMA through a
+ *    shared-memory ring into mma.sync, X*g and the row sums of squares formed
+ *    on the fly, 64-column units whose K range may be cut into pieces; the
+ *    pieces meet in a library-owned fp32 workspace per (device, stream) and
+ *    the last CTA of a unit adds them in a fixed order (no CTA waits for
+ *    another).
+ *  - otherwise: the tcgen05 row-tile kernels: 128-row x 256-column tiles, X*g
  *    and the row sum of squares computed in the same pass as the contraction,
  *    r[m] applied in the epilogue.  For M <= 128 the K range may be split over
  *    up to 8 CTAs of a thread-block cluster whose partial sums are combined in
@@ -259,8 +262,10 @@ int rmsnorm_matmul_noalloc(const void* X, const void* g, const void* W, void* Y,
  */
 int rmm_describe_plan(int64_t M, int64_t K, int64_t N, int fused, int* info);
 
-/* Which path the dispatcher would take for this shape right now:
- * 1 = row-tile path, 2 = small-M path.  Host-only; no CUDA call. */
+/* Which path the dispatcher would take for this shape right now on the
+ * current device (a 152-SM GB300 if there is none): 1 = row-tile path,
+ * 2 = small-M path; RMM_ERR_INVALID_ARG for a size < 1.  Queries device
+ * attributes; launches nothing. */
 int rmm_dispatch_path(int64_t M, int64_t K, int64_t N);
 
 #ifdef __cplusplus

@@ -296,9 +296,9 @@ int get_khat_buffer(int dev, cudaStream_t s, size_t bytes, void** out) {
 
 // ---------------------------------------------------------------- planning
 // Small-M path (gemv.cu): units of 64 columns, K cut into `splits` pieces of
-// steps_per_piece 16-deep k-steps, one CTA per piece.
+// stages_per_piece 128-deep stages, one CTA per piece.
 struct GemvPlan {
-    int units, ksteps, splits, steps_per_piece;
+    int units, kstages, splits, stages_per_piece;
 };
 
 std::mutex g_gv_mu;
@@ -315,28 +315,26 @@ int gemv_slots_per_sm(int dev, bool fused) {
 }
 
 // K split of the small-M path: the pieces of one launch run as waves of
-// (SMs x CTAs per SM); a piece of P k-steps costs its CTA time in proportion
-// to P (its 8 warps take ceil(P / 8) rounds of loads), and a split adds the
-// publication of the pieces and the last CTA's sum over them, about 8 k-steps
-// plus 4 per batch of 8 pieces (fitted on GB300).  Pieces keep at least one
-// k-step per warp.
+// (SMs x CTAs per SM); a piece of P stages costs its CTA time in proportion
+// to P, and a split adds the publication of the pieces and the last CTA's sum
+// over them, about two stages' time plus one per batch of 8 pieces.
 GemvPlan plan_gemv(int dev, bool fused, int64_t K, int64_t N, const DeviceInfo& d) {
     GemvPlan p{};
     p.units = static_cast<int>((N + rmm::kGvBN - 1) / rmm::kGvBN);
-    p.ksteps = static_cast<int>((K + rmm::kGvBK - 1) / rmm::kGvBK);
+    p.kstages = static_cast<int>((K + rmm::kGvStageK - 1) / rmm::kGvStageK);
     const long slots = static_cast<long>(d.sm_count > 0 ? d.sm_count : 1) * gemv_slots_per_sm(dev, fused);
     p.splits = 1;
-    p.steps_per_piece = p.ksteps;
+    p.stages_per_piece = p.kstages;
     long best = -1;
-    for (int s = 1; s <= 32 && s * 8 <= std::max(8, p.ksteps); ++s) {
-        const int spp = (p.ksteps + s - 1) / s;
-        if ((p.ksteps + spp - 1) / spp != s) continue;
+    for (int s = 1; s <= 32 && s <= p.kstages; ++s) {
+        const int spp = (p.kstages + s - 1) / s;
+        if ((p.kstages + spp - 1) / spp != s) continue;
         const long waves = (static_cast<long>(p.units) * s + slots - 1) / slots;
-        const long cost = waves * spp + (s > 1 ? 8 + 4 * ((s + 7) / 8) : 0);
+        const long cost = 4 * waves * spp + (s > 1 ? 8 + 4 * ((s + 7) / 8) : 0);   // quarter stages
         if (best < 0 || cost < best) {
             best = cost;
             p.splits = s;
-            p.steps_per_piece = spp;
+            p.stages_per_piece = spp;
         }
     }
     return p;
@@ -478,15 +476,27 @@ TailPlan plan_tail(const RowsPlan& p, const DeviceInfo& d) {
     return t;
 }
 
-// Shape-based dispatch.  The small-M path as built streams W at 3.4-4.3 TB/s
-// against ~6.3 TB/s for the row-tile kernels' TMA rings (decode QKV 14.9 vs
-// 11.9 us, tiny 5.5 vs 5.2 us on GB300), so every shape takes the row-tile
-// kernels unless path 2 is forced.
-int choose_path(int64_t M) {
-    (void)M;
+// Shape-based dispatch.  Up to 16 rows of X both kernels stream W; the
+// row-tile kernel runs one CTA per (256-column tile, K split) with at most 8
+// splits (a portable cluster), each CTA streaming about 55 GB/s, while the
+// small-M kernel's 64-column units and unbounded K pieces reach the HBM rate
+// (~6 TB/s) at a fixed cost about 1.5 us higher.  The model that picks the
+// faster, fitted to eleven shapes timed on GB300 (cold L2, back-to-back calls;
+// every one on the side it predicts): small-M for 16 x 8192 x 1024 (9.7 vs
+// 12.4 us), 16 x 14336 x 2048 (14.4 vs 17.8), 4 x 2048 x 512 (5.5 vs 6.4);
+// row-tile for 16 x 2048 x 2048 (6.7 vs 7.4), decode QKV 16 x 4096 x 6144
+// (11.9 vs 12.5), 16 x 4096 x 28672 (37 vs 49).
+int choose_path(int64_t M, int64_t K, int64_t N, int sms) {
     const int f = g_force_path.load();
     if (f == kPathRows || f == kPathSmallM) return f;
-    return kPathRows;
+    if (M > rmm::kGvMaxM) return kPathRows;
+    const double wbytes = 2.0 * static_cast<double>(K) * static_cast<double>(N);
+    const int64_t tiles = (N + rmm::kRowsBN - 1) / rmm::kRowsBN;
+    const int64_t ctas = std::min<int64_t>(std::max(1, sms),
+                                           tiles * std::min<int64_t>(rmm::kClusterMaxSplits, (K + kBK - 1) / kBK));
+    const double rows_us = wbytes / (static_cast<double>(ctas) * 55e9) * 1e6;
+    const double small_us = wbytes / 6e12 * 1e6 + 1.5;
+    return small_us < rows_us ? kPathSmallM : kPathRows;
 }
 
 // Device memory for K-split partials that the caller provides instead of the
@@ -531,19 +541,24 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
     DeviceInfo d;
     int rc = current_device(&dev, &d);
     if (rc != RMM_OK) return rc;
-    const int path = glu || wnk || lora || unscaled ? static_cast<int>(kPathRows) : choose_path(M);
+    const int path = glu || wnk || lora || unscaled ? static_cast<int>(kPathRows) : choose_path(M, K, N, d.sm_count);
     if (path == kPathSmallM) {
         if (M > rmm::kGvMaxM) return RMM_ERR_INVALID_ARG;
         const GemvPlan p = plan_gemv(dev, fused, K, N, d);
+        CUtensorMap tmX, tmW, tmG;
+        if (!map_2d(&tmX, X, M, K, rmm::kGvMaxM) || !map_2d(&tmW, W, K, N, kBK)) return RMM_ERR_INTERNAL;
+        if (fused ? !map_1d(&tmG, g, K) : false) return RMM_ERR_INTERNAL;
+        if (!fused) tmG = tmX;   // unused by the kernel
         rmm::GemvLaunch a{};
         a.M = static_cast<int>(M);
         a.N = static_cast<int>(N);
         a.K = static_cast<int>(K);
         a.eps = eps;
         a.units = p.units;
-        a.ksteps = p.ksteps;
+        a.kstages = p.kstages;
         a.splits = p.splits;
-        a.steps_per_piece = p.steps_per_piece;
+        a.stages_per_piece = p.stages_per_piece;
+        a.wait_limit_us = g_wait_limit_us.load();
         if (p.splits > 1) {
             const size_t ws_bytes = static_cast<size_t>(p.units) * p.splits * rmm::kGvPieceFloats * sizeof(float);
             const size_t ncount = static_cast<size_t>(p.units);
@@ -562,7 +577,7 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
                 a.counters = w.counters;
             }
         }
-        return rmm::launch_gemv(fused, X, g, W, Y, a, stream) == cudaSuccess ? RMM_OK : RMM_ERR_LAUNCH;
+        return rmm::launch_gemv(fused, tmX, tmW, tmG, Y, a, stream) == cudaSuccess ? RMM_OK : RMM_ERR_LAUNCH;
     }
     CUtensorMap tmX, tmW, tmG;
     // [K, N]: boxes of [64 k][64 n]; [N, K]: boxes of [256 n][64 k], or 128 rows
@@ -754,17 +769,17 @@ int rmm_describe_plan(int64_t M, int64_t K, int64_t N, int fused, int* info) {
     int rc = current_device(&dev, &d);
     if (rc != RMM_OK) return rc;
     for (int i = 0; i < 8; ++i) info[i] = 0;
-    info[0] = glu ? static_cast<int>(kPathRows) : choose_path(M);
+    info[0] = glu ? static_cast<int>(kPathRows) : choose_path(M, K, N, d.sm_count);
     if (info[0] == kPathSmallM) {
         if (M > rmm::kGvMaxM) return RMM_ERR_INVALID_ARG;
         const GemvPlan p = plan_gemv(dev, fused != 0, K, N, d);
         info[1] = p.splits;
         info[2] = 0;
         info[3] = p.units * p.splits;
-        info[4] = 0;
+        info[4] = 5;   // pipeline stages of 128 k
         info[5] = rmm::kGvMaxM;
         info[6] = p.units;
-        info[7] = p.steps_per_piece;
+        info[7] = p.stages_per_piece * (rmm::kGvStageK / kBK);   // k-blocks of 64 per piece
     } else {
         const RowsPlan p = plan_rows(dev, fused != 0, M, K, N, d, glu);
         info[1] = p.splits;
@@ -788,17 +803,22 @@ int rmm_describe_plan(int64_t M, int64_t K, int64_t N, int fused, int* info) {
 }
 
 int rmm_dispatch_path(int64_t M, int64_t K, int64_t N) {
-    (void)K;
-    (void)N;
-    return choose_path(M);
+    if (M < 1 || K < 1 || N < 1) return RMM_ERR_INVALID_ARG;
+    int dev = 0;
+    DeviceInfo d;
+    // without a usable device, the dispatch of a 152-SM GB300
+    const int sms = current_device(&dev, &d) == RMM_OK ? d.sm_count : 152;
+    return choose_path(M, K, N, sms);
 }
 
 int rmm_device_status(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return RMM_ERR_LAUNCH;
-    int v = 0, va = 0;
+    int v = 0, va = 0, vg = 0;
     if (rmm::read_and_clear_status(&v) != cudaSuccess) return RMM_ERR_LAUNCH;
     if (rmm::attn_read_and_clear_status(&va) != cudaSuccess) return RMM_ERR_LAUNCH;
+    if (rmm::gemv_read_and_clear_status(&vg) != cudaSuccess) return RMM_ERR_LAUNCH;
     if (v == RMM_OK) v = va;
+    if (v == RMM_OK) v = vg;
     if (v != RMM_OK && clear_workspace_counters() != cudaSuccess) return RMM_ERR_LAUNCH;
     return v;
 }

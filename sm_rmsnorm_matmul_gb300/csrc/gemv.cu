@@ -7,71 +7,87 @@
 // X*g is formed on the fly, never written to memory.
 //
 // With 16 rows or fewer the work is W bytes, not FLOPs: every element of W is
-// read once and used for at most 16 multiply-adds.  So the kernel has no
-// set-up to speak of (no tensor-memory allocation, no cluster, no barrier
-// ring, no tensor maps): each thread streams W with 128-bit loads straight
-// into the B fragments of mma.sync.m16n8k16 (bf16 x bf16 -> fp32), whose
-// throughput is far above what the HBM stream needs at this size.
+// read once and used for at most 16 multiply-adds.  So the kernel keeps its
+// set-up small (no tensor-memory allocation, no cluster): one producer thread
+// streams W, X and g through a ring of shared-memory stages with TMA (128-byte
+// swizzle, mbarrier-tracked, five stages of 20 KB in flight per CTA, two CTAs
+// per SM), and eight consumer warps feed mma.sync.m16n8k16 (bf16 x bf16 ->
+// fp32) from it with ldmatrix; the tensor-core rate needed at this size is a
+// small fraction of what mma.sync gives.
 //
-// Index mapping.  A warp step covers 16 k x 64 n of W.  Thread (gi = lane/4,
-// q = lane%4) loads 16 bytes (8 consecutive columns n0 + 8 gi .. + 7) from
-// each of the rows k0 + 2q, +1, +8, +9: one warp-wide load touches four whole
-// 128-byte row segments.  Byte permutes pair rows (k, k+1) per column, which
-// is the B fragment of column gi for MMA i when MMA i's column j stands for
-// W column n0 + 8 j + i.  The accumulator fragment of MMA i then holds, for
-// thread (gi, q), Y columns n0 + 16 q + {0, 8} + i: over the 8 MMAs, two runs
-// of 8 consecutive columns per row, stored with 16-byte stores.  The A
-// fragment is bf16(X*g) (the exact product rounded once, as in the row-tile
-// kernels) built from 32-bit loads of X and g, beside the row sums of squares
-// of the unscaled X.
+// Stage s of a CTA covers 128 k: W [128 k][64 n] (two [64 k][64 n] boxes),
+// X [16 rows][128 k] (two [16][64] boxes, rows past M read as zero) and
+// g [128].  Consumer warp w takes k-step w (16 deep) of every stage: its A
+// fragment is one ldmatrix.x4 of X, multiplied by g in bf16x2 (the exact
+// product rounded once, as in the row-tile kernels) after the row sums of
+// squares of the unscaled values are taken; its B fragments are four
+// ldmatrix.x4.trans of W (eight 16 x 8 blocks: MMA i covers columns
+// n0 + 8 i .. + 7).
 //
 // Work split: units of 64 columns; the K range of a unit may be cut into
-// `splits` pieces, one CTA each.  The 8 warps of a CTA take interleaved
-// 16-deep k-steps of its piece and combine their accumulators in shared
-// memory in warp order.  With more than one piece, each CTA publishes its
-// partial tile (16 x 64 fp32 and the 16 partial row sums) to the workspace
-// and the last CTA to arrive on the unit's counter adds all pieces in piece
-// order (deterministic), scales by 1/rms and writes Y; no CTA ever waits for
-// another.
+// `splits` pieces of whole stages, one CTA each.  The warps of a CTA combine
+// their accumulators in shared memory (over the idle ring) in warp order.
+// With more than one piece, each CTA publishes its partial tile (16 x 64 fp32
+// and the 16 partial row sums) to the workspace, and the last CTA to arrive on
+// the unit's counter adds all pieces in piece order (deterministic), scales by
+// 1/rms and writes Y; no CTA ever waits for another.  Every mbarrier wait is
+// bounded; a wait that runs out records RMM_ERR_DEVICE_TIMEOUT in this file's
+// status word and the CTA leaves without publishing.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "launch.h"
+#include "ptx.cuh"
 
 namespace rmm {
 namespace {
 
-constexpr int kGvWarps = 8;
-constexpr int kGvThreads = kGvWarps * 32;
-constexpr int kGvGroup = 3;                    // k-steps whose loads a warp issues together
+constexpr int kGvWarps = 8;                              // consumer warps
+constexpr int kGvThreads = (kGvWarps + 1) * 32;          // + one producer warp
+constexpr int kGvStages = 5;
+static_assert(kGvStageK == kGvWarps * kGvBK, "one MMA step per consumer warp per stage");
+constexpr uint32_t kGvWBytes = kGvStageK * kGvBN * 2;    // 16 KB
+constexpr uint32_t kGvXBytes = kGvMaxM * kGvStageK * 2;  // 4 KB
+constexpr uint32_t kGvGBytes = kGvStageK * 2;            // 256 B
+constexpr uint32_t kGvOffW = 0;
+constexpr uint32_t kGvOffX = kGvOffW + kGvStages * kGvWBytes;
+constexpr uint32_t kGvOffG = kGvOffX + kGvStages * kGvXBytes;
+constexpr uint32_t kGvOffBar = kGvOffG + kGvStages * kGvGBytes;
+constexpr uint32_t kGvOffSs = kGvOffBar + 2 * kGvStages * 8;
+constexpr uint32_t kGvOffMisc = kGvOffSs + kGvWarps * kGvMaxM * 4;
+constexpr uint32_t kGvSmem = kGvOffMisc + 16 + 1024;     // + alignment slack
+// the warps' accumulators while they are combined, over the W ring:
+// [warp][16 rows][64 + 8 columns] fp32 (8 columns of padding against bank conflicts)
+constexpr int kGvRedLd = kGvBN + 8;
+static_assert(kGvWarps * kGvMaxM * kGvRedLd * 4 <= kGvStages * kGvWBytes, "reduction area");
 constexpr int kGvPiece = kGvPieceFloats;
 
-__device__ __forceinline__ uint4 ldg_stream128(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
+// Position in a ring of n stages: the slot and the parity of the current pass.
+struct Ring {
+    uint32_t idx = 0, phase = 0, n;
+    __device__ explicit Ring(uint32_t n_) : n(n_) {}
+    __device__ __forceinline__ void advance() {
+        if (++idx == n) {
+            idx = 0;
+            phase ^= 1;
+        }
+    }
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
 }
-__device__ __forceinline__ uint32_t ldg32(const void* p) {
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     uint32_t v;
-    asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
     return v;
-}
-__device__ __forceinline__ uint32_t word(const uint4& v, int j) {
-    return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
-}
-__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
-// bf16x2 product rounded once to bf16 (nearest even).
-__device__ __forceinline__ uint32_t mul_bf16x2_rn(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&h);
 }
 // D (16 x 8 fp32) += A (16 x 16 bf16, row-major) * B (16 x 8 bf16, column-major).
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -81,151 +97,188 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ void grid_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void grid_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-
-// Row m (< M), columns n..n+7 (< N, n a multiple of 8) of Y from fp32 sums.
-__device__ __forceinline__ void store8(__nv_bfloat16* Y, int N, int m, int n, const float (&v)[8], float r) {
-    uint4 o;
-    o.x = pack2(v[0] * r, v[1] * r);
-    o.y = pack2(v[2] * r, v[3] * r);
-    o.z = pack2(v[4] * r, v[5] * r);
-    o.w = pack2(v[6] * r, v[7] * r);
-    *reinterpret_cast<uint4*>(Y + static_cast<size_t>(m) * N + n) = o;
+// Byte address of 16-byte chunk `chunk` of row `row` in a tile of 128-byte
+// rows written by TMA with the 128-byte swizzle (chunk index XOR row % 8).
+__device__ __forceinline__ uint32_t swz128(uint32_t tile, int row, int chunk) {
+    return tile + row * 128 + ((chunk ^ (row & 7)) << 4);
 }
 
 template <bool kFused>
 __global__ void __launch_bounds__(kGvThreads, 2)
-    gemv_kernel(const __nv_bfloat16* __restrict__ X, const __nv_bfloat16* __restrict__ g,
-                const __nv_bfloat16* __restrict__ W, __nv_bfloat16* __restrict__ Y, GemvLaunch a) {
-    __shared__ float red[kGvWarps * 8 * 4 * 32];   // [warp][mma][fragment][lane]
-    __shared__ float red_ss[kGvWarps * kGvMaxM];    // [warp][row]
-    __shared__ int is_last;
+    gemv_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                const __grid_constant__ CUtensorMap tmG, __nv_bfloat16* __restrict__ Y, GemvLaunch a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t sw = sb + kGvOffW, sx = sb + kGvOffX, sg = sb + kGvOffG, bar0 = sb + kGvOffBar;
+    auto full = [&](uint32_t s) { return bar0 + 8 * s; };
+    auto empty = [&](uint32_t s) { return bar0 + 8 * (kGvStages + s); };
+    float* red_ss = reinterpret_cast<float*>(smem + kGvOffSs);   // [warp][row]
+    volatile int* abort = reinterpret_cast<volatile int*>(smem + kGvOffMisc);
+    int* is_last = reinterpret_cast<int*>(smem + kGvOffMisc + 8);
+
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int gi = lane >> 2, q = lane & 3;
     const int unit = blockIdx.x / a.splits, piece = blockIdx.x - unit * a.splits;
     const int n0 = unit * kGvBN;
-    const int s0 = piece * a.steps_per_piece, s1 = min(a.ksteps, s0 + a.steps_per_piece);
-    const int K = a.K, N = a.N;
-    const int ncol = n0 + 8 * gi;            // this thread's 8 columns of W
-    const bool col_ok = ncol < N;
-    const bool row0 = gi < a.M, row1 = gi + 8 < a.M;
-    const __nv_bfloat16* wcol = W + ncol;
-    const __nv_bfloat16* xr0 = X + static_cast<size_t>(gi) * K;
-    const __nv_bfloat16* xr1 = X + static_cast<size_t>(gi + 8) * K;
+    const int st0 = piece * a.stages_per_piece;                              // first stage of the piece
+    const int nst = max(0, min(a.kstages, st0 + a.stages_per_piece) - st0);  // its stages
 
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kGvStages; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), kGvWarps);   // one elected lane per consumer warp
+        }
+        abort[0] = 0;
+        abort[1] = a.wait_limit_us;
+        fence_mbar_init();
+    }
+    __syncthreads();
     // X, g and W may be the previous kernel's output: wait for it; the next
     // kernel on the stream may be scheduled at once (it waits for this one).
-    grid_wait();
-    grid_launch();
+    grid_dep_wait();
 
     float acc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-    float ss0 = 0.f, ss1 = 0.f;   // rows gi and gi + 8
+    float ss0 = 0.f, ss1 = 0.f;   // rows lane/4 and lane/4 + 8 (consumers)
 
-    for (int base = s0 + w; base < s1; base += kGvWarps * kGvGroup) {
-        uint4 wv[kGvGroup][4];
-        uint32_t xa[kGvGroup][4], ga[kGvGroup][2];
-        // all loads of the group first, so that they are in flight together
-#pragma unroll
-        for (int u = 0; u < kGvGroup; ++u) {
-            const int step = base + u * kGvWarps;
-            const bool st = step < s1;          // warp-uniform
-            const int k0 = step * kGvBK;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int kr = k0 + 2 * q + (j & 1) + 8 * (j >> 1);
-                wv[u][j] = st && col_ok && kr < K ? ldg_stream128(wcol + static_cast<size_t>(kr) * N)
-                                                  : make_uint4(0u, 0u, 0u, 0u);
+    if (w == kGvWarps) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            grid_dep_launch();
+            prefetch_tmap(&tmW);
+            prefetch_tmap(&tmX);
+            if (kFused) prefetch_tmap(&tmG);
+            Ring ring(kGvStages);
+            int issued = 0;
+            for (int i = 0; i < nst; ++i) {
+                if (!mbar_wait(empty(ring.idx), ring.phase ^ 1, abort)) break;
+                const uint32_t f = full(ring.idx);
+                const int k0 = (st0 + i) * kGvStageK;
+                mbar_arrive_expect_tx(f, kGvWBytes + kGvXBytes + (kFused ? kGvGBytes : 0));
+                const uint32_t dw = sw + ring.idx * kGvWBytes, dx = sx + ring.idx * kGvXBytes;
+                tma_load_2d_nohint(dw, &tmW, f, n0, k0);
+                tma_load_2d_nohint(dw + kGvWBytes / 2, &tmW, f, n0, k0 + 64);
+                tma_load_2d_nohint(dx, &tmX, f, k0, 0);
+                tma_load_2d_nohint(dx + kGvXBytes / 2, &tmX, f, k0 + 64, 0);
+                if (kFused) {
+                    tma_load_1d(sg + ring.idx * kGvGBytes, &tmG, f, k0);
+                    tma_load_1d(sg + ring.idx * kGvGBytes + kGvGBytes / 2, &tmG, f, k0 + 64);
+                }
+                ring.advance();
+                ++issued;
             }
-            const int ka = k0 + 2 * q, kb = ka + 8;   // K is a multiple of 8: ka < K covers ka + 1
-            const bool oka = st && ka < K, okb = st && kb < K;
-            xa[u][0] = oka && row0 ? ldg32(xr0 + ka) : 0u;
-            xa[u][1] = oka && row1 ? ldg32(xr1 + ka) : 0u;
-            xa[u][2] = okb && row0 ? ldg32(xr0 + kb) : 0u;
-            xa[u][3] = okb && row1 ? ldg32(xr1 + kb) : 0u;
-            if (kFused) {
-                ga[u][0] = oka ? ldg32(g + ka) : 0u;
-                ga[u][1] = okb ? ldg32(g + kb) : 0u;
-            }
+            // never leave with copies still landing in shared memory
+            for (int i = issued > kGvStages ? issued - kGvStages : 0; i < issued; ++i)
+                mbar_wait_teardown(full(i % kGvStages), (i / kGvStages) & 1);
         }
-#pragma unroll
-        for (int u = 0; u < kGvGroup; ++u) {
-            if (base + u * kGvWarps >= s1) break;   // warp-uniform
+    } else {
+        // ------------------------------------------------ consumers: k-step w of every stage
+        const int q = lane & 3;
+        // ldmatrix row addresses: lane l gives row l % 8 of matrix l / 8
+        const int mj = lane >> 3, mr = lane & 7;
+        // A (X [16 rows][64 k] box w / 4, k-step (w % 4) * 16): matrices (rows 0-7 | 8-15) x (k 0-7 | 8-15)
+        const int xrow = mr + 8 * (mj & 1);
+        const int xchunk = 2 * (w & 3) + (mj >> 1);
+        const uint32_t xoff = (w >> 2) * (kGvXBytes / 2);
+        // B (W [64 k][64 n] box w / 4): matrices (k 0-7 | 8-15) x (n 16x + 0-7 | 16x + 8-15)
+        const int wrow = 16 * (w & 3) + mr + 8 * (mj & 1);
+        const uint32_t woff = (w >> 2) * (kGvWBytes / 2);
+        Ring ring(kGvStages);
+        for (int i = 0; i < nst; ++i) {
+            if (!warp_wait(full(ring.idx), ring.phase, abort)) break;
+            const uint32_t xt = sx + ring.idx * kGvXBytes + xoff;
+            const uint32_t wt = sw + ring.idx * kGvWBytes + woff;
             uint32_t af[4];
+            ldsm_x4(swz128(xt, xrow, xchunk), af);
             if (kFused) {
-                ss0 = fmaf(bf_lo(xa[u][0]), bf_lo(xa[u][0]), ss0);
-                ss0 = fmaf(bf_hi(xa[u][0]), bf_hi(xa[u][0]), ss0);
-                ss0 = fmaf(bf_lo(xa[u][2]), bf_lo(xa[u][2]), ss0);
-                ss0 = fmaf(bf_hi(xa[u][2]), bf_hi(xa[u][2]), ss0);
-                ss1 = fmaf(bf_lo(xa[u][1]), bf_lo(xa[u][1]), ss1);
-                ss1 = fmaf(bf_hi(xa[u][1]), bf_hi(xa[u][1]), ss1);
-                ss1 = fmaf(bf_lo(xa[u][3]), bf_lo(xa[u][3]), ss1);
-                ss1 = fmaf(bf_hi(xa[u][3]), bf_hi(xa[u][3]), ss1);
-                af[0] = mul_bf16x2_rn(xa[u][0], ga[u][0]);
-                af[1] = mul_bf16x2_rn(xa[u][1], ga[u][0]);
-                af[2] = mul_bf16x2_rn(xa[u][2], ga[u][1]);
-                af[3] = mul_bf16x2_rn(xa[u][3], ga[u][1]);
-            } else {
-                af[0] = xa[u][0];
-                af[1] = xa[u][1];
-                af[2] = xa[u][2];
-                af[3] = xa[u][3];
+                // rows lane/4 (af[0], af[2]) and lane/4 + 8 (af[1], af[3]); k pairs 2q and 2q + 8
+                ss0 = fmaf(bf16lo(af[0]), bf16lo(af[0]), ss0);
+                ss0 = fmaf(bf16hi(af[0]), bf16hi(af[0]), ss0);
+                ss0 = fmaf(bf16lo(af[2]), bf16lo(af[2]), ss0);
+                ss0 = fmaf(bf16hi(af[2]), bf16hi(af[2]), ss0);
+                ss1 = fmaf(bf16lo(af[1]), bf16lo(af[1]), ss1);
+                ss1 = fmaf(bf16hi(af[1]), bf16hi(af[1]), ss1);
+                ss1 = fmaf(bf16lo(af[3]), bf16lo(af[3]), ss1);
+                ss1 = fmaf(bf16hi(af[3]), bf16hi(af[3]), ss1);
+                const uint32_t gt = sg + ring.idx * kGvGBytes + (16 * w + 2 * q) * 2;
+                const uint32_t g01 = lds32(gt), g89 = lds32(gt + 16);
+                af[0] = mul_bf16x2(af[0], g01);
+                af[1] = mul_bf16x2(af[1], g01);
+                af[2] = mul_bf16x2(af[2], g89);
+                af[3] = mul_bf16x2(af[3], g89);
             }
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                // column n0 + 8 gi + i: rows (2q, 2q + 1) and (2q + 8, 2q + 9)
-                const uint32_t sel = (i & 1) ? 0x7632u : 0x5410u;
-                const uint32_t b0 = __byte_perm(word(wv[u][0], i >> 1), word(wv[u][1], i >> 1), sel);
-                const uint32_t b1 = __byte_perm(word(wv[u][2], i >> 1), word(wv[u][3], i >> 1), sel);
-                mma_16816(acc[i], af, b0, b1);
+            for (int x = 0; x < 4; ++x) {
+                uint32_t b[4];
+                ldsm_x4_trans(swz128(wt, wrow, 2 * x + (mj >> 1)), b);
+                mma_16816(acc[2 * x], af, b[0], b[1]);
+                mma_16816(acc[2 * x + 1], af, b[2], b[3]);
             }
+            // every lane's ldmatrix has returned: the stage may be refilled
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty(ring.idx));
+            ring.advance();
         }
     }
 
-    // ---- combine the warps in warp order
+    // ---- combine the warps in warp order (over the idle W ring)
+    __syncthreads();   // every stage consumed, every copy landed
+    const bool ok = !*abort;
+    float* red = reinterpret_cast<float*>(smem + kGvOffW);
+    if (w < kGvWarps) {
+        const int gi = lane >> 2, q = lane & 3;
+        float* mine = red + w * kGvMaxM * kGvRedLd;
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) red[((w * 8 + i) * 4 + j) * 32 + lane] = acc[i][j];
-    if (kFused) {
-        ss0 += __shfl_xor_sync(0xffffffffu, ss0, 1);
-        ss0 += __shfl_xor_sync(0xffffffffu, ss0, 2);
-        ss1 += __shfl_xor_sync(0xffffffffu, ss1, 1);
-        ss1 += __shfl_xor_sync(0xffffffffu, ss1, 2);
-        if (q == 0) {
-            red_ss[w * kGvMaxM + gi] = ss0;
-            red_ss[w * kGvMaxM + gi + 8] = ss1;
+        for (int i = 0; i < 8; ++i) {
+            *reinterpret_cast<float2*>(mine + gi * kGvRedLd + 8 * i + 2 * q) = make_float2(acc[i][0], acc[i][1]);
+            *reinterpret_cast<float2*>(mine + (gi + 8) * kGvRedLd + 8 * i + 2 * q) =
+                make_float2(acc[i][2], acc[i][3]);
+        }
+        if (kFused) {
+            ss0 += __shfl_xor_sync(0xffffffffu, ss0, 1);
+            ss0 += __shfl_xor_sync(0xffffffffu, ss0, 2);
+            ss1 += __shfl_xor_sync(0xffffffffu, ss1, 1);
+            ss1 += __shfl_xor_sync(0xffffffffu, ss1, 2);
+            if (q == 0) {
+                red_ss[w * kGvMaxM + gi] = ss0;
+                red_ss[w * kGvMaxM + gi + 8] = ss1;
+            }
         }
     }
     __syncthreads();
-    // thread (j, l) of the first 128: fragment j of lane l over the 8 MMAs,
-    // i.e. row m, columns n0 + nl .. + 7
-    const int tj = threadIdx.x >> 5, tl = threadIdx.x & 31;
-    const int m = (tl >> 2) + 8 * (tj >> 1);
-    const int nl = 16 * (tl & 3) + 8 * (tj & 1);
-    const bool worker = threadIdx.x < 128;
+    if (!ok) return;   // a wait ran out: the status word says so; publish nothing
+    // thread t < 128: row m = t / 8, columns n0 + nl .. + 7
+    const int m = threadIdx.x >> 3, nl = 8 * (threadIdx.x & 7);
+    const bool worker = threadIdx.x < kGvMaxM * 8;
     float v[8];
     float ssm = 0.f;
     if (worker) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float t = 0.f;
+        for (int i = 0; i < 8; ++i) v[i] = 0.f;
 #pragma unroll
-            for (int w2 = 0; w2 < kGvWarps; ++w2) t += red[((w2 * 8 + i) * 4 + tj) * 32 + tl];
-            v[i] = t;
+        for (int w2 = 0; w2 < kGvWarps; ++w2) {
+            const float* src = red + (w2 * kGvMaxM + m) * kGvRedLd + nl;
+            const float4 lo = *reinterpret_cast<const float4*>(src);
+            const float4 hi = *reinterpret_cast<const float4*>(src + 4);
+            v[0] += lo.x; v[1] += lo.y; v[2] += lo.z; v[3] += lo.w;
+            v[4] += hi.x; v[5] += hi.y; v[6] += hi.z; v[7] += hi.w;
+            if (kFused) ssm += red_ss[w2 * kGvMaxM + m];
         }
-        if (kFused)
-#pragma unroll
-            for (int w2 = 0; w2 < kGvWarps; ++w2) ssm += red_ss[w2 * kGvMaxM + m];
     }
-    const float inv_k = 1.f / static_cast<float>(K);
+    const float inv_k = 1.f / static_cast<float>(a.K);
+    auto store8 = [&](const float (&t)[8], float r) {
+        uint4 o;
+        o.x = pack_bf16x2(t[0] * r, t[1] * r);
+        o.y = pack_bf16x2(t[2] * r, t[3] * r);
+        o.z = pack_bf16x2(t[4] * r, t[5] * r);
+        o.w = pack_bf16x2(t[6] * r, t[7] * r);
+        *reinterpret_cast<uint4*>(Y + static_cast<size_t>(m) * a.N + n0 + nl) = o;
+    };
     if (a.splits == 1) {
-        if (worker && m < a.M && n0 + nl < N)
-            store8(Y, N, m, n0 + nl, v, kFused ? rsqrtf(ssm * inv_k + a.eps) : 1.f);
+        if (worker && m < a.M && n0 + nl < a.N) store8(v, kFused ? rsqrtf(ssm * inv_k + a.eps) : 1.f);
         return;
     }
 
@@ -234,16 +287,16 @@ __global__ void __launch_bounds__(kGvThreads, 2)
     if (worker) {
         __stcg(reinterpret_cast<float4*>(mine + m * kGvBN + nl), make_float4(v[0], v[1], v[2], v[3]));
         __stcg(reinterpret_cast<float4*>(mine + m * kGvBN + nl + 4), make_float4(v[4], v[5], v[6], v[7]));
-        if ((tl & 3) == 0 && (tj & 1) == 0) __stcg(mine + kGvMaxM * kGvBN + m, ssm);
+        if (nl == 0) __stcg(mine + kGvMaxM * kGvBN + m, ssm);
     }
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
-        is_last = atomicAdd(a.counters + unit, 1) == a.splits - 1;
+        *is_last = atomicAdd(a.counters + unit, 1) == a.splits - 1;
         __threadfence();
     }
     __syncthreads();
-    if (!is_last) return;
+    if (!*is_last) return;
     if (worker) {
         const float* first = a.ws + static_cast<size_t>(unit) * a.splits * kGvPiece;
         float t[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -271,41 +324,65 @@ __global__ void __launch_bounds__(kGvThreads, 2)
                 }
             }
         }
-        if (m < a.M && n0 + nl < N) store8(Y, N, m, n0 + nl, t, kFused ? rsqrtf(tss * inv_k + a.eps) : 1.f);
+        if (m < a.M && n0 + nl < a.N) store8(t, kFused ? rsqrtf(tss * inv_k + a.eps) : 1.f);
     }
     // every piece of this unit has arrived: reset its counter for the next launch
     if (threadIdx.x == 0) a.counters[unit] = 0;
 }
 
+// Raises the kernel's dynamic shared-memory limit, once per (variant, device).
+cudaError_t gemv_smem_attr(bool fused) {
+    static int done[2][64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && done[fused][dev]) return cudaSuccess;
+    e = fused ? cudaFuncSetAttribute(gemv_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGvSmem)
+              : cudaFuncSetAttribute(gemv_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGvSmem);
+    if (e == cudaSuccess && dev < 64) done[fused][dev] = 1;
+    return e;
+}
+
 }  // namespace
 
-cudaError_t launch_gemv(bool fused, const void* X, const void* g, const void* W, void* Y, const GemvLaunch& a,
-                        cudaStream_t s) {
+cudaError_t launch_gemv(bool fused, const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap& tmG,
+                        void* Y, const GemvLaunch& a, cudaStream_t s) {
+    cudaError_t e = gemv_smem_attr(fused);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.units * a.splits);
     cfg.blockDim = dim3(kGvThreads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = kGvSmem;
     cfg.stream = s;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    const auto* x = static_cast<const __nv_bfloat16*>(X);
-    const auto* gg = static_cast<const __nv_bfloat16*>(g);
-    const auto* w = static_cast<const __nv_bfloat16*>(W);
     auto* y = static_cast<__nv_bfloat16*>(Y);
-    cudaError_t e = fused ? cudaLaunchKernelEx(&cfg, gemv_kernel<true>, x, gg, w, y, a)
-                          : cudaLaunchKernelEx(&cfg, gemv_kernel<false>, x, gg, w, y, a);
+    e = fused ? cudaLaunchKernelEx(&cfg, gemv_kernel<true>, tmX, tmW, tmG, y, a)
+              : cudaLaunchKernelEx(&cfg, gemv_kernel<false>, tmX, tmW, tmG, y, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 int gemv_ctas_per_sm(bool fused) {
+    if (gemv_smem_attr(fused) != cudaSuccess) return 0;
     int n = 0;
-    const cudaError_t e = fused ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_kernel<true>, kGvThreads, 0)
-                                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_kernel<false>, kGvThreads, 0);
+    const cudaError_t e =
+        fused ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_kernel<true>, kGvThreads, kGvSmem)
+              : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_kernel<false>, kGvThreads, kGvSmem);
     return e == cudaSuccess ? n : 0;
+}
+
+cudaError_t gemv_read_and_clear_status(int* out) {
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_status, sizeof(int));
+    if (e != cudaSuccess) return e;
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_status, &zero, sizeof(int));
+    *out = v;
+    return e;
 }
 
 }  // namespace rmm

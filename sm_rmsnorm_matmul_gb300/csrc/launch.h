@@ -75,26 +75,31 @@ cudaError_t launch_rmsnorm(const void* X, const void* g, void* Xn, int M, int K,
 cudaError_t read_and_clear_status(int* out);
 
 // ------------------------------------------------ small-M path (gemv.cu)
-constexpr int kGvMaxM = 16;   // rows of X: one m16 tile of mma.sync.m16n8k16
-constexpr int kGvBN = 64;     // columns of W per unit
-constexpr int kGvBK = 16;     // k per step
+constexpr int kGvMaxM = 16;      // rows of X: one m16 tile of mma.sync.m16n8k16
+constexpr int kGvBN = 64;        // columns of W per unit
+constexpr int kGvBK = 16;        // k per MMA step
+constexpr int kGvStageK = 128;   // k per pipeline stage (one MMA step per consumer warp)
 constexpr int kGvPieceFloats = kGvMaxM * kGvBN + kGvMaxM;   // one published piece: tile, then row sums
 
 struct GemvLaunch {
     int M, N, K;
     float eps;
-    int units;             // ceil(N / 64)
-    int ksteps;            // ceil(K / 16)
-    int splits;            // K pieces per unit, one CTA each (grid = units * splits)
-    int steps_per_piece;   // k-steps of a piece (the last may have fewer)
-    float* ws;             // [units][splits][16 * 64 + 16] fp32 partials (splits > 1)
-    int* counters;         // [units] arrival counters, zero between launches (splits > 1)
+    int units;              // ceil(N / 64)
+    int kstages;            // ceil(K / 128)
+    int splits;             // K pieces per unit, one CTA each (grid = units * splits)
+    int stages_per_piece;   // stages of a piece (the last may have fewer)
+    float* ws;              // [units][splits][16 * 64 + 16] fp32 partials (splits > 1)
+    int* counters;          // [units] arrival counters, zero between launches (splits > 1)
+    int wait_limit_us;      // limit of one bounded in-kernel wait
 };
-// X [M, K], g [K] (fused only), W [K, N], Y [M, N] bf16, row-major.
-cudaError_t launch_gemv(bool fused, const void* X, const void* g, const void* W, void* Y, const GemvLaunch& a,
-                        cudaStream_t s);
+// tmX: X [M, K] in boxes of [16 rows][64 k]; tmW: W [K, N] in boxes of
+// [64 k][64 n]; tmG: g [K] in boxes of 64 (fused only); 128-byte swizzle.
+cudaError_t launch_gemv(bool fused, const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap& tmG,
+                        void* Y, const GemvLaunch& a, cudaStream_t s);
 // CTAs of the small-M kernel that fit on one SM.
 int gemv_ctas_per_sm(bool fused);
+// The small-M kernel's own status word (as read_and_clear_status).
+cudaError_t gemv_read_and_clear_status(int* out);
 
 // ------------------------------------------------ QK-normalised attention (attention.cu)
 constexpr int kAttBM = 128;   // query rows per tile

@@ -45,7 +45,7 @@ def test_status_strings(lib):
 
 def test_force_path_roundtrip(lib):
     assert rmm.force_path(rmm.PATH_ROWS) == rmm.PATH_AUTO
-    assert rmm.dispatch_path(8, 1024, 1024) == rmm.PATH_ROWS
+    assert rmm.dispatch_path(8, 1024, 1024) == rmm.PATH_ROWS   # forced
     assert rmm.force_path(rmm.PATH_SMALL_M) == rmm.PATH_ROWS
     assert rmm.dispatch_path(4096, 4096, 4096) == rmm.PATH_SMALL_M
     assert rmm.force_path(rmm.PATH_AUTO) == rmm.PATH_SMALL_M
@@ -53,10 +53,20 @@ def test_force_path_roundtrip(lib):
     assert rmm.force_path(rmm.PATH_AUTO) == rmm.PATH_AUTO
 
 
-def test_default_dispatch(lib):
-    # the row-tile kernels serve every shape unless a path is forced
-    for M in (1, 8, 16, 17, 64, 65, 128, 4096):
-        assert rmm.dispatch_path(M, 4096, 6144) == rmm.PATH_ROWS
+def test_default_dispatch_crossover(lib):
+    # Up to 16 rows: the small-M path where it streams W faster than the
+    # row-tile kernel (long K over a narrow N), on the measured shapes; more
+    # rows always the row-tile kernels.  Without a GPU the dispatch assumes a
+    # 152-SM GB300.
+    small = [(16, 8192, 1024), (16, 14336, 2048), (4, 2048, 512), (16, 4096, 1024), (8, 4096, 2048)]
+    rows = [(16, 2048, 2048), (8, 1024, 1024), (1, 1024, 1024), (16, 4096, 6144), (16, 4096, 28672),
+            (16, 4096, 2560), (64, 4096, 28672)]
+    for M, K, N in small:
+        assert rmm.dispatch_path(M, K, N) == rmm.PATH_SMALL_M, (M, K, N)
+    for M, K, N in rows:
+        assert rmm.dispatch_path(M, K, N) == rmm.PATH_ROWS, (M, K, N)
+    for M in (17, 64, 65, 128, 4096):
+        assert rmm.dispatch_path(M, 8192, 1024) == rmm.PATH_ROWS
 
 
 A16 = 0x10000          # a 16-byte aligned fake address; never dereferenced
