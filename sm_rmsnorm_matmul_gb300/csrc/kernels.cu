@@ -749,7 +749,7 @@ __device__ __forceinline__ bool ta_unit(const RowsLaunch& a, int i, TaUnit& u) {
     return true;
 }
 
-template <bool kGlu, bool kWnk, bool kLora>
+template <bool kGlu, bool kWnk, bool kLora, bool kHilo>
 __global__ void __launch_bounds__(kThreads, 1)
     rows_ta_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmT,
@@ -829,6 +829,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kOutBN = kGlu ? kRowsBN / 2 : kRowsBN;
     // the low-rank adapter stage: its own instantiations (kLora), plain [K, N] form only
     static_assert(!kLora || (!kGlu && !kWnk), "the adapter stage is for the plain form");
+    // the hi/lo output of the adapter's T: its own instantiation (kHilo), unscaled plain form
+    static_assert(!kHilo || (!kGlu && !kWnk && !kLora), "the hi/lo output is for the plain form");
 
     if (warp == 0 || warp == 3) {
         // ------------------------------------------------ TMA producers
@@ -919,14 +921,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             float ssp[8];   // independent partial sums: no long dependency chain
 #pragma unroll
             for (int c = 0; c < 8; ++c) ssp[c] = 0.f;
-            for (int kb = un.kb0; kb < un.kb1 + (kLora ? un.extra : 0); ++kb) {
-                const bool ext = kLora && kb >= un.kb1;   // the adapter stage: T rows, no gain, no statistic
-                if (!warp_wait(xfull0 + 8 * xr.idx, xr.phase, abort)) { ok = false; break; }
-                const uint32_t xt = sx + xr.idx * kTaXBytes + xrow;
-                const uint32_t gt = sg + xr.idx * kGBytes;
-                uint4 xv[8];
+            // The X rows of block kb + 1 are loaded from shared memory before
+            // block kb's store into tensor memory, so that the two overlap.
+            const int kend = un.kb1 + (kLora ? un.extra : 0);
+            uint4 xv[8];
+            if (!warp_wait(xfull0 + 8 * xr.idx, xr.phase, abort)) { ok = false; break; }
 #pragma unroll
-                for (int c = 0; c < 8; ++c) xv[c] = lds128(xt + ((c ^ swz) << 4));
+            for (int c = 0; c < 8; ++c) xv[c] = lds128(sx + xr.idx * kTaXBytes + xrow + ((c ^ swz) << 4));
+            for (int kb = un.kb0; kb < kend; ++kb) {
+                const bool ext = kLora && kb >= un.kb1;   // the adapter stages: T rows, no gain, no statistic
+                const uint32_t gt = sg + xr.idx * kGBytes;   // g of this block (the slot of its X)
                 uint32_t out[32];
                 if (!ext) {
 #pragma unroll
@@ -955,6 +959,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(xempty0 + 8 * xr.idx);
                 xr.advance();
+                if (kb + 1 < kend) {
+                    if (!warp_wait(xfull0 + 8 * xr.idx, xr.phase, abort)) { ok = false; break; }
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) xv[c] = lds128(sx + xr.idx * kTaXBytes + xrow + ((c ^ swz) << 4));
+                }
                 if (!warp_wait(aempty0 + 8 * ar.idx, ar.phase ^ 1, abort)) { ok = false; break; }
                 tmem_st_32x32(tmem + kTaACol + ar.idx * 32 + lane_base, out);
                 tc_fence_before();
@@ -1081,7 +1090,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             acc[h].z += t4.z;
                             acc[h].w += t4.w;
                         }
-                    if (m < a.M && n0 + col < (!kGlu && a.hilo ? kBK : Nout)) {
+                    if (m < a.M && n0 + col < (kHilo ? kBK : Nout)) {
                         const float r = rr[rl];
                         float o4[4];
                         if constexpr (kGlu) {
@@ -1094,7 +1103,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             o4[1] = acc[0].y * r;
                             o4[2] = acc[0].z * r;
                             o4[3] = acc[0].w * r;
-                            if (a.hilo) {
+                            if constexpr (kHilo) {
                                 store_hilo4(Y + static_cast<size_t>(m) * (2 * kBK), col, o4[0], o4[1], o4[2], o4[3]);
                                 continue;
                             }
@@ -1117,8 +1126,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t pk[kOutBN / 2];   // the row's outputs, packed as bf16x2
             // a hilo output: the first 64 accumulator columns as hi (words
             // 0..31, columns 0..63 of Y) and lo (words 32..63, columns 64..127)
-            const bool hilo = !kGlu && a.hilo;
-            if (hilo) {
+            constexpr bool hilo = kHilo;
+            if constexpr (hilo) {
 #pragma unroll
                 for (int c = 0; c < kBK / 16; ++c) {
                     uint32_t v[16];
@@ -1130,8 +1139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
 #pragma unroll
-            for (int c = 0; c < kOutBN / 16; ++c) {
-                if (hilo) break;
+            for (int c = 0; c < (hilo ? 0 : kOutBN / 16); ++c) {
                 uint32_t v[16];
                 tmem_ld_32x16(taddr + c * 16, v);
                 if constexpr (kGlu) {
@@ -1305,11 +1313,14 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
     if ((glu || wnk || lora) && !fused) return cudaErrorInvalidValue;
     if (lora && (glu || wnk)) return cudaErrorInvalidValue;
     if (fused && !split && a.xrows == kRowsBM) {
-        auto ta = lora ? rows_ta_kernel<false, false, true>
-                : wnk  ? (glu ? rows_ta_kernel<true, true, false> : rows_ta_kernel<false, true, false>)
-                       : (glu ? rows_ta_kernel<true, false, false> : rows_ta_kernel<false, false, false>);
+        const bool hilo = a.hilo != 0;
+        if (hilo && (glu || wnk || lora)) return cudaErrorInvalidValue;
+        auto ta = hilo ? rows_ta_kernel<false, false, false, true>
+                : lora ? rows_ta_kernel<false, false, true, false>
+                : wnk  ? (glu ? rows_ta_kernel<true, true, false, false> : rows_ta_kernel<false, true, false, false>)
+                       : (glu ? rows_ta_kernel<true, false, false, false> : rows_ta_kernel<false, false, false, false>);
         cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(ta),
-                                         lora ? 18 : wnk ? (glu ? 15 : 14) : (glu ? 9 : 6));
+                                         hilo ? 19 : lora ? 18 : wnk ? (glu ? 15 : 14) : (glu ? 9 : 6));
         if (e != cudaSuccess) return e;
         // The pieces of a tail tile wait for one another: launched as a
         // cooperative grid, every CTA is resident at once (or the launch
