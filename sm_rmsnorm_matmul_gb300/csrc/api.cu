@@ -444,35 +444,71 @@ RowsPlan plan_rows(int dev, bool fused, int64_t M, int64_t K, int64_t N, const D
     return p;
 }
 
-// K split of the last tiles of the fused kernel for several row tiles.  When
-// the tiles leave a last wave at most half full, those tiles are cut along K
-// so that every CTA has a share of them.  When all the tiles fill at most half
-// the SMs (one partial wave, e.g. a contraction with a narrow N such as the
-// adapter's T), every tile is cut, one piece per CTA, up to one CTA per SM.
+// K split of the last units of the fused kernel for several row tiles.  A
+// unit is one tile, or (paired) the two row blocks of one column tile, taken
+// by one CTA slot (a CTA or a cluster of two).  When the units leave a last
+// wave at most half full, those units are cut along K so that every slot has
+// a share of them.  When all the units fill at most half the slots (one
+// partial wave, e.g. a contraction with a narrow N such as the adapter's T),
+// every unit is cut, one piece per slot, up to one slot per SM or pair of SMs.
 // The pieces of a tile wait for one another, so the launch is cooperative.
 struct TailPlan {
-    int tiles = 0;    // tail tiles (0: every tile whole)
-    int pieces = 1;   // K pieces per tail tile
+    int tiles = 0;    // tail units (0: every unit whole)
+    int pieces = 1;   // K pieces per tail unit
     int kbp = 0;      // k-blocks per piece
-    int grid = 0;     // CTAs of the launch
+    int grid = 0;     // slots of the launch
 };
-TailPlan plan_tail(const RowsPlan& p, const DeviceInfo& d) {
+TailPlan plan_tail(int units, int grid, int k_blocks, int slots) {
     TailPlan t;
-    t.grid = p.grid;
-    const int tiles = p.m_tiles * p.n_tiles;
-    const int sms = d.sm_count > 0 ? d.sm_count : 1;
-    const bool few = tiles <= p.grid && 2 * tiles <= sms;
-    const int grid = few ? sms : p.grid;
-    const int rem = tiles % grid;
-    if (!((tiles > grid || few) && rem > 0 && 2 * rem <= grid && p.k_blocks >= 2)) return t;
-    const int pmax = grid / rem;
-    const int kbp = (p.k_blocks + pmax - 1) / pmax;
-    const int pieces = (p.k_blocks + kbp - 1) / kbp;
+    t.grid = grid;
+    const bool few = units <= grid && 2 * units <= slots;
+    const int g = few ? slots : grid;
+    const int rem = units % g;
+    if (!((units > g || few) && rem > 0 && 2 * rem <= g && k_blocks >= 2)) return t;
+    const int pmax = g / rem;
+    const int kbp = (k_blocks + pmax - 1) / pmax;
+    const int pieces = (k_blocks + kbp - 1) / kbp;
     if (pieces < 2) return t;
     t.tiles = rem;
     t.pieces = pieces;
     t.kbp = kbp;
-    if (few) t.grid = tiles * pieces;   // every tile cut: one CTA per piece
+    if (few) t.grid = units * pieces;   // every unit cut: one slot per piece
+    return t;
+}
+
+std::mutex g_pair_mu;
+std::map<int, int> g_pair_occ;
+
+// Clusters of two of the paired fused kernel resident at once on `dev`.
+int pair_clusters(int dev) {
+    std::lock_guard<std::mutex> lk(g_pair_mu);
+    auto it = g_pair_occ.find(dev);
+    if (it != g_pair_occ.end()) return it->second;
+    const int n = rmm::rows_pair_max_active_clusters();
+    g_pair_occ[dev] = n;
+    return n;
+}
+
+// Launch shape of the fused kernel for several row tiles: paired (clusters
+// of two CTAs sharing W, for the plain form) where clusters of two can be
+// resident, its units, and the K split of its last units.
+struct TaPlan {
+    bool pair;
+    int kc;        // CTAs per slot
+    int units;     // units of kc row blocks x one column tile
+    TailPlan tail;
+    int ctas;      // grid size
+};
+TaPlan plan_ta(int dev, const RowsPlan& p, const DeviceInfo& d, bool plain) {
+    TaPlan t{};
+    const int sms = d.sm_count > 0 ? d.sm_count : 1;
+    const int clusters = plain ? pair_clusters(dev) : 0;
+    t.pair = clusters > 0;
+    t.kc = t.pair ? 2 : 1;
+    t.units = ((p.m_tiles + t.kc - 1) / t.kc) * p.n_tiles;
+    const int slots = t.pair ? clusters : sms;
+    t.tail = plan_tail(t.units, std::min(t.units, slots), p.k_blocks, slots);
+    t.ctas = t.tail.grid * t.kc;
     return t;
 }
 
@@ -625,9 +661,12 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
     if (fused && !p.cluster && p.xrows == rmm::kRowsBM) {
         if (!map_2d_store(&tmY, Y, M, hilo ? 2 * kBK : glu ? N / 2 : N)) return RMM_ERR_INTERNAL;
         a.tmY = &tmY;
-        const TailPlan t = plan_tail(p, d);
+        const TaPlan tp = plan_ta(dev, p, d, !glu && !wnk && !lora && !hilo);
+        const TailPlan& t = tp.tail;
+        a.pair = tp.pair ? 1 : 0;
+        a.grid = tp.ctas;
         if (t.tiles > 0) {
-            const int rem = t.tiles, pieces = t.pieces;
+            const int rem = t.tiles * tp.kc, pieces = t.pieces;   // tail tiles
             {
                 constexpr size_t kPieceBytes = static_cast<size_t>(rmm::kRowsBM) * rmm::kRowsBN * sizeof(float);
                 const size_t units = static_cast<size_t>(rem) * pieces;
@@ -649,10 +688,9 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
                     a.ws_ss = w.ss;
                     a.ws_count = w.counters;
                 }
-                a.tail_tiles = rem;
+                a.tail_tiles = t.tiles;   // in units
                 a.tail_pieces = pieces;
                 a.tail_kbp = t.kbp;
-                a.grid = t.grid;
             }
         }
     }
@@ -790,12 +828,12 @@ int rmm_describe_plan(int64_t M, int64_t K, int64_t N, int fused, int* info) {
         info[6] = p.m_tiles * p.n_tiles;
         info[7] = p.kb_per_split;
         if (fused != 0 && !p.cluster && p.xrows == rmm::kRowsBM) {
-            // the fused kernel for several row tiles: its tail tiles' K pieces
-            const TailPlan t = plan_tail(p, d);
-            if (t.tiles > 0) {
-                info[1] = t.pieces;
-                info[3] = t.grid;
-                info[7] = t.kbp;
+            // the fused kernel for several row tiles: its grid and its tail tiles' K pieces
+            const TaPlan tp = plan_ta(dev, p, d, !glu);
+            info[3] = tp.ctas;
+            if (tp.tail.tiles > 0) {
+                info[1] = tp.tail.pieces;
+                info[7] = tp.tail.kbp;
             }
         }
     }

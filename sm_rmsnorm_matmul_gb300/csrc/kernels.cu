@@ -720,16 +720,19 @@ constexpr uint32_t kTaOffMisc = kTaOffRr + kRowsBM * 4;
 constexpr uint32_t kTaSmem = kTaOffMisc + 16 + 1024;
 constexpr uint32_t kTaAccCol = 0, kTaACol = 256;
 
-// Work of CTA b of G in rows_ta_kernel, in order: whole tiles b, b + G, ...
-// below full = tiles - tail_tiles; then, if b < tail_tiles * tail_pieces, K
-// piece b % tail_pieces of tail tile b / tail_pieces (tile full + that).
+// Work of CTA slot b of G in rows_ta_kernel (a slot is one CTA, or a pair of
+// CTAs that share W: their tiles are the two row blocks of a "unit" of
+// kC = 2 row blocks x one column tile), in order: whole units b, b + G, ...
+// below full = units - tail_tiles; then, if b < tail_tiles * tail_pieces, K
+// piece b % tail_pieces of tail unit b / tail_pieces (unit full + that).
 struct TaUnit {
     int t, kb0, kb1, piece;   // piece < 0: the whole K range
     int extra;                // adapter stages that follow (whole tile, or piece 0 of a tail tile)
 };
+template <int kC>
 __device__ __forceinline__ bool ta_unit(const RowsLaunch& a, int i, TaUnit& u) {
-    const int G = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
-    const int full = a.m_tiles * a.n_tiles - a.tail_tiles;
+    const int G = static_cast<int>(gridDim.x) / kC, b = static_cast<int>(blockIdx.x) / kC;
+    const int full = ((a.m_tiles + kC - 1) / kC) * a.n_tiles - a.tail_tiles;
     const int t = b + i * G;
     if (t < full) {
         u.t = t;
@@ -749,7 +752,7 @@ __device__ __forceinline__ bool ta_unit(const RowsLaunch& a, int i, TaUnit& u) {
     return true;
 }
 
-template <bool kGlu, bool kWnk, bool kLora, bool kHilo>
+template <bool kGlu, bool kWnk, bool kLora, bool kHilo, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     rows_ta_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmT,
@@ -786,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < kTaWStages; ++s) {
             mbar_init(wfull0 + 8 * s, 1);
-            mbar_init(wempty0 + 8 * s, 1);
+            mbar_init(wempty0 + 8 * s, kPair ? 2 : 1);   // paired: both CTAs' MMAs read the slot
         }
         for (int s = 0; s < kTaAStages; ++s) {
             mbar_init(afull0 + 8 * s, 4);
@@ -817,12 +820,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // paired: the peer's barriers exist before any copy or commit targets them
+    if (kPair) cluster_sync_all();
     // Set-up above overlaps the previous kernel on the stream; its writes are
     // visible after grid_dep_wait().  The next kernel may then be scheduled.
     grid_dep_wait();
     if (threadIdx.x == 0) grid_dep_launch();
     const uint32_t tmem = *tmem_holder;
-    const int num_tiles = a.m_tiles * a.n_tiles;
+    // Paired (kPair): the two CTAs of a cluster take the two row blocks of each
+    // unit and share its W stages, each loading half of every stage's boxes
+    // multicast to both.  Units are counted in pairs of row blocks.
+    constexpr int kC = kPair ? 2 : 1;
+    const int rank = kPair ? static_cast<int>(cluster_ctarank()) : 0;
+    const int m_units = (a.m_tiles + kC - 1) / kC;
+    const int num_tiles = m_units * a.n_tiles;
+    static_assert(!kPair || (!kGlu && !kWnk && !kLora && !kHilo), "the paired form is the plain one");
     // Output columns: N, or F = N / 2 for the gated form, whose tile covers
     // 128 output columns read from gate columns n0.. and up columns F + n0..
     const int Nout = kGlu ? a.N / 2 : a.N;
@@ -844,9 +856,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t full0 = load_x ? xfull0 : wfull0, empty0 = load_x ? xempty0 : wempty0;
             bool ok = true;
             TaUnit un;
-            for (int i = 0; ok && ta_unit(a, i, un); ++i) {
+            for (int i = 0; ok && ta_unit<kC>(a, i, un); ++i) {
                 int mb, nb;
-                rows_tile_coords(un.t, a.m_tiles, a.n_tiles, mb, nb);
+                rows_tile_coords(un.t, m_units, a.n_tiles, mb, nb);
+                mb = mb * kC + rank;
                 const int n0 = nb * kOutBN;
                 for (int kb = un.kb0; kb < un.kb1 + (kLora ? un.extra : 0); ++kb) {
                     const bool ext = kLora && kb >= un.kb1;   // the adapter stages: T (hi, lo) and B
@@ -857,6 +870,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_2d_nohint(sx + ring.idx * kTaXBytes, ext ? &tmT : &tmX, f,
                                            (ext ? kb - un.kb1 : kb) * kBK, mb * kRowsBM);
                         if (!ext) tma_load_1d(sg + ring.idx * kGBytes, &tmG, f, kb * kBK);
+                    } else if constexpr (kPair) {
+                        // this CTA's two of the stage's (up to) four boxes, to both CTAs
+                        const uint32_t bytes = w_stage_bytes<false, false>(n0, a.N);
+                        mbar_arrive_expect_tx(f, bytes);
+                        const int nbox = static_cast<int>(bytes / kWBoxBytes);
+                        for (int j = 2 * rank; j < 2 * rank + 2 && j < nbox; ++j)
+                            tma_load_2d_mc(sw + ring.idx * kRowsWBytes + j * kWBoxBytes, &tmW, f, n0 + 64 * j,
+                                           kb * kBK, 0x3);
                     } else {
                         mbar_arrive_expect_tx(f, w_stage_bytes<kGlu, kWnk>(n0, a.N));
                         load_w_stage<kGlu, kWnk>(sw + ring.idx * kRowsWBytes, ext ? &tmB : &tmW, f, n0,
@@ -879,7 +900,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t tl = 0;
             bool ok = true;
             TaUnit un;
-            for (int i = 0; ok && ta_unit(a, i, un); ++i, ++tl) {
+            for (int i = 0; ok && ta_unit<kC>(a, i, un); ++i, ++tl) {
                 if (!mbar_wait(accempty, (tl & 1) ^ 1, abort)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + kTaAccCol;
@@ -892,7 +913,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
                         mma_bf16_ts(d, a0 + kk * 8, w_desc<kWnk>(b0, kk), idesc, kb != un.kb0 || kk != 0);
-                    mma_commit(wempty0 + 8 * wr.idx);
+                    if constexpr (kPair) mma_commit_mc(wempty0 + 8 * wr.idx, 0x3);   // both CTAs' slots
+                    else mma_commit(wempty0 + 8 * wr.idx);
                     mma_commit(aempty0 + 8 * ar.idx);
                     wr.advance();
                     ar.advance();
@@ -914,7 +936,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t tl = 0;
         bool ok = true;
         TaUnit un;
-        for (int i = 0; ok && ta_unit(a, i, un); ++i, ++tl) {
+        for (int i = 0; ok && ta_unit<kC>(a, i, un); ++i, ++tl) {
             const uint32_t buf = tl & 1, use = tl >> 1;
             // sr[buf] is free once the epilogue read it for the tile two back
             if (!warp_wait(srempty0 + 8 * buf, (use & 1) ^ 1, abort)) break;
@@ -998,7 +1020,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t chunks = 0;   // staging buffer uses so far
         uint32_t tl = 0;
         TaUnit un;
-        for (int i = 0; ta_unit(a, i, un); ++i, ++tl) {
+        for (int i = 0; ta_unit<kC>(a, i, un); ++i, ++tl) {
             const uint32_t buf = tl & 1, use = tl >> 1;
             if (!warp_wait(accfull, tl & 1, abort)) break;
             if (!warp_wait(srfull0 + 8 * buf, use & 1, abort)) break;
@@ -1007,7 +1029,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(srempty0 + 8 * buf);
             int mb, nb;
-            rows_tile_coords(un.t, a.m_tiles, a.n_tiles, mb, nb);
+            rows_tile_coords(un.t, m_units, a.n_tiles, mb, nb);
+            mb = mb * kC + rank;
             const int n0 = nb * kOutBN;
             const uint32_t taddr = tmem + kTaAccCol + (static_cast<uint32_t>(q * 32) << 16);
             if (un.piece >= 0) {
@@ -1016,7 +1039,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // pieces, then reduce rows [r0, r1) of the tile over all
                 // pieces in piece order and write them to Y.
                 const int P = a.tail_pieces;
-                const int tail = un.t - (num_tiles - a.tail_tiles);
+                const int tail = (un.t - (num_tiles - a.tail_tiles)) * kC + rank;   // tail tile
                 const size_t slot = static_cast<size_t>(tail) * P;
                 float* wrow = a.ws_acc + ((slot + un.piece) * kRowsBM + row) * kRowsBN;
 #pragma unroll 4
@@ -1177,7 +1200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           pk[c * 16 + 4 * j + 2], pk[c * 16 + 4 * j + 3]));
                     fence_proxy_async_smem();
                     if (!(ok = epi_sync())) break;
-                    if (e == 0) {
+                    if (e == 0 && mb < a.m_tiles) {   // (a paired unit's second row block may lie past M)
                         tma_store_2d(&tmY, sbuf, n0 + c * 32, mb * kRowsBM);
                         bulk_commit_group();
                     }
@@ -1191,6 +1214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    // paired: the peer may still copy or commit into this CTA until it is done
+    if (kPair) cluster_sync_all();
     if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
@@ -1315,17 +1340,22 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
     if (fused && !split && a.xrows == kRowsBM) {
         const bool hilo = a.hilo != 0;
         if (hilo && (glu || wnk || lora)) return cudaErrorInvalidValue;
-        auto ta = hilo ? rows_ta_kernel<false, false, false, true>
-                : lora ? rows_ta_kernel<false, false, true, false>
-                : wnk  ? (glu ? rows_ta_kernel<true, true, false, false> : rows_ta_kernel<false, true, false, false>)
-                       : (glu ? rows_ta_kernel<true, false, false, false> : rows_ta_kernel<false, false, false, false>);
+        const bool pair = a.pair != 0;
+        if (pair && (hilo || glu || wnk || lora)) return cudaErrorInvalidValue;
+        auto ta = pair ? rows_ta_kernel<false, false, false, false, true>
+                : hilo ? rows_ta_kernel<false, false, false, true, false>
+                : lora ? rows_ta_kernel<false, false, true, false, false>
+                : wnk  ? (glu ? rows_ta_kernel<true, true, false, false, false>
+                              : rows_ta_kernel<false, true, false, false, false>)
+                       : (glu ? rows_ta_kernel<true, false, false, false, false>
+                              : rows_ta_kernel<false, false, false, false, false>);
         cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(ta),
-                                         hilo ? 19 : lora ? 18 : wnk ? (glu ? 15 : 14) : (glu ? 9 : 6));
+                                         pair ? 20 : hilo ? 19 : lora ? 18 : wnk ? (glu ? 15 : 14) : (glu ? 9 : 6));
         if (e != cudaSuccess) return e;
         // The pieces of a tail tile wait for one another: launched as a
         // cooperative grid, every CTA is resident at once (or the launch
         // fails), whatever else shares the device.
-        e = launch_ex(ta, a.grid, kTaSmem, 1, s, a.tail_tiles > 0, tmX, tmW, tmG, tmT, tmB, *a.tmY, y, a);
+        e = launch_ex(ta, a.grid, kTaSmem, pair ? 2 : 1, s, a.tail_tiles > 0, tmX, tmW, tmG, tmT, tmB, *a.tmY, y, a);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
@@ -1371,6 +1401,10 @@ int max_active_clusters(Kern kern, int slot, int splits, size_t smem) {
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
     return n;
+}
+
+int rows_pair_max_active_clusters() {
+    return max_active_clusters(rows_ta_kernel<false, false, false, false, true>, 20, 2, kTaSmem);
 }
 
 int rows_max_active_clusters(bool fused, int splits, size_t smem, bool glu, bool wnk, bool lora) {

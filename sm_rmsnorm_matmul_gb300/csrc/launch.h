@@ -31,6 +31,8 @@ bool rows_overlay_fits(int xrows, int stages, int splits, int MP, bool glu = fal
 size_t rows_stage_bytes(int xrows);
 int rows_max_active_clusters(bool fused, int splits, size_t smem, bool glu = false, bool wnk = false,
                              bool lora = false);
+// Clusters of two CTAs of the paired fused kernel that fit on the device at once.
+int rows_pair_max_active_clusters();
 struct RowsLaunch {
     int M, N, K;
     float eps;
@@ -52,6 +54,9 @@ struct RowsLaunch {
     int cluster;               // 1: the splits of a tile form a cluster
     int xrows, MP, stages;
     int grid;
+    int pair;                  // 1: fused kernel for several row tiles, CTAs in clusters of two that
+                               // take the two row blocks of each unit and share its W stages
+                               // (tiles and tail tiles then count units of two row blocks)
     const CUtensorMap* tmY;    // Y in boxes of [128 rows][32 columns], 64-byte swizzle
                                // (used by the fused kernel for several row tiles)
     // Fused kernel for several row tiles: the last tail_tiles tiles (those a
