@@ -824,7 +824,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kPair) cluster_sync_all();
     // Set-up above overlaps the previous kernel on the stream; its writes are
     // visible after grid_dep_wait().  The next kernel may then be scheduled.
-    grid_dep_wait();
+    // With the adapter the previous kernel is the launch that computes T,
+    // which itself waited for its own predecessor before letting this one
+    // start: X, g, W and B are visible already, and only the loads of T (the
+    // adapter stages) and the K pieces' workspace (which that launch may use
+    // too) wait for it.
+    if (!kLora) grid_dep_wait();
     if (threadIdx.x == 0) grid_dep_launch();
     const uint32_t tmem = *tmem_holder;
     // Paired (kPair): the two CTAs of a cluster take the two row blocks of each
@@ -865,6 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool ext = kLora && kb >= un.kb1;   // the adapter stages: T (hi, lo) and B
                     if (!mbar_wait(empty0 + 8 * ring.idx, ring.phase ^ 1, abort)) { ok = false; break; }
                     const uint32_t f = full0 + 8 * ring.idx;
+                    if (kLora && ext && load_x) grid_dep_wait();   // T is the previous launch's output
                     if (load_x) {
                         mbar_arrive_expect_tx(f, kTaXBytes + (ext ? 0 : kGBytes));
                         tma_load_2d_nohint(sx + ring.idx * kTaXBytes, ext ? &tmT : &tmX, f,
@@ -1041,6 +1047,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int P = a.tail_pieces;
                 const int tail = (un.t - (num_tiles - a.tail_tiles)) * kC + rank;   // tail tile
                 const size_t slot = static_cast<size_t>(tail) * P;
+                if (kLora) grid_dep_wait();   // the launch that computes T may use the workspace
                 float* wrow = a.ws_acc + ((slot + un.piece) * kRowsBM + row) * kRowsBN;
 #pragma unroll 4
                 for (int c = 0; c < kRowsBN / 16; ++c) {

@@ -129,6 +129,30 @@ def test_tail_tiles_cut_along_k(rmm, M, K, N):
     assert torch.equal(Y, run_fused(rmm, X, g, W, 1e-6))
 
 
+def test_tail_tiles_with_another_stream_holding_sms(rmm):
+    # The pieces of a tail tile wait for one another; the launch is
+    # cooperative, so all its CTAs are resident together even while kernels
+    # on another stream hold SMs: the call completes with a clean status and
+    # the right result.
+    from sm_rmsnorm_matmul_gb300 import inputs
+    M, K, N = 1280, 1024, 4096
+    assert rmm.describe_plan(M, K, N)["splits"] > 1   # tail tiles cut along K
+    X, g, W = inputs.random_problem(M, K, N, seed=77, x_kind="row_scaled")
+    Xd, gd, Wd = X.cuda(), g.cuda(), W.cuda()
+    a = torch.randn(8192, 8192, device="cuda", dtype=torch.bfloat16)
+    other = torch.cuda.Stream()
+    main = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(other):
+        for _ in range(8):      # a few milliseconds of full-device GEMMs
+            a = (a @ a).clamp_(-1, 1)
+    Y = rmm.rmsnorm_matmul(Xd, gd, Wd, 1e-6, stream=main)
+    other.synchronize()
+    main.synchronize()
+    assert rmm.device_status() == 0
+    assert_close(Y.cpu(), oracle.rmsnorm_matmul(X, g, W, 1e-6), f"{M}x{K}x{N} beside another stream")
+
+
 # One row tile of 65..128 rows: the K-split receive blocks are too large to
 # sit beside the pipeline, so they reuse the pipeline buffers once every
 # split has finished its last MMA (handshake between the CTAs of a cluster).
