@@ -489,9 +489,12 @@ int pair_clusters(int dev) {
     return n;
 }
 
-// Launch shape of the fused kernel for several row tiles: paired (clusters
-// of two CTAs sharing W, for the plain form) where clusters of two can be
-// resident, its units, and the K split of its last units.
+// Launch shape of the fused kernel for several row tiles: its units, the K
+// split of its last units, and whether it runs paired (clusters of two CTAs
+// sharing W, for the plain form).  Paired only where clusters of two can be
+// resident and the units need no K-split tail: a launch that is both a
+// cluster launch and cooperative is not used (two such launches faulted the
+// GPU when replayed under the profiler, though none did otherwise).
 struct TaPlan {
     bool pair;
     int kc;        // CTAs per slot
@@ -500,15 +503,24 @@ struct TaPlan {
     int ctas;      // grid size
 };
 TaPlan plan_ta(int dev, const RowsPlan& p, const DeviceInfo& d, bool plain) {
-    TaPlan t{};
     const int sms = d.sm_count > 0 ? d.sm_count : 1;
     const int clusters = plain ? pair_clusters(dev) : 0;
-    t.pair = clusters > 0;
-    t.kc = t.pair ? 2 : 1;
-    t.units = ((p.m_tiles + t.kc - 1) / t.kc) * p.n_tiles;
-    const int slots = t.pair ? clusters : sms;
-    t.tail = plan_tail(t.units, std::min(t.units, slots), p.k_blocks, slots);
-    t.ctas = t.tail.grid * t.kc;
+    TaPlan t{};
+    if (clusters > 0) {
+        t.pair = true;
+        t.kc = 2;
+        t.units = ((p.m_tiles + 1) / 2) * p.n_tiles;
+        t.tail = plan_tail(t.units, std::min(t.units, clusters), p.k_blocks, clusters);
+        if (t.tail.tiles == 0) {
+            t.ctas = t.tail.grid * 2;
+            return t;
+        }
+    }
+    t.pair = false;
+    t.kc = 1;
+    t.units = p.m_tiles * p.n_tiles;
+    t.tail = plan_tail(t.units, std::min(t.units, sms), p.k_blocks, sms);
+    t.ctas = t.tail.grid;
     return t;
 }
 

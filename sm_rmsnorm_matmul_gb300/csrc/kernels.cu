@@ -820,8 +820,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // paired: the peer's barriers exist before any copy or commit targets them
-    if (kPair) cluster_sync_all();
+    // Paired: launched as clusters of two, or not at all (a launch without
+    // them reports an internal error and does no work: no cluster operation
+    // may run).
+    if (kPair) {
+        uint32_t nct;
+        asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(nct));
+        if (nct != 2 || a.tail_tiles != 0) {
+            if (threadIdx.x == 0) atomicCAS(&g_status, 0, kStatusInternal);
+            if (warp == 2) {
+                tc_fence_after();
+                tmem_dealloc(*tmem_holder, 512);
+            }
+            return;
+        }
+        // the peer's barriers exist before any copy or commit targets them
+        cluster_sync_all();
+    }
     // Set-up above overlaps the previous kernel on the stream; its writes are
     // visible after grid_dep_wait().  The next kernel may then be scheduled.
     // With the adapter the previous kernel is the launch that computes T,
@@ -897,6 +912,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t n = ring.n;
             for (uint32_t i = issued > n ? issued - n : 0; i < issued; ++i)
                 mbar_wait_teardown(full0 + 8 * (i % n), (i / n) & 1);
+            // Paired: the MMAs of both CTAs release every W slot in both CTAs
+            // (commit multicast), and those arrivals land asynchronously.
+            // Wait until the last use of each slot has been released by both,
+            // so that after the exit barrier no arrival is still in flight
+            // towards the peer (or from it into this CTA).
+            if (kPair && !load_x)
+                for (uint32_t i = issued > n ? issued - n : 0; i < issued; ++i)
+                    mbar_wait_teardown(empty0 + 8 * (i % n), (i / n) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer

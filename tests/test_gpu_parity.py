@@ -153,6 +153,32 @@ def test_tail_tiles_with_another_stream_holding_sms(rmm):
     assert_close(Y.cpu(), oracle.rmsnorm_matmul(X, g, W, 1e-6), f"{M}x{K}x{N} beside another stream")
 
 
+@pytest.mark.parametrize("M,K,N", [(2048, 512, 3840),    # paired CTAs, whole tiles
+                                   (1280, 1024, 4096)])   # tail tiles cut along K (cooperative)
+def test_prefill_calls_replayed_from_a_cuda_graph(rmm, M, K, N):
+    # the benchmark's way of calling: captured once, replayed; the same bits
+    # as an eager call, and the oracle's result
+    from sm_rmsnorm_matmul_gb300 import inputs
+    X, g, W = inputs.random_problem(M, K, N, seed=M + N, x_kind="row_scaled")
+    Xd, gd, Wd = X.cuda(), g.cuda(), W.cuda()
+    eager = run_fused(rmm, X, g, W, 1e-6)
+    s = torch.cuda.Stream()
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    with torch.cuda.stream(s):
+        rmm.rmsnorm_matmul(Xd, gd, Wd, 1e-6, out=Y, stream=s)   # workspace, if any, before capture
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        rmm.rmsnorm_matmul(Xd, gd, Wd, 1e-6, out=Y, stream=s)
+    for _ in range(2):
+        Y.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert rmm.device_status() == 0
+        assert torch.equal(Y.cpu(), eager)
+    assert_close(eager, oracle.rmsnorm_matmul(X, g, W, 1e-6), f"{M}x{K}x{N}")
+
+
 # One row tile of 65..128 rows: the K-split receive blocks are too large to
 # sit beside the pipeline, so they reuse the pipeline buffers once every
 # split has finished its last MMA (handshake between the CTAs of a cluster).
