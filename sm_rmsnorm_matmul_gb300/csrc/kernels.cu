@@ -924,7 +924,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(kRowsBM, kRowsBN, false, !kWnk);
+            // the hi/lo output (N <= 64) multiplies one 64-column box of W, not a 256-wide padded tile
+            constexpr uint32_t idesc = idesc_bf16_f32(kRowsBM, kHilo ? kBK : kRowsBN, false, !kWnk);
             Ring wr(kTaWStages), ar(kTaAStages);
             uint32_t tl = 0;
             bool ok = true;
@@ -991,9 +992,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t gs[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            const float x0 = bf16lo(xs[i]), x1 = bf16hi(xs[i]);
-                            ssp[c] = fmaf(x0, x0, ssp[c]);
-                            ssp[c] = fmaf(x1, x1, ssp[c]);
+                            ssp[c] = fma_sq_bf16x2(xs[i], ssp[c]);
                             out[c * 4 + i] = mul_bf16x2(xs[i], gs[i]);
                         }
                     }
@@ -1072,8 +1071,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const size_t slot = static_cast<size_t>(tail) * P;
                 if (kLora) grid_dep_wait();   // the launch that computes T may use the workspace
                 float* wrow = a.ws_acc + ((slot + un.piece) * kRowsBM + row) * kRowsBN;
+                // accumulator columns the reduction reads (a hi/lo output has 64)
+                constexpr int kPartCols = kHilo ? kBK : kRowsBN;
 #pragma unroll 4
-                for (int c = 0; c < kRowsBN / 16; ++c) {
+                for (int c = 0; c < kPartCols / 16; ++c) {
                     uint32_t v[16];
                     tmem_ld_32x16(taddr + c * 16, v);
 #pragma unroll
@@ -1106,9 +1107,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // partial at accumulator column col and the up partial 128
                 // columns further
                 constexpr int kHalves = kGlu ? 2 : 1;
-                const int items = (r1 - r0) * (kOutBN / 4);
+                constexpr int kRedBN = kHilo ? kBK : kOutBN;   // output columns of the tile
+                const int items = (r1 - r0) * (kRedBN / 4);
                 for (int it = e; ok && it < items; it += 128) {
-                    const int rl = it / (kOutBN / 4), col = (it % (kOutBN / 4)) * 4;
+                    const int rl = it / (kRedBN / 4), col = (it % (kRedBN / 4)) * 4;
                     const int m = mb * kRowsBM + r0 + rl;
                     const float* src = a.ws_acc + (slot * kRowsBM + r0 + rl) * kRowsBN + col;
                     float4 acc[kHalves];
@@ -1252,6 +1254,387 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ------------------------------------------- tall tiles: 256 rows per CTA
+// The kernel for many row tiles (prefill-like shapes) of the plain form:
+// each CTA computes a tile of 256 rows (two halves of 128, one M = 128 MMA
+// each) by 256 columns, so that every W stage it loads feeds both halves.
+// Per 128 x 256 x 64 of work a CTA then takes in 32 KB (16 KB of X, half of
+// a 32 KB W stage) instead of the 48 KB of a 128-row tile, and on GB300 the
+// operand delivery into each SM, not the tensor pipe, bounds the 128-row
+// kernels (the tensor pipe is active about half the time there while shared
+// memory is far from busy).  The two accumulators fill tensor memory
+// (2 x 256 columns), so the MMA reads A from shared memory: in the fused form
+// the transform warps multiply each X stage by g in place, one row per
+// thread, before the MMAs read it.  X, g and W of a k-block share one stage,
+// which the MMAs' commit releases.  Warps: 0 TMA producer, 1 MMA issuer,
+// 2 tensor-memory allocation, 4-11 transform and epilogue (warps 4-7 the
+// first half's rows, 8-11 the second's; each thread keeps its row from the
+// transform, with the row's sum of squares in registers, to the epilogue).
+// Tiles and tail pieces are those of the 128-row kernel with 256-row tiles.
+constexpr int kTtLook = 2;   // k-blocks of the next tile transformed before an epilogue
+constexpr uint32_t kTtXBytes = kTtBM * kBK * 2;               // 32 KB
+constexpr uint32_t kTtStageBytes = kTtXBytes + kRowsWBytes;   // 64 KB: X, then W
+constexpr uint32_t kTtOutBytes = kRowsBM * 32 * 2;            // 8 KB: 128 rows x 32 bf16 of Y
+constexpr uint32_t kTtOffOut = kTtStages * kTtStageBytes;     // two staging buffers per half
+constexpr uint32_t kTtOffG = kTtOffOut + 4 * kTtOutBytes;
+constexpr uint32_t kTtOffBar = kTtOffG + kTtStages * kGBytes;
+// full, ready, empty per stage; accfull, accempty, mmadone, episync[2], tailsync
+constexpr uint32_t kTtNumBars = 3 * kTtStages + 6;
+constexpr uint32_t kTtOffRr = kTtOffBar + ((kTtNumBars * 8 + 15) / 16) * 16;   // 1/rms of a piece's rows
+constexpr uint32_t kTtOffMisc = kTtOffRr + kTtBM * 4;
+constexpr uint32_t kTtSmem = kTtOffMisc + 16 + 1024;
+static_assert(kTtSmem <= 232448, "the tall-tile kernel's shared memory exceeds the opt-in limit");
+
+template <bool kFused>
+__global__ void __launch_bounds__(kThreads, 1)
+    tall_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmY,
+                __nv_bfloat16* __restrict__ Y, RowsLaunch a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t sg = sb + kTtOffG, sout = sb + kTtOffOut;
+    const uint32_t bar0 = sb + kTtOffBar;
+    const uint32_t full0 = bar0, ready0 = bar0 + 8 * kTtStages, empty0 = bar0 + 16 * kTtStages;
+    const uint32_t accfull = bar0 + 24 * kTtStages, accempty = accfull + 8, mmadone = accfull + 16;
+    const uint32_t episync0 = accfull + 24, tailsync = accfull + 40;
+    float* rr = reinterpret_cast<float*>(smem + kTtOffRr);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kTtOffMisc);
+    volatile int* abort = reinterpret_cast<volatile int*>(smem + kTtOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTtStages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(ready0 + 8 * s, 8);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        mbar_init(accfull, 1);
+        mbar_init(accempty, 8);
+        mbar_init(mmadone, 1);
+        mbar_init(episync0, 4);
+        mbar_init(episync0 + 8, 4);
+        mbar_init(tailsync, 8);
+        abort[0] = 0;
+        abort[1] = a.wait_limit_us;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmX);
+        prefetch_tmap(&tmW);
+        if (kFused) prefetch_tmap(&tmG);
+        prefetch_tmap(&tmY);
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(tmem_holder), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // Set-up above overlaps the previous kernel on the stream; its writes are
+    // visible after grid_dep_wait().  The next kernel may then be scheduled.
+    grid_dep_wait();
+    if (threadIdx.x == 0) grid_dep_launch();
+    const uint32_t tmem = *tmem_holder;
+    const int num_tiles = a.m_tiles * a.n_tiles;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            Ring ring(kTtStages);
+            uint32_t issued = 0;
+            bool ok = true;
+            TaUnit un;
+            for (int i = 0; ok && ta_unit<1>(a, i, un); ++i) {
+                int mb, nb;
+                rows_tile_coords(un.t, a.m_tiles, a.n_tiles, mb, nb);
+                const int n0 = nb * kRowsBN;
+                const uint32_t wbytes = w_stage_bytes<false, false>(n0, a.N);
+                for (int kb = un.kb0; kb < un.kb1; ++kb) {
+                    if (!mbar_wait(empty0 + 8 * ring.idx, ring.phase ^ 1, abort)) { ok = false; break; }
+                    const uint32_t f = full0 + 8 * ring.idx;
+                    const uint32_t st = sb + ring.idx * kTtStageBytes;
+                    mbar_arrive_expect_tx(f, kTtXBytes + wbytes + (kFused ? kGBytes : 0u));
+                    // two boxes of 128 rows (a box past M reads zeros)
+                    tma_load_2d_nohint(st, &tmX, f, kb * kBK, mb * kTtBM);
+                    tma_load_2d_nohint(st + kTtXBytes / 2, &tmX, f, kb * kBK, mb * kTtBM + kRowsBM);
+                    load_w_stage<false, false>(st + kTtXBytes, &tmW, f, n0, kb, a.N, a.N);
+                    if (kFused) tma_load_1d(sg + ring.idx * kGBytes, &tmG, f, kb * kBK);
+                    ring.advance();
+                    ++issued;
+                }
+            }
+            // never leave with copies still landing in shared memory
+            const uint32_t n = ring.n;
+            for (uint32_t i = issued > n ? issued - n : 0; i < issued; ++i)
+                mbar_wait_teardown(full0 + 8 * (i % n), (i / n) & 1);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(kRowsBM, kRowsBN, false, true);
+            Ring ring(kTtStages);
+            uint32_t tl = 0;
+            bool ok = true;
+            TaUnit un;
+            for (int i = 0; ok && ta_unit<1>(a, i, un); ++i, ++tl) {
+                if (!mbar_wait(accempty, (tl & 1) ^ 1, abort)) break;
+                tc_fence_after();
+                for (int kb = un.kb0; kb < un.kb1; ++kb) {
+                    // fused: the stage once the transform has applied g; plain: once it has landed
+                    if (!mbar_wait((kFused ? ready0 : full0) + 8 * ring.idx, ring.phase, abort)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t st = sb + ring.idx * kTtStageBytes;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            mma_bf16_ss(tmem + h * kRowsBN, sdesc_sw128(st + h * (kTtXBytes / 2) + kk * 32, 16, 1024),
+                                        w_desc<false>(st + kTtXBytes, kk), idesc, kb != un.kb0 || kk != 0);
+                    mma_commit(empty0 + 8 * ring.idx);
+                    ring.advance();
+                }
+                if (!ok) break;
+                mma_commit(accfull);
+            }
+            mma_commit(mmadone);
+            mbar_wait_teardown(mmadone, 0);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------ transform and epilogue
+        const int hh = (warp - 4) >> 2;                // half of the tile
+        const int q = warp & 3;                        // lane quarter this warp may access
+        const int rh = q * 32 + lane;                  // row within the half (tensor-memory lane)
+        const int row = hh * kRowsBM + rh;             // row of the tile
+        const int et = threadIdx.x - 128;              // 0..255
+        const uint32_t xrow = static_cast<uint32_t>(row) * 128;
+        const uint32_t swz = static_cast<uint32_t>(row & 7);
+        const uint32_t taddr = tmem + hh * kRowsBN + (static_cast<uint32_t>(q * 32) << 16);
+        const float inv_k = 1.f / static_cast<float>(a.K);
+        const uint32_t episync = episync0 + 8 * hh;
+        uint32_t ep = 0, tp = 0;
+        // the four warps of this half; all eight warps
+        auto half_sync = [&]() {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(episync);
+            return warp_wait(episync, (ep++) & 1, abort);
+        };
+        auto all_sync = [&]() {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tailsync);
+            return warp_wait(tailsync, (tp++) & 1, abort);
+        };
+        const uint32_t rswz = static_cast<uint32_t>((rh >> 1) & 3);
+        uint32_t chunks = 0;   // staging buffer uses so far (per half)
+        // Epilogue of one tile: wait for its accumulators, read this thread's
+        // accumulator row (scaled, bf16) into registers and release tensor
+        // memory at once; then store Y through the half's two 8 KB staging
+        // buffers with TMA stores (64-byte swizzle: the 16-byte chunk j of
+        // row r sits at chunk j ^ ((r >> 1) & 3)).  ss: the row's sum of
+        // squares over the tile's k-blocks.
+        auto epilogue = [&](const TaUnit& un, uint32_t tl, float ss) -> bool {
+            if (!warp_wait(accfull, tl & 1, abort)) return false;
+            tc_fence_after();
+            int mb, nb;
+            rows_tile_coords(un.t, a.m_tiles, a.n_tiles, mb, nb);
+            const int n0 = nb * kRowsBN, m0 = mb * kTtBM;
+            if (un.piece >= 0) {
+                // A K piece of a tail tile: publish the fp32 partial and the
+                // partial row sums of squares, wait for the tile's other
+                // pieces, then reduce rows [r0, r1) of the tile over all
+                // pieces in piece order and write them to Y.
+                const int P = a.tail_pieces;
+                const int tail = un.t - (num_tiles - a.tail_tiles);
+                const size_t slot = static_cast<size_t>(tail) * P;
+                float* wrow = a.ws_acc + ((slot + un.piece) * kTtBM + row) * kRowsBN;
+#pragma unroll 4
+                for (int c = 0; c < kRowsBN / 16; ++c) {
+                    uint32_t v[16];
+                    tmem_ld_32x16(taddr + c * 16, v);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        __stcg(reinterpret_cast<float4*>(wrow + c * 16 + 4 * j),
+                               make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                           __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])));
+                }
+                __stcg(a.ws_ss + (slot + un.piece) * kTtBM + row, ss);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(accempty);
+                __threadfence();
+                int* cnt = a.ws_count + 2 * tail;
+                bool ok = all_sync();
+                if (et == 0) {
+                    atomicAdd(cnt, 1);
+                    ok = spin_until_ge(cnt, P, abort) && ok;
+                }
+                ok = all_sync() && ok && !*abort;
+                const int r0 = (un.piece * kTtBM) / P, r1 = ((un.piece + 1) * kTtBM) / P;
+                if (ok && et < r1 - r0) {
+                    float tot = 0.f;
+                    for (int p2 = 0; p2 < P; ++p2) tot += __ldcg(a.ws_ss + (slot + p2) * kTtBM + r0 + et);
+                    rr[et] = kFused ? rsqrtf(tot * inv_k + a.eps) : 1.f;
+                }
+                ok = all_sync() && ok;
+                // items: 4 output columns of one row
+                const int items = (r1 - r0) * (kRowsBN / 4);
+                for (int it = et; ok && it < items; it += 256) {
+                    const int rl = it / (kRowsBN / 4), col = (it % (kRowsBN / 4)) * 4;
+                    const int m = m0 + r0 + rl;
+                    const float* src = a.ws_acc + (slot * kTtBM + r0 + rl) * kRowsBN + col;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    int p2 = 0;
+                    for (; p2 + 4 <= P; p2 += 4) {
+                        float4 t4[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            t4[j] = __ldcg(reinterpret_cast<const float4*>(
+                                src + static_cast<size_t>(p2 + j) * kTtBM * kRowsBN));
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            acc.x += t4[j].x;
+                            acc.y += t4[j].y;
+                            acc.z += t4[j].z;
+                            acc.w += t4[j].w;
+                        }
+                    }
+                    for (; p2 < P; ++p2) {
+                        const float4 t4 =
+                            __ldcg(reinterpret_cast<const float4*>(src + static_cast<size_t>(p2) * kTtBM * kRowsBN));
+                        acc.x += t4.x;
+                        acc.y += t4.y;
+                        acc.z += t4.z;
+                        acc.w += t4.w;
+                    }
+                    if (m < a.M && n0 + col < a.N) {
+                        const float r = rr[rl];
+                        uint2 o;
+                        o.x = pack_bf16x2(acc.x * r, acc.y * r);
+                        o.y = pack_bf16x2(acc.z * r, acc.w * r);
+                        *reinterpret_cast<uint2*>(Y + static_cast<size_t>(m) * a.N + n0 + col) = o;
+                    }
+                }
+                // the last piece through resets the tile's counters for the next launch
+                all_sync();
+                if (et == 0 && atomicAdd(cnt + 1, 1) == P - 1) {
+                    atomicExch(cnt, 0);
+                    atomicExch(cnt + 1, 0);
+                }
+                return ok;
+            }
+            const float r = kFused ? rsqrtf(ss * inv_k + a.eps) : 1.f;
+            uint32_t pk[kRowsBN / 2];   // the row's outputs, packed as bf16x2
+#pragma unroll
+            for (int c = 0; c < kRowsBN / 16; ++c) {
+                uint32_t v[16];
+                tmem_ld_32x16(taddr + c * 16, v);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    pk[c * 8 + i] = pack_bf16x2(__uint_as_float(v[2 * i]) * r, __uint_as_float(v[2 * i + 1]) * r);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(accempty);   // the MMA may start the next tile
+            bool ok = true;
+            const bool rows_in = m0 + hh * kRowsBM < a.M;   // (a half past M is not stored)
+#pragma unroll
+            for (int c = 0; c < kRowsBN / 32; ++c) {
+                if (n0 + c * 32 < a.N) {             // block-uniform
+                    const uint32_t sbuf = sout + (2 * hh + (chunks & 1)) * kTtOutBytes;
+                    // the store issued two chunks ago must have read this buffer
+                    if (rh == 0) bulk_wait_group_read<1>();
+                    if (!(ok = half_sync())) break;
+                    const uint32_t rbase = sbuf + rh * 64;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        sts128(rbase + ((j ^ rswz) << 4),
+                               make_uint4(pk[c * 16 + 4 * j], pk[c * 16 + 4 * j + 1], pk[c * 16 + 4 * j + 2],
+                                          pk[c * 16 + 4 * j + 3]));
+                    fence_proxy_async_smem();
+                    if (!(ok = half_sync())) break;
+                    if (rh == 0 && rows_in) {
+                        tma_store_2d(&tmY, sbuf, n0 + c * 32, m0 + hh * kRowsBM);
+                        bulk_commit_group();
+                    }
+                    ++chunks;
+                }
+            }
+            return ok;
+        };
+
+        uint32_t it = 0, tl = 0;   // k-blocks so far (the stage ring's position); tiles so far
+        bool ok = true;
+        bool pend = false;         // a tile whose epilogue has not run yet
+        TaUnit pun{};
+        uint32_t ptl = 0;
+        float pss = 0.f;
+        TaUnit un{};
+        // One pass per tile and a last one without k-blocks; the pending
+        // epilogue runs after kTtLook k-blocks of the next tile, or at the end
+        // of a shorter one (a single call site, inlined once).
+        for (int i = 0;; ++i) {
+            const bool have = ok && ta_unit<1>(a, i, un);
+            const int kb1 = have ? un.kb1 : 0;
+            float ssp[8];   // independent partial sums: no long dependency chain
+#pragma unroll
+            for (int c = 0; c < 8; ++c) ssp[c] = 0.f;
+            int done = 0;
+            for (int kb = have ? un.kb0 : 0;;) {
+                if (pend && (done == kTtLook || kb == kb1)) {
+                    pend = false;
+                    if (!(ok = epilogue(pun, ptl, pss))) break;
+                    continue;
+                }
+                if (kb == kb1) break;
+                if constexpr (kFused) {
+                    // X*g in place, rounded to bf16, and the row's sum of squares
+                    const uint32_t s = it % kTtStages;
+                    if (!warp_wait(full0 + 8 * s, (it / kTtStages) & 1, abort)) { ok = false; break; }
+                    const uint32_t xa = sb + s * kTtStageBytes + xrow;
+                    const uint32_t gt = sg + s * kGBytes;
+                    uint4 xv[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) xv[c] = lds128(xa + ((c ^ swz) << 4));
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 gv = lds128(gt + c * 16);
+                        const uint32_t xw[4] = {xv[c].x, xv[c].y, xv[c].z, xv[c].w};
+                        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+                        uint32_t o[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            ssp[c] = fma_sq_bf16x2(xw[u], ssp[c]);
+                            o[u] = mul_bf16x2(xw[u], gw[u]);
+                        }
+                        sts128(xa + ((c ^ swz) << 4), make_uint4(o[0], o[1], o[2], o[3]));
+                    }
+                    // the MMA (async proxy) reads what these threads wrote
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(ready0 + 8 * s);
+                }
+                ++kb;
+                ++it;
+                ++done;
+            }
+            if (!have || !ok) break;
+            pend = true;
+            pun = un;
+            ptl = tl++;
+            pss = ((ssp[0] + ssp[1]) + (ssp[2] + ssp[3])) + ((ssp[4] + ssp[5]) + (ssp[6] + ssp[7]));
+        }
+        if (rh == 0) bulk_wait_group_all();   // Y is written before the CTA exits
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 // ------------------------------------------------------------ unfused RMSNorm
 constexpr int kNormThreads = 256;
 
@@ -1367,6 +1750,16 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
     const bool glu = a.glu != 0, wnk = a.w_nk != 0, lora = a.lora != 0;
     if ((glu || wnk || lora) && !fused) return cudaErrorInvalidValue;
     if (lora && (glu || wnk)) return cudaErrorInvalidValue;
+    if (a.tall) {
+        if (glu || wnk || lora || a.hilo || a.unscaled || split) return cudaErrorInvalidValue;
+        auto tk = fused ? tall_kernel<true> : tall_kernel<false>;
+        cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(tk), fused ? 21 : 22);
+        if (e != cudaSuccess) return e;
+        // cooperative with tail pieces, as the 128-row kernel
+        e = launch_ex(tk, a.grid, kTtSmem, 1, s, a.tail_tiles > 0, tmX, tmW, fused ? tmG : tmX, *a.tmY, y, a);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     if (fused && !split && a.xrows == kRowsBM) {
         const bool hilo = a.hilo != 0;
         if (hilo && (glu || wnk || lora)) return cudaErrorInvalidValue;

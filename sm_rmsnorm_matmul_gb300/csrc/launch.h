@@ -18,6 +18,11 @@ constexpr int kRowsMaxStages = 6;
 
 constexpr int kClusterMaxSplits = 8;   // portable cluster size
 
+// 256-row path (the plain form over many row tiles): CTA tile 256 x 256, two
+// M = 128 halves sharing each W stage, in three pipeline stages.
+constexpr int kTtBM = 2 * kRowsBM;
+constexpr int kTtStages = 3;
+
 // Row-tile path shared memory: xrows = rows of X loaded per stage (128, or
 // M rounded up to 16 for a single row tile); red_slots = K splits reduced
 // through a cluster (0 without); MP = M rounded up to 16; overlay: the
@@ -54,12 +59,13 @@ struct RowsLaunch {
     int cluster;               // 1: the splits of a tile form a cluster
     int xrows, MP, stages;
     int grid;
+    int tall;                  // 1: the 256-row kernel (plain form; m_tiles then counts 256-row tiles)
     int pair;                  // 1: fused kernel for several row tiles, CTAs in clusters of two that
                                // take the two row blocks of each unit and share its W stages
                                // (tiles and tail tiles then count units of two row blocks)
     const CUtensorMap* tmY;    // Y in boxes of [128 rows][32 columns], 64-byte swizzle
                                // (used by the fused kernel for several row tiles)
-    // Fused kernel for several row tiles: the last tail_tiles tiles (those a
+    // Fused kernel for several row tiles, and the 256-row kernel: the last tail_tiles tiles (those a
     // whole wave of CTAs would leave mostly idle) are cut along K into
     // tail_pieces pieces of tail_kbp k-blocks, one per CTA, and reduced
     // through global memory.  0 tail tiles: every tile is whole.

@@ -551,6 +551,17 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 __device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+// acc + lo^2, then + hi^2, for the two bf16 halves of w: fp32 fused
+// multiply-adds with bf16 multiplicands (the mixed-precision form of fma,
+// whose operands widen exactly), the same values as fmaf on bf16lo/bf16hi
+// without unpacking the halves first.
+__device__ __forceinline__ float fma_sq_bf16x2(uint32_t w, float acc) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\t"
+        "fma.rn.f32.bf16 %0, l, l, %0;\n\tfma.rn.f32.bf16 %0, h, h, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(w));
+    return acc;
+}
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
