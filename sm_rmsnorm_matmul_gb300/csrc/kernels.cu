@@ -703,17 +703,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 // 32 columns (128 rows x 64 bf16 each).
 constexpr int kTaXStages = 4;
 constexpr int kTaWStages = 4;
+// Paired: a CTA's W slot holds half a stage (16 KB); the same 192 KB then
+// hold six X slots and six W half-slots.
+constexpr int kTaXStagesPair = 6;
+constexpr int kTaWStagesPair = 6;
 constexpr int kTaAStages = 8;
 constexpr uint32_t kTaXBytes = kRowsBM * kBK * 2;    // 16 KB
 constexpr uint32_t kTaStageOut = kRowsBM * 32 * 2;   // 8 KB: 128 rows x 32 bf16 of Y
 constexpr uint32_t kTaOffX = 0;
 constexpr uint32_t kTaOffW = kTaOffX + kTaXStages * kTaXBytes;
+constexpr uint32_t kTaOffWPair = kTaOffX + kTaXStagesPair * kTaXBytes;
 constexpr uint32_t kTaOffOut = kTaOffW + kTaWStages * kRowsWBytes;   // 2 staging buffers
+static_assert(kTaOffWPair + kTaWStagesPair * (kRowsWBytes / 2) == kTaOffOut, "paired rings fill the same memory");
 constexpr uint32_t kTaOffG = kTaOffOut + 2 * kTaStageOut;
-constexpr uint32_t kTaOffBar = kTaOffG + kTaXStages * kGBytes;
+constexpr uint32_t kTaOffBar = kTaOffG + kTaXStagesPair * kGBytes;
 // xfull, xempty, wfull, wempty, afull, aempty, accfull, accempty, srfull[2], srempty[2],
 // mmadone, episync
-constexpr uint32_t kTaNumBars = 2 * kTaXStages + 2 * kTaWStages + 2 * kTaAStages + 8;
+constexpr uint32_t kTaNumBars = 2 * kTaXStagesPair + 2 * kTaWStagesPair + 2 * kTaAStages + 8;
 constexpr uint32_t kTaOffSr = kTaOffBar + ((kTaNumBars * 8 + 15) / 16) * 16;
 constexpr uint32_t kTaOffRr = kTaOffSr + 2 * kRowsBM * 4;    // 1/rms of a piece's rows
 constexpr uint32_t kTaOffMisc = kTaOffRr + kRowsBM * 4;
@@ -761,13 +767,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     const uint32_t sb = smem_u32(smem);
-    const uint32_t sx = sb + kTaOffX, sw = sb + kTaOffW, sg = sb + kTaOffG;
+    // rings: X, W (paired: half stages), A (tensor memory)
+    constexpr int kXSt = kPair ? kTaXStagesPair : kTaXStages;
+    constexpr int kWSt = kPair ? kTaWStagesPair : kTaWStages;
+    constexpr uint32_t kWSlot = kPair ? kRowsWBytes / 2 : kRowsWBytes;
+    const uint32_t sx = sb + kTaOffX, sw = sb + (kPair ? kTaOffWPair : kTaOffW), sg = sb + kTaOffG;
     const uint32_t bar0 = sb + kTaOffBar;
     uint32_t nb_ = 0;
-    const uint32_t xfull0 = bar0 + 8 * nb_; nb_ += kTaXStages;
-    const uint32_t xempty0 = bar0 + 8 * nb_; nb_ += kTaXStages;
-    const uint32_t wfull0 = bar0 + 8 * nb_; nb_ += kTaWStages;
-    const uint32_t wempty0 = bar0 + 8 * nb_; nb_ += kTaWStages;
+    const uint32_t xfull0 = bar0 + 8 * nb_; nb_ += kTaXStagesPair;
+    const uint32_t xempty0 = bar0 + 8 * nb_; nb_ += kTaXStagesPair;
+    const uint32_t wfull0 = bar0 + 8 * nb_; nb_ += kTaWStagesPair;
+    const uint32_t wempty0 = bar0 + 8 * nb_; nb_ += kTaWStagesPair;
     const uint32_t afull0 = bar0 + 8 * nb_; nb_ += kTaAStages;
     const uint32_t aempty0 = bar0 + 8 * nb_; nb_ += kTaAStages;
     const uint32_t accfull = bar0 + 8 * nb_++;
@@ -782,21 +792,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort = reinterpret_cast<volatile int*>(smem + kTaOffMisc + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Paired: launched as clusters of two, or not at all (a launch without
+    // them reports an internal error and does no work: no cluster or
+    // tensor-memory operation may run, the pair allocation least of all).
+    if (kPair) {
+        uint32_t nct;
+        asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(nct));
+        if (nct != 2 || a.tail_tiles != 0) {
+            if (threadIdx.x == 0) atomicCAS(&g_status, 0, kStatusInternal);
+            return;
+        }
+    }
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kTaXStages; ++s) {
+        for (int s = 0; s < kXSt; ++s) {
             mbar_init(xfull0 + 8 * s, 1);
             mbar_init(xempty0 + 8 * s, 4);
         }
-        for (int s = 0; s < kTaWStages; ++s) {
+        for (int s = 0; s < kWSt; ++s) {
             mbar_init(wfull0 + 8 * s, 1);
-            mbar_init(wempty0 + 8 * s, kPair ? 2 : 1);   // paired: both CTAs' MMAs read the slot
+            mbar_init(wempty0 + 8 * s, 1);
         }
         for (int s = 0; s < kTaAStages; ++s) {
-            mbar_init(afull0 + 8 * s, 4);
+            // paired, rank 0: the k-block's one "ready" barrier for the MMA: this CTA's W
+            // copies (one arrival and their bytes), its four transform warps and rank 1's signal
+            mbar_init(afull0 + 8 * s, kPair && cluster_ctarank() == 0 ? 6 : 4);
             mbar_init(aempty0 + 8 * s, 1);
         }
         mbar_init(accfull, 1);
-        mbar_init(accempty, 4);
+        mbar_init(accempty, kPair ? 8 : 4);   // paired: both CTAs' epilogue warps release it
         for (int b = 0; b < 2; ++b) {
             mbar_init(srfull0 + 8 * b, 4);
             mbar_init(srempty0 + 8 * b, 4);
@@ -814,29 +837,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmY);
     }
     if (warp == 2) {
-        tmem_alloc(smem_u32(tmem_holder), 512);
-        tmem_relinquish();
+        if constexpr (kPair) {
+            tmem_alloc_pair(smem_u32(tmem_holder), 512);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_holder), 512);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // Paired: launched as clusters of two, or not at all (a launch without
-    // them reports an internal error and does no work: no cluster operation
-    // may run).
-    if (kPair) {
-        uint32_t nct;
-        asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(nct));
-        if (nct != 2 || a.tail_tiles != 0) {
-            if (threadIdx.x == 0) atomicCAS(&g_status, 0, kStatusInternal);
-            if (warp == 2) {
-                tc_fence_after();
-                tmem_dealloc(*tmem_holder, 512);
-            }
-            return;
-        }
-        // the peer's barriers exist before any copy or commit targets them
-        cluster_sync_all();
-    }
+    // paired: the peer's barriers exist before any signal or commit targets them
+    if (kPair) cluster_sync_all();
     // Set-up above overlaps the previous kernel on the stream; its writes are
     // visible after grid_dep_wait().  The next kernel may then be scheduled.
     // With the adapter the previous kernel is the launch that computes T,
@@ -848,8 +861,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) grid_dep_launch();
     const uint32_t tmem = *tmem_holder;
     // Paired (kPair): the two CTAs of a cluster take the two row blocks of each
-    // unit and share its W stages, each loading half of every stage's boxes
-    // multicast to both.  Units are counted in pairs of row blocks.
+    // unit (256 x 256) as one pair MMA of M = 256: each loads its own X rows
+    // and half of every W stage (columns [128 rank, 128 rank + 128) of the
+    // tile) and keeps its rows' A slots and accumulator in its own tensor
+    // memory; rank 0 issues the MMAs once its own stage and rank 1's (which
+    // rank 1's MMA warp signals) are ready.  Per 128 x 256 x 64 of work a CTA
+    // takes in 32 KB (its X rows and half a W stage) instead of 48 KB.  Units
+    // are counted in pairs of row blocks.
     constexpr int kC = kPair ? 2 : 1;
     const int rank = kPair ? static_cast<int>(cluster_ctarank()) : 0;
     const int m_units = (a.m_tiles + kC - 1) / kC;
@@ -871,7 +889,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // loads W, warp 3 loads X and g.
         if (lane == 0) {
             const bool load_x = warp == 3;
-            Ring ring(load_x ? kTaXStages : kTaWStages);
+            Ring ring(load_x ? kXSt : kWSt);
+            Ring rr(kTaAStages);   // paired, rank 0, W: the k-block's ready barrier (its A slot's)
             uint32_t issued = 0;
             const uint32_t full0 = load_x ? xfull0 : wfull0, empty0 = load_x ? xempty0 : wempty0;
             bool ok = true;
@@ -883,7 +902,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int n0 = nb * kOutBN;
                 for (int kb = un.kb0; kb < un.kb1 + (kLora ? un.extra : 0); ++kb) {
                     const bool ext = kLora && kb >= un.kb1;   // the adapter stages: T (hi, lo) and B
-                    if (!mbar_wait(empty0 + 8 * ring.idx, ring.phase ^ 1, abort)) { ok = false; break; }
+                    // (paired: rank 0's commit releases W slots in both CTAs)
+                    if (!(kPair && !load_x ? mbar_wait_cluster(empty0 + 8 * ring.idx, ring.phase ^ 1, abort)
+                                           : mbar_wait(empty0 + 8 * ring.idx, ring.phase ^ 1, abort))) {
+                        ok = false;
+                        break;
+                    }
                     const uint32_t f = full0 + 8 * ring.idx;
                     if (kLora && ext && load_x) grid_dep_wait();   // T is the previous launch's output
                     if (load_x) {
@@ -892,68 +916,128 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            (ext ? kb - un.kb1 : kb) * kBK, mb * kRowsBM);
                         if (!ext) tma_load_1d(sg + ring.idx * kGBytes, &tmG, f, kb * kBK);
                     } else if constexpr (kPair) {
-                        // this CTA's two of the stage's (up to) four boxes, to both CTAs
-                        const uint32_t bytes = w_stage_bytes<false, false>(n0, a.N);
-                        mbar_arrive_expect_tx(f, bytes);
-                        const int nbox = static_cast<int>(bytes / kWBoxBytes);
-                        for (int j = 2 * rank; j < 2 * rank + 2 && j < nbox; ++j)
-                            tma_load_2d_mc(sw + ring.idx * kRowsWBytes + j * kWBoxBytes, &tmW, f, n0 + 64 * j,
-                                           kb * kBK, 0x3);
+                        // this CTA's half of the stage: columns n0 + 128 rank + [0, 128), the boxes inside N;
+                        // rank 0's copies complete on the k-block's ready barrier (its A slot's)
+                        const int c0 = n0 + 128 * rank;
+                        const int nbox = c0 >= a.N ? 0 : min(2, (a.N - c0 + 63) / 64);
+                        const uint32_t fw = rank == 0 ? afull0 + 8 * rr.idx : f;
+                        mbar_arrive_expect_tx(fw, static_cast<uint32_t>(nbox) * kWBoxBytes);
+                        for (int j = 0; j < nbox; ++j)
+                            tma_load_2d_nohint(sw + ring.idx * kWSlot + j * kWBoxBytes, &tmW, fw, c0 + 64 * j,
+                                               kb * kBK);
                     } else {
                         mbar_arrive_expect_tx(f, w_stage_bytes<kGlu, kWnk>(n0, a.N));
                         load_w_stage<kGlu, kWnk>(sw + ring.idx * kRowsWBytes, ext ? &tmB : &tmW, f, n0,
                                                  ext ? 0 : kb, a.N, Nout);
                     }
                     ring.advance();
+                    rr.advance();
                     ++issued;
                 }
             }
-            // never leave with copies still landing in shared memory
+            // never leave with copies still landing in shared memory (paired,
+            // rank 0's W: they complete on the ready barriers)
+            const bool on_ready = kPair && !load_x && rank == 0;
+            const uint32_t tn = on_ready ? rr.n : ring.n, tfull0 = on_ready ? afull0 : full0;
+            for (uint32_t i = issued > tn ? issued - tn : 0; i < issued; ++i)
+                mbar_wait_teardown(tfull0 + 8 * (i % tn), (i / tn) & 1);
             const uint32_t n = ring.n;
-            for (uint32_t i = issued > n ? issued - n : 0; i < issued; ++i)
-                mbar_wait_teardown(full0 + 8 * (i % n), (i / n) & 1);
-            // Paired: the MMAs of both CTAs release every W slot in both CTAs
-            // (commit multicast), and those arrivals land asynchronously.
-            // Wait until the last use of each slot has been released by both,
-            // so that after the exit barrier no arrival is still in flight
-            // towards the peer (or from it into this CTA).
+            // Paired: rank 0's MMAs release every W slot of both CTAs (commit
+            // multicast), and those arrivals land asynchronously.  Wait until
+            // the last use of each slot has been released, so that after the
+            // exit barrier no arrival is still in flight towards this CTA.
             if (kPair && !load_x)
                 for (uint32_t i = issued > n ? issued - n : 0; i < issued; ++i)
                     mbar_wait_teardown(empty0 + 8 * (i % n), (i / n) & 1);
         }
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            // the hi/lo output (N <= 64) multiplies one 64-column box of W, not a 256-wide padded tile
-            constexpr uint32_t idesc = idesc_bf16_f32(kRowsBM, kHilo ? kBK : kRowsBN, false, !kWnk);
-            Ring wr(kTaWStages), ar(kTaAStages);
-            uint32_t tl = 0;
-            bool ok = true;
-            TaUnit un;
-            for (int i = 0; ok && ta_unit<kC>(a, i, un); ++i, ++tl) {
-                if (!mbar_wait(accempty, (tl & 1) ^ 1, abort)) break;
-                tc_fence_after();
-                const uint32_t d = tmem + kTaAccCol;
-                for (int kb = un.kb0; kb < un.kb1 + (kLora ? un.extra : 0); ++kb) {
-                    if (!mbar_wait(wfull0 + 8 * wr.idx, wr.phase, abort)) { ok = false; break; }
-                    if (!mbar_wait(afull0 + 8 * ar.idx, ar.phase, abort)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t a0 = tmem + kTaACol + ar.idx * 32;
-                    const uint32_t b0 = sw + wr.idx * kRowsWBytes;
-#pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        mma_bf16_ts(d, a0 + kk * 8, w_desc<kWnk>(b0, kk), idesc, kb != un.kb0 || kk != 0);
-                    if constexpr (kPair) mma_commit_mc(wempty0 + 8 * wr.idx, 0x3);   // both CTAs' slots
-                    else mma_commit(wempty0 + 8 * wr.idx);
-                    mma_commit(aempty0 + 8 * ar.idx);
-                    wr.advance();
-                    ar.advance();
+        if constexpr (kPair) {
+            if (rank == 1) {
+                // ------------------------------------------------ paired, rank 1: stage-ready signals
+                // Each k-block's W half and A slot of this CTA, once in place, are
+                // announced on rank 0's ready barrier of the k-block (its A slot's).
+                if (lane == 0) {
+                    Ring wr(kWSt), ar(kTaAStages);
+                    const uint32_t ready_r0 = mapa_shared(afull0, 0);
+                    bool ok = true;
+                    TaUnit un;
+                    for (int i = 0; ok && ta_unit<kC>(a, i, un); ++i) {
+                        for (int kb = un.kb0; kb < un.kb1; ++kb) {
+                            if (!mbar_wait(wfull0 + 8 * wr.idx, wr.phase, abort)) { ok = false; break; }
+                            if (!mbar_wait(afull0 + 8 * ar.idx, ar.phase, abort)) { ok = false; break; }
+                            mbar_arrive_remote_relaxed(ready_r0 + 8 * ar.idx);
+                            wr.advance();
+                            ar.advance();
+                        }
+                    }
                 }
-                if (!ok) break;
-                mma_commit(accfull);
+            } else {
+                // ------------------------------------------------ paired, rank 0: pair MMA issuer
+                if (lane == 0) {
+                    constexpr uint32_t idesc = idesc_bf16_f32(2 * kRowsBM, kRowsBN, false, true);
+                    Ring wr(kWSt), ar(kTaAStages);
+                    uint32_t tl = 0;
+                    bool ok = true;
+                    TaUnit un;
+                    for (int i = 0; ok && ta_unit<kC>(a, i, un); ++i, ++tl) {
+                        // both CTAs' epilogues have read the accumulator
+                        if (!mbar_wait_cluster(accempty, (tl & 1) ^ 1, abort)) break;
+                        tc_fence_after();
+                        const uint32_t d = tmem + kTaAccCol;
+                        for (int kb = un.kb0; kb < un.kb1; ++kb) {
+                            // both CTAs' W halves and A slots of this k-block
+                            if (!mbar_wait_cluster(afull0 + 8 * ar.idx, ar.phase, abort)) { ok = false; break; }
+                            tc_fence_after();
+                            const uint32_t a0 = tmem + kTaACol + ar.idx * 32;
+                            const uint32_t b0 = sw + wr.idx * kWSlot;
+#pragma unroll
+                            for (int kk = 0; kk < kBK / 16; ++kk)
+                                mma_bf16_ts_pair(d, a0 + kk * 8, w_desc<false>(b0, kk), idesc, kb != un.kb0 || kk != 0);
+                            mma_commit_pair_mc(wempty0 + 8 * wr.idx, 0x3);   // both CTAs' W halves
+                            mma_commit_pair_mc(aempty0 + 8 * ar.idx, 0x3);   // both CTAs' A slots
+                            wr.advance();
+                            ar.advance();
+                        }
+                        if (!ok) break;
+                        mma_commit_pair_mc(accfull, 0x3);
+                    }
+                    mma_commit_pair_mc(mmadone, 0x1);
+                    mbar_wait_teardown(mmadone, 0);
+                }
             }
-            mma_commit(mmadone);
-            mbar_wait_teardown(mmadone, 0);
+        } else {
+            // ------------------------------------------------ MMA issuer
+            if (lane == 0) {
+                // the hi/lo output (N <= 64) multiplies one 64-column box of W, not a 256-wide padded tile
+                constexpr uint32_t idesc = idesc_bf16_f32(kRowsBM, kHilo ? kBK : kRowsBN, false, !kWnk);
+                Ring wr(kTaWStages), ar(kTaAStages);
+                uint32_t tl = 0;
+                bool ok = true;
+                TaUnit un;
+                for (int i = 0; ok && ta_unit<kC>(a, i, un); ++i, ++tl) {
+                    if (!mbar_wait(accempty, (tl & 1) ^ 1, abort)) break;
+                    tc_fence_after();
+                    const uint32_t d = tmem + kTaAccCol;
+                    for (int kb = un.kb0; kb < un.kb1 + (kLora ? un.extra : 0); ++kb) {
+                        if (!mbar_wait(wfull0 + 8 * wr.idx, wr.phase, abort)) { ok = false; break; }
+                        if (!mbar_wait(afull0 + 8 * ar.idx, ar.phase, abort)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t a0 = tmem + kTaACol + ar.idx * 32;
+                        const uint32_t b0 = sw + wr.idx * kRowsWBytes;
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            mma_bf16_ts(d, a0 + kk * 8, w_desc<kWnk>(b0, kk), idesc, kb != un.kb0 || kk != 0);
+                        mma_commit(wempty0 + 8 * wr.idx);
+                        mma_commit(aempty0 + 8 * ar.idx);
+                        wr.advance();
+                        ar.advance();
+                    }
+                    if (!ok) break;
+                    mma_commit(accfull);
+                }
+                mma_commit(mmadone);
+                mbar_wait_teardown(mmadone, 0);
+            }
         }
     } else if (warp >= 4 && warp < 8) {
         // ------------------------------------------------ transform: X*g -> tensor memory
@@ -962,8 +1046,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t xrow = static_cast<uint32_t>(row) * 128;
         const uint32_t swz = static_cast<uint32_t>(row & 7);
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-        Ring xr(kTaXStages), ar(kTaAStages);
-        uint32_t tl = 0;
+        Ring xr(kXSt), ar(kTaAStages);
+        uint32_t tl = 0, a_used = 0;
         bool ok = true;
         TaUnit un;
         for (int i = 0; ok && ta_unit<kC>(a, i, un); ++i, ++tl) {
@@ -1014,18 +1098,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < 8; ++c) xv[c] = lds128(sx + xr.idx * kTaXBytes + xrow + ((c ^ swz) << 4));
                 }
-                if (!warp_wait(aempty0 + 8 * ar.idx, ar.phase ^ 1, abort)) { ok = false; break; }
+                // (paired: rank 0's commit releases A slots in both CTAs)
+                if (!(kPair ? warp_wait_cluster(aempty0 + 8 * ar.idx, ar.phase ^ 1, abort)
+                            : warp_wait(aempty0 + 8 * ar.idx, ar.phase ^ 1, abort))) {
+                    ok = false;
+                    break;
+                }
                 tmem_st_32x32(tmem + kTaACol + ar.idx * 32 + lane_base, out);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(afull0 + 8 * ar.idx);
                 ar.advance();
+                ++a_used;
             }
             if (!ok) break;
             sr[buf * kRowsBM + row] = ((ssp[0] + ssp[1]) + (ssp[2] + ssp[3])) +
                                       ((ssp[4] + ssp[5]) + (ssp[6] + ssp[7]));
             __syncwarp();
             if (lane == 0) mbar_arrive(srfull0 + 8 * buf);
+        }
+        // Paired: the commits that release the last use of each A slot land
+        // asynchronously; wait for them, so that after the exit barrier no
+        // arrival is still in flight towards this CTA.
+        if (kPair && warp == 4 && lane == 0) {
+            const uint32_t n = ar.n;
+            for (uint32_t i = a_used > n ? a_used - n : 0; i < a_used; ++i)
+                mbar_wait_teardown(aempty0 + 8 * (i % n), (i / n) & 1);
         }
     } else if (warp >= 8) {
         // ------------------------------------------------ epilogue
@@ -1050,7 +1148,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         TaUnit un;
         for (int i = 0; ta_unit<kC>(a, i, un); ++i, ++tl) {
             const uint32_t buf = tl & 1, use = tl >> 1;
-            if (!warp_wait(accfull, tl & 1, abort)) break;
+            // (paired: rank 0's commit signals both CTAs)
+            if (!(kPair ? warp_wait_cluster(accfull, tl & 1, abort) : warp_wait(accfull, tl & 1, abort))) break;
             if (!warp_wait(srfull0 + 8 * buf, use & 1, abort)) break;
             tc_fence_after();
             const float ss_row = sr[buf * kRowsBM + row];
@@ -1214,7 +1313,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(accempty);   // the MMA may start the next tile
+            // the MMA may start the next tile (paired: rank 0's, once both CTAs' epilogues are here)
+            if (lane == 0) {
+                if constexpr (kPair) mbar_arrive_remote(mapa_shared(accempty, 0));
+                else mbar_arrive(accempty);
+            }
             bool ok = true;
             const int nstore = hilo ? 2 * kBK : Nout;   // columns of Y
 #pragma unroll
@@ -1246,11 +1349,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    // paired: the peer may still copy or commit into this CTA until it is done
+    // paired: the peer may still signal this CTA, or rank 0's MMAs read this
+    // CTA's memory, until it is done
     if (kPair) cluster_sync_all();
     if (warp == 2) {
         tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        if constexpr (kPair) tmem_dealloc_pair(tmem, 512);
+        else tmem_dealloc(tmem, 512);
     }
 }
 

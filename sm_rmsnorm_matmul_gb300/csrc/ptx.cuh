@@ -124,6 +124,24 @@ __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity,
     return __all_sync(0xffffffffu, ok);
 }
 
+// mbar_wait for one thread, with acquire semantics at cluster scope (a
+// barrier that a peer CTA of the cluster, or a multicast commit, arrives on).
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i)
+            if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer() - t0 > wait_limit_ns(abort)) {
+            atomicCAS(&g_status, 0, kStatusTimeout);
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
 // Global-memory flag with acquire semantics at GPU scope.
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
     int v;
@@ -174,6 +192,17 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 }
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+// As mbar_arrive_remote without the release: for a signal whose data is
+// already complete in memory when the arriving thread decides to arrive (it
+// has waited for the local barrier that the data's own writes completed:
+// a TMA copy's transaction count, or tensor-memory stores followed by
+// tcgen05.wait::st), read only by the tensor core after the waiter's
+// tcgen05.fence::after_thread_sync.  On GB300 the release form cost about
+// 1,600 cycles per arrive on a busy SM.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");
 }
 __device__ __forceinline__ void st_dsmem_f32(uint32_t cluster_addr, float v) {
@@ -398,6 +427,45 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+// ---- The pair MMA (cta_group::2): the two CTAs of a cluster of two compute
+// one M = 256 tile, rows 0-127 from CTA rank 0 and 128-255 from rank 1 (A
+// and the accumulator in each CTA's tensor memory at the same address), B
+// split along N (the first half from rank 0's shared memory, the second
+// from rank 1's, at the same offset).  Rank 0 issues the MMAs and commits.
+// Every tensor-memory allocation, MMA and commit of a kernel that uses it
+// carries cta_group::2; allocation and deallocation are done by one warp in
+// each of the two CTAs together.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void mma_bf16_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrives on the mbarrier at offset bar of the CTAs in mask once the pair
+// MMAs issued so far have completed.
+__device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"(mask)
         : "memory");
 }
 
