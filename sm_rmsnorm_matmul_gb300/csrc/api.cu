@@ -490,11 +490,16 @@ int pair_clusters(int dev) {
 }
 
 // Launch shape of the fused kernel for several row tiles: its units, the K
-// split of its last units, and whether it runs paired (clusters of two CTAs
-// sharing W, for the plain form).  Paired only where clusters of two can be
-// resident and the units need no K-split tail: a launch that is both a
-// cluster launch and cooperative is not used (two such launches faulted the
-// GPU when replayed under the profiler, though none did otherwise).
+// split of its last units, and whether it runs paired (clusters of two CTAs,
+// one pair MMA per 256-row unit, for the plain form).  The paired kernel
+// never cuts units along K: a launch that is both a cluster launch and
+// cooperative is not used (two such launches faulted the GPU when replayed
+// under the profiler, though none did otherwise).  It is chosen where clusters
+// of two can be resident and either its units need no K-split tail or at
+// most a fifth of its cluster-rounds would sit idle in the last round (on
+// GB300 a paired round is ~7% shorter than the 128-row kernel's wave, and the
+// K-split tail costs more than that: 4096 x 4096 x 6144, six paired rounds
+// of which the last is 5% busy, 158 us against 163 us with the tail cut).
 struct TaPlan {
     bool pair;
     int kc;        // CTAs per slot
@@ -511,7 +516,10 @@ TaPlan plan_ta(int dev, const RowsPlan& p, const DeviceInfo& d, bool plain) {
         t.kc = 2;
         t.units = ((p.m_tiles + 1) / 2) * p.n_tiles;
         t.tail = plan_tail(t.units, std::min(t.units, clusters), p.k_blocks, clusters);
-        if (t.tail.tiles == 0) {
+        const int rounds = (t.units + clusters - 1) / clusters;
+        if (t.tail.tiles == 0 || 5 * t.units >= 4 * rounds * clusters) {
+            t.tail = TailPlan{};
+            t.tail.grid = std::min(t.units, clusters);
             t.ctas = t.tail.grid * 2;
             return t;
         }

@@ -69,7 +69,7 @@ CASES = [
     ("decode_qkv_16x4096x6144", 0, False),
     ((16, 8192, 1024), 0, True),                   # small-M path, K cut into pieces
     ("decode_gatedmlp_64x4096x28672", 0, False),   # row-tile kernel, whole tiles
-    ("prefill_qkv_4096x4096x6144", 0, True),      # 8 tail tiles cut into 16 K pieces
+    ("prefill_qkv_4096x4096x6144", 0, False),     # paired CTAs, whole units
     ((1280, 1024, 4096), 0, True),                 # 8 tail tiles
     ((1200, 1000, 4104), 0, True),                 # 18 tail tiles, partial row, column and K blocks
     ("tiny_8x1024x1024", 1, False),                # row-tile kernel, K split inside a cluster
