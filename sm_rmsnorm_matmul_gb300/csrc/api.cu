@@ -723,7 +723,7 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
     } else if (fused && !p.cluster && p.xrows == rmm::kRowsBM) {
         if (!map_2d_store(&tmY, Y, M, hilo ? 2 * kBK : glu ? N / 2 : N)) return RMM_ERR_INTERNAL;
         a.tmY = &tmY;
-        const TaPlan tp = plan_ta(dev, p, d, !glu && !wnk && !lora && !hilo);
+        const TaPlan tp = plan_ta(dev, p, d, !glu && !wnk && !hilo);   // (paired: plain or with the adapter)
         const TailPlan& t = tp.tail;
         a.pair = tp.pair ? 1 : 0;
         a.grid = tp.ctas;

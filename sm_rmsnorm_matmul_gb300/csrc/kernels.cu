@@ -872,7 +872,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rank = kPair ? static_cast<int>(cluster_ctarank()) : 0;
     const int m_units = (a.m_tiles + kC - 1) / kC;
     const int num_tiles = m_units * a.n_tiles;
-    static_assert(!kPair || (!kGlu && !kWnk && !kLora && !kHilo), "the paired form is the plain one");
+    static_assert(!kPair || (!kGlu && !kWnk && !kHilo), "the paired form is the plain one, with or without the adapter");
     // Output columns: N, or F = N / 2 for the gated form, whose tile covers
     // 128 output columns read from gate columns n0.. and up columns F + n0..
     const int Nout = kGlu ? a.N / 2 : a.N;
@@ -918,13 +918,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else if constexpr (kPair) {
                         // this CTA's half of the stage: columns n0 + 128 rank + [0, 128), the boxes inside N;
                         // rank 0's copies complete on the k-block's ready barrier (its A slot's)
+                        // (adapter stages: the same columns of B's rows)
                         const int c0 = n0 + 128 * rank;
                         const int nbox = c0 >= a.N ? 0 : min(2, (a.N - c0 + 63) / 64);
                         const uint32_t fw = rank == 0 ? afull0 + 8 * rr.idx : f;
                         mbar_arrive_expect_tx(fw, static_cast<uint32_t>(nbox) * kWBoxBytes);
                         for (int j = 0; j < nbox; ++j)
-                            tma_load_2d_nohint(sw + ring.idx * kWSlot + j * kWBoxBytes, &tmW, fw, c0 + 64 * j,
-                                               kb * kBK);
+                            tma_load_2d_nohint(sw + ring.idx * kWSlot + j * kWBoxBytes, ext ? &tmB : &tmW, fw,
+                                               c0 + 64 * j, ext ? 0 : kb * kBK);
                     } else {
                         mbar_arrive_expect_tx(f, w_stage_bytes<kGlu, kWnk>(n0, a.N));
                         load_w_stage<kGlu, kWnk>(sw + ring.idx * kRowsWBytes, ext ? &tmB : &tmW, f, n0,
@@ -962,7 +963,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bool ok = true;
                     TaUnit un;
                     for (int i = 0; ok && ta_unit<kC>(a, i, un); ++i) {
-                        for (int kb = un.kb0; kb < un.kb1; ++kb) {
+                        for (int kb = un.kb0; kb < un.kb1 + (kLora ? un.extra : 0); ++kb) {
                             if (!mbar_wait(wfull0 + 8 * wr.idx, wr.phase, abort)) { ok = false; break; }
                             if (!mbar_wait(afull0 + 8 * ar.idx, ar.phase, abort)) { ok = false; break; }
                             mbar_arrive_remote_relaxed(ready_r0 + 8 * ar.idx);
@@ -984,7 +985,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!mbar_wait_cluster(accempty, (tl & 1) ^ 1, abort)) break;
                         tc_fence_after();
                         const uint32_t d = tmem + kTaAccCol;
-                        for (int kb = un.kb0; kb < un.kb1; ++kb) {
+                        for (int kb = un.kb0; kb < un.kb1 + (kLora ? un.extra : 0); ++kb) {
                             // both CTAs' W halves and A slots of this k-block
                             if (!mbar_wait_cluster(afull0 + 8 * ar.idx, ar.phase, abort)) { ok = false; break; }
                             tc_fence_after();
@@ -1869,8 +1870,9 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
         const bool hilo = a.hilo != 0;
         if (hilo && (glu || wnk || lora)) return cudaErrorInvalidValue;
         const bool pair = a.pair != 0;
-        if (pair && (hilo || glu || wnk || lora)) return cudaErrorInvalidValue;
-        auto ta = pair ? rows_ta_kernel<false, false, false, false, true>
+        if (pair && (hilo || glu || wnk)) return cudaErrorInvalidValue;
+        auto ta = pair ? (lora ? rows_ta_kernel<false, false, true, false, true>
+                               : rows_ta_kernel<false, false, false, false, true>)
                 : hilo ? rows_ta_kernel<false, false, false, true, false>
                 : lora ? rows_ta_kernel<false, false, true, false, false>
                 : wnk  ? (glu ? rows_ta_kernel<true, true, false, false, false>
@@ -1878,7 +1880,7 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
                        : (glu ? rows_ta_kernel<true, false, false, false, false>
                               : rows_ta_kernel<false, false, false, false, false>);
         cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(ta),
-                                         pair ? 20 : hilo ? 19 : lora ? 18 : wnk ? (glu ? 15 : 14) : (glu ? 9 : 6));
+                                         pair ? (lora ? 23 : 20) : hilo ? 19 : lora ? 18 : wnk ? (glu ? 15 : 14) : (glu ? 9 : 6));
         if (e != cudaSuccess) return e;
         // The pieces of a tail tile wait for one another: launched as a
         // cooperative grid, every CTA is resident at once (or the launch

@@ -153,6 +153,20 @@ def test_tail_tiles_with_another_stream_holding_sms(rmm):
     assert_close(Y.cpu(), oracle.rmsnorm_matmul(X, g, W, 1e-6), f"{M}x{K}x{N} beside another stream")
 
 
+# The paired kernel (two CTAs, one pair MMA per 256-row unit) on ragged units:
+# the last unit's second row block past M, and a last column tile whose
+# second half (rank 1's W columns) lies wholly past N.
+@pytest.mark.parametrize("M,K,N", [(2432, 520, 3840), (3840, 1024, 1152)])
+def test_paired_ragged_units(rmm, M, K, N):
+    from sm_rmsnorm_matmul_gb300 import inputs
+    p = rmm.describe_plan(M, K, N)
+    assert p["splits"] == 1 and p["cluster"] == 0 and p["grid"] % 2 == 0
+    X, g, W = inputs.random_problem(M, K, N, seed=M + K + N, x_kind="row_scaled")
+    Y = run_fused(rmm, X, g, W, 1e-5)
+    assert_close(Y, oracle.rmsnorm_matmul(X, g, W, 1e-5), f"{M}x{K}x{N} paired")
+    assert torch.equal(Y, run_fused(rmm, X, g, W, 1e-5))
+
+
 @pytest.mark.parametrize("M,K,N", [(2048, 512, 3840),    # paired CTAs, whole tiles
                                    (1280, 1024, 4096)])   # tail tiles cut along K (cooperative)
 def test_prefill_calls_replayed_from_a_cuda_graph(rmm, M, K, N):
@@ -286,6 +300,7 @@ LORA = [
     (300, 520, 264, 24),     # several row tiles, ragged
     (4096, 4096, 6144, 64),  # prefill QKV shape (the benchmark's adapter line): T's launch cut along K
     (20000, 1024, 512, 56),  # 157 row tiles for T's launch: whole tiles (TMA stores) and a K-cut tail
+    (2432, 520, 3840, 40),   # paired main kernel: 19 row blocks (the last unit's second past M), ragged K
 ]
 
 
