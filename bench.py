@@ -583,7 +583,7 @@ def main():
     if args.workload in inputs.ATTENTION_WORKLOADS:
         # one attention line alone (profiling and quick checks)
         return run_attention_only(args, inputs.ATTENTION_WORKLOADS[args.workload], rank)
-    w = inputs.WORKLOADS[args.workload]
+    w = inputs.WORKLOADS[args.workload] if args.workload in inputs.WORKLOADS else inputs.PROFILE_CASES[args.workload]
 
     if args.impl == "reference":
         return run_reference(args, w, ws, rank)

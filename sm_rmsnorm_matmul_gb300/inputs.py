@@ -74,6 +74,20 @@ WORKLOADS = {
 
 WORKLOAD_ORDER = list(WORKLOADS)
 
+# Small cases of the prefill kernels, for profiler captures that replay a
+# launch many times (inputs still larger than L2, a few hundred MB on the
+# device).  `bench.py --workload` accepts them; no benchmark line uses them.
+PROFILE_CASES = {
+    w.name: w
+    for w in (
+        # paired kernel: 19 row-block pairs x 4 column tiles = 76 units, one round;
+        # the unfused pair times the 256-row kernel on it
+        Workload("paired_prefill_4864x8192x1024", 4864, 8192, 1024, 1e-5, 5, 1.0 / math.sqrt(8192)),
+        # the 256-row kernel of the unfused pair: 16 x 16 = 256 whole tiles, two waves
+        Workload("unfused_prefill_4096x8192x4096", 4096, 8192, 4096, 1e-5, 6, 1.0 / math.sqrt(8192)),
+    )
+}
+
 
 def sample_rows(M: int, count: int = 256) -> list[int]:
     """Rows r_i = 64*i + (i mod 64) clipped to [0, M), plus the last row.
