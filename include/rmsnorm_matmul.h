@@ -87,6 +87,11 @@ typedef enum {
  *    another, so such a launch is cooperative: all its CTAs (at most one per
  *    SM) are resident at once, or the launch fails with RMM_ERR_LAUNCH (for
  *    example on a device partition with fewer SMs than the device reports).
+ *    Where clusters of two fit and the 256-row units of a tile pair need no
+ *    such cut (or leave at most a fifth of their rounds idle), the two CTAs
+ *    of a cluster instead compute each 256 x 256 unit together as one MMA of
+ *    M = 256 (tcgen05 cta_group::2), each loading half of every W stage;
+ *    units are never cut along K there.
  * The workspace is allocated on first use of a shape that needs it (make that
  * first call outside any CUDA-graph capture).
  * Returns an rmm_status.
@@ -165,7 +170,9 @@ int rmsnorm(const void* X, const void* g, void* Xn,
 /*
  * Unfused MatMul alone (the second kernel of that pair):
  *   C[m,n] = bf16( sum_k A[m,k] * B[k,n] ),  A [M,K], B [K,N], C [M,N] bf16,
- * fp32 accumulation on the tensor cores.  Same validation rules.
+ * fp32 accumulation on the tensor cores.  Same validation rules.  From 512
+ * rows of A up it runs tiles of 256 rows (two M = 128 MMAs sharing each B
+ * stage), the last tiles cut along K as above.
  */
 int matmul(const void* A, const void* B, void* C,
            int64_t M, int64_t K, int64_t N, cudaStream_t stream);
@@ -256,7 +263,10 @@ int rmsnorm_matmul_noalloc(const void* X, const void* g, const void* W, void* Y,
  * size, pipeline stages, padded rows MP, column tiles, k-blocks per split.
  * For the fused kernel over several row tiles, the K splits and k-blocks per
  * split are those of its tail tiles (1 split: every tile whole), and splits
- * without a cluster mean partial sums in the workspace.  The plan described is
+ * without a cluster mean partial sums in the workspace (the grid counts CTAs:
+ * twice the clusters when the tile pairs run as pair MMAs).  For matmul()
+ * from 512 rows up (fused = 0), padded rows 256 and 3 stages mark the 256-row
+ * kernel, whose column tiles count 256-row tiles.  The plan described is
  * rmsnorm_matmul()'s, which rmsnorm_matmul_noalloc() runs too.
  * Queries device attributes; launches nothing.
  */
