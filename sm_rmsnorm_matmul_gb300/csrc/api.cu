@@ -699,7 +699,7 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
         if (t.tiles > 0) {
             constexpr size_t kPieceBytes = static_cast<size_t>(rmm::kTtBM) * rmm::kRowsBN * sizeof(float);
             const size_t pieces = static_cast<size_t>(t.tiles) * t.pieces;
-            const size_t ss_bytes = pieces * rmm::kTtBM * sizeof(float);
+            const size_t ss_bytes = 0;   // (unfused: no row sums)
             const size_t ncount = static_cast<size_t>(t.tiles) * 2;
             if (fixed) {
                 if (!fixed->place(pieces * kPieceBytes, ss_bytes, &a.ws_acc, &a.ws_ss) ||

@@ -1361,50 +1361,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------- tall tiles: 256 rows per CTA
-// The kernel for many row tiles (prefill-like shapes) of the plain form:
-// each CTA computes a tile of 256 rows (two halves of 128, one M = 128 MMA
-// each) by 256 columns, so that every W stage it loads feeds both halves.
-// Per 128 x 256 x 64 of work a CTA then takes in 32 KB (16 KB of X, half of
-// a 32 KB W stage) instead of the 48 KB of a 128-row tile, and on GB300 the
-// operand delivery into each SM, not the tensor pipe, bounds the 128-row
-// kernels (the tensor pipe is active about half the time there while shared
-// memory is far from busy).  The two accumulators fill tensor memory
-// (2 x 256 columns), so the MMA reads A from shared memory: in the fused form
-// the transform warps multiply each X stage by g in place, one row per
-// thread, before the MMAs read it.  X, g and W of a k-block share one stage,
-// which the MMAs' commit releases.  Warps: 0 TMA producer, 1 MMA issuer,
-// 2 tensor-memory allocation, 4-11 transform and epilogue (warps 4-7 the
-// first half's rows, 8-11 the second's; each thread keeps its row from the
-// transform, with the row's sum of squares in registers, to the epilogue).
-// Tiles and tail pieces are those of the 128-row kernel with 256-row tiles.
-constexpr int kTtLook = 2;   // k-blocks of the next tile transformed before an epilogue
+// The unfused contraction for many row tiles (prefill-like shapes): each CTA
+// computes a tile of 256 rows (two halves of 128, one M = 128 MMA each) by
+// 256 columns, so that every W stage it loads feeds both halves.  Per
+// 128 x 256 x 64 of work a CTA then takes in 32 KB (16 KB of A, half of a
+// 32 KB W stage) instead of the 48 KB of a 128-row tile; on GB300 the operand
+// delivery into each SM, not the tensor pipe, bounds the 128-row kernels.
+// The two accumulators fill tensor memory (2 x 256 columns) and the MMAs read
+// A from shared memory as the copy wrote it; A and W of a k-block share one
+// stage, which the MMAs' commit releases.  (The fused form would have to
+// multiply each A stage by g in place first, which holds the stage through
+// that transform: measured slower than the 128-row fused kernel.)  Warps:
+// 0 TMA producer, 1 MMA issuer, 2 tensor-memory allocation, 4-11 epilogue
+// (warps 4-7 the first half's rows, 8-11 the second's).  Tiles and tail
+// pieces are those of the 128-row kernel with 256-row tiles.
 constexpr uint32_t kTtXBytes = kTtBM * kBK * 2;               // 32 KB
-constexpr uint32_t kTtStageBytes = kTtXBytes + kRowsWBytes;   // 64 KB: X, then W
-constexpr uint32_t kTtOutBytes = kRowsBM * 32 * 2;            // 8 KB: 128 rows x 32 bf16 of Y
+constexpr uint32_t kTtStageBytes = kTtXBytes + kRowsWBytes;   // 64 KB: A, then W
+constexpr uint32_t kTtOutBytes = kRowsBM * 32 * 2;            // 8 KB: 128 rows x 32 bf16 of C
 constexpr uint32_t kTtOffOut = kTtStages * kTtStageBytes;     // two staging buffers per half
-constexpr uint32_t kTtOffG = kTtOffOut + 4 * kTtOutBytes;
-constexpr uint32_t kTtOffBar = kTtOffG + kTtStages * kGBytes;
-// full, ready, empty per stage; accfull, accempty, mmadone, episync[2], tailsync
-constexpr uint32_t kTtNumBars = 3 * kTtStages + 6;
-constexpr uint32_t kTtOffRr = kTtOffBar + ((kTtNumBars * 8 + 15) / 16) * 16;   // 1/rms of a piece's rows
-constexpr uint32_t kTtOffMisc = kTtOffRr + kTtBM * 4;
+constexpr uint32_t kTtOffBar = kTtOffOut + 4 * kTtOutBytes;
+// full, empty per stage; accfull, accempty, mmadone, episync[2], tailsync
+constexpr uint32_t kTtNumBars = 2 * kTtStages + 6;
+constexpr uint32_t kTtOffMisc = kTtOffBar + ((kTtNumBars * 8 + 15) / 16) * 16;
 constexpr uint32_t kTtSmem = kTtOffMisc + 16 + 1024;
 static_assert(kTtSmem <= 232448, "the tall-tile kernel's shared memory exceeds the opt-in limit");
 
-template <bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
     tall_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmY,
-                __nv_bfloat16* __restrict__ Y, RowsLaunch a) {
+                const __grid_constant__ CUtensorMap tmY, __nv_bfloat16* __restrict__ Y, RowsLaunch a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     const uint32_t sb = smem_u32(smem);
-    const uint32_t sg = sb + kTtOffG, sout = sb + kTtOffOut;
+    const uint32_t sout = sb + kTtOffOut;
     const uint32_t bar0 = sb + kTtOffBar;
-    const uint32_t full0 = bar0, ready0 = bar0 + 8 * kTtStages, empty0 = bar0 + 16 * kTtStages;
-    const uint32_t accfull = bar0 + 24 * kTtStages, accempty = accfull + 8, mmadone = accfull + 16;
+    const uint32_t full0 = bar0, empty0 = bar0 + 8 * kTtStages;
+    const uint32_t accfull = bar0 + 16 * kTtStages, accempty = accfull + 8, mmadone = accfull + 16;
     const uint32_t episync0 = accfull + 24, tailsync = accfull + 40;
-    float* rr = reinterpret_cast<float*>(smem + kTtOffRr);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kTtOffMisc);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + kTtOffMisc + 4);
 
@@ -1412,7 +1404,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTtStages; ++s) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(ready0 + 8 * s, 8);
             mbar_init(empty0 + 8 * s, 1);
         }
         mbar_init(accfull, 1);
@@ -1428,7 +1419,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmX);
         prefetch_tmap(&tmW);
-        if (kFused) prefetch_tmap(&tmG);
         prefetch_tmap(&tmY);
     }
     if (warp == 2) {
@@ -1461,12 +1451,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!mbar_wait(empty0 + 8 * ring.idx, ring.phase ^ 1, abort)) { ok = false; break; }
                     const uint32_t f = full0 + 8 * ring.idx;
                     const uint32_t st = sb + ring.idx * kTtStageBytes;
-                    mbar_arrive_expect_tx(f, kTtXBytes + wbytes + (kFused ? kGBytes : 0u));
+                    mbar_arrive_expect_tx(f, kTtXBytes + wbytes);
                     // two boxes of 128 rows (a box past M reads zeros)
                     tma_load_2d_nohint(st, &tmX, f, kb * kBK, mb * kTtBM);
                     tma_load_2d_nohint(st + kTtXBytes / 2, &tmX, f, kb * kBK, mb * kTtBM + kRowsBM);
                     load_w_stage<false, false>(st + kTtXBytes, &tmW, f, n0, kb, a.N, a.N);
-                    if (kFused) tma_load_1d(sg + ring.idx * kGBytes, &tmG, f, kb * kBK);
                     ring.advance();
                     ++issued;
                 }
@@ -1488,8 +1477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(accempty, (tl & 1) ^ 1, abort)) break;
                 tc_fence_after();
                 for (int kb = un.kb0; kb < un.kb1; ++kb) {
-                    // fused: the stage once the transform has applied g; plain: once it has landed
-                    if (!mbar_wait((kFused ? ready0 : full0) + 8 * ring.idx, ring.phase, abort)) { ok = false; break; }
+                    if (!mbar_wait(full0 + 8 * ring.idx, ring.phase, abort)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t st = sb + ring.idx * kTtStageBytes;
 #pragma unroll
@@ -1508,16 +1496,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait_teardown(mmadone, 0);
         }
     } else if (warp >= 4) {
-        // ------------------------------------------------ transform and epilogue
+        // ------------------------------------------------ epilogue
+        // Read this thread's accumulator row (bf16) into registers and
+        // release tensor memory at once; then store C through the half's two
+        // 8 KB staging buffers with TMA stores (64-byte swizzle: the 16-byte
+        // chunk j of row r sits at chunk j ^ ((r >> 1) & 3)), overlapped with
+        // the next tile's main loop.
         const int hh = (warp - 4) >> 2;                // half of the tile
         const int q = warp & 3;                        // lane quarter this warp may access
         const int rh = q * 32 + lane;                  // row within the half (tensor-memory lane)
         const int row = hh * kRowsBM + rh;             // row of the tile
         const int et = threadIdx.x - 128;              // 0..255
-        const uint32_t xrow = static_cast<uint32_t>(row) * 128;
-        const uint32_t swz = static_cast<uint32_t>(row & 7);
         const uint32_t taddr = tmem + hh * kRowsBN + (static_cast<uint32_t>(q * 32) << 16);
-        const float inv_k = 1.f / static_cast<float>(a.K);
         const uint32_t episync = episync0 + 8 * hh;
         uint32_t ep = 0, tp = 0;
         // the four warps of this half; all eight warps
@@ -1533,23 +1523,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         const uint32_t rswz = static_cast<uint32_t>((rh >> 1) & 3);
         uint32_t chunks = 0;   // staging buffer uses so far (per half)
-        // Epilogue of one tile: wait for its accumulators, read this thread's
-        // accumulator row (scaled, bf16) into registers and release tensor
-        // memory at once; then store Y through the half's two 8 KB staging
-        // buffers with TMA stores (64-byte swizzle: the 16-byte chunk j of
-        // row r sits at chunk j ^ ((r >> 1) & 3)).  ss: the row's sum of
-        // squares over the tile's k-blocks.
-        auto epilogue = [&](const TaUnit& un, uint32_t tl, float ss) -> bool {
-            if (!warp_wait(accfull, tl & 1, abort)) return false;
+        uint32_t tl = 0;
+        TaUnit un;
+        for (int i = 0; ta_unit<1>(a, i, un); ++i, ++tl) {
+            if (!warp_wait(accfull, tl & 1, abort)) break;
             tc_fence_after();
             int mb, nb;
             rows_tile_coords(un.t, a.m_tiles, a.n_tiles, mb, nb);
             const int n0 = nb * kRowsBN, m0 = mb * kTtBM;
             if (un.piece >= 0) {
-                // A K piece of a tail tile: publish the fp32 partial and the
-                // partial row sums of squares, wait for the tile's other
-                // pieces, then reduce rows [r0, r1) of the tile over all
-                // pieces in piece order and write them to Y.
+                // A K piece of a tail tile: publish the fp32 partial, wait for
+                // the tile's other pieces, then reduce rows [r0, r1) of the
+                // tile over all pieces in piece order and write them to C.
                 const int P = a.tail_pieces;
                 const int tail = un.t - (num_tiles - a.tail_tiles);
                 const size_t slot = static_cast<size_t>(tail) * P;
@@ -1564,7 +1549,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
                                            __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])));
                 }
-                __stcg(a.ws_ss + (slot + un.piece) * kTtBM + row, ss);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(accempty);
@@ -1577,12 +1561,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ok = all_sync() && ok && !*abort;
                 const int r0 = (un.piece * kTtBM) / P, r1 = ((un.piece + 1) * kTtBM) / P;
-                if (ok && et < r1 - r0) {
-                    float tot = 0.f;
-                    for (int p2 = 0; p2 < P; ++p2) tot += __ldcg(a.ws_ss + (slot + p2) * kTtBM + r0 + et);
-                    rr[et] = kFused ? rsqrtf(tot * inv_k + a.eps) : 1.f;
-                }
-                ok = all_sync() && ok;
                 // items: 4 output columns of one row
                 const int items = (r1 - r0) * (kRowsBN / 4);
                 for (int it = et; ok && it < items; it += 256) {
@@ -1614,10 +1592,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         acc.w += t4.w;
                     }
                     if (m < a.M && n0 + col < a.N) {
-                        const float r = rr[rl];
                         uint2 o;
-                        o.x = pack_bf16x2(acc.x * r, acc.y * r);
-                        o.y = pack_bf16x2(acc.z * r, acc.w * r);
+                        o.x = pack_bf16x2(acc.x, acc.y);
+                        o.y = pack_bf16x2(acc.z, acc.w);
                         *reinterpret_cast<uint2*>(Y + static_cast<size_t>(m) * a.N + n0 + col) = o;
                     }
                 }
@@ -1627,17 +1604,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     atomicExch(cnt, 0);
                     atomicExch(cnt + 1, 0);
                 }
-                return ok;
+                if (!ok) break;
+                continue;
             }
-            const float r = kFused ? rsqrtf(ss * inv_k + a.eps) : 1.f;
             uint32_t pk[kRowsBN / 2];   // the row's outputs, packed as bf16x2
 #pragma unroll
             for (int c = 0; c < kRowsBN / 16; ++c) {
                 uint32_t v[16];
                 tmem_ld_32x16(taddr + c * 16, v);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    pk[c * 8 + i] = pack_bf16x2(__uint_as_float(v[2 * i]) * r, __uint_as_float(v[2 * i + 1]) * r);
+                for (int j = 0; j < 8; ++j)
+                    pk[c * 8 + j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
             }
             tc_fence_before();
             __syncwarp();
@@ -1666,71 +1643,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++chunks;
                 }
             }
-            return ok;
-        };
-
-        uint32_t it = 0, tl = 0;   // k-blocks so far (the stage ring's position); tiles so far
-        bool ok = true;
-        bool pend = false;         // a tile whose epilogue has not run yet
-        TaUnit pun{};
-        uint32_t ptl = 0;
-        float pss = 0.f;
-        TaUnit un{};
-        // One pass per tile and a last one without k-blocks; the pending
-        // epilogue runs after kTtLook k-blocks of the next tile, or at the end
-        // of a shorter one (a single call site, inlined once).
-        for (int i = 0;; ++i) {
-            const bool have = ok && ta_unit<1>(a, i, un);
-            const int kb1 = have ? un.kb1 : 0;
-            float ssp[8];   // independent partial sums: no long dependency chain
-#pragma unroll
-            for (int c = 0; c < 8; ++c) ssp[c] = 0.f;
-            int done = 0;
-            for (int kb = have ? un.kb0 : 0;;) {
-                if (pend && (done == kTtLook || kb == kb1)) {
-                    pend = false;
-                    if (!(ok = epilogue(pun, ptl, pss))) break;
-                    continue;
-                }
-                if (kb == kb1) break;
-                if constexpr (kFused) {
-                    // X*g in place, rounded to bf16, and the row's sum of squares
-                    const uint32_t s = it % kTtStages;
-                    if (!warp_wait(full0 + 8 * s, (it / kTtStages) & 1, abort)) { ok = false; break; }
-                    const uint32_t xa = sb + s * kTtStageBytes + xrow;
-                    const uint32_t gt = sg + s * kGBytes;
-                    uint4 xv[8];
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) xv[c] = lds128(xa + ((c ^ swz) << 4));
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint4 gv = lds128(gt + c * 16);
-                        const uint32_t xw[4] = {xv[c].x, xv[c].y, xv[c].z, xv[c].w};
-                        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-                        uint32_t o[4];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            ssp[c] = fma_sq_bf16x2(xw[u], ssp[c]);
-                            o[u] = mul_bf16x2(xw[u], gw[u]);
-                        }
-                        sts128(xa + ((c ^ swz) << 4), make_uint4(o[0], o[1], o[2], o[3]));
-                    }
-                    // the MMA (async proxy) reads what these threads wrote
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(ready0 + 8 * s);
-                }
-                ++kb;
-                ++it;
-                ++done;
-            }
-            if (!have || !ok) break;
-            pend = true;
-            pun = un;
-            ptl = tl++;
-            pss = ((ssp[0] + ssp[1]) + (ssp[2] + ssp[3])) + ((ssp[4] + ssp[5]) + (ssp[6] + ssp[7]));
+            if (!ok) break;
         }
-        if (rh == 0) bulk_wait_group_all();   // Y is written before the CTA exits
+        if (rh == 0) bulk_wait_group_all();   // C is written before the CTA exits
     }
 
     tc_fence_before();
@@ -1857,12 +1772,11 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
     if ((glu || wnk || lora) && !fused) return cudaErrorInvalidValue;
     if (lora && (glu || wnk)) return cudaErrorInvalidValue;
     if (a.tall) {
-        if (glu || wnk || lora || a.hilo || a.unscaled || split) return cudaErrorInvalidValue;
-        auto tk = fused ? tall_kernel<true> : tall_kernel<false>;
-        cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(tk), fused ? 21 : 22);
+        if (fused || glu || wnk || lora || a.hilo || a.unscaled || split) return cudaErrorInvalidValue;
+        cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(tall_kernel), 22);
         if (e != cudaSuccess) return e;
         // cooperative with tail pieces, as the 128-row kernel
-        e = launch_ex(tk, a.grid, kTtSmem, 1, s, a.tail_tiles > 0, tmX, tmW, fused ? tmG : tmX, *a.tmY, y, a);
+        e = launch_ex(tall_kernel, a.grid, kTtSmem, 1, s, a.tail_tiles > 0, tmX, tmW, *a.tmY, y, a);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }

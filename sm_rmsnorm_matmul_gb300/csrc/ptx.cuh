@@ -342,16 +342,6 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src,
         : "memory");
 }
 
-// Prefetch a 2-D box into L2 (no shared memory, no completion).  Reads that
-// follow still go through L2, which stays coherent with any later writer, so
-// a prefetch can never make a reader see stale data.
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* m, int c0, int c1) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(m)),
-                 "r"(c0), "r"(c1)
-                 : "memory");
-}
-
 // 2-D tiled store smem -> global (clipped to the tensor's bounds); completes
 // as part of this thread's current bulk group.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int c0, int c1) {
