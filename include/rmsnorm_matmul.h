@@ -203,8 +203,9 @@ int rmm_device_status(cudaStream_t stream);
  * fault).  wait_limit_ns > 0 sets the limit of every bounded in-kernel wait
  * (microsecond resolution, at most the 2 s default; 0 restores the default).
  * skip_sends != 0 makes the row-tile kernels' K-split reduction skip the
- * stores of its partials (and qknorm_attention's loader leave out its first
- * key/value stage), so that each waiting CTA's wait runs out:
+ * stores of its partials, the paired prefill kernel's second CTA leave out
+ * its first "stage ready" signal (and qknorm_attention's loader leave out its
+ * first key/value stage), so that each waiting CTA's wait runs out:
  * the kernel then records RMM_ERR_DEVICE_TIMEOUT, skips its remaining work,
  * frees its tensor memory and exits normally, and rmm_device_status() reports
  * it.  Both settings are process-wide host state, passed to every later

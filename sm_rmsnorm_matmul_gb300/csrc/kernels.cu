@@ -940,8 +940,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // rank 0's W: they complete on the ready barriers)
             const bool on_ready = kPair && !load_x && rank == 0;
             const uint32_t tn = on_ready ? rr.n : ring.n, tfull0 = on_ready ? afull0 : full0;
+            // (after a timed-out wait the rest are not waited for: an aborted launch stays short)
             for (uint32_t i = issued > tn ? issued - tn : 0; i < issued; ++i)
-                mbar_wait_teardown(tfull0 + 8 * (i % tn), (i / tn) & 1);
+                if (!mbar_wait_teardown(tfull0 + 8 * (i % tn), (i / tn) & 1)) break;
             const uint32_t n = ring.n;
             // Paired: rank 0's MMAs release every W slot of both CTAs (commit
             // multicast), and those arrivals land asynchronously.  Wait until
@@ -949,7 +950,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // exit barrier no arrival is still in flight towards this CTA.
             if (kPair && !load_x)
                 for (uint32_t i = issued > n ? issued - n : 0; i < issued; ++i)
-                    mbar_wait_teardown(empty0 + 8 * (i % n), (i / n) & 1);
+                    if (!mbar_wait_teardown(empty0 + 8 * (i % n), (i / n) & 1)) break;
         }
     } else if (warp == 1) {
         if constexpr (kPair) {
@@ -966,7 +967,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int kb = un.kb0; kb < un.kb1 + (kLora ? un.extra : 0); ++kb) {
                             if (!mbar_wait(wfull0 + 8 * wr.idx, wr.phase, abort)) { ok = false; break; }
                             if (!mbar_wait(afull0 + 8 * ar.idx, ar.phase, abort)) { ok = false; break; }
-                            mbar_arrive_remote_relaxed(ready_r0 + 8 * ar.idx);
+                            // (test hook: leave out the first signal, so that rank 0's wait runs out)
+                            if (!(a.test_skip_sends && i == 0 && kb == un.kb0))
+                                mbar_arrive_remote_relaxed(ready_r0 + 8 * ar.idx);
                             wr.advance();
                             ar.advance();
                         }
@@ -1124,7 +1127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kPair && warp == 4 && lane == 0) {
             const uint32_t n = ar.n;
             for (uint32_t i = a_used > n ? a_used - n : 0; i < a_used; ++i)
-                mbar_wait_teardown(aempty0 + 8 * (i % n), (i / n) & 1);
+                if (!mbar_wait_teardown(aempty0 + 8 * (i % n), (i / n) & 1)) break;
         }
     } else if (warp >= 8) {
         // ------------------------------------------------ epilogue

@@ -52,6 +52,33 @@ def test_timeout_is_reported_and_the_context_recovers(rmm):
     assert bad == 0, max_abs
 
 
+def test_paired_timeout_is_reported_and_the_context_recovers(rmm):
+    # the paired prefill kernel (one pair MMA per 256-row unit, two CTAs of a
+    # cluster): the second CTA leaves out its first "stage ready" signal, the
+    # first CTA's MMA issuer waits for it until the limit, and every role of
+    # both CTAs leaves its loop through its own bounded waits
+    from sm_rmsnorm_matmul_gb300 import inputs
+    M, K, N = 2048, 512, 3840
+    plan = rmm.describe_plan(M, K, N)
+    assert plan["splits"] == 1 and plan["grid"] % 2 == 0
+    X, g, W = inputs.random_problem(M, K, N, seed=37, x_kind="row_scaled")
+    Xd, gd, Wd = X.cuda(), g.cuda(), W.cuda()
+    l = rmm.lib()
+    assert rmm.device_status() == 0
+    assert l.rmm_test_hooks(1, 50_000_000) == 0
+    try:
+        rmm.rmsnorm_matmul(Xd, gd, Wd, 1e-6)
+        assert rmm.device_status() == 5                  # RMM_ERR_DEVICE_TIMEOUT
+    finally:
+        assert l.rmm_test_hooks(0, 0) == 0
+    Y = rmm.rmsnorm_matmul(Xd, gd, Wd, 1e-6)
+    torch.cuda.synchronize()
+    assert rmm.device_status() == 0
+    rows = list(range(0, M, 16))
+    bad, max_abs, _ = oracle.tolerance_violations(Y.cpu()[rows], oracle.rmsnorm_matmul(X[rows], g, W, 1e-6))
+    assert bad == 0, max_abs
+
+
 def test_hook_rejects_negative_limit(rmm):
     assert rmm.lib().rmm_test_hooks(0, -1) == 1
 
