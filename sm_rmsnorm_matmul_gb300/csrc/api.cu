@@ -723,7 +723,7 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
     } else if (fused && !p.cluster && p.xrows == rmm::kRowsBM) {
         if (!map_2d_store(&tmY, Y, M, hilo ? 2 * kBK : glu ? N / 2 : N)) return RMM_ERR_INTERNAL;
         a.tmY = &tmY;
-        const TaPlan tp = plan_ta(dev, p, d, !glu && !wnk && !hilo);   // (paired: plain or with the adapter)
+        const TaPlan tp = plan_ta(dev, p, d, !wnk && !hilo);   // (paired: plain, gated or with the adapter)
         const TailPlan& t = tp.tail;
         a.pair = tp.pair ? 1 : 0;
         a.grid = tp.ctas;
@@ -903,7 +903,7 @@ int rmm_describe_plan(int64_t M, int64_t K, int64_t N, int fused, int* info) {
             info[7] = t.tiles > 0 ? t.kbp : p.k_blocks;
         } else if (fused != 0 && !p.cluster && p.xrows == rmm::kRowsBM) {
             // the fused kernel for several row tiles: its grid and its tail tiles' K pieces
-            const TaPlan tp = plan_ta(dev, p, d, !glu);
+            const TaPlan tp = plan_ta(dev, p, d, true);
             info[3] = tp.ctas;
             if (tp.tail.tiles > 0) {
                 info[1] = tp.tail.pieces;

@@ -872,7 +872,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rank = kPair ? static_cast<int>(cluster_ctarank()) : 0;
     const int m_units = (a.m_tiles + kC - 1) / kC;
     const int num_tiles = m_units * a.n_tiles;
-    static_assert(!kPair || (!kGlu && !kWnk && !kHilo), "the paired form is the plain one, with or without the adapter");
+    static_assert(!kPair || (!kWnk && !kHilo), "the paired form is the [K, N] one: plain, gated or with the adapter");
     // Output columns: N, or F = N / 2 for the gated form, whose tile covers
     // 128 output columns read from gate columns n0.. and up columns F + n0..
     const int Nout = kGlu ? a.N / 2 : a.N;
@@ -918,9 +918,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else if constexpr (kPair) {
                         // this CTA's half of the stage: columns n0 + 128 rank + [0, 128), the boxes inside N;
                         // rank 0's copies complete on the k-block's ready barrier (its A slot's)
-                        // (adapter stages: the same columns of B's rows)
-                        const int c0 = n0 + 128 * rank;
-                        const int nbox = c0 >= a.N ? 0 : min(2, (a.N - c0 + 63) / 64);
+                        // (adapter stages: the same columns of B's rows; gated: rank 0 the
+                        // tile's gate columns, rank 1 its up columns, so that each CTA's
+                        // accumulator row holds both, as unpaired)
+                        const int c0 = kGlu ? (rank == 0 ? n0 : Nout + n0) : n0 + 128 * rank;
+                        const int nbox = kGlu ? 2 : c0 >= a.N ? 0 : min(2, (a.N - c0 + 63) / 64);
                         const uint32_t fw = rank == 0 ? afull0 + 8 * rr.idx : f;
                         mbar_arrive_expect_tx(fw, static_cast<uint32_t>(nbox) * kWBoxBytes);
                         for (int j = 0; j < nbox; ++j)
@@ -1787,8 +1789,9 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
         const bool hilo = a.hilo != 0;
         if (hilo && (glu || wnk || lora)) return cudaErrorInvalidValue;
         const bool pair = a.pair != 0;
-        if (pair && (hilo || glu || wnk)) return cudaErrorInvalidValue;
+        if (pair && (hilo || wnk)) return cudaErrorInvalidValue;
         auto ta = pair ? (lora ? rows_ta_kernel<false, false, true, false, true>
+                         : glu ? rows_ta_kernel<true, false, false, false, true>
                                : rows_ta_kernel<false, false, false, false, true>)
                 : hilo ? rows_ta_kernel<false, false, false, true, false>
                 : lora ? rows_ta_kernel<false, false, true, false, false>
@@ -1797,7 +1800,7 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
                        : (glu ? rows_ta_kernel<true, false, false, false, false>
                               : rows_ta_kernel<false, false, false, false, false>);
         cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(ta),
-                                         pair ? (lora ? 23 : 20) : hilo ? 19 : lora ? 18 : wnk ? (glu ? 15 : 14) : (glu ? 9 : 6));
+                                         pair ? (lora ? 23 : glu ? 21 : 20) : hilo ? 19 : lora ? 18 : wnk ? (glu ? 15 : 14) : (glu ? 9 : 6));
         if (e != cudaSuccess) return e;
         // The pieces of a tail tile wait for one another: launched as a
         // cooperative grid, every CTA is resident at once (or the launch

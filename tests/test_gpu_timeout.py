@@ -83,12 +83,14 @@ def test_hook_rejects_negative_limit(rmm):
     assert rmm.lib().rmm_test_hooks(0, -1) == 1
 
 
-def test_attention_timeout_is_reported_and_the_context_recovers(rmm):
+@pytest.mark.parametrize("D", [128, 64])
+def test_attention_timeout_is_reported_and_the_context_recovers(rmm, D):
     # the same hook makes the attention loader leave out its first key/value
     # stage: both MMA issuers' waits for it run out, every role leaves its
-    # loop, and the CTA frees its tensor memory and exits
+    # loop, and the CTA frees its tensor memory and exits (both head
+    # dimensions: each has its own kernel instantiation)
     from sm_rmsnorm_matmul_gb300 import inputs
-    B, S, Hq, Hkv, D = 1, 512, 4, 2, 128
+    B, S, Hq, Hkv = 1, 512, 4, 2
     qkv, gq, gk = inputs.attention_inputs(B, S, Hq, Hkv, D, seed=7)
     Qd, Kd, Vd = inputs.split_qkv(qkv.cuda(), B, S, Hq, Hkv, D)
     l = rmm.lib()
