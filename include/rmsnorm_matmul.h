@@ -258,8 +258,7 @@ int rmsnorm_matmul_noalloc(const void* X, const void* g, const void* W, void* Y,
  * Launch plan the library would use for this shape on the current device
  * (introspection for tests and benchmarks; `fused` = 1 for rmsnorm_matmul,
  * 0 for matmul, 2 for rmsnorm_matmul_swiglu, whose N is the width of W; the
- * plan described is that of weights stored [K, N]: with RMM_WEIGHT_NK the
- * fused prefill kernel runs unpaired, its tiles' K split planned alike).
+ * plan does not depend on RMM_WEIGHT_NK).
  * Fills info[0..7] with: path (1 row-tile, 2 small-M),
  * K splits, 1 if the splits reduce through a cluster's shared memory, grid
  * size, pipeline stages, padded rows MP, column tiles, k-blocks per split.

@@ -723,9 +723,11 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
     } else if (fused && !p.cluster && p.xrows == rmm::kRowsBM) {
         if (!map_2d_store(&tmY, Y, M, hilo ? 2 * kBK : glu ? N / 2 : N)) return RMM_ERR_INTERNAL;
         a.tmY = &tmY;
-        const TaPlan tp = plan_ta(dev, p, d, !wnk && !hilo);   // (paired: plain, gated or with the adapter)
+        const TaPlan tp = plan_ta(dev, p, d, !hilo);   // (paired: every form but T's hi/lo output)
         const TailPlan& t = tp.tail;
         a.pair = tp.pair ? 1 : 0;
+        // paired, weights stored [N, K]: each CTA loads boxes of 128 weight rows
+        if (tp.pair && wnk && !map_2d(&tmW, W, N, K, rmm::kRowsBN / 2)) return RMM_ERR_INTERNAL;
         a.grid = tp.ctas;
         if (t.tiles > 0) {
             const int rem = t.tiles * tp.kc, pieces = t.pieces;   // tail tiles

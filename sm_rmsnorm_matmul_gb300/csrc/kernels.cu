@@ -872,7 +872,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rank = kPair ? static_cast<int>(cluster_ctarank()) : 0;
     const int m_units = (a.m_tiles + kC - 1) / kC;
     const int num_tiles = m_units * a.n_tiles;
-    static_assert(!kPair || (!kWnk && !kHilo), "the paired form is the [K, N] one: plain, gated or with the adapter");
+    static_assert(!kPair || !kHilo, "the hi/lo output runs unpaired");
     // Output columns: N, or F = N / 2 for the gated form, whose tile covers
     // 128 output columns read from gate columns n0.. and up columns F + n0..
     const int Nout = kGlu ? a.N / 2 : a.N;
@@ -921,13 +921,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // (adapter stages: the same columns of B's rows; gated: rank 0 the
                         // tile's gate columns, rank 1 its up columns, so that each CTA's
                         // accumulator row holds both, as unpaired)
+                        // Weights stored [N, K]: one [128 n][64 k] box of those columns' rows,
+                        // K-major (the tensor map's box is 128 rows for paired launches).
                         const int c0 = kGlu ? (rank == 0 ? n0 : Nout + n0) : n0 + 128 * rank;
-                        const int nbox = kGlu ? 2 : c0 >= a.N ? 0 : min(2, (a.N - c0 + 63) / 64);
                         const uint32_t fw = rank == 0 ? afull0 + 8 * rr.idx : f;
-                        mbar_arrive_expect_tx(fw, static_cast<uint32_t>(nbox) * kWBoxBytes);
-                        for (int j = 0; j < nbox; ++j)
-                            tma_load_2d_nohint(sw + ring.idx * kWSlot + j * kWBoxBytes, ext ? &tmB : &tmW, fw,
-                                               c0 + 64 * j, ext ? 0 : kb * kBK);
+                        if constexpr (kWnk) {
+                            mbar_arrive_expect_tx(fw, kWSlot);
+                            tma_load_2d_nohint(sw + ring.idx * kWSlot, &tmW, fw, kb * kBK, c0);
+                        } else {
+                            const int nbox = kGlu ? 2 : c0 >= a.N ? 0 : min(2, (a.N - c0 + 63) / 64);
+                            mbar_arrive_expect_tx(fw, static_cast<uint32_t>(nbox) * kWBoxBytes);
+                            for (int j = 0; j < nbox; ++j)
+                                tma_load_2d_nohint(sw + ring.idx * kWSlot + j * kWBoxBytes, ext ? &tmB : &tmW, fw,
+                                                   c0 + 64 * j, ext ? 0 : kb * kBK);
+                        }
                     } else {
                         mbar_arrive_expect_tx(f, w_stage_bytes<kGlu, kWnk>(n0, a.N));
                         load_w_stage<kGlu, kWnk>(sw + ring.idx * kRowsWBytes, ext ? &tmB : &tmW, f, n0,
@@ -980,7 +987,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 // ------------------------------------------------ paired, rank 0: pair MMA issuer
                 if (lane == 0) {
-                    constexpr uint32_t idesc = idesc_bf16_f32(2 * kRowsBM, kRowsBN, false, true);
+                    constexpr uint32_t idesc = idesc_bf16_f32(2 * kRowsBM, kRowsBN, false, !kWnk);
                     Ring wr(kWSt), ar(kTaAStages);
                     uint32_t tl = 0;
                     bool ok = true;
@@ -998,7 +1005,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint32_t b0 = sw + wr.idx * kWSlot;
 #pragma unroll
                             for (int kk = 0; kk < kBK / 16; ++kk)
-                                mma_bf16_ts_pair(d, a0 + kk * 8, w_desc<false>(b0, kk), idesc, kb != un.kb0 || kk != 0);
+                                mma_bf16_ts_pair(d, a0 + kk * 8, w_desc<kWnk>(b0, kk), idesc, kb != un.kb0 || kk != 0);
                             mma_commit_pair_mc(wempty0 + 8 * wr.idx, 0x3);   // both CTAs' W halves
                             mma_commit_pair_mc(aempty0 + 8 * ar.idx, 0x3);   // both CTAs' A slots
                             wr.advance();
@@ -1712,7 +1719,7 @@ __global__ void __launch_bounds__(kNormThreads)
 // Raises a kernel's dynamic shared-memory limit to the device's opt-in
 // maximum, once per (kernel slot, device).
 cudaError_t ensure_smem_attr(const void* func, int slot) {
-    static int done[24][64] = {};
+    static int done[32][64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -1789,10 +1796,12 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
         const bool hilo = a.hilo != 0;
         if (hilo && (glu || wnk || lora)) return cudaErrorInvalidValue;
         const bool pair = a.pair != 0;
-        if (pair && (hilo || wnk)) return cudaErrorInvalidValue;
-        auto ta = pair ? (lora ? rows_ta_kernel<false, false, true, false, true>
-                         : glu ? rows_ta_kernel<true, false, false, false, true>
-                               : rows_ta_kernel<false, false, false, false, true>)
+        if (pair && hilo) return cudaErrorInvalidValue;
+        auto ta = pair ? (lora  ? rows_ta_kernel<false, false, true, false, true>
+                          : wnk ? (glu ? rows_ta_kernel<true, true, false, false, true>
+                                       : rows_ta_kernel<false, true, false, false, true>)
+                          : glu ? rows_ta_kernel<true, false, false, false, true>
+                                : rows_ta_kernel<false, false, false, false, true>)
                 : hilo ? rows_ta_kernel<false, false, false, true, false>
                 : lora ? rows_ta_kernel<false, false, true, false, false>
                 : wnk  ? (glu ? rows_ta_kernel<true, true, false, false, false>
@@ -1800,7 +1809,7 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
                        : (glu ? rows_ta_kernel<true, false, false, false, false>
                               : rows_ta_kernel<false, false, false, false, false>);
         cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(ta),
-                                         pair ? (lora ? 23 : glu ? 21 : 20) : hilo ? 19 : lora ? 18 : wnk ? (glu ? 15 : 14) : (glu ? 9 : 6));
+                                         pair ? (lora ? 23 : wnk ? (glu ? 25 : 24) : glu ? 21 : 20) : hilo ? 19 : lora ? 18 : wnk ? (glu ? 15 : 14) : (glu ? 9 : 6));
         if (e != cudaSuccess) return e;
         // The pieces of a tail tile wait for one another: launched as a
         // cooperative grid, every CTA is resident at once (or the launch

@@ -290,6 +290,27 @@ def test_weight_nk(rmm, M, K, N, gated):
         assert_close(Y.cpu(), oracle.rmsnorm_matmul(X, g, W, 1e-6), f"[N,K] {M}x{K}x{N}")
 
 
+# The paired prefill kernel with weights stored [N, K] (each CTA loads boxes
+# of 128 weight rows; gated: the gate rows in one CTA, the up rows in the
+# other): the same bits as the [K, N] layout, and the oracle at the plain
+# bound on unit-RMS outputs (millions of outputs: reading S25).
+@pytest.mark.parametrize("gated", [False, True])
+def test_weight_nk_paired(rmm, gated):
+    from sm_rmsnorm_matmul_gb300 import inputs
+    M, K, N = 2048, 520, 3840
+    X, g, W = inputs.random_problem(M, K, N, seed=11 + gated, x_kind="row_scaled")
+    Xd, gd = X.cuda(), g.cuda()
+    Y_nk = rmm.rmsnorm_matmul_ex(Xd, gd, W.t().contiguous().cuda(), 1e-6, weight_nk=True, gated=gated)
+    Y_kn = rmm.rmsnorm_matmul_ex(Xd, gd, W.cuda(), 1e-6, weight_nk=False, gated=gated)
+    torch.cuda.synchronize()
+    assert rmm.device_status() == 0
+    assert torch.equal(Y_nk, Y_kn)
+    if gated:
+        assert_gated_close(Y_nk.cpu(), X, g, W, 1e-6, f"[N,K] paired gated {M}x{K}x{N}")
+    else:
+        assert_close(Y_nk.cpu(), oracle.rmsnorm_matmul(X, g, W, 1e-6), f"[N,K] paired {M}x{K}x{N}")
+
+
 # ------------------------------------------------------- low-rank adapter
 # rmsnorm_matmul_lora: Y = RMSNorm(X) @ (W + A @ B), A [K,R], B [R,N].
 LORA = [
