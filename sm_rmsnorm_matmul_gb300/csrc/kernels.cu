@@ -198,7 +198,7 @@ __host__ __device__ inline RowsLayout rows_layout(int xrows, int stages, int red
     L.red_block = red_slots > 0 ? MP * (4 + rows_owned_max(red_slots, glu) * (glu ? 2 : 1) * 128) : 0;
     L.off_red = overlay ? 0 : ((L.off_g + stages * kGBytes + 15) / 16) * 16;
     L.off_bar = overlay ? ((L.off_g + stages * kGBytes + 15) / 16) * 16 : L.off_red + red_slots * L.red_block;
-    const uint32_t nbars = 3 * kRowsMaxStages + 10;
+    const uint32_t nbars = 4 * kRowsMaxStages + 10;
     L.off_sr = L.off_bar + ((nbars * 8 + 15) / 16) * 16;
     L.off_misc = L.off_sr + 2 * kRowsBM * 4;
     L.total = L.off_misc + 16 + 1024;
@@ -237,6 +237,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // with the receive blocks over the pipeline buffers: every other split's
     // buffers are idle, so its blocks may be stored
     const uint32_t redgo = bar0 + 8 * (3 * kRowsMaxStages + 9);
+    // fused: stage s's X tile and g slice have landed (its W lands on
+    // full(s)), so the transform of a stage runs while its W is still on
+    // the way, and the MMA waits for both
+    auto xland = [&](uint32_t s) { return bar0 + 8 * (3 * kRowsMaxStages + 10 + s); };
     float* sr = reinterpret_cast<float*>(smem + L.off_sr);         // [2][128] row sums of squares
     const uint32_t red_addr = sb + L.off_red;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.off_misc);
@@ -269,14 +273,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto lora_extra = [&](int sp) { return kLora && sp == 0 ? kLoraStages : 0; };
     // Loads of stage s = k-block kb of the unit whose tile starts at row block
     // mb and output column n0 (kb >= k_blocks: adapter stage kb - k_blocks).
+    // (Fused: X and g complete on xland(s), W on full(s).)
     auto issue = [&](uint32_t s, int kb, int mb, int n0) {
         const bool ext = kLora && kb >= a.k_blocks;
-        mbar_arrive_expect_tx(full(s), xbytes + w_stage_bytes<kGlu, kWnk>(n0, a.N) +
-                                           (kFused && !ext ? kGBytes : 0));
-        tma_load_2d_nohint(sx + s * xbytes, ext ? &tmT : &tmX, full(s), (ext ? kb - a.k_blocks : kb) * kBK,
+        const uint32_t xbar = kFused ? xland(s) : full(s);
+        if (kFused) {
+            mbar_arrive_expect_tx(xbar, xbytes + (!ext ? kGBytes : 0));
+            mbar_arrive_expect_tx(full(s), w_stage_bytes<kGlu, kWnk>(n0, a.N));
+        } else {
+            mbar_arrive_expect_tx(full(s), xbytes + w_stage_bytes<kGlu, kWnk>(n0, a.N));
+        }
+        tma_load_2d_nohint(sx + s * xbytes, ext ? &tmT : &tmX, xbar, (ext ? kb - a.k_blocks : kb) * kBK,
                            mb * kRowsBM);
+        if (kFused && !ext) tma_load_1d(sg + s * kGBytes, &tmG, xbar, kb * kBK);
         load_w_stage<kGlu, kWnk>(sw + s * kRowsWBytes, ext ? &tmB : &tmW, full(s), n0, ext ? 0 : kb, a.N, Nout);
-        if (kFused && !ext) tma_load_1d(sg + s * kGBytes, &tmG, full(s), kb * kBK);
     };
     // k-blocks of the first unit that thread 0 (the producer) issues before
     // the CTA-wide set-up barrier, as soon as its barriers exist and the
@@ -288,6 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(full(s), 1);
             mbar_init(xform(s), 4);   // one elected lane per transform warp
             mbar_init(empty(s), 1);
+            mbar_init(xland(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accfull(b), 1);
@@ -365,7 +376,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // never leave with copies still landing in shared memory
             const uint32_t pending = it < static_cast<uint32_t>(S) ? it : S;
-            for (uint32_t i = it - pending; i < it; ++i) mbar_wait_teardown(full(i % S), (i / S) & 1);
+            for (uint32_t i = it - pending; i < it; ++i) {
+                if (!mbar_wait_teardown(full(i % S), (i / S) & 1)) break;
+                if (kFused && !mbar_wait_teardown(xland(i % S), (i / S) & 1)) break;
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
@@ -384,7 +398,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int kend = kb1 + lora_extra(sp);
                 for (int kb = kb0; kb < kend; ++kb) {
                     const uint32_t s = ring.idx, ph = ring.phase;
-                    if (!mbar_wait(kFused ? xform(s) : full(s), ph, abort)) { ok = false; break; }
+                    if (!mbar_wait(full(s), ph, abort) || (kFused && !mbar_wait(xform(s), ph, abort))) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
                     const uint32_t a0 = sx + s * xbytes, b0 = sw + s * kRowsWBytes;
 #pragma unroll
@@ -426,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int kend = kb1 + lora_extra(sp);
                 for (int kb = kb0; kb < kend; ++kb) {
                     const uint32_t s = ring.idx, ph = ring.phase;
-                    if (!warp_wait(full(s), ph, abort)) { ok = false; break; }
+                    if (!warp_wait(xland(s), ph, abort)) { ok = false; break; }
                     if (!kLora || kb < kb1) {   // (the adapter stage needs no transform)
                         const uint4 gv = lds128(sg + s * kGBytes + kc * 16);
                         const uint32_t xt = sx + s * xbytes + swz_off;
@@ -525,12 +542,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // One (tile, split) unit per CTA, one row tile (M <= 128); the K
         // splits of the tile are the CTAs of this cluster.  Chunk c of 32
         // columns belongs to CTA c % splits.  Every warp takes part:
-        //  1. the warps of each tensor-memory lane quarter that holds rows
-        //     (three per quarter, taking every third chunk) read the
+        //  1. warps 4..11 of each tensor-memory lane quarter that holds rows
+        //     (two per quarter, taking every other chunk) read the
         //     accumulator and store each chunk straight from registers into
         //     its owner's receive block for this split (st.async; the bytes
         //     complete on the owner's redfull) or, for their own chunks, into
-        //     their own block; with it go the row sums of squares;
+        //     their own block; with it go the row sums of squares.  Warps 0
+        //     and 1 (producer, MMA) are left out: they reach this point last,
+        //     and their first cluster-barrier wait (~0.6 us even when every
+        //     peer has long arrived) would hold up the sends;
         //  2. once every split's block has arrived, all threads add the
         //     blocks in split order (fixed, whatever the arrival order),
         //     scale by 1/rms and write this CTA's chunks of Y.
@@ -565,13 +585,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   static_cast<uint32_t>((split - 1) * rows_here * (4 + owned * kUnitChunks * 128)));
         cluster_wait();    // the peers' barriers are initialised
         // 1. tensor memory -> owners
-        if (have && q * 32 < rows_here &&
+        const int wteam = team - 1;   // chunk team of warps 4..11
+        if (have && team >= 1 && q * 32 < rows_here &&
             warp_wait(accfull(0), 0, abort) && (!kFused || warp_wait(srfull(0), 0, abort)) &&
             (!a.red_overlay || [&] {
                 // The last MMA is done, so this CTA's pipeline buffers, which
                 // hold its receive blocks, are idle: tell the other splits,
                 // then wait until theirs are idle too.
-                if (threadIdx.x == 0)
+                if (threadIdx.x == 128)
                     for (int p = 0; p < split; ++p)
                         if (p != me) mbar_arrive_remote(mapa_shared(redgo, p));
                 return warp_wait_cluster(redgo, 0, abort);
@@ -579,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
             const uint32_t swz = static_cast<uint32_t>(row & 7);
-            for (int c = team; c < kRowsChunks; c += kThreads / 128) {
+            for (int c = wteam; c < kRowsChunks; c += 2) {
                 const int unit = kGlu ? (c & (kRowsChunks / 2 - 1)) : c, half = kGlu ? c / (kRowsChunks / 2) : 0;
                 if (unit >= nunits) continue;   // warp-uniform
                 uint32_t v[32];
@@ -603,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (team == 0 && row < rows_here) {
+            if (team == 1 && row < rows_here) {
                 const float ssv = kFused ? sr[row] : 0.f;
                 const uint32_t dst = my_block + row * 4;
                 *reinterpret_cast<float*>(smem + (dst - sb)) = ssv;
