@@ -80,7 +80,9 @@ typedef enum {
  *    and the row sum of squares computed in the same pass as the contraction,
  *    r[m] applied in the epilogue.  For M <= 128 the K range may be split over
  *    up to 8 CTAs of a thread-block cluster whose partial sums are combined in
- *    shared memory, in a fixed order.  For more row tiles, when the tiles
+ *    shared memory, in a fixed order; with a K split over at most 32 rows the
+ *    plain form may use 128-column tiles instead (twice the CTAs, half the
+ *    partial sums each exchanges).  For more row tiles, when the tiles
  *    leave a last wave of CTAs at most half full, those last tiles are cut
  *    along K, one piece per CTA, and the pieces are combined, in a fixed
  *    order, through the same workspace; the pieces of a tile wait for one
@@ -267,7 +269,9 @@ int rmsnorm_matmul_noalloc(const void* X, const void* g, const void* W, void* Y,
  * without a cluster mean partial sums in the workspace (the grid counts CTAs:
  * twice the clusters when the tile pairs run as pair MMAs).  For matmul()
  * from 512 rows up (fused = 0), padded rows 256 and 3 stages mark the 256-row
- * kernel, whose column tiles count 256-row tiles.  The plan described is
+ * kernel, whose column tiles count 256-row tiles; with a K split over at
+ * most 32 rows the column tiles may be 128 columns wide (then N / 128 of
+ * them, rounded up).  The plan described is
  * rmsnorm_matmul()'s, which rmsnorm_matmul_noalloc() runs too.
  * Queries device attributes; launches nothing.
  */

@@ -343,29 +343,31 @@ GemvPlan plan_gemv(int dev, bool fused, int64_t K, int64_t N, const DeviceInfo& 
 struct RowsPlan {
     int m_tiles, n_tiles, k_blocks, splits, kb_per_split, cluster, xrows, MP, stages, grid;
     int overlay;
+    int bn = rmm::kRowsBN;   // columns of a tile
 };
 
 int rows_stages(int xrows, int red_slots, int MP, const DeviceInfo& d, bool overlay = false,
-                bool glu = false) {
-    const size_t fixed = rmm::rows_smem_bytes(xrows, 0, red_slots, MP, overlay, glu);
-    const size_t per = rmm::rows_stage_bytes(xrows);
+                bool glu = false, int bn = rmm::kRowsBN) {
+    const size_t fixed = rmm::rows_smem_bytes(xrows, 0, red_slots, MP, overlay, glu, bn);
+    const size_t per = rmm::rows_stage_bytes(xrows, bn);
     const size_t avail = d.smem_optin > 0 ? static_cast<size_t>(d.smem_optin) : 227 * 1024;
     int st = avail > fixed ? static_cast<int>((avail - fixed) / per) : 0;
     st = std::min(rmm::kRowsMaxStages, st);
     // the X tiles are padded to 1 KB as a whole
-    while (st > 0 && rmm::rows_smem_bytes(xrows, st, red_slots, MP, overlay, glu) > avail) --st;
+    while (st > 0 && rmm::rows_smem_bytes(xrows, st, red_slots, MP, overlay, glu, bn) > avail) --st;
     return st;
 }
 
 std::mutex g_rows_occ_mu;
-std::map<std::tuple<int, bool, int, size_t, bool, bool, bool>, int> g_rows_occ;
+std::map<std::tuple<int, bool, int, size_t, bool, bool, bool, int>, int> g_rows_occ;
 
-int rows_max_clusters(int dev, bool fused, int splits, size_t smem, bool glu, bool wnk, bool lora) {
+int rows_max_clusters(int dev, bool fused, int splits, size_t smem, bool glu, bool wnk, bool lora,
+                      int bn = rmm::kRowsBN) {
     std::lock_guard<std::mutex> lk(g_rows_occ_mu);
-    auto key = std::make_tuple(dev, fused, splits, smem, glu, wnk, lora);
+    auto key = std::make_tuple(dev, fused, splits, smem, glu, wnk, lora, bn);
     auto it = g_rows_occ.find(key);
     if (it != g_rows_occ.end()) return it->second;
-    const int n = rmm::rows_max_active_clusters(fused, splits, smem, glu, wnk, lora);
+    const int n = rmm::rows_max_active_clusters(fused, splits, smem, glu, wnk, lora, bn);
     g_rows_occ[key] = n;
     return n;
 }
@@ -398,19 +400,30 @@ RowsPlan plan_rows(int dev, bool fused, int64_t M, int64_t K, int64_t N, const D
     p.xrows = p.MP;
     double best = 1e300;
     const double w_total = static_cast<double>(K) * N * 2;
-    for (int s = 1; s <= rmm::kClusterMaxSplits && s <= p.k_blocks; ++s) {
+    // Tiles of 256 columns, or (plain [K, N] form, K split, at most 32 rows)
+    // of 128: twice the CTAs for a K split, and half the partial sums each
+    // CTA exchanges; with more rows the X tile, loaded again for every W
+    // stage, would grow to the size of the stage's W.  (Measured: 8 x 1024 x
+    // 1024 5.30 -> 4.72 us; 16 x 4096 x 6144 keeps 256 columns, as three
+    // splits of 48 tiles do not fit as clusters, and two splits took 17.3 us
+    // against 11.7: a CTA streams W at ~55-60 GB/s whatever its stage count.)
+    for (int bn : {rmm::kRowsBN, rmm::kRowsBN / 2}) {
+    const bool narrow = bn != rmm::kRowsBN;
+    if (narrow && (glu || wnk || lora || p.MP > 32)) continue;
+    const int n_tiles = glu ? static_cast<int>((N / 2 + bn / 2 - 1) / (bn / 2)) : static_cast<int>((N + bn - 1) / bn);
+    for (int s = narrow ? 2 : 1; s <= rmm::kClusterMaxSplits && s <= p.k_blocks; ++s) {
         const int kbps = (p.k_blocks + s - 1) / s;
         if ((p.k_blocks + kbps - 1) / kbps != s) continue;
         const int red_slots = s > 1 ? s : 0;
-        int st = rows_stages(p.xrows, red_slots, p.MP, d, false, glu);
+        int st = rows_stages(p.xrows, red_slots, p.MP, d, false, glu, bn);
         // A receive area of its own that leaves fewer than 3 stages: put the
         // receive blocks over the pipeline buffers instead.  The extra
         // handshake measured ~0.5 us, more than going from 3 to 5 stages
         // bought (M = 64), less than going from 2 stages or none (M > 64).
         bool overlay = false;
         if (s > 1 && st < 3) {
-            const int so = rows_stages(p.xrows, red_slots, p.MP, d, true, glu);
-            if (so > st && so >= 2 && rmm::rows_overlay_fits(p.xrows, so, s, p.MP, glu)) {
+            const int so = rows_stages(p.xrows, red_slots, p.MP, d, true, glu, bn);
+            if (so > st && so >= 2 && rmm::rows_overlay_fits(p.xrows, so, s, p.MP, glu, bn)) {
                 st = so;
                 overlay = true;
             }
@@ -419,17 +432,19 @@ RowsPlan plan_rows(int dev, bool fused, int64_t M, int64_t K, int64_t N, const D
         int resident = sms;
         if (s > 1) {
             resident = rows_max_clusters(dev, fused, s,
-                                         rmm::rows_smem_bytes(p.xrows, st, red_slots, p.MP, overlay, glu),
-                                         glu, wnk, lora) * s;
+                                         rmm::rows_smem_bytes(p.xrows, st, red_slots, p.MP, overlay, glu, bn),
+                                         glu, wnk, lora, bn) * s;
             if (resident <= 0) continue;
         }
-        const long units = static_cast<long>(p.n_tiles) * s;
+        const long units = static_cast<long>(n_tiles) * s;
         // a K split runs one (tile, split) unit per CTA, all resident at once
         if (s > 1 && units > resident) continue;
         const long waves = (units + resident - 1) / resident;
-        const double per_cta = static_cast<double>(waves) * kbps * rmm::kRowsBN * kBK * 2 / 55e9;
-        const double cost = std::max(per_cta, w_total / 6.0e12) * 1e6 + waves * 1.0 + (s > 1 ? 1.5 : 0.5) +
-                            (overlay ? 0.7 : 0.0);
+        const double per_cta = static_cast<double>(waves) * kbps * bn * kBK * 2 / 55e9;
+        // the reduction: ~0.5 us, plus ~1 us for the exchange of a 256-column
+        // tile's partial sums (proportional to the tile's columns)
+        const double red = s > 1 ? 0.5 + 1.0 * bn / rmm::kRowsBN : 0.5;
+        const double cost = std::max(per_cta, w_total / 6.0e12) * 1e6 + waves * 1.0 + red + (overlay ? 0.7 : 0.0);
         if (cost < best - 1e-9) {
             best = cost;
             p.splits = s;
@@ -437,8 +452,11 @@ RowsPlan plan_rows(int dev, bool fused, int64_t M, int64_t K, int64_t N, const D
             p.cluster = s > 1 ? 1 : 0;
             p.stages = st;
             p.overlay = overlay ? 1 : 0;
+            p.bn = bn;
+            p.n_tiles = n_tiles;
             p.grid = static_cast<int>(std::min<long>(units, resident));
         }
+    }
     }
     if (p.cluster) p.grid = (p.grid / p.splits) * p.splits;
     return p;
@@ -669,6 +687,7 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
     a.stages = p.stages;
     a.grid = p.grid;
     a.red_overlay = p.overlay;
+    a.bn = p.bn;
     a.glu = glu ? 1 : 0;
     a.w_nk = wnk ? 1 : 0;
     a.unscaled = unscaled ? 1 : 0;

@@ -119,9 +119,12 @@ struct RowsLayout {
 // 128 gate columns then the 128 matching up columns).  Unit u is reduced by
 // CTA u % S, which therefore owns at most ceil(units / S) units.
 constexpr int kRowsChunks = kRowsBN / 32;
-__host__ __device__ inline int rows_red_units(bool glu) { return glu ? kRowsChunks / 2 : kRowsChunks; }
-__host__ __device__ inline int rows_owned_max(int splits, bool glu) {
-    return (rows_red_units(glu) + splits - 1) / splits;
+// (chunks: of the tile, 8 for 256 columns, 4 for the 128-column tile)
+__host__ __device__ inline int rows_red_units(bool glu, int chunks = kRowsChunks) {
+    return glu ? chunks / 2 : chunks;
+}
+__host__ __device__ inline int rows_owned_max(int splits, bool glu, int chunks = kRowsChunks) {
+    return (rows_red_units(glu, chunks) + splits - 1) / splits;
 }
 
 // Swish gate, single precision: silu(z) = z * sigmoid(z) = h (1 + tanh h)
@@ -142,20 +145,21 @@ __device__ __forceinline__ float glu_out(float gate, float up, float r) {
     return silu_f(gate * r) * (up * r);
 }
 
-// One W stage: k-block kb by the tile's 256 accumulator columns, into the
-// 32 KB slot at dst.  Weights stored [K, N] (N contiguous): [64 k][64 n] boxes,
+// One W stage: k-block kb by the tile's kBN (256, or 128 for the plain
+// [K, N] form) accumulator columns, into the slot at dst (kBN * 128 bytes).  Weights stored [K, N] (N contiguous): [64 k][64 n] boxes,
 // N-major for the MMA, as many as fall inside N.  Weights stored [N, K] (K
 // contiguous, the layout of a linear layer's weight): one [256 n][64 k] box,
 // K-major, rows past N read as zeros.  Gated: accumulator columns 0..127 come
 // from the gate columns n0.. and 128..255 from the up columns Nout + n0.. (a
 // box past the gate half reads up columns, one past N zeros; neither reaches
 // an output).  w_stage_bytes() gives the bytes the copies deliver.
-template <bool kGlu, bool kWnk>
+template <bool kGlu, bool kWnk, int kBN = kRowsBN>
 __device__ __forceinline__ uint32_t w_stage_bytes(int n0, int N) {
+    static_assert(kBN == kRowsBN || (!kGlu && !kWnk), "128-column W stages: plain [K, N] form only");
     if constexpr (kWnk || kGlu) return kRowsWBytes;
-    else return static_cast<uint32_t>(min(4, (N - n0 + 63) / 64)) * kWBoxBytes;
+    else return static_cast<uint32_t>(min(kBN / 64, (N - n0 + 63) / 64)) * kWBoxBytes;
 }
-template <bool kGlu, bool kWnk>
+template <bool kGlu, bool kWnk, int kBN = kRowsBN>
 __device__ __forceinline__ void load_w_stage(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int n0,
                                              int kb, int N, int Nout) {
     if constexpr (kWnk) {
@@ -166,7 +170,7 @@ __device__ __forceinline__ void load_w_stage(uint32_t dst, const CUtensorMap* tm
             tma_load_2d_nohint(dst, tm, bar, kb * kBK, n0);
         }
     } else {
-        const int nbox = static_cast<int>(w_stage_bytes<kGlu, kWnk>(n0, N) / kWBoxBytes);
+        const int nbox = static_cast<int>(w_stage_bytes<kGlu, kWnk, kBN>(n0, N) / kWBoxBytes);
         for (int j = 0; j < nbox; ++j)
             tma_load_2d_nohint(dst + j * kWBoxBytes, tm, bar, kGlu && j >= 2 ? Nout + n0 + 64 * (j - 2) : n0 + 64 * j,
                                kb * kBK);
@@ -189,13 +193,13 @@ __device__ __forceinline__ uint64_t w_desc(uint32_t b0, int kk) {
 // receive blocks occupy the start of the pipeline buffers, which are idle by
 // the time they fill.
 __host__ __device__ inline RowsLayout rows_layout(int xrows, int stages, int red_slots, int MP,
-                                                  bool overlay = false, bool glu = false) {
+                                                  bool overlay = false, bool glu = false, int bn = kRowsBN) {
     RowsLayout L;
     L.xbytes = xrows * kBK * 2;
     L.off_x = 0;
     L.off_w = ((stages * L.xbytes + 1023) / 1024) * 1024;
-    L.off_g = L.off_w + stages * kRowsWBytes;
-    L.red_block = red_slots > 0 ? MP * (4 + rows_owned_max(red_slots, glu) * (glu ? 2 : 1) * 128) : 0;
+    L.off_g = L.off_w + stages * static_cast<uint32_t>(bn) * kBK * 2;
+    L.red_block = red_slots > 0 ? MP * (4 + rows_owned_max(red_slots, glu, bn / 32) * (glu ? 2 : 1) * 128) : 0;
     L.off_red = overlay ? 0 : ((L.off_g + stages * kGBytes + 15) / 16) * 16;
     L.off_bar = overlay ? ((L.off_g + stages * kGBytes + 15) / 16) * 16 : L.off_red + red_slots * L.red_block;
     const uint32_t nbars = 4 * kRowsMaxStages + 10;
@@ -206,7 +210,10 @@ __host__ __device__ inline RowsLayout rows_layout(int xrows, int stages, int red
 }
 
 
-template <bool kFused, bool kSplit, bool kGlu, bool kWnk, bool kLora>
+// kBN: accumulator columns of a tile, 256, or 128 (plain [K, N] form with a
+// K split: twice the CTAs for the same K split, half the partial sums each
+// CTA exchanges).
+template <bool kFused, bool kSplit, bool kGlu, bool kWnk, bool kLora, int kBN = kRowsBN>
 __global__ void __launch_bounds__(kThreads, 1)
     rows_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                 const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmT,
@@ -215,11 +222,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = align1024(smem_raw);
     const int S = a.stages;
     const int split = kSplit ? a.splits : 1;
-    const RowsLayout L = rows_layout(a.xrows, S, kSplit ? split : 0, a.MP, kSplit && a.red_overlay, kGlu);
+    static_assert(kBN == kRowsBN || (kSplit && !kGlu && !kWnk && !kLora), "128-column tiles: plain K split only");
+    constexpr uint32_t kWBytes = kBN * kBK * 2;    // one W stage
+    constexpr int kChunks = kBN / 32;              // 32-column chunks of a tile
+    const RowsLayout L = rows_layout(a.xrows, S, kSplit ? split : 0, a.MP, kSplit && a.red_overlay, kGlu, kBN);
     // Output columns: N, or F = N / 2 for the gated form, whose tile covers
     // 128 output columns from two W column ranges (gate, then up).
     const int Nout = kGlu ? a.N / 2 : a.N;
-    constexpr int kOutBN = kGlu ? kRowsBN / 2 : kRowsBN;
+    constexpr int kOutBN = kGlu ? kBN / 2 : kBN;
     const uint32_t xbytes = L.xbytes;
     const uint32_t sb = smem_u32(smem);
     const uint32_t sx = sb + L.off_x, sw = sb + L.off_w, sg = sb + L.off_g;
@@ -279,14 +289,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t xbar = kFused ? xland(s) : full(s);
         if (kFused) {
             mbar_arrive_expect_tx(xbar, xbytes + (!ext ? kGBytes : 0));
-            mbar_arrive_expect_tx(full(s), w_stage_bytes<kGlu, kWnk>(n0, a.N));
+            mbar_arrive_expect_tx(full(s), w_stage_bytes<kGlu, kWnk, kBN>(n0, a.N));
         } else {
-            mbar_arrive_expect_tx(full(s), xbytes + w_stage_bytes<kGlu, kWnk>(n0, a.N));
+            mbar_arrive_expect_tx(full(s), xbytes + w_stage_bytes<kGlu, kWnk, kBN>(n0, a.N));
         }
         tma_load_2d_nohint(sx + s * xbytes, ext ? &tmT : &tmX, xbar, (ext ? kb - a.k_blocks : kb) * kBK,
                            mb * kRowsBM);
         if (kFused && !ext) tma_load_1d(sg + s * kGBytes, &tmG, xbar, kb * kBK);
-        load_w_stage<kGlu, kWnk>(sw + s * kRowsWBytes, ext ? &tmB : &tmW, full(s), n0, ext ? 0 : kb, a.N, Nout);
+        load_w_stage<kGlu, kWnk, kBN>(sw + s * kWBytes, ext ? &tmB : &tmW, full(s), n0, ext ? 0 : kb, a.N, Nout);
     };
     // k-blocks of the first unit that thread 0 (the producer) issues before
     // the CTA-wide set-up barrier, as soon as its barriers exist and the
@@ -384,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(kRowsBM, kRowsBN, false, !kWnk);
+            constexpr uint32_t idesc = idesc_bf16_f32(kRowsBM, kBN, false, !kWnk);
             uint32_t it = 0, tl = 0;
             Ring ring(S);
             bool ok = true;
@@ -394,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t buf = tl & 1, use = tl >> 1;
                 if (!mbar_wait(accempty(buf), (use & 1) ^ 1, abort)) break;
                 tc_fence_after();
-                const uint32_t d = tmem + buf * kRowsBN;
+                const uint32_t d = tmem + buf * kBN;
                 const int kend = kb1 + lora_extra(sp);
                 for (int kb = kb0; kb < kend; ++kb) {
                     const uint32_t s = ring.idx, ph = ring.phase;
@@ -403,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = sx + s * xbytes, b0 = sw + s * kRowsWBytes;
+                    const uint32_t a0 = sx + s * xbytes, b0 = sw + s * kWBytes;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
                         mma_bf16_ss(d, sdesc_sw128(a0 + kk * 32, 16, 1024), w_desc<kWnk>(b0, kk), idesc,
@@ -494,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // a hilo output writes all 64 columns of each half (zeros past N)
             const int ncols = !kGlu && a.hilo ? kBK : min(kOutBN, Nout - n0);
             const int rows_here = min(kRowsBM, a.M - mb * kRowsBM);   // valid rows of this tile
-            const uint32_t taddr = tmem + buf * kRowsBN + (static_cast<uint32_t>(q * 32) << 16);
+            const uint32_t taddr = tmem + buf * kBN + (static_cast<uint32_t>(q * 32) << 16);
             const bool warp_has_rows = q * 32 < rows_here;              // warp-uniform
             const int m = mb * kRowsBM + row;
             const float r = kFused && !a.unscaled ? rsqrtf(sr[buf * kRowsBM + row] * inv_k + a.eps) : 1.f;
@@ -600,8 +610,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
             const uint32_t swz = static_cast<uint32_t>(row & 7);
-            for (int c = wteam; c < kRowsChunks; c += 2) {
-                const int unit = kGlu ? (c & (kRowsChunks / 2 - 1)) : c, half = kGlu ? c / (kRowsChunks / 2) : 0;
+            for (int c = wteam; c < kChunks; c += 2) {
+                const int unit = kGlu ? (c & (kChunks / 2 - 1)) : c, half = kGlu ? c / (kChunks / 2) : 0;
                 if (unit >= nunits) continue;   // warp-uniform
                 uint32_t v[32];
                 tmem_ld_32x32(taddr + c * 32, v);
@@ -1755,14 +1765,14 @@ cudaError_t ensure_smem_attr(const void* func, int slot) {
 
 }  // namespace
 
-size_t rows_smem_bytes(int xrows, int stages, int red_slots, int MP, bool overlay, bool glu) {
-    return rows_layout(xrows, stages, red_slots, MP, overlay, glu).total;
+size_t rows_smem_bytes(int xrows, int stages, int red_slots, int MP, bool overlay, bool glu, int bn) {
+    return rows_layout(xrows, stages, red_slots, MP, overlay, glu, bn).total;
 }
-bool rows_overlay_fits(int xrows, int stages, int splits, int MP, bool glu) {
-    const RowsLayout L = rows_layout(xrows, stages, splits, MP, true, glu);
+bool rows_overlay_fits(int xrows, int stages, int splits, int MP, bool glu, int bn) {
+    const RowsLayout L = rows_layout(xrows, stages, splits, MP, true, glu, bn);
     return static_cast<uint32_t>(splits) * L.red_block <= L.off_g;
 }
-size_t rows_stage_bytes(int xrows) { return xrows * kBK * 2 + kRowsWBytes + kGBytes; }
+size_t rows_stage_bytes(int xrows, int bn) { return xrows * kBK * 2 + static_cast<size_t>(bn) * kBK * 2 + kGBytes; }
 // Launch with programmatic dependent launch (the kernel's set-up may overlap
 // the previous kernel on the stream) and, optionally, a 1-D cluster, or as a
 // cooperative grid (all CTAs resident at once, or the launch fails).
@@ -1839,6 +1849,7 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
+    const int bn = a.bn ? a.bn : kRowsBN;   // (0: the default width)
     decltype(&rows_kernel<true, true, true, true, false>) kern;
     int slot;
     if (lora) {
@@ -1851,14 +1862,22 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
     } else if (glu) {
         kern = split ? rows_kernel<true, true, true, false, false> : rows_kernel<true, false, true, false, false>;
         slot = split ? 8 : 7;
+    } else if (bn == kRowsBN / 2) {
+        if (!split) return cudaErrorInvalidValue;   // 128-column tiles: K split only
+        kern = fused ? rows_kernel<true, true, false, false, false, kRowsBN / 2>
+                     : rows_kernel<false, true, false, false, false, kRowsBN / 2>;
+        slot = fused ? 26 : 27;
     } else {
         kern = fused ? (split ? rows_kernel<true, true, false, false, false> : rows_kernel<true, false, false, false, false>)
                      : (split ? rows_kernel<false, true, false, false, false> : rows_kernel<false, false, false, false, false>);
         slot = (fused ? 0 : 1) + (split ? 4 : 0);
     }
+    if (bn != kRowsBN && bn != kRowsBN / 2) return cudaErrorInvalidValue;
+    if (bn != kRowsBN && (glu || wnk || lora)) return cudaErrorInvalidValue;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), slot);
     if (e != cudaSuccess) return e;
-    const size_t smem = rows_smem_bytes(a.xrows, a.stages, split ? a.splits : 0, a.MP, split && a.red_overlay, glu);
+    const size_t smem =
+        rows_smem_bytes(a.xrows, a.stages, split ? a.splits : 0, a.MP, split && a.red_overlay, glu, bn);
     e = launch_ex(kern, a.grid, smem, split ? a.splits : 1, s, false, tmX, tmW, tmG, tmT, tmB, y, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -1887,7 +1906,10 @@ int rows_pair_max_active_clusters() {
     return max_active_clusters(rows_ta_kernel<false, false, false, false, true>, 20, 2, kTaSmem);
 }
 
-int rows_max_active_clusters(bool fused, int splits, size_t smem, bool glu, bool wnk, bool lora) {
+int rows_max_active_clusters(bool fused, int splits, size_t smem, bool glu, bool wnk, bool lora, int bn) {
+    if (bn == kRowsBN / 2)
+        return fused ? max_active_clusters(rows_kernel<true, true, false, false, false, kRowsBN / 2>, 26, splits, smem)
+                     : max_active_clusters(rows_kernel<false, true, false, false, false, kRowsBN / 2>, 27, splits, smem);
     if (lora) return max_active_clusters(rows_kernel<true, true, false, false, true>, 17, splits, smem);
     if (wnk)
         return glu ? max_active_clusters(rows_kernel<true, true, true, true, false>, 13, splits, smem)

@@ -14,7 +14,7 @@ constexpr int kBK = 64;          // K extent of one pipeline stage (128 B of bf1
 // Row-tile path: CTA tile 128 (rows of X) x 256 (columns of W).
 constexpr int kRowsBM = 128;
 constexpr int kRowsBN = 256;
-constexpr int kRowsMaxStages = 6;
+constexpr int kRowsMaxStages = 12;
 
 constexpr int kClusterMaxSplits = 8;   // portable cluster size
 
@@ -28,14 +28,15 @@ constexpr int kTtStages = 3;
 // through a cluster (0 without); MP = M rounded up to 16; overlay: the
 // splits' receive blocks reuse the pipeline buffers instead of an area of
 // their own.
-// glu: the gated form (reduction units of two chunks).
+// glu: the gated form (reduction units of two chunks).  bn: columns of a
+// tile, kRowsBN or kRowsBN / 2 (the plain [K, N] form with a K split).
 size_t rows_smem_bytes(int xrows, int stages, int red_slots, int MP, bool overlay = false,
-                       bool glu = false);
+                       bool glu = false, int bn = kRowsBN);
 // The receive blocks of a K split over `splits` CTAs fit the pipeline buffers.
-bool rows_overlay_fits(int xrows, int stages, int splits, int MP, bool glu = false);
-size_t rows_stage_bytes(int xrows);
+bool rows_overlay_fits(int xrows, int stages, int splits, int MP, bool glu = false, int bn = kRowsBN);
+size_t rows_stage_bytes(int xrows, int bn = kRowsBN);
 int rows_max_active_clusters(bool fused, int splits, size_t smem, bool glu = false, bool wnk = false,
-                             bool lora = false);
+                             bool lora = false, int bn = kRowsBN);
 // Clusters of two CTAs of the paired fused kernel that fit on the device at once.
 int rows_pair_max_active_clusters();
 struct RowsLaunch {
@@ -57,6 +58,8 @@ struct RowsLaunch {
     int wait_limit_us;         // limit of one bounded in-kernel wait
     int test_skip_sends;       // test hook: the K-split reduction skips its stores
     int cluster;               // 1: the splits of a tile form a cluster
+    int bn;                    // columns of a tile of the row-tile kernel: kRowsBN (or 0), or
+                               // kRowsBN / 2 (plain [K, N] form with a K split)
     int xrows, MP, stages;
     int grid;
     int tall;                  // 1: the 256-row kernel (plain form; m_tiles then counts 256-row tiles)
