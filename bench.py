@@ -776,7 +776,9 @@ def kernel_name(rmm, w):
     if plan["path"] == 2:
         return f"gemv_kernel<fused> ({plan['splits']} K pieces per 64-column unit)"
     if plan["cluster"]:
-        return f"rows_kernel<fused, K split x{plan['splits']} in a cluster>"
+        bn = -(-w.N // plan["tiles"]) if plan["tiles"] else 256
+        width = ", 128-column tiles" if bn <= 128 else ""
+        return f"rows_kernel<fused, K split x{plan['splits']} in a cluster{width}>"
     if w.M > 128:
         return "rows_ta_kernel (A operand in tensor memory)"
     return "rows_kernel<fused>"
