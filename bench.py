@@ -293,9 +293,12 @@ def replay_times(torch, stream, graphs, n):
 
 
 def bench_workload(torch, rmm, inputs, w, K, W_warm, device, stream, l2, with_unfused=True,
-                   sampler=None, barrier=None, gated=False, weight_nk=False, lora_r=0, replays=0):
+                   sampler=None, barrier=None, gated=False, weight_nk=False, lora_r=0, replays=0,
+                   folded=False):
     """gated: time the gated form (Y [M, N/2]); weight_nk: W stored [N, K];
-    lora_r > 0: the low-rank adapter form with rank lora_r; replays > 0: replay
+    lora_r > 0: the low-rank adapter form with rank lora_r; folded: the gain
+    folded into W once before timing (fold_gain), then rmsnorm_matmul_folded
+    per step; replays > 0: replay
     the timed steps that many more times (reported beside the timed run, which
     alone gives the result)."""
     n_copies = n_rotating_copies(w, l2)
@@ -304,10 +307,13 @@ def bench_workload(torch, rmm, inputs, w, K, W_warm, device, stream, l2, with_un
                                weight_nk=weight_nk)
     if lora_r:
         A, B = (t.to(device) for t in inputs.lora_adapter(w.K, w.N, lora_r, seed=w.seed + 100))
+    wgs = [rmm.fold_gain(c[1], c[2]) for c in copies] if folded else None
 
     def step(i):
         x, g, wt, y = copies[i]
-        if lora_r:
+        if folded:
+            rmm.rmsnorm_matmul_folded(x, wgs[i], w.eps, out=y, stream=stream)
+        elif lora_r:
             rmm.rmsnorm_matmul_lora(x, g, wt, A, B, w.eps, out=y, stream=stream)
         elif gated or weight_nk:
             rmm.rmsnorm_matmul_ex(x, g, wt, w.eps, weight_nk=weight_nk, gated=gated, out=y, stream=stream)
@@ -652,6 +658,21 @@ def main():
                                    with_unfused=False, sampler=sampler, weight_nk=True)
                 e = shape_entry(ww, r["secs"] / k, r, peaks, k)
                 e["workload"] += " (W stored [N, K])"
+                shapes.append(e)
+                del r
+                torch.cuda.empty_cache()
+            # the gain folded into the weights once (inference weights), then
+            # one kernel per call that reads raw X
+            for name in ("decode_qkv_16x4096x6144", "prefill_qkv_4096x4096x6144",
+                         "large_prefill_16384x8192x8192"):
+                ww = inputs.WORKLOADS[name]
+                est = max(ww.flops / (peaks["bf16_tflops"] * 1e12), ww.bytes_xwy / (peaks["hbm_gbs"] * 1e9))
+                k = int(min(5000, max(20, 0.2 / max(est, 1e-7))))
+                r = bench_workload(torch, rmm, inputs, ww, k, 3, device, stream, l2,
+                                   with_unfused=True, sampler=sampler, folded=True)
+                e = shape_entry(ww, r["secs"] / k, r, peaks, k)
+                e["workload"] += " (gain folded into W once)"
+                e["path"] = "256-row kernel, row statistic in-kernel" if ww.M > 128 else e["path"] + ", gain of ones"
                 shapes.append(e)
                 del r
                 torch.cuda.empty_cache()

@@ -180,6 +180,37 @@ int matmul(const void* A, const void* B, void* C,
            int64_t M, int64_t K, int64_t N, cudaStream_t stream);
 
 /*
+ * RMSNorm + MatMul with the gain folded into the weights.  RMSNorm's gain
+ * scales the columns of the row vector that meets W, so
+ *   (X[m,:] * g * r[m]) @ W = r[m] * (X[m,:] @ W'),  W'[k,n] = g[k] * W[k,n]
+ * (the review page's RMSNorm, eq. (1), with its MatMul).  Where g and W stay
+ * fixed across calls (inference weights), W' is formed once by fold_gain()
+ * and every call then reads raw X as the MMA's A operand:
+ *
+ * fold_gain:  Wg[k,n] = bf16( g[k] * W[k,n] ),  g [K], W and Wg [K,N] bf16
+ *   (the product of two bf16 values is exact in fp32: one rounding).  N must
+ *   be a multiple of 8; Wg may not overlap g or W.  Asynchronous on `stream`.
+ *
+ * rmsnorm_matmul_folded:  Y[m,n] = bf16( r[m] * sum_k X[m,k] * Wg[k,n] ),
+ *   r[m] = 1 / sqrt( mean_k X[m,k]^2 + eps ),  X [M,K], Wg [K,N], Y [M,N] bf16,
+ *   fp32 accumulation.  The same rules on sizes, alignment and overlap as
+ *   rmsnorm_matmul().  From 129 rows up it runs the 256-row kernel: two
+ *   M = 128 MMAs per W stage read X as the copy wrote it, two more warps read
+ *   each X stage for the row sums of squares, and the epilogue scales row m
+ *   by r[m]; the last tiles are cut along K as for matmul() (partial products
+ *   and partial row sums combined in piece order through a library-owned
+ *   workspace, so the call may allocate device memory like rmsnorm_matmul()).
+ *   Up to 128 rows it runs rmsnorm_matmul()'s kernels with a library-owned
+ *   gain of ones (allocated on the first call with a longer K; that call may
+ *   not be made during stream capture, which returns RMM_ERR_INTERNAL).
+ *   The result differs from rmsnorm_matmul(X, g, W)'s only in where the bf16
+ *   rounding of the gain product falls (g*W instead of X*g).
+ */
+int fold_gain(const void* g, const void* W, void* Wg, int64_t K, int64_t N, cudaStream_t stream);
+int rmsnorm_matmul_folded(const void* X, const void* Wg, void* Y, int64_t M, int64_t K, int64_t N,
+                          float eps, cudaStream_t stream);
+
+/*
  * Test and benchmark switch for the dispatcher of rmsnorm_matmul() and
  * matmul(): 0 = shape-based choice (default), 1 = always the row-tile path,
  * 2 = always the small-M path (requires M <= 16; larger M returns

@@ -27,6 +27,7 @@ __all__ = [
     "force_path",
     "dispatch_path", "describe_plan", "device_status", "status_string", "STATUS", "PATH_AUTO",
     "PATH_ROWS", "PATH_SMALL_M", "ABI_FUNCTIONS", "rmsnorm_heads", "qknorm_attention",
+    "fold_gain", "rmsnorm_matmul_folded",
 ]
 
 STATUS = {
@@ -42,7 +43,7 @@ ABI_FUNCTIONS = ("rmsnorm_matmul", "rmsnorm", "matmul", "rmm_force_path",
                  "rmm_device_status", "rmm_status_string", "rmm_dispatch_path",
                  "rmsnorm_matmul_noalloc", "rmm_describe_plan", "rmsnorm_matmul_swiglu",
                  "rmsnorm_matmul_ex", "rmm_test_hooks", "rmsnorm_matmul_lora",
-                 "rmsnorm_heads", "qknorm_attention")
+                 "rmsnorm_heads", "qknorm_attention", "fold_gain", "rmsnorm_matmul_folded")
 
 
 class RmmError(RuntimeError):
@@ -63,6 +64,8 @@ def _bind(l: ctypes.CDLL) -> ctypes.CDLL:
     l.rmsnorm_matmul_ex.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, ctypes.c_uint, vp]
     l.rmsnorm.argtypes = [vp, vp, vp, i64, i64, f32, vp]
     l.matmul.argtypes = [vp, vp, vp, i64, i64, i64, vp]
+    l.fold_gain.argtypes = [vp, vp, vp, i64, i64, vp]
+    l.rmsnorm_matmul_folded.argtypes = [vp, vp, vp, i64, i64, i64, f32, vp]
     l.rmm_force_path.argtypes = [i32]
     l.rmm_device_status.argtypes = [vp]
     l.rmm_status_string.argtypes = [i32]
@@ -78,7 +81,7 @@ def _bind(l: ctypes.CDLL) -> ctypes.CDLL:
                  "rmsnorm",
                  "matmul", "rmm_force_path", "rmm_device_status", "rmm_dispatch_path",
                  "rmm_describe_plan", "rmm_test_hooks", "rmsnorm_matmul_lora",
-                 "rmsnorm_heads", "qknorm_attention"):
+                 "rmsnorm_heads", "qknorm_attention", "fold_gain", "rmsnorm_matmul_folded"):
         getattr(l, name).restype = i32
     return l
 
@@ -302,6 +305,47 @@ def rmsnorm_matmul_noalloc(X, g, W, eps: float = 1e-6, out=None, stream=None):
     _raise(lib().rmsnorm_matmul_noalloc(X.data_ptr(), g.data_ptr(), W.data_ptr(), out.data_ptr(),
                                         M, K, N, float(eps), _stream_ptr(stream)),
            "rmsnorm_matmul_noalloc")
+    return out
+
+
+def fold_gain(g, W, out=None, stream=None):
+    """Wg[K,N] = bf16(g[k] * W[k,n]): the gain folded into the weights, once,
+    for rmsnorm_matmul_folded()."""
+    import torch
+    _check_bf16("g", g, 1)
+    _check_bf16("W", W, 2)
+    K, N = W.shape
+    if g.shape[0] != K:
+        raise ValueError("g must have K elements")
+    if out is None:
+        out = torch.empty_like(W)
+    else:
+        _check_bf16("out", out, 2)
+        if tuple(out.shape) != (K, N):
+            raise ValueError(f"out must have shape {(K, N)}")
+    _raise(lib().fold_gain(g.data_ptr(), W.data_ptr(), out.data_ptr(), K, N, _stream_ptr(stream)),
+           "fold_gain")
+    return out
+
+
+def rmsnorm_matmul_folded(X, Wg, eps: float = 1e-6, out=None, stream=None):
+    """Y[M,N] = bf16(r[m] * (X @ Wg)) with r[m] = rsqrt(mean(X[m]^2) + eps):
+    rmsnorm_matmul(X, g, W) for Wg = fold_gain(g, W)."""
+    import torch
+    _check_bf16("X", X, 2)
+    _check_bf16("Wg", Wg, 2)
+    M, K = X.shape
+    if Wg.shape[0] != K:
+        raise ValueError("inner dimensions differ")
+    N = Wg.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    else:
+        _check_bf16("out", out, 2)
+        if tuple(out.shape) != (M, N):
+            raise ValueError(f"out must have shape {(M, N)}")
+    _raise(lib().rmsnorm_matmul_folded(X.data_ptr(), Wg.data_ptr(), out.data_ptr(), M, K, N, float(eps),
+                                       _stream_ptr(stream)), "rmsnorm_matmul_folded")
     return out
 
 

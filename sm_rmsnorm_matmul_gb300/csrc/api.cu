@@ -11,6 +11,7 @@
 #include <cstdint>
 #include <cstring>
 #include <map>
+#include <vector>
 #include <tuple>
 #include <mutex>
 #include <utility>
@@ -616,13 +617,16 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
                     int64_t K, int64_t N, float eps, cudaStream_t stream, const FixedScratch* fixed = nullptr,
                     bool glu = false, bool wnk = false, bool unscaled = false,
                     const void* lora_t = nullptr, const void* lora_b = nullptr, int64_t R = 0,
-                    bool hilo = false) {
+                    bool hilo = false, bool fold = false) {
+    // fold: W holds the gain folded in (fused must be false): the 256-row
+    // kernel with the row statistic, for every shape
     const bool lora = lora_t != nullptr;
     int dev = 0;
     DeviceInfo d;
     int rc = current_device(&dev, &d);
     if (rc != RMM_OK) return rc;
-    const int path = glu || wnk || lora || unscaled ? static_cast<int>(kPathRows) : choose_path(M, K, N, d.sm_count);
+    const int path =
+        glu || wnk || lora || unscaled || fold ? static_cast<int>(kPathRows) : choose_path(M, K, N, d.sm_count);
     if (path == kPathSmallM) {
         if (M > rmm::kGvMaxM) return RMM_ERR_INVALID_ARG;
         const GemvPlan p = plan_gemv(dev, fused, K, N, d);
@@ -669,7 +673,7 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
         if (!map_1d(&tmG, g, K)) return RMM_ERR_INTERNAL;
     }
     const RowsPlan p = plan_rows(dev, fused, M, K, N, d, glu, wnk, lora);
-    if (!map_2d(&tmX, X, M, K, p.xrows)) return RMM_ERR_INTERNAL;
+    if (!map_2d(&tmX, X, M, K, fold ? rmm::kRowsBM : p.xrows)) return RMM_ERR_INTERNAL;
     if (!fused) tmG = tmX;
     rmm::RowsLaunch a{};
     a.M = static_cast<int>(M);
@@ -704,13 +708,19 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
     a.tail_tiles = 0;
     a.tail_pieces = 1;
     a.tail_kbp = p.k_blocks;
-    const bool tall = !glu && !wnk && !lora && !unscaled && !p.cluster && p.xrows == rmm::kRowsBM && use_tall(fused, M);
+    const bool tall =
+        fold || (!glu && !wnk && !lora && !unscaled && !p.cluster && p.xrows == rmm::kRowsBM && use_tall(fused, M));
     if (tall) {
         // tiles of 256 rows, the last ones cut along K as for the 128-row kernel
         if (!map_2d_store(&tmY, Y, M, N)) return RMM_ERR_INTERNAL;
         a.tmY = &tmY;
         a.tall = 1;
+        a.fold = fold ? 1 : 0;
         a.m_tiles = static_cast<int>((M + rmm::kTtBM - 1) / rmm::kTtBM);
+        a.n_tiles = static_cast<int>((N + rmm::kRowsBN - 1) / rmm::kRowsBN);
+        a.bn = rmm::kRowsBN;
+        a.splits = 1;
+        a.cluster = 0;
         const int sms = d.sm_count > 0 ? d.sm_count : 1;
         const int units = a.m_tiles * a.n_tiles;
         const TailPlan t = plan_tail(units, std::min(units, sms), p.k_blocks, sms);
@@ -718,7 +728,8 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
         if (t.tiles > 0) {
             constexpr size_t kPieceBytes = static_cast<size_t>(rmm::kTtBM) * rmm::kRowsBN * sizeof(float);
             const size_t pieces = static_cast<size_t>(t.tiles) * t.pieces;
-            const size_t ss_bytes = 0;   // (unfused: no row sums)
+            // the folded form's partial row sums of squares (unfused: none)
+            const size_t ss_bytes = fold ? pieces * rmm::kTtBM * sizeof(float) : 0;
             const size_t ncount = static_cast<size_t>(t.tiles) * 2;
             if (fixed) {
                 if (!fixed->place(pieces * kPieceBytes, ss_bytes, &a.ws_acc, &a.ws_ss) ||
@@ -856,6 +867,64 @@ int matmul(const void* A, const void* B, void* C, int64_t M, int64_t K, int64_t 
                     {{A, static_cast<size_t>(M) * K * 2}, {B, static_cast<size_t>(K) * N * 2}});
     if (rc != RMM_OK) return rc;
     return run_contraction(false, A, nullptr, B, C, M, K, N, 0.f, stream);
+}
+
+}  // extern "C"
+
+// A gain of ones, [K] bf16, per device: the folded form of a single row tile
+// runs the fused row-tile kernels with it (X * 1 = X exactly).  Grown when a
+// longer K arrives; an outgrown buffer is kept, since calls on other streams
+// may still read it.  Returns nullptr if it has to grow during stream capture.
+std::mutex g_ones_mu;
+std::map<int, std::pair<void*, int64_t>> g_ones;
+
+const void* ones_gain(int dev, int64_t K, cudaStream_t s) {
+    std::lock_guard<std::mutex> lk(g_ones_mu);
+    auto& e = g_ones[dev];
+    if (e.first && e.second >= K) return e.first;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return nullptr;
+    const int64_t n = std::max<int64_t>(round_up_pow2(static_cast<size_t>(K)), 4096);
+    void* p = nullptr;
+    if (cudaMalloc(&p, static_cast<size_t>(n) * 2) != cudaSuccess) return nullptr;
+    std::vector<uint16_t> one(static_cast<size_t>(n), 0x3F80);   // bf16 1.0
+    if (cudaMemcpy(p, one.data(), static_cast<size_t>(n) * 2, cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaFree(p);
+        return nullptr;
+    }
+    e = {p, n};
+    return p;
+}
+
+extern "C" {
+
+int fold_gain(const void* g, const void* W, void* Wg, int64_t K, int64_t N, cudaStream_t stream) {
+    if (K < 1 || N < 1 || K > (int64_t(1) << 31) || N > (int64_t(1) << 31) || N % 8 != 0)
+        return RMM_ERR_INVALID_ARG;
+    int rc = check_ptrs(Wg, static_cast<size_t>(K) * N * 2,
+                        {{g, static_cast<size_t>(K) * 2}, {W, static_cast<size_t>(K) * N * 2}});
+    if (rc != RMM_OK) return rc;
+    return rmm::launch_fold_gain(g, W, Wg, K, N, stream) == cudaSuccess ? RMM_OK : RMM_ERR_LAUNCH;
+}
+
+int rmsnorm_matmul_folded(const void* X, const void* Wg, void* Y, int64_t M, int64_t K, int64_t N, float eps,
+                          cudaStream_t stream) {
+    int rc = check_sizes(M, K, N, eps, true);
+    if (rc == kNoop) return RMM_OK;
+    if (rc != RMM_OK) return rc;
+    rc = check_ptrs(Y, static_cast<size_t>(M) * N * 2,
+                    {{X, static_cast<size_t>(M) * K * 2}, {Wg, static_cast<size_t>(K) * N * 2}});
+    if (rc != RMM_OK) return rc;
+    if (M <= rmm::kRowsBM) {
+        // one row tile: the fused row-tile (or small-M) kernel with a gain of ones
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return RMM_ERR_UNSUPPORTED_DEVICE;
+        const void* ones = ones_gain(dev, K, stream);
+        if (!ones) return RMM_ERR_INTERNAL;
+        return run_contraction(true, X, ones, Wg, Y, M, K, N, eps, stream);
+    }
+    return run_contraction(false, X, nullptr, Wg, Y, M, K, N, eps, stream, nullptr, false, false, false, nullptr,
+                           nullptr, 0, false, true);
 }
 
 int rmsnorm(const void* X, const void* g, void* Xn, int64_t M, int64_t K, float eps,

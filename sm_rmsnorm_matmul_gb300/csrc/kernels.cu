@@ -21,6 +21,8 @@
 // warps (tensor memory -> registers -> scale by r -> bf16).
 // A third kernel, rmsnorm_kernel, is the unfused RMSNorm kept for comparison.
 // The small-M path (at most 16 rows of X) is in gemv.cu.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -1418,17 +1420,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 // 0 TMA producer, 1 MMA issuer, 2 tensor-memory allocation, 4-11 epilogue
 // (warps 4-7 the first half's rows, 8-11 the second's).  Tiles and tail
 // pieces are those of the 128-row kernel with 256-row tiles.
+//
+// kStat: RMSNorm with the gain already folded into the weights (W' = diag(g)
+// W, prepared once; (X diag(g)) W = X W'): A is raw X as the copy wrote it,
+// and warps 2-3 read every A stage once more for the row sums of squares
+// (each of their 64 threads four rows of the tile; the stage is released
+// when both the MMAs and they are done).  The epilogue scales row m by
+// 1/rms_m; tail pieces publish their partial row sums with their partial
+// products and the reducing piece adds both in piece order.
 constexpr uint32_t kTtXBytes = kTtBM * kBK * 2;               // 32 KB
 constexpr uint32_t kTtStageBytes = kTtXBytes + kRowsWBytes;   // 64 KB: A, then W
 constexpr uint32_t kTtOutBytes = kRowsBM * 32 * 2;            // 8 KB: 128 rows x 32 bf16 of C
 constexpr uint32_t kTtOffOut = kTtStages * kTtStageBytes;     // two staging buffers per half
 constexpr uint32_t kTtOffBar = kTtOffOut + 4 * kTtOutBytes;
-// full, empty per stage; accfull, accempty, mmadone, episync[2], tailsync
-constexpr uint32_t kTtNumBars = 2 * kTtStages + 6;
-constexpr uint32_t kTtOffMisc = kTtOffBar + ((kTtNumBars * 8 + 15) / 16) * 16;
+// full, empty per stage; accfull, accempty, mmadone, episync[2], tailsync,
+// srfull, srempty
+constexpr uint32_t kTtNumBars = 2 * kTtStages + 8;
+constexpr uint32_t kTtOffSr = kTtOffBar + ((kTtNumBars * 8 + 15) / 16) * 16;   // [256] row sums (kStat)
+constexpr uint32_t kTtOffMisc = kTtOffSr + kTtBM * 4;
 constexpr uint32_t kTtSmem = kTtOffMisc + 16 + 1024;
 static_assert(kTtSmem <= 232448, "the tall-tile kernel's shared memory exceeds the opt-in limit");
 
+template <bool kStat>
 __global__ void __launch_bounds__(kThreads, 1)
     tall_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                 const __grid_constant__ CUtensorMap tmY, __nv_bfloat16* __restrict__ Y, RowsLaunch a) {
@@ -1440,6 +1453,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t full0 = bar0, empty0 = bar0 + 8 * kTtStages;
     const uint32_t accfull = bar0 + 16 * kTtStages, accempty = accfull + 8, mmadone = accfull + 16;
     const uint32_t episync0 = accfull + 24, tailsync = accfull + 40;
+    // kStat: the tile's row sums of squares are in sr / have been read
+    const uint32_t srfull = accfull + 48, srempty = accfull + 56;
+    float* sr = reinterpret_cast<float*>(smem + kTtOffSr);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kTtOffMisc);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + kTtOffMisc + 4);
 
@@ -1447,7 +1463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTtStages; ++s) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, kStat ? 3 : 1);   // the MMAs' commit (+ warps 2-3)
         }
         mbar_init(accfull, 1);
         mbar_init(accempty, 8);
@@ -1455,6 +1471,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(episync0, 4);
         mbar_init(episync0 + 8, 4);
         mbar_init(tailsync, 8);
+        mbar_init(srfull, 2);    // one lane of each of warps 2-3
+        mbar_init(srempty, 8);   // one lane of each epilogue warp
         abort[0] = 0;
         abort[1] = a.wait_limit_us;
         fence_mbar_init();
@@ -1538,6 +1556,51 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(mmadone);
             mbar_wait_teardown(mmadone, 0);
         }
+    } else if (kStat && (warp == 2 || warp == 3)) {
+        // ------------------------------------------------ row sums of squares
+        // Thread st of 64 takes rows st + 64 j of every A stage: the whole
+        // row, its eight 16-byte pieces read from lane-rotated positions so
+        // that the eight lanes of an access phase hit distinct banks.
+        const int st = threadIdx.x - 64;
+        Ring ring(kTtStages);
+        uint32_t tl = 0;
+        bool ok = true;
+        TaUnit un;
+        for (int i = 0; ok && ta_unit<1>(a, i, un); ++i, ++tl) {
+            float ss[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int kb = un.kb0; kb < un.kb1; ++kb) {
+                if (!warp_wait(full0 + 8 * ring.idx, ring.phase, abort)) { ok = false; break; }
+                const uint32_t stg = sb + ring.idx * kTtStageBytes;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int r = st + 64 * j;
+                    const uint32_t rowp = stg + (r >> 7) * (kTtXBytes / 2) + (r & 127) * 128;
+#pragma unroll
+                    for (int c0 = 0; c0 < 8; c0 += 4) {
+                        uint4 v[4];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) v[c] = lds128(rowp + (((c0 + c + lane) & 7) << 4));
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            ss[j] = fma_sq_bf16x2(v[c].x, ss[j]);
+                            ss[j] = fma_sq_bf16x2(v[c].y, ss[j]);
+                            ss[j] = fma_sq_bf16x2(v[c].z, ss[j]);
+                            ss[j] = fma_sq_bf16x2(v[c].w, ss[j]);
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty0 + 8 * ring.idx);
+                ring.advance();
+            }
+            if (!ok) break;
+            // the epilogue has read the previous tile's sums
+            if (tl > 0 && !warp_wait(srempty, (tl - 1) & 1, abort)) break;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sr[st + 64 * j] = ss[j];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(srfull);
+        }
     } else if (warp >= 4) {
         // ------------------------------------------------ epilogue
         // Read this thread's accumulator row (bf16) into registers and
@@ -1568,8 +1631,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t chunks = 0;   // staging buffer uses so far (per half)
         uint32_t tl = 0;
         TaUnit un;
+        const float inv_k = 1.f / static_cast<float>(a.K);
         for (int i = 0; ta_unit<1>(a, i, un); ++i, ++tl) {
             if (!warp_wait(accfull, tl & 1, abort)) break;
+            // kStat: this tile's (or piece's) row sum of squares
+            float ssr = 0.f;
+            if (kStat) {
+                if (!warp_wait(srfull, tl & 1, abort)) break;
+                ssr = sr[row];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(srempty);
+            }
             tc_fence_after();
             int mb, nb;
             rows_tile_coords(un.t, a.m_tiles, a.n_tiles, mb, nb);
@@ -1592,6 +1664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
                                            __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])));
                 }
+                if (kStat) __stcg(a.ws_ss + (slot + un.piece) * kTtBM + row, ssr);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(accempty);
@@ -1634,6 +1707,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         acc.z += t4.z;
                         acc.w += t4.w;
                     }
+                    if (kStat) {
+                        // the row's sum of squares over the pieces, in piece order
+                        const float* ssrc = a.ws_ss + slot * kTtBM + r0 + rl;
+                        float tot = 0.f;
+                        for (int p3 = 0; p3 < P; ++p3) tot += __ldcg(ssrc + static_cast<size_t>(p3) * kTtBM);
+                        const float rr = rsqrtf(tot * inv_k + a.eps);
+                        acc.x *= rr;
+                        acc.y *= rr;
+                        acc.z *= rr;
+                        acc.w *= rr;
+                    }
                     if (m < a.M && n0 + col < a.N) {
                         uint2 o;
                         o.x = pack_bf16x2(acc.x, acc.y);
@@ -1651,13 +1735,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
             uint32_t pk[kRowsBN / 2];   // the row's outputs, packed as bf16x2
+            const float rr = kStat ? rsqrtf(ssr * inv_k + a.eps) : 1.f;
 #pragma unroll
             for (int c = 0; c < kRowsBN / 16; ++c) {
                 uint32_t v[16];
                 tmem_ld_32x16(taddr + c * 16, v);
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    pk[c * 8 + j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                    pk[c * 8 + j] = pack_bf16x2(__uint_as_float(v[2 * j]) * rr, __uint_as_float(v[2 * j + 1]) * rr);
             }
             tc_fence_before();
             __syncwarp();
@@ -1747,6 +1832,27 @@ __global__ void __launch_bounds__(kNormThreads)
     }
 }
 
+// ------------------------------------------------------------ gain folding
+// W'[k, n] = bf16(g[k] W[k, n]): the product of two bf16 values is exact in
+// fp32, so W' holds one rounding of it.  One thread per 8 columns of a row
+// (N a multiple of 8).
+__global__ void __launch_bounds__(kNormThreads)
+    fold_gain_kernel(const __nv_bfloat16* __restrict__ g, const __nv_bfloat16* W, __nv_bfloat16* Wg,
+                     int64_t K, int64_t N) {
+    const int64_t per_row = N / 8, total = K * per_row;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kNormThreads + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * kNormThreads) {
+        const int64_t k = i / per_row;
+        const float gk = __bfloat162float(g[k]);
+        const uint4 v = reinterpret_cast<const uint4*>(W)[i];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[j] = pack_bf16x2(bf16lo(w[j]) * gk, bf16hi(w[j]) * gk);
+        reinterpret_cast<uint4*>(Wg)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
 // Raises a kernel's dynamic shared-memory limit to the device's opt-in
 // maximum, once per (kernel slot, device).
 cudaError_t ensure_smem_attr(const void* func, int slot) {
@@ -1816,10 +1922,11 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
     if (lora && (glu || wnk)) return cudaErrorInvalidValue;
     if (a.tall) {
         if (fused || glu || wnk || lora || a.hilo || a.unscaled || split) return cudaErrorInvalidValue;
-        cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(tall_kernel), 22);
+        auto tk = a.fold ? tall_kernel<true> : tall_kernel<false>;
+        cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(tk), a.fold ? 28 : 22);
         if (e != cudaSuccess) return e;
         // cooperative with tail pieces, as the 128-row kernel
-        e = launch_ex(tall_kernel, a.grid, kTtSmem, 1, s, a.tail_tiles > 0, tmX, tmW, *a.tmY, y, a);
+        e = launch_ex(tk, a.grid, kTtSmem, 1, s, a.tail_tiles > 0, tmX, tmW, *a.tmY, y, a);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
@@ -1924,6 +2031,20 @@ cudaError_t launch_rmsnorm(const void* X, const void* g, void* Xn, int M, int K,
     rmsnorm_kernel<<<M, kNormThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(X),
                                              static_cast<const __nv_bfloat16*>(g),
                                              static_cast<__nv_bfloat16*>(Xn), K, eps);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fold_gain(const void* g, const void* W, void* Wg, int64_t K, int64_t N, cudaStream_t s) {
+    const int64_t total = K * (N / 8);
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaErrorInvalidDevice;
+    const int64_t want = (total + kNormThreads - 1) / kNormThreads;
+    const int grid = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(sms) * 8));
+    fold_gain_kernel<<<grid > 0 ? grid : 1, kNormThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(g),
+                                                                static_cast<const __nv_bfloat16*>(W),
+                                                                static_cast<__nv_bfloat16*>(Wg), K, N);
     return cudaGetLastError();
 }
 

@@ -63,6 +63,8 @@ struct RowsLaunch {
     int xrows, MP, stages;
     int grid;
     int tall;                  // 1: the 256-row kernel (plain form; m_tiles then counts 256-row tiles)
+    int fold;                  // 1 (with tall): W holds the gain folded in (W' = diag(g) W); the kernel
+                               // forms the row sums of squares and scales Y by 1/rms
     int pair;                  // 1: fused kernel for several row tiles, CTAs in clusters of two that
                                // take the two row blocks of each unit and share its W stages
                                // (tiles and tail tiles then count units of two row blocks)
@@ -84,6 +86,8 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
                         const RowsLaunch& a, cudaStream_t s);
 cudaError_t launch_rmsnorm(const void* X, const void* g, void* Xn, int M, int K, float eps,
                            cudaStream_t s);
+// W'[k, n] = bf16(g[k] * W[k, n]) for W, W' [K, N] (N a multiple of 8).
+cudaError_t launch_fold_gain(const void* g, const void* W, void* Wg, int64_t K, int64_t N, cudaStream_t s);
 
 // Copies the in-kernel status word to *out and clears it (synchronous).
 cudaError_t read_and_clear_status(int* out);
