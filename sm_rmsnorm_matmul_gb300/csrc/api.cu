@@ -725,12 +725,15 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
         const int units = a.m_tiles * a.n_tiles;
         const TailPlan t = plan_tail(units, std::min(units, sms), p.k_blocks, sms);
         a.grid = t.grid;
-        if (t.tiles > 0) {
+        if (t.tiles > 0 || fold) {
             constexpr size_t kPieceBytes = static_cast<size_t>(rmm::kTtBM) * rmm::kRowsBN * sizeof(float);
             const size_t pieces = static_cast<size_t>(t.tiles) * t.pieces;
-            // the folded form's partial row sums of squares (unfused: none)
-            const size_t ss_bytes = fold ? pieces * rmm::kTtBM * sizeof(float) : 0;
-            const size_t ncount = static_cast<size_t>(t.tiles) * 2;
+            // the folded form: the pieces' partial row sums of squares, then each
+            // row block's published r; counters: two per tail tile, then a flag
+            // and a reader count per row block (unfused: pieces' counters only)
+            const size_t rblocks = fold ? static_cast<size_t>(a.m_tiles) : 0;
+            const size_t ss_bytes = fold ? (pieces + rblocks) * rmm::kTtBM * sizeof(float) : 0;
+            const size_t ncount = static_cast<size_t>(t.tiles) * 2 + 2 * rblocks;
             if (fixed) {
                 if (!fixed->place(pieces * kPieceBytes, ss_bytes, &a.ws_acc, &a.ws_ss) ||
                     ncount * sizeof(int) > fixed->counter_bytes)
@@ -746,9 +749,11 @@ int run_contraction(bool fused, const void* X, const void* g, const void* W, voi
                 a.ws_ss = w.ss;
                 a.ws_count = w.counters;
             }
-            a.tail_tiles = t.tiles;
-            a.tail_pieces = t.pieces;
-            a.tail_kbp = t.kbp;
+            if (t.tiles > 0) {
+                a.tail_tiles = t.tiles;
+                a.tail_pieces = t.pieces;
+                a.tail_kbp = t.kbp;
+            }
         }
     } else if (fused && !p.cluster && p.xrows == rmm::kRowsBM) {
         if (!map_2d_store(&tmY, Y, M, hilo ? 2 * kBK : glu ? N / 2 : N)) return RMM_ERR_INTERNAL;

@@ -1441,6 +1441,40 @@ constexpr uint32_t kTtOffMisc = kTtOffSr + kTtBM * 4;
 constexpr uint32_t kTtSmem = kTtOffMisc + 16 + 1024;
 static_assert(kTtSmem <= 232448, "the tall-tile kernel's shared memory exceeds the opt-in limit");
 
+// kStat: how a tile gets its rows' statistic.  A row block's first column
+// tile (nb = 0), when whole, forms it and publishes r to the workspace
+// (kTtPublish); the row block's other whole tiles read it there (kTtRead) and
+// skip the extra pass over X; tail pieces form their partial sums
+// (kTtPiece); a whole tile whose row block's first tile is a tail tile forms
+// its own (kTtSelf).  A reader waits for the flag of a tile with a smaller
+// index, which its CTA or an earlier one reaches first, so the launch (all
+// CTAs resident: cooperative) cannot deadlock.
+enum { kTtSelf = 0, kTtPublish = 1, kTtRead = 2, kTtPiece = 3 };
+__device__ __forceinline__ int tt_tile_index(int mb, int nb, int m_tiles, int n_tiles) {
+    constexpr int G = 8;   // as rows_tile_coords
+    const int group = mb / G, first = group * G, gsz = min(m_tiles - first, G);
+    return group * G * n_tiles + nb * gsz + (mb - first);
+}
+__device__ __forceinline__ int tt_stat_mode(const RowsLaunch& a, const TaUnit& un, int mb, int nb) {
+    if (un.piece >= 0) return kTtPiece;
+    const int limit = a.m_tiles * a.n_tiles - a.tail_tiles;   // whole tiles: index < limit
+    if (tt_tile_index(mb, 0, a.m_tiles, a.n_tiles) >= limit) return kTtSelf;
+    return nb == 0 ? kTtPublish : kTtRead;
+}
+// whole tiles of row block mb that read its published r
+__device__ __forceinline__ int tt_readers(const RowsLaunch& a, int mb) {
+    const int limit = a.m_tiles * a.n_tiles - a.tail_tiles;
+    int n = 0;
+    for (int nb = 1; nb < a.n_tiles; ++nb) n += tt_tile_index(mb, nb, a.m_tiles, a.n_tiles) < limit;
+    return n;
+}
+// [m_tiles][256] published r, after the tail pieces' row sums
+__device__ __forceinline__ float* tt_r_base(const RowsLaunch& a) {
+    return a.ws_ss + static_cast<size_t>(a.tail_tiles) * a.tail_pieces * kTtBM;
+}
+// [m_tiles] flags, then [m_tiles] reader counts, after the tail counters
+__device__ __forceinline__ int* tt_flags(const RowsLaunch& a) { return a.ws_count + 2 * a.tail_tiles; }
+
 template <bool kStat>
 __global__ void __launch_bounds__(kThreads, 1)
     tall_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
@@ -1560,19 +1594,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ row sums of squares
         // Thread st of 64 takes rows st + 64 j of every A stage: the whole
         // row, its eight 16-byte pieces read from lane-rotated positions so
-        // that the eight lanes of an access phase hit distinct banks.
+        // that the eight lanes of an access phase hit distinct banks.  Tiles
+        // that read their row block's published r skip the reads (but keep
+        // step with the stages).
         const int st = threadIdx.x - 64;
         Ring ring(kTtStages);
-        uint32_t tl = 0;
+        uint32_t ts = 0;   // tiles whose sums went through sr
         bool ok = true;
         TaUnit un;
-        for (int i = 0; ok && ta_unit<1>(a, i, un); ++i, ++tl) {
+        for (int i = 0; ok && ta_unit<1>(a, i, un); ++i) {
+            int mb, nb;
+            rows_tile_coords(un.t, a.m_tiles, a.n_tiles, mb, nb);
+            const int mode = tt_stat_mode(a, un, mb, nb);
             float ss[4] = {0.f, 0.f, 0.f, 0.f};
             for (int kb = un.kb0; kb < un.kb1; ++kb) {
                 if (!warp_wait(full0 + 8 * ring.idx, ring.phase, abort)) { ok = false; break; }
                 const uint32_t stg = sb + ring.idx * kTtStageBytes;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
+                    if (mode == kTtRead) break;
                     const int r = st + 64 * j;
                     const uint32_t rowp = stg + (r >> 7) * (kTtXBytes / 2) + (r & 127) * 128;
 #pragma unroll
@@ -1594,12 +1634,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ring.advance();
             }
             if (!ok) break;
+            if (mode == kTtRead) continue;
             // the epilogue has read the previous tile's sums
-            if (tl > 0 && !warp_wait(srempty, (tl - 1) & 1, abort)) break;
+            if (ts > 0 && !warp_wait(srempty, (ts - 1) & 1, abort)) break;
 #pragma unroll
             for (int j = 0; j < 4; ++j) sr[st + 64 * j] = ss[j];
             __syncwarp();
             if (lane == 0) mbar_arrive(srfull);
+            ++ts;
+            if (mode == kTtPublish && tt_readers(a, mb) > 0) {
+                // the row block's r for its other tiles: values, then the flag
+                // (which the last of them resets)
+                float* rb = tt_r_base(a) + static_cast<size_t>(mb) * kTtBM;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) __stcg(rb + st + 64 * j, rsqrtf(ss[j] * (1.f / a.K) + a.eps));
+                named_bar_sync(1, 64);
+                if (st == 0) {
+                    __threadfence();
+                    atomicExch(tt_flags(a) + mb, 1);
+                }
+            }
         }
     } else if (warp >= 4) {
         // ------------------------------------------------ epilogue
@@ -1632,20 +1686,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t tl = 0;
         TaUnit un;
         const float inv_k = 1.f / static_cast<float>(a.K);
+        uint32_t ts = 0;   // (kStat) tiles whose sums came through sr
         for (int i = 0; ta_unit<1>(a, i, un); ++i, ++tl) {
             if (!warp_wait(accfull, tl & 1, abort)) break;
-            // kStat: this tile's (or piece's) row sum of squares
-            float ssr = 0.f;
-            if (kStat) {
-                if (!warp_wait(srfull, tl & 1, abort)) break;
-                ssr = sr[row];
-                __syncwarp();
-                if (lane == 0) mbar_arrive(srempty);
-            }
-            tc_fence_after();
             int mb, nb;
             rows_tile_coords(un.t, a.m_tiles, a.n_tiles, mb, nb);
             const int n0 = nb * kRowsBN, m0 = mb * kTtBM;
+            // kStat: this tile's (or piece's) row sum of squares, or the
+            // row block's r as its first tile published it
+            float ssr = 0.f, rr = 1.f;
+            if (kStat) {
+                if (tt_stat_mode(a, un, mb, nb) == kTtRead) {
+                    int* flag = tt_flags(a) + mb;
+                    if (!spin_until_ge(flag, 1, abort)) break;
+                    rr = __ldcg(tt_r_base(a) + static_cast<size_t>(mb) * kTtBM + row);
+                    // the last of the row block's readers resets its flag for the next call
+                    __syncwarp();
+                    if (lane == 0 && atomicAdd(flag + a.m_tiles, 1) == 8 * tt_readers(a, mb) - 1) {
+                        atomicExch(flag + a.m_tiles, 0);
+                        atomicExch(flag, 0);
+                    }
+                } else {
+                    if (!warp_wait(srfull, ts & 1, abort)) break;
+                    ssr = sr[row];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(srempty);
+                    ++ts;
+                    rr = rsqrtf(ssr * inv_k + a.eps);
+                }
+            }
+            tc_fence_after();
             if (un.piece >= 0) {
                 // A K piece of a tail tile: publish the fp32 partial, wait for
                 // the tile's other pieces, then reduce rows [r0, r1) of the
@@ -1735,7 +1805,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
             uint32_t pk[kRowsBN / 2];   // the row's outputs, packed as bf16x2
-            const float rr = kStat ? rsqrtf(ssr * inv_k + a.eps) : 1.f;
 #pragma unroll
             for (int c = 0; c < kRowsBN / 16; ++c) {
                 uint32_t v[16];
@@ -1926,7 +1995,8 @@ cudaError_t launch_rows(bool fused, const CUtensorMap& tmX, const CUtensorMap& t
         cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(tk), a.fold ? 28 : 22);
         if (e != cudaSuccess) return e;
         // cooperative with tail pieces, as the 128-row kernel
-        e = launch_ex(tk, a.grid, kTtSmem, 1, s, a.tail_tiles > 0, tmX, tmW, *a.tmY, y, a);
+        // (folded: tiles wait for their row block's first tile, in another CTA)
+        e = launch_ex(tk, a.grid, kTtSmem, 1, s, a.tail_tiles > 0 || a.fold != 0, tmX, tmW, *a.tmY, y, a);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
