@@ -576,6 +576,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--shapes", choices=["all", "none"], default="all")
+    ap.add_argument("--form", choices=["fused", "folded"], default="fused",
+                    help="the timed call: rmsnorm_matmul, or rmsnorm_matmul_folded on a W with the "
+                         "gain folded in once before timing (profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--reference-budget", type=float, default=90.0,
@@ -616,7 +619,8 @@ def main():
     with ClockSampler(gpu_id) as sampler:
         main_res = bench_workload(torch, rmm, inputs, w, args.steps, args.warmup, device,
                                   stream, l2, with_unfused=True, sampler=sampler,
-                                  barrier=barrier, replays=4 if ws == 1 else 0)
+                                  barrier=barrier, replays=4 if ws == 1 else 0,
+                                  folded=args.form == "folded")
         host = main_res["host"]
         e2e_steps = max(3, min(args.steps, 200))
         e2e_secs, h2d, d2h = e2e_bench(torch, rmm, w, host, device, stream, e2e_steps)
@@ -710,7 +714,8 @@ def main():
                 "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4)}
     roof["traffic"] = traffic_from_profile(w.name)
     roof["peak_source"] = peak_src
-    roof["kernel"] = kernel_name(rmm, w)
+    roof["kernel"] = (kernel_name(rmm, w) if args.form == "fused" or w.M <= 128
+                      else "tall_kernel<row statistic> (gain folded into W)")
     roof["algorithmic_bytes_per_launch"] = w.bytes_algorithmic
 
     out = {
@@ -735,6 +740,8 @@ def main():
                   if main_res["n_copies"] > 1 else
                   f"inputs ({w.bytes_algorithmic / 1e6:.0f} MB) larger than L2 ({l2 / 1e6:.0f} MB)",
             "timing": "CUDA graphs of back-to-back C-ABI calls, CUDA events on the launch stream",
+            "form": "rmsnorm_matmul" if args.form == "fused" else
+                    "rmsnorm_matmul_folded (gain folded into W once, before timing)",
             "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
         },
         "tflops": round(w.flops / t_step / 1e12, 2),
