@@ -201,8 +201,10 @@ int matmul(const void* A, const void* B, void* C,
  *   and partial row sums combined in piece order through a library-owned
  *   workspace, so the call may allocate device memory like rmsnorm_matmul()).
  *   Up to 128 rows it runs rmsnorm_matmul()'s kernels with a library-owned
- *   gain of ones (allocated on the first call with a longer K; that call may
- *   not be made during stream capture, which returns RMM_ERR_INTERNAL).
+ *   gain of ones (allocated on the first call with a longer K and kept, like
+ *   the workspaces, for the life of the process: that call may not be made
+ *   during stream capture, which returns RMM_ERR_INTERNAL, and the device may
+ *   not be reset while the library is in use).
  *   The result differs from rmsnorm_matmul(X, g, W)'s only in where the bf16
  *   rounding of the gain product falls (g*W instead of X*g).
  */
