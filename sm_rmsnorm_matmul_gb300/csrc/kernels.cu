@@ -1445,10 +1445,12 @@ static_assert(kTtSmem <= 232448, "the tall-tile kernel's shared memory exceeds t
 // tile (nb = 0), when whole, forms it and publishes r to the workspace
 // (kTtPublish); the row block's other whole tiles read it there (kTtRead) and
 // skip the extra pass over X; tail pieces form their partial sums
-// (kTtPiece); a whole tile whose row block's first tile is a tail tile forms
-// its own (kTtSelf).  A reader waits for the flag of a tile with a smaller
-// index, which its CTA or an earlier one reaches first, so the launch (all
-// CTAs resident: cooperative) cannot deadlock.
+// (kTtPiece).  A whole tile whose row block's first tile were a tail tile
+// would form its own (kTtSelf); with tail tiles the last indices and a row
+// block's first tile its smallest, that does not arise, but the check costs
+// nothing.  A reader waits for the flag of a tile with a smaller index, which
+// every CTA reaches before any larger one of its own, so the launch (all CTAs
+// resident: cooperative) cannot deadlock.
 enum { kTtSelf = 0, kTtPublish = 1, kTtRead = 2, kTtPiece = 3 };
 __device__ __forceinline__ int tt_tile_index(int mb, int nb, int m_tiles, int n_tiles) {
     constexpr int G = 8;   // as rows_tile_coords
