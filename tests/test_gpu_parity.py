@@ -480,3 +480,34 @@ def test_streams_are_honoured(rmm):
 
 def test_device_status_clean(rmm):
     assert rmm.device_status() == 0
+
+
+# ---------------------------------- paired, a last round of a few units
+# 2048 x 520 x 2560: 8 row-block pairs x 10 column tiles = 80 paired units on
+# 76 clusters of two: a second round of 4 units, in every paired form.
+@pytest.mark.parametrize("form", ["plain", "gated", "weight_nk", "lora"])
+def test_paired_small_last_round(rmm, form):
+    from sm_rmsnorm_matmul_gb300 import inputs
+    M, K, N = 2048, 520, 2560
+    if form == "lora":
+        X, g, W, A, B = inputs.lora_problem(M, K, N, 40, seed=7)
+        Y = rmm.rmsnorm_matmul_lora(X.cuda(), g.cuda(), W.cuda(), A.cuda(), B.cuda(), 1e-5)
+        torch.cuda.synchronize()
+        assert rmm.device_status() == 0
+        assert_close(Y.cpu(), oracle.rmsnorm_matmul_lora(X, g, W, A, B, 1e-5), "lora, small last round")
+        return
+    X, g, W = inputs.random_problem(M, K, N, seed=5, x_kind="row_scaled")
+    Xd, gd = X.cuda(), g.cuda()
+    if form == "gated":
+        Y = rmm.rmsnorm_matmul_swiglu(Xd, gd, W.cuda(), 1e-5)
+        torch.cuda.synchronize()
+        assert rmm.device_status() == 0
+        assert_gated_close(Y.cpu(), X, g, W, 1e-5, "gated, small last round")
+        return
+    Wd = W.t().contiguous().cuda() if form == "weight_nk" else W.cuda()
+    Y = rmm.rmsnorm_matmul_ex(Xd, gd, Wd, 1e-5, weight_nk=form == "weight_nk")
+    torch.cuda.synchronize()
+    assert rmm.device_status() == 0
+    assert_close(Y.cpu(), oracle.rmsnorm_matmul(X, g, W, 1e-5), f"{form}, small last round")
+    # deterministic: the same bits again
+    assert torch.equal(Y, rmm.rmsnorm_matmul_ex(Xd, gd, Wd, 1e-5, weight_nk=form == "weight_nk"))
