@@ -98,3 +98,32 @@ def test_folded_rows_of_zeros(rmm):
     Y = folded(rmm, X, g, W, 1e-6)
     assert torch.count_nonzero(Y[5]) == 0 and torch.count_nonzero(Y[290]) == 0
     assert_close(Y, oracle.rmsnorm_matmul(X, g, W, 1e-6), "zero rows")
+
+
+def test_folded_beside_another_stream_holding_sms(rmm):
+    """Tiles wait for their row block's published r, so the folded launch is
+    cooperative: all its CTAs are resident together even while kernels on
+    another stream hold SMs; the call completes with a clean status and the
+    right result, and calls on two streams (each with its own workspace)
+    both do."""
+    from sm_rmsnorm_matmul_gb300 import inputs
+    M, K, N = 2048, 1024, 4096
+    X, g, W = inputs.random_problem(M, K, N, seed=31, x_kind="row_scaled")
+    Xd, Wg = X.cuda(), rmm.fold_gain(g.cuda(), W.cuda())
+    a = torch.randn(8192, 8192, device="cuda", dtype=torch.bfloat16)
+    other = torch.cuda.Stream()
+    second = torch.cuda.Stream()
+    main = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(other):
+        for _ in range(8):      # a few milliseconds of full-device GEMMs
+            a = (a @ a).clamp_(-1, 1)
+    Y = rmm.rmsnorm_matmul_folded(Xd, Wg, 1e-6, stream=main)
+    Y2 = rmm.rmsnorm_matmul_folded(Xd, Wg, 1e-6, stream=second)
+    other.synchronize()
+    second.synchronize()
+    main.synchronize()
+    assert rmm.device_status() == 0
+    ref = oracle.rmsnorm_matmul(X, g, W, 1e-6)
+    assert_close(Y.cpu(), ref, "folded beside another stream")
+    assert torch.equal(Y, Y2)
