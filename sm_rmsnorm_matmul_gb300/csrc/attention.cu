@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kHeadsWarps * 32)
 constexpr int kAttThreads = 352;    // warp 0 TMA, 1 MMA A + TMEM, 2-5 softmax A, 6-9 softmax B, 10 MMA B
 constexpr int kAttStages = 2;       // K and V slots
 constexpr uint32_t kAttBox = kAttBM * 64 * 2;      // 16 KB: [128 rows][64 columns], one SW128 box
-constexpr uint32_t kAttNumBars = 18;
+constexpr uint32_t kAttNumBars = 20;
 static_assert(kAttNumBars * 8 <= 256, "barrier area");
 // Shared memory for head dimension D: query tiles A and B, two K and two V
 // tiles (each [128][D]), barriers, the TMEM address and abort words.
@@ -259,7 +259,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     auto kv_empty = [&](uint32_t i) { return bar0 + 40 + 8 * i; };
     auto turn = [&](int x) { return bar0 + 56 + 8 * x; };      // issuer x may issue
     auto s_full = [&](int x) { return bar0 + 72 + 8 * x; };
-    auto p_full = [&](int x) { return bar0 + 88 + 8 * x; };
+    // P of keys 64h .. 64h + 63 of tile x is in tensor memory
+    auto p_full = [&](int x, int h) { return h ? bar0 + 144 + 8 * x : bar0 + 88 + 8 * x; };
     auto o_final = [&](int x) { return bar0 + 104 + 8 * x; };
     auto o_empty = [&](int x) { return bar0 + 120 + 8 * x; };
     const uint32_t mmadone = bar0 + 136;
@@ -282,7 +283,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             mbar_init(kv_empty(x), 2);   // one commit per issuer
             mbar_init(turn(x), 1);
             mbar_init(s_full(x), 1);
-            mbar_init(p_full(x), 4);     // one lane per softmax warp
+            mbar_init(p_full(x, 0), 4);  // one lane per softmax warp
+            mbar_init(p_full(x, 1), 4);
             mbar_init(o_final(x), 1);
             mbar_init(o_empty(x), 4);
         }
@@ -442,7 +444,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                 for (int j = 0; j < cur.nkv; ++j, ++g) {
                     const uint32_t st = g & 1;
                     if (!mbar_wait(kv_full(st), (g >> 1) & 1, abort)) { ok = false; break; }
-                    if (j < n && !mbar_wait(p_full(x), pi & 1, abort)) { ok = false; break; }
+                    if (j < n && !mbar_wait(p_full(x, 0), pi & 1, abort)) { ok = false; break; }
                     // the first P V of a block overwrites O: the previous
                     // block's epilogue has read it (one arrival per block)
                     if (j == 0 && n > 0 && t > 0 && !mbar_wait(o_empty(x), (t - 1) & 1, abort)) {
@@ -458,19 +460,23 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                     // The turn passes four MMAs before the end of this issuer's
                     // work for the stage: the other issuer wakes while they
                     // are issued (its own MMAs do not depend on these).
+                    // The P V of the first 64 keys runs while the softmax
+                    // computes the second half of P.
                     if (j < n) {
+                        pv_steps(st, j > 0, 0, 4);
+                        if (!mbar_wait(p_full(x, 1), pi & 1, abort)) { ok = false; break; }
+                        tc_fence_after();
                         ++pi;
                         if (j + 1 < n) {
-                            pv_steps(st, j > 0, 0, kAttBN / 16);
+                            pv_steps(st, true, 4, kAttBN / 16);
                             s_steps((g + 1) & 1, 0, 4);
                             mbar_arrive(turn(x ^ 1));
                             s_steps((g + 1) & 1, 4, kD / 16);
                             mma_commit(s_full(x));
                             if (j + 2 == n) mma_commit(q_empty);   // that was the last score product
                         } else {
-                            pv_steps(st, j > 0, 0, 4);
                             mbar_arrive(turn(x ^ 1));
-                            pv_steps(st, j > 0, 4, kAttBN / 16);
+                            pv_steps(st, true, 4, kAttBN / 16);
                             mma_commit(o_final(x));
                         }
                     } else {
@@ -546,16 +552,21 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                     for (int i = 0; i < kAttBN; ++i)
                         if (i >= lim) v[i] = 0xff800000u;   // -inf
                 }
-                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                // eight independent chains of three-input maxima
+                float mx[8];
 #pragma unroll
-                for (int i = 0; i < kAttBN; i += 8) {
-                    mx[0] = max3f(mx[0], __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
-                    mx[1] = max3f(mx[1], __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
-                    mx[2] = max3f(mx[2], __uint_as_float(v[i + 4]), __uint_as_float(v[i + 5]));
-                    mx[3] = max3f(mx[3], __uint_as_float(v[i + 6]), __uint_as_float(v[i + 7]));
-                }
+                for (int c = 0; c < 8; ++c) mx[c] = max3f(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]),
+                                                          __uint_as_float(v[16 + 2 * c]));
+#pragma unroll
+                for (int i = 32; i < kAttBN; i += 16)
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        mx[c] = max3f(mx[c], __uint_as_float(v[i + 2 * c]), __uint_as_float(v[i + 2 * c + 1]));
+#pragma unroll
+                for (int c = 0; c < 8; ++c) mx[c] = fmaxf(mx[c], __uint_as_float(v[17 + 2 * c]));
                 // rc > 0: the maximum of the scaled scores is rc times the maximum
-                const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * rc;
+                const float m_tile = fmaxf(fmaxf(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5])),
+                                           fmaxf(mx[6], mx[7])) * rc;
                 float alpha = 1.f;
                 bool rescale = false;
                 if (j == 0) {
@@ -568,35 +579,43 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                     l *= alpha;
                     rescale = true;
                 }
+                // P in two halves of 64 keys (32 columns each), each handed
+                // over as soon as it is stored: the P V of the first half
+                // runs during the second half's exponentials
                 const uint64_t negm = pack_f32x2(-m_ref, -m_ref);
                 uint64_t acc[4] = {0, 0, 0, 0};   // packed partial row sums (0.0f pairs)
-                uint32_t pk[kAttBN / 2];
 #pragma unroll
-                for (int i = 0; i < kAttBN / 2; ++i) {
-                    const uint64_t d = fma_f32x2(pack_f32x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
-                                                 rc2, negm);
-                    const float p0 = ex2_approx(lo_f32(d)), p1 = ex2_approx(hi_f32(d));
-                    acc[i & 3] = add_f32x2(acc[i & 3], pack_f32x2(p0, p1));
-                    pk[i] = pack_bf16x2(p0, p1);
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t pk[kAttBN / 4];
+#pragma unroll
+                    for (int i = 0; i < kAttBN / 4; ++i) {
+                        const int e = hf * (kAttBN / 2) + 2 * i;
+                        const uint64_t d = fma_f32x2(pack_f32x2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                                                     rc2, negm);
+                        const float p0 = ex2_approx(lo_f32(d)), p1 = ex2_approx(hi_f32(d));
+                        acc[i & 3] = add_f32x2(acc[i & 3], pack_f32x2(p0, p1));
+                        pk[i] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st_32x32(sbuf + hf * (kAttBN / 4), pk);
+                    if (hf == 0 && __any_sync(0xffffffffu, rescale)) {
+                        // O holds this block's P_0..P_{j-1} V, complete: S_j was
+                        // issued after the last of those products and has
+                        // completed; P_j V starts once the first half is handed over
+#pragma unroll 1
+                        for (int cc = 0; cc < kD / 32; ++cc) {
+                            uint32_t o[32];
+                            tmem_ld_32x32(obuf + cc * 32, o);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                            tmem_st_32x32(obuf + cc * 32, o);
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(p_full(x, hf));
                 }
-                tmem_st_32x32_x64(sbuf, pk);
                 const uint64_t tsum = add_f32x2(add_f32x2(acc[0], acc[1]), add_f32x2(acc[2], acc[3]));
                 l += lo_f32(tsum) + hi_f32(tsum);
-                if (__any_sync(0xffffffffu, rescale)) {
-                    // O holds this block's P_0..P_{j-1} V, complete: S_j was
-                    // issued after the last of those products and has completed
-#pragma unroll 1
-                    for (int cc = 0; cc < kD / 32; ++cc) {
-                        uint32_t o[32];
-                        tmem_ld_32x32(obuf + cc * 32, o);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tmem_st_32x32(obuf + cc * 32, o);
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(p_full(x));
             }
             if (!ok) break;
             // ------------------------------------------------ epilogue: O / l -> bf16 -> global
