@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kHeadsWarps * 32)
 constexpr int kAttThreads = 352;    // warp 0 TMA, 1 MMA A + TMEM, 2-5 softmax A, 6-9 softmax B, 10 MMA B
 constexpr int kAttStages = 2;       // K and V slots
 constexpr uint32_t kAttBox = kAttBM * 64 * 2;      // 16 KB: [128 rows][64 columns], one SW128 box
-constexpr uint32_t kAttNumBars = 20;
+constexpr uint32_t kAttNumBars = 26;
 static_assert(kAttNumBars * 8 <= 256, "barrier area");
 // Shared memory for head dimension D: query tiles A and B, two K and two V
 // tiles (each [128][D]), barriers, the TMEM address and abort words.
@@ -206,8 +206,11 @@ constexpr uint32_t att_tile_bytes(int D) { return kAttBM * D * 2; }
 constexpr uint32_t att_off_bar(int D) { return (2 + 2 * kAttStages) * att_tile_bytes(D); }
 constexpr uint32_t att_smem_bytes(int D) { return att_off_bar(D) + 256 + 16 + 1024; }   // + alignment slack
 // Tensor memory, per query tile x (columns x * 256 ..): the score buffer S
-// (P overwrites its first 64 columns, two bf16 per column), then O (D columns).
+// (128 columns), then O (D columns).  P (two bf16 per column, 64 columns)
+// overwrites the first half of S for D = 128; for D = 64 it has the last 64
+// columns to itself, so the next S can be computed while P is.
 constexpr uint32_t kAttColO = 128, kAttTmemCols = 512;
+constexpr uint32_t att_col_p(int D) { return D == 64 ? kAttColO + 64 : 0; }
 constexpr float kAttRescale = 8.f;   // rescale O only when the row max grows by > 2^8
 
 // One block of 256 query rows of one head of one sequence.
@@ -243,6 +246,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                             const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV, AttnLaunch a) {
     static_assert(kD == 64 || kD == 128, "head dimension");
+    // P apart from S: the next score product does not wait for this P V
+    constexpr bool kPSep = att_col_p(kD) != 0;
     constexpr uint32_t kTile = att_tile_bytes(kD);   // a Q, K or V tile
     constexpr int kBoxes = kD / 64;                  // SW128 boxes of 64 columns per tile
     constexpr uint32_t kOffK = 2 * kTile, kOffV = kOffK + kAttStages * kTile;
@@ -261,6 +266,9 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     auto s_full = [&](int x) { return bar0 + 72 + 8 * x; };
     // P of keys 64h .. 64h + 63 of tile x is in tensor memory
     auto p_full = [&](int x, int h) { return h ? bar0 + 144 + 8 * x : bar0 + 88 + 8 * x; };
+    // (P apart from S) the softmax has read S / the P V of key half h has completed
+    auto s_empty = [&](int x) { return bar0 + 160 + 8 * x; };
+    auto pv_done = [&](int x, int h) { return bar0 + 176 + 8 * (2 * x + h); };
     auto o_final = [&](int x) { return bar0 + 104 + 8 * x; };
     auto o_empty = [&](int x) { return bar0 + 120 + 8 * x; };
     const uint32_t mmadone = bar0 + 136;
@@ -285,6 +293,9 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             mbar_init(s_full(x), 1);
             mbar_init(p_full(x, 0), 4);  // one lane per softmax warp
             mbar_init(p_full(x, 1), 4);
+            mbar_init(s_empty(x), 4);
+            mbar_init(pv_done(x, 0), 1);
+            mbar_init(pv_done(x, 1), 1);
             mbar_init(o_final(x), 1);
             mbar_init(o_empty(x), 4);
         }
@@ -404,9 +415,19 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                     mma_bf16_ss(dS, dq + off, b0 + off, idesc_s, kk > 0);
                 }
             };
-            auto issue_s = [&](uint32_t kslot) {
+            uint32_t ns = 0;   // score tiles issued (P apart from S)
+            auto issue_s = [&](uint32_t kslot) -> bool {
+                if constexpr (kPSep) {
+                    // the score buffer is free once the softmax has read the last S
+                    if (ns > 0) {
+                        if (!mbar_wait(s_empty(x), (ns - 1) & 1, abort)) return false;
+                        tc_fence_after();
+                    }
+                    ++ns;
+                }
                 s_steps(kslot, 0, kD / 16);
                 mma_commit(s_full(x));
+                return true;
             };
             // O_x += P V: A = P from tensor memory (keys 16kk.. in columns
             // 8kk..), B = V MN-major (dims contiguous), steps k0 .. k1 - 1 of 8
@@ -415,14 +436,15 @@ __global__ void __launch_bounds__(kAttThreads, 1)
 #pragma unroll
                 for (int kk = k0; kk < k1; ++kk) {
                     const uint64_t off = ((kk >> 2) * (kTile / 2) + (kk & 3) * 2048) >> 4;
-                    mma_bf16_ts(dS + kAttColO, dS + kk * 8, b0 + off, idesc_o, acc || kk > 0);
+                    mma_bf16_ts(dS + kAttColO, dS + att_col_p(kD) + kk * 8, b0 + off, idesc_o, acc || kk > 0);
                 }
             };
             // the first score product of a block; a query tile with at most
             // one key tile has then read its query tile for the last time
-            auto begin_block = [&](const AttnBlock& B, uint32_t kslot) {
-                if (B.n(x) > 0) issue_s(kslot);
+            auto begin_block = [&](const AttnBlock& B, uint32_t kslot) -> bool {
+                if (B.n(x) > 0 && !issue_s(kslot)) return false;
                 if (B.n(x) <= 1) mma_commit(q_empty);
+                return true;
             };
             uint32_t g = 0, t = 0, pi = 0;   // stages, blocks, P tiles consumed
             const bool any = block_id(0) >= 0;
@@ -430,7 +452,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             bool ok = any && mbar_wait(k0_full, 0, abort) && mbar_wait(q_full, 0, abort);
             if (ok) {
                 tc_fence_after();
-                begin_block(cur, 0);
+                ok = begin_block(cur, 0);
                 mma_commit(kv_empty(1));   // the first K_0 read: "stage -1" of slot 1
             }
             // Each issuer waits for stage g before releasing it, so neither
@@ -444,6 +466,38 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                 for (int j = 0; j < cur.nkv; ++j, ++g) {
                     const uint32_t st = g & 1;
                     if (!mbar_wait(kv_full(st), (g >> 1) & 1, abort)) { ok = false; break; }
+                    if constexpr (kPSep) {
+                        // S_{j+1} as soon as the softmax has read S_j, then
+                        // P_j V in two halves as P_j's halves arrive (no turns:
+                        // the softmax does not wait for P V)
+                        if (j < n) {
+                            if (j + 1 < n) {
+                                if (!issue_s((g + 1) & 1)) { ok = false; break; }
+                                if (j + 2 == n) mma_commit(q_empty);   // the last score product
+                            }
+                            if (j == 0 && t > 0 && !mbar_wait(o_empty(x), (t - 1) & 1, abort)) {
+                                ok = false;
+                                break;
+                            }
+                            if (!mbar_wait(p_full(x, 0), pi & 1, abort)) { ok = false; break; }
+                            tc_fence_after();
+                            pv_steps(st, j > 0, 0, 4);
+                            mma_commit(pv_done(x, 0));
+                            if (!mbar_wait(p_full(x, 1), pi & 1, abort)) { ok = false; break; }
+                            tc_fence_after();
+                            ++pi;
+                            pv_steps(st, true, 4, kAttBN / 16);
+                            mma_commit(pv_done(x, 1));
+                            if (j + 1 == n) mma_commit(o_final(x));
+                        }
+                        if (j + 1 == cur.nkv && has_next) {
+                            if (!mbar_wait(q_full, (t + 1) & 1, abort)) { ok = false; break; }
+                            tc_fence_after();
+                            if (!begin_block(nxt, (g + 1) & 1)) { ok = false; break; }
+                        }
+                        mma_commit(kv_empty(st));
+                        continue;
+                    }
                     if (j < n && !mbar_wait(p_full(x, 0), pi & 1, abort)) { ok = false; break; }
                     // the first P V of a block overwrites O: the previous
                     // block's epilogue has read it (one arrival per block)
@@ -489,7 +543,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                         // during this stage, and its K_0, in this stage
                         if (!mbar_wait(q_full, (t + 1) & 1, abort)) { ok = false; break; }
                         tc_fence_after();
-                        begin_block(nxt, (g + 1) & 1);
+                        if (!begin_block(nxt, (g + 1) & 1)) { ok = false; break; }
                     }
                     mma_commit(kv_empty(st));
                 }
@@ -543,6 +597,11 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                 tc_fence_after();
                 uint32_t v[kAttBN];
                 tmem_ld_32x32_x128(sbuf, v);
+                if constexpr (kPSep) {   // S is in registers: the buffer may take the next S
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(s_empty(x));
+                }
                 // keys past the sequence end, and after the query when causal
                 const int kbase = j * kAttBN;
                 int lim = min(kAttBN, a.S - kbase);
@@ -596,11 +655,22 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                         acc[i & 3] = add_f32x2(acc[i & 3], pack_f32x2(p0, p1));
                         pk[i] = pack_bf16x2(p0, p1);
                     }
-                    tmem_st_32x32(sbuf + hf * (kAttBN / 4), pk);
+                    // (P apart from S) the last tile's P V has read this half
+                    if (kPSep && si > 0 && !warp_wait(pv_done(x, hf), (si - 1) & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tmem_st_32x32(sbuf + att_col_p(kD) + hf * (kAttBN / 4), pk);
                     if (hf == 0 && __any_sync(0xffffffffu, rescale)) {
-                        // O holds this block's P_0..P_{j-1} V, complete: S_j was
-                        // issued after the last of those products and has
-                        // completed; P_j V starts once the first half is handed over
+                        // (P apart from S) O must hold all of the last tile's P V
+                        if (kPSep && !warp_wait(pv_done(x, 1), (si - 1) & 1, abort)) {
+                            ok = false;
+                            break;
+                        }
+                        // O holds this block's P_0..P_{j-1} V, complete (with P
+                        // in S: S_j was issued after the last of those products
+                        // and has completed); P_j V starts once the first half
+                        // is handed over
 #pragma unroll 1
                         for (int cc = 0; cc < kD / 32; ++cc) {
                             uint32_t o[32];
@@ -614,6 +684,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(p_full(x, hf));
                 }
+                if (!ok) break;
                 const uint64_t tsum = add_f32x2(add_f32x2(acc[0], acc[1]), add_f32x2(acc[2], acc[3]));
                 l += lo_f32(tsum) + hi_f32(tsum);
             }

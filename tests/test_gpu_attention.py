@@ -152,12 +152,14 @@ def test_first_causal_row_is_first_value(rmm):
     assert torch.equal(O[:, 0], want)
 
 
-def test_rescaled_rows(rmm):
+@pytest.mark.parametrize("D", [128, 64])
+def test_rescaled_rows(rmm, D):
     # every query of a head equals one direction u and so does one late key:
     # that key's score dwarfs the first tile's, so the running maximum jumps
-    # by far more than 2^8 and the accumulator is rescaled
+    # by far more than 2^8 and the accumulator is rescaled (for D = 64 after
+    # the previous tile's P V, which P apart from S lets run late, completes)
     from sm_rmsnorm_matmul_gb300 import inputs
-    B, S, Hq, Hkv, D = 1, 700, 2, 1, 128
+    B, S, Hq, Hkv = 1, 700, 2, 1
     qkv, gq, gk = inputs.attention_inputs(B, S, Hq, Hkv, D, 21)
     gq = torch.full((D,), 1.5, dtype=torch.bfloat16)
     gk = torch.full((D,), 1.5, dtype=torch.bfloat16)
@@ -188,13 +190,15 @@ def test_explicit_scale_and_eps(rmm):
     assert_attention_close(O.cpu(), Q, K, V, gq, gk, 0.25, False, "explicit scale and eps", scale=1.0 / 16)
 
 
+@pytest.mark.parametrize("D", [128, 64])
 @pytest.mark.parametrize("B,S,Hq,Hkv,causal", [
     (2, 2048, 16, 4, False),   # full attention, two sequences
     (1, 3000, 32, 8, True),    # ragged length: the last block half past the end, a partial last band
 ])
-def test_large_sampled_rows(rmm, B, S, Hq, Hkv, causal):
+def test_large_sampled_rows(rmm, B, S, Hq, Hkv, causal, D):
+    """Several blocks per CTA: the key stream, the score buffer and (D = 64)
+    the P columns carry over from one block to the next."""
     from sm_rmsnorm_matmul_gb300 import inputs
-    D = 128
     qkv, gq, gk = inputs.attention_inputs(B, S, Hq, Hkv, D, seed=S + Hq)
     Q, K, V = inputs.split_qkv(qkv, B, S, Hq, Hkv, D)
     Qd, Kd, Vd = inputs.split_qkv(qkv.cuda(), B, S, Hq, Hkv, D)
@@ -222,11 +226,13 @@ def test_output_row_stride(rmm):
     assert bool((wide[:, Hq * D:] == 7.0).all())
 
 
-def test_full_size_sampled_rows(rmm):
-    # the benchmark's workload (one 4096-token sequence, 32 query heads over
+@pytest.mark.parametrize("name", ["prefill_attention_1x4096_h32_kv8_d128_causal",
+                                  "prefill_attention_1x4096_h32_kv8_d64_causal"])
+def test_full_size_sampled_rows(rmm, name):
+    # the benchmark's workloads (one 4096-token sequence, 32 query heads over
     # 8 key/value heads, causal), sampled query positions checked one by one
     from sm_rmsnorm_matmul_gb300 import inputs
-    w = inputs.ATTENTION_WORKLOADS["prefill_attention_1x4096_h32_kv8_d128_causal"]
+    w = inputs.ATTENTION_WORKLOADS[name]
     qkv, gq, gk = inputs.attention_inputs(w.B, w.S, w.Hq, w.Hkv, w.D, w.seed)
     Q, K, V = inputs.split_qkv(qkv, w.B, w.S, w.Hq, w.Hkv, w.D)
     Qd, Kd, Vd = inputs.split_qkv(qkv.cuda(), w.B, w.S, w.Hq, w.Hkv, w.D)
