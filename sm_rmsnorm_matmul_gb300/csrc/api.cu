@@ -1108,6 +1108,8 @@ int qknorm_attention(const void* Q, int64_t ldq, const void* K, int64_t ldk, con
     a.O = O;
     a.ldo = ldo;
     a.test_skip_loads = g_skip_sends.load();
+    a.gq = gq;
+    a.gk = gk;
     return rmm::launch_qknorm_attention(tmQ, tmK, tmV, a, stream) == cudaSuccess
                ? RMM_OK
                : RMM_ERR_LAUNCH;

@@ -212,6 +212,11 @@ constexpr uint32_t att_smem_bytes(int D) { return att_off_bar(D) + 256 + 16 + 10
 constexpr uint32_t kAttColO = 128, kAttTmemCols = 512;
 constexpr uint32_t att_col_p(int D) { return D == 64 ? kAttColO + 64 : 0; }
 constexpr float kAttRescale = 8.f;   // rescale O only when the row max grows by > 2^8
+// Scores of normalised queries and keys are bounded (Cauchy-Schwarz): with
+// G = max_i |gq_i gk_i|, |rc S| <= qscale * D * G.  Up to a bound of 50 (in
+// log2 units) every softmax weight 2^(s - bound) stays above 2^-100, a normal
+// float, and the bound serves as the reference instead of a running maximum.
+constexpr float kAttBoundMax = 50.f;
 
 // One block of 256 query rows of one head of one sequence.
 struct AttnBlock {
@@ -563,6 +568,17 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         const uint32_t sbuf = tmem + x * 256 + lane_base;
         const uint32_t obuf = sbuf + kAttColO;
         uint32_t t = 0, si = 0, ob = 0;   // blocks, S tiles consumed, blocks with output
+        // G = max |gq_i gk_i| (the same in every CTA, so is the choice below)
+        float gm = 0.f;
+        for (int i = lane; i < kD; i += 32)
+            gm = fmaxf(gm, fabsf(__bfloat162float(static_cast<const __nv_bfloat16*>(a.gq)[i]) *
+                                 __bfloat162float(static_cast<const __nv_bfloat16*>(a.gk)[i])));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
+        // the bound, with a margin for the bf16 rounding of the keys and the
+        // accumulation order
+        gm *= 1.f + 1.f / 64;
+        const bool bounded = a.qscale * kD * gm <= kAttBoundMax;
         bool ok = true;
         for (int r = 0; ok && block_id(r) >= 0; ++r, ++t) {
             const AttnBlock B = attn_block(a, block_id(r));
@@ -588,7 +604,9 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             if (lane == 0) mbar_arrive(q_empty);
             const float rc = rsqrtf(((ss[0] + ss[1]) + (ss[2] + ss[3])) * (1.f / kD) + a.eps) * a.qscale;
             const uint64_t rc2 = pack_f32x2(rc, rc);
-            float m_ref = 0.f, l = 0.f;
+            // bounded: this row's own bound, rc |Q_row| sqrt(D) G (at most qscale D G)
+            float m_ref = bounded ? rc * sqrtf(((ss[0] + ss[1]) + (ss[2] + ss[3])) * kD) * gm : 0.f;
+            float l = 0.f;
             for (int j = 0; j < n; ++j, ++si) {
                 if (!warp_wait(s_full(x), si & 1, abort)) {
                     ok = false;
@@ -611,32 +629,35 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                     for (int i = 0; i < kAttBN; ++i)
                         if (i >= lim) v[i] = 0xff800000u;   // -inf
                 }
-                // eight independent chains of three-input maxima
-                float mx[8];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) mx[c] = max3f(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]),
-                                                          __uint_as_float(v[16 + 2 * c]));
-#pragma unroll
-                for (int i = 32; i < kAttBN; i += 16)
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        mx[c] = max3f(mx[c], __uint_as_float(v[i + 2 * c]), __uint_as_float(v[i + 2 * c + 1]));
-#pragma unroll
-                for (int c = 0; c < 8; ++c) mx[c] = fmaxf(mx[c], __uint_as_float(v[17 + 2 * c]));
-                // rc > 0: the maximum of the scaled scores is rc times the maximum
-                const float m_tile = fmaxf(fmaxf(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5])),
-                                           fmaxf(mx[6], mx[7])) * rc;
                 float alpha = 1.f;
                 bool rescale = false;
-                if (j == 0) {
-                    m_ref = m_tile == -INFINITY ? 0.f : m_tile;
-                } else if (m_tile > m_ref + kAttRescale) {
-                    // weights stay below 2^8 relative to m_ref; beyond that the
-                    // reference moves and O and l are scaled down to it
-                    alpha = ex2_approx(m_ref - m_tile);
-                    m_ref = m_tile;
-                    l *= alpha;
-                    rescale = true;
+                if (!bounded) {
+                    // a running maximum: eight independent chains of three-input maxima
+                    float mx[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        mx[c] = max3f(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]),
+                                      __uint_as_float(v[16 + 2 * c]));
+#pragma unroll
+                    for (int i = 32; i < kAttBN; i += 16)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            mx[c] = max3f(mx[c], __uint_as_float(v[i + 2 * c]), __uint_as_float(v[i + 2 * c + 1]));
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) mx[c] = fmaxf(mx[c], __uint_as_float(v[17 + 2 * c]));
+                    // rc > 0: the maximum of the scaled scores is rc times the maximum
+                    const float m_tile = fmaxf(fmaxf(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5])),
+                                               fmaxf(mx[6], mx[7])) * rc;
+                    if (j == 0) {
+                        m_ref = m_tile == -INFINITY ? 0.f : m_tile;
+                    } else if (m_tile > m_ref + kAttRescale) {
+                        // weights stay below 2^8 relative to m_ref; beyond that the
+                        // reference moves and O and l are scaled down to it
+                        alpha = ex2_approx(m_ref - m_tile);
+                        m_ref = m_tile;
+                        l *= alpha;
+                        rescale = true;
+                    }
                 }
                 // P in two halves of 64 keys (32 columns each), each handed
                 // over as soon as it is stored: the P V of the first half

@@ -138,6 +138,8 @@ struct AttnLaunch {
     void* O;          // output [B, S, Hq, D], row stride ldo elements
     long long ldo;
     int test_skip_loads;   // test hook: the producer leaves out its first K/V stage
+    const void* gq;   // the query and key gains [D] (bf16): they bound the scores
+    const void* gk;
 };
 
 // Y[t,h,:] = RMSNorm(X[t,h,:]; g, eps) * g2 for T rows of H heads of D

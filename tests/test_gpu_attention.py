@@ -144,25 +144,44 @@ def test_qknorm_attention_head_dim_64(rmm, B, S, Hq, Hkv, causal):
     assert_attention_close(O, Q, K, V, gq, gk, 1e-6, causal, f"D=64 attention {B}x{S} {Hq}/{Hkv}")
 
 
-def test_first_causal_row_is_first_value(rmm):
-    # one visible key: softmax weight exactly 1, O = bf16(V[0]) exactly
-    O, Q, K, V, gq, gk = run(rmm, 1, 64, 4, 2, True, seed=9)
-    rep = 2
-    want = V[:, 0].repeat_interleave(rep, dim=1)
-    assert torch.equal(O[:, 0], want)
+@pytest.mark.parametrize("gain_scale", [1.0, 2.5])
+def test_first_causal_row_is_first_value(rmm, gain_scale):
+    """One visible key: softmax weight 1, O = V[0].  With the scores' bound as
+    the reference (gains U(0.5, 1.5)) the weight is 2^(s - bound), rounded to
+    bf16 for P V but summed unrounded, so O is V[0] within one bf16 unit in
+    the last place; with a running maximum (gains 2.5 times larger) the
+    weight is 2^0 = 1 and O = V[0] exactly."""
+    from sm_rmsnorm_matmul_gb300 import inputs
+    B, S, Hq, Hkv, D = 1, 64, 4, 2, 128
+    qkv, gq, gk = inputs.attention_inputs(B, S, Hq, Hkv, D, 9)
+    gq = (gq.float() * gain_scale).to(torch.bfloat16)
+    gk = (gk.float() * gain_scale).to(torch.bfloat16)
+    _, _, V = inputs.split_qkv(qkv, B, S, Hq, Hkv, D)
+    Qd, Kd, Vd = inputs.split_qkv(qkv.cuda(), B, S, Hq, Hkv, D)
+    O = rmm.qknorm_attention(Qd, Kd, Vd, gq.cuda(), gk.cuda(), 1e-6, causal=True).cpu()
+    torch.cuda.synchronize()
+    assert rmm.device_status() == 0
+    want = V[:, 0].repeat_interleave(Hq // Hkv, dim=1)
+    if gain_scale == 1.0:
+        assert torch.allclose(O[:, 0].float(), want.float(), rtol=2.0 ** -7, atol=0.0)
+    else:
+        assert torch.equal(O[:, 0], want)
 
 
-@pytest.mark.parametrize("D", [128, 64])
-def test_rescaled_rows(rmm, D):
+@pytest.mark.parametrize("D,gain", [(128, 1.5), (64, 1.5), (128, 2.5), (64, 2.5)])
+def test_rescaled_rows(rmm, D, gain):
     # every query of a head equals one direction u and so does one late key:
-    # that key's score dwarfs the first tile's, so the running maximum jumps
-    # by far more than 2^8 and the accumulator is rescaled (for D = 64 after
-    # the previous tile's P V, which P apart from S lets run late, completes)
+    # that key's score dwarfs the first tile's by far more than 2^8.  With
+    # gains of 1.5 the scores' bound (scale * log2(e) * D * gain^2 <= 50)
+    # is the softmax reference and the weights span ~2^-70 .. 1; with gains
+    # of 2.5 the bound is too loose, the kernel keeps a running maximum and
+    # the accumulator is rescaled (for D = 64 after the previous tile's P V,
+    # which P apart from S lets run late, completes)
     from sm_rmsnorm_matmul_gb300 import inputs
     B, S, Hq, Hkv = 1, 700, 2, 1
     qkv, gq, gk = inputs.attention_inputs(B, S, Hq, Hkv, D, 21)
-    gq = torch.full((D,), 1.5, dtype=torch.bfloat16)
-    gk = torch.full((D,), 1.5, dtype=torch.bfloat16)
+    gq = torch.full((D,), gain, dtype=torch.bfloat16)
+    gk = torch.full((D,), gain, dtype=torch.bfloat16)
     t = qkv.view(B * S, Hq + 2 * Hkv, D)
     u = torch.randn(D, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
     t[:, 0] = u
@@ -207,6 +226,24 @@ def test_large_sampled_rows(rmm, B, S, Hq, Hkv, causal, D):
     assert rmm.device_status() == 0
     qpos = sorted({0, 127, 128, 255, 256, S - 129, S - 128, S - 1} | set(inputs.sample_rows(S, 24)))
     assert_attention_close(O.cpu(), Q, K, V, gq, gk, 1e-6, causal, f"{B}x{S} {Hq}/{Hkv}", qpos=qpos)
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_running_maximum_sampled_rows(rmm, D):
+    """Gains of 1.25 .. 3.75 make the scores' bound too loose to serve as the
+    softmax reference: the running maximum across several blocks per CTA."""
+    from sm_rmsnorm_matmul_gb300 import inputs
+    B, S, Hq, Hkv, causal = 1, 3000, 32, 8, True
+    qkv, gq, gk = inputs.attention_inputs(B, S, Hq, Hkv, D, seed=S + D)
+    gq = (gq.float() * 2.5).to(torch.bfloat16)
+    gk = (gk.float() * 2.5).to(torch.bfloat16)
+    Q, K, V = inputs.split_qkv(qkv, B, S, Hq, Hkv, D)
+    Qd, Kd, Vd = inputs.split_qkv(qkv.cuda(), B, S, Hq, Hkv, D)
+    O = rmm.qknorm_attention(Qd, Kd, Vd, gq.cuda(), gk.cuda(), 1e-6, causal=causal)
+    torch.cuda.synchronize()
+    assert rmm.device_status() == 0
+    qpos = sorted({0, 127, 128, 255, 256, S - 129, S - 128, S - 1} | set(inputs.sample_rows(S, 24)))
+    assert_attention_close(O.cpu(), Q, K, V, gq, gk, 1e-6, causal, f"running maximum D={D}", qpos=qpos)
 
 
 def test_output_row_stride(rmm):
