@@ -65,7 +65,11 @@ int rmsnorm_heads(const void* X, int64_t ldx, const void* g, void* Y, int64_t ld
  * in fp32 (the query normalisation is a row scale of the scores), so Kg is
  * the only rounded operand.  Scores accumulate in fp32 in tensor memory, the
  * softmax weights are rounded to bf16 for the second product, the output
- * accumulates in fp32 and is rounded once.  Two kernel launches on `stream`:
+ * accumulates in fp32 and is rounded once.  The softmax subtracts, per query
+ * row, a reference no smaller than (about) its largest score: the row's
+ * Cauchy-Schwarz bound on its scores when the gains keep every such bound at
+ * most 50 (log2 units, scale * log2(e) * D * max_i |gq_i gk_i|), so that no
+ * weight falls below 2^-100, else a running maximum.  Two kernel launches on `stream`:
  * the key pass and a persistent attention kernel (one CTA per SM).
  */
 int qknorm_attention(const void* Q, int64_t ldq, const void* K, int64_t ldk, const void* V,
