@@ -168,15 +168,22 @@ def test_first_causal_row_is_first_value(rmm, gain_scale):
         assert torch.equal(O[:, 0], want)
 
 
-@pytest.mark.parametrize("D,gain", [(128, 1.5), (64, 1.5), (128, 2.5), (64, 2.5)])
+@pytest.mark.parametrize("D,gain", [(128, 1.5), (64, 1.5), (128, 1.7265625), (64, 2.046875),
+                                    (128, 2.5), (64, 2.5)])
 def test_rescaled_rows(rmm, D, gain):
     # every query of a head equals one direction u and so does one late key:
     # that key's score dwarfs the first tile's by far more than 2^8.  With
-    # gains of 1.5 the scores' bound (scale * log2(e) * D * gain^2 <= 50)
-    # is the softmax reference and the weights span ~2^-70 .. 1; with gains
-    # of 2.5 the bound is too loose, the kernel keeps a running maximum and
-    # the accumulator is rescaled (for D = 64 after the previous tile's P V,
-    # which P apart from S lets run late, completes)
+    # gains of 1.5 the scores' bound (scale * log2(e) * D * gain^2, times
+    # 1 + 1/64) is at most 50 and serves as the softmax reference: the
+    # weights span ~2^-70 .. 1.  Gains of 1.7265625 (D = 128) and 2.046875
+    # (D = 64) put the bound just below 50 (49.4, 49.1): rows that see only
+    # the opposite keys have every weight near 2^-98, the smallest the
+    # bound allows.  With gains of 2.5 the bound is too loose, the kernel
+    # keeps a running maximum and the accumulator is rescaled (for D = 64
+    # after the previous tile's P V, which P apart from S lets run late,
+    # completes)
+    bound = (1.0 / D ** 0.5) * 1.4426950408889634 * D * gain * gain * (1 + 1 / 64)
+    assert (bound <= 50.0) == (gain < 2.1)
     from sm_rmsnorm_matmul_gb300 import inputs
     B, S, Hq, Hkv = 1, 700, 2, 1
     qkv, gq, gk = inputs.attention_inputs(B, S, Hq, Hkv, D, 21)
