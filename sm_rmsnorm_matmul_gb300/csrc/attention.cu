@@ -177,13 +177,18 @@ __global__ void __launch_bounds__(kHeadsWarps * 32)
 // stride left the heaviest CTA 30% above the mean).  A block holds
 // two 128-row query tiles, A (rows q0 .. q0 + 127) and B (q0 + 128 ..), each
 // with its own score buffer, output accumulator, group of four softmax warps
-// and MMA issuing thread.  The issuers take turns, A then B for every key
-// tile (a pair of turn barriers): that keeps the two tiles half a period
-// apart, so the tensor cores work on one tile's products while the other
-// tile's softmax runs, and each issuer does its waits and releases while the
-// other one issues (an issuing thread stalls whenever the tensor pipe's queue
-// is full).  Without the turns the two issuers drift into step and both
-// softmaxes run while the pipe idles.
+// and MMA issuing thread.  The softmax hands P over in two halves of 64
+// keys, so the P V of the first half runs during the second half's
+// exponentials.  For D = 128, where P overwrites half of the score buffer,
+// the issuers take turns, A then B for every key tile (a pair of turn
+// barriers): that keeps the two tiles half a period apart, so the tensor
+// cores work on one tile's products while the other tile's softmax runs, and
+// each issuer does its waits and releases while the other one issues (an
+// issuing thread stalls whenever the tensor pipe's queue is full).  Without
+// the turns the two issuers drift into step and both softmaxes run while the
+// pipe idles.  For D = 64, P has tensor-memory columns of its own: the next
+// score product runs as soon as the softmax has read the scores, the softmax
+// never waits for a P V of its own tile, and the issuers take no turns.
 //
 // Both tiles read the same K and V tiles, loaded once, as one stream across
 // the CTA's blocks: stage g of a two-deep ring holds V_j of the current
